@@ -1,0 +1,197 @@
+"""CPU oracle for Hybrid-SWA attention over a dual KV pool.
+
+TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and
+bench.py's cpu_baseline / reference leg import this package. It shares no
+code with the CUDA library (``hybrid_sliding_window_dual_gb300``) and never
+imports it.
+
+* ``attention``  -- float64 paged Full / SWA GQA attention (hswa_oracle.c)
+* ``append_kv``  -- slot-mapped write of new K/V rows into a pool
+* ``swa_pack`` / ``swa_unpack`` -- transfer of in-window SWA tokens only
+* ``pool.DualPool`` -- dual-pool bookkeeping (reserve, release, ...)
+
+Source: "MiMo-V2.5 Series Inference Full-Link Optimization" Sec. 1.1 and
+Sec. 2.1; "Tiered KV Cache Offloading in vLLM", hybrid-model support
+(sliding-window layers move only the tokens inside their window).
+
+Parity status: every function here is pinned by tests/test_oracle.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+from .pool import DualPool, NoSpace  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hswa_oracle.c")
+_OUT = os.path.join(_HERE, "_build", "libhswa_oracle.so")
+_lib = None
+
+
+def build(force=False):
+    """Compile the C oracle with gcc (plain -O2, OpenMP, no fast-math)."""
+    if not force and os.path.exists(_OUT) and os.path.getmtime(_OUT) >= os.path.getmtime(_SRC):
+        return _OUT
+    os.makedirs(os.path.dirname(_OUT), exist_ok=True)
+    tmp = _OUT + ".tmp%d" % os.getpid()
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                           _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _OUT)
+    return _OUT
+
+
+def load_library(path):
+    """ctypes handle on a compiled oracle library (the default one, or a
+    test-built variant of the same source)."""
+    lib = ctypes.CDLL(path)
+    lib.hswa_oracle_attention.restype = ctypes.c_int
+    lib.hswa_oracle_attention.argtypes = [
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    lib.hswa_oracle_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def threads():
+    return _load().hswa_oracle_threads()
+
+
+def _raw(x):
+    """numpy view of a CPU array/tensor: (contiguous array, dtype code)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), 1
+            if x.dtype == torch.float32:
+                return x.numpy(), 0
+            raise TypeError("oracle inputs are fp32 or bf16, got %s" % x.dtype)
+    except ImportError:
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, 0
+    if x.dtype == np.uint16:
+        return x, 1
+    raise TypeError("oracle inputs are float32 or raw bf16 (uint16), got %s" % x.dtype)
+
+
+def attention(q, k_pool, v_pool, block_table, q_seq, q_pos, window, scale, lib=None):
+    """float64 attention for each query row.
+
+    q: [nq, Hq, d]; k_pool, v_pool: [pages, Hkv, P, d] (same dtype as q);
+    block_table: int32 [rows, max_pages]; q_seq[i]: table row of query i;
+    q_pos[i]: its position t; window: W (SWA layer) or 0 (Full layer).
+    Returns float64 [nq, Hq, d].
+    """
+    qa, dt = _raw(q)
+    ka, dk = _raw(k_pool)
+    va, dv = _raw(v_pool)
+    assert dt == dk == dv, "q, k and v must share a dtype"
+    nq, hq, d = qa.shape
+    pages, hkv, P, d2 = ka.shape
+    assert d2 == d and va.shape == ka.shape
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    qs = np.ascontiguousarray(q_seq, dtype=np.int32)
+    qp = np.ascontiguousarray(q_pos, dtype=np.int64)
+    assert qs.shape == (nq,) and qp.shape == (nq,)
+    out = np.zeros((nq, hq, d), np.float64)
+    rc = (lib or _load()).hswa_oracle_attention(
+        nq, qs.ctypes.data, qp.ctypes.data, hq, hkv, d, P, int(window), float(scale), dt,
+        qa.ctypes.data, ka.ctypes.data, va.ctypes.data, pages, bt.ctypes.data,
+        bt.shape[1], out.ctypes.data)
+    if rc == -1:
+        raise IndexError("a key's block-table entry is not a live page")
+    if rc != 0:
+        raise ValueError("bad attention sizes")
+    return out
+
+
+def append_kv(pool, new, slots):
+    """pool[slot // P, :, slot % P, :] = new[t] for every token t (slot -1 skipped).
+
+    pool: numpy [pages, Hkv, P, d]; new: [T, Hkv, d]; returns nothing."""
+    P = pool.shape[2]
+    for t, slot in enumerate(np.asarray(slots).tolist()):
+        if slot < 0:
+            continue
+        pool[slot // P, :, slot % P, :] = new[t]
+
+
+def swa_window_counts(seq_len, window):
+    """n_s = min(L_s, W) in-window tokens per sequence, and their prefix sum."""
+    n = np.minimum(np.asarray(seq_len, np.int64), window)
+    off = np.zeros(len(n) + 1, np.int64)
+    off[1:] = np.cumsum(n)
+    return n, off
+
+
+def swa_pack(k_pool, v_pool, swa_bt, seq_len, window):
+    """Pack the in-window tokens of sequences 0..n-1 of one SWA layer.
+
+    For each sequence s in order, n_s = min(L_s, W) tokens at positions
+    [L_s - n_s, L_s): a K block [Hkv][n_s][d] followed by a V block
+    [Hkv][n_s][d]. Returns a flat array of the pool's element type.
+    """
+    P = k_pool.shape[2]
+    hkv, d = k_pool.shape[1], k_pool.shape[3]
+    n, off = swa_window_counts(seq_len, window)
+    out = np.zeros(int(off[-1]) * 2 * hkv * d, k_pool.dtype)
+    for s in range(len(n)):
+        L = int(seq_len[s])
+        base = int(off[s]) * 2 * hkv * d
+        ns = int(n[s])
+        for which, pool in ((0, k_pool), (1, v_pool)):
+            block = np.zeros((hkv, ns, d), pool.dtype)
+            for i, t in enumerate(range(L - ns, L)):
+                page = int(swa_bt[s, t // P])
+                if page < 0:
+                    raise IndexError("in-window token without an SWA page")
+                block[:, i, :] = pool[page, :, t % P, :]
+            start = base + which * hkv * ns * d
+            out[start:start + hkv * ns * d] = block.reshape(-1)
+    return out
+
+
+def swa_unpack(packed, k_pool, v_pool, swa_bt, seq_len, window):
+    """Inverse of swa_pack: write the packed tokens back into the pools."""
+    P = k_pool.shape[2]
+    hkv, d = k_pool.shape[1], k_pool.shape[3]
+    n, off = swa_window_counts(seq_len, window)
+    for s in range(len(n)):
+        L = int(seq_len[s])
+        base = int(off[s]) * 2 * hkv * d
+        ns = int(n[s])
+        for which, pool in ((0, k_pool), (1, v_pool)):
+            start = base + which * hkv * ns * d
+            block = packed[start:start + hkv * ns * d].reshape(hkv, ns, d)
+            for i, t in enumerate(range(L - ns, L)):
+                page = int(swa_bt[s, t // P])
+                if page < 0:
+                    raise IndexError("in-window token without an SWA page")
+                pool[page, :, t % P, :] = block[:, i, :]
+
+
+def kv_bytes(pool: DualPool, layer_kinds, seq_ids, kv_bytes_per_token):
+    """KV bytes held by the dual pool for the given sequences (live pages),
+    summed over layers: Full layers count Full pages, SWA layers SWA pages."""
+    n_full = sum(1 for k in layer_kinds if k == 0)
+    n_swa = len(layer_kinds) - n_full
+    full = sum(pool.live_full_pages(s) for s in seq_ids)
+    swa = sum(pool.live_swa_pages(s) for s in seq_ids)
+    page_bytes = pool.P * kv_bytes_per_token
+    return (n_full * full + n_swa * swa) * page_bytes
