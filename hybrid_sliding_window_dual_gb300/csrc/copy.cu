@@ -1,0 +1,160 @@
+// Copy kernels of the dual KV pool: slot-mapped KV append and the
+// in-window SWA gather / scatter.
+//
+// "MiMo-V2.5 Series Inference Full-Link Optimization", Sec. 2.1 (KVCache
+// Dual Pool): Full layers keep every token in the Full pool, SWA layers keep
+// the window in the SWA pool; cross-tier transfer moves only SWA-mask data.
+// "Tiered KV Cache Offloading in vLLM", hybrid models: sliding-window layers
+// reload only the tokens inside their window.
+//
+// All three kernels are HBM- (or host-link-) bound 16-byte copies: a warp
+// moves whole 16-byte chunks of a token's K or V row, so a row of
+// d * sizeof(dtype) bytes is read and written with full 32-byte sectors.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace hswa {
+namespace {
+
+using chunk_t = uint4;  // 16 bytes
+
+// k_new / v_new [T][Hkv][row] -> pool [page][Hkv][P][row], row = d * esize
+__global__ void append_kv_kernel(const chunk_t *__restrict__ k, const chunk_t *__restrict__ v, chunk_t *kp,
+                                 chunk_t *vp, const int32_t *__restrict__ slots, int64_t n_tokens, int32_t hkv,
+                                 int32_t page, int32_t chunks_per_row, int64_t pool_slots, int *err) {
+    const int64_t per_tok = (int64_t)hkv * chunks_per_row;
+    const int64_t total = n_tokens * per_tok;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_tok;
+        const int64_t r = i - t * per_tok;  // g * chunks_per_row + c
+        const int32_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= pool_slots) {
+            set_error(err, HSWA_ERR_BOUNDS);
+            continue;
+        }
+        const int64_t g = r / chunks_per_row, c = r - g * chunks_per_row;
+        const int64_t dst = (((int64_t)(slot / page) * hkv + g) * page + slot % page) * chunks_per_row + c;
+        kp[dst] = k[i];
+        vp[dst] = v[i];
+    }
+}
+
+// One CTA strip per sequence (blockIdx.y). Packed order per sequence:
+// [K | V][Hkv][n_s tokens][row chunks].
+template <bool kGather>
+__global__ void swa_xfer_kernel(chunk_t *kp, chunk_t *vp, chunk_t *packed, const int32_t *__restrict__ swa_bt,
+                                const int32_t *__restrict__ seq_len, const int64_t *__restrict__ tok_offset,
+                                int32_t bt_stride, int32_t hkv, int32_t page, int32_t window,
+                                int32_t chunks_per_row, int32_t num_pages, int *err) {
+    const int32_t s = blockIdx.y;
+    const int32_t L = seq_len[s];
+    const int64_t n = (int64_t)(L < window ? L : window);
+    if (n <= 0) return;
+    const int64_t per_kind = (int64_t)hkv * n * chunks_per_row;
+    chunk_t *seq_base = packed + tok_offset[s] * 2 * hkv * chunks_per_row;
+    const int32_t *btrow = swa_bt + (int64_t)s * bt_stride;
+    for (int64_t f = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; f < 2 * per_kind;
+         f += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t which = f / per_kind;
+        int64_t r = f - which * per_kind;
+        const int64_t g = r / (n * chunks_per_row);
+        r -= g * n * chunks_per_row;
+        const int64_t i = r / chunks_per_row, c = r - i * chunks_per_row;
+        const int64_t t = L - n + i;  // token position
+        const int64_t lp = t / page;
+        const int32_t pg = lp < bt_stride ? btrow[lp] : -1;
+        if (pg < 0 || pg >= num_pages) {
+            set_error(err, HSWA_ERR_BOUNDS);
+            continue;
+        }
+        chunk_t *pool = which ? vp : kp;
+        const int64_t at = (((int64_t)pg * hkv + g) * page + t % page) * chunks_per_row + c;
+        if (kGather)
+            seq_base[f] = pool[at];
+        else
+            pool[at] = seq_base[f];
+    }
+}
+
+int esize(const hswa_config &c) { return c.dtype == HSWA_DTYPE_F32 ? 4 : 2; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+int grid_for(int64_t work, int block) {
+    const int64_t g = (work + block - 1) / block;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(g, (int64_t)sm_count() * 32));
+}
+
+}  // namespace
+}  // namespace hswa
+
+using namespace hswa;
+
+extern "C" int hswa_append_kv(const hswa_pool *pool, const hswa_layer *layer, const void *k, const void *v,
+                              const int32_t *d_slots, int n_tokens, hswa_stream_t stream) {
+    if (!pool || !layer || n_tokens < 0 || (n_tokens > 0 && (!k || !v || !d_slots)) || !layer->k_pool ||
+        !layer->v_pool || (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA))
+        return HSWA_ERR_INVALID_ARG;
+    const hswa_config &c = pool->cfg;
+    const int64_t row_bytes = (int64_t)c.head_dim * esize(c);
+    if (row_bytes % 16 || !aligned16(k) || !aligned16(v) || !aligned16(layer->k_pool) || !aligned16(layer->v_pool))
+        return HSWA_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return HSWA_OK;
+    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+    const int32_t cpr = (int32_t)(row_bytes / 16);
+    const int64_t work = (int64_t)n_tokens * c.n_kv_heads * cpr;
+    set_last_kernel("append_kv");
+    append_kv_kernel<<<grid_for(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        (const chunk_t *)k, (const chunk_t *)v, (chunk_t *)layer->k_pool, (chunk_t *)layer->v_pool, d_slots,
+        n_tokens, c.n_kv_heads, c.page_size, cpr, (int64_t)num_pages * c.page_size, error_word());
+    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+}
+
+static int swa_xfer(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
+                    const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, void *buf, bool gather,
+                    hswa_stream_t stream) {
+    if (!pool || !layer || !d_swa_bt || !d_seq_len || !d_tok_offset || !buf || n_seqs < 0 ||
+        n_seqs > pool->cfg.max_seqs || layer->kind != HSWA_KIND_SWA || layer->window <= 0 || !layer->k_pool ||
+        !layer->v_pool)
+        return HSWA_ERR_INVALID_ARG;
+    const hswa_config &c = pool->cfg;
+    const int64_t row_bytes = (int64_t)c.head_dim * esize(c);
+    if (row_bytes % 16 || !aligned16(buf) || !aligned16(layer->k_pool) || !aligned16(layer->v_pool))
+        return HSWA_ERR_UNSUPPORTED;
+    if (n_seqs == 0) return HSWA_OK;
+    const int32_t cpr = (int32_t)(row_bytes / 16);
+    const int block = 256;
+    const int64_t per_seq_max = 2LL * c.n_kv_heads * layer->window * cpr;
+    const int gx = (int)std::min<int64_t>((per_seq_max + block * 4 - 1) / (block * 4), 1024);
+    set_last_kernel(gather ? "swa_gather" : "swa_scatter");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    dim3 grid(std::max(gx, 1), n_seqs);
+    if (gather)
+        swa_xfer_kernel<true><<<grid, block, 0, st>>>((chunk_t *)layer->k_pool, (chunk_t *)layer->v_pool,
+                                                      (chunk_t *)buf, d_swa_bt, d_seq_len, d_tok_offset,
+                                                      c.max_pages_per_seq, c.n_kv_heads, c.page_size,
+                                                      layer->window, cpr, c.swa_pages, error_word());
+    else
+        swa_xfer_kernel<false><<<grid, block, 0, st>>>((chunk_t *)layer->k_pool, (chunk_t *)layer->v_pool,
+                                                       (chunk_t *)buf, d_swa_bt, d_seq_len, d_tok_offset,
+                                                       c.max_pages_per_seq, c.n_kv_heads, c.page_size,
+                                                       layer->window, cpr, c.swa_pages, error_word());
+    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+}
+
+extern "C" int hswa_swa_gather(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
+                               const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, void *dst,
+                               hswa_stream_t stream) {
+    return swa_xfer(pool, layer, d_swa_bt, d_seq_len, d_tok_offset, n_seqs, dst, true, stream);
+}
+
+extern "C" int hswa_swa_scatter(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
+                                const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, const void *src,
+                                hswa_stream_t stream) {
+    return swa_xfer(pool, layer, d_swa_bt, d_seq_len, d_tok_offset, n_seqs, const_cast<void *>(src), false,
+                    stream);
+}

@@ -1,0 +1,655 @@
+// Decode attention over the dual KV pool (one new token per sequence).
+//
+// "MiMo-V2.5 Series Inference Full-Link Optimization", Sec. 1.2: decode is
+// close to memory-bandwidth-bound and its cost follows the KV bytes read;
+// Sec. 2.1 / 5.1: Full layers read the O(N) Full pool, SWA layers only the
+// O(W) window of the SWA pool.
+//
+// Fast path (bf16, d = 128, 8 query heads per kv head, page 64):
+//   * The work is the list of (sequence, kv head, page) units, sequences in
+//     order. Each CTA takes an equal contiguous share of that list
+//     (stream-K style), so CTAs stay balanced whatever the length mix. A
+//     piece of a (sequence, kv head) segment that a CTA covers alone is
+//     written straight to o; a segment cut between CTAs leaves partial
+//     (max, sum, unnormalised o) records that decode_combine merges.
+//   * Warp 1 (producer) streams one page of one kv head per stage: K and V
+//     as two 64x64 tensor-map boxes each (128-byte swizzle), plus the 8 query
+//     rows at the first page of a piece, into a 3-stage mbarrier ring.
+//   * Warp 0 (consumer) computes S^T = K Q^T (16 keys x 8 heads per
+//     mma.m16n8k16, the 8 GQA heads filling N = 8), an online softmax in the
+//     log2 domain, transposes P with movmatrix and accumulates
+//     O^T += V^T P^T with V^T read by ldmatrix.trans.
+// Generic path (any dtype / head_dim / ratio / page): one warp per
+// (sequence, query head) with CUDA-core dot products.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "kernels.h"
+
+namespace hswa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kG = 8;
+constexpr int kP = 64;
+constexpr int kStages = 3;
+constexpr uint32_t kBoxBytes = 64 * 128;           // 64 rows x 128 bytes
+constexpr uint32_t kPageHeadBytes = 2 * kBoxBytes;  // one page of one kv head
+constexpr uint32_t kQBytes = kG * kD * 2;
+
+enum : int32_t { kFirst = 1, kLast = 2, kDirect = 4, kSkip = 8 };
+
+struct StageDesc {
+    int32_t seq, kvh, lo, hi, flags, slot, pad0, pad1;
+};
+
+struct DecodeSmem {
+    uint8_t k[kStages][kPageHeadBytes];
+    uint8_t v[kStages][kPageHeadBytes];
+    uint8_t q[kStages][kQBytes];
+    StageDesc desc[kStages];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int32_t abort;
+};
+
+constexpr size_t kDecodeSmemBytes = sizeof(DecodeSmem) + 1024;  // + alignment slack
+
+struct Partial {
+    float m[kG];
+    float l[kG];
+    float o[kG][kD];
+};
+
+struct DecodeArgs {
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *o;
+    const int32_t *bt;
+    const int32_t *seq_len;
+    const int32_t *useg;  // [n_seqs + 1] unit prefix sum
+    Partial *part;        // [n_ctas][2]
+    int32_t n_seqs, bt_stride, hkv, hq, window, num_pages;
+    float scale_log2;
+    int *err;
+};
+
+// Keys [lo, hi) a decode query of a sequence with L keys attends.
+__device__ __forceinline__ void key_range(int32_t L, int32_t window, int32_t &lo, int32_t &hi) {
+    hi = L;
+    lo = (window > 0 && L - window > 0) ? L - window : 0;
+}
+
+// Unit prefix sum over sequences: units(s) = Hkv * pages touched by [lo, hi).
+__global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int32_t hkv, int32_t page,
+                            int32_t window, int32_t *__restrict__ useg) {
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int32_t base = 0; base < n; base += blockDim.x) {
+        const int32_t i = base + tid;
+        int32_t u = 0;
+        if (i < n) {
+            int32_t lo, hi;
+            key_range(seq_len[i], window, lo, hi);
+            if (hi > lo) u = hkv * ((hi - 1) / page - lo / page + 1);
+        }
+        int32_t x = u;  // inclusive warp scan
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_tot[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int32_t t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, t, off);
+                if (lane >= off) t += y;
+            }
+            warp_tot[lane] = t;  // inclusive scan of warp totals
+        }
+        __syncthreads();
+        const int32_t excl = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + x - u;
+        if (i < n) useg[i] = excl;
+        __syncthreads();
+        if (tid == blockDim.x - 1) carry = excl + u;
+        __syncthreads();
+    }
+    if (tid == 0) useg[n] = carry;
+}
+
+__device__ __forceinline__ int64_t cta_start(int64_t c, int64_t U, int64_t N) { return c * U / N; }
+
+// Largest c with cta_start(c) <= u.
+__device__ __forceinline__ int64_t cta_of(int64_t u, int64_t U, int64_t N) { return ((u + 1) * N - 1) / U; }
+
+// Largest s with useg[s] <= u (useg non-decreasing, useg[0] = 0 <= u < useg[n]).
+__device__ int32_t find_seq(const int32_t *useg, int32_t n, int64_t u) {
+    int32_t lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (useg[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Byte offset of the 16-byte chunk holding (row, d..d+7) in a stage buffer
+// loaded as two 64-column boxes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int row, int d) {
+    return (uint32_t)((d >> 6) * kBoxBytes + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+__device__ void decode_producer(DecodeSmem &sm, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeArgs &a,
+                                int64_t u0, int64_t u1) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        prefetch_tmap(tk);
+        prefetch_tmap(tv);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_parity[kStages];
+    bool issued[kStages];
+    for (int i = 0; i < kStages; ++i) issued[i] = false, issued_parity[i] = 0;
+
+    int64_t u = u0;
+    int32_t s = u0 < u1 ? find_seq(a.useg, a.n_seqs, u0) : 0;
+    while (u < u1) {
+        while (a.useg[s + 1] <= u) ++s;  // skip sequences without units
+        int32_t lo, hi;
+        key_range(a.seq_len[s], a.window, lo, hi);
+        const int32_t pf = lo / kP;
+        const int32_t npg = (hi - 1) / kP - pf + 1;
+        const int64_t seg0 = a.useg[s];
+        const int32_t g = (int32_t)((u - seg0) / npg);
+        const int32_t pi = (int32_t)((u - seg0) % npg);
+        const int64_t seg_start = seg0 + (int64_t)g * npg, seg_end = seg_start + npg;
+        const int64_t piece_end = seg_end < u1 ? seg_end : u1;
+        const int32_t n = (int32_t)(piece_end - u);
+        const bool direct = (u == seg_start) && (piece_end == seg_end);
+        const int32_t slot = (u == u0) ? 0 : 1;
+        const int32_t *btrow = a.bt + (int64_t)s * a.bt_stride;
+        int32_t mine = -1;
+        for (int32_t j = 0; j < n; ++j) {
+            if ((j & 31) == 0)
+                mine = (j + lane < n && pf + pi + j + lane < a.bt_stride) ? btrow[pf + pi + j + lane] : -1;
+            const int32_t page = __shfl_sync(0xffffffffu, mine, j & 31);
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(&sm.empty[stage], phase ^ 1, a.err) && !*(volatile int32_t *)&sm.abort;
+                if (ok) {
+                    const int32_t lp = pf + pi + j;
+                    const int32_t key0 = lp * kP;
+                    StageDesc &d = sm.desc[stage];
+                    d.seq = s;
+                    d.kvh = g;
+                    d.lo = lo - key0 > 0 ? lo - key0 : 0;
+                    d.hi = hi - key0 < kP ? hi - key0 : kP;
+                    d.slot = slot;
+                    int32_t flags = (j == 0 ? kFirst : 0) | (j == n - 1 ? kLast : 0) | (direct ? kDirect : 0);
+                    const bool valid = page >= 0 && page < a.num_pages;
+                    if (!valid) {
+                        set_error(a.err, HSWA_ERR_BOUNDS);
+                        flags |= kSkip;
+                    }
+                    d.flags = flags;
+                    const uint32_t bytes = (valid ? 4 * kBoxBytes : 0) + (j == 0 ? kQBytes : 0);
+                    if (bytes) {
+                        mbar_arrive_expect_tx(&sm.full[stage], bytes);
+                        if (valid) {
+                            const int32_t row = (page * a.hkv + g) * kP;
+                            tma_load_2d(sm.k[stage], tk, 0, row, &sm.full[stage]);
+                            tma_load_2d(sm.k[stage] + kBoxBytes, tk, 64, row, &sm.full[stage]);
+                            tma_load_2d(sm.v[stage], tv, 0, row, &sm.full[stage]);
+                            tma_load_2d(sm.v[stage] + kBoxBytes, tv, 64, row, &sm.full[stage]);
+                        }
+                        if (j == 0)
+                            bulk_g2s(sm.q[stage], a.q + ((int64_t)s * a.hq + (int64_t)g * kG) * kD, kQBytes,
+                                     &sm.full[stage]);
+                    } else {
+                        mbar_arrive(&sm.full[stage]);
+                    }
+                    issued[stage] = true;
+                    issued_parity[stage] = phase;
+                } else {
+                    sm.abort = 1;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) goto drain;
+            if (++stage == kStages) stage = 0, phase ^= 1;
+        }
+        u = piece_end;
+    }
+drain:
+    // never leave the CTA with copies still landing in its shared memory
+    if (lane == 0)
+        for (int i = 0; i < kStages; ++i)
+            if (issued[i]) mbar_wait(&sm.full[i], issued_parity[i], a.err);
+}
+
+__device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0, int64_t u1) {
+    const int lane = threadIdx.x & 31;
+    const int gr = lane >> 2;  // fragment row group
+    const int qd = lane & 3;   // fragment column pair
+    uint32_t qf[8][2];
+    float oacc[8][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int stage = 0;
+    uint32_t phase = 0;
+    const uint32_t kbase = smem_u32(sm.k[0]), vbase = smem_u32(sm.v[0]);
+
+    for (int64_t u = u0; u < u1; ++u) {
+        bool ok = mbar_wait(&sm.full[stage], phase, a.err) && !*(volatile int32_t *)&sm.abort;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0) sm.abort = 1;
+            return;
+        }
+        const StageDesc d = sm.desc[stage];
+        if (d.flags & kFirst) {
+            const uint32_t *qs = reinterpret_cast<const uint32_t *>(sm.q[stage]);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qf[ks][0] = qs[(gr * kD + ks * 16 + 2 * qd) >> 1];
+                qf[ks][1] = qs[(gr * kD + ks * 16 + 8 + 2 * qd) >> 1];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+        if (!(d.flags & kSkip)) {
+            const uint32_t kb = kbase + stage * kPageHeadBytes, vb = vbase + stage * kPageHeadBytes;
+            // S^T = K Q^T : 4 tiles of 16 keys
+            float sacc[4][4];
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                sacc[kt][0] = sacc[kt][1] = sacc[kt][2] = sacc[kt][3] = 0.f;
+                const int row = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kb + swz(row, ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+                    mma_bf16_16816(sacc[kt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                }
+            }
+            // scale to log2 units and mask keys outside [lo, hi)
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                const int r0 = kt * 16 + gr, r1 = r0 + 8;
+                const bool v0 = r0 >= d.lo && r0 < d.hi, v1 = r1 >= d.lo && r1 < d.hi;
+                sacc[kt][0] = v0 ? sacc[kt][0] * a.scale_log2 : -INFINITY;
+                sacc[kt][1] = v0 ? sacc[kt][1] * a.scale_log2 : -INFINITY;
+                sacc[kt][2] = v1 ? sacc[kt][2] * a.scale_log2 : -INFINITY;
+                sacc[kt][3] = v1 ? sacc[kt][3] * a.scale_log2 : -INFINITY;
+                mx0 = fmaxf(mx0, fmaxf(sacc[kt][0], sacc[kt][2]));
+                mx1 = fmaxf(mx1, fmaxf(sacc[kt][1], sacc[kt][3]));
+            }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            // a stage holds at least one valid key, so n0 and n1 are finite
+            const float al0 = fast_exp2(m0 - n0), al1 = fast_exp2(m1 - n1);
+            m0 = n0;
+            m1 = n1;
+            uint32_t pb[4][2];
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                const float p0 = fast_exp2(sacc[kt][0] - n0), p1 = fast_exp2(sacc[kt][1] - n1);
+                const float p2 = fast_exp2(sacc[kt][2] - n0), p3 = fast_exp2(sacc[kt][3] - n1);
+                const uint32_t x0 = pack_bf16(p0, p1), x1 = pack_bf16(p2, p3);
+                // sum what the MMA will see (the bf16-rounded weights)
+                const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162 *>(&x0);
+                const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162 *>(&x1);
+                ps0 += __low2float(r0) + __low2float(r1);
+                ps1 += __high2float(r0) + __high2float(r1);
+                pb[kt][0] = movmatrix_t(x0);
+                pb[kt][1] = movmatrix_t(x1);
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                oacc[dt][0] *= al0;
+                oacc[dt][1] *= al1;
+                oacc[dt][2] *= al0;
+                oacc[dt][3] *= al1;
+            }
+            // O^T += V^T P^T
+            const int j = lane >> 3;
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                const int key = kt * 16 + (lane & 7) + (j >> 1) * 8;
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(vb + swz(key, dt * 16 + (j & 1) * 8), a0, a1, a2, a3);
+                    mma_bf16_16816(oacc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+
+        if (d.flags & kLast) {
+            float t0 = l0, t1 = l1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                t0 += __shfl_xor_sync(0xffffffffu, t0, off);
+                t1 += __shfl_xor_sync(0xffffffffu, t1, off);
+            }
+            const int h0 = 2 * qd, h1 = 2 * qd + 1;
+            if (d.flags & kDirect) {
+                const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
+                __nv_bfloat16 *o0 = a.o + ((int64_t)d.seq * a.hq + (int64_t)d.kvh * kG + h0) * kD;
+                __nv_bfloat16 *o1 = o0 + kD;
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    o0[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][0] * i0);
+                    o1[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][1] * i1);
+                    o0[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][2] * i0);
+                    o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][3] * i1);
+                }
+            } else {
+                Partial &p = a.part[(int64_t)blockIdx.x * 2 + d.slot];
+                if (gr == 0) {
+                    p.m[h0] = m0;
+                    p.m[h1] = m1;
+                    p.l[h0] = t0;
+                    p.l[h1] = t1;
+                }
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    p.o[h0][dt * 16 + gr] = oacc[dt][0];
+                    p.o[h1][dt * 16 + gr] = oacc[dt][1];
+                    p.o[h0][dt * 16 + gr + 8] = oacc[dt][2];
+                    p.o[h1][dt * 16 + gr + 8] = oacc[dt][3];
+                }
+            }
+        }
+        if (++stage == kStages) stage = 0, phase ^= 1;
+    }
+}
+
+__global__ void __launch_bounds__(64) decode_mma_bf16_d128(const __grid_constant__ CUtensorMap tk,
+                                                           const __grid_constant__ CUtensorMap tv, DecodeArgs a) {
+    extern __shared__ uint8_t raw[];
+    DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int64_t U = a.useg[a.n_seqs], N = gridDim.x;
+    if (U == 0) return;
+    const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
+    if (threadIdx.x >= 32)
+        decode_producer(sm, &tk, &tv, a, u0, u1);
+    else
+        decode_consumer(sm, a, u0, u1);
+}
+
+// Merge the partial records of segments split between CTAs; write zeros
+// for sequences without keys.
+__global__ void __launch_bounds__(256) decode_combine(DecodeArgs a, int32_t n_ctas) {
+    const int32_t s = blockIdx.y, g = blockIdx.x;
+    const int64_t U = a.useg[a.n_seqs], N = n_ctas;
+    const int32_t units = a.useg[s + 1] - a.useg[s];
+    const int h = threadIdx.x >> 5, d0 = (threadIdx.x & 31) * 4;
+    __nv_bfloat16 *out = a.o + ((int64_t)s * a.hq + (int64_t)g * kG + h) * kD + d0;
+    if (units == 0) {
+        for (int i = 0; i < 4; ++i) out[i] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const int32_t npg = units / a.hkv;
+    const int64_t lo = a.useg[s] + (int64_t)g * npg, hi = lo + npg;  // [lo, hi)
+    const int64_t c_lo = cta_of(lo, U, N), c_hi = cta_of(hi - 1, U, N);
+    if (c_lo == c_hi) return;
+    float M = -INFINITY;
+    for (int64_t c = c_lo; c <= c_hi; ++c) {
+        if (cta_start(c, U, N) == cta_start(c + 1, U, N)) continue;
+        const int slot = (c == c_lo && cta_start(c, U, N) < lo) ? 1 : 0;
+        M = fmaxf(M, a.part[c * 2 + slot].m[h]);
+    }
+    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int64_t c = c_lo; c <= c_hi; ++c) {
+        if (cta_start(c, U, N) == cta_start(c + 1, U, N)) continue;
+        const int slot = (c == c_lo && cta_start(c, U, N) < lo) ? 1 : 0;
+        const Partial &p = a.part[c * 2 + slot];
+        const float w = p.m[h] == -INFINITY ? 0.f : fast_exp2(p.m[h] - M);
+        L += w * p.l[h];
+        for (int i = 0; i < 4; ++i) acc[i] += w * p.o[h][d0 + i];
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int i = 0; i < 4; ++i) out[i] = __float2bfloat16_rn(acc[i] * inv);
+}
+
+// ----------------------------------------------------------- generic path
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+}  // namespace
+
+// One warp per (query row, query head): query position t, keys [lo, t].
+// mode 0: decode, n_rows sequences (row i = sequence i, t = L_i - 1);
+// mode 1: prefill, n_rows = max rows per sequence; row r < n_s of sequence s
+//         is q row q_start[s] + r at t = prefix[s] + r.
+template <typename T, int MAXE>
+__global__ void attention_generic(const T *__restrict__ q, T *__restrict__ o, const T *__restrict__ kp,
+                                  const T *__restrict__ vp, const int32_t *__restrict__ bt,
+                                  const int32_t *__restrict__ seq_len, const int32_t *__restrict__ prefix,
+                                  const int32_t *__restrict__ q_start, int32_t n_rows, int32_t n_seqs,
+                                  int32_t bt_stride, int32_t hq, int32_t hkv, int32_t d, int32_t page,
+                                  int32_t window, int32_t num_pages, float scale, int mode, int *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t per_seq = mode == 0 ? hq : (int64_t)n_rows * hq;
+    if (wid >= per_seq * (mode == 0 ? n_rows : n_seqs)) return;
+    const int32_t h = (int32_t)(wid % hq);
+    const int32_t g = (int32_t)((int64_t)h * hkv / hq);
+    int32_t s, t, row;
+    if (mode == 0) {
+        s = row = (int32_t)(wid / hq);
+        t = seq_len[s] - 1;
+    } else {
+        s = (int32_t)(wid / per_seq);
+        const int32_t r = (int32_t)((wid / hq) % n_rows);
+        if (r >= q_start[s + 1] - q_start[s]) return;
+        row = q_start[s] + r;
+        t = prefix[s] + r;
+    }
+    float qv[MAXE], acc[MAXE];
+    const int ne = (d + 31) / 32;
+    const T *qrow = q + ((int64_t)row * hq + h) * d;
+#pragma unroll
+    for (int e = 0; e < MAXE; ++e) {
+        const int c = lane + 32 * e;
+        qv[e] = (e < ne && c < d) ? to_f(qrow[c]) * scale : 0.f;
+        acc[e] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const int32_t lo = (window > 0 && t - window + 1 > 0) ? t - window + 1 : 0;
+    const int32_t *btrow = bt + (int64_t)s * bt_stride;
+    for (int32_t j = lo; j <= t; ++j) {
+        const int32_t pg = j / page < bt_stride ? btrow[j / page] : -1;
+        if (pg < 0 || pg >= num_pages) {
+            if (lane == 0) set_error(err, HSWA_ERR_BOUNDS);
+            continue;
+        }
+        const int64_t base = (((int64_t)pg * hkv + g) * page + j % page) * d;
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < MAXE; ++e) {
+            const int c = lane + 32 * e;
+            if (e < ne && c < d) dot += qv[e] * to_f(kp[base + c]);
+        }
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        const float nm = fmaxf(m, dot);
+        const float alpha = expf(m - nm), p = expf(dot - nm);
+        l = l * alpha + p;
+#pragma unroll
+        for (int e = 0; e < MAXE; ++e) {
+            const int c = lane + 32 * e;
+            const float vv = (e < ne && c < d) ? to_f(vp[base + c]) : 0.f;
+            acc[e] = acc[e] * alpha + p * vv;
+        }
+        m = nm;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    T *orow = o + ((int64_t)row * hq + h) * d;
+#pragma unroll
+    for (int e = 0; e < MAXE; ++e) {
+        const int c = lane + 32 * e;
+        if (e < ne && c < d) orow[c] = from_f<T>(acc[e] * inv);
+    }
+}
+
+// Launch the generic kernel for decode (mode 0) or prefill (mode 1).
+int launch_attention_generic(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                             const int32_t *bt, const int32_t *seq_len, const int32_t *prefix,
+                             const int32_t *q_start, int32_t n_rows, int32_t n_seqs, float scale, int mode,
+                             cudaStream_t st) {
+    const hswa_config &c = pool->cfg;
+    if (c.head_dim > 256) return HSWA_ERR_UNSUPPORTED;
+    if (n_rows == 0) return HSWA_OK;
+    const int32_t window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
+    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+    const int64_t threads = (int64_t)n_rows * (mode == 0 ? 1 : n_seqs) * c.n_q_heads * 32;
+    const int block = 256;
+    const int64_t grid = (threads + block - 1) / block;
+    if (grid > INT32_MAX) return HSWA_ERR_UNSUPPORTED;
+    int *err = error_word();
+    if (c.dtype == HSWA_DTYPE_F32) {
+        set_last_kernel(mode == 0 ? "decode_generic_f32" : "prefill_generic_f32");
+        attention_generic<float, 8><<<(int)grid, block, 0, st>>>(
+            (const float *)q, (float *)o, (const float *)layer->k_pool, (const float *)layer->v_pool, bt, seq_len,
+            prefix, q_start, n_rows, n_seqs, c.max_pages_per_seq, c.n_q_heads, c.n_kv_heads, c.head_dim,
+            c.page_size, window, num_pages, scale, mode, err);
+    } else {
+        set_last_kernel(mode == 0 ? "decode_generic_bf16" : "prefill_generic_bf16");
+        attention_generic<__nv_bfloat16, 8><<<(int)grid, block, 0, st>>>(
+            (const __nv_bfloat16 *)q, (__nv_bfloat16 *)o, (const __nv_bfloat16 *)layer->k_pool,
+            (const __nv_bfloat16 *)layer->v_pool, bt, seq_len, prefix, q_start, n_rows, n_seqs,
+            c.max_pages_per_seq, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, window, num_pages, scale,
+            mode, err);
+    }
+    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+}
+
+namespace {
+
+bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
+    const hswa_config &c = pool->cfg;
+    return c.dtype == HSWA_DTYPE_BF16 && c.head_dim == kD && c.n_q_heads == kG * c.n_kv_heads &&
+           c.page_size == kP && ((uintptr_t)q & 15) == 0 && ((uintptr_t)o & 15) == 0 &&
+           ((uintptr_t)layer->k_pool & 15) == 0 && ((uintptr_t)layer->v_pool & 15) == 0;
+}
+
+int decode_ctas_per_sm() {
+    static int v = -1;
+    if (v < 0) {
+        if (cudaFuncSetAttribute(decode_mma_bf16_d128, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDecodeSmemBytes) != cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128, 64, kDecodeSmemBytes) !=
+            cudaSuccess)
+            n = 1;
+        v = std::max(1, n);
+    }
+    return v;
+}
+
+constexpr int kMaxCtasPerSm = 4;
+
+size_t useg_bytes(int n_seqs) { return ((size_t)(n_seqs + 1) * 4 + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace hswa
+
+using namespace hswa;
+
+extern "C" size_t hswa_decode_workspace_size(const hswa_pool *pool, int n_seqs) {
+    if (!pool || n_seqs < 0) return 0;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 192;  // no device visible: size for the largest part
+    return useg_bytes(n_seqs) + (size_t)sms * kMaxCtasPerSm * 2 * sizeof(Partial);
+}
+
+extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                           const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale, void *ws,
+                           size_t ws_bytes, hswa_stream_t stream) {
+    if (!pool || !layer || !q || !o || !d_bt || !d_seq_len || n_seqs < 0 || n_seqs > pool->cfg.max_seqs ||
+        !layer->k_pool || !layer->v_pool || (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA) ||
+        (layer->kind == HSWA_KIND_SWA && layer->window <= 0))
+        return HSWA_ERR_INVALID_ARG;
+    if (n_seqs == 0) return HSWA_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!decode_fast_ok(pool, layer, q, o))
+        return launch_attention_generic(pool, layer, q, o, d_bt, d_seq_len, nullptr, nullptr, n_seqs, n_seqs, scale,
+                                        0, st);
+    const hswa_config &c = pool->cfg;
+    const int sms = sm_count();
+    if (sms <= 0) return HSWA_ERR_CUDA;
+    const int per_sm = decode_ctas_per_sm();
+    if (per_sm <= 0) return HSWA_ERR_CUDA;
+    const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
+    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < useg_bytes(n_seqs) + (size_t)n_ctas * 2 * sizeof(Partial))
+        return HSWA_ERR_INVALID_ARG;
+    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
+    if (!make_tmap_2d(&tk, layer->k_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tv, layer->v_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return HSWA_ERR_CUDA;
+    DecodeArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.bt = d_bt;
+    a.seq_len = d_seq_len;
+    a.useg = static_cast<int32_t *>(ws);
+    a.part = reinterpret_cast<Partial *>(static_cast<uint8_t *>(ws) + useg_bytes(n_seqs));
+    a.n_seqs = n_seqs;
+    a.bt_stride = c.max_pages_per_seq;
+    a.hkv = c.n_kv_heads;
+    a.hq = c.n_q_heads;
+    a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
+    a.num_pages = num_pages;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.err = error_word();
+    set_last_kernel("decode_mma_bf16_d128");
+    decode_plan<<<1, 1024, 0, st>>>(d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, const_cast<int32_t *>(a.useg));
+    decode_mma_bf16_d128<<<n_ctas, 64, kDecodeSmemBytes, st>>>(tk, tv, a);
+    decode_combine<<<dim3(c.n_kv_heads, n_seqs), 256, 0, st>>>(a, n_ctas);
+    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+}

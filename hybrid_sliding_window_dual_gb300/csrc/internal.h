@@ -1,0 +1,79 @@
+// Internal declarations shared by the host-side sources of libhswa.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "hswa.h"
+
+// FIFO free list of page indices (ring buffer; never holds more than the
+// pool's page count).
+struct PageQueue {
+    std::vector<int32_t> ring;
+    int64_t head = 0;
+    int64_t count = 0;
+
+    void init(int32_t capacity, const int32_t *order) {
+        ring.assign(capacity, 0);
+        for (int32_t i = 0; i < capacity; ++i) ring[i] = order ? order[i] : i;
+        head = 0;
+        count = capacity;
+    }
+    int32_t pop() {
+        int32_t v = ring[head];
+        head = (head + 1) % (int64_t)ring.size();
+        --count;
+        return v;
+    }
+    void push(int32_t v) {
+        ring[(head + count) % (int64_t)ring.size()] = v;
+        ++count;
+    }
+    int32_t at(int64_t i) const { return ring[(head + i) % (int64_t)ring.size()]; }
+};
+
+struct hswa_pool {
+    hswa_config cfg;
+    PageQueue full_free, swa_free;
+    std::vector<int32_t> full_bt, swa_bt;  // [max_seqs][max_pages_per_seq]
+    std::vector<int32_t> seq_len;          // [max_seqs]
+
+    // Entries changed since the last hswa_sync_tables, as flat indices into
+    // the concatenation [full_bt | swa_bt | seq_len]; each index listed once.
+    std::vector<uint8_t> dirty_flag;
+    std::vector<int64_t> dirty_list;
+    bool need_full_upload = true;
+    const void *last_dev[3] = {nullptr, nullptr, nullptr};
+
+    // pinned staging for the table upload, and the event that says when the
+    // last copy out of it has finished
+    void *staging = nullptr;
+    size_t staging_bytes = 0;
+    void *staging_event = nullptr;  // cudaEvent_t
+    int device = -1;
+
+    int64_t table_entries() const { return (int64_t)cfg.max_seqs * cfg.max_pages_per_seq; }
+    void mark(int64_t flat) {
+        if (!dirty_flag[flat]) {
+            dirty_flag[flat] = 1;
+            dirty_list.push_back(flat);
+        }
+    }
+    void set_full(int32_t s, int32_t p, int32_t v) {
+        int64_t i = (int64_t)s * cfg.max_pages_per_seq + p;
+        full_bt[i] = v;
+        mark(i);
+    }
+    void set_swa(int32_t s, int32_t p, int32_t v) {
+        int64_t i = (int64_t)s * cfg.max_pages_per_seq + p;
+        swa_bt[i] = v;
+        mark(table_entries() + i);
+    }
+    void set_len(int32_t s, int32_t v) {
+        seq_len[s] = v;
+        mark(2 * table_entries() + s);
+    }
+};
+
+// Releases the CUDA resources of a pool (defined with the CUDA sources).
+void hswa_pool_release_device(hswa_pool *pool);

@@ -1,0 +1,129 @@
+"""PyTorch-side plumbing around the C ABI: device memory for the layer pools,
+the block tables and the decode workspace, and the stream to enqueue on.
+
+No attention arithmetic happens here; every step calls a libhswa entry point.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _binding as B
+
+_TORCH_DTYPE = {B.HSWA_DTYPE_F32: torch.float32, B.HSWA_DTYPE_BF16: torch.bfloat16}
+
+
+class DualPoolSession:
+    """A dual pool on one GPU: host bookkeeping (libhswa) + device buffers.
+
+    ``layer_kinds`` lists HSWA_KIND_FULL / HSWA_KIND_SWA per layer; each
+    layer gets its own K and V pool tensors unless ``share_full_pool`` is set,
+    in which case all Full layers read one physical Full pool (used where the
+    per-layer Full pools would not fit in HBM; the bytes each layer reads are
+    the same).
+    """
+
+    def __init__(self, config: B.Config, layer_kinds, full_free_order=None, swa_free_order=None,
+                 device="cuda", share_full_pool=False, stream=None, init="zeros"):
+        self.cfg = config
+        self.device = torch.device(device)
+        self.stream = stream
+        self.pool = B.hswa_pool_create(config, full_free_order, swa_free_order)
+        self.dtype = _TORCH_DTYPE[config.dtype]
+        rows = (config.max_seqs, config.max_pages_per_seq)
+        self.d_full_bt = torch.full(rows, -1, dtype=torch.int32, device=self.device)
+        self.d_swa_bt = torch.full(rows, -1, dtype=torch.int32, device=self.device)
+        self.d_seq_len = torch.zeros(config.max_seqs, dtype=torch.int32, device=self.device)
+        self.kinds = list(layer_kinds)
+        self.k, self.v, self.layers = [], [], []
+        shared = None
+        for kind in self.kinds:
+            pages = config.full_pages if kind == B.HSWA_KIND_FULL else config.swa_pages
+            shape = (pages, config.n_kv_heads, config.page_size, config.head_dim)
+            if kind == B.HSWA_KIND_FULL and share_full_pool and shared is not None:
+                k, v = shared
+            else:
+                alloc = torch.zeros if init == "zeros" else torch.empty
+                k = alloc(shape, dtype=self.dtype, device=self.device)
+                v = alloc(shape, dtype=self.dtype, device=self.device)
+                if kind == B.HSWA_KIND_FULL and share_full_pool:
+                    shared = (k, v)
+            self.k.append(k)
+            self.v.append(v)
+            self.layers.append(B.Layer(kind=kind, window=config.window, k_pool=k.data_ptr(),
+                                       v_pool=v.data_ptr()))
+        self.ws = None
+
+    def close(self):
+        if self.pool:
+            B.hswa_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -------------------------------------------------------- bookkeeping
+    def reserve(self, seq_ids, n_new):
+        return B.hswa_reserve(self.pool, seq_ids, n_new)
+
+    def release(self, seq_ids):
+        return B.hswa_swa_release(self.pool, seq_ids)
+
+    def seq_free(self, seq_ids):
+        B.hswa_seq_free(self.pool, seq_ids)
+
+    def swa_drop(self, seq_ids):
+        return B.hswa_swa_drop(self.pool, seq_ids)
+
+    def swa_restore(self, seq_ids):
+        return B.hswa_swa_restore(self.pool, seq_ids)
+
+    def tables(self):
+        return B.hswa_get_tables(self.pool, self.cfg)
+
+    def sync(self):
+        B.hswa_sync_tables(self.pool, self.d_full_bt, self.d_swa_bt, self.d_seq_len, self.stream)
+
+    def bt(self, layer):
+        return self.d_full_bt if self.kinds[layer] == B.HSWA_KIND_FULL else self.d_swa_bt
+
+    # ------------------------------------------------------------ device
+    def workspace(self, n_seqs):
+        need = B.hswa_decode_workspace_size(self.pool, n_seqs)
+        if self.ws is None or self.ws.numel() < need:
+            self.ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self.ws
+
+    def append(self, layer, k, v, d_slots):
+        B.hswa_append_kv(self.pool, self.layers[layer], k, v, d_slots, k.shape[0], self.stream)
+
+    def decode(self, layer, q, o, n_seqs, scale):
+        ws = self.workspace(n_seqs)
+        B.hswa_decode(self.pool, self.layers[layer], q, o, self.bt(layer), self.d_seq_len, n_seqs, scale, ws,
+                      ws.numel(), self.stream)
+
+    def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale):
+        B.hswa_prefill_chunk(self.pool, self.layers[layer], q, o, self.bt(layer), d_prefix_len, d_q_start,
+                             n_seqs, max_q_len, scale, self.stream)
+
+    def gather(self, layer, d_tok_offset, n_seqs, dst):
+        B.hswa_swa_gather(self.pool, self.layers[layer], self.d_swa_bt, self.d_seq_len, d_tok_offset, n_seqs,
+                          dst, self.stream)
+
+    def scatter(self, layer, d_tok_offset, n_seqs, src):
+        B.hswa_swa_scatter(self.pool, self.layers[layer], self.d_swa_bt, self.d_seq_len, d_tok_offset, n_seqs,
+                           src, self.stream)
+
+    def check(self):
+        return B.hswa_check(self.stream)
+
+
+def window_offsets(seq_len, window):
+    """Prefix sum of min(L_s, W) as int64 [n + 1] (packed-buffer offsets)."""
+    n = np.minimum(np.asarray(seq_len, np.int64), window)
+    off = np.zeros(len(n) + 1, np.int64)
+    off[1:] = np.cumsum(n)
+    return off

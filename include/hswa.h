@@ -1,0 +1,255 @@
+/*
+ * hswa.h -- Hybrid sliding-window attention over a dual KV pool (GB300, sm_103a).
+ *
+ * C ABI of libhswa.so. Plain pointers and sizes only.
+ *
+ * Method: "MiMo-V2.5 Series Inference Full-Link Optimization: Pushing Hybrid
+ * SWA Efficiency to the Extreme".
+ *   Sec. 1.1 (Computational Complexity Analysis): most layers attend only to
+ *     a sliding window of W = 128 tokens, a few (10 of 70) to the whole
+ *     sequence; prefill is close to compute-bound.
+ *   Sec. 1.2 (KVCache Storage Analysis): SWA layers keep only the window;
+ *     decode is close to memory-bandwidth-bound.
+ *   Sec. 2.1 (KVCache Dual Pool): a Full pool (O(N) per sequence) and an SWA
+ *     pool (O(W)), one logical sequence view with the Full index
+ *     authoritative and a Full -> SWA mapping, a joint capacity check at
+ *     admission, cross-tier transfer of SWA-mask data only, and release of
+ *     out-of-window SWA slots tied to the request lifecycle (after each
+ *     prefill chunk, at request end, every N decode tokens) with at least the
+ *     last W tokens kept (window-safety rule).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Pool layout. A layer's K pool and V pool are each
+ *     [num_pages][n_kv_heads][page_size][head_dim]
+ * elements of the pool dtype (fp32 or bf16), row-major. num_pages is
+ * cfg.full_pages for a Full layer and cfg.swa_pages for an SWA layer. All
+ * layers of one kind share one block table: a page index means the same
+ * page in every layer of that kind.
+ *
+ * Logical pages. Token position t of a sequence lies on logical page
+ * t / page_size, row t % page_size. full_bt[s][p] is the Full page of
+ * logical page p of sequence s; swa_bt[s][p] is its SWA page, or -1 when
+ * that logical page holds no SWA slot (released, or never reserved). Both
+ * tables are int32 [max_seqs][max_pages_per_seq], row-major. A slot is
+ * page * page_size + t % page_size.
+ *
+ * Sequences. Sequence ids are 0 .. max_seqs-1. Batched device calls work on
+ * sequences 0 .. n_seqs-1: row i of q / o belongs to table row i.
+ *
+ * GQA. Query head h reads kv head h / (n_q_heads / n_kv_heads).
+ *
+ * Ownership. The caller allocates and owns every device and host buffer
+ * (pools, q, o, tables, workspace, staging). The library owns only the
+ * host-side state behind hswa_pool (free lists and host mirrors of the
+ * tables) and never keeps a caller pointer beyond the call, except that
+ * hswa_sync_tables remembers which device tables it last wrote to.
+ *
+ * Ordering. Device calls enqueue work on the given stream and return
+ * without waiting. Host calls (reserve, release, ...) act on host state
+ * at once. Pool memory must hold finite values beyond a sequence's last
+ * token (allocate it zeroed): masked keys get probability exactly 0, but
+ * 0 * NaN would still be NaN.
+ *
+ * Errors. Every call checks its arguments before launching anything and
+ * returns one of the HSWA_* status codes below; no exception crosses the
+ * ABI. Device-side index checks and bounded waits do not trap: they set a
+ * device error word that hswa_check reads back.
+ */
+#ifndef HSWA_H
+#define HSWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status */
+#define HSWA_OK 0
+#define HSWA_ERR_INVALID_ARG 1 /* bad pointer, size, id or ordering          */
+#define HSWA_ERR_NO_SPACE 2    /* Full or SWA pool short of pages; no change  */
+#define HSWA_ERR_UNSUPPORTED 3 /* dtype / head_dim / head ratio not built     */
+#define HSWA_ERR_CUDA 4        /* a CUDA runtime call or launch failed        */
+#define HSWA_ERR_TIMEOUT 5     /* a bounded device wait gave up               */
+#define HSWA_ERR_BOUNDS 6      /* a device index check failed (access skipped)*/
+
+#define HSWA_KIND_FULL 0
+#define HSWA_KIND_SWA 1
+
+#define HSWA_DTYPE_F32 0
+#define HSWA_DTYPE_BF16 1
+
+/* A CUDA stream (the same handle as cudaStream_t); NULL = default stream. */
+typedef struct CUstream_st *hswa_stream_t;
+
+typedef struct hswa_pool hswa_pool; /* opaque host-side bookkeeping */
+
+typedef struct hswa_config {
+    int32_t window;            /* W: tokens kept by release (> 0)               */
+    int32_t page_size;         /* P: token slots per page (> 0)                 */
+    int32_t n_q_heads;         /* Hq                                            */
+    int32_t n_kv_heads;        /* Hkv, divides Hq                               */
+    int32_t head_dim;          /* d                                             */
+    int32_t dtype;             /* HSWA_DTYPE_*                                  */
+    int32_t full_pages;        /* pages in the Full pool                        */
+    int32_t swa_pages;         /* pages in the SWA pool                         */
+    int32_t max_seqs;          /* rows of each block table                      */
+    int32_t max_pages_per_seq; /* columns of each block table                   */
+} hswa_config;
+
+typedef struct hswa_layer {
+    int32_t kind;   /* HSWA_KIND_FULL or HSWA_KIND_SWA                          */
+    int32_t window; /* keys per query for an SWA layer (> 0); ignored for Full  */
+    void *k_pool;   /* device [num_pages][Hkv][P][d], caller-owned             */
+    void *v_pool;   /* device, same shape                                      */
+} hswa_layer;
+
+/* ------------------------------------------------ pool bookkeeping (host) */
+
+/* Create the bookkeeping of a dual pool (Sec. 2.1, KVCache Dual Pool).
+ * full_free_order / swa_free_order: the initial FIFO free lists, a
+ * permutation of 0..full_pages-1 (resp. swa_pages-1); NULL means ascending.
+ * Every table entry starts at -1 and every length at 0. *out receives the
+ * pool; free it with hswa_pool_destroy. */
+int hswa_pool_create(const hswa_config *cfg, const int32_t *full_free_order,
+                     const int32_t *swa_free_order, hswa_pool **out);
+int hswa_pool_destroy(hswa_pool *pool);
+
+/* Reserve slots for new tokens (Sec. 2.1: the access request checks the Full
+ * and the SWA capacity together). seq_ids[0..n) strictly ascending; n_new[i]
+ * tokens (>= 0) are added at positions L_i .. L_i + n_new[i] - 1. Every
+ * logical page those tokens touch that has no Full page takes one from the
+ * head of the Full free list, and likewise for SWA, in ascending (sequence,
+ * logical page) order. full_slot_out / swa_slot_out (host, sum(n_new)
+ * entries, may be NULL) receive the slots of the new tokens, sequences
+ * concatenated in argument order. If either pool is short, returns
+ * HSWA_ERR_NO_SPACE and changes nothing. Lengths grow by n_new. */
+int hswa_reserve(hswa_pool *pool, int n, const int32_t *seq_ids, const int32_t *n_new,
+                 int32_t *full_slot_out, int32_t *swa_slot_out);
+
+/* Release out-of-window SWA pages (Sec. 2.1, SWA-aware prefix cache tree:
+ * release after each prefill chunk, at request end and every N decode
+ * tokens; keep at least the last W tokens). For each listed sequence of
+ * length L, every SWA page on logical page p with (p + 1) * P <= L - W goes
+ * to the tail of the SWA free list, in ascending (sequence, page) order, and
+ * its entry becomes -1. seq_ids need not be sorted (they are processed in
+ * ascending order). *n_freed_out (may be NULL) gets the count. */
+int hswa_swa_release(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_freed_out);
+
+/* Request end: return all Full and SWA pages of the sequences (ascending
+ * sequence, then page) and set their lengths to 0. */
+int hswa_seq_free(hswa_pool *pool, int n, const int32_t *seq_ids);
+
+/* Evict the SWA segment of each sequence alone, keeping its Full pages
+ * (Sec. 2.1: the out-of-window SWA segment can be evicted while the Full
+ * segment stays). Used after hswa_swa_gather has copied the window out. */
+int hswa_swa_drop(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_freed_out);
+
+/* Give SWA pages to every in-window logical page (positions
+ * [L - min(L, W), L)) of each sequence that has none, from the head of the
+ * SWA free list in ascending (sequence, page) order; all or nothing
+ * (HSWA_ERR_NO_SPACE). Used before hswa_swa_scatter reloads a window. */
+int hswa_swa_restore(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_alloc_out);
+
+/* Host mirrors, for inspection: copies the Full table, the SWA table
+ * (int32 [max_seqs][max_pages_per_seq] each) and lengths (int32
+ * [max_seqs]); any pointer may be NULL. */
+int hswa_get_tables(const hswa_pool *pool, int32_t *full_bt, int32_t *swa_bt, int32_t *seq_len);
+
+/* Free lists in FIFO order: kind HSWA_KIND_FULL or HSWA_KIND_SWA. *count
+ * gets the length; out (may be NULL) receives up to cap entries. */
+int hswa_get_free_list(const hswa_pool *pool, int kind, int32_t *out, int32_t cap, int32_t *count);
+
+/* ------------------------------------------------- device-side calls */
+
+/* Bring the device tables (int32 [max_seqs][max_pages_per_seq] each, and
+ * lengths int32 [max_seqs]) up to date with the host state, enqueued on
+ * stream: the changed entries are packed into a pinned staging buffer owned
+ * by the pool and one small kernel reads them from there (device-mapped host
+ * memory) and writes them. The staging buffer is reused only after that
+ * kernel has finished. The first call, or a call with other device pointers
+ * than the last one, uploads the whole tables and waits for the copy. */
+int hswa_sync_tables(hswa_pool *pool, int32_t *d_full_bt, int32_t *d_swa_bt, int32_t *d_seq_len,
+                     hswa_stream_t stream);
+
+/* KV append (Sec. 2.1, dual pool: Full layers write only the Full pool and
+ * SWA layers only the SWA pool). For each token t < n_tokens with
+ * d_slots[t] >= 0: pool[slot / P][g][slot % P][:] = new[t][g][:] for K and V.
+ * k, v: device [n_tokens][Hkv][d] in the pool dtype. d_slots: device int32,
+ * the full_slot (Full layer) or swa_slot (SWA layer) array from
+ * hswa_reserve. A slot past the pool sets HSWA_ERR_BOUNDS on the device
+ * and is skipped. */
+int hswa_append_kv(const hswa_pool *pool, const hswa_layer *layer, const void *k, const void *v,
+                   const int32_t *d_slots, int n_tokens, hswa_stream_t stream);
+
+/* Bytes of workspace hswa_decode needs for a batch of n_seqs sequences. */
+size_t hswa_decode_workspace_size(const hswa_pool *pool, int n_seqs);
+
+/* One decode step of attention (Sec. 1.2: decode is memory-bound; Sec. 5.1:
+ * decode reads the SWA pool). For sequence i < n_seqs with L = d_seq_len[i]
+ * keys (the new token already appended), query q[i][h] at position L - 1
+ * attends keys [0, L) for a Full layer and [max(0, L - W), L) for an SWA
+ * layer, W = layer->window:
+ *     o[i][h] = softmax_j(scale * <q[i][h], k_j>) v_j.
+ * q, o: device [n_seqs][Hq][d] in the pool dtype. d_bt: device table of the
+ * layer's kind. L = 0 gives o = 0. ws: device workspace of at least
+ * hswa_decode_workspace_size bytes (split-K partial results), caller-owned,
+ * not read before it is written. A table entry outside the pool sets
+ * HSWA_ERR_BOUNDS on the device; that page is skipped. */
+int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale,
+                void *ws, size_t ws_bytes, hswa_stream_t stream);
+
+/* One chunked-prefill chunk of attention (Sec. 1.1: chunked prefill is
+ * close to compute-bound). Sequence i < n_seqs has d_prefix_len[i] cached
+ * tokens and n_i = d_q_start[i+1] - d_q_start[i] new tokens whose K/V are
+ * already appended; query row r (0 <= r < n_i) sits at position
+ * t = prefix + r and attends keys [0, t] (Full) or [max(0, t - W + 1), t]
+ * (SWA). q, o: device [d_q_start[n_seqs]][Hq][d]; d_q_start: device int32
+ * [n_seqs + 1], non-decreasing from 0. max_q_len >= every n_i (sizes the
+ * grid). */
+int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                       const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
+                       int n_seqs, int max_q_len, float scale, hswa_stream_t stream);
+
+/* Transfer by SWA mask (Sec. 2.1, Data Transfer: only in-window data moves;
+ * "Tiered KV Cache Offloading in vLLM", hybrid models: sliding-window
+ * layers reload only the tokens in their window). For sequence i < n_seqs
+ * with L_i = d_seq_len[i], n_i = min(L_i, W) tokens at positions
+ * [L_i - n_i, L_i) of one SWA layer are packed into dst as a K block
+ * [Hkv][n_i][d] then a V block [Hkv][n_i][d], starting at element
+ * 2 * Hkv * d * d_tok_offset[i]; d_tok_offset: device int64 [n_seqs + 1],
+ * the prefix sum of n_i. W = layer->window. dst may be device memory or
+ * pinned host memory mapped into the device address space. An in-window
+ * token without an SWA page sets HSWA_ERR_BOUNDS and is skipped. The
+ * caller must not reuse dst until work enqueued after this call on stream
+ * has finished. */
+int hswa_swa_gather(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
+                    const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, void *dst,
+                    hswa_stream_t stream);
+
+/* Inverse of hswa_swa_gather: write a packed buffer back into the layer's
+ * SWA pool pages named by d_swa_bt (after hswa_swa_restore). */
+int hswa_swa_scatter(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
+                     const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs,
+                     const void *src, hswa_stream_t stream);
+
+/* Wait for stream, then read and clear the device error word of the
+ * current device: HSWA_OK, HSWA_ERR_BOUNDS or HSWA_ERR_TIMEOUT (or
+ * HSWA_ERR_CUDA if the wait itself failed). */
+int hswa_check(hswa_stream_t stream);
+
+/* Name of the kernel variant the last device call on this host thread
+ * launched (e.g. "decode_mma_bf16_d128"); "" before any launch. */
+const char *hswa_last_kernel(void);
+
+/* Human-readable name of a status code. */
+const char *hswa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSWA_H */

@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/hswa.h declares, and its host-side pool bookkeeping matches the
+oracle's bit for bit (tables, slots, free lists) on random call traces."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import hswa_workloads as wl
+import oracle
+import hybrid_sliding_window_dual_gb300 as H
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"^[A-Za-z_][\w \*]*?\b(hswa_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("hswa_append_kv", "hswa_decode", "hswa_prefill_chunk", "hswa_swa_release",
+                     "hswa_swa_gather", "hswa_swa_scatter", "hswa_reserve", "hswa_pool_create"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(H.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def make_pair(W=128, P=16, full=600, swa=120, S=6, MP=64, seed=0, permute=True):
+    fo = wl.permutation(full, seed) if permute else None
+    so = wl.permutation(swa, seed + 100) if permute else None
+    cfg = H.Config(window=W, page_size=P, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                   dtype=H.HSWA_DTYPE_BF16, full_pages=full, swa_pages=swa, max_seqs=S,
+                   max_pages_per_seq=MP)
+    lib_pool = H.hswa_pool_create(cfg, fo, so)
+    ora = oracle.DualPool(W, P, full, swa, S, MP, full_free_order=fo, swa_free_order=so)
+    return cfg, lib_pool, ora
+
+
+def assert_same_state(cfg, lib_pool, ora):
+    f, s, lens = H.hswa_get_tables(lib_pool, cfg)
+    assert np.array_equal(f, ora.full_bt)
+    assert np.array_equal(s, ora.swa_bt)
+    assert np.array_equal(lens.astype(np.int64), ora.seq_len)
+    assert np.array_equal(H.hswa_get_free_list(lib_pool, H.HSWA_KIND_FULL), np.array(ora.full_free, np.int32))
+    assert np.array_equal(H.hswa_get_free_list(lib_pool, H.HSWA_KIND_SWA), np.array(ora.swa_free, np.int32))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bookkeeping_matches_oracle_on_random_trace(seed):
+    rng = np.random.default_rng(seed)
+    cfg, lp, ora = make_pair(seed=seed)
+    S = cfg.max_seqs
+    for step in range(400):
+        op = rng.choice(["reserve", "reserve", "reserve", "release", "free", "drop_restore"])
+        ids = np.sort(rng.choice(S, size=int(rng.integers(1, S + 1)), replace=False))
+        if op == "reserve":
+            n_new = rng.choice([0, 1, 1, 5, 17, 40], size=len(ids))
+            try:
+                exp = ora.reserve(ids, n_new)
+            except oracle.NoSpace:
+                with pytest.raises(H.NoSpace):
+                    H.hswa_reserve(lp, ids, n_new)
+            except ValueError:
+                with pytest.raises(H.HswaError):
+                    H.hswa_reserve(lp, ids, n_new)
+            else:
+                got = H.hswa_reserve(lp, ids, n_new)
+                assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1])
+        elif op == "release":
+            assert H.hswa_swa_release(lp, ids[::-1]) == ora.swa_release(ids)
+        elif op == "free":
+            H.hswa_seq_free(lp, ids[:1])
+            ora.seq_free(ids[:1])
+        else:
+            assert H.hswa_swa_drop(lp, ids) == ora.swa_drop(ids)
+            try:
+                n = ora.swa_restore(ids)
+            except oracle.NoSpace:
+                with pytest.raises(H.NoSpace):
+                    H.hswa_swa_restore(lp, ids)
+            else:
+                assert H.hswa_swa_restore(lp, ids) == n
+        assert_same_state(cfg, lp, ora)
+    H.hswa_pool_destroy(lp)
+
+
+def test_invalid_arguments_are_rejected():
+    cfg, lp, _ = make_pair()
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_reserve(lp, [3, 1], [1, 1])  # not ascending
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    with pytest.raises(H.HswaError):
+        H.hswa_reserve(lp, [cfg.max_seqs], [1])  # id out of range
+    with pytest.raises(H.HswaError):
+        H.hswa_reserve(lp, [0], [-1])
+    with pytest.raises(H.HswaError):
+        H.hswa_reserve(lp, [0], [cfg.max_pages_per_seq * cfg.page_size + 1])
+    with pytest.raises(H.HswaError):
+        H.hswa_swa_release(lp, [2, 2])
+    bad = H.Config(window=0, page_size=16, n_q_heads=8, n_kv_heads=2, head_dim=64, dtype=1,
+                   full_pages=8, swa_pages=8, max_seqs=2, max_pages_per_seq=4)
+    with pytest.raises(H.HswaError):
+        H.hswa_pool_create(bad)
+    bad.window, bad.n_kv_heads = 128, 3  # 8 % 3 != 0
+    with pytest.raises(H.HswaError):
+        H.hswa_pool_create(bad)
+    bad.n_kv_heads = 2
+    with pytest.raises(H.HswaError):
+        H.hswa_pool_create(bad, full_free_order=[0, 1, 2, 3, 4, 5, 6, 6])  # not a permutation
+    H.hswa_pool_destroy(lp)
+
+
+def test_no_space_leaves_state_unchanged():
+    cfg, lp, ora = make_pair(full=20, swa=6, permute=False)
+    H.hswa_reserve(lp, [0], [60])
+    ora.reserve([0], [60])
+    with pytest.raises(H.NoSpace):
+        H.hswa_reserve(lp, [1, 2], [16, 40])  # SWA needs 4 more, has 2
+    assert_same_state(cfg, lp, ora)
+    H.hswa_pool_destroy(lp)
+
+
+def test_device_calls_validate_before_launching():
+    """Argument errors come back as status codes without touching a GPU."""
+    cfg, lp, _ = make_pair()
+    layer = H.Layer(kind=7, window=128, k_pool=16, v_pool=16)
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_decode(lp, layer, 16, 16, 16, 16, 1, 1.0, 256, 1 << 20)
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    layer = H.Layer(kind=H.HSWA_KIND_SWA, window=0, k_pool=16, v_pool=16)
+    with pytest.raises(H.HswaError):
+        H.hswa_prefill_chunk(lp, layer, 16, 16, 16, 16, 16, 1, 4, 1.0)
+    with pytest.raises(H.HswaError):
+        H.hswa_swa_gather(lp, H.Layer(kind=H.HSWA_KIND_FULL, window=128, k_pool=16, v_pool=16),
+                          16, 16, 16, 1, 16)
+    assert H.hswa_decode_workspace_size(lp, 64) > 0
+    H.hswa_pool_destroy(lp)
