@@ -1,0 +1,471 @@
+"""Benchmark of the Hybrid-SWA dual-pool hot path on one GB300 (or N replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hswa|reference]
+                [--workload decode_batch|chunked_prefill]
+
+decode_batch (default): 64 sequences, cached lengths uniform in [1024, 32768],
+64 Q / 8 KV heads, d 128, page 64, bf16, one Full and one SWA (W = 128) layer.
+One step = reserve one token per sequence (both pools) -> sync the device
+tables -> append K/V to the Full and the SWA pool -> decode the Full layer ->
+decode the SWA layer; the SWA release runs every 64 steps.
+Metric: algorithmic HBM bytes of the step (valid KV rows read, q read, o
+written, new K/V read and written) per second.
+
+chunked_prefill: 8 sequences, cached prefix uniform in [8192, 65536], a
+4096-token chunk each; one step = reserve the chunk -> sync -> append ->
+prefill the Full layer -> prefill the SWA layer -> release. Metric: TFLOP/s
+over the valid (query, key) pairs, 4 * d * Hq per pair.
+
+With --impl reference the CPU oracle runs the same workload on a bounded
+sample of sequences per step and reports the same metric.
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import hswa_workloads as wl  # noqa: E402
+
+KV_ROW = {wl.DTYPE_BF16: 2, wl.DTYPE_F32: 4}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ dist helpers
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- workloads
+def decode_bytes(w, lens_after):
+    """Algorithmic bytes of one decode step over the Full and the SWA layer."""
+    es = KV_ROW[w.dtype]
+    row = w.n_kv_heads * w.head_dim * es          # one K (or V) row of all kv heads
+    B = len(lens_after)
+    full_kv = 2 * row * int(np.sum(lens_after))
+    swa_kv = 2 * row * int(np.sum(np.minimum(lens_after, w.window)))
+    qo = 2 * B * w.n_q_heads * w.head_dim * es   # q read + o written, per layer
+    new = 2 * 2 * B * row                          # new K/V read + written, per layer
+    return {"full_kv": full_kv, "swa_kv": swa_kv, "full_layer": full_kv + qo + new,
+            "swa_layer": swa_kv + qo + new, "step": full_kv + swa_kv + 2 * (qo + new)}
+
+
+def prefill_flops(w, prefix, chunk):
+    """Valid (query, key) pairs x 4 d Hq for a Full and an SWA layer."""
+    full = sum(c * p + c * (c + 1) // 2 for p, c in zip(prefix, chunk))
+    swa = sum(sum(min(p + r + 1, w.window) for r in range(c)) for p, c in zip(prefix, chunk))
+    k = 4 * w.head_dim * w.n_q_heads
+    return {"full": k * full, "swa": k * swa, "step": k * (full + swa)}
+
+
+class DecodeBatch:
+    """The decode-batch workload on the GPU through the C ABI."""
+
+    def __init__(self, w, extra_steps):
+        import torch
+        import hybrid_sliding_window_dual_gb300 as H
+        from hybrid_sliding_window_dual_gb300.session import DualPoolSession
+        self.H, self.torch, self.w = H, torch, w
+        B, P, W = len(w.cached), w.page_size, w.window
+        self.B = B
+        full_pages = sum(math.ceil((L + extra_steps + 1) / P) for L in w.cached) + 16
+        swa_pages = B * (math.ceil((W + 4096) / P) + 2) + 16
+        max_pages = max(math.ceil((L + extra_steps + 1) / P) for L in w.cached) + 1
+        cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                       head_dim=w.head_dim, dtype=w.dtype, full_pages=full_pages, swa_pages=swa_pages,
+                       max_seqs=B, max_pages_per_seq=max_pages)
+        self.stream = torch.cuda.Stream()
+        self.sess = DualPoolSession(cfg, [wl.KIND_FULL, wl.KIND_SWA], wl.permutation(full_pages, w.seed),
+                                    wl.permutation(swa_pages, w.seed + 1), stream=self.stream, init="empty")
+        for s, L in enumerate(w.cached):
+            for start in range(0, L, 4096):
+                self.sess.reserve([s], [min(4096, L - start)])
+                self.sess.release([s])
+        with torch.cuda.stream(self.stream):
+            for i in range(2):
+                for t, seed in ((self.sess.k[i], 10 + i), (self.sess.v[i], 20 + i)):
+                    g = torch.Generator(device="cuda")
+                    g.manual_seed(seed)
+                    flat = t.view(-1)
+                    for j in range(0, flat.numel(), 1 << 28):
+                        n = min(1 << 28, flat.numel() - j)
+                        flat[j:j + n] = torch.randn(n, generator=g, device="cuda").to(t.dtype)
+            self.sess.sync()
+        dt = wl.TORCH_DTYPE[w.dtype]
+        self.q = [wl.normal((B, w.n_q_heads, w.head_dim), 100 + i, w.dtype, "cuda") for i in range(2)]
+        self.kn = [wl.normal((B, w.n_kv_heads, w.head_dim), 200 + i, w.dtype, "cuda") for i in range(2)]
+        self.vn = [wl.normal((B, w.n_kv_heads, w.head_dim), 300 + i, w.dtype, "cuda") for i in range(2)]
+        self.o = [torch.empty(B, w.n_q_heads, w.head_dim, dtype=dt, device="cuda") for _ in range(2)]
+        # double-buffered pinned staging for the slots of a step, each buffer
+        # reused only after its previous copy has run
+        self.slot_host = [torch.empty(2, B, dtype=torch.int32, pin_memory=True) for _ in range(2)]
+        self.slot_ready = [None, None]
+        self.slot_dev = torch.empty(2, B, dtype=torch.int32, device="cuda")
+        self.sess.workspace(B)
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        self.steps_done = 0
+        self.launches = 0
+        self.decode_events = []
+        # host-buffer (end-to-end) variants
+        self.h_q = [x.cpu().pin_memory() for x in self.q]
+        self.h_kn = [x.cpu().pin_memory() for x in self.kn]
+        self.h_vn = [x.cpu().pin_memory() for x in self.vn]
+        self.h_o = [torch.empty_like(x, device="cpu").pin_memory() for x in self.o]
+        torch.cuda.synchronize()
+
+    def lens(self):
+        return self.sess.tables()[2][:self.B].astype(np.int64)
+
+    def step(self, time_full_decode=False, host_io=False):
+        torch, sess, B = self.torch, self.sess, self.B
+        fs, ss = sess.reserve(range(B), [1] * B)
+        buf = self.steps_done & 1
+        if self.slot_ready[buf] is not None:
+            self.slot_ready[buf].synchronize()
+        with torch.cuda.stream(self.stream):
+            self.slot_host[buf][0].numpy()[:] = fs
+            self.slot_host[buf][1].numpy()[:] = ss
+            self.slot_dev.copy_(self.slot_host[buf], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(self.stream)
+            self.slot_ready[buf] = ev
+            sess.sync()
+            self.launches += 1
+            for i in range(2):
+                if host_io:
+                    self.q[i].copy_(self.h_q[i], non_blocking=True)
+                    self.kn[i].copy_(self.h_kn[i], non_blocking=True)
+                    self.vn[i].copy_(self.h_vn[i], non_blocking=True)
+                sess.append(i, self.kn[i], self.vn[i], self.slot_dev[i])
+                if time_full_decode and i == 0:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(self.stream)
+                sess.decode(i, self.q[i], self.o[i], B, self.scale)
+                if time_full_decode and i == 0:
+                    e1.record(self.stream)
+                    self.decode_events.append((e0, e1))
+                if host_io:
+                    self.h_o[i].copy_(self.o[i], non_blocking=True)
+                self.launches += 4
+        self.steps_done += 1
+        if self.steps_done % 64 == 0:
+            sess.release(range(B))
+        if host_io:
+            # the step's result is read on the host
+            self.stream.synchronize()
+
+    def finish(self):
+        self.stream.synchronize()
+        st = self.sess.check()
+        if st != 0:
+            raise RuntimeError("device status %d after benchmark" % st)
+
+
+def time_steps(run, steps, stream, world):
+    import torch
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3
+
+
+def run_decode(args, world, rank, local):
+    import torch
+    w = wl.decode_batch()
+    total_steps = args.warmup + 2 * args.steps + 2
+    bench = DecodeBatch(w, total_steps)
+    hbm, _, _, peak_kind = peaks()
+    # clocks are sampled from before the warm-up to the end of the timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    for _ in range(args.warmup):
+        bench.step()
+    bench.stream.synchronize()
+    bytes_before = decode_bytes(w, bench.lens() + 1)  # lengths the first timed step decodes
+    launches0 = bench.launches
+    secs = time_steps(lambda: bench.step(time_full_decode=True), args.steps, bench.stream, world)
+    clock_info = clocks.stop()
+    launches = bench.launches - launches0
+    bytes_after = decode_bytes(w, bench.lens())
+    step_bytes = 0.5 * (bytes_before["step"] + bytes_after["step"])  # lengths grow by one per step
+    full_layer_bytes = 0.5 * (bytes_before["full_layer"] + bytes_after["full_layer"])
+    dec_ms = [a.elapsed_time(b) for a, b in bench.decode_events]
+    bench.decode_events.clear()
+    # end to end: host buffers in, host buffers out, copies inside the timed region
+    e2e_secs = time_steps(lambda: bench.step(host_io=True), args.steps, bench.stream, world)
+    bench.finish()
+    secs = max_over_ranks(secs, world)
+    e2e_secs = max_over_ranks(e2e_secs, world)
+    total_bytes = sum_over_ranks(step_bytes * args.steps, world)
+    value = total_bytes / secs / 1e9
+    es = KV_ROW[w.dtype]
+    B = len(w.cached)
+    h2d = 2 * (B * w.n_q_heads * w.head_dim * es + 2 * B * w.n_kv_heads * w.head_dim * es)
+    d2h = 2 * B * w.n_q_heads * w.head_dim * es
+    dec_s = float(np.mean(dec_ms)) / 1e3
+    achieved = full_layer_bytes / dec_s / 1e9
+    line = {
+        "metric": "Hybrid-SWA attn: decode HBM GB/s and prefill TFLOP/s (% of GB300 peak)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode_batch", "seqs": B, "cached_len": "uniform[1024,32768] seed 2",
+                   "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+                   "page": w.page_size, "window": w.window, "layers": "1 Full + 1 SWA",
+                   "l2": "inputs larger than L2 (%.1f GB KV per step)" % (step_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "decode_mma_bf16_d128 (Full layer; plan + main + combine)",
+                     "peak_source": peak_kind, "frac_of_8tbs": round(achieved / 8000.0, 4)},
+        "e2e": {"value": round(total_bytes / e2e_secs / 1e9 * (1.0), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clock_info,
+        "tokens_per_s": round(world * B * args.steps / secs, 1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(w, budget_s=args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_decode_state(w, samples):
+    """Oracle-side state of the decode-batch workload: bookkeeping for every
+    sequence, KV values only on the pages of the sampled sequences."""
+    import oracle
+    P, W = w.page_size, w.window
+    B = len(w.cached)
+    full_pages = sum(math.ceil((L + 256) / P) for L in w.cached) + 16
+    swa_pages = B * (math.ceil((W + 4096) / P) + 2) + 16
+    max_pages = max(math.ceil((L + 256) / P) for L in w.cached) + 1
+    pool = oracle.DualPool(W, P, full_pages, swa_pages, B, max_pages, wl.permutation(full_pages, w.seed),
+                           wl.permutation(swa_pages, w.seed + 1))
+    for s, L in enumerate(w.cached):
+        for start in range(0, L, 4096):
+            pool.reserve([s], [min(4096, L - start)])
+            pool.swa_release([s])
+    rng = np.random.default_rng(7)
+    kv = []
+    for kind, bt, n in ((0, pool.full_bt, full_pages), (1, pool.swa_bt, swa_pages)):
+        shape = (n, w.n_kv_heads, P, w.head_dim)
+        k = np.zeros(shape, np.uint16)
+        v = np.zeros(shape, np.uint16)
+        for s in samples:
+            for p in bt[s][bt[s] >= 0]:
+                k[p] = (rng.standard_normal(shape[1:]).astype(np.float32).view(np.uint32) >> 16)
+                v[p] = (rng.standard_normal(shape[1:]).astype(np.float32).view(np.uint32) >> 16)
+        kv.append((k, v))
+    return pool, kv
+
+
+def oracle_decode_step(w, pool, kv, samples, seed):
+    """One decode step of the oracle on the sampled sequences: reserve,
+    append, Full and SWA attention. Returns the algorithmic bytes covered."""
+    import oracle
+    B = len(w.cached)
+    fs, ss = pool.reserve(range(B), [1] * B)
+    rng = np.random.default_rng(seed)
+    lens = pool.seq_len[samples]
+    nbytes = 0
+    for layer, (slots, bt) in enumerate(((fs, pool.full_bt), (ss, pool.swa_bt))):
+        k, v = kv[layer]
+        newk = (rng.standard_normal((len(samples), w.n_kv_heads, w.head_dim)).astype(np.float32)
+                .view(np.uint32) >> 16).astype(np.uint16)
+        newv = newk[::-1].copy()
+        oracle.append_kv(k, newk, slots[samples])
+        oracle.append_kv(v, newv, slots[samples])
+        q = (rng.standard_normal((len(samples), w.n_q_heads, w.head_dim)).astype(np.float32)
+             .view(np.uint32) >> 16).astype(np.uint16)
+        oracle.attention(q, k, v, bt, np.array(samples), lens - 1, 0 if layer == 0 else w.window,
+                         1.0 / math.sqrt(w.head_dim))
+    b = decode_bytes(w, lens)
+    return b["step"]
+
+
+def cpu_baseline_decode(w, budget_s=20.0):
+    import oracle
+    B = len(w.cached)
+    samples = list(range(8))
+    pool, kv = oracle_decode_state(w, samples)
+    t0 = time.perf_counter()
+    done_bytes, steps = 0, 0
+    while time.perf_counter() - t0 < budget_s and steps < 200:
+        done_bytes += oracle_decode_step(w, pool, kv, samples, steps)
+        steps += 1
+    el = time.perf_counter() - t0
+    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": "%d decode steps over sequences %s of %d (Full + SWA layer, bookkeeping for all), %.1f s"
+                      % (steps, samples, B, el)}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: same workload, metric and unit."""
+    if rank != 0:
+        return None
+    import oracle
+    w = wl.decode_batch()
+    B = len(w.cached)
+    per_step = 2
+    samples_all = list(range(B))
+    pool, kv = oracle_decode_state(w, samples_all[:per_step * 2])
+    for i in range(args.warmup):
+        oracle_decode_step(w, pool, kv, samples_all[:per_step], i)
+    t0 = time.perf_counter()
+    total = 0
+    for i in range(args.steps):
+        total += oracle_decode_step(w, pool, kv, samples_all[per_step:2 * per_step], 1000 + i)
+    el = time.perf_counter() - t0
+    value = total / el / 1e9
+    return {
+        "impl": "reference", "metric": "Hybrid-SWA attn: decode HBM GB/s and prefill TFLOP/s (% of GB300 peak)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_batch", "seqs": B, "sample_per_step": per_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": "%d of %d sequences per step, Full + SWA layer" % (per_step, B)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="hswa", choices=["hswa", "reference"])
+    ap.add_argument("--workload", default="decode_batch", choices=["decode_batch"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    world, rank, local = dist_setup(args)
+    line = run_decode(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -607,11 +607,12 @@ extern "C" size_t hswa_decode_workspace_size(const hswa_pool *pool, int n_seqs) 
 extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                            const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale, void *ws,
                            size_t ws_bytes, hswa_stream_t stream) {
-    if (!pool || !layer || !q || !o || !d_bt || !d_seq_len || n_seqs < 0 || n_seqs > pool->cfg.max_seqs ||
-        !layer->k_pool || !layer->v_pool || (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA) ||
+    if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs ||
+        (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA) ||
         (layer->kind == HSWA_KIND_SWA && layer->window <= 0))
         return HSWA_ERR_INVALID_ARG;
     if (n_seqs == 0) return HSWA_OK;
+    if (!q || !o || !d_bt || !d_seq_len || !layer->k_pool || !layer->v_pool) return HSWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (!decode_fast_ok(pool, layer, q, o))
         return launch_attention_generic(pool, layer, q, o, d_bt, d_seq_len, nullptr, nullptr, n_seqs, n_seqs, scale,

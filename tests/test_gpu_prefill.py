@@ -1,0 +1,99 @@
+"""Chunked-prefill parity: libhswa (GPU) against the float64 oracle.
+
+A chunk of new tokens per sequence is reserved on both sides, appended with
+hswa_append_kv, and hswa_prefill_chunk runs for a Full layer (keys [0, t])
+and an SWA layer (keys [t - W + 1, t]); every output row checked is compared
+element by element with the oracle. The SWA release after the chunk must
+leave identical tables on both sides."""
+import numpy as np
+import pytest
+import torch
+
+import hswa_workloads as wl
+import oracle
+import hybrid_sliding_window_dual_gb300 as H
+from scenario import Scenario, TOL, device_out, max_err, raw_host
+
+FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
+
+
+def run_prefill_chunk(sc, chunk, seed, row_samples=None, expect_kernel=None):
+    """chunk[s] new tokens for sequence s. row_samples: per-sequence list of
+    chunk rows to check (None = all)."""
+    B = len(sc.cached)
+    prefix = sc.ora.seq_len[:B].copy()
+    chunk = np.asarray(chunk, np.int64)
+    q_start = np.zeros(B + 1, np.int64)
+    q_start[1:] = np.cumsum(chunk)
+    T = int(q_start[-1])
+    full_slots, swa_slots = sc.reserve(range(B), chunk)
+    sc.sess.sync()
+    d_prefix = torch.as_tensor(prefix.astype(np.int32), device="cuda")
+    d_qs = torch.as_tensor(q_start.astype(np.int32), device="cuda")
+    seqs = list(range(B))
+    errs = {}
+    for layer, kind in enumerate(sc.kinds):
+        slots = full_slots if kind == FULL else swa_slots
+        snap = sc.snapshot(layer, seqs)
+        q = sc.gen((T, sc.hq, sc.d), seed + 10 * layer)
+        kn = sc.gen((T, sc.hkv, sc.d), seed + 10 * layer + 1)
+        vn = sc.gen((T, sc.hkv, sc.d), seed + 10 * layer + 2)
+        qd = sc.to_dev(q)
+        o = torch.full_like(qd, float("nan"))
+        sc.sess.append(layer, sc.to_dev(kn), sc.to_dev(vn), torch.as_tensor(slots, device="cuda"))
+        sc.sess.prefill(layer, qd, o, d_prefix, d_qs, B, int(chunk.max()) if B else 0, sc.scale)
+        assert sc.sess.check() == 0
+        if expect_kernel:
+            assert H.hswa_last_kernel() == expect_kernel
+        sc.oracle_append(snap, slots, (raw_host(kn), raw_host(vn)), sc.P)
+        rows, q_seq, q_pos = [], [], []
+        for s in range(B):
+            rs = range(int(chunk[s])) if row_samples is None else row_samples[s]
+            for r in rs:
+                rows.append(int(q_start[s]) + r)
+                q_seq.append(s)
+                q_pos.append(int(prefix[s]) + r)
+        rows = np.array(rows, np.int64)
+        exp = oracle.attention(raw_host(q)[rows], snap[0], snap[1], snap[2], np.array(q_seq), np.array(q_pos),
+                               sc.window(layer), sc.scale)
+        got = device_out(o)[rows]
+        assert np.isfinite(got).all()
+        errs[kind] = max_err(got, exp)
+        assert errs[kind] <= TOL[sc.dtype], (kind, errs[kind])
+    sc.release(range(B))
+    sc.sess.sync()
+    sc.assert_tables_equal(device=True)
+    return errs
+
+
+@pytest.mark.gpu
+def test_tiny_workload_decode_then_chunk():
+    """Two sequences (300 and 77 cached), 4 Q / 1 KV heads, d 64, page 16,
+    fp32: one decode token each, then a 64-token chunk on the second
+    sequence crossing the W = 128 boundary, then release."""
+    w = wl.tiny()
+    sc = Scenario(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page_size, w.window, w.dtype, w.cached, seed=w.seed)
+    from test_gpu_decode import run_decode_step
+    run_decode_step(sc, [0, 1], seed=11)
+    sc.release([0, 1])
+    run_prefill_chunk(sc, [0, 64], seed=21)
+    assert sc.ora.seq_len[1] == 142
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [(8, 2, 64, 16, wl.DTYPE_BF16, 40), (4, 1, 64, 16, wl.DTYPE_F32, 128)])
+def test_prefill_generic_ragged(shape):
+    hq, hkv, d, P, dtype, W = shape
+    cached = [0, 5, 16, 200]
+    sc = Scenario(hq, hkv, d, P, W, dtype, cached, seed=12, extra_tokens=300)
+    run_prefill_chunk(sc, [33, 0, 100, 257], seed=5)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("permute", [False, True])
+def test_prefill_bf16_d128_ragged(permute):
+    """Chunks that are not multiples of the tile, prefixes that are not
+    multiples of the page, an empty chunk and a chunk from position 0."""
+    cached = [0, 70, 1000, 129, 4000]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=13, permute=permute, extra_tokens=700)
+    run_prefill_chunk(sc, [300, 1, 0, 513, 129], seed=9)
