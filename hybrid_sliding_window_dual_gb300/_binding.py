@@ -67,6 +67,7 @@ _SIG = {
     "hswa_decode_workspace_size": (ctypes.c_size_t, [_P, _I]),
     "hswa_decode": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _I, ctypes.c_float, _P,
                          ctypes.c_size_t, _P]),
+    "hswa_decode_noalloc": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _I, ctypes.c_float, _P]),
     "hswa_prefill_chunk": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I,
                                 ctypes.c_float, _P]),
     "hswa_swa_gather": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
@@ -212,6 +213,11 @@ def hswa_decode_workspace_size(pool, n_seqs):
 def hswa_decode(pool, layer: Layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, stream=None):
     _check(lib.hswa_decode(pool, ctypes.byref(layer), _ptr(q), _ptr(o), _ptr(d_bt), _ptr(d_seq_len),
                            int(n_seqs), float(scale), _ptr(ws), int(ws_bytes), _stream(stream)), "hswa_decode")
+
+
+def hswa_decode_noalloc(pool, layer: Layer, q, o, d_bt, d_seq_len, n_seqs, scale, stream=None):
+    _check(lib.hswa_decode_noalloc(pool, ctypes.byref(layer), _ptr(q), _ptr(o), _ptr(d_bt), _ptr(d_seq_len),
+                                   int(n_seqs), float(scale), _stream(stream)), "hswa_decode_noalloc")
 
 
 def hswa_prefill_chunk(pool, layer: Layer, q, o, d_bt, d_prefix_len, d_q_start, n_seqs, max_q_len, scale,

@@ -22,6 +22,7 @@
 // Generic path (any dtype / head_dim / ratio / page): one warp per
 // (sequence, query head) with CUDA-core dot products.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -653,4 +654,48 @@ extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const
     decode_mma_bf16_d128<<<n_ctas, 64, kDecodeSmemBytes, st>>>(tk, tv, a);
     decode_combine<<<dim3(c.n_kv_heads, n_seqs), 256, 0, st>>>(a, n_ctas);
     return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+}
+
+// ---------------------------------------------------- no-allocation decode
+// The split-K scratch of hswa_decode_noalloc: a fixed array in the device
+// image. Host code only ever passes the address cudaGetSymbolAddress gives
+// for it on the current device; the host-side symbol is a stand-in, not a
+// device address.
+static __device__ __align__(256) uint8_t g_decode_scratch[HSWA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64] = {};
+
+// Device address of the scratch array on the current device (looked up once
+// per device, with that device current), or nullptr.
+void *decode_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+}  // namespace
+
+extern "C" int hswa_decode_noalloc(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                                   const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale,
+                                   hswa_stream_t stream) {
+    if (!pool || n_seqs < 0 || n_seqs > HSWA_DECODE_NOALLOC_MAX_SEQS) return HSWA_ERR_INVALID_ARG;
+    if (n_seqs > 0 && layer && decode_fast_ok(pool, layer, q, o)) {
+        // the exact scratch the fast path will use must fit the fixed array
+        const int sms = sm_count();
+        const int per_sm = decode_ctas_per_sm();
+        if (sms <= 0 || per_sm <= 0) return HSWA_ERR_CUDA;
+        const size_t need = useg_bytes(n_seqs) + (size_t)sms * std::min(per_sm, kMaxCtasPerSm) * 2 * sizeof(Partial);
+        if (need > HSWA_DECODE_NOALLOC_SCRATCH_BYTES) return HSWA_ERR_INVALID_ARG;
+    }
+    void *ws = decode_scratch();
+    if (!ws) return HSWA_ERR_CUDA;
+    return hswa_decode(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, HSWA_DECODE_NOALLOC_SCRATCH_BYTES,
+                       stream);
 }

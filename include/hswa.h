@@ -236,6 +236,34 @@ int hswa_swa_scatter(const hswa_pool *pool, const hswa_layer *layer, const int32
                      const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs,
                      const void *src, hswa_stream_t stream);
 
+/* Decode without any device allocation by the caller or the library.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot hand over a workspace: a host program that is only given the
+ * pool, q and o pointers by another component that owns all device memory
+ * (for instance an engine that has reserved the whole HBM for KV pages), or
+ * a latency-critical loop that must not pay for an allocation. It computes
+ * exactly what hswa_decode computes, with the same arguments minus the
+ * workspace: the split-K scratch lives in a fixed array of
+ * HSWA_DECODE_NOALLOC_SCRATCH_BYTES in the library's device image, which
+ * every GPU that loads the library keeps until the process exits.
+ *
+ * Limits: n_seqs <= HSWA_DECODE_NOALLOC_MAX_SEQS, and the launch must fit
+ * the fixed scratch (it does on any part with up to 500 resident decode
+ * CTAs); otherwise the call returns HSWA_ERR_INVALID_ARG and launches
+ * nothing. The first call on a device looks up the scratch address with
+ * that device current; make that first call before any stream capture.
+ * All calls on a device share the one scratch array: two calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race
+ * on it. Nothing in the scratch has to start at zero; it keeps whatever the
+ * last call left there. Calls no cudaMalloc, cudaFree or other allocating
+ * routine. */
+#define HSWA_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define HSWA_DECODE_NOALLOC_MAX_SEQS 16384
+int hswa_decode_noalloc(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                        const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale,
+                        hswa_stream_t stream);
+
 /* Wait for stream, then read and clear the device error word of the
  * current device: HSWA_OK, HSWA_ERR_BOUNDS or HSWA_ERR_TIMEOUT (or
  * HSWA_ERR_CUDA if the wait itself failed). */
