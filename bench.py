@@ -264,6 +264,114 @@ class DecodeBatch:
             raise RuntimeError("device status %d after benchmark" % st)
 
 
+class ChunkedPrefill:
+    """The chunked-prefill workload on the GPU through the C ABI.
+
+    Setup reserves the cached prefixes (chunk by chunk, releasing the SWA
+    window after each) and then the 4096-token chunk of every sequence. A
+    timed step appends the chunk's K/V to the Full and the SWA pool and runs
+    the Full and the SWA prefill; repeating it recomputes the same chunk, so
+    every step has the same prefixes. The SWA release of the chunk runs once,
+    after the last step."""
+
+    def __init__(self, w):
+        import torch
+        import hybrid_sliding_window_dual_gb300 as H
+        from hybrid_sliding_window_dual_gb300.session import DualPoolSession
+        self.torch, self.w = torch, w
+        B, P, W, C = len(w.cached), w.page_size, w.window, w.n_new
+        self.B = B
+        full_pages = sum(math.ceil((L + C) / P) for L in w.cached) + 16
+        swa_pages = B * (math.ceil((W + C) / P) + 2) + 16
+        max_pages = max(math.ceil((L + C) / P) for L in w.cached) + 1
+        cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                       head_dim=w.head_dim, dtype=w.dtype, full_pages=full_pages, swa_pages=swa_pages,
+                       max_seqs=B, max_pages_per_seq=max_pages)
+        self.stream = torch.cuda.Stream()
+        self.sess = DualPoolSession(cfg, [wl.KIND_FULL, wl.KIND_SWA], wl.permutation(full_pages, w.seed),
+                                    wl.permutation(swa_pages, w.seed + 1), stream=self.stream, init="empty")
+        for s, L in enumerate(w.cached):
+            for start in range(0, L, C):
+                self.sess.reserve([s], [min(C, L - start)])
+                self.sess.release([s])
+        self.prefix = np.array(w.cached, np.int64)
+        fs, ss = self.sess.reserve(range(B), [C] * B)
+        with torch.cuda.stream(self.stream):
+            for i in range(2):
+                for t, seed in ((self.sess.k[i], 10 + i), (self.sess.v[i], 20 + i)):
+                    g = torch.Generator(device="cuda")
+                    g.manual_seed(seed)
+                    flat = t.view(-1)
+                    for j in range(0, flat.numel(), 1 << 28):
+                        n = min(1 << 28, flat.numel() - j)
+                        flat[j:j + n] = torch.randn(n, generator=g, device="cuda").to(t.dtype)
+            self.sess.sync()
+        T = B * C
+        self.T, self.C = T, C
+        dt = wl.TORCH_DTYPE[w.dtype]
+        self.slots = [torch.as_tensor(fs, device="cuda"), torch.as_tensor(ss, device="cuda")]
+        self.q = [wl.normal((T, w.n_q_heads, w.head_dim), 400 + i, w.dtype, "cuda") for i in range(2)]
+        self.kn = [wl.normal((T, w.n_kv_heads, w.head_dim), 500 + i, w.dtype, "cuda") for i in range(2)]
+        self.vn = [wl.normal((T, w.n_kv_heads, w.head_dim), 600 + i, w.dtype, "cuda") for i in range(2)]
+        self.o = [torch.empty(T, w.n_q_heads, w.head_dim, dtype=dt, device="cuda") for _ in range(2)]
+        self.d_prefix = torch.as_tensor(self.prefix.astype(np.int32), device="cuda")
+        self.d_qs = torch.arange(0, T + 1, C, dtype=torch.int32, device="cuda")
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        self.events = [[], []]
+        self.launches = 0
+        torch.cuda.synchronize()
+
+    def flops(self):
+        return prefill_flops(self.w, self.prefix.tolist(), [self.C] * self.B)
+
+    def step(self, timed=False):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            for i in range(2):
+                self.sess.append(i, self.kn[i], self.vn[i], self.slots[i])
+                if timed:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(self.stream)
+                self.sess.prefill(i, self.q[i], self.o[i], self.d_prefix, self.d_qs, self.B, self.C, self.scale)
+                if timed:
+                    e1.record(self.stream)
+                    self.events[i].append((e0, e1))
+                self.launches += 2
+
+    def finish(self):
+        self.sess.release(range(self.B))
+        self.stream.synchronize()
+        st = self.sess.check()
+        if st != 0:
+            raise RuntimeError("device status %d after benchmark" % st)
+
+
+def measure_prefill(steps, warmup):
+    """Whole-chunk TFLOP/s of the chunked-prefill workload (valid pairs only)."""
+    w = wl.chunked_prefill()
+    pb = ChunkedPrefill(w)
+    for _ in range(warmup):
+        pb.step()
+    pb.stream.synchronize()
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(pb.stream)
+    for _ in range(steps):
+        pb.step(timed=True)
+    e1.record(pb.stream)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) / 1e3
+    f = pb.flops()
+    full_ms = float(np.mean([a.elapsed_time(b) for a, b in pb.events[0]]))
+    swa_ms = float(np.mean([a.elapsed_time(b) for a, b in pb.events[1]]))
+    pb.finish()
+    return {"step_tflops": f["step"] * steps / secs / 1e12, "ms_per_step": secs / steps * 1e3,
+            "full_tflops": f["full"] / (full_ms / 1e3) / 1e12, "full_ms": full_ms,
+            "swa_tflops": f["swa"] / (swa_ms / 1e3) / 1e12, "swa_ms": swa_ms,
+            "valid_tflop_per_step": f["step"] / 1e12, "tokens_per_s": pb.T * steps / secs,
+            "launches": pb.launches}
+
+
 def time_steps(run, steps, stream, world):
     import torch
     barrier(world)
@@ -335,6 +443,20 @@ def run_decode(args, world, rank, local):
         "clocks": clock_info,
         "tokens_per_s": round(world * B * args.steps / secs, 1),
     }
+    if not args.no_prefill:
+        del bench
+        torch.cuda.empty_cache()
+        _, bf16, bf16_sus, _ = peaks()
+        pf = measure_prefill(args.prefill_steps, 1)
+        line["prefill"] = {
+            "workload": "chunked_prefill (8 seqs, prefix U[8192,65536] seed 3, chunk 4096, Full + SWA layer)",
+            "tflops": round(pf["step_tflops"], 1), "unit": "TFLOP/s", "frac": round(pf["step_tflops"] / bf16_sus, 4),
+            "peak": bf16_sus, "peak_kind": "bf16 sustained (measured)",
+            "full_layer_tflops": round(pf["full_tflops"], 1), "full_layer_ms": round(pf["full_ms"], 3),
+            "swa_layer_tflops": round(pf["swa_tflops"], 2), "swa_layer_ms": round(pf["swa_ms"], 3),
+            "valid_tflop_per_step": round(pf["valid_tflop_per_step"], 3),
+            "ms_per_step": round(pf["ms_per_step"], 3), "tokens_per_s": round(pf["tokens_per_s"], 1),
+            "kernel": "prefill_tc_bf16_d128"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(w, budget_s=args.cpu_budget)
     return line
@@ -450,6 +572,8 @@ def main():
     ap.add_argument("--workload", default="decode_batch", choices=["decode_batch"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-steps", type=int, default=5)
     args = ap.parse_args()
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -3,22 +3,501 @@
 // "MiMo-V2.5 Series Inference Full-Link Optimization", Sec. 1.1: in chunked
 // prefill the attention is close to compute-bound; SWA layers attend only to
 // the last W tokens, so their cost per query is O(W) instead of O(N).
+//
+// Fast path (bf16, d = 128, page 64, an even number of query heads per kv
+// head): one CTA per (sequence, block of 128 chunk rows, pair of query heads
+// of one kv head), on the 5th-generation tensor cores.
+//   * S = Q K^T and O += P V are tcgen05.mma (M = 128 rows, N = 128, K = 16)
+//     with fp32 accumulators in tensor memory: S_A, S_B, O_A, O_B take the
+//     512 TMEM columns of the SM; P (bf16) is written back over S and read by
+//     the PV MMA straight from TMEM.
+//   * Warp 8 streams Q (once) and K / V tiles of 128 keys (two pages, two
+//     64-column boxes per page, 128-byte swizzle) by TMA into a 4-slot ring.
+//   * Warp 9 issues the MMAs (one thread) and commits them to mbarriers.
+//   * Warps 0-3 and 4-7 own query head A and B: one thread per query row
+//     reads its row of S from TMEM, applies the causal / window mask on the
+//     tiles that need it, keeps the running max in the log2 domain and only
+//     rescales O (in TMEM) when the max grows by more than 2^8, writes P,
+//     and at the end normalises its row of O and stores it.
+//   * The KV range of a block is clipped to the tiles its rows can see: all
+//     of [0, t] for a Full layer, [t - W + 1, t] for an SWA layer.
+// Every wait is bounded; on a timeout the CTA records HSWA_ERR_TIMEOUT,
+// drains its copies and MMAs, frees its TMEM and returns.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
+
+namespace hswa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kP = 64;
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per KV tile (two pages)
+constexpr int kSlots = 4;
+constexpr uint32_t kTileBytes = kBN * kD * 2;  // 32 KB: one K or V tile
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column half (128 rows x 128 B)
+constexpr uint32_t kBoxBytes = kP * 128;         // one page x 64 columns
+constexpr int kThreads = 320;
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+
+struct PrefillSmem {
+    uint8_t q[2][kTileBytes];          // Q_A, Q_B: [d half][128 rows][128 B]
+    uint8_t kv[kSlots][kTileBytes];    // K or V tiles: [d half][128 keys][128 B]
+    uint64_t q_full;
+    uint64_t kv_full[kSlots], kv_empty[kSlots];
+    uint64_t s_full[2], p_full[2], o_final[2];
+    uint32_t tmem_base;
+    int32_t abort;
+};
+constexpr size_t kPrefillSmemBytes = sizeof(PrefillSmem) + 1024;
+
+struct PrefillArgs {
+    const int32_t *bt;
+    const int32_t *prefix;
+    const int32_t *q_start;
+    __nv_bfloat16 *o;
+    int32_t n_seqs, bt_stride, hq, hkv, window, num_pages;
+    int32_t kv_rows;  // rows of the pool tensor map (OOB row = zero fill)
+    float scale_log2;
+    int *err;
+};
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle, sm_100 format.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= 1ull << 46;  // descriptor version
+    d |= 2ull << 61;  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N.
+constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
+constexpr uint32_t kIdescPV = idesc_bf16(kBM, kD, true);
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+#define HSWA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                   "=r"(r[i + 6]), "=r"(r[i + 7])
+#define HSWA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                   "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : HSWA_R8(0), HSWA_R8(8), HSWA_R8(16), HSWA_R8(24)
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        HSWA_W8(0), HSWA_W8(8), HSWA_W8(16), HSWA_W8(24)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------- work unit
+struct Unit {
+    int32_t s, qb, hp, g;
+    int32_t n_rows;     // valid rows of this block
+    int32_t row0;       // q row of the block's first row
+    int32_t p0;         // position of the first row
+    int32_t tile_lo;    // first KV tile (128 keys)
+    int32_t n_tiles;
+    int32_t L;          // keys of the sequence after the chunk
+};
+
+__device__ __forceinline__ bool make_unit(const PrefillArgs &a, Unit &u) {
+    u.hp = blockIdx.x;
+    u.qb = blockIdx.y;
+    u.s = blockIdx.z;
+    const int32_t g_heads = a.hq / a.hkv;
+    u.g = (2 * u.hp) / g_heads;
+    const int32_t q0 = a.q_start[u.s], n = a.q_start[u.s + 1] - q0;
+    if (u.qb * kBM >= n) return false;
+    u.n_rows = min(kBM, n - u.qb * kBM);
+    u.row0 = q0 + u.qb * kBM;
+    const int32_t pre = a.prefix[u.s];
+    u.p0 = pre + u.qb * kBM;
+    u.L = pre + n;
+    const int32_t t_max = u.p0 + u.n_rows - 1;
+    const int32_t key_lo = (a.window > 0 && u.p0 - a.window + 1 > 0) ? u.p0 - a.window + 1 : 0;
+    u.tile_lo = key_lo / kBN;
+    u.n_tiles = t_max / kBN - u.tile_lo + 1;
+    return true;
+}
+
+// ------------------------------------------------------------------ roles
+__device__ void prefill_producer(PrefillSmem &sm, const CUtensorMap *tq, const CUtensorMap *tk,
+                                 const CUtensorMap *tv, const PrefillArgs &a, const Unit &u) {
+    prefetch_tmap(tq);
+    prefetch_tmap(tk);
+    prefetch_tmap(tv);
+    mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+    for (int x = 0; x < 2; ++x)
+        for (int dh = 0; dh < 2; ++dh)
+            tma_load_3d(sm.q[x] + dh * kHalfBytes, tq, dh * 64, 2 * u.hp + x, u.row0, &sm.q_full);
+    const int32_t *btrow = a.bt + (int64_t)u.s * a.bt_stride;
+    // pages the block's rows can see; the first tile may start on an older
+    // page (released for an SWA layer), which is filled with zeros instead
+    const int32_t last_page = (u.L - 1) / kP;
+    const int32_t first_page = (a.window > 0 && u.p0 - a.window + 1 > 0 ? u.p0 - a.window + 1 : 0) / kP;
+    int issued = 0;
+    for (int i = 0; i < 2 * u.n_tiles; ++i) {
+        const int slot = i % kSlots;
+        if (!mbar_wait(&sm.kv_empty[slot], ((i / kSlots) & 1) ^ 1, a.err) || *(volatile int32_t *)&sm.abort) {
+            sm.abort = 1;
+            break;
+        }
+        const CUtensorMap *map = (i & 1) ? tv : tk;
+        const int32_t tile = u.tile_lo + (i >> 1);
+        mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
+        for (int pg = 0; pg < 2; ++pg) {
+            const int32_t lp = tile * 2 + pg;
+            int32_t row = a.kv_rows;  // out of range: the copy fills zeros
+            if (lp >= first_page && lp <= last_page) {
+                const int32_t page = lp < a.bt_stride ? btrow[lp] : -1;
+                if (page >= 0 && page < a.num_pages)
+                    row = (page * a.hkv + u.g) * kP;
+                else
+                    set_error(a.err, HSWA_ERR_BOUNDS);
+            }
+            for (int dh = 0; dh < 2; ++dh)
+                tma_load_2d(sm.kv[slot] + dh * kHalfBytes + pg * kBoxBytes, map, dh * 64, row, &sm.kv_full[slot]);
+        }
+        ++issued;
+    }
+    // drain: never leave copies landing in shared memory after the CTA ends
+    for (int i = max(0, issued - kSlots); i < issued; ++i) mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err);
+}
+
+__device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u) {
+    const uint32_t tbase = sm.tmem_base;
+    const uint32_t t_s[2] = {tbase, tbase + 128}, t_o[2] = {tbase + 256, tbase + 384};
+    const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+    bool ok = mbar_wait(&sm.q_full, 0, a.err);
+    tc_fence_after();
+    // S_x = Q_x K^T over d = 128: 8 steps of K = 16 (32 bytes inside a 128-byte swizzle row)
+    auto issue_s = [&](int x, uint32_t k_addr) {
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            mma_ss(t_s[x], sdesc(q_addr[x] + off, 16, 1024), sdesc(k_addr + off, 16, 1024), kIdescQK, kk > 0);
+        }
+    };
+    // O_x += P_x V over 128 keys: 8 steps of K = 16 keys (2048 bytes of V rows)
+    auto issue_pv = [&](int x, uint32_t v_addr, bool first_tile) {
+        for (int kk = 0; kk < 8; ++kk)
+            mma_ts(t_o[x], t_s[x] + kk * 8, sdesc(v_addr + kk * 2048, kHalfBytes, 1024), kIdescPV,
+                   (first_tile && kk == 0) ? 0u : 1u);
+    };
+    const int n = u.n_tiles;
+    if (ok && n > 0) {
+        // tile 0: S_A(0), S_B(0)
+        ok = mbar_wait(&sm.kv_full[0], 0, a.err);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t k0 = smem_u32(sm.kv[0]);
+            issue_s(0, k0);
+            mma_commit(&sm.s_full[0]);
+            issue_s(1, k0);
+            mma_commit(&sm.s_full[1]);
+            mma_commit(&sm.kv_empty[0]);
+        }
+        for (int j = 0; ok && j < n; ++j) {
+            const int iv = 2 * j + 1, ik = 2 * j + 2;
+            const int sv = iv % kSlots, sk = ik % kSlots;
+            ok = mbar_wait(&sm.kv_full[sv], (iv / kSlots) & 1, a.err) && mbar_wait(&sm.p_full[0], j & 1, a.err) &&
+                 !*(volatile int32_t *)&sm.abort;
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t v_addr = smem_u32(sm.kv[sv]);
+            issue_pv(0, v_addr, j == 0);
+            const bool more = j + 1 < n;
+            uint32_t k_addr = 0;
+            if (more) {
+                ok = mbar_wait(&sm.kv_full[sk], (ik / kSlots) & 1, a.err);
+                if (!ok) break;
+                tc_fence_after();
+                k_addr = smem_u32(sm.kv[sk]);
+                issue_s(0, k_addr);
+                mma_commit(&sm.s_full[0]);
+            }
+            ok = mbar_wait(&sm.p_full[1], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(1, v_addr, j == 0);
+            mma_commit(&sm.kv_empty[sv]);
+            if (more) {
+                issue_s(1, k_addr);
+                mma_commit(&sm.s_full[1]);
+                mma_commit(&sm.kv_empty[sk]);
+            }
+        }
+    }
+    mma_commit(&sm.o_final[0]);
+    mma_commit(&sm.o_final[1]);
+    if (!ok) sm.abort = 1;
+}
+
+__device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Unit &u, int x) {
+    const int warp = (threadIdx.x >> 5) & 3;
+    const int r = warp * 32 + (threadIdx.x & 31);  // query row of this thread
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_s = sm.tmem_base + lane_off + 128 * x;
+    const uint32_t t_o = sm.tmem_base + lane_off + 256 + 128 * x;
+    const int32_t t = u.p0 + min(r, u.n_rows - 1);  // rows past the chunk repeat the last valid row
+    const int32_t t_min = u.p0, t_max = u.p0 + u.n_rows - 1;
+    const int32_t W = a.window;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < u.n_tiles; ++j) {
+        ok = mbar_wait(&sm.s_full[x], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + 32 * c, sr[c]);
+        tmem_wait_ld();
+        const int32_t k0 = (u.tile_lo + j) * kBN;
+        const bool need_mask = (k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1);
+        const int32_t hi_c = t - k0;                         // keys c <= hi_c
+        const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;    // keys c >= lo_c
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float v = __uint_as_float(sr[c][i]) * a.scale_log2;
+                if (need_mask) {
+                    const int col = c * 32 + i;
+                    v = (col <= hi_c && col >= lo_c) ? v : -INFINITY;
+                }
+                sr[c][i] = __float_as_uint(v);
+                mx = fmaxf(mx, v);
+            }
+        // A new reference max only when the row max grows by more than 2^8;
+        // then O (nothing before the first PV) and l are rescaled. TMEM loads
+        // and stores are warp-wide, so the whole warp takes the rescale path
+        // when any of its rows needs it (the others scale by 1).
+        const bool need = mx > m_used + kRescaleLog2;
+        const bool resc = need && j > 0 && m_used != -INFINITY;
+        const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + 32 * c, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                tmem_st32(t_o + 32 * c, ov);
+            }
+        }
+        l *= alpha;
+        if (need) m_used = mx;
+        const float m_safe = m_used == -INFINITY ? 0.f : m_used;
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float p0 = fast_exp2(__uint_as_float(sr[c][2 * i]) - m_safe);
+                const float p1 = fast_exp2(__uint_as_float(sr[c][2 * i + 1]) - m_safe);
+                sum += p0 + p1;
+                pk[i] = pack_bf16(p0, p1);
+            }
+            // P row: 16 packed columns per 32 keys, written over the start of S
+            if (c & 1) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sr[c - 1][16 + i] = pk[i];
+                tmem_st32(t_s + 32 * (c >> 1), sr[c - 1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sr[c][i] = pk[i];
+            }
+        }
+        l += sum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[x]);
+    }
+    // epilogue: wait for the last PV (always: TMEM is freed after this
+    // function returns), normalise this row of O and store it
+    const bool fin = mbar_wait(&sm.o_final[x], 0, a.err);
+    ok = __all_sync(0xffffffffu, ok && fin);
+    if (!ok) {
+        sm.abort = 1;
+        return;
+    }
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int h = 2 * u.hp + x;
+    uint4 *dst = reinterpret_cast<uint4 *>(a.o + ((int64_t)(u.row0 + r) * a.hq + h) * kD);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(t_o + 32 * c, ov);
+        tmem_wait_ld();
+        if (r < u.n_rows) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
+                w.y = pack_bf16(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
+                w.z = pack_bf16(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
+                w.w = pack_bf16(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
+                dst[c * 4 + i] = w;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_bf16_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, PrefillArgs a) {
+    Unit u;
+    if (!make_unit(a, u)) return;
+    extern __shared__ uint8_t raw[];
+    PrefillSmem &sm =
+        *reinterpret_cast<PrefillSmem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.q_full, 1);
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&sm.kv_full[i], 1);
+            mbar_init(&sm.kv_empty[i], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&sm.s_full[x], 1);
+            mbar_init(&sm.p_full[x], 128);
+            mbar_init(&sm.o_final[x], 1);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32(&sm.tmem_base)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp < 8)
+        prefill_softmax(sm, a, u, warp >> 2);
+    else if (warp == 8) {
+        if ((threadIdx.x & 31) == 0) prefill_producer(sm, &tq, &tk, &tv, a, u);
+        __syncwarp();
+    } else {
+        if ((threadIdx.x & 31) == 0) prefill_mma(sm, a, u);
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(sm.tmem_base));
+}
+
+bool prefill_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
+    const hswa_config &c = pool->cfg;
+    const int g = c.n_q_heads / c.n_kv_heads;
+    return c.dtype == HSWA_DTYPE_BF16 && c.head_dim == kD && c.page_size == kP && g % 2 == 0 &&
+           ((uintptr_t)q & 15) == 0 && ((uintptr_t)o & 15) == 0 && ((uintptr_t)layer->k_pool & 15) == 0 &&
+           ((uintptr_t)layer->v_pool & 15) == 0;
+}
+
+}  // namespace
+}  // namespace hswa
 
 using namespace hswa;
 
 extern "C" int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                                   const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
-                                  int n_seqs, int max_q_len, float scale, hswa_stream_t stream) {
-    if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs || max_q_len < 0 ||
+                                  int n_seqs, int total_q, int max_q_len, float scale, hswa_stream_t stream) {
+    if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs || max_q_len < 0 || total_q < 0 ||
+        (n_seqs > 0 && max_q_len > total_q) ||
         (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA) ||
         (layer->kind == HSWA_KIND_SWA && layer->window <= 0))
         return HSWA_ERR_INVALID_ARG;
-    if (n_seqs == 0 || max_q_len == 0) return HSWA_OK;
+    if (n_seqs == 0 || max_q_len == 0 || total_q == 0) return HSWA_OK;
     if (!q || !o || !d_bt || !d_prefix_len || !d_q_start || !layer->k_pool || !layer->v_pool)
         return HSWA_ERR_INVALID_ARG;
-    return launch_attention_generic(pool, layer, q, o, d_bt, nullptr, d_prefix_len, d_q_start, max_q_len, n_seqs,
-                                    scale, 1, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!prefill_fast_ok(pool, layer, q, o))
+        return launch_attention_generic(pool, layer, q, o, d_bt, nullptr, d_prefix_len, d_q_start, max_q_len,
+                                        n_seqs, scale, 1, st);
+    const hswa_config &c = pool->cfg;
+    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+    const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
+    if (rows >= (1ull << 31)) return HSWA_ERR_UNSUPPORTED;
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_3d(&tq, q, kD, c.n_q_heads, (uint64_t)total_q, 64, 1, kBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tk, layer->k_pool, rows, kD, kP, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tv, layer->v_pool, rows, kD, kP, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return HSWA_ERR_CUDA;
+    PrefillArgs a;
+    a.bt = d_bt;
+    a.prefix = d_prefix_len;
+    a.q_start = d_q_start;
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.n_seqs = n_seqs;
+    a.bt_stride = c.max_pages_per_seq;
+    a.hq = c.n_q_heads;
+    a.hkv = c.n_kv_heads;
+    a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
+    a.num_pages = num_pages;
+    a.kv_rows = (int32_t)rows;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.err = error_word();
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(prefill_tc_bf16_d128, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPrefillSmemBytes) != cudaSuccess)
+            return HSWA_ERR_CUDA;
+        attr = true;
+    }
+    set_last_kernel("prefill_tc_bf16_d128");
+    dim3 grid(c.n_q_heads / 2, (max_q_len + kBM - 1) / kBM, n_seqs);
+    prefill_tc_bf16_d128<<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
 }

@@ -107,7 +107,7 @@ class DualPoolSession:
 
     def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale):
         B.hswa_prefill_chunk(self.pool, self.layers[layer], q, o, self.bt(layer), d_prefix_len, d_q_start,
-                             n_seqs, max_q_len, scale, self.stream)
+                             n_seqs, q.shape[0], max_q_len, scale, self.stream)
 
     def gather(self, layer, d_tok_offset, n_seqs, dst):
         B.hswa_swa_gather(self.pool, self.layers[layer], self.d_swa_bt, self.d_seq_len, d_tok_offset, n_seqs,

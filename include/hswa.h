@@ -207,12 +207,14 @@ int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
  * tokens and n_i = d_q_start[i+1] - d_q_start[i] new tokens whose K/V are
  * already appended; query row r (0 <= r < n_i) sits at position
  * t = prefix + r and attends keys [0, t] (Full) or [max(0, t - W + 1), t]
- * (SWA). q, o: device [d_q_start[n_seqs]][Hq][d]; d_q_start: device int32
- * [n_seqs + 1], non-decreasing from 0. max_q_len >= every n_i (sizes the
- * grid). */
+ * (SWA). q, o: device [total_q][Hq][d] with total_q = d_q_start[n_seqs];
+ * d_q_start: device int32 [n_seqs + 1], non-decreasing from 0; max_q_len >=
+ * every n_i (sizes the grid). The host passes total_q and max_q_len because
+ * it cannot read d_q_start without waiting for the device; rows are never
+ * read past total_q. */
 int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                        const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
-                       int n_seqs, int max_q_len, float scale, hswa_stream_t stream);
+                       int n_seqs, int total_q, int max_q_len, float scale, hswa_stream_t stream);
 
 /* Transfer by SWA mask (Sec. 2.1, Data Transfer: only in-window data moves;
  * "Tiered KV Cache Offloading in vLLM", hybrid models: sliding-window

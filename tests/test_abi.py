@@ -143,7 +143,7 @@ def test_device_calls_validate_before_launching():
     assert e.value.status == H.HSWA_ERR_INVALID_ARG
     layer = H.Layer(kind=H.HSWA_KIND_SWA, window=0, k_pool=16, v_pool=16)
     with pytest.raises(H.HswaError):
-        H.hswa_prefill_chunk(lp, layer, 16, 16, 16, 16, 16, 1, 4, 1.0)
+        H.hswa_prefill_chunk(lp, layer, 16, 16, 16, 16, 16, 1, 4, 4, 1.0)
     with pytest.raises(H.HswaError):
         H.hswa_swa_gather(lp, H.Layer(kind=H.HSWA_KIND_FULL, window=128, k_pool=16, v_pool=16),
                           16, 16, 16, 1, 16)

@@ -97,3 +97,36 @@ def test_prefill_bf16_d128_ragged(permute):
     cached = [0, 70, 1000, 129, 4000]
     sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=13, permute=permute, extra_tokens=700)
     run_prefill_chunk(sc, [300, 1, 0, 513, 129], seed=9)
+
+
+@pytest.mark.gpu
+def test_prefill_fast_path_dispatch_and_window_wider_than_chunk():
+    """Tile-aligned and unaligned prefixes around the window edge."""
+    cached = [127, 128, 255, 256, 60]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=14, extra_tokens=400)
+    run_prefill_chunk(sc, [128, 129, 1, 256, 300], seed=3, expect_kernel="prefill_tc_bf16_d128")
+
+
+@pytest.mark.gpu
+def test_chunked_prefill_full_size_sampled():
+    """8 sequences, cached prefix uniform in [8192, 65536], 4096-token chunk,
+    64/8 heads, d 128, page 64: the chunked-prefill workload in the launch
+    configuration the benchmark times. The oracle checks rows at the tile
+    edges and the chunk ends of every sequence, on every head."""
+    w = wl.chunked_prefill()
+    sc = Scenario(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page_size, w.window, w.dtype, w.cached, seed=w.seed,
+                  extra_tokens=w.n_new + 64)
+    rows = [0, 1, 127, 128, 129, 1000, 2047, 4094, 4095]
+    run_prefill_chunk(sc, [w.n_new] * len(w.cached), seed=77, row_samples=[rows] * len(w.cached),
+                      expect_kernel="prefill_tc_bf16_d128")
+
+
+@pytest.mark.gpu
+def test_prefill_swa_after_release_reads_only_live_pages():
+    """Prefixes built chunk by chunk with a release after each, so the SWA
+    pages below the window are gone; the SWA prefill must neither read them
+    nor report them (its first key tile may start below the window)."""
+    cached = [1000, 777, 130, 2049]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=15, chunk=100, extra_tokens=600)
+    assert (sc.ora.swa_bt[:, :10] < 0).any()
+    run_prefill_chunk(sc, [200, 129, 64, 500], seed=4, expect_kernel="prefill_tc_bf16_d128")
