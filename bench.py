@@ -346,9 +346,8 @@ class ChunkedPrefill:
             raise RuntimeError("device status %d after benchmark" % st)
 
 
-def measure_prefill(steps, warmup):
+def measure_prefill(steps, warmup, w):
     """Whole-chunk TFLOP/s of the chunked-prefill workload (valid pairs only)."""
-    w = wl.chunked_prefill()
     pb = ChunkedPrefill(w)
     for _ in range(warmup):
         pb.step()
@@ -387,9 +386,20 @@ def time_steps(run, steps, stream, world):
     return e0.elapsed_time(e1) / 1e3
 
 
+def workload(args, name):
+    if name == "decode_batch":
+        w = wl.decode_batch()
+    else:
+        w = wl.chunked_prefill()
+    if args.seqs:
+        import dataclasses
+        w = dataclasses.replace(w, cached=w.cached[:args.seqs])
+    return w
+
+
 def run_decode(args, world, rank, local):
     import torch
-    w = wl.decode_batch()
+    w = workload(args, "decode_batch")
     total_steps = args.warmup + 2 * args.steps + 2
     bench = DecodeBatch(w, total_steps)
     hbm, _, _, peak_kind = peaks()
@@ -447,7 +457,7 @@ def run_decode(args, world, rank, local):
         del bench
         torch.cuda.empty_cache()
         _, bf16, bf16_sus, _ = peaks()
-        pf = measure_prefill(args.prefill_steps, 1)
+        pf = measure_prefill(args.prefill_steps, 1, workload(args, "chunked_prefill"))
         line["prefill"] = {
             "workload": "chunked_prefill (8 seqs, prefix U[8192,65536] seed 3, chunk 4096, Full + SWA layer)",
             "tflops": round(pf["step_tflops"], 1), "unit": "TFLOP/s", "frac": round(pf["step_tflops"] / bf16_sus, 4),
@@ -563,13 +573,47 @@ def run_reference(args, world, rank):
     }
 
 
+def run_prefill_line(args, world, rank, local):
+    """--workload chunked_prefill: one line whose value is the chunk's TFLOP/s."""
+    w = workload(args, "chunked_prefill")
+    _, bf16, bf16_sus, kind = peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    barrier(world)
+    pf = measure_prefill(args.steps, args.warmup, w)
+    clock_info = clocks.stop()
+    secs = max_over_ranks(pf["ms_per_step"] * args.steps / 1e3, world)
+    total = sum_over_ranks(pf["valid_tflop_per_step"] * args.steps, world)
+    value = total / secs
+    return {
+        "metric": "Hybrid-SWA attn: decode HBM GB/s and prefill TFLOP/s (% of GB300 peak)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "chunked_prefill", "seqs": len(w.cached), "prefix": "uniform[8192,65536] seed 3",
+                   "chunk": w.n_new, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+                   "page": w.page_size, "window": w.window, "layers": "1 Full + 1 SWA",
+                   "l2": "inputs larger than L2", "flops": "4 d Hq per valid (query, key) pair"},
+        "roofline": {"bound": "tensor", "achieved": round(pf["full_tflops"], 1), "peak": bf16_sus,
+                     "unit": "TFLOP/s", "frac": round(pf["full_tflops"] / bf16_sus, 4), "traffic": None,
+                     "kernel": "prefill_tc_bf16_d128 (Full layer)", "peak_source": kind + " sustained",
+                     "frac_of_burst": round(pf["full_tflops"] / bf16, 4)},
+        "swa_layer_tflops": round(pf["swa_tflops"], 2),
+        "gpu_launches": 4 * args.steps,
+        "clocks": clock_info,
+        "tokens_per_s": round(world * pf["tokens_per_s"], 1),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="hswa", choices=["hswa", "reference"])
-    ap.add_argument("--workload", default="decode_batch", choices=["decode_batch"])
+    ap.add_argument("--workload", default="decode_batch", choices=["decode_batch", "chunked_prefill"])
+    ap.add_argument("--seqs", type=int, default=0, help="use only the first N sequences (small profiling case)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
@@ -583,7 +627,10 @@ def main():
             print(json.dumps(line), flush=True)
         return
     world, rank, local = dist_setup(args)
-    line = run_decode(args, world, rank, local)
+    if args.workload == "chunked_prefill":
+        line = run_prefill_line(args, world, rank, local)
+    else:
+        line = run_decode(args, world, rank, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -128,6 +128,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        HSWA_W8(0), HSWA_W8(8)
+        : "memory");
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -206,47 +220,53 @@ __device__ void prefill_producer(PrefillSmem &sm, const CUtensorMap *tq, const C
     for (int i = max(0, issued - kSlots); i < issued; ++i) mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err);
 }
 
+// S_x = Q_x K^T over d = 128: 8 steps of K = 16 (32 bytes inside a 128-byte
+// swizzle row; the second half of d is the second 16 KB block).
+__device__ __forceinline__ void issue_s(uint32_t t_s, uint32_t q_addr, uint32_t k_addr) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+        mma_ss(t_s, sdesc(q_addr + off, 16, 1024), sdesc(k_addr + off, 16, 1024), kIdescQK, kk > 0);
+    }
+}
+
+// O_x += P_x V over 128 keys: 8 steps of K = 16 keys; P_x (bf16 pairs) sits in
+// the first 64 columns of S_x, V is MN-major (d contiguous) with the two
+// 64-column halves 16 KB apart.
+__device__ __forceinline__ void issue_pv(uint32_t t_o, uint32_t t_p, uint32_t v_addr, bool first_tile) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ts(t_o, t_p + kk * 8, sdesc(v_addr + kk * 2048, kHalfBytes, 1024), kIdescPV,
+               (first_tile && kk == 0) ? 0u : 1u);
+}
+
 __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u) {
     const uint32_t tbase = sm.tmem_base;
-    const uint32_t t_s[2] = {tbase, tbase + 128}, t_o[2] = {tbase + 256, tbase + 384};
-    const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+    const uint32_t ts0 = tbase, ts1 = tbase + 128, to0 = tbase + 256, to1 = tbase + 384;
+    const uint32_t qa0 = smem_u32(sm.q[0]), qa1 = smem_u32(sm.q[1]);
     bool ok = mbar_wait(&sm.q_full, 0, a.err);
     tc_fence_after();
-    // S_x = Q_x K^T over d = 128: 8 steps of K = 16 (32 bytes inside a 128-byte swizzle row)
-    auto issue_s = [&](int x, uint32_t k_addr) {
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            mma_ss(t_s[x], sdesc(q_addr[x] + off, 16, 1024), sdesc(k_addr + off, 16, 1024), kIdescQK, kk > 0);
-        }
-    };
-    // O_x += P_x V over 128 keys: 8 steps of K = 16 keys (2048 bytes of V rows)
-    auto issue_pv = [&](int x, uint32_t v_addr, bool first_tile) {
-        for (int kk = 0; kk < 8; ++kk)
-            mma_ts(t_o[x], t_s[x] + kk * 8, sdesc(v_addr + kk * 2048, kHalfBytes, 1024), kIdescPV,
-                   (first_tile && kk == 0) ? 0u : 1u);
-    };
     const int n = u.n_tiles;
     if (ok && n > 0) {
-        // tile 0: S_A(0), S_B(0)
-        ok = mbar_wait(&sm.kv_full[0], 0, a.err);
+        ok = mbar_wait(&sm.kv_full[0], 0, a.err);  // K(0)
         if (ok) {
             tc_fence_after();
             const uint32_t k0 = smem_u32(sm.kv[0]);
-            issue_s(0, k0);
+            issue_s(ts0, qa0, k0);
             mma_commit(&sm.s_full[0]);
-            issue_s(1, k0);
+            issue_s(ts1, qa1, k0);
             mma_commit(&sm.s_full[1]);
             mma_commit(&sm.kv_empty[0]);
         }
         for (int j = 0; ok && j < n; ++j) {
-            const int iv = 2 * j + 1, ik = 2 * j + 2;
+            const int iv = 2 * j + 1, ik = 2 * j + 2;  // ring items V(j), K(j + 1)
             const int sv = iv % kSlots, sk = ik % kSlots;
             ok = mbar_wait(&sm.kv_full[sv], (iv / kSlots) & 1, a.err) && mbar_wait(&sm.p_full[0], j & 1, a.err) &&
                  !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
             const uint32_t v_addr = smem_u32(sm.kv[sv]);
-            issue_pv(0, v_addr, j == 0);
+            issue_pv(to0, ts0, v_addr, j == 0);
             const bool more = j + 1 < n;
             uint32_t k_addr = 0;
             if (more) {
@@ -254,21 +274,23 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
                 if (!ok) break;
                 tc_fence_after();
                 k_addr = smem_u32(sm.kv[sk]);
-                issue_s(0, k_addr);
+                issue_s(ts0, qa0, k_addr);
                 mma_commit(&sm.s_full[0]);
             }
             ok = mbar_wait(&sm.p_full[1], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
-            issue_pv(1, v_addr, j == 0);
+            issue_pv(to1, ts1, v_addr, j == 0);
             mma_commit(&sm.kv_empty[sv]);
             if (more) {
-                issue_s(1, k_addr);
+                issue_s(ts1, qa1, k_addr);
                 mma_commit(&sm.s_full[1]);
                 mma_commit(&sm.kv_empty[sk]);
             }
         }
     }
+    // tracks every MMA issued above: the softmax warps wait on it before
+    // reading O and before the TMEM is freed
     mma_commit(&sm.o_final[0]);
     mma_commit(&sm.o_final[1]);
     if (!ok) sm.abort = 1;
@@ -283,7 +305,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
     const int32_t t = u.p0 + min(r, u.n_rows - 1);  // rows past the chunk repeat the last valid row
     const int32_t t_min = u.p0, t_max = u.p0 + u.n_rows - 1;
     const int32_t W = a.window;
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY, l = 0.f;  // running max (log2 units) and sum of P
     bool ok = true;
     for (int j = 0; j < u.n_tiles; ++j) {
         ok = mbar_wait(&sm.s_full[x], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
@@ -295,29 +317,52 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
         for (int c = 0; c < 4; ++c) tmem_ld32(t_s + 32 * c, sr[c]);
         tmem_wait_ld();
         const int32_t k0 = (u.tile_lo + j) * kBN;
-        const bool need_mask = (k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1);
-        const int32_t hi_c = t - k0;                         // keys c <= hi_c
-        const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;    // keys c >= lo_c
-        float mx = -INFINITY;
+        // raw scores: the scale (> 0) does not change which keys win the max
+        if ((k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1)) {
+            const int32_t hi_c = t - k0;                       // keys c <= hi_c
+            const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;  // keys c >= lo_c
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = c * 32 + i;
+                    if (col > hi_c || col < lo_c) sr[c][i] = __float_as_uint(-INFINITY);
+                }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float v = __uint_as_float(sr[c][i]) * a.scale_log2;
-                if (need_mask) {
-                    const int col = c * 32 + i;
-                    v = (col <= hi_c && col >= lo_c) ? v : -INFINITY;
-                }
-                sr[c][i] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
+            for (int i = 0; i < 32; i += 4) {
+                m0 = max3(m0, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+                m1 = max3(m1, __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
             }
+        const float mx = fmaxf(m0, m1) * a.scale_log2;
         // A new reference max only when the row max grows by more than 2^8;
-        // then O (nothing before the first PV) and l are rescaled. TMEM loads
-        // and stores are warp-wide, so the whole warp takes the rescale path
-        // when any of its rows needs it (the others scale by 1).
+        // then O (nothing before the first PV) and l are rescaled.
         const bool need = mx > m_used + kRescaleLog2;
         const bool resc = need && j > 0 && m_used != -INFINITY;
         const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
+        if (need) m_used = mx;
+        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            // P = 2^(s * scale - m), packed to bf16 pairs in place, then its
+            // 16 columns (32 keys) written over the start of S
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i]), a.scale_log2, neg_m));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i + 1]), a.scale_log2, neg_m));
+                sum0 += p0;
+                sum1 += p1;
+                sr[c][i] = pack_bf16(p0, p1);
+            }
+            tmem_st16(t_s + 16 * c, sr[c]);
+        }
+        // the O rescale comes after the P store (the S registers are free
+        // then); TMEM loads and stores are warp-wide, so the whole warp takes
+        // this path when any of its rows needs it (the others scale by 1)
         if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -329,31 +374,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
                 tmem_st32(t_o + 32 * c, ov);
             }
         }
-        l *= alpha;
-        if (need) m_used = mx;
-        const float m_safe = m_used == -INFINITY ? 0.f : m_used;
-        float sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float p0 = fast_exp2(__uint_as_float(sr[c][2 * i]) - m_safe);
-                const float p1 = fast_exp2(__uint_as_float(sr[c][2 * i + 1]) - m_safe);
-                sum += p0 + p1;
-                pk[i] = pack_bf16(p0, p1);
-            }
-            // P row: 16 packed columns per 32 keys, written over the start of S
-            if (c & 1) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sr[c - 1][16 + i] = pk[i];
-                tmem_st32(t_s + 32 * (c >> 1), sr[c - 1]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sr[c][i] = pk[i];
-            }
-        }
-        l += sum;
+        l = l * alpha + (sum0 + sum1);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&sm.p_full[x]);
@@ -452,6 +473,7 @@ extern "C" int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer
                                   const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
                                   int n_seqs, int total_q, int max_q_len, float scale, hswa_stream_t stream) {
     if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs || max_q_len < 0 || total_q < 0 ||
+        !(scale > 0.f) ||
         (n_seqs > 0 && max_q_len > total_q) ||
         (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA) ||
         (layer->kind == HSWA_KIND_SWA && layer->window <= 0))

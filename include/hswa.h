@@ -211,7 +211,7 @@ int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
  * d_q_start: device int32 [n_seqs + 1], non-decreasing from 0; max_q_len >=
  * every n_i (sizes the grid). The host passes total_q and max_q_len because
  * it cannot read d_q_start without waiting for the device; rows are never
- * read past total_q. */
+ * read past total_q. scale must be > 0 (HSWA_ERR_INVALID_ARG otherwise). */
 int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                        const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
                        int n_seqs, int total_q, int max_q_len, float scale, hswa_stream_t stream);
