@@ -371,6 +371,207 @@ def measure_prefill(steps, warmup, w):
             "launches": pb.launches}
 
 
+def fill_normal(t, seed):
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    flat = t.view(-1)
+    for j in range(0, flat.numel(), 1 << 28):
+        n = min(1 << 28, flat.numel() - j)
+        flat[j:j + n] = torch.randn(n, generator=g, device="cuda").to(t.dtype)
+
+
+def hybrid70_bytes(w, lens):
+    """Algorithmic bytes of one 70-layer decode step and the pool sizing."""
+    es = KV_ROW[w.dtype]
+    row = w.n_kv_heads * w.head_dim * es
+    B = len(lens)
+    n_full = sum(1 for k in w.layer_kinds if k == wl.KIND_FULL)
+    n_swa = len(w.layer_kinds) - n_full
+    full_kv = 2 * row * int(np.sum(lens))
+    swa_kv = 2 * row * int(np.sum(np.minimum(lens, w.window)))
+    per_layer = 2 * B * w.n_q_heads * w.head_dim * es + 2 * 2 * B * row
+    return {"step": n_full * full_kv + n_swa * swa_kv + len(w.layer_kinds) * per_layer,
+            "full_layer": full_kv + per_layer, "n_full": n_full, "n_swa": n_swa}
+
+
+class Hybrid70:
+    """The 70-layer attention-only decode step (10 Full + 60 SWA, Full at
+    every 7th layer), batch 128 at 128K cached tokens each. The ten Full
+    layers read one physical Full pool (640 GiB of per-layer Full pools do
+    not fit in HBM; each layer still reads its 64 GiB from HBM)."""
+
+    def __init__(self, w, extra_steps, n_seqs=None):
+        import torch
+        import hybrid_sliding_window_dual_gb300 as H
+        from hybrid_sliding_window_dual_gb300.session import DualPoolSession
+        self.torch, self.w = torch, w
+        B, P, W = len(w.cached), w.page_size, w.window
+        self.B = B
+        pages_per_seq = math.ceil((max(w.cached) + extra_steps + 1) / P)
+        full_pages = B * pages_per_seq + 16
+        swa_pages = B * (math.ceil((W + 64) / P) + 2) + math.ceil((W + 4096) / P) + 16
+        cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                       head_dim=w.head_dim, dtype=w.dtype, full_pages=full_pages, swa_pages=swa_pages,
+                       max_seqs=B, max_pages_per_seq=pages_per_seq + 1)
+        self.stream = torch.cuda.Stream()
+        self.sess = DualPoolSession(cfg, list(w.layer_kinds), None, None, stream=self.stream, init="empty",
+                                    share_full_pool=True)
+        for s, L in enumerate(w.cached):
+            for start in range(0, L, 4096):
+                self.sess.reserve([s], [min(4096, L - start)])
+                self.sess.release([s])
+        self.full_pool_layer = list(w.layer_kinds).index(wl.KIND_FULL)
+        with torch.cuda.stream(self.stream):
+            for i, kind in enumerate(w.layer_kinds):
+                if kind == wl.KIND_FULL and i != self.full_pool_layer:
+                    continue
+                fill_normal(self.sess.k[i], 1000 + 2 * i)
+                fill_normal(self.sess.v[i], 1001 + 2 * i)
+            self.sess.sync()
+        dt = wl.TORCH_DTYPE[w.dtype]
+        nl = len(w.layer_kinds)
+        self.q = [wl.normal((B, w.n_q_heads, w.head_dim), 2000 + i, w.dtype, "cuda") for i in range(nl)]
+        self.kn = [wl.normal((B, w.n_kv_heads, w.head_dim), 3000 + i, w.dtype, "cuda") for i in range(nl)]
+        self.vn = [wl.normal((B, w.n_kv_heads, w.head_dim), 4000 + i, w.dtype, "cuda") for i in range(nl)]
+        self.o = [torch.empty(B, w.n_q_heads, w.head_dim, dtype=dt, device="cuda") for _ in range(nl)]
+        self.slot_host = torch.empty(2, B, dtype=torch.int32, pin_memory=True)
+        self.slot_dev = torch.empty(2, B, dtype=torch.int32, device="cuda")
+        self.sess.workspace(B)
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        self.steps_done = 0
+        self.launches = 0
+        self.full_events = []
+        torch.cuda.synchronize()
+
+    def lens(self):
+        return self.sess.tables()[2][:self.B].astype(np.int64)
+
+    def step(self, timed=False):
+        torch, sess, B = self.torch, self.sess, self.B
+        fs, ss = sess.reserve(range(B), [1] * B)
+        self.stream.synchronize()  # the slot staging of the previous step has been copied
+        with torch.cuda.stream(self.stream):
+            self.slot_host[0].numpy()[:] = fs
+            self.slot_host[1].numpy()[:] = ss
+            self.slot_dev.copy_(self.slot_host, non_blocking=True)
+            sess.sync()
+            self.launches += 1
+            for i, kind in enumerate(self.w.layer_kinds):
+                sess.append(i, self.kn[i], self.vn[i], self.slot_dev[0 if kind == wl.KIND_FULL else 1])
+                if timed and kind == wl.KIND_FULL:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(self.stream)
+                sess.decode(i, self.q[i], self.o[i], B, self.scale)
+                if timed and kind == wl.KIND_FULL:
+                    e1.record(self.stream)
+                    self.full_events.append((e0, e1))
+                self.launches += 4
+        self.steps_done += 1
+        if self.steps_done % 64 == 0:
+            sess.release(range(B))
+
+    def sizing(self):
+        """Dual pool (per-layer Full pools + live SWA pages) against one O(N)
+        pool for all 70 layers, in bytes, at the current lengths."""
+        w = self.w
+        page_bytes = 2 * w.n_kv_heads * w.page_size * w.head_dim * KV_ROW[w.dtype]
+        f, s, lens = self.sess.tables()
+        full_live = int((f >= 0).sum())
+        swa_live = int((s >= 0).sum())
+        n_full = sum(1 for k in w.layer_kinds if k == wl.KIND_FULL)
+        n_swa = len(w.layer_kinds) - n_full
+        dual = (n_full * full_live + n_swa * swa_live) * page_bytes
+        single = len(w.layer_kinds) * full_live * page_bytes
+        return {"dual_pool_bytes": dual, "single_pool_bytes": single, "ratio": round(dual / single, 5),
+                "capacity_gain": round(single / dual, 3), "live_swa_pages_per_seq": round(swa_live / self.B, 2)}
+
+
+class SwaTransfer:
+    """Transfer by SWA mask: 256 sequences (lognormal lengths, median 16K, cap
+    256K), 60 SWA layers. A step gathers the in-window tokens of every layer
+    into a pinned host buffer (the kernel writes host memory directly), evicts
+    the SWA segments, gives the windows fresh pages and scatters the host
+    copies back."""
+
+    def __init__(self, w):
+        import torch
+        import hybrid_sliding_window_dual_gb300 as H
+        from hybrid_sliding_window_dual_gb300.session import DualPoolSession, window_offsets
+        self.torch, self.w, self.H = torch, w, H
+        B, P, W = len(w.cached), w.page_size, w.window
+        self.B = B
+        extra = 4 * 64 + 8
+        full_pages = sum(math.ceil((L + extra) / P) for L in w.cached) + 16
+        swa_pages = 2 * B * (math.ceil((W + 64) / P) + 2) + math.ceil((W + 4096) / P) + 16
+        max_pages = max(math.ceil((L + extra) / P) for L in w.cached) + 1
+        cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                       head_dim=w.head_dim, dtype=w.dtype, full_pages=full_pages, swa_pages=swa_pages,
+                       max_seqs=B, max_pages_per_seq=max_pages)
+        self.stream = torch.cuda.Stream()
+        self.sess = DualPoolSession(cfg, list(w.layer_kinds), None, wl.permutation(swa_pages, w.seed),
+                                    stream=self.stream, init="empty")
+        for s, L in enumerate(w.cached):
+            for start in range(0, L, 4096):
+                self.sess.reserve([s], [min(4096, L - start)])
+                self.sess.release([s])
+        with torch.cuda.stream(self.stream):
+            for i in range(len(w.layer_kinds)):
+                fill_normal(self.sess.k[i], 5000 + 2 * i)
+                fill_normal(self.sess.v[i], 5001 + 2 * i)
+            self.sess.sync()
+        self.window_offsets = window_offsets
+        self.refresh_offsets()
+        n = int(self.off[-1]) * 2 * w.n_kv_heads * w.head_dim
+        self.host = [torch.empty(n, dtype=wl.TORCH_DTYPE[w.dtype], pin_memory=True)
+                     for _ in range(len(w.layer_kinds))]
+        self.launches = 0
+        torch.cuda.synchronize()
+
+    def refresh_offsets(self):
+        lens = self.sess.tables()[2][:self.B]
+        self.off = self.window_offsets(lens, self.w.window)
+        self.d_off = self.torch.as_tensor(self.off, device="cuda")
+
+    def moved_bytes(self):
+        return int(self.off[-1]) * 2 * self.w.n_kv_heads * self.w.head_dim * KV_ROW[self.w.dtype]
+
+    def gather_all(self):
+        with self.torch.cuda.stream(self.stream):
+            for i in range(len(self.w.layer_kinds)):
+                self.sess.gather(i, self.d_off, self.B, self.host[i])
+                self.launches += 1
+
+    def scatter_all(self):
+        with self.torch.cuda.stream(self.stream):
+            for i in range(len(self.w.layer_kinds)):
+                self.sess.scatter(i, self.d_off, self.B, self.host[i])
+                self.launches += 1
+
+    def evict_and_restore(self):
+        self.stream.synchronize()
+        self.sess.swa_drop(range(self.B))
+        self.sess.swa_restore(range(self.B))
+        with self.torch.cuda.stream(self.stream):
+            self.sess.sync()
+            self.launches += 1
+
+    def release_rounds(self, rounds=4, tokens=64):
+        """Ring release: `tokens` decode tokens per sequence, then one release."""
+        times, live = [], []
+        for _ in range(rounds):
+            for _ in range(tokens):
+                self.sess.reserve(range(self.B), [1] * self.B)
+            t0 = time.perf_counter()
+            self.sess.release(range(self.B))
+            times.append(time.perf_counter() - t0)
+            live.append(int((self.sess.tables()[1] >= 0).sum(axis=1).max()))
+        with self.torch.cuda.stream(self.stream):
+            self.sess.sync()
+        self.refresh_offsets()
+        return times, live
+
+
 def time_steps(run, steps, stream, world):
     import torch
     barrier(world)
@@ -467,6 +668,24 @@ def run_decode(args, world, rank, local):
             "valid_tflop_per_step": round(pf["valid_tflop_per_step"], 3),
             "ms_per_step": round(pf["ms_per_step"], 3), "tokens_per_s": round(pf["tokens_per_s"], 1),
             "kernel": "prefill_tc_bf16_d128"}
+    if not args.no_hybrid70:
+        h = measure_hybrid70(args.hybrid_steps, 2)
+        line["hybrid70"] = {
+            "workload": "hybrid70 (10 Full + 60 SWA layers, batch 128 x 131072 cached, 64/8 heads, d 128)",
+            "gbs": round(h["gbs"], 1), "unit": "GB/s", "frac": round(h["gbs"] / hbm, 4),
+            "ms_per_step": round(h["ms_per_step"], 3), "tokens_per_s": round(h["tokens_per_s"], 1),
+            "full_layer_gbs": round(h["full_layer_gbs"], 1), "full_layer_ms": round(h["full_layer_ms"], 3),
+            "step_gb": round(h["step_bytes"] / 1e9, 2), "sizing": h["sizing"],
+            "note": "the 10 Full layers read one physical 64 GiB Full pool"}
+    if not args.no_transfer:
+        t = measure_transfer(3)
+        line["swa_transfer"] = {
+            "workload": "swa_transfer (256 seqs, lognormal median 16K cap 256K, 60 SWA layers, pinned host)",
+            "gather_gbs": round(t["gather_gbs"], 1), "scatter_gbs": round(t["scatter_gbs"], 1), "unit": "GB/s",
+            "gb_each_way": round(t["bytes_each_way"] / 1e9, 3),
+            "gb_if_whole_sequences": round(t["bytes_if_full_sequences"] / 1e9, 1),
+            "release_us_per_call": round(t["release_us_per_call"], 1),
+            "max_live_swa_pages_per_seq_after_release": t["max_live_swa_pages_per_seq_after_release"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(w, budget_s=args.cpu_budget)
     return line
@@ -573,6 +792,73 @@ def run_reference(args, world, rank):
     }
 
 
+def measure_hybrid70(steps, warmup, n_seqs=None):
+    import torch
+    w = wl.hybrid70()
+    if n_seqs:
+        import dataclasses
+        w = dataclasses.replace(w, cached=w.cached[:n_seqs])
+    hb = Hybrid70(w, warmup + steps + 2)
+    for _ in range(warmup):
+        hb.step()
+    hb.stream.synchronize()
+    before = hybrid70_bytes(w, hb.lens() + 1)
+    l0 = hb.launches
+    secs = time_steps(lambda: hb.step(timed=True), steps, hb.stream, 1)
+    after = hybrid70_bytes(w, hb.lens())
+    step_bytes = 0.5 * (before["step"] + after["step"])
+    full_ms = float(np.mean([a.elapsed_time(b) for a, b in hb.full_events]))
+    sizing = hb.sizing()
+    st = hb.sess.check()
+    if st != 0:
+        raise RuntimeError("device status %d after hybrid70" % st)
+    out = {"gbs": step_bytes * steps / secs / 1e9, "ms_per_step": secs / steps * 1e3,
+           "full_layer_gbs": 0.5 * (before["full_layer"] + after["full_layer"]) / (full_ms / 1e3) / 1e9,
+           "full_layer_ms": full_ms, "step_bytes": step_bytes, "tokens_per_s": len(w.cached) * steps / secs,
+           "launches": hb.launches - l0, "sizing": sizing}
+    del hb
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_transfer(steps):
+    import torch
+    w = wl.swa_transfer()
+    tb = SwaTransfer(w)
+    moved = tb.moved_bytes() * len(w.layer_kinds)
+    # warm-up round trip
+    tb.gather_all()
+    tb.evict_and_restore()
+    tb.scatter_all()
+    tb.stream.synchronize()
+    g_s = s_s = 0.0
+    for _ in range(steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(tb.stream)
+        tb.gather_all()
+        e[1].record(tb.stream)
+        tb.stream.synchronize()
+        tb.evict_and_restore()
+        e[2].record(tb.stream)
+        tb.scatter_all()
+        e[3].record(tb.stream)
+        tb.stream.synchronize()
+        g_s += e[0].elapsed_time(e[1]) / 1e3
+        s_s += e[2].elapsed_time(e[3]) / 1e3
+    rel_times, live = tb.release_rounds()
+    st = tb.sess.check()
+    if st != 0:
+        raise RuntimeError("device status %d after transfer" % st)
+    full_len = sum(w.cached) * 2 * w.n_kv_heads * w.head_dim * KV_ROW[w.dtype] * len(w.layer_kinds)
+    out = {"gather_gbs": moved * steps / g_s / 1e9, "scatter_gbs": moved * steps / s_s / 1e9,
+           "bytes_each_way": moved, "bytes_if_full_sequences": full_len,
+           "release_us_per_call": 1e6 * float(np.median(rel_times)),
+           "max_live_swa_pages_per_seq_after_release": max(live), "launches": tb.launches}
+    del tb
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill_line(args, world, rank, local):
     """--workload chunked_prefill: one line whose value is the chunk's TFLOP/s."""
     w = workload(args, "chunked_prefill")
@@ -617,6 +903,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-hybrid70", action="store_true")
+    ap.add_argument("--no-transfer", action="store_true")
+    ap.add_argument("--hybrid-steps", type=int, default=5)
     ap.add_argument("--prefill-steps", type=int, default=5)
     args = ap.parse_args()
     if args.impl == "reference":

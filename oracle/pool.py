@@ -82,11 +82,13 @@ class DualPool:
         full_slot, swa_slot = [], []
         for s, n in zip(seq_ids, n_new):
             L = int(self.seq_len[s])
-            for t in range(L, L + n):
-                full_slot.append(int(self.full_bt[s, t // P]) * P + t % P)
-                swa_slot.append(int(self.swa_bt[s, t // P]) * P + t % P)
+            t = np.arange(L, L + n, dtype=np.int64)  # positions of the new tokens
+            full_slot.append(self.full_bt[s, t // P].astype(np.int64) * P + t % P)
+            swa_slot.append(self.swa_bt[s, t // P].astype(np.int64) * P + t % P)
             self.seq_len[s] = L + n
-        return np.array(full_slot, np.int32), np.array(swa_slot, np.int32)
+        if not full_slot:
+            return np.zeros(0, np.int32), np.zeros(0, np.int32)
+        return np.concatenate(full_slot).astype(np.int32), np.concatenate(swa_slot).astype(np.int32)
 
     # ------------------------------------------------------------------ a7
     def swa_release(self, seq_ids):
