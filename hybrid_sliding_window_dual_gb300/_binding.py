@@ -73,6 +73,7 @@ _SIG = {
     "hswa_swa_gather": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
     "hswa_swa_scatter": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
     "hswa_check": (_I, [_P]),
+    "hswa_selftest_bounded_wait": (_I, [_P]),
     "hswa_last_kernel": (ctypes.c_char_p, []),
     "hswa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -240,6 +241,10 @@ def hswa_swa_scatter(pool, layer: Layer, d_swa_bt, d_seq_len, d_tok_offset, n_se
 def hswa_check(stream=None):
     """Wait for the stream and return the device status word (0 = clean)."""
     return int(lib.hswa_check(_stream(stream)))
+
+
+def hswa_selftest_bounded_wait(stream=None):
+    _check(lib.hswa_selftest_bounded_wait(_stream(stream)), "hswa_selftest_bounded_wait")
 
 
 def hswa_last_kernel():

@@ -113,9 +113,30 @@ __global__ void apply_table_updates(const int64_t *__restrict__ idx, const int32
     }
 }
 
+// Waits on an mbarrier that nothing completes, with the same bounded wait
+// the attention kernels use: it must give up, record HSWA_ERR_TIMEOUT and
+// return, leaving the context usable.
+__global__ void selftest_bounded_wait(int *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, err);
+}
+
 }  // namespace hswa
 
 using namespace hswa;
+
+extern "C" int hswa_selftest_bounded_wait(hswa_stream_t stream) {
+    int *err = error_word();
+    if (!err) return HSWA_ERR_CUDA;
+    set_last_kernel("selftest_bounded_wait");
+    selftest_bounded_wait<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
+    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+}
 
 void hswa_pool_release_device(hswa_pool *pool) {
     if (pool->staging_event) {

@@ -271,6 +271,13 @@ int hswa_decode_noalloc(const hswa_pool *pool, const hswa_layer *layer, const vo
  * HSWA_ERR_CUDA if the wait itself failed). */
 int hswa_check(hswa_stream_t stream);
 
+/* Diagnostic (no counterpart on the pages): launch one block that waits on
+ * an mbarrier nothing completes, through the bounded wait every kernel of
+ * the library uses. After about a second of GPU time the wait gives up and
+ * the device error word reads HSWA_ERR_TIMEOUT (see hswa_check); the context
+ * stays usable. Returns the launch status. */
+int hswa_selftest_bounded_wait(hswa_stream_t stream);
+
 /* Name of the kernel variant the last device call on this host thread
  * launched (e.g. "decode_mma_bf16_d128"); "" before any launch. */
 const char *hswa_last_kernel(void);
