@@ -260,6 +260,36 @@ class DecodeBatch:
             # the step's result is read on the host
             self.stream.synchronize()
 
+    def breakdown(self, steps):
+        """Average device time of each call of the decode step (events around
+        every call; a diagnostic, not the timed bench)."""
+        torch, sess, B = self.torch, self.sess, self.B
+        names = ["sync", "append_full", "decode_full", "append_swa", "decode_swa"]
+        acc = {n: 0.0 for n in names}
+        for _ in range(steps):
+            fs, ss = sess.reserve(range(B), [1] * B)
+            self.stream.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            with torch.cuda.stream(self.stream):
+                self.slot_host[0][0].numpy()[:] = fs
+                self.slot_host[0][1].numpy()[:] = ss
+                self.slot_dev.copy_(self.slot_host[0], non_blocking=True)
+                ev[0].record(self.stream)
+                sess.sync()
+                ev[1].record(self.stream)
+                for i in range(2):
+                    sess.append(i, self.kn[i], self.vn[i], self.slot_dev[i])
+                    ev[2 + 2 * i].record(self.stream)
+                    sess.decode(i, self.q[i], self.o[i], B, self.scale)
+                    ev[3 + 2 * i].record(self.stream)
+            self.stream.synchronize()
+            for k, n in enumerate(names):
+                acc[n] += ev[k].elapsed_time(ev[k + 1]) * 1e3
+            self.steps_done += 1
+            if self.steps_done % 64 == 0:
+                sess.release(range(B))
+        return {n: round(v / steps, 2) for n, v in acc.items()}
+
     def finish(self):
         self.stream.synchronize()
         st = self.sess.check()
@@ -604,7 +634,7 @@ def workload(args, name):
 def run_decode(args, world, rank, local):
     import torch
     w = workload(args, "decode_batch")
-    total_steps = args.warmup + 2 * args.steps + 2
+    total_steps = args.warmup + 2 * args.steps + 64
     bench = DecodeBatch(w, total_steps)
     hbm, _, _, peak_kind = peaks()
     # clocks are sampled from before the warm-up to the end of the timed region
@@ -624,6 +654,8 @@ def run_decode(args, world, rank, local):
     full_layer_bytes = 0.5 * (bytes_before["full_layer"] + bytes_after["full_layer"])
     dec_ms = [a.elapsed_time(b) for a, b in bench.decode_events]
     bench.decode_events.clear()
+    if args.breakdown:
+        bd = bench.breakdown(50)
     # end to end: host buffers in, host buffers out, copies inside the timed region
     e2e_secs = time_steps(lambda: bench.step(host_io=True), args.steps, bench.stream, world)
     bench.finish()
@@ -657,6 +689,8 @@ def run_decode(args, world, rank, local):
         "clocks": clock_info,
         "tokens_per_s": round(world * B * args.steps / secs, 1),
     }
+    if args.breakdown:
+        line["breakdown_us"] = bd
     if not args.no_prefill:
         del bench
         torch.cuda.empty_cache()
@@ -685,6 +719,9 @@ def run_decode(args, world, rank, local):
         line["swa_transfer"] = {
             "workload": "swa_transfer (256 seqs, lognormal median 16K cap 256K, 60 SWA layers, pinned host)",
             "gather_gbs": round(t["gather_gbs"], 1), "scatter_gbs": round(t["scatter_gbs"], 1), "unit": "GB/s",
+            "memcpy_d2h_gbs": round(t["memcpy_d2h_gbs"], 1), "memcpy_h2d_gbs": round(t["memcpy_h2d_gbs"], 1),
+            "gather_frac_of_memcpy": round(t["gather_gbs"] / t["memcpy_d2h_gbs"], 3),
+            "scatter_frac_of_memcpy": round(t["scatter_gbs"] / t["memcpy_h2d_gbs"], 3),
             "gb_each_way": round(t["bytes_each_way"] / 1e9, 3),
             "gb_if_whole_sequences": round(t["bytes_if_full_sequences"] / 1e9, 1),
             "release_us_per_call": round(t["release_us_per_call"], 1),
@@ -848,6 +885,25 @@ def measure_transfer(steps):
         tb.stream.synchronize()
         g_s += e[0].elapsed_time(e[1]) / 1e3
         s_s += e[2].elapsed_time(e[3]) / 1e3
+    # the host-link ceiling: a copy-engine memcpy of one layer's packed bytes
+    one = tb.host[0].numel()
+    dev = torch.empty(one, dtype=tb.host[0].dtype, device="cuda")
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with torch.cuda.stream(tb.stream):
+        for _ in range(2):
+            dev.copy_(tb.host[0], non_blocking=True)
+        e[0].record(tb.stream)
+        for _ in range(5):
+            tb.host[1].copy_(dev, non_blocking=True)
+        e[1].record(tb.stream)
+        for _ in range(5):
+            dev.copy_(tb.host[1], non_blocking=True)
+        e[2].record(tb.stream)
+    tb.stream.synchronize()
+    nbytes = one * dev.element_size()
+    d2h = 5 * nbytes / (e[0].elapsed_time(e[1]) / 1e3) / 1e9
+    h2d = 5 * nbytes / (e[1].elapsed_time(e[2]) / 1e3) / 1e9
+    del dev
     rel_times, live = tb.release_rounds()
     st = tb.sess.check()
     if st != 0:
@@ -856,7 +912,8 @@ def measure_transfer(steps):
     out = {"gather_gbs": moved * steps / g_s / 1e9, "scatter_gbs": moved * steps / s_s / 1e9,
            "bytes_each_way": moved, "bytes_if_full_sequences": full_len,
            "release_us_per_call": 1e6 * float(np.median(rel_times)),
-           "max_live_swa_pages_per_seq_after_release": max(live), "launches": tb.launches}
+           "max_live_swa_pages_per_seq_after_release": max(live), "launches": tb.launches,
+           "memcpy_d2h_gbs": d2h, "memcpy_h2d_gbs": h2d}
     del tb
     torch.cuda.empty_cache()
     return out
@@ -909,6 +966,7 @@ def main():
     ap.add_argument("--no-hybrid70", action="store_true")
     ap.add_argument("--no-transfer", action="store_true")
     ap.add_argument("--hybrid-steps", type=int, default=5)
+    ap.add_argument("--breakdown", action="store_true", help="per-call device times of the decode step")
     ap.add_argument("--prefill-steps", type=int, default=5)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -142,7 +142,14 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+#define HSWA_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]), \
+                    "+r"(r[i + 6]), "+r"(r[i + 7])
+
+// Wait for this thread's TMEM loads; the loaded registers are operands so
+// that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : HSWA_RW8(0), HSWA_RW8(8), HSWA_RW8(16), HSWA_RW8(24)::"memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------- work unit
@@ -312,31 +319,34 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        // S row in four 32-column chunks; each load overlaps the mask and
+        // max work of the chunk before it
         uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + 32 * c, sr[c]);
-        tmem_wait_ld();
         const int32_t k0 = (u.tile_lo + j) * kBN;
-        // raw scores: the scale (> 0) does not change which keys win the max
-        if ((k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1)) {
-            const int32_t hi_c = t - k0;                       // keys c <= hi_c
-            const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;  // keys c >= lo_c
+        const bool masked = (k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1);
+        const int32_t hi_c = t - k0;                       // keys c <= hi_c
+        const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;  // keys c >= lo_c
+        float m0 = -INFINITY, m1 = -INFINITY;
+        tmem_ld32(t_s, sr[0]);
+        tmem_wait_ld(sr[0]);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+            if (c + 1 < 4) tmem_ld32(t_s + 32 * (c + 1), sr[c + 1]);
+            // raw scores: the scale (> 0) does not change which keys win the max
+            if (masked) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int col = c * 32 + i;
                     if (col > hi_c || col < lo_c) sr[c][i] = __float_as_uint(-INFINITY);
                 }
-        }
-        float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
+            }
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 m0 = max3(m0, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
                 m1 = max3(m1, __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
             }
+            if (c + 1 < 4) tmem_wait_ld(sr[c + 1]);
+        }
         const float mx = fmaxf(m0, m1) * a.scale_log2;
         // A new reference max only when the row max grows by more than 2^8;
         // then O (nothing before the first PV) and l are rescaled.
@@ -345,18 +355,20 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
         const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
         if (need) m_used = mx;
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-        float sum0 = 0.f, sum1 = 0.f;
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
+        float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            // P = 2^(s * scale - m), packed to bf16 pairs in place, then its
-            // 16 columns (32 keys) written over the start of S
+            // P = 2^(s * scale - m) two keys at a time (packed f32x2 FMA and
+            // add), packed to bf16 pairs in place, then its 16 columns (32
+            // keys) written over the start of S
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i]), a.scale_log2, neg_m));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i + 1]), a.scale_log2, neg_m));
-                sum0 += p0;
-                sum1 += p1;
-                sr[c][i] = pack_bf16(p0, p1);
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                                            sc2, nm2);
+                const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                sum2 = __fadd2_rn(sum2, p);
+                sr[c][i] = pack_bf16(p.x, p.y);
             }
             tmem_st16(t_s + 16 * c, sr[c]);
         }
@@ -368,13 +380,13 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
             for (int c = 0; c < 4; ++c) {
                 uint32_t ov[32];
                 tmem_ld32(t_o + 32 * c, ov);
-                tmem_wait_ld();
+                tmem_wait_ld(ov);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
                 tmem_st32(t_o + 32 * c, ov);
             }
         }
-        l = l * alpha + (sum0 + sum1);
+        l = l * alpha + (sum2.x + sum2.y);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&sm.p_full[x]);
@@ -395,7 +407,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
     for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
         tmem_ld32(t_o + 32 * c, ov);
-        tmem_wait_ld();
+        tmem_wait_ld(ov);
         if (r < u.n_rows) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
