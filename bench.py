@@ -6,8 +6,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hswa|reference]
 decode_batch (default): 64 sequences, cached lengths uniform in [1024, 32768],
 64 Q / 8 KV heads, d 128, page 64, bf16, one Full and one SWA (W = 128) layer.
 One step = reserve one token per sequence (both pools) -> sync the device
-tables -> append K/V to the Full and the SWA pool -> decode the Full layer ->
-decode the SWA layer; the SWA release runs every 64 steps.
+tables -> append + decode the Full layer -> append + decode the SWA layer
+(hswa_decode_append: the append is fused into the decode); the SWA release
+runs every 64 steps.
 Metric: algorithmic HBM bytes of the step (valid KV rows read, q read, o
 written, new K/V read and written) per second.
 
@@ -241,18 +242,18 @@ class DecodeBatch:
                     self.q[i].copy_(self.h_q[i], non_blocking=True)
                     self.kn[i].copy_(self.h_kn[i], non_blocking=True)
                     self.vn[i].copy_(self.h_vn[i], non_blocking=True)
-                sess.append(i, self.kn[i], self.vn[i], self.slot_dev[i])
                 if time_full_decode and i == 0:
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(self.stream)
-                sess.decode(i, self.q[i], self.o[i], B, self.scale)
+                # append the new token's K/V and attend, one call (plan, main, combine)
+                sess.decode_append(i, self.q[i], self.kn[i], self.vn[i], self.slot_dev[i], self.o[i], B, self.scale)
                 if time_full_decode and i == 0:
                     e1.record(self.stream)
                     self.decode_events.append((e0, e1))
                 if host_io:
                     self.h_o[i].copy_(self.o[i], non_blocking=True)
-                self.launches += 4
+                self.launches += 3
         self.steps_done += 1
         if self.steps_done % 64 == 0:
             sess.release(range(B))
@@ -288,7 +289,24 @@ class DecodeBatch:
             self.steps_done += 1
             if self.steps_done % 64 == 0:
                 sess.release(range(B))
-        return {n: round(v / steps, 2) for n, v in acc.items()}
+        out = {n: round(v / steps, 2) for n, v in acc.items()}
+        # the same calls queued back to back (launch latency hidden)
+        def queued(fn, reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.stream):
+                e0.record(self.stream)
+                for _ in range(reps):
+                    fn()
+                e1.record(self.stream)
+            self.stream.synchronize()
+            return round(e0.elapsed_time(e1) * 1e3 / reps, 2)
+        out["queued_append"] = queued(lambda: sess.append(1, self.kn[1], self.vn[1], self.slot_dev[1]), 200)
+        out["queued_decode_swa"] = queued(lambda: sess.decode(1, self.q[1], self.o[1], B, self.scale), 200)
+        out["queued_decode_full"] = queued(lambda: sess.decode(0, self.q[0], self.o[0], B, self.scale), 20)
+        out["queued_decode_append_swa"] = queued(
+            lambda: sess.decode_append(1, self.q[1], self.kn[1], self.vn[1], self.slot_dev[1], self.o[1], B,
+                                       self.scale), 200)
+        return out
 
     def finish(self):
         self.stream.synchronize()
@@ -491,15 +509,15 @@ class Hybrid70:
             sess.sync()
             self.launches += 1
             for i, kind in enumerate(self.w.layer_kinds):
-                sess.append(i, self.kn[i], self.vn[i], self.slot_dev[0 if kind == wl.KIND_FULL else 1])
                 if timed and kind == wl.KIND_FULL:
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(self.stream)
-                sess.decode(i, self.q[i], self.o[i], B, self.scale)
+                sess.decode_append(i, self.q[i], self.kn[i], self.vn[i],
+                                   self.slot_dev[0 if kind == wl.KIND_FULL else 1], self.o[i], B, self.scale)
                 if timed and kind == wl.KIND_FULL:
                     e1.record(self.stream)
                     self.full_events.append((e0, e1))
-                self.launches += 4
+                self.launches += 3
         self.steps_done += 1
         if self.steps_done % 64 == 0:
             sess.release(range(B))
@@ -681,7 +699,7 @@ def run_decode(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "decode_mma_bf16_d128 (Full layer; plan + main + combine)",
+                     "kernel": "decode_mma_bf16_d128 with fused append (Full layer; plan + main + combine)",
                      "peak_source": peak_kind, "frac_of_8tbs": round(achieved / 8000.0, 4)},
         "e2e": {"value": round(total_bytes / e2e_secs / 1e9 * (1.0), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -67,6 +67,8 @@ _SIG = {
     "hswa_decode_workspace_size": (ctypes.c_size_t, [_P, _I]),
     "hswa_decode": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _I, ctypes.c_float, _P,
                          ctypes.c_size_t, _P]),
+    "hswa_decode_append": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float, _P,
+                                ctypes.c_size_t, _P]),
     "hswa_decode_noalloc": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _I, ctypes.c_float, _P]),
     "hswa_prefill_chunk": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I, _I,
                                 ctypes.c_float, _P]),
@@ -214,6 +216,13 @@ def hswa_decode_workspace_size(pool, n_seqs):
 def hswa_decode(pool, layer: Layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, stream=None):
     _check(lib.hswa_decode(pool, ctypes.byref(layer), _ptr(q), _ptr(o), _ptr(d_bt), _ptr(d_seq_len),
                            int(n_seqs), float(scale), _ptr(ws), int(ws_bytes), _stream(stream)), "hswa_decode")
+
+
+def hswa_decode_append(pool, layer: Layer, q, k_new, v_new, d_slots, o, d_bt, d_seq_len, n_seqs, scale, ws,
+                       ws_bytes, stream=None):
+    _check(lib.hswa_decode_append(pool, ctypes.byref(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(d_slots),
+                                  _ptr(o), _ptr(d_bt), _ptr(d_seq_len), int(n_seqs), float(scale), _ptr(ws),
+                                  int(ws_bytes), _stream(stream)), "hswa_decode_append")
 
 
 def hswa_decode_noalloc(pool, layer: Layer, q, o, d_bt, d_seq_len, n_seqs, scale, stream=None):

@@ -24,6 +24,22 @@ int *error_word();
 void set_last_kernel(const char *name);
 // Host: number of SMs of the current device (cached per device).
 int sm_count();
+// Host: launch a kernel with programmatic stream serialization (PDL).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 // Host: encode a 2-D bf16 tensor map (row-major [rows][cols], box
 // [box_rows][box_cols], 128-byte swizzle). Returns false on failure.
 bool make_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
@@ -85,6 +101,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
         }
     }
     return true;
+}
+
+// ----------------------------------------------- programmatic dependent launch
+// A kernel launched with the programmatic-serialization attribute may start
+// before its predecessor in the stream has finished: it must wait before
+// touching anything the predecessor writes. Both are no-ops otherwise.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Order this thread's generic-proxy global writes before its later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ----------------------------------------------------------- bulk copies

@@ -68,8 +68,14 @@ struct DecodeArgs {
     __nv_bfloat16 *o;
     const int32_t *bt;
     const int32_t *seq_len;
-    const int32_t *useg;  // [n_seqs + 1] unit prefix sum
+    const int4 *sdesc;    // [n_seqs + 1] {first unit, key lo, key hi, units}; [n].x = total
+    __nv_bfloat16 *k_pool, *v_pool;
     Partial *part;        // [n_ctas][2]
+    // optional fused append: new K / V rows [n_seqs][Hkv][d] written at
+    // slots[s] before the page that holds them is streamed (null = none)
+    const int32_t *slots;
+    const __nv_bfloat16 *k_new, *v_new;
+    int64_t pool_slots;
     int32_t n_seqs, bt_stride, hkv, hq, window, num_pages;
     float scale_log2;
     int *err;
@@ -81,19 +87,22 @@ __device__ __forceinline__ void key_range(int32_t L, int32_t window, int32_t &lo
     lo = (window > 0 && L - window > 0) ? L - window : 0;
 }
 
-// Unit prefix sum over sequences: units(s) = Hkv * pages touched by [lo, hi).
+// Per-sequence descriptors: the first unit of the sequence (prefix sum of
+// units(s) = Hkv * pages touched by the key range [lo, hi)), lo, hi, units.
+// desc[n].x is the total number of units.
 __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int32_t hkv, int32_t page,
-                            int32_t window, int32_t *__restrict__ useg) {
+                            int32_t window, int4 *__restrict__ desc) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    pdl_wait();
+    pdl_launch_dependents();
     if (tid == 0) carry = 0;
     __syncthreads();
     for (int32_t base = 0; base < n; base += blockDim.x) {
         const int32_t i = base + tid;
-        int32_t u = 0;
+        int32_t u = 0, lo = 0, hi = 0;
         if (i < n) {
-            int32_t lo, hi;
             key_range(seq_len[i], window, lo, hi);
             if (hi > lo) u = hkv * ((hi - 1) / page - lo / page + 1);
         }
@@ -114,12 +123,12 @@ __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int3
         }
         __syncthreads();
         const int32_t excl = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + x - u;
-        if (i < n) useg[i] = excl;
+        if (i < n) desc[i] = make_int4(excl, lo, hi, u);
         __syncthreads();
         if (tid == blockDim.x - 1) carry = excl + u;
         __syncthreads();
     }
-    if (tid == 0) useg[n] = carry;
+    if (tid == 0) desc[n] = make_int4(carry, 0, 0, 0);
 }
 
 __device__ __forceinline__ int64_t cta_start(int64_t c, int64_t U, int64_t N) { return c * U / N; }
@@ -127,17 +136,23 @@ __device__ __forceinline__ int64_t cta_start(int64_t c, int64_t U, int64_t N) { 
 // Largest c with cta_start(c) <= u.
 __device__ __forceinline__ int64_t cta_of(int64_t u, int64_t U, int64_t N) { return ((u + 1) * N - 1) / U; }
 
-// Largest s with useg[s] <= u (useg non-decreasing, useg[0] = 0 <= u < useg[n]).
-__device__ int32_t find_seq(const int32_t *useg, int32_t n, int64_t u) {
-    int32_t lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (useg[mid] <= u)
-            lo = mid;
-        else
-            hi = mid - 1;
+// Largest s in [0, n) with desc[s].x <= u (first units non-decreasing,
+// desc[0].x = 0 <= u). A 32-way search: every lane probes one position, so
+// each step is one round of loads for the whole warp.
+__device__ int32_t find_seq(const int4 *desc, int32_t n, int64_t u) {
+    const int lane = threadIdx.x & 31;
+    int32_t lo = 0, hi = n - 1;  // the answer lies in [lo, hi]
+    while (hi - lo >= 32) {
+        const int32_t step = (hi - lo + 32) / 32;
+        const int32_t idx = min(lo + lane * step, hi);
+        const unsigned m = __ballot_sync(0xffffffffu, desc[idx].x <= u);
+        const int32_t last = 31 - __clz(m);  // lane 0 probes lo, always true
+        lo += last * step;
+        hi = min(lo + step - 1, hi);
     }
-    return lo;
+    const int32_t idx = lo + lane;
+    const unsigned m = __ballot_sync(0xffffffffu, idx <= hi && desc[idx].x <= u);
+    return lo + 31 - __clz(m);
 }
 
 // Byte offset of the 16-byte chunk holding (row, d..d+7) in a stage buffer
@@ -160,14 +175,26 @@ __device__ void decode_producer(DecodeSmem &sm, const CUtensorMap *tk, const CUt
     for (int i = 0; i < kStages; ++i) issued[i] = false, issued_parity[i] = 0;
 
     int64_t u = u0;
-    int32_t s = u0 < u1 ? find_seq(a.useg, a.n_seqs, u0) : 0;
+    int32_t s = 0;
+    int4 d = make_int4(0, 0, 0, 0), dn = d;
+    if (u0 < u1) {
+        s = find_seq(a.sdesc, a.n_seqs, u0);
+        d = a.sdesc[s];
+        dn = a.sdesc[s + 1];  // prefetched: the next sequence's descriptor
+    }
+    // block-table entries of the current sequence, 32 pages per batch, one
+    // page per lane; reused by the kv heads of the sequence
+    int32_t cached_s = -1, cached_batch = -1, mine = -1;
     while (u < u1) {
-        while (a.useg[s + 1] <= u) ++s;  // skip sequences without units
-        int32_t lo, hi;
-        key_range(a.seq_len[s], a.window, lo, hi);
+        while (u >= (int64_t)d.x + d.w) {  // next sequence with units
+            ++s;
+            d = dn;
+            dn = a.sdesc[s + 1];
+        }
+        const int32_t lo = d.y, hi = d.z;
         const int32_t pf = lo / kP;
-        const int32_t npg = (hi - 1) / kP - pf + 1;
-        const int64_t seg0 = a.useg[s];
+        const int32_t npg = d.w / a.hkv;
+        const int64_t seg0 = d.x;
         const int32_t g = (int32_t)((u - seg0) / npg);
         const int32_t pi = (int32_t)((u - seg0) % npg);
         const int64_t seg_start = seg0 + (int64_t)g * npg, seg_end = seg_start + npg;
@@ -176,11 +203,34 @@ __device__ void decode_producer(DecodeSmem &sm, const CUtensorMap *tk, const CUt
         const bool direct = (u == seg_start) && (piece_end == seg_end);
         const int32_t slot = (u == u0) ? 0 : 1;
         const int32_t *btrow = a.bt + (int64_t)s * a.bt_stride;
-        int32_t mine = -1;
         for (int32_t j = 0; j < n; ++j) {
-            if ((j & 31) == 0)
-                mine = (j + lane < n && pf + pi + j + lane < a.bt_stride) ? btrow[pf + pi + j + lane] : -1;
-            const int32_t page = __shfl_sync(0xffffffffu, mine, j & 31);
+            const int32_t p = pi + j;  // page index in the sequence's key range
+            if (s != cached_s || (p >> 5) != cached_batch) {
+                cached_s = s;
+                cached_batch = p >> 5;
+                const int32_t q = (p & ~31) + lane;
+                mine = (q < npg && pf + q < a.bt_stride) ? btrow[pf + q] : -1;
+            }
+            const int32_t page = __shfl_sync(0xffffffffu, mine, p & 31);
+            if (a.slots && p == npg - 1) {
+                // fused append: the new token (position hi - 1) lies on the
+                // last page of the range; write its K and V rows of this kv
+                // head (lanes 0-15: K, 16-31: V, 16 bytes each) before the
+                // page is streamed
+                const int32_t slot = a.slots[s];
+                if (slot >= 0 && slot < a.pool_slots) {
+                    const int64_t dst = (((int64_t)(slot / kP) * a.hkv + g) * kP + slot % kP) * kD;
+                    const int64_t src = ((int64_t)s * a.hkv + g) * kD;
+                    const int c = (lane & 15) * 8;
+                    const __nv_bfloat16 *from = (lane < 16 ? a.k_new : a.v_new) + src + c;
+                    __nv_bfloat16 *to = (lane < 16 ? a.k_pool : a.v_pool) + dst + c;
+                    *reinterpret_cast<uint4 *>(to) = *reinterpret_cast<const uint4 *>(from);
+                } else if (slot >= a.pool_slots && lane == 0) {
+                    set_error(a.err, HSWA_ERR_BOUNDS);
+                }
+                fence_proxy_async_global();
+                __syncwarp();
+            }
             bool ok = true;
             if (lane == 0) {
                 ok = mbar_wait(&sm.empty[stage], phase ^ 1, a.err) && !*(volatile int32_t *)&sm.abort;
@@ -397,7 +447,9 @@ __global__ void __launch_bounds__(64) decode_mma_bf16_d128(const __grid_constant
         fence_barrier_init();
     }
     __syncthreads();
-    const int64_t U = a.useg[a.n_seqs], N = gridDim.x;
+    pdl_wait();  // the plan (and the table update before it) is complete
+    pdl_launch_dependents();
+    const int64_t U = a.sdesc[a.n_seqs].x, N = gridDim.x;
     if (U == 0) return;
     const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
     if (threadIdx.x >= 32)
@@ -410,8 +462,11 @@ __global__ void __launch_bounds__(64) decode_mma_bf16_d128(const __grid_constant
 // for sequences without keys.
 __global__ void __launch_bounds__(256) decode_combine(DecodeArgs a, int32_t n_ctas) {
     const int32_t s = blockIdx.y, g = blockIdx.x;
-    const int64_t U = a.useg[a.n_seqs], N = n_ctas;
-    const int32_t units = a.useg[s + 1] - a.useg[s];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t U = a.sdesc[a.n_seqs].x, N = n_ctas;
+    const int4 d = a.sdesc[s];
+    const int32_t units = d.w;
     const int h = threadIdx.x >> 5, d0 = (threadIdx.x & 31) * 4;
     __nv_bfloat16 *out = a.o + ((int64_t)s * a.hq + (int64_t)g * kG + h) * kD + d0;
     if (units == 0) {
@@ -419,7 +474,7 @@ __global__ void __launch_bounds__(256) decode_combine(DecodeArgs a, int32_t n_ct
         return;
     }
     const int32_t npg = units / a.hkv;
-    const int64_t lo = a.useg[s] + (int64_t)g * npg, hi = lo + npg;  // [lo, hi)
+    const int64_t lo = d.x + (int64_t)g * npg, hi = lo + npg;  // [lo, hi)
     const int64_t c_lo = cta_of(lo, U, N), c_hi = cta_of(hi - 1, U, N);
     if (c_lo == c_hi) return;
     float M = -INFINITY;
@@ -589,7 +644,7 @@ int decode_ctas_per_sm() {
 
 constexpr int kMaxCtasPerSm = 4;
 
-size_t useg_bytes(int n_seqs) { return ((size_t)(n_seqs + 1) * 4 + 255) & ~(size_t)255; }
+size_t desc_bytes(int n_seqs) { return ((size_t)(n_seqs + 1) * sizeof(int4) + 255) & ~(size_t)255; }
 
 }  // namespace
 }  // namespace hswa
@@ -602,12 +657,16 @@ extern "C" size_t hswa_decode_workspace_size(const hswa_pool *pool, int n_seqs) 
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 192;  // no device visible: size for the largest part
-    return useg_bytes(n_seqs) + (size_t)sms * kMaxCtasPerSm * 2 * sizeof(Partial);
+    return desc_bytes(n_seqs) + (size_t)sms * kMaxCtasPerSm * 2 * sizeof(Partial);
 }
 
-extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
-                           const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale, void *ws,
-                           size_t ws_bytes, hswa_stream_t stream) {
+namespace hswa {
+namespace {
+
+// Decode with an optional fused append (slots / k_new / v_new non-null).
+int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o, const int32_t *d_bt,
+                const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes, const int32_t *slots,
+                const void *k_new, const void *v_new, hswa_stream_t stream) {
     if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs ||
         (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA) ||
         (layer->kind == HSWA_KIND_SWA && layer->window <= 0))
@@ -615,16 +674,23 @@ extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const
     if (n_seqs == 0) return HSWA_OK;
     if (!q || !o || !d_bt || !d_seq_len || !layer->k_pool || !layer->v_pool) return HSWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (!decode_fast_ok(pool, layer, q, o))
+    const bool fused = slots != nullptr;
+    if (!decode_fast_ok(pool, layer, q, o) ||
+        (fused && (((uintptr_t)k_new & 15) || ((uintptr_t)v_new & 15)))) {
+        if (fused) {
+            const int rc = hswa_append_kv(pool, layer, k_new, v_new, slots, n_seqs, stream);
+            if (rc != HSWA_OK) return rc;
+        }
         return launch_attention_generic(pool, layer, q, o, d_bt, d_seq_len, nullptr, nullptr, n_seqs, n_seqs, scale,
                                         0, st);
+    }
     const hswa_config &c = pool->cfg;
     const int sms = sm_count();
     if (sms <= 0) return HSWA_ERR_CUDA;
     const int per_sm = decode_ctas_per_sm();
     if (per_sm <= 0) return HSWA_ERR_CUDA;
     const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
-    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < useg_bytes(n_seqs) + (size_t)n_ctas * 2 * sizeof(Partial))
+    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < desc_bytes(n_seqs) + (size_t)n_ctas * 2 * sizeof(Partial))
         return HSWA_ERR_INVALID_ARG;
     const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
     CUtensorMap tk, tv;
@@ -639,8 +705,14 @@ extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const
     a.o = static_cast<__nv_bfloat16 *>(o);
     a.bt = d_bt;
     a.seq_len = d_seq_len;
-    a.useg = static_cast<int32_t *>(ws);
-    a.part = reinterpret_cast<Partial *>(static_cast<uint8_t *>(ws) + useg_bytes(n_seqs));
+    a.sdesc = static_cast<const int4 *>(ws);
+    a.k_pool = static_cast<__nv_bfloat16 *>(layer->k_pool);
+    a.v_pool = static_cast<__nv_bfloat16 *>(layer->v_pool);
+    a.part = reinterpret_cast<Partial *>(static_cast<uint8_t *>(ws) + desc_bytes(n_seqs));
+    a.slots = slots;
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.pool_slots = (int64_t)num_pages * kP;
     a.n_seqs = n_seqs;
     a.bt_stride = c.max_pages_per_seq;
     a.hkv = c.n_kv_heads;
@@ -649,11 +721,34 @@ extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const
     a.num_pages = num_pages;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = error_word();
-    set_last_kernel("decode_mma_bf16_d128");
-    decode_plan<<<1, 1024, 0, st>>>(d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, const_cast<int32_t *>(a.useg));
-    decode_mma_bf16_d128<<<n_ctas, 64, kDecodeSmemBytes, st>>>(tk, tv, a);
-    decode_combine<<<dim3(c.n_kv_heads, n_seqs), 256, 0, st>>>(a, n_ctas);
-    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+    set_last_kernel(fused ? "decode_mma_bf16_d128+append" : "decode_mma_bf16_d128");
+    // three launches chained with programmatic dependent launch: each one
+    // is scheduled while its predecessor finishes and waits for it on entry
+    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window,
+                   static_cast<int4 *>(ws)) != cudaSuccess ||
+        launch_pdl(decode_mma_bf16_d128, dim3(n_ctas), dim3(64), kDecodeSmemBytes, st, tk, tv, a) != cudaSuccess ||
+        launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs), dim3(256), 0, st, a, n_ctas) != cudaSuccess)
+        return HSWA_ERR_CUDA;
+    return HSWA_OK;
+}
+
+}  // namespace
+}  // namespace hswa
+
+extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                           const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale, void *ws,
+                           size_t ws_bytes, hswa_stream_t stream) {
+    return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, nullptr, nullptr, nullptr,
+                       stream);
+}
+
+extern "C" int hswa_decode_append(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *k_new,
+                                  const void *v_new, const int32_t *d_slots, void *o, const int32_t *d_bt,
+                                  const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes,
+                                  hswa_stream_t stream) {
+    if (!k_new || !v_new || !d_slots) return HSWA_ERR_INVALID_ARG;
+    return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, d_slots, k_new, v_new,
+                       stream);
 }
 
 // ---------------------------------------------------- no-allocation decode
@@ -691,7 +786,7 @@ extern "C" int hswa_decode_noalloc(const hswa_pool *pool, const hswa_layer *laye
         const int sms = sm_count();
         const int per_sm = decode_ctas_per_sm();
         if (sms <= 0 || per_sm <= 0) return HSWA_ERR_CUDA;
-        const size_t need = useg_bytes(n_seqs) + (size_t)sms * std::min(per_sm, kMaxCtasPerSm) * 2 * sizeof(Partial);
+        const size_t need = desc_bytes(n_seqs) + (size_t)sms * std::min(per_sm, kMaxCtasPerSm) * 2 * sizeof(Partial);
         if (need > HSWA_DECODE_NOALLOC_SCRATCH_BYTES) return HSWA_ERR_INVALID_ARG;
     }
     void *ws = decode_scratch();

@@ -105,6 +105,11 @@ class DualPoolSession:
         B.hswa_decode(self.pool, self.layers[layer], q, o, self.bt(layer), self.d_seq_len, n_seqs, scale, ws,
                       ws.numel(), self.stream)
 
+    def decode_append(self, layer, q, k_new, v_new, d_slots, o, n_seqs, scale):
+        ws = self.workspace(n_seqs)
+        B.hswa_decode_append(self.pool, self.layers[layer], q, k_new, v_new, d_slots, o, self.bt(layer),
+                             self.d_seq_len, n_seqs, scale, ws, ws.numel(), self.stream)
+
     def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale):
         B.hswa_prefill_chunk(self.pool, self.layers[layer], q, o, self.bt(layer), d_prefix_len, d_q_start,
                              n_seqs, q.shape[0], max_q_len, scale, self.stream)

@@ -202,6 +202,18 @@ int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
                 const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale,
                 void *ws, size_t ws_bytes, hswa_stream_t stream);
 
+/* hswa_append_kv followed by hswa_decode in one call, for a decode step of
+ * one new token per sequence: k_new, v_new are device [n_seqs][Hkv][d] (row i
+ * = sequence i's new token) and d_slots[i] its slot in the layer kind's pool
+ * (from hswa_reserve); d_seq_len already counts the new token. On the fast
+ * path the CTA that streams the page holding a sequence's last token first
+ * writes that token's K and V rows there, so the append costs no launch of
+ * its own. Same result as the two calls in a row. */
+int hswa_decode_append(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *k_new,
+                       const void *v_new, const int32_t *d_slots, void *o, const int32_t *d_bt,
+                       const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes,
+                       hswa_stream_t stream);
+
 /* One chunked-prefill chunk of attention (Sec. 1.1: chunked prefill is
  * close to compute-bound). Sequence i < n_seqs has d_prefix_len[i] cached
  * tokens and n_i = d_q_start[i+1] - d_q_start[i] new tokens whose K/V are

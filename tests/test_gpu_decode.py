@@ -147,3 +147,39 @@ def test_decode_batch_full_size_sampled():
     B = len(w.cached)
     samples = sorted({0, 1, int(np.argmax(w.cached)), B - 1})
     run_decode_step(sc, samples, seed=1234, expect_kernel="decode_mma_bf16_d128")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [(64, 8, 128, 64, wl.DTYPE_BF16), (8, 2, 64, 16, wl.DTYPE_BF16)])
+def test_decode_append_fused_matches_oracle_and_separate_calls(shape):
+    """hswa_decode_append gives the oracle's result, leaves the pool exactly as
+    hswa_append_kv does, and matches append + decode bit for bit."""
+    hq, hkv, d, P, dtype = shape
+    cached = [0, 1, 63, 64, 65, 127, 700, 3000]
+    B = len(cached)
+    a = Scenario(hq, hkv, d, P, 128, dtype, cached, seed=21)
+    b = Scenario(hq, hkv, d, P, 128, dtype, cached, seed=21)
+    fa, sa = a.reserve(range(B), [1] * B)
+    fb, sb = b.reserve(range(B), [1] * B)
+    a.sess.sync()
+    b.sess.sync()
+    for layer, kind in enumerate(a.kinds):
+        slots = fa if kind == FULL else sa
+        snap = a.snapshot(layer, list(range(B)))
+        q = a.gen((B, hq, d), 300 + layer)
+        kn = a.gen((B, hkv, d), 310 + layer)
+        vn = a.gen((B, hkv, d), 320 + layer)
+        ds = torch.as_tensor(slots, device="cuda")
+        o_fused = torch.full((B, hq, d), float("nan"), dtype=a.sess.dtype, device="cuda")
+        a.sess.decode_append(layer, a.to_dev(q), a.to_dev(kn), a.to_dev(vn), ds, o_fused, B, a.scale)
+        assert a.sess.check() == 0
+        o_sep = torch.full_like(o_fused, float("nan"))
+        b.sess.append(layer, b.to_dev(kn), b.to_dev(vn), ds)
+        b.sess.decode(layer, b.to_dev(q), o_sep, B, b.scale)
+        assert b.sess.check() == 0
+        assert torch.equal(o_fused.view(torch.int16), o_sep.view(torch.int16))
+        assert torch.equal(a.sess.k[layer], b.sess.k[layer]) and torch.equal(a.sess.v[layer], b.sess.v[layer])
+        a.oracle_append(snap, slots, (raw_host(kn), raw_host(vn)), P)
+        exp = oracle.attention(raw_host(q), snap[0], snap[1], snap[2], np.arange(B), a.ora.seq_len[:B] - 1,
+                               a.window(layer), a.scale)
+        assert max_err(device_out(o_fused), exp) <= TOL[dtype]
