@@ -41,6 +41,29 @@ import hswa_workloads as wl  # noqa: E402
 KV_ROW = {wl.DTYPE_BF16: 2, wl.DTYPE_F32: 4}
 
 
+# DRAM traffic of the decode kernel per launch over its algorithmic bytes, from
+# one ncu capture at full size (profiles/decode_mma_bf16_d128_decode_batch_traffic.md),
+# valid only for the kernel sources it was taken on.
+DECODE_TRAFFIC = {"ratio": 1.0022, "sources": ("decode.cu", "common.cuh"),
+                  "sha256": "3b00ecb5aadadabf5869dbc5b7242efc44f20ef6580b1ff411cdd8b3aeb58845"}
+
+
+def source_digest(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "hybrid_sliding_window_dual_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def decode_traffic(alg_bytes):
+    """Captured traffic scaled to this launch, or None if the kernel changed."""
+    if DECODE_TRAFFIC["sha256"] != source_digest(DECODE_TRAFFIC["sources"]):
+        return None
+    return int(DECODE_TRAFFIC["ratio"] * alg_bytes)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -698,7 +721,7 @@ def run_decode(args, world, rank, local):
                    "l2": "inputs larger than L2 (%.1f GB KV per step)" % (step_bytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": decode_traffic(full_layer_bytes),
                      "kernel": "decode_mma_bf16_d128 with fused append (Full layer; plan + main + combine)",
                      "peak_source": peak_kind, "frac_of_8tbs": round(achieved / 8000.0, 4)},
         "e2e": {"value": round(total_bytes / e2e_secs / 1e9 * (1.0), 2), "unit": "GB/s",
