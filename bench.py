@@ -545,6 +545,77 @@ class Hybrid70:
         if self.steps_done % 64 == 0:
             sess.release(range(B))
 
+    def offload(self):
+        """Untimed: gather every SWA window to pinned host memory, evict the
+        SWA segments and give the windows new pages (their bytes are stale
+        until reloaded)."""
+        torch, sess, B = self.torch, self.sess, self.B
+        from hybrid_sliding_window_dual_gb300.session import window_offsets
+        swa = [i for i, k in enumerate(self.w.layer_kinds) if k == wl.KIND_SWA]
+        lens = self.lens()
+        off = window_offsets(lens, self.w.window)
+        self.d_off = torch.as_tensor(off, device="cuda")
+        n = int(off[-1]) * 2 * self.w.n_kv_heads * self.w.head_dim
+        if not hasattr(self, "host") or self.host[0].numel() != n:
+            self.host = [torch.empty(n, dtype=wl.TORCH_DTYPE[self.w.dtype], pin_memory=True) for _ in swa]
+        with torch.cuda.stream(self.stream):
+            for buf, ly in zip(self.host, swa):
+                sess.gather(ly, self.d_off, B, buf)
+        self.stream.synchronize()
+        sess.swa_drop(range(B))
+        sess.swa_restore(range(B))
+        with torch.cuda.stream(self.stream):
+            sess.sync()
+            self.d_len_snap = sess.d_seq_len.clone()
+        self.stream.synchronize()
+        self.reload_bytes = len(swa) * n * KV_ROW[self.w.dtype]
+        return swa
+
+    def reload_step(self, mode):
+        """One 70-layer step whose SWA windows all come back from the host
+        tier: "serial" (every window before layer 0), "direct" (scatter
+        kernels reading pinned host memory on a side stream, layer by layer)
+        or "staged" (copy engines into a staging ring, device scatter right
+        before each layer). Returns the device time in ms."""
+        torch, sess, B = self.torch, self.sess, self.B
+        swa = self.offload()
+        if not hasattr(self, "side"):
+            self.side = torch.cuda.Stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fs, ss = sess.reserve(range(B), [1] * B)
+        self.stream.synchronize()
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            self.slot_host[0].numpy()[:] = fs
+            self.slot_host[1].numpy()[:] = ss
+            self.slot_dev.copy_(self.slot_host, non_blocking=True)
+            sess.sync()
+            self.side.wait_stream(self.stream)
+            events, staged = {}, None
+            if mode == "staged":
+                from hybrid_sliding_window_dual_gb300.session import LayerwiseReload
+                n = self.host[0].numel()
+                if not hasattr(self, "staging"):
+                    self.staging = [torch.empty(n, dtype=self.host[0].dtype, device="cuda") for _ in range(8)]
+                staged = LayerwiseReload(sess, swa, self.d_len_snap, self.d_off, B, self.host, self.side,
+                                         self.staging)
+                staged.start(self.stream)
+            else:
+                events = sess.reload_async(swa, self.d_len_snap, self.d_off, B, self.host, self.side)
+                if mode == "serial":
+                    self.stream.wait_stream(self.side)
+            for i, kind in enumerate(self.w.layer_kinds):
+                if mode == "direct" and i in events:
+                    self.stream.wait_event(events[i])
+                if staged is not None:
+                    staged.before_layer(i, self.stream)
+                sess.decode_append(i, self.q[i], self.kn[i], self.vn[i],
+                                   self.slot_dev[0 if kind == wl.KIND_FULL else 1], self.o[i], B, self.scale)
+            e1.record(self.stream)
+        self.stream.synchronize()
+        self.steps_done += 1
+        return e0.elapsed_time(e1)
+
     def sizing(self):
         """Dual pool (per-layer Full pools + live SWA pages) against one O(N)
         pool for all 70 layers, in bytes, at the current lengths."""
@@ -754,6 +825,11 @@ def run_decode(args, world, rank, local):
             "ms_per_step": round(h["ms_per_step"], 3), "tokens_per_s": round(h["tokens_per_s"], 1),
             "full_layer_gbs": round(h["full_layer_gbs"], 1), "full_layer_ms": round(h["full_layer_ms"], 3),
             "step_gb": round(h["step_bytes"] / 1e9, 2), "sizing": h["sizing"],
+            "swa_reload": {"gb_from_host": round(h["reload"]["bytes"] / 1e9, 3),
+                           "step_ms_resident": round(h["reload"]["step_ms_resident"], 3),
+                           "step_ms_serial_reload": round(h["reload"]["step_ms_serial"], 3),
+                           "step_ms_layerwise_direct": round(h["reload"]["step_ms_direct"], 3),
+                           "step_ms_layerwise_staged": round(h["reload"]["step_ms_staged"], 3)},
             "note": "the 10 Full layers read one physical 64 GiB Full pool"}
     if not args.no_transfer:
         t = measure_transfer(3)
@@ -890,13 +966,18 @@ def measure_hybrid70(steps, warmup, n_seqs=None):
     step_bytes = 0.5 * (before["step"] + after["step"])
     full_ms = float(np.mean([a.elapsed_time(b) for a, b in hb.full_events]))
     sizing = hb.sizing()
+    # reload of every SWA window from the host tier inside one step
+    reload = {"bytes": 0, "step_ms_resident": secs / steps * 1e3}
+    for mode in ("serial", "direct", "staged"):
+        reload["step_ms_" + mode] = float(np.mean([hb.reload_step(mode) for _ in range(2)]))
+    reload["bytes"] = hb.reload_bytes
     st = hb.sess.check()
     if st != 0:
         raise RuntimeError("device status %d after hybrid70" % st)
     out = {"gbs": step_bytes * steps / secs / 1e9, "ms_per_step": secs / steps * 1e3,
            "full_layer_gbs": 0.5 * (before["full_layer"] + after["full_layer"]) / (full_ms / 1e3) / 1e9,
            "full_layer_ms": full_ms, "step_bytes": step_bytes, "tokens_per_s": len(w.cached) * steps / secs,
-           "launches": hb.launches - l0, "sizing": sizing}
+           "launches": hb.launches - l0, "sizing": sizing, "reload": reload}
     del hb
     torch.cuda.empty_cache()
     return out

@@ -122,6 +122,20 @@ class DualPoolSession:
         B.hswa_swa_scatter(self.pool, self.layers[layer], self.d_swa_bt, self.d_seq_len, d_tok_offset, n_seqs,
                            src, self.stream)
 
+    def reload_async(self, layer_ids, d_seq_len, d_tok_offset, n_seqs, host_bufs, stream):
+        """Reload offloaded SWA windows layer by layer with the scatter kernel
+        reading pinned host memory directly, on a side stream; one event per
+        layer ({layer: event}) for the compute stream to wait on."""
+        events = {}
+        with torch.cuda.stream(stream):
+            for ly, buf in zip(layer_ids, host_bufs):
+                B.hswa_swa_scatter(self.pool, self.layers[ly], self.d_swa_bt, d_seq_len, d_tok_offset, n_seqs,
+                                   buf, stream)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                events[ly] = ev
+        return events
+
     def check(self):
         return B.hswa_check(self.stream)
 
@@ -132,3 +146,62 @@ def window_offsets(seq_len, window):
     off = np.zeros(len(n) + 1, np.int64)
     off[1:] = np.cumsum(n)
     return off
+
+
+class LayerwiseReload:
+    """Layer-by-layer reload of offloaded SWA windows, overlapped with the
+    attention of earlier layers ("MiMo-V2.5 Series Inference Full-Link
+    Optimization", Sec. 2.1, asynchronous layer-by-layer pulling).
+
+    The copy engines move each layer's packed window from pinned host memory
+    into one of ``n_staging`` device staging buffers on ``copy_stream``; right
+    before an SWA layer's attention, ``before_layer`` makes the compute stream
+    wait for that copy and scatters the window from staging into the layer's
+    pool pages (hswa_swa_scatter, device to device). The copy stream runs
+    ``n_staging`` layers ahead; a staging buffer is refilled only after its
+    scatter has run. ``d_seq_len`` is the lengths the windows were gathered at
+    (a snapshot), so the step's own reserve may change the live lengths.
+    """
+
+    def __init__(self, sess, layer_ids, d_seq_len, d_tok_offset, n_seqs, host_bufs, copy_stream, staging):
+        self.sess, self.layers = sess, list(layer_ids)
+        self.d_seq_len, self.d_off, self.n = d_seq_len, d_tok_offset, n_seqs
+        self.host, self.copy, self.staging = list(host_bufs), copy_stream, list(staging)
+        self.copied = {}
+        self.free = [None] * len(self.staging)
+        self.next = 0
+
+    def _enqueue_copy(self):
+        k = self.next
+        if k >= len(self.layers):
+            return
+        slot = k % len(self.staging)
+        with torch.cuda.stream(self.copy):
+            if self.free[slot] is not None:
+                self.copy.wait_event(self.free[slot])
+            n = self.host[k].numel()
+            self.staging[slot][:n].copy_(self.host[k], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(self.copy)
+            self.copied[self.layers[k]] = (ev, slot, n)
+        self.next += 1
+
+    def start(self, compute_stream):
+        """Enqueue the first copies (after the work already on compute_stream)."""
+        self.copy.wait_stream(compute_stream)
+        for _ in range(len(self.staging)):
+            self._enqueue_copy()
+
+    def before_layer(self, layer, compute_stream):
+        """Call before enqueueing `layer`'s attention on compute_stream."""
+        if layer not in self.copied:
+            return
+        ev, slot, n = self.copied.pop(layer)
+        with torch.cuda.stream(compute_stream):
+            compute_stream.wait_event(ev)
+            B.hswa_swa_scatter(self.sess.pool, self.sess.layers[layer], self.sess.d_swa_bt, self.d_seq_len,
+                               self.d_off, self.n, self.staging[slot][:n], compute_stream)
+            free = torch.cuda.Event()
+            free.record(compute_stream)
+            self.free[slot] = free
+        self._enqueue_copy()

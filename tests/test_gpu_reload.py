@@ -1,0 +1,87 @@
+"""Layer-by-layer reload of offloaded SWA windows, overlapped with attention
+(MiMo page, Sec. 2.1: asynchronous layer-by-layer pulling).
+
+Two identical dual pools run the same decode step over a 14-layer hybrid
+model (Full at every 7th layer). Pool b first offloads every SWA window to
+pinned host memory, evicts the SWA segments, gives the windows new pages and
+overwrites the SWA pools with a sentinel; its step then reloads each layer's
+window on a side stream while earlier layers compute, waiting only right
+before each SWA layer. Every layer's output must equal pool a's bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hswa_workloads as wl
+from hybrid_sliding_window_dual_gb300.session import LayerwiseReload, window_offsets
+from scenario import Scenario
+
+
+def make(seed):
+    kinds = tuple(wl.KIND_FULL if i % 7 == 6 else wl.KIND_SWA for i in range(14))
+    cached = [5, 127, 128, 129, 700, 2000, 4095, 64, 1, 300, 3333, 256]
+    return Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, layer_kinds=kinds, seed=seed, permute=True,
+                    swa_pages=len(cached) * 8 + 40)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", ["serial", "direct", "staged"])
+def test_layerwise_reload_step_equals_resident_step(mode):
+    a, b = make(61), make(61)
+    B = len(a.cached)
+    kinds = a.kinds
+    swa_layers = [i for i, k in enumerate(kinds) if k == wl.KIND_SWA]
+    # offload pool b's windows, evict, restore to new pages, poison the pools
+    lens = b.ora.seq_len[:B].copy()
+    off = window_offsets(lens, b.W)
+    d_off = torch.as_tensor(off, device="cuda")
+    n = int(off[-1]) * 2 * 8 * 128
+    host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in swa_layers]
+    for buf, ly in zip(host, swa_layers):
+        b.sess.gather(ly, d_off, B, buf)
+    assert b.sess.check() == 0
+    assert b.sess.swa_drop(range(B)) == b.ora.swa_drop(range(B))
+    assert b.sess.swa_restore(range(B)) == b.ora.swa_restore(range(B))
+    b.sess.sync()
+    for ly in swa_layers:
+        b.sess.k[ly].fill_(7.0)
+        b.sess.v[ly].fill_(-7.0)
+    d_len_snap = b.sess.d_seq_len.clone()
+    torch.cuda.synchronize()
+    # the step on both pools
+    outs = {}
+    side = torch.cuda.Stream()
+    for name, sc in (("a", a), ("b", b)):
+        fs, ss = sc.reserve(range(B), [1] * B)
+        sc.sess.sync()
+        d_fs = torch.as_tensor(fs, device="cuda")
+        d_ss = torch.as_tensor(ss, device="cuda")
+        events, staged = {}, None
+        cur = torch.cuda.current_stream()
+        if name == "b":
+            side.wait_stream(cur)
+            if mode == "direct":    # the scatter kernel reads pinned host memory, side stream
+                events = sc.sess.reload_async(swa_layers, d_len_snap, d_off, B, host, side)
+            elif mode == "serial":  # every window back before the first layer
+                sc.sess.reload_async(swa_layers, d_len_snap, d_off, B, host, side)
+                cur.wait_stream(side)
+            else:                   # copy engines into a 3-buffer staging ring
+                staging = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+                staged = LayerwiseReload(sc.sess, swa_layers, d_len_snap, d_off, B, host, side, staging)
+                staged.start(cur)
+        res = []
+        for ly, kind in enumerate(kinds):
+            q = sc.to_dev(sc.gen((B, 64, 128), 900 + ly))
+            kn = sc.to_dev(sc.gen((B, 8, 128), 950 + ly))
+            vn = sc.to_dev(sc.gen((B, 8, 128), 990 + ly))
+            if ly in events:
+                cur.wait_event(events[ly])
+            if staged is not None:
+                staged.before_layer(ly, cur)
+            o = torch.empty_like(q)
+            sc.sess.decode_append(ly, q, kn, vn, d_fs if kind == wl.KIND_FULL else d_ss, o, B, sc.scale)
+            res.append(o)
+        assert sc.sess.check() == 0
+        outs[name] = res
+    for ly in range(len(kinds)):
+        assert torch.equal(outs["a"][ly].view(torch.int16), outs["b"][ly].view(torch.int16)), ly
