@@ -55,6 +55,12 @@ def load_library(path):
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
     lib.hswa_oracle_threads.restype = ctypes.c_int
+    lib.hswa_oracle_attention_fp8.restype = ctypes.c_int
+    lib.hswa_oracle_attention_fp8.argtypes = [
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
     return lib
 
 
@@ -119,6 +125,54 @@ def attention(q, k_pool, v_pool, block_table, q_seq, q_pos, window, scale, lib=N
     if rc != 0:
         raise ValueError("bad attention sizes")
     return out
+
+
+def attention_fp8(q, k_codes, k_scale, v_codes, v_scale, block_table, q_seq, q_pos, window, scale,
+                  lib=None):
+    """float64 attention over an FP8 pool (exact dequantization).
+
+    k_codes: uint8 [pages, Hkv, P, d]; v_codes: uint8 [pages, Hkv, d, P]
+    (pages stored transposed); k_scale, v_scale: float32 [pages, Hkv, P, d/128].
+    q: [nq, Hq, d] fp32 or bf16. Returns float64 [nq, Hq, d]."""
+    qa, dt = _raw(q)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    nq, hq, d = qa.shape
+    pages, hkv, P, d2 = kc.shape
+    assert d2 == d and vc.shape == (pages, hkv, d, P) and ks.shape == (pages, hkv, P, d // 128)
+    assert vs.shape == ks.shape
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    qs = np.ascontiguousarray(q_seq, dtype=np.int32)
+    qp = np.ascontiguousarray(q_pos, dtype=np.int64)
+    out = np.zeros((nq, hq, d), np.float64)
+    rc = (lib or _load()).hswa_oracle_attention_fp8(
+        nq, qs.ctypes.data, qp.ctypes.data, hq, hkv, d, P, int(window), float(scale), dt, qa.ctypes.data,
+        kc.ctypes.data, ks.ctypes.data, vc.ctypes.data, vs.ctypes.data, pages, bt.ctypes.data, bt.shape[1],
+        out.ctypes.data)
+    if rc == -1:
+        raise IndexError("a key's block-table entry is not a live page")
+    if rc != 0:
+        raise ValueError("bad attention sizes")
+    return out
+
+
+def append_kv_fp8(k_codes, k_scale, v_codes, v_scale, k_new, v_new, slots):
+    """Quantize new K/V rows ([T, Hkv, d] fp32 values) per 128-element tile
+    and write them at their slots: K row-major, V into the transposed page."""
+    from .fp8 import quantize_tiles
+    P = k_codes.shape[2]
+    kq, ks = quantize_tiles(k_new)
+    vq, vs = quantize_tiles(v_new)
+    for t, slot in enumerate(np.asarray(slots).tolist()):
+        if slot < 0:
+            continue
+        page, row = slot // P, slot % P
+        k_codes[page, :, row, :] = kq[t]
+        k_scale[page, :, row, :] = ks[t]
+        v_codes[page, :, :, row] = vq[t]
+        v_scale[page, :, row, :] = vs[t]
 
 
 def append_kv(pool, new, slots):

@@ -122,6 +122,99 @@ int hswa_oracle_attention(int64_t n_queries, const int32_t *q_seq,
     return bad ? -1 : 0;
 }
 
+/* Value of an E4M3 code (OCP 8-bit float: 1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, subnormals, S.1111.111 = NaN). */
+static double e4m3_value(uint8_t c)
+{
+    const int e = (c >> 3) & 0xF, m = c & 0x7;
+    if ((c & 0x7F) == 0x7F)
+        return NAN;
+    const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (c & 0x80) ? -mag : mag;
+}
+
+/*
+ * The same attention over an FP8 KV cache ("Baidu AI Cloud: Day-0 support
+ * for hybrid-architecture LLMs", Optimization 2 item 2: FP8 per token, per
+ * head, per 128-element tile). Keys and values are the exact dequantized
+ * values code * scale:
+ *   k_codes [num_pages][Hkv][P][d]   E4M3, k_scale [num_pages][Hkv][P][d/128]
+ *   v_codes [num_pages][Hkv][d][P]   E4M3 (each page stored transposed),
+ *   v_scale [num_pages][Hkv][P][d/128]
+ * q is fp32 (dtype 0) or bf16 (dtype 1). Returns as hswa_oracle_attention.
+ */
+int hswa_oracle_attention_fp8(int64_t n_queries, const int32_t *q_seq, const int64_t *q_pos,
+                              int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                              int window, double scale, int q_dtype, const void *q,
+                              const uint8_t *k_codes, const float *k_scale,
+                              const uint8_t *v_codes, const float *v_scale, int64_t num_pages,
+                              const int32_t *block_table, int64_t bt_stride, double *o)
+{
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || head_dim % 128 != 0 ||
+        page_size <= 0 || n_q_heads % n_kv_heads != 0 || window < 0)
+        return -2;
+    const int tiles = head_dim / 128;
+    int bad = 0;
+    const int64_t total = n_queries * n_q_heads;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t qi = 0; qi < total; ++qi) {
+        const int64_t i = qi / n_q_heads;
+        const int h = (int)(qi % n_q_heads);
+        const int g = (int)(((int64_t)h * n_kv_heads) / n_q_heads);
+        const int64_t t = q_pos[i];
+        const int32_t *bt = block_table + (int64_t)q_seq[i] * bt_stride;
+        const int64_t lo = (window > 0 && t - window + 1 > 0) ? t - window + 1 : 0;
+        const int64_t n_keys = t - lo + 1;
+        double *out = o + qi * head_dim;
+        double *score = (double *)malloc(sizeof(double) * (size_t)(n_keys > 0 ? n_keys : 1));
+        int64_t *blk = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_keys > 0 ? n_keys : 1));
+        int my_bad = 0;
+
+        double m = -INFINITY;
+        for (int64_t j = lo; j <= t; ++j) {
+            const int32_t page = bt[j / page_size];
+            if (page < 0 || page >= num_pages) {
+                my_bad = 1;
+                break;
+            }
+            const int64_t b = (int64_t)page * n_kv_heads + g;  /* (page, kv head) block */
+            const int64_t row = j % page_size;
+            double dot = 0.0;
+            for (int c = 0; c < head_dim; ++c) {
+                const double kv = e4m3_value(k_codes[(b * page_size + row) * head_dim + c]) *
+                                  (double)k_scale[(b * page_size + row) * tiles + c / 128];
+                dot += elem(q, qi * head_dim + c, q_dtype) * kv;
+            }
+            score[j - lo] = scale * dot;
+            blk[j - lo] = b * page_size + row;  /* (block, row) index */
+            if (score[j - lo] > m)
+                m = score[j - lo];
+        }
+        for (int c = 0; c < head_dim; ++c)
+            out[c] = 0.0;
+        if (my_bad) {
+#pragma omp atomic write
+            bad = 1;
+        } else if (n_keys > 0) {
+            double z = 0.0;
+            for (int64_t jj = 0; jj < n_keys; ++jj) {
+                const double w = exp(score[jj] - m);
+                const int64_t b = blk[jj] / page_size, row = blk[jj] % page_size;
+                z += w;
+                for (int c = 0; c < head_dim; ++c)
+                    out[c] += w * e4m3_value(v_codes[(b * head_dim + c) * page_size + row]) *
+                              (double)v_scale[(b * page_size + row) * tiles + c / 128];
+            }
+            for (int c = 0; c < head_dim; ++c)
+                out[c] /= z;
+        }
+        free(score);
+        free(blk);
+    }
+    return bad ? -1 : 0;
+}
+
 /* Number of OpenMP threads the attention loop runs on. */
 int hswa_oracle_threads(void)
 {
