@@ -179,6 +179,43 @@ def decode_bytes(w, lens_after):
             "swa_layer": swa_kv + qo + new, "step": full_kv + swa_kv + 2 * (qo + new)}
 
 
+def decode_bytes_fp8(w, lens_after):
+    """Algorithmic bytes of one decode step over FP8 pools: per key and kv
+    head one E4M3 byte per element of K and of V plus their two fp32 scales."""
+    row = w.n_kv_heads * (w.head_dim + 4)  # one K (or V) row of all kv heads, with its scale
+    B = len(lens_after)
+    es = KV_ROW[w.dtype]
+    full_kv = 2 * row * int(np.sum(lens_after))
+    swa_kv = 2 * row * int(np.sum(np.minimum(lens_after, w.window)))
+    qo = 2 * B * w.n_q_heads * w.head_dim * es
+    new = 2 * B * w.n_kv_heads * w.head_dim * es + 2 * B * row  # bf16 new K/V read, FP8 rows written
+    return {"full_kv": full_kv, "swa_kv": swa_kv, "full_layer": full_kv + qo + new,
+            "swa_layer": swa_kv + qo + new, "step": full_kv + swa_kv + 2 * (qo + new)}
+
+
+def measure_decode_fp8(steps, warmup):
+    """The decode-batch step over FP8 pools: GB/s of FP8 bytes and tokens/s."""
+    import torch
+    w = wl.decode_batch()
+    bench = DecodeBatch(w, warmup + steps + 8, fp8=True)
+    for _ in range(warmup):
+        bench.step()
+    bench.stream.synchronize()
+    before = decode_bytes_fp8(w, bench.lens() + 1)
+    secs = time_steps(lambda: bench.step(time_full_decode=True), steps, bench.stream, 1)
+    after = decode_bytes_fp8(w, bench.lens())
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in bench.decode_events]))
+    bench.finish()
+    step_bytes = 0.5 * (before["step"] + after["step"])
+    full_bytes = 0.5 * (before["full_layer"] + after["full_layer"])
+    out = {"gbs": step_bytes * steps / secs / 1e9, "ms_per_step": secs / steps * 1e3,
+           "tokens_per_s": len(w.cached) * steps / secs, "full_layer_gbs": full_bytes / (dec_ms / 1e3) / 1e9,
+           "full_layer_ms": dec_ms}
+    del bench
+    torch.cuda.empty_cache()
+    return out
+
+
 def prefill_flops(w, prefix, chunk):
     """Valid (query, key) pairs x 4 d Hq for a Full and an SWA layer."""
     full = sum(c * p + c * (c + 1) // 2 for p, c in zip(prefix, chunk))
@@ -188,9 +225,10 @@ def prefill_flops(w, prefix, chunk):
 
 
 class DecodeBatch:
-    """The decode-batch workload on the GPU through the C ABI."""
+    """The decode-batch workload on the GPU through the C ABI (bf16 pools, or
+    FP8 E4M3 pools with per-token-head scales when fp8=True)."""
 
-    def __init__(self, w, extra_steps):
+    def __init__(self, w, extra_steps, fp8=False):
         import torch
         import hybrid_sliding_window_dual_gb300 as H
         from hybrid_sliding_window_dual_gb300.session import DualPoolSession
@@ -200,9 +238,10 @@ class DecodeBatch:
         full_pages = sum(math.ceil((L + extra_steps + 1) / P) for L in w.cached) + 16
         swa_pages = B * (math.ceil((W + 4096) / P) + 2) + 16
         max_pages = max(math.ceil((L + extra_steps + 1) / P) for L in w.cached) + 1
+        self.fp8 = fp8
         cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
-                       head_dim=w.head_dim, dtype=w.dtype, full_pages=full_pages, swa_pages=swa_pages,
-                       max_seqs=B, max_pages_per_seq=max_pages)
+                       head_dim=w.head_dim, dtype=H.HSWA_DTYPE_FP8_E4M3 if fp8 else w.dtype,
+                       full_pages=full_pages, swa_pages=swa_pages, max_seqs=B, max_pages_per_seq=max_pages)
         self.stream = torch.cuda.Stream()
         self.sess = DualPoolSession(cfg, [wl.KIND_FULL, wl.KIND_SWA], wl.permutation(full_pages, w.seed),
                                     wl.permutation(swa_pages, w.seed + 1), stream=self.stream, init="empty")
@@ -213,12 +252,20 @@ class DecodeBatch:
         with torch.cuda.stream(self.stream):
             for i in range(2):
                 for t, seed in ((self.sess.k[i], 10 + i), (self.sess.v[i], 20 + i)):
-                    g = torch.Generator(device="cuda")
-                    g.manual_seed(seed)
-                    flat = t.view(-1)
-                    for j in range(0, flat.numel(), 1 << 28):
-                        n = min(1 << 28, flat.numel() - j)
-                        flat[j:j + n] = torch.randn(n, generator=g, device="cuda").to(t.dtype)
+                    if fp8:  # seeded E4M3 codes without the NaN patterns
+                        g = torch.Generator(device="cuda")
+                        g.manual_seed(seed)
+                        flat = t.view(-1)
+                        for j in range(0, flat.numel(), 1 << 28):
+                            n = min(1 << 28, flat.numel() - j)
+                            mag = torch.randint(0, 0x7F, (n,), generator=g, device="cuda", dtype=torch.int32)
+                            sgn = torch.randint(0, 2, (n,), generator=g, device="cuda", dtype=torch.int32)
+                            flat[j:j + n] = (mag | (sgn << 7)).to(torch.uint8)
+                    else:
+                        fill_normal(t, seed)
+                if fp8:
+                    self.sess.ks[i].uniform_(0.001, 0.011)
+                    self.sess.vs[i].uniform_(0.001, 0.011)
             self.sess.sync()
         dt = wl.TORCH_DTYPE[w.dtype]
         self.q = [wl.normal((B, w.n_q_heads, w.head_dim), 100 + i, w.dtype, "cuda") for i in range(2)]
@@ -803,6 +850,17 @@ def run_decode(args, world, rank, local):
     }
     if args.breakdown:
         line["breakdown_us"] = bd
+    if not args.no_fp8:
+        del bench
+        torch.cuda.empty_cache()
+        f8 = measure_decode_fp8(200, 5)
+        line["fp8_decode"] = {
+            "workload": "decode_batch over FP8 E4M3 pools (scale per token, kv head, 128-element tile)",
+            "gbs": round(f8["gbs"], 1), "unit": "GB/s", "frac": round(f8["gbs"] / hbm, 4),
+            "ms_per_step": round(f8["ms_per_step"], 4), "tokens_per_s": round(f8["tokens_per_s"], 1),
+            "full_layer_gbs": round(f8["full_layer_gbs"], 1), "full_layer_ms": round(f8["full_layer_ms"], 4),
+            "kernel": "decode_mma_fp8_d128"}
+        bench = None
     if not args.no_prefill:
         del bench
         torch.cuda.empty_cache()
@@ -1085,6 +1143,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-hybrid70", action="store_true")
     ap.add_argument("--no-transfer", action="store_true")
     ap.add_argument("--hybrid-steps", type=int, default=5)

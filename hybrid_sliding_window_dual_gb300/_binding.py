@@ -27,6 +27,7 @@ HSWA_KIND_FULL = 0
 HSWA_KIND_SWA = 1
 HSWA_DTYPE_F32 = 0
 HSWA_DTYPE_BF16 = 1
+HSWA_DTYPE_FP8_E4M3 = 2
 
 
 class HswaError(RuntimeError):
@@ -47,7 +48,8 @@ class Config(ctypes.Structure):
 
 class Layer(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p)]
+                ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p

@@ -12,6 +12,8 @@
 // d * sizeof(dtype) bytes is read and written with full 32-byte sectors.
 #include <algorithm>
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -80,6 +82,50 @@ __global__ void swa_xfer_kernel(chunk_t *kp, chunk_t *vp, chunk_t *packed, const
     }
 }
 
+// FP8 append: one warp per (token, kv head). Each lane holds 4 of the 128
+// elements of the K row and of the V row; the warp's amax gives the tile's
+// scale = amax / 448 (1 for an all-zero tile), each element is divided by it
+// (correctly rounded) and rounded to the nearest E4M3 code, saturating. K is
+// written as a row of the page, V into column `row` of the transposed page.
+__global__ void append_kv_fp8_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                                     uint8_t *kp, uint8_t *vp, float *ks, float *vs,
+                                     const int32_t *__restrict__ slots, int64_t n_tokens, int32_t hkv,
+                                     int32_t page, int64_t pool_slots, int *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    if (w >= n_tokens * hkv) return;
+    const int64_t t = w / hkv;
+    const int32_t g = (int32_t)(w % hkv);
+    const int32_t slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= pool_slots) {
+        if (lane == 0) set_error(err, HSWA_ERR_BOUNDS);
+        return;
+    }
+    const int64_t blk = (int64_t)(slot / page) * hkv + g;  // (page, kv head) block
+    const int32_t row = slot % page;
+    for (int which = 0; which < 2; ++which) {
+        const __nv_bfloat16 *src = (which ? v : k) + (t * hkv + g) * 128 + lane * 4;
+        float x[4];
+        for (int i = 0; i < 4; ++i) x[i] = __bfloat162float(src[i]);
+        float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        uint8_t q[4];
+        for (int i = 0; i < 4; ++i)
+            q[i] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[i], scale), __NV_SATFINITE, __NV_E4M3);
+        if (which == 0) {
+            uint8_t *dst = kp + (blk * page + row) * 128 + lane * 4;
+            *reinterpret_cast<uint32_t *>(dst) =
+                (uint32_t)q[0] | ((uint32_t)q[1] << 8) | ((uint32_t)q[2] << 16) | ((uint32_t)q[3] << 24);
+            if (lane == 0) ks[blk * page + row] = scale;
+        } else {
+            for (int i = 0; i < 4; ++i) vp[(blk * 128 + lane * 4 + i) * page + row] = q[i];
+            if (lane == 0) vs[blk * page + row] = scale;
+        }
+    }
+}
+
 int esize(const hswa_config &c) { return c.dtype == HSWA_DTYPE_F32 ? 4 : 2; }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
@@ -100,6 +146,19 @@ extern "C" int hswa_append_kv(const hswa_pool *pool, const hswa_layer *layer, co
         !layer->v_pool || (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA))
         return HSWA_ERR_INVALID_ARG;
     const hswa_config &c = pool->cfg;
+    if (c.dtype == HSWA_DTYPE_FP8_E4M3) {
+        if (c.head_dim != 128) return HSWA_ERR_UNSUPPORTED;
+        if (!layer->k_scale || !layer->v_scale) return HSWA_ERR_INVALID_ARG;
+        if (n_tokens == 0) return HSWA_OK;
+        const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+        const int64_t threads = (int64_t)n_tokens * c.n_kv_heads * 32;
+        set_last_kernel("append_kv_fp8");
+        append_kv_fp8_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+            (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, (uint8_t *)layer->k_pool, (uint8_t *)layer->v_pool,
+            layer->k_scale, layer->v_scale, d_slots, n_tokens, c.n_kv_heads, c.page_size,
+            (int64_t)num_pages * c.page_size, error_word());
+        return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+    }
     const int64_t row_bytes = (int64_t)c.head_dim * esize(c);
     if (row_bytes % 16 || !aligned16(k) || !aligned16(v) || !aligned16(layer->k_pool) || !aligned16(layer->v_pool))
         return HSWA_ERR_UNSUPPORTED;
@@ -122,6 +181,7 @@ static int swa_xfer(const hswa_pool *pool, const hswa_layer *layer, const int32_
         !layer->v_pool)
         return HSWA_ERR_INVALID_ARG;
     const hswa_config &c = pool->cfg;
+    if (c.dtype == HSWA_DTYPE_FP8_E4M3) return HSWA_ERR_UNSUPPORTED;
     const int64_t row_bytes = (int64_t)c.head_dim * esize(c);
     if (row_bytes % 16 || !aligned16(buf) || !aligned16(layer->k_pool) || !aligned16(layer->v_pool))
         return HSWA_ERR_UNSUPPORTED;

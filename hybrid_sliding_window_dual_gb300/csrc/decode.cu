@@ -24,6 +24,9 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
@@ -46,6 +49,7 @@ struct StageDesc {
 };
 
 struct DecodeSmem {
+    static constexpr int kStages = ::hswa::kStages;
     uint8_t k[kStages][kPageHeadBytes];
     uint8_t v[kStages][kPageHeadBytes];
     uint8_t q[kStages][kQBytes];
@@ -56,6 +60,34 @@ struct DecodeSmem {
 };
 
 constexpr size_t kDecodeSmemBytes = sizeof(DecodeSmem) + 1024;  // + alignment slack
+
+// FP8 pools: a stage holds one page of one kv head as E4M3 codes, K as
+// [64 keys][128 B] (128-byte swizzle) and V transposed as [128 d][64 B]
+// (64-byte swizzle), plus the 64 K and 64 V scales of the page.
+constexpr uint32_t kK8Bytes = kP * kD;
+constexpr uint32_t kV8Bytes = kD * kP;
+constexpr uint32_t kScaleBytes = kP * 4;
+
+constexpr int kConsumers8 = 4;  // FP8 consumer warps, one 16-key group of a page each
+
+struct DecodeSmem8 {
+    static constexpr int kStages = 3;
+    uint8_t k[kStages][kK8Bytes];
+    uint8_t v[kStages][kV8Bytes];
+    uint8_t q[kStages][kQBytes];
+    float ks[kStages][kP];
+    float vs[kStages][kP];
+    // end-of-piece merge of the consumer warps' (max, sum, o) states
+    float mo[kConsumers8 - 1][kG][kD];
+    float mm[kConsumers8 - 1][kG];
+    float ml[kConsumers8 - 1][kG];
+    StageDesc desc[kStages];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int32_t abort;
+};
+
+constexpr size_t kDecodeSmem8Bytes = sizeof(DecodeSmem8) + 1024;
 
 struct Partial {
     float m[kG];
@@ -70,6 +102,7 @@ struct DecodeArgs {
     const int32_t *seq_len;
     const int4 *sdesc;    // [n_seqs + 1] {first unit, key lo, key hi, units}; [n].x = total
     __nv_bfloat16 *k_pool, *v_pool;
+    const float *k_scale, *v_scale;  // FP8 pools: [pages][Hkv][P] each
     Partial *part;        // [n_ctas][2]
     // optional fused append: new K / V rows [n_seqs][Hkv][d] written at
     // slots[s] before the page that holds them is streamed (null = none)
@@ -161,8 +194,10 @@ __device__ __forceinline__ uint32_t swz(int row, int d) {
     return (uint32_t)((d >> 6) * kBoxBytes + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4));
 }
 
-__device__ void decode_producer(DecodeSmem &sm, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeArgs &a,
+template <bool kFP8, class Smem>
+__device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeArgs &a,
                                 int64_t u0, int64_t u1) {
+    constexpr int kStages = Smem::kStages;
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
         prefetch_tmap(tk);
@@ -212,7 +247,7 @@ __device__ void decode_producer(DecodeSmem &sm, const CUtensorMap *tk, const CUt
                 mine = (q < npg && pf + q < a.bt_stride) ? btrow[pf + q] : -1;
             }
             const int32_t page = __shfl_sync(0xffffffffu, mine, p & 31);
-            if (a.slots && p == npg - 1) {
+            if (!kFP8 && a.slots && p == npg - 1) {
                 // fused append: the new token (position hi - 1) lies on the
                 // last page of the range; write its K and V rows of this kv
                 // head (lanes 0-15: K, 16-31: V, 16 bytes each) before the
@@ -250,15 +285,25 @@ __device__ void decode_producer(DecodeSmem &sm, const CUtensorMap *tk, const CUt
                         flags |= kSkip;
                     }
                     d.flags = flags;
-                    const uint32_t bytes = (valid ? 4 * kBoxBytes : 0) + (j == 0 ? kQBytes : 0);
+                    const uint32_t page_bytes = kFP8 ? kK8Bytes + kV8Bytes + 2 * kScaleBytes : 4 * kBoxBytes;
+                    const uint32_t bytes = (valid ? page_bytes : 0) + (j == 0 ? kQBytes : 0);
                     if (bytes) {
                         mbar_arrive_expect_tx(&sm.full[stage], bytes);
                         if (valid) {
-                            const int32_t row = (page * a.hkv + g) * kP;
-                            tma_load_2d(sm.k[stage], tk, 0, row, &sm.full[stage]);
-                            tma_load_2d(sm.k[stage] + kBoxBytes, tk, 64, row, &sm.full[stage]);
-                            tma_load_2d(sm.v[stage], tv, 0, row, &sm.full[stage]);
-                            tma_load_2d(sm.v[stage] + kBoxBytes, tv, 64, row, &sm.full[stage]);
+                            const int32_t blk = page * a.hkv + g;  // (page, kv head) block
+                            if constexpr (kFP8) {
+                                auto &s8 = reinterpret_cast<DecodeSmem8 &>(sm);
+                                tma_load_2d(s8.k[stage], tk, 0, blk * kP, &sm.full[stage]);
+                                tma_load_2d(s8.v[stage], tv, 0, blk * kD, &sm.full[stage]);
+                                bulk_g2s(s8.ks[stage], a.k_scale + (int64_t)blk * kP, kScaleBytes, &sm.full[stage]);
+                                bulk_g2s(s8.vs[stage], a.v_scale + (int64_t)blk * kP, kScaleBytes, &sm.full[stage]);
+                            } else {
+                                const int32_t row = blk * kP;
+                                tma_load_2d(sm.k[stage], tk, 0, row, &sm.full[stage]);
+                                tma_load_2d(sm.k[stage] + kBoxBytes, tk, 64, row, &sm.full[stage]);
+                                tma_load_2d(sm.v[stage], tv, 0, row, &sm.full[stage]);
+                                tma_load_2d(sm.v[stage] + kBoxBytes, tv, 64, row, &sm.full[stage]);
+                            }
                         }
                         if (j == 0)
                             bulk_g2s(sm.q[stage], a.q + ((int64_t)s * a.hq + (int64_t)g * kG) * kD, kQBytes,
@@ -453,9 +498,280 @@ __global__ void __launch_bounds__(64) decode_mma_bf16_d128(const __grid_constant
     if (U == 0) return;
     const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
     if (threadIdx.x >= 32)
-        decode_producer(sm, &tk, &tv, a, u0, u1);
+        decode_producer<false>(sm, &tk, &tv, a, u0, u1);
     else
         decode_consumer(sm, a, u0, u1);
+}
+
+// ---------------------------------------------------------- FP8 decode
+// Key rows of a 16-key group in the order the QK MMA's A rows take them:
+// after the movmatrix transpose of S^T, thread (g, q) then holds P for the
+// keys 4q..4q+3 that one 32-bit load of an E4M3 row gives the PV MMA.
+__device__ __forceinline__ int key_of_row(int r) { return 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3); }
+
+// 16-byte chunk of (row, byte) in a [rows][128 B] tile with the 128-byte
+// swizzle, and in a [rows][64 B] tile with the 64-byte swizzle.
+__device__ __forceinline__ uint32_t swz128(int row, int byte) {
+    return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7)) & 7) << 4));
+}
+__device__ __forceinline__ uint32_t swz64(int row, int byte) {
+    return (uint32_t)(row * 64 + ((((byte >> 4) ^ (row >> 1)) & 3) << 4));
+}
+
+// Four E4M3 codes (bytes b0..b3 of r) as two f16 pairs {b0, b1}, {b2, b3},
+// each value times 2^-8: the code's exponent and mantissa bits land in the
+// low exponent and high mantissa bits of the f16 (the exponent biases differ
+// by 8), which also holds for subnormals. The sign is moved up by adding the
+// sign bit to itself (the carry clears bit 7 and sets bit 8) before the
+// shift. Callers fold the 2^8 into the scales.
+__device__ __forceinline__ void e4m3x4_f16x2x2(uint32_t r, uint32_t &lo, uint32_t &hi) {
+    const uint32_t t0 = __byte_perm(r, 0u, 0x4140);  // {b0, 0, b1, 0}
+    const uint32_t t1 = __byte_perm(r, 0u, 0x4342);  // {b2, 0, b3, 0}
+    lo = (t0 + (t0 & 0x00800080u)) << 7;
+    hi = (t1 + (t1 & 0x00800080u)) << 7;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers8 * 32) : "memory"); }
+
+// The consumers over FP8 pages. Warp w takes the 16 keys 16w..16w+15 of
+// every page: S^T = (K codes as f16) Q^T with the key rows taken in
+// key_of_row order and d read 4 codes at a time (Q's fragments use the same d
+// order), times the per-key K scale; an online softmax of its own; P times
+// the per-key V scale feeds the f16 PV MMA, whose A operand (V^T) comes from
+// the transposed page without any transpose. At the end of a piece warps 1-3
+// hand their (max, sum, o) to warp 0 through shared memory, which merges and
+// writes.
+__device__ void decode_consumer_fp8(DecodeSmem8 &sm, const DecodeArgs &a, int64_t u0, int64_t u1) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int gr = lane >> 2, qd = lane & 3;
+    constexpr int kStages = DecodeSmem8::kStages;
+    uint32_t qf[8][2];
+    float oacc[8][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int stage = 0;
+    uint32_t phase = 0;
+    const uint32_t kbase = smem_u32(sm.k[0]), vbase = smem_u32(sm.v[0]);
+    const int j = lane >> 3;
+    const int ar = (lane & 7) + 8 * (j & 1);  // A row this lane addresses in ldmatrix (QK)
+    const int c0 = w * 16 + key_of_row(gr), c1 = w * 16 + key_of_row(gr + 8);  // keys of this thread's S rows
+
+    for (int64_t u = u0; u < u1; ++u) {
+        bool ok = mbar_wait(&sm.full[stage], phase, a.err) && !*(volatile int32_t *)&sm.abort;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0) sm.abort = 1;
+            return;
+        }
+        const StageDesc d = sm.desc[stage];
+        if (d.flags & kFirst) {
+            const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm.q[stage]) + gr * kD;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int c = ks * 16 + 4 * qd;
+                qf[ks][0] = pack_f16(__bfloat162float(qs[c]), __bfloat162float(qs[c + 1]));
+                qf[ks][1] = pack_f16(__bfloat162float(qs[c + 2]), __bfloat162float(qs[c + 3]));
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+        const bool any = !(d.flags & kSkip) && w * 16 + 15 >= d.lo && w * 16 < d.hi;
+        if (any) {
+            const uint32_t kb = kbase + stage * kK8Bytes, vb = vbase + stage * kV8Bytes;
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int key = w * 16 + key_of_row(ar);
+#pragma unroll
+            for (int dc = 0; dc < 4; ++dc) {
+                uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+                ldsm_x4(kb + swz128(key, dc * 32 + 16 * (j >> 1)), r0, r1, r2, r3);
+                e4m3x4_f16x2x2(r0, a0, a2);
+                e4m3x4_f16x2x2(r1, a1, a3);
+                mma_f16_16816(sacc, a0, a1, a2, a3, qf[2 * dc][0], qf[2 * dc][1]);
+                e4m3x4_f16x2x2(r2, a0, a2);
+                e4m3x4_f16x2x2(r3, a1, a3);
+                mma_f16_16816(sacc, a0, a1, a2, a3, qf[2 * dc + 1][0], qf[2 * dc + 1][1]);
+            }
+            const bool v0 = c0 >= d.lo && c0 < d.hi, v1 = c1 >= d.lo && c1 < d.hi;
+            // K codes entered the MMA as value * 2^-8
+            const float s0 = sm.ks[stage][c0] * (256.f * a.scale_log2);
+            const float s1 = sm.ks[stage][c1] * (256.f * a.scale_log2);
+            sacc[0] = v0 ? sacc[0] * s0 : -INFINITY;
+            sacc[1] = v0 ? sacc[1] * s0 : -INFINITY;
+            sacc[2] = v1 ? sacc[2] * s1 : -INFINITY;
+            sacc[3] = v1 ? sacc[3] * s1 : -INFINITY;
+            float mx0 = fmaxf(sacc[0], sacc[2]), mx1 = fmaxf(sacc[1], sacc[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            // this warp saw at least one valid key in the piece so far (n > -inf),
+            // else it keeps nothing and P stays 0
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float b0 = n0 == -INFINITY ? 0.f : n0, b1 = n1 == -INFINITY ? 0.f : n1;
+            const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
+            const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
+            m0 = n0;
+            m1 = n1;
+            const float p0 = fast_exp2(sacc[0] - b0), p1 = fast_exp2(sacc[1] - b1);
+            const float p2 = fast_exp2(sacc[2] - b0), p3 = fast_exp2(sacc[3] - b1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            // V codes enter the MMA as value * 2^-8: P carries the 2^8
+            const float w0 = sm.vs[stage][c0] * 256.f, w1 = sm.vs[stage][c1] * 256.f;
+            const uint32_t pb0 = movmatrix_t(pack_f16(p0 * w0, p1 * w0));
+            const uint32_t pb1 = movmatrix_t(pack_f16(p2 * w1, p3 * w1));
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                oacc[dt][0] *= al0;
+                oacc[dt][1] *= al1;
+                oacc[dt][2] *= al0;
+                oacc[dt][3] *= al1;
+            }
+            // O^T += V^T P^T: A rows are d (two 16-row tiles per load), 4 key codes per 32-bit word
+#pragma unroll
+            for (int dp = 0; dp < 4; ++dp) {
+                uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+                ldsm_x4(vb + swz64(dp * 32 + j * 8 + (lane & 7), w * 16), r0, r1, r2, r3);
+                e4m3x4_f16x2x2(r0, a0, a2);
+                e4m3x4_f16x2x2(r1, a1, a3);
+                mma_f16_16816(oacc[2 * dp], a0, a1, a2, a3, pb0, pb1);
+                e4m3x4_f16x2x2(r2, a0, a2);
+                e4m3x4_f16x2x2(r3, a1, a3);
+                mma_f16_16816(oacc[2 * dp + 1], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+
+        if (d.flags & kLast) {
+            float t0 = l0, t1 = l1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                t0 += __shfl_xor_sync(0xffffffffu, t0, off);
+                t1 += __shfl_xor_sync(0xffffffffu, t1, off);
+            }
+            const int h0 = 2 * qd, h1 = 2 * qd + 1;
+            if (w > 0) {  // hand this warp's state to warp 0
+                if (gr == 0) {
+                    sm.mm[w - 1][h0] = m0;
+                    sm.mm[w - 1][h1] = m1;
+                    sm.ml[w - 1][h0] = t0;
+                    sm.ml[w - 1][h1] = t1;
+                }
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    sm.mo[w - 1][h0][dt * 16 + gr] = oacc[dt][0];
+                    sm.mo[w - 1][h1][dt * 16 + gr] = oacc[dt][1];
+                    sm.mo[w - 1][h0][dt * 16 + gr + 8] = oacc[dt][2];
+                    sm.mo[w - 1][h1][dt * 16 + gr + 8] = oacc[dt][3];
+                }
+            }
+            consumer_bar();
+            if (w == 0) {
+                float M0 = m0, M1 = m1;
+                for (int i = 0; i < kConsumers8 - 1; ++i) {
+                    M0 = fmaxf(M0, sm.mm[i][h0]);
+                    M1 = fmaxf(M1, sm.mm[i][h1]);
+                }
+                const float e0 = M0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
+                const float e1 = M1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
+                t0 *= e0;
+                t1 *= e1;
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    oacc[dt][0] *= e0;
+                    oacc[dt][1] *= e1;
+                    oacc[dt][2] *= e0;
+                    oacc[dt][3] *= e1;
+                }
+                for (int i = 0; i < kConsumers8 - 1; ++i) {
+                    const float f0 = M0 == -INFINITY ? 0.f : fast_exp2(sm.mm[i][h0] - M0);
+                    const float f1 = M1 == -INFINITY ? 0.f : fast_exp2(sm.mm[i][h1] - M1);
+                    t0 += f0 * sm.ml[i][h0];
+                    t1 += f1 * sm.ml[i][h1];
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        oacc[dt][0] += f0 * sm.mo[i][h0][dt * 16 + gr];
+                        oacc[dt][1] += f1 * sm.mo[i][h1][dt * 16 + gr];
+                        oacc[dt][2] += f0 * sm.mo[i][h0][dt * 16 + gr + 8];
+                        oacc[dt][3] += f1 * sm.mo[i][h1][dt * 16 + gr + 8];
+                    }
+                }
+                if (d.flags & kDirect) {
+                    const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
+                    __nv_bfloat16 *o0 = a.o + ((int64_t)d.seq * a.hq + (int64_t)d.kvh * kG + h0) * kD;
+                    __nv_bfloat16 *o1 = o0 + kD;
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        o0[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][0] * i0);
+                        o1[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][1] * i1);
+                        o0[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][2] * i0);
+                        o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][3] * i1);
+                    }
+                } else {
+                    Partial &p = a.part[(int64_t)blockIdx.x * 2 + d.slot];
+                    if (gr == 0) {
+                        p.m[h0] = M0;
+                        p.m[h1] = M1;
+                        p.l[h0] = t0;
+                        p.l[h1] = t1;
+                    }
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        p.o[h0][dt * 16 + gr] = oacc[dt][0];
+                        p.o[h1][dt * 16 + gr] = oacc[dt][1];
+                        p.o[h0][dt * 16 + gr + 8] = oacc[dt][2];
+                        p.o[h1][dt * 16 + gr + 8] = oacc[dt][3];
+                    }
+                }
+            }
+            consumer_bar();  // the merge area is free again
+        }
+        if (++stage == kStages) stage = 0, phase ^= 1;
+    }
+}
+
+__global__ void __launch_bounds__(32 * (kConsumers8 + 1)) decode_mma_fp8_d128(const __grid_constant__ CUtensorMap tk,
+                                                                           const __grid_constant__ CUtensorMap tv,
+                                                                           DecodeArgs a) {
+    extern __shared__ uint8_t raw[];
+    DecodeSmem8 &sm =
+        *reinterpret_cast<DecodeSmem8 *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < DecodeSmem8::kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], kConsumers8);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t U = a.sdesc[a.n_seqs].x, N = gridDim.x;
+    if (U == 0) return;
+    const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
+    if (threadIdx.x >= 32 * kConsumers8)
+        decode_producer<true>(sm, &tk, &tv, a, u0, u1);
+    else
+        decode_consumer_fp8(sm, a, u0, u1);
 }
 
 // Merge the partial records of segments split between CTAs; write zeros
@@ -592,7 +908,7 @@ int launch_attention_generic(const hswa_pool *pool, const hswa_layer *layer, con
                              const int32_t *q_start, int32_t n_rows, int32_t n_seqs, float scale, int mode,
                              cudaStream_t st) {
     const hswa_config &c = pool->cfg;
-    if (c.head_dim > 256) return HSWA_ERR_UNSUPPORTED;
+    if (c.head_dim > 256 || c.dtype == HSWA_DTYPE_FP8_E4M3) return HSWA_ERR_UNSUPPORTED;
     if (n_rows == 0) return HSWA_OK;
     const int32_t window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
     const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
@@ -619,6 +935,30 @@ int launch_attention_generic(const hswa_pool *pool, const hswa_layer *layer, con
 }
 
 namespace {
+
+bool decode_fp8_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
+    const hswa_config &c = pool->cfg;
+    return c.dtype == HSWA_DTYPE_FP8_E4M3 && c.head_dim == kD && c.n_q_heads == kG * c.n_kv_heads &&
+           c.page_size == kP && layer->k_scale && layer->v_scale && ((uintptr_t)q & 15) == 0 &&
+           ((uintptr_t)o & 15) == 0 && ((uintptr_t)layer->k_pool & 15) == 0 && ((uintptr_t)layer->v_pool & 15) == 0 &&
+           ((uintptr_t)layer->k_scale & 15) == 0 && ((uintptr_t)layer->v_scale & 15) == 0;
+}
+
+int decode_fp8_ctas_per_sm() {
+    static int v = -1;
+    if (v < 0) {
+        if (cudaFuncSetAttribute(decode_mma_fp8_d128, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDecodeSmem8Bytes) != cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_fp8_d128, 32 * (kConsumers8 + 1),
+                                                          kDecodeSmem8Bytes) !=
+            cudaSuccess)
+            n = 1;
+        v = std::max(1, n);
+    }
+    return v;
+}
 
 bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
     const hswa_config &c = pool->cfg;
@@ -663,6 +1003,71 @@ extern "C" size_t hswa_decode_workspace_size(const hswa_pool *pool, int n_seqs) 
 namespace hswa {
 namespace {
 
+int fill_args(DecodeArgs &a, const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+              const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale, void *ws) {
+    const hswa_config &c = pool->cfg;
+    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.bt = d_bt;
+    a.seq_len = d_seq_len;
+    a.sdesc = static_cast<const int4 *>(ws);
+    a.k_pool = static_cast<__nv_bfloat16 *>(layer->k_pool);
+    a.v_pool = static_cast<__nv_bfloat16 *>(layer->v_pool);
+    a.k_scale = layer->k_scale;
+    a.v_scale = layer->v_scale;
+    a.part = reinterpret_cast<Partial *>(static_cast<uint8_t *>(ws) + desc_bytes(n_seqs));
+    a.slots = nullptr;
+    a.k_new = a.v_new = nullptr;
+    a.pool_slots = (int64_t)num_pages * kP;
+    a.n_seqs = n_seqs;
+    a.bt_stride = c.max_pages_per_seq;
+    a.hkv = c.n_kv_heads;
+    a.hq = c.n_q_heads;
+    a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
+    a.num_pages = num_pages;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.err = error_word();
+    return num_pages;
+}
+
+// Decode over an FP8 pool (a fused append quantizes first, as its own launch).
+int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o, const int32_t *d_bt,
+               const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes, const int32_t *slots,
+               const void *k_new, const void *v_new, hswa_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!decode_fp8_ok(pool, layer, q, o)) return HSWA_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    const int per_sm = decode_fp8_ctas_per_sm();
+    if (sms <= 0 || per_sm <= 0) return HSWA_ERR_CUDA;
+    const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
+    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < desc_bytes(n_seqs) + (size_t)n_ctas * 2 * sizeof(Partial))
+        return HSWA_ERR_INVALID_ARG;
+    if (slots) {
+        const int rc = hswa_append_kv(pool, layer, k_new, v_new, slots, n_seqs, stream);
+        if (rc != HSWA_OK) return rc;
+    }
+    const hswa_config &c = pool->cfg;
+    DecodeArgs a;
+    const int32_t num_pages = fill_args(a, pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws);
+    const uint64_t blocks = (uint64_t)num_pages * c.n_kv_heads;
+    CUtensorMap tk, tv;
+    if (!make_tmap_2d(&tk, layer->k_pool, blocks * kP, kD, kP, kD, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tv, layer->v_pool, blocks * kD, kP, kD, kP, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                      CU_TENSOR_MAP_SWIZZLE_64B))
+        return HSWA_ERR_CUDA;
+    set_last_kernel(slots ? "append_kv_fp8+decode_mma_fp8_d128" : "decode_mma_fp8_d128");
+    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window,
+                   static_cast<int4 *>(ws)) != cudaSuccess ||
+        launch_pdl(decode_mma_fp8_d128, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)), kDecodeSmem8Bytes, st, tk, tv,
+                   a) !=
+            cudaSuccess ||
+        launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs), dim3(256), 0, st, a, n_ctas) != cudaSuccess)
+        return HSWA_ERR_CUDA;
+    return HSWA_OK;
+}
+
 // Decode with an optional fused append (slots / k_new / v_new non-null).
 int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o, const int32_t *d_bt,
                 const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes, const int32_t *slots,
@@ -675,6 +1080,9 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     if (!q || !o || !d_bt || !d_seq_len || !layer->k_pool || !layer->v_pool) return HSWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool fused = slots != nullptr;
+    if (pool->cfg.dtype == HSWA_DTYPE_FP8_E4M3)
+        return decode_fp8(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, slots, k_new, v_new,
+                          stream);
     if (!decode_fast_ok(pool, layer, q, o) ||
         (fused && (((uintptr_t)k_new & 15) || ((uintptr_t)v_new & 15)))) {
         if (fused) {

@@ -22,7 +22,8 @@ namespace {
 bool valid_config(const hswa_config *c) {
     return c && c->window > 0 && c->page_size > 0 && c->n_q_heads > 0 && c->n_kv_heads > 0 &&
            c->n_q_heads % c->n_kv_heads == 0 && c->head_dim > 0 &&
-           (c->dtype == HSWA_DTYPE_F32 || c->dtype == HSWA_DTYPE_BF16) && c->full_pages > 0 &&
+           (c->dtype == HSWA_DTYPE_F32 || c->dtype == HSWA_DTYPE_BF16 || c->dtype == HSWA_DTYPE_FP8_E4M3) &&
+           c->full_pages > 0 &&
            c->swa_pages > 0 && c->max_seqs > 0 && c->max_pages_per_seq > 0 &&
            (int64_t)c->max_pages_per_seq * c->page_size <= INT32_MAX &&
            (int64_t)c->full_pages * c->page_size <= INT32_MAX &&

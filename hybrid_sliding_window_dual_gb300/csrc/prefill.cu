@@ -494,6 +494,7 @@ extern "C" int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer
     if (!q || !o || !d_bt || !d_prefix_len || !d_q_start || !layer->k_pool || !layer->v_pool)
         return HSWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (pool->cfg.dtype == HSWA_DTYPE_FP8_E4M3) return HSWA_ERR_UNSUPPORTED;
     if (!prefill_fast_ok(pool, layer, q, o))
         return launch_attention_generic(pool, layer, q, o, d_bt, nullptr, d_prefix_len, d_q_start, max_q_len,
                                         n_seqs, scale, 1, st);

@@ -70,7 +70,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 static size_t elem_bytes(CUtensorMapDataType t) {
-    return t == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
+    return t == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : t == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;
 }
 
 bool make_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,

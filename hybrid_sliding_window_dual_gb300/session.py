@@ -10,7 +10,8 @@ import torch
 
 from . import _binding as B
 
-_TORCH_DTYPE = {B.HSWA_DTYPE_F32: torch.float32, B.HSWA_DTYPE_BF16: torch.bfloat16}
+_TORCH_DTYPE = {B.HSWA_DTYPE_F32: torch.float32, B.HSWA_DTYPE_BF16: torch.bfloat16,
+                B.HSWA_DTYPE_FP8_E4M3: torch.uint8}
 
 
 class DualPoolSession:
@@ -35,23 +36,34 @@ class DualPoolSession:
         self.d_swa_bt = torch.full(rows, -1, dtype=torch.int32, device=self.device)
         self.d_seq_len = torch.zeros(config.max_seqs, dtype=torch.int32, device=self.device)
         self.kinds = list(layer_kinds)
-        self.k, self.v, self.layers = [], [], []
+        self.k, self.v, self.ks, self.vs, self.layers = [], [], [], [], []
+        self.fp8 = config.dtype == B.HSWA_DTYPE_FP8_E4M3
         shared = None
         for kind in self.kinds:
             pages = config.full_pages if kind == B.HSWA_KIND_FULL else config.swa_pages
-            shape = (pages, config.n_kv_heads, config.page_size, config.head_dim)
+            P, d, hkv = config.page_size, config.head_dim, config.n_kv_heads
+            shape = (pages, hkv, P, d)
             if kind == B.HSWA_KIND_FULL and share_full_pool and shared is not None:
-                k, v = shared
+                k, v, ks, vs = shared
             else:
                 alloc = torch.zeros if init == "zeros" else torch.empty
                 k = alloc(shape, dtype=self.dtype, device=self.device)
-                v = alloc(shape, dtype=self.dtype, device=self.device)
+                # FP8 pools keep each page of V transposed, [d][P], plus fp32
+                # scales per (token, kv head, 128-element tile)
+                v = alloc((pages, hkv, d, P) if self.fp8 else shape, dtype=self.dtype, device=self.device)
+                ks = vs = None
+                if self.fp8:
+                    ks = torch.ones((pages, hkv, P, d // 128), dtype=torch.float32, device=self.device)
+                    vs = torch.ones_like(ks)
                 if kind == B.HSWA_KIND_FULL and share_full_pool:
-                    shared = (k, v)
+                    shared = (k, v, ks, vs)
             self.k.append(k)
             self.v.append(v)
-            self.layers.append(B.Layer(kind=kind, window=config.window, k_pool=k.data_ptr(),
-                                       v_pool=v.data_ptr()))
+            self.ks.append(ks)
+            self.vs.append(vs)
+            self.layers.append(B.Layer(kind=kind, window=config.window, k_pool=k.data_ptr(), v_pool=v.data_ptr(),
+                                       k_scale=ks.data_ptr() if ks is not None else None,
+                                       v_scale=vs.data_ptr() if vs is not None else None))
         self.ws = None
 
     def close(self):

@@ -80,6 +80,18 @@ extern "C" {
 
 #define HSWA_DTYPE_F32 0
 #define HSWA_DTYPE_BF16 1
+/* FP8 KV cache ("Baidu AI Cloud: Day-0 support for hybrid-architecture
+ * LLMs", Optimization 2, KV Cache FP8 Tiled Quantization): K and V are E4M3
+ * codes with one fp32 scale per (token, kv head, 128-element tile), value =
+ * code * scale. Layout per layer: k_pool [pages][Hkv][P][d] bytes, v_pool
+ * [pages][Hkv][d][P] bytes (each page stored transposed), k_scale and
+ * v_scale [pages][Hkv][P][d / 128] fp32. q, o and the new K/V handed to the
+ * append stay bf16; the append quantizes: scale = amax / 448 (1 if amax is
+ * 0), code = round-to-nearest-even(x / scale) saturating at 448. Supported
+ * by hswa_append_kv, hswa_decode and hswa_decode_append with d = 128,
+ * 8 query heads per kv head and P = 64; other calls return
+ * HSWA_ERR_UNSUPPORTED. */
+#define HSWA_DTYPE_FP8_E4M3 2
 
 /* A CUDA stream (the same handle as cudaStream_t); NULL = default stream. */
 typedef struct CUstream_st *hswa_stream_t;
@@ -92,7 +104,7 @@ typedef struct hswa_config {
     int32_t n_q_heads;         /* Hq                                            */
     int32_t n_kv_heads;        /* Hkv, divides Hq                               */
     int32_t head_dim;          /* d                                             */
-    int32_t dtype;             /* HSWA_DTYPE_*                                  */
+    int32_t dtype;             /* HSWA_DTYPE_* of the pools                     */
     int32_t full_pages;        /* pages in the Full pool                        */
     int32_t swa_pages;         /* pages in the SWA pool                         */
     int32_t max_seqs;          /* rows of each block table                      */
@@ -103,7 +115,9 @@ typedef struct hswa_layer {
     int32_t kind;   /* HSWA_KIND_FULL or HSWA_KIND_SWA                          */
     int32_t window; /* keys per query for an SWA layer (> 0); ignored for Full  */
     void *k_pool;   /* device [num_pages][Hkv][P][d], caller-owned             */
-    void *v_pool;   /* device, same shape                                      */
+    void *v_pool;   /* device, same shape ([num_pages][Hkv][d][P] for FP8)     */
+    float *k_scale; /* FP8 only: device [num_pages][Hkv][P][d/128], else NULL  */
+    float *v_scale; /* FP8 only: same shape                                    */
 } hswa_layer;
 
 /* ------------------------------------------------ pool bookkeeping (host) */

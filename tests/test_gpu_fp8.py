@@ -1,0 +1,119 @@
+"""FP8 (E4M3) KV cache on the GPU against the oracle.
+
+The cached history is seeded random E4M3 codes (no NaN pattern) with seeded
+positive scales; new tokens are bf16 and quantized by hswa_append_kv. The
+codes and scales the library writes must equal the oracle's quantizer bit
+for bit, and hswa_decode / hswa_decode_append over the FP8 pools must match
+the oracle's float64 attention over the exactly dequantized pools (max abs
+2e-2, the bf16 I/O tolerance)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import hswa_workloads as wl
+import oracle
+import hybrid_sliding_window_dual_gb300 as H
+from hybrid_sliding_window_dual_gb300.session import DualPoolSession
+from scenario import raw_host
+
+FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
+HQ, HKV, D, P, W = 64, 8, 128, 64, 128
+
+
+def seeded_codes(shape, seed):
+    """Random E4M3 codes without the NaN patterns 0x7f / 0xff."""
+    g = torch.Generator().manual_seed(seed)
+    mag = torch.randint(0, 0x7F, shape, generator=g, dtype=torch.int32)
+    sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int32) << 7
+    return (mag | sign).to(torch.uint8)
+
+
+def seeded_scales(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return 0.001 + 0.01 * torch.rand(shape, generator=g, dtype=torch.float32)
+
+
+class Fp8Case:
+    def __init__(self, cached, seed, kinds=(FULL, SWA)):
+        B = len(cached)
+        full_pages = sum(math.ceil((L + 8) / P) for L in cached) + 4
+        swa_pages = B * 5 + 80
+        mp = max(math.ceil((L + 8) / P) for L in cached) + 1
+        self.cfg = H.Config(window=W, page_size=P, n_q_heads=HQ, n_kv_heads=HKV, head_dim=D,
+                            dtype=H.HSWA_DTYPE_FP8_E4M3, full_pages=full_pages, swa_pages=swa_pages, max_seqs=B,
+                            max_pages_per_seq=mp)
+        fo, so = wl.permutation(full_pages, seed), wl.permutation(swa_pages, seed + 1)
+        self.sess = DualPoolSession(self.cfg, kinds, fo, so)
+        self.ora = oracle.DualPool(W, P, full_pages, swa_pages, B, mp, fo, so)
+        self.kinds, self.B, self.cached = list(kinds), B, list(cached)
+        for s, L in enumerate(cached):
+            for start in range(0, L, 4096):
+                n = min(4096, L - start)
+                a = self.sess.reserve([s], [n])
+                b = self.ora.reserve([s], [n])
+                assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+                assert self.sess.release([s]) == self.ora.swa_release([s])
+        self.sess.sync()
+        for i in range(len(kinds)):
+            for t, seed_i in ((self.sess.k[i], 10), (self.sess.v[i], 20)):
+                t.copy_(seeded_codes(tuple(t.shape), seed * 100 + seed_i + i))
+            for t, seed_i in ((self.sess.ks[i], 30), (self.sess.vs[i], 40)):
+                t.copy_(seeded_scales(tuple(t.shape), seed * 100 + seed_i + i))
+        torch.cuda.synchronize()
+        self.host = [[x.cpu().numpy().copy() for x in (self.sess.k[i], self.sess.ks[i], self.sess.v[i],
+                                                        self.sess.vs[i])] for i in range(len(kinds))]
+
+    def table(self, layer):
+        return self.ora.full_bt if self.kinds[layer] == FULL else self.ora.swa_bt
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fused", [False, True])
+def test_fp8_append_and_decode_match_oracle(fused):
+    cached = [0, 1, 63, 64, 65, 127, 128, 700, 3000, 9000]
+    c = Fp8Case(cached, seed=71)
+    B = c.B
+    fs, ss = c.sess.reserve(range(B), [1] * B)
+    efs, ess = c.ora.reserve(range(B), [1] * B)
+    assert np.array_equal(fs, efs) and np.array_equal(ss, ess)
+    c.sess.sync()
+    scale = 1 / math.sqrt(D)
+    for layer, kind in enumerate(c.kinds):
+        slots = fs if kind == FULL else ss
+        q = wl.normal((B, HQ, D), 500 + layer, wl.DTYPE_BF16)
+        kn = wl.normal((B, HKV, D), 510 + layer, wl.DTYPE_BF16) * 3
+        vn = wl.normal((B, HKV, D), 520 + layer, wl.DTYPE_BF16) * 0.5
+        o = torch.full((B, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ds = torch.as_tensor(slots, device="cuda")
+        if fused:
+            c.sess.decode_append(layer, q.cuda(), kn.cuda(), vn.cuda(), ds, o, B, scale)
+        else:
+            c.sess.append(layer, kn.cuda(), vn.cuda(), ds)
+            c.sess.decode(layer, q.cuda(), o, B, scale)
+        assert c.sess.check() == 0
+        assert H.hswa_last_kernel().endswith("decode_mma_fp8_d128")
+        kc, ks, vc, vs = c.host[layer]
+        oracle.append_kv_fp8(kc, ks, vc, vs, kn.float().numpy(), vn.float().numpy(), slots)
+        # the library's quantized rows and scales, bit for bit
+        assert np.array_equal(c.sess.k[layer].cpu().numpy(), kc)
+        assert np.array_equal(c.sess.v[layer].cpu().numpy(), vc)
+        assert np.array_equal(c.sess.ks[layer].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+        assert np.array_equal(c.sess.vs[layer].cpu().numpy().view(np.uint32), vs.view(np.uint32))
+        exp = oracle.attention_fp8(raw_host(q), kc, ks, vc, vs, c.table(layer), np.arange(B),
+                                   c.ora.seq_len[:B] - 1, 0 if kind == FULL else W, scale)
+        got = o.float().cpu().numpy()
+        assert np.isfinite(got).all()
+        err = float(np.abs(got - exp).max())
+        assert err <= 2e-2, (layer, err)
+
+
+@pytest.mark.gpu
+def test_fp8_unsupported_calls_say_so():
+    c = Fp8Case([100], seed=72)
+    with pytest.raises(H.HswaError) as e:
+        q = torch.zeros(1, HQ, D, dtype=torch.bfloat16, device="cuda")
+        c.sess.prefill(0, q, q, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                       torch.tensor([0, 1], dtype=torch.int32, device="cuda"), 1, 1, 0.1)
+    assert e.value.status == H.HSWA_ERR_UNSUPPORTED
