@@ -216,6 +216,47 @@ def measure_decode_fp8(steps, warmup):
     return out
 
 
+def measure_decode_multi(reps, token_counts=(1, 2, 4, 8)):
+    """Multi-token decode (n_tok query tokens per sequence at positions
+    L - n_tok .. L - 1) over the decode-batch pools: one step is the Full and
+    the SWA layer of hswa_decode_multi, events around each layer. Returns per
+    n_tok the step time, query tokens/s and the Full layer's GB/s (KV bytes
+    read once, q and o of every token)."""
+    import torch
+    w = wl.decode_batch()
+    bench = DecodeBatch(w, 8, hold=max(token_counts))
+    sess, B, es = bench.sess, bench.B, KV_ROW[w.dtype]
+    lens = bench.lens()
+    kv = decode_bytes(w, lens)
+    out = {}
+    for T in token_counts:
+        q = [wl.normal((B * T, w.n_q_heads, w.head_dim), 700 + 10 * T + i, w.dtype, "cuda") for i in range(2)]
+        o = [torch.empty_like(x) for x in q]
+        sess.workspace(B, T)
+        ev = []
+        with torch.cuda.stream(bench.stream):
+            for r in range(reps + 3):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record(bench.stream)
+                sess.decode_multi(0, q[0], o[0], B, T, bench.scale)
+                e[1].record(bench.stream)
+                sess.decode_multi(1, q[1], o[1], B, T, bench.scale)
+                e[2].record(bench.stream)
+                if r >= 3:
+                    ev.append(e)
+        bench.stream.synchronize()
+        assert sess.check() == 0
+        full_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
+        step_ms = float(np.mean([a.elapsed_time(c) for a, _, c in ev]))
+        full_bytes = kv["full_kv"] + 2 * B * T * w.n_q_heads * w.head_dim * es
+        out[T] = {"step_ms": step_ms, "full_layer_ms": full_ms, "tokens_per_s": B * T / (step_ms / 1e3),
+                  "full_layer_gbs": full_bytes / (full_ms / 1e3) / 1e9}
+    bench.finish()
+    del bench
+    torch.cuda.empty_cache()
+    return out
+
+
 def prefill_flops(w, prefix, chunk):
     """Valid (query, key) pairs x 4 d Hq for a Full and an SWA layer."""
     full = sum(c * p + c * (c + 1) // 2 for p, c in zip(prefix, chunk))
@@ -228,7 +269,7 @@ class DecodeBatch:
     """The decode-batch workload on the GPU through the C ABI (bf16 pools, or
     FP8 E4M3 pools with per-token-head scales when fp8=True)."""
 
-    def __init__(self, w, extra_steps, fp8=False):
+    def __init__(self, w, extra_steps, fp8=False, hold=0):
         import torch
         import hybrid_sliding_window_dual_gb300 as H
         from hybrid_sliding_window_dual_gb300.session import DualPoolSession
@@ -245,10 +286,14 @@ class DecodeBatch:
         self.stream = torch.cuda.Stream()
         self.sess = DualPoolSession(cfg, [wl.KIND_FULL, wl.KIND_SWA], wl.permutation(full_pages, w.seed),
                                     wl.permutation(swa_pages, w.seed + 1), stream=self.stream, init="empty")
+        # the last `hold` tokens are reserved after the last release (the
+        # draft tokens of a multi-token step keep the window of the first)
         for s, L in enumerate(w.cached):
-            for start in range(0, L, 4096):
-                self.sess.reserve([s], [min(4096, L - start)])
+            for start in range(0, L - hold, 4096):
+                self.sess.reserve([s], [min(4096, L - hold - start)])
                 self.sess.release([s])
+            if hold:
+                self.sess.reserve([s], [hold])
         with torch.cuda.stream(self.stream):
             for i in range(2):
                 for t, seed in ((self.sess.k[i], 10 + i), (self.sess.v[i], 20 + i)):
@@ -861,6 +906,20 @@ def run_decode(args, world, rank, local):
             "full_layer_gbs": round(f8["full_layer_gbs"], 1), "full_layer_ms": round(f8["full_layer_ms"], 4),
             "kernel": "decode_mma_fp8_d128"}
         bench = None
+    if not args.no_multi:
+        del bench
+        torch.cuda.empty_cache()
+        mt = measure_decode_multi(50)
+        base = mt[1]["step_ms"]
+        line["multi_token_decode"] = {
+            "workload": "decode_batch, n_tok query tokens per sequence (MTP / speculative verification), "
+                        "Full + SWA layer per step, no append",
+            "kernel": "decode_mma_bf16_d128<n_tok>",
+            "by_n_tok": {str(T): {"step_ms": round(v["step_ms"], 4), "tokens_per_s": round(v["tokens_per_s"], 1),
+                                  "full_layer_gbs": round(v["full_layer_gbs"], 1),
+                                  "frac": round(v["full_layer_gbs"] / hbm, 4),
+                                  "time_vs_1": round(v["step_ms"] / base, 3)} for T, v in mt.items()}}
+        bench = None
     if not args.no_prefill:
         del bench
         torch.cuda.empty_cache()
@@ -1144,6 +1203,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-multi", action="store_true")
     ap.add_argument("--no-hybrid70", action="store_true")
     ap.add_argument("--no-transfer", action="store_true")
     ap.add_argument("--hybrid-steps", type=int, default=5)

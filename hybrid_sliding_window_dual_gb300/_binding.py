@@ -28,6 +28,7 @@ HSWA_KIND_SWA = 1
 HSWA_DTYPE_F32 = 0
 HSWA_DTYPE_BF16 = 1
 HSWA_DTYPE_FP8_E4M3 = 2
+HSWA_DECODE_MAX_TOKENS = 8
 
 
 class HswaError(RuntimeError):
@@ -72,6 +73,9 @@ _SIG = {
     "hswa_decode_append": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_float, _P,
                                 ctypes.c_size_t, _P]),
     "hswa_decode_noalloc": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _I, ctypes.c_float, _P]),
+    "hswa_decode_multi_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
+    "hswa_decode_multi": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _I, _I, ctypes.c_float, _P,
+                               ctypes.c_size_t, _P]),
     "hswa_prefill_chunk": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I, _I,
                                 ctypes.c_float, _P]),
     "hswa_swa_gather": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
@@ -225,6 +229,16 @@ def hswa_decode_append(pool, layer: Layer, q, k_new, v_new, d_slots, o, d_bt, d_
     _check(lib.hswa_decode_append(pool, ctypes.byref(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(d_slots),
                                   _ptr(o), _ptr(d_bt), _ptr(d_seq_len), int(n_seqs), float(scale), _ptr(ws),
                                   int(ws_bytes), _stream(stream)), "hswa_decode_append")
+
+
+def hswa_decode_multi_workspace_size(pool, n_seqs, n_tok):
+    return int(lib.hswa_decode_multi_workspace_size(pool, int(n_seqs), int(n_tok)))
+
+
+def hswa_decode_multi(pool, layer: Layer, q, o, d_bt, d_seq_len, n_seqs, n_tok, scale, ws, ws_bytes, stream=None):
+    _check(lib.hswa_decode_multi(pool, ctypes.byref(layer), _ptr(q), _ptr(o), _ptr(d_bt), _ptr(d_seq_len),
+                                 int(n_seqs), int(n_tok), float(scale), _ptr(ws), int(ws_bytes), _stream(stream)),
+           "hswa_decode_multi")
 
 
 def hswa_decode_noalloc(pool, layer: Layer, q, o, d_bt, d_seq_len, n_seqs, scale, stream=None):

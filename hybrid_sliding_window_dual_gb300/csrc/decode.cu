@@ -45,21 +45,28 @@ constexpr uint32_t kQBytes = kG * kD * 2;
 enum : int32_t { kFirst = 1, kLast = 2, kDirect = 4, kSkip = 8 };
 
 struct StageDesc {
-    int32_t seq, kvh, lo, hi, flags, slot, pad0, pad1;
+    int32_t seq, kvh, lo, hi, flags, slot;
+    int32_t key0;  // absolute position of the page's first key
+    int32_t len;   // keys of the sequence (its last query sits at len - 1)
 };
 
-struct DecodeSmem {
-    static constexpr int kStages = ::hswa::kStages;
+// kTok query tokens per sequence share every streamed page (one consumer
+// warp each): 1 for plain decode, up to 4 for multi-token decode.
+template <int kTok_>
+struct DecodeSmemT {
+    static constexpr int kTok = kTok_;
+    static constexpr int kStages = kTok_ <= 2 ? ::hswa::kStages : 2;
     uint8_t k[kStages][kPageHeadBytes];
     uint8_t v[kStages][kPageHeadBytes];
-    uint8_t q[kStages][kQBytes];
+    uint8_t q[kStages][kTok * kQBytes];
     StageDesc desc[kStages];
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int32_t abort;
 };
 
-constexpr size_t kDecodeSmemBytes = sizeof(DecodeSmem) + 1024;  // + alignment slack
+template <int kTok>
+constexpr size_t decode_smem_bytes() { return sizeof(DecodeSmemT<kTok>) + 1024; }  // + alignment slack
 
 // FP8 pools: a stage holds one page of one kv head as E4M3 codes, K as
 // [64 keys][128 B] (128-byte swizzle) and V transposed as [128 d][64 B]
@@ -110,21 +117,23 @@ struct DecodeArgs {
     const __nv_bfloat16 *k_new, *v_new;
     int64_t pool_slots;
     int32_t n_seqs, bt_stride, hkv, hq, window, num_pages;
+    int32_t n_tok;  // query tokens per sequence (multi-token decode), 1 otherwise
     float scale_log2;
     int *err;
 };
 
-// Keys [lo, hi) a decode query of a sequence with L keys attends.
-__device__ __forceinline__ void key_range(int32_t L, int32_t window, int32_t &lo, int32_t &hi) {
+// Keys [lo, hi) that the last n_tok query tokens of a sequence with L keys
+// attend together (positions L - n_tok .. L - 1; W keys each for SWA).
+__device__ __forceinline__ void key_range(int32_t L, int32_t window, int32_t n_tok, int32_t &lo, int32_t &hi) {
     hi = L;
-    lo = (window > 0 && L - window > 0) ? L - window : 0;
+    lo = (window > 0 && L - n_tok + 1 - window > 0) ? L - n_tok + 1 - window : 0;
 }
 
 // Per-sequence descriptors: the first unit of the sequence (prefix sum of
 // units(s) = Hkv * pages touched by the key range [lo, hi)), lo, hi, units.
 // desc[n].x is the total number of units.
 __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int32_t hkv, int32_t page,
-                            int32_t window, int4 *__restrict__ desc) {
+                            int32_t window, int32_t n_tok, int4 *__restrict__ desc) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -136,7 +145,7 @@ __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int3
         const int32_t i = base + tid;
         int32_t u = 0, lo = 0, hi = 0;
         if (i < n) {
-            key_range(seq_len[i], window, lo, hi);
+            key_range(seq_len[i], window, n_tok, lo, hi);
             if (hi > lo) u = hkv * ((hi - 1) / page - lo / page + 1);
         }
         int32_t x = u;  // inclusive warp scan
@@ -278,6 +287,8 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                     d.lo = lo - key0 > 0 ? lo - key0 : 0;
                     d.hi = hi - key0 < kP ? hi - key0 : kP;
                     d.slot = slot;
+                    d.key0 = key0;
+                    d.len = hi;
                     int32_t flags = (j == 0 ? kFirst : 0) | (j == n - 1 ? kLast : 0) | (direct ? kDirect : 0);
                     const bool valid = page >= 0 && page < a.num_pages;
                     if (!valid) {
@@ -286,7 +297,7 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                     }
                     d.flags = flags;
                     const uint32_t page_bytes = kFP8 ? kK8Bytes + kV8Bytes + 2 * kScaleBytes : 4 * kBoxBytes;
-                    const uint32_t bytes = (valid ? page_bytes : 0) + (j == 0 ? kQBytes : 0);
+                    const uint32_t bytes = (valid ? page_bytes : 0) + (j == 0 ? a.n_tok * kQBytes : 0);
                     if (bytes) {
                         mbar_arrive_expect_tx(&sm.full[stage], bytes);
                         if (valid) {
@@ -305,9 +316,11 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                                 tma_load_2d(sm.v[stage] + kBoxBytes, tv, 64, row, &sm.full[stage]);
                             }
                         }
-                        if (j == 0)
-                            bulk_g2s(sm.q[stage], a.q + ((int64_t)s * a.hq + (int64_t)g * kG) * kD, kQBytes,
-                                     &sm.full[stage]);
+                        if (j == 0)  // the 8 query rows of each token of this kv head
+                            for (int w = 0; w < a.n_tok; ++w)
+                                bulk_g2s(sm.q[stage] + w * kQBytes,
+                                         a.q + (((int64_t)s * a.n_tok + w) * a.hq + (int64_t)g * kG) * kD, kQBytes,
+                                         &sm.full[stage]);
                     } else {
                         mbar_arrive(&sm.full[stage]);
                     }
@@ -330,7 +343,9 @@ drain:
             if (issued[i]) mbar_wait(&sm.full[i], issued_parity[i], a.err);
 }
 
-__device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0, int64_t u1) {
+template <int kTok>
+__device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int64_t u0, int64_t u1, int w) {
+    constexpr int kStages = DecodeSmemT<kTok>::kStages;
     const int lane = threadIdx.x & 31;
     const int gr = lane >> 2;  // fragment row group
     const int qd = lane & 3;   // fragment column pair
@@ -350,7 +365,7 @@ __device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0,
         }
         const StageDesc d = sm.desc[stage];
         if (d.flags & kFirst) {
-            const uint32_t *qs = reinterpret_cast<const uint32_t *>(sm.q[stage]);
+            const uint32_t *qs = reinterpret_cast<const uint32_t *>(sm.q[stage] + w * kQBytes);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 qf[ks][0] = qs[(gr * kD + ks * 16 + 2 * qd) >> 1];
@@ -376,12 +391,20 @@ __device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0,
                     mma_bf16_16816(sacc[kt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
                 }
             }
-            // scale to log2 units and mask keys outside [lo, hi)
+            // scale to log2 units and mask the keys this token does not see:
+            // its position is t = len - n_tok + w; keys (key0 + r) <= t and,
+            // for SWA, > t - W, inside the page's part of the range [lo, hi)
+            int32_t r_lo = d.lo, r_hi = d.hi;  // one token: the stage's range is its own
+            if constexpr (kTok > 1) {
+                const int32_t t = d.len - a.n_tok + w;
+                r_hi = min(d.hi, t - d.key0 + 1);
+                if (a.window > 0) r_lo = max(d.lo, t - a.window + 1 - d.key0);
+            }
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
                 const int r0 = kt * 16 + gr, r1 = r0 + 8;
-                const bool v0 = r0 >= d.lo && r0 < d.hi, v1 = r1 >= d.lo && r1 < d.hi;
+                const bool v0 = r0 >= r_lo && r0 < r_hi, v1 = r1 >= r_lo && r1 < r_hi;
                 sacc[kt][0] = v0 ? sacc[kt][0] * a.scale_log2 : -INFINITY;
                 sacc[kt][1] = v0 ? sacc[kt][1] * a.scale_log2 : -INFINITY;
                 sacc[kt][2] = v1 ? sacc[kt][2] * a.scale_log2 : -INFINITY;
@@ -394,17 +417,27 @@ __device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0,
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
             }
+            // with several tokens a page can hold no key that a token sees
+            // (n = -inf): then nothing is kept and P stays 0
             const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-            // a stage holds at least one valid key, so n0 and n1 are finite
-            const float al0 = fast_exp2(m0 - n0), al1 = fast_exp2(m1 - n1);
+            float b0 = n0, b1 = n1, al0, al1;
+            if constexpr (kTok > 1) {
+                b0 = n0 == -INFINITY ? 0.f : n0;
+                b1 = n1 == -INFINITY ? 0.f : n1;
+                al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
+                al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
+            } else {  // a stage holds at least one key of the range: n0, n1 finite
+                al0 = fast_exp2(m0 - n0);
+                al1 = fast_exp2(m1 - n1);
+            }
             m0 = n0;
             m1 = n1;
             uint32_t pb[4][2];
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
-                const float p0 = fast_exp2(sacc[kt][0] - n0), p1 = fast_exp2(sacc[kt][1] - n1);
-                const float p2 = fast_exp2(sacc[kt][2] - n0), p3 = fast_exp2(sacc[kt][3] - n1);
+                const float p0 = fast_exp2(sacc[kt][0] - b0), p1 = fast_exp2(sacc[kt][1] - b1);
+                const float p2 = fast_exp2(sacc[kt][2] - b0), p3 = fast_exp2(sacc[kt][3] - b1);
                 const uint32_t x0 = pack_bf16(p0, p1), x1 = pack_bf16(p2, p3);
                 // sum what the MMA will see (the bf16-rounded weights)
                 const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162 *>(&x0);
@@ -449,7 +482,8 @@ __device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0,
             const int h0 = 2 * qd, h1 = 2 * qd + 1;
             if (d.flags & kDirect) {
                 const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
-                __nv_bfloat16 *o0 = a.o + ((int64_t)d.seq * a.hq + (int64_t)d.kvh * kG + h0) * kD;
+                __nv_bfloat16 *o0 =
+                    a.o + (((int64_t)d.seq * a.n_tok + w) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
                 __nv_bfloat16 *o1 = o0 + kD;
 #pragma unroll
                 for (int dt = 0; dt < 8; ++dt) {
@@ -459,7 +493,7 @@ __device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0,
                     o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][3] * i1);
                 }
             } else {
-                Partial &p = a.part[(int64_t)blockIdx.x * 2 + d.slot];
+                Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + w];
                 if (gr == 0) {
                     p.m[h0] = m0;
                     p.m[h1] = m1;
@@ -479,14 +513,17 @@ __device__ void decode_consumer(DecodeSmem &sm, const DecodeArgs &a, int64_t u0,
     }
 }
 
-__global__ void __launch_bounds__(64) decode_mma_bf16_d128(const __grid_constant__ CUtensorMap tk,
-                                                           const __grid_constant__ CUtensorMap tv, DecodeArgs a) {
+template <int kTok>
+__global__ void __launch_bounds__(32 * (kTok + 1)) decode_mma_bf16_d128(const __grid_constant__ CUtensorMap tk,
+                                                                      const __grid_constant__ CUtensorMap tv,
+                                                                      DecodeArgs a) {
+    using Smem = DecodeSmemT<kTok>;
     extern __shared__ uint8_t raw[];
-    DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < Smem::kStages; ++i) {
             mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], 1);
+            mbar_init(&sm.empty[i], a.n_tok);
         }
         sm.abort = 0;
         fence_barrier_init();
@@ -497,10 +534,11 @@ __global__ void __launch_bounds__(64) decode_mma_bf16_d128(const __grid_constant
     const int64_t U = a.sdesc[a.n_seqs].x, N = gridDim.x;
     if (U == 0) return;
     const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
-    if (threadIdx.x >= 32)
+    const int warp = threadIdx.x >> 5;
+    if (warp == kTok)
         decode_producer<false>(sm, &tk, &tv, a, u0, u1);
-    else
-        decode_consumer(sm, a, u0, u1);
+    else if (warp < a.n_tok)
+        decode_consumer<kTok>(sm, a, u0, u1, warp);
 }
 
 // ---------------------------------------------------------- FP8 decode
@@ -777,14 +815,14 @@ __global__ void __launch_bounds__(32 * (kConsumers8 + 1)) decode_mma_fp8_d128(co
 // Merge the partial records of segments split between CTAs; write zeros
 // for sequences without keys.
 __global__ void __launch_bounds__(256) decode_combine(DecodeArgs a, int32_t n_ctas) {
-    const int32_t s = blockIdx.y, g = blockIdx.x;
+    const int32_t s = blockIdx.y / a.n_tok, w = blockIdx.y % a.n_tok, g = blockIdx.x;
     pdl_wait();
     pdl_launch_dependents();
     const int64_t U = a.sdesc[a.n_seqs].x, N = n_ctas;
     const int4 d = a.sdesc[s];
     const int32_t units = d.w;
     const int h = threadIdx.x >> 5, d0 = (threadIdx.x & 31) * 4;
-    __nv_bfloat16 *out = a.o + ((int64_t)s * a.hq + (int64_t)g * kG + h) * kD + d0;
+    __nv_bfloat16 *out = a.o + (((int64_t)s * a.n_tok + w) * a.hq + (int64_t)g * kG + h) * kD + d0;
     if (units == 0) {
         for (int i = 0; i < 4; ++i) out[i] = __float2bfloat16_rn(0.f);
         return;
@@ -797,16 +835,16 @@ __global__ void __launch_bounds__(256) decode_combine(DecodeArgs a, int32_t n_ct
     for (int64_t c = c_lo; c <= c_hi; ++c) {
         if (cta_start(c, U, N) == cta_start(c + 1, U, N)) continue;
         const int slot = (c == c_lo && cta_start(c, U, N) < lo) ? 1 : 0;
-        M = fmaxf(M, a.part[c * 2 + slot].m[h]);
+        M = fmaxf(M, a.part[(c * 2 + slot) * a.n_tok + w].m[h]);
     }
     float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int64_t c = c_lo; c <= c_hi; ++c) {
         if (cta_start(c, U, N) == cta_start(c + 1, U, N)) continue;
         const int slot = (c == c_lo && cta_start(c, U, N) < lo) ? 1 : 0;
-        const Partial &p = a.part[c * 2 + slot];
-        const float w = p.m[h] == -INFINITY ? 0.f : fast_exp2(p.m[h] - M);
-        L += w * p.l[h];
-        for (int i = 0; i < 4; ++i) acc[i] += w * p.o[h][d0 + i];
+        const Partial &p = a.part[(c * 2 + slot) * a.n_tok + w];
+        const float wt = p.m[h] == -INFINITY ? 0.f : fast_exp2(p.m[h] - M);
+        L += wt * p.l[h];
+        for (int i = 0; i < 4; ++i) acc[i] += wt * p.o[h][d0 + i];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int i = 0; i < 4; ++i) out[i] = __float2bfloat16_rn(acc[i] * inv);
@@ -829,7 +867,8 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return
 }  // namespace
 
 // One warp per (query row, query head): query position t, keys [lo, t].
-// mode 0: decode, n_rows sequences (row i = sequence i, t = L_i - 1);
+// mode 0: decode, n_rows = sequences x n_tok (row i is token i mod n_tok of
+//         sequence i / n_tok, t = L - n_tok + i mod n_tok);
 // mode 1: prefill, n_rows = max rows per sequence; row r < n_s of sequence s
 //         is q row q_start[s] + r at t = prefix[s] + r.
 template <typename T, int MAXE>
@@ -838,7 +877,8 @@ __global__ void attention_generic(const T *__restrict__ q, T *__restrict__ o, co
                                   const int32_t *__restrict__ seq_len, const int32_t *__restrict__ prefix,
                                   const int32_t *__restrict__ q_start, int32_t n_rows, int32_t n_seqs,
                                   int32_t bt_stride, int32_t hq, int32_t hkv, int32_t d, int32_t page,
-                                  int32_t window, int32_t num_pages, float scale, int mode, int *err) {
+                                  int32_t window, int32_t num_pages, float scale, int mode, int32_t n_tok,
+                                  int *err) {
     const int lane = threadIdx.x & 31;
     const int64_t wid = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t per_seq = mode == 0 ? hq : (int64_t)n_rows * hq;
@@ -847,8 +887,9 @@ __global__ void attention_generic(const T *__restrict__ q, T *__restrict__ o, co
     const int32_t g = (int32_t)((int64_t)h * hkv / hq);
     int32_t s, t, row;
     if (mode == 0) {
-        s = row = (int32_t)(wid / hq);
-        t = seq_len[s] - 1;
+        row = (int32_t)(wid / hq);
+        s = row / n_tok;
+        t = seq_len[s] - n_tok + row % n_tok;
     } else {
         s = (int32_t)(wid / per_seq);
         const int32_t r = (int32_t)((wid / hq) % n_rows);
@@ -906,7 +947,7 @@ __global__ void attention_generic(const T *__restrict__ q, T *__restrict__ o, co
 int launch_attention_generic(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                              const int32_t *bt, const int32_t *seq_len, const int32_t *prefix,
                              const int32_t *q_start, int32_t n_rows, int32_t n_seqs, float scale, int mode,
-                             cudaStream_t st) {
+                             cudaStream_t st, int32_t n_tok) {
     const hswa_config &c = pool->cfg;
     if (c.head_dim > 256 || c.dtype == HSWA_DTYPE_FP8_E4M3) return HSWA_ERR_UNSUPPORTED;
     if (n_rows == 0) return HSWA_OK;
@@ -922,14 +963,14 @@ int launch_attention_generic(const hswa_pool *pool, const hswa_layer *layer, con
         attention_generic<float, 8><<<(int)grid, block, 0, st>>>(
             (const float *)q, (float *)o, (const float *)layer->k_pool, (const float *)layer->v_pool, bt, seq_len,
             prefix, q_start, n_rows, n_seqs, c.max_pages_per_seq, c.n_q_heads, c.n_kv_heads, c.head_dim,
-            c.page_size, window, num_pages, scale, mode, err);
+            c.page_size, window, num_pages, scale, mode, n_tok, err);
     } else {
         set_last_kernel(mode == 0 ? "decode_generic_bf16" : "prefill_generic_bf16");
         attention_generic<__nv_bfloat16, 8><<<(int)grid, block, 0, st>>>(
             (const __nv_bfloat16 *)q, (__nv_bfloat16 *)o, (const __nv_bfloat16 *)layer->k_pool,
             (const __nv_bfloat16 *)layer->v_pool, bt, seq_len, prefix, q_start, n_rows, n_seqs,
             c.max_pages_per_seq, c.n_q_heads, c.n_kv_heads, c.head_dim, c.page_size, window, num_pages, scale,
-            mode, err);
+            mode, n_tok, err);
     }
     return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
 }
@@ -967,19 +1008,35 @@ bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *
            ((uintptr_t)layer->k_pool & 15) == 0 && ((uintptr_t)layer->v_pool & 15) == 0;
 }
 
-int decode_ctas_per_sm() {
+template <int kTok>
+int decode_ctas_per_sm_t() {
     static int v = -1;
     if (v < 0) {
-        if (cudaFuncSetAttribute(decode_mma_bf16_d128, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDecodeSmemBytes) != cudaSuccess)
+        constexpr size_t smem = decode_smem_bytes<kTok>();
+        if (cudaFuncSetAttribute(decode_mma_bf16_d128<kTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128, 64, kDecodeSmemBytes) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128<kTok>, 32 * (kTok + 1), smem) !=
             cudaSuccess)
             n = 1;
         v = std::max(1, n);
     }
     return v;
+}
+
+int decode_ctas_per_sm() { return decode_ctas_per_sm_t<1>(); }
+
+// Kernel instantiation (consumer warps) serving n_tok query tokens.
+int tok_variant(int n_tok) { return n_tok <= 2 ? n_tok : n_tok <= 4 ? 4 : 8; }
+
+int decode_ctas_per_sm_for(int n_tok) {
+    switch (tok_variant(n_tok)) {
+    case 1: return decode_ctas_per_sm_t<1>();
+    case 2: return decode_ctas_per_sm_t<2>();
+    case 4: return decode_ctas_per_sm_t<4>();
+    default: return decode_ctas_per_sm_t<8>();
+    }
 }
 
 constexpr int kMaxCtasPerSm = 4;
@@ -991,13 +1048,17 @@ size_t desc_bytes(int n_seqs) { return ((size_t)(n_seqs + 1) * sizeof(int4) + 25
 
 using namespace hswa;
 
-extern "C" size_t hswa_decode_workspace_size(const hswa_pool *pool, int n_seqs) {
-    if (!pool || n_seqs < 0) return 0;
+extern "C" size_t hswa_decode_multi_workspace_size(const hswa_pool *pool, int n_seqs, int n_tok) {
+    if (!pool || n_seqs < 0 || n_tok < 1 || n_tok > HSWA_DECODE_MAX_TOKENS) return 0;
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 192;  // no device visible: size for the largest part
-    return desc_bytes(n_seqs) + (size_t)sms * kMaxCtasPerSm * 2 * sizeof(Partial);
+    return desc_bytes(n_seqs) + (size_t)sms * kMaxCtasPerSm * 2 * n_tok * sizeof(Partial);
+}
+
+extern "C" size_t hswa_decode_workspace_size(const hswa_pool *pool, int n_seqs) {
+    return hswa_decode_multi_workspace_size(pool, n_seqs, 1);
 }
 
 namespace hswa {
@@ -1026,6 +1087,7 @@ int fill_args(DecodeArgs &a, const hswa_pool *pool, const hswa_layer *layer, con
     a.hq = c.n_q_heads;
     a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
     a.num_pages = num_pages;
+    a.n_tok = 1;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = error_word();
     return num_pages;
@@ -1058,7 +1120,7 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
                       CU_TENSOR_MAP_SWIZZLE_64B))
         return HSWA_ERR_CUDA;
     set_last_kernel(slots ? "append_kv_fp8+decode_mma_fp8_d128" : "decode_mma_fp8_d128");
-    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window,
+    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, 1,
                    static_cast<int4 *>(ws)) != cudaSuccess ||
         launch_pdl(decode_mma_fp8_d128, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)), kDecodeSmem8Bytes, st, tk, tv,
                    a) !=
@@ -1068,11 +1130,20 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
     return HSWA_OK;
 }
 
-// Decode with an optional fused append (slots / k_new / v_new non-null).
+template <int kTok>
+cudaError_t launch_decode_kernel(int n_ctas, cudaStream_t st, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const DecodeArgs &a) {
+    return launch_pdl(decode_mma_bf16_d128<kTok>, dim3(n_ctas), dim3(32 * (kTok + 1)), decode_smem_bytes<kTok>(), st,
+                      tk, tv, a);
+}
+
+// Decode of n_tok query tokens per sequence, with an optional fused append
+// of one new token (slots / k_new / v_new non-null, n_tok == 1 only).
 int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o, const int32_t *d_bt,
-                const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes, const int32_t *slots,
-                const void *k_new, const void *v_new, hswa_stream_t stream) {
-    if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs ||
+                const int32_t *d_seq_len, int n_seqs, int n_tok, float scale, void *ws, size_t ws_bytes,
+                const int32_t *slots, const void *k_new, const void *v_new, hswa_stream_t stream) {
+    if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs || n_tok < 1 ||
+        n_tok > HSWA_DECODE_MAX_TOKENS || (slots && n_tok != 1) ||
         (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA) ||
         (layer->kind == HSWA_KIND_SWA && layer->window <= 0))
         return HSWA_ERR_INVALID_ARG;
@@ -1080,27 +1151,36 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     if (!q || !o || !d_bt || !d_seq_len || !layer->k_pool || !layer->v_pool) return HSWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool fused = slots != nullptr;
-    if (pool->cfg.dtype == HSWA_DTYPE_FP8_E4M3)
+    if (pool->cfg.dtype == HSWA_DTYPE_FP8_E4M3) {
+        if (n_tok != 1) return HSWA_ERR_UNSUPPORTED;
         return decode_fp8(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, slots, k_new, v_new,
                           stream);
+    }
     if (!decode_fast_ok(pool, layer, q, o) ||
         (fused && (((uintptr_t)k_new & 15) || ((uintptr_t)v_new & 15)))) {
         if (fused) {
             const int rc = hswa_append_kv(pool, layer, k_new, v_new, slots, n_seqs, stream);
             if (rc != HSWA_OK) return rc;
         }
-        return launch_attention_generic(pool, layer, q, o, d_bt, d_seq_len, nullptr, nullptr, n_seqs, n_seqs, scale,
-                                        0, st);
+        return launch_attention_generic(pool, layer, q, o, d_bt, d_seq_len, nullptr, nullptr, n_seqs * n_tok,
+                                        n_seqs, scale, 0, st, n_tok);
     }
     const hswa_config &c = pool->cfg;
+    if ((int64_t)n_seqs * n_tok > 65535) return HSWA_ERR_UNSUPPORTED;  // rows of the combine grid
     const int sms = sm_count();
     if (sms <= 0) return HSWA_ERR_CUDA;
-    const int per_sm = decode_ctas_per_sm();
+    const int per_sm = decode_ctas_per_sm_for(n_tok);
     if (per_sm <= 0) return HSWA_ERR_CUDA;
     const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
-    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < desc_bytes(n_seqs) + (size_t)n_ctas * 2 * sizeof(Partial))
+    if (!ws || ((uintptr_t)ws & 255) ||
+        ws_bytes < desc_bytes(n_seqs) + (size_t)n_ctas * 2 * n_tok * sizeof(Partial))
         return HSWA_ERR_INVALID_ARG;
-    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+    DecodeArgs a;
+    const int32_t num_pages = fill_args(a, pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws);
+    a.slots = slots;
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.n_tok = n_tok;
     CUtensorMap tk, tv;
     const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
     if (!make_tmap_2d(&tk, layer->k_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -1108,34 +1188,21 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
         !make_tmap_2d(&tv, layer->v_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return HSWA_ERR_CUDA;
-    DecodeArgs a;
-    a.q = static_cast<const __nv_bfloat16 *>(q);
-    a.o = static_cast<__nv_bfloat16 *>(o);
-    a.bt = d_bt;
-    a.seq_len = d_seq_len;
-    a.sdesc = static_cast<const int4 *>(ws);
-    a.k_pool = static_cast<__nv_bfloat16 *>(layer->k_pool);
-    a.v_pool = static_cast<__nv_bfloat16 *>(layer->v_pool);
-    a.part = reinterpret_cast<Partial *>(static_cast<uint8_t *>(ws) + desc_bytes(n_seqs));
-    a.slots = slots;
-    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
-    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-    a.pool_slots = (int64_t)num_pages * kP;
-    a.n_seqs = n_seqs;
-    a.bt_stride = c.max_pages_per_seq;
-    a.hkv = c.n_kv_heads;
-    a.hq = c.n_q_heads;
-    a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
-    a.num_pages = num_pages;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    a.err = error_word();
     set_last_kernel(fused ? "decode_mma_bf16_d128+append" : "decode_mma_bf16_d128");
     // three launches chained with programmatic dependent launch: each one
     // is scheduled while its predecessor finishes and waits for it on entry
-    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window,
-                   static_cast<int4 *>(ws)) != cudaSuccess ||
-        launch_pdl(decode_mma_bf16_d128, dim3(n_ctas), dim3(64), kDecodeSmemBytes, st, tk, tv, a) != cudaSuccess ||
-        launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs), dim3(256), 0, st, a, n_ctas) != cudaSuccess)
+    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok,
+                   static_cast<int4 *>(ws)) != cudaSuccess)
+        return HSWA_ERR_CUDA;
+    cudaError_t e;
+    switch (tok_variant(n_tok)) {
+    case 1: e = launch_decode_kernel<1>(n_ctas, st, tk, tv, a); break;
+    case 2: e = launch_decode_kernel<2>(n_ctas, st, tk, tv, a); break;
+    case 4: e = launch_decode_kernel<4>(n_ctas, st, tk, tv, a); break;
+    default: e = launch_decode_kernel<8>(n_ctas, st, tk, tv, a); break;
+    }
+    if (e != cudaSuccess ||
+        launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * n_tok), dim3(256), 0, st, a, n_ctas) != cudaSuccess)
         return HSWA_ERR_CUDA;
     return HSWA_OK;
 }
@@ -1146,7 +1213,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
 extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                            const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale, void *ws,
                            size_t ws_bytes, hswa_stream_t stream) {
-    return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, nullptr, nullptr, nullptr,
+    return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, 1, scale, ws, ws_bytes, nullptr, nullptr, nullptr,
                        stream);
 }
 
@@ -1155,8 +1222,15 @@ extern "C" int hswa_decode_append(const hswa_pool *pool, const hswa_layer *layer
                                   const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes,
                                   hswa_stream_t stream) {
     if (!k_new || !v_new || !d_slots) return HSWA_ERR_INVALID_ARG;
-    return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, d_slots, k_new, v_new,
+    return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, 1, scale, ws, ws_bytes, d_slots, k_new, v_new,
                        stream);
+}
+
+extern "C" int hswa_decode_multi(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                                 const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, int n_tok, float scale,
+                                 void *ws, size_t ws_bytes, hswa_stream_t stream) {
+    return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, n_tok, scale, ws, ws_bytes, nullptr, nullptr,
+                       nullptr, stream);
 }
 
 // ---------------------------------------------------- no-allocation decode

@@ -103,8 +103,8 @@ class DualPoolSession:
         return self.d_full_bt if self.kinds[layer] == B.HSWA_KIND_FULL else self.d_swa_bt
 
     # ------------------------------------------------------------ device
-    def workspace(self, n_seqs):
-        need = B.hswa_decode_workspace_size(self.pool, n_seqs)
+    def workspace(self, n_seqs, n_tok=1):
+        need = B.hswa_decode_multi_workspace_size(self.pool, n_seqs, n_tok)
         if self.ws is None or self.ws.numel() < need:
             self.ws = torch.empty(need, dtype=torch.uint8, device=self.device)
         return self.ws
@@ -121,6 +121,12 @@ class DualPoolSession:
         ws = self.workspace(n_seqs)
         B.hswa_decode_append(self.pool, self.layers[layer], q, k_new, v_new, d_slots, o, self.bt(layer),
                              self.d_seq_len, n_seqs, scale, ws, ws.numel(), self.stream)
+
+    def decode_multi(self, layer, q, o, n_seqs, n_tok, scale):
+        """n_tok query tokens per sequence (q, o: [n_seqs * n_tok, Hq, d])."""
+        ws = self.workspace(n_seqs, n_tok)
+        B.hswa_decode_multi(self.pool, self.layers[layer], q, o, self.bt(layer), self.d_seq_len, n_seqs, n_tok,
+                            scale, ws, ws.numel(), self.stream)
 
     def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale):
         B.hswa_prefill_chunk(self.pool, self.layers[layer], q, o, self.bt(layer), d_prefix_len, d_q_start,

@@ -228,6 +228,34 @@ int hswa_decode_append(const hswa_pool *pool, const hswa_layer *layer, const voi
                        const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes,
                        hswa_stream_t stream);
 
+/* Most query tokens per sequence hswa_decode_multi takes. */
+#define HSWA_DECODE_MAX_TOKENS 8
+
+/* Bytes of workspace hswa_decode_multi needs for n_seqs sequences of n_tok
+ * query tokens each (0 for an n_tok outside [1, HSWA_DECODE_MAX_TOKENS]). */
+size_t hswa_decode_multi_workspace_size(const hswa_pool *pool, int n_seqs, int n_tok);
+
+/* Decode of n_tok query tokens per sequence in one pass over the KV pages:
+ * the verification step of multi-token prediction or speculative decoding
+ * ("MiMo-V2.5 Series Inference Full-Link Optimization", Sec. 5.2 MTP
+ * Optimization: 3-layer MTP decode; "Following the Bottleneck: Optimizing
+ * MiniMax M3 on AMD Instinct MI355X", EAGLE3 adds a second decode loop:
+ * multi-token verification, each flattened query row mapped back to its
+ * request and its speculative position). For sequence i < n_seqs with
+ * L = d_seq_len[i] keys (all n_tok new tokens already appended), query token
+ * w < n_tok sits at position t = L - n_tok + w and attends keys [0, t] for a
+ * Full layer and [max(0, t - W + 1), t] for an SWA layer (causal among the
+ * new tokens). q, o: device [n_seqs][n_tok][Hq][d] in the pool dtype (row
+ * i * n_tok + w). A token with t < 0 gets o = 0. n_tok = 1 is hswa_decode.
+ * ws: device workspace of at least hswa_decode_multi_workspace_size bytes.
+ * The SWA pages must still hold positions from L - n_tok + 1 - W on: release
+ * out-of-window pages before the draft tokens are reserved. Bf16 pools only
+ * for n_tok > 1 (HSWA_ERR_UNSUPPORTED on an FP8 pool); n_tok outside
+ * [1, HSWA_DECODE_MAX_TOKENS] gives HSWA_ERR_INVALID_ARG. */
+int hswa_decode_multi(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                      const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, int n_tok, float scale,
+                      void *ws, size_t ws_bytes, hswa_stream_t stream);
+
 /* One chunked-prefill chunk of attention (Sec. 1.1: chunked prefill is
  * close to compute-bound). Sequence i < n_seqs has d_prefix_len[i] cached
  * tokens and n_i = d_q_start[i+1] - d_q_start[i] new tokens whose K/V are

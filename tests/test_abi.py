@@ -148,4 +148,14 @@ def test_device_calls_validate_before_launching():
         H.hswa_swa_gather(lp, H.Layer(kind=H.HSWA_KIND_FULL, window=128, k_pool=16, v_pool=16),
                           16, 16, 16, 1, 16)
     assert H.hswa_decode_workspace_size(lp, 64) > 0
+    # multi-token decode: the token count is checked first
+    ok_layer = H.Layer(kind=H.HSWA_KIND_FULL, window=0, k_pool=16, v_pool=16)
+    for n_tok in (0, -1, H.HSWA_DECODE_MAX_TOKENS + 1):
+        assert H.hswa_decode_multi_workspace_size(lp, 64, n_tok) == 0
+        with pytest.raises(H.HswaError) as e:
+            H.hswa_decode_multi(lp, ok_layer, 16, 16, 16, 16, 1, n_tok, 1.0, 256, 1 << 20)
+        assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    sizes = [H.hswa_decode_multi_workspace_size(lp, 64, t) for t in range(1, H.HSWA_DECODE_MAX_TOKENS + 1)]
+    assert sizes[0] == H.hswa_decode_workspace_size(lp, 64)
+    assert all(b > a for a, b in zip(sizes, sizes[1:]))
     H.hswa_pool_destroy(lp)

@@ -117,3 +117,13 @@ def test_fp8_unsupported_calls_say_so():
         c.sess.prefill(0, q, q, torch.zeros(1, dtype=torch.int32, device="cuda"),
                        torch.tensor([0, 1], dtype=torch.int32, device="cuda"), 1, 1, 0.1)
     assert e.value.status == H.HSWA_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_fp8_multi_token_decode_is_unsupported():
+    c = Fp8Case([100, 7], seed=73)
+    q = torch.zeros(2 * 2, HQ, D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(H.HswaError) as e:
+        c.sess.decode_multi(0, q, q.clone(), 2, 2, 0.1)
+    assert e.value.status == H.HSWA_ERR_UNSUPPORTED
+    assert c.sess.check() == 0

@@ -1,0 +1,131 @@
+"""Multi-token decode parity: hswa_decode_multi (GPU) against the float64 oracle.
+
+Each case reserves n_tok new tokens per sequence, appends their K/V, and
+runs one decode over all n_tok query tokens of every sequence: token w sits
+at position L - n_tok + w and sees keys up to itself (Full) or the W keys
+ending at itself (SWA). Every output element is compared with the oracle
+evaluated at those positions (bf16: max abs 2e-2, fp32: 1e-5)."""
+import numpy as np
+import pytest
+import torch
+
+import hswa_workloads as wl
+import oracle
+import hybrid_sliding_window_dual_gb300 as H
+from scenario import Scenario, TOL, device_out, max_err, raw_host
+
+FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
+
+
+def run_multi_step(sc, n_tok, seed, samples=None, expect_kernel=None):
+    B = len(sc.cached)
+    samples = list(range(B)) if samples is None else samples
+    full_slots, swa_slots = sc.reserve(range(B), [n_tok] * B)
+    sc.sess.sync()
+    errs = {}
+    for layer, kind in enumerate(sc.kinds):
+        slots = full_slots if kind == FULL else swa_slots
+        kn = sc.gen((B * n_tok, sc.hkv, sc.d), seed + 10 * layer + 1)
+        vn = sc.gen((B * n_tok, sc.hkv, sc.d), seed + 10 * layer + 2)
+        sc.sess.append(layer, sc.to_dev(kn), sc.to_dev(vn), torch.as_tensor(slots, device="cuda"))
+        q = sc.gen((B * n_tok, sc.hq, sc.d), seed + 10 * layer)
+        qd = sc.to_dev(q)
+        o = torch.full_like(qd, float("nan"))
+        sc.sess.decode_multi(layer, qd, o, B, n_tok, sc.scale)
+        assert sc.sess.check() == 0
+        if expect_kernel:
+            assert H.hswa_last_kernel() == expect_kernel
+        snap = sc.snapshot(layer, samples)
+        lens = sc.ora.seq_len[samples]
+        rows = (np.asarray(samples)[:, None] * n_tok + np.arange(n_tok)[None, :]).reshape(-1)
+        q_seq = np.repeat(np.arange(len(samples)), n_tok)
+        q_pos = (lens[:, None] - n_tok + np.arange(n_tok)[None, :]).reshape(-1)
+        exp = oracle.attention(raw_host(q)[rows], snap[0], snap[1], snap[2], q_seq, q_pos, sc.window(layer),
+                               sc.scale)
+        got = device_out(o)[rows]
+        assert np.isfinite(got).all()
+        errs[kind] = max_err(got, exp)
+        assert errs[kind] <= TOL[sc.dtype], (kind, n_tok, errs[kind])
+    return errs
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_tok", [1, 2, 3, 4, 5, 8])
+def test_multi_token_decode_ragged_lengths(n_tok):
+    # lengths around page edges and the window (W = 128, P = 64), one empty
+    # sequence whose first new token sees only itself
+    cached = [0, 1, 61, 62, 63, 64, 125, 126, 127, 128, 129, 191, 700, 3000]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=7, extra_tokens=16)
+    run_multi_step(sc, n_tok, seed=300 + n_tok, expect_kernel="decode_mma_bf16_d128")
+
+
+@pytest.mark.gpu
+def test_multi_token_decode_steps_with_release():
+    """Verification steps of 3 tokens; release before each reserve."""
+    cached = [5, 130, 255, 1000, 2047]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=8, extra_tokens=64)
+    for step in range(12):
+        sc.release(range(len(cached)))
+        sc.sess.sync()
+        run_multi_step(sc, 3, seed=400 + step)
+
+
+@pytest.mark.gpu
+def test_multi_token_one_equals_single_token_decode_bitwise():
+    """n_tok = 1 runs the same kernel as hswa_decode: identical bytes."""
+    cached = [3, 64, 300, 5000]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=9)
+    B = len(cached)
+    full_slots, swa_slots = sc.reserve(range(B), [1] * B)
+    sc.sess.sync()
+    for layer, kind in enumerate(sc.kinds):
+        q = sc.to_dev(sc.gen((B, sc.hq, sc.d), 70 + layer))
+        a = torch.empty_like(q)
+        b = torch.empty_like(q)
+        sc.sess.decode(layer, q, a, B, sc.scale)
+        sc.sess.decode_multi(layer, q, b, B, 1, sc.scale)
+        assert sc.sess.check() == 0
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [(4, 1, 64, 16, wl.DTYPE_F32), (16, 4, 128, 64, wl.DTYPE_BF16)])
+def test_multi_token_generic_path(shape):
+    hq, hkv, d, P, dtype = shape
+    cached = [0, 3, 17, 100, 300]
+    sc = Scenario(hq, hkv, d, P, 40, dtype, cached, seed=11, extra_tokens=16)
+    run_multi_step(sc, 4, seed=500)
+
+
+@pytest.mark.gpu
+def test_multi_token_full_size_batch_sampled():
+    """The decode_batch shape (Hq 64, Hkv 8, d 128, P 64, W 128) with 256
+    sequences of mixed lengths, 4 tokens each; oracle on sampled sequences."""
+    rng = np.random.default_rng(12)
+    cached = list(rng.integers(1, 16384, 256))
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=12, permute=True, chunk=8192)
+    samples = sorted(set(rng.integers(0, 256, 12).tolist()) | {0, 255})
+    run_multi_step(sc, 4, seed=600, samples=samples)
+
+
+@pytest.mark.gpu
+def test_multi_token_rejects_bad_token_counts_and_small_workspace():
+    cached = [10, 20]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=13)
+    q = sc.to_dev(sc.gen((2 * 8, sc.hq, sc.d), 1))
+    o = torch.empty_like(q)
+    ws = sc.sess.workspace(2, 8)
+    for n_tok in (0, H.HSWA_DECODE_MAX_TOKENS + 1):
+        assert H.hswa_decode_multi_workspace_size(sc.sess.pool, 2, n_tok) == 0
+        with pytest.raises(H.HswaError) as e:
+            H.hswa_decode_multi(sc.sess.pool, sc.sess.layers[0], q, o, sc.sess.bt(0), sc.sess.d_seq_len, 2, n_tok,
+                                sc.scale, ws, ws.numel())
+        assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    # 8 tokens with only the bytes a 1-token decode needs
+    small = H.hswa_decode_multi_workspace_size(sc.sess.pool, 2, 1)
+    assert H.hswa_decode_multi_workspace_size(sc.sess.pool, 2, 8) > small
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_decode_multi(sc.sess.pool, sc.sess.layers[0], q, o, sc.sess.bt(0), sc.sess.d_seq_len, 2, 8,
+                            sc.scale, ws, small)
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    assert sc.sess.check() == 0
