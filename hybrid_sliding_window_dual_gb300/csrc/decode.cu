@@ -343,15 +343,20 @@ drain:
             if (issued[i]) mbar_wait(&sm.full[i], issued_parity[i], a.err);
 }
 
-template <int kTok>
-__device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int64_t u0, int64_t u1, int w) {
+// One consumer warp: kTPW query tokens (w0 .. w0 + kTPW - 1) of the stage's
+// (sequence, kv head), 8 query heads each. Every K and V fragment read from
+// shared memory feeds the MMAs of all kTPW tokens.
+template <int kTok, int kTPW>
+__device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int64_t u0, int64_t u1, int w0) {
     constexpr int kStages = DecodeSmemT<kTok>::kStages;
     const int lane = threadIdx.x & 31;
     const int gr = lane >> 2;  // fragment row group
     const int qd = lane & 3;   // fragment column pair
-    uint32_t qf[8][2];
-    float oacc[8][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t qf[kTPW][8][2];
+    float oacc[kTPW][8][4];
+    float m0[kTPW], m1[kTPW], l0[kTPW], l1[kTPW];
+#pragma unroll
+    for (int j = 0; j < kTPW; ++j) m0[j] = m1[j] = -INFINITY, l0[j] = l1[j] = 0.f;
     int stage = 0;
     uint32_t phase = 0;
     const uint32_t kbase = smem_u32(sm.k[0]), vbase = smem_u32(sm.v[0]);
@@ -365,107 +370,121 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
         }
         const StageDesc d = sm.desc[stage];
         if (d.flags & kFirst) {
-            const uint32_t *qs = reinterpret_cast<const uint32_t *>(sm.q[stage] + w * kQBytes);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                qf[ks][0] = qs[(gr * kD + ks * 16 + 2 * qd) >> 1];
-                qf[ks][1] = qs[(gr * kD + ks * 16 + 8 + 2 * qd) >> 1];
+            for (int j = 0; j < kTPW; ++j) {
+                // a token past n_tok has no query row loaded; its keys are all
+                // masked below and it writes nothing
+                const uint32_t *qs = reinterpret_cast<const uint32_t *>(sm.q[stage] + (w0 + j) * kQBytes);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qf[j][ks][0] = qs[(gr * kD + ks * 16 + 2 * qd) >> 1];
+                    qf[j][ks][1] = qs[(gr * kD + ks * 16 + 8 + 2 * qd) >> 1];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) oacc[j][i][0] = oacc[j][i][1] = oacc[j][i][2] = oacc[j][i][3] = 0.f;
+                m0[j] = m1[j] = -INFINITY;
+                l0[j] = l1[j] = 0.f;
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
         }
         if (!(d.flags & kSkip)) {
             const uint32_t kb = kbase + stage * kPageHeadBytes, vb = vbase + stage * kPageHeadBytes;
-            // S^T = K Q^T : 4 tiles of 16 keys
-            float sacc[4][4];
+            // S^T = K Q^T : 4 tiles of 16 keys, per token
+            float sacc[kTPW][4][4];
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
-                sacc[kt][0] = sacc[kt][1] = sacc[kt][2] = sacc[kt][3] = 0.f;
+#pragma unroll
+                for (int j = 0; j < kTPW; ++j) sacc[j][kt][0] = sacc[j][kt][1] = sacc[j][kt][2] = sacc[j][kt][3] = 0.f;
                 const int row = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(kb + swz(row, ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
-                    mma_bf16_16816(sacc[kt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+#pragma unroll
+                    for (int j = 0; j < kTPW; ++j) mma_bf16_16816(sacc[j][kt], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
                 }
             }
-            // scale to log2 units and mask the keys this token does not see:
-            // its position is t = len - n_tok + w; keys (key0 + r) <= t and,
-            // for SWA, > t - W, inside the page's part of the range [lo, hi)
-            int32_t r_lo = d.lo, r_hi = d.hi;  // one token: the stage's range is its own
-            if constexpr (kTok > 1) {
-                const int32_t t = d.len - a.n_tok + w;
-                r_hi = min(d.hi, t - d.key0 + 1);
-                if (a.window > 0) r_lo = max(d.lo, t - a.window + 1 - d.key0);
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            uint32_t pb[kTPW][4][2];
 #pragma unroll
-            for (int kt = 0; kt < 4; ++kt) {
-                const int r0 = kt * 16 + gr, r1 = r0 + 8;
-                const bool v0 = r0 >= r_lo && r0 < r_hi, v1 = r1 >= r_lo && r1 < r_hi;
-                sacc[kt][0] = v0 ? sacc[kt][0] * a.scale_log2 : -INFINITY;
-                sacc[kt][1] = v0 ? sacc[kt][1] * a.scale_log2 : -INFINITY;
-                sacc[kt][2] = v1 ? sacc[kt][2] * a.scale_log2 : -INFINITY;
-                sacc[kt][3] = v1 ? sacc[kt][3] * a.scale_log2 : -INFINITY;
-                mx0 = fmaxf(mx0, fmaxf(sacc[kt][0], sacc[kt][2]));
-                mx1 = fmaxf(mx1, fmaxf(sacc[kt][1], sacc[kt][3]));
-            }
+            for (int j = 0; j < kTPW; ++j) {
+                // scale to log2 units and mask the keys this token does not
+                // see: its position is t = len - n_tok + w; keys (key0 + r)
+                // <= t and, for SWA, > t - W, inside the page's part of the
+                // range [lo, hi)
+                int32_t r_lo = d.lo, r_hi = d.hi;  // one token: the stage's range is its own
+                if constexpr (kTok > 1) {
+                    const int w = w0 + j;
+                    const int32_t t = d.len - a.n_tok + w;
+                    r_hi = w < a.n_tok ? min(d.hi, t - d.key0 + 1) : 0;
+                    if (a.window > 0) r_lo = max(d.lo, t - a.window + 1 - d.key0);
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            // with several tokens a page can hold no key that a token sees
-            // (n = -inf): then nothing is kept and P stays 0
-            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-            float b0 = n0, b1 = n1, al0, al1;
-            if constexpr (kTok > 1) {
-                b0 = n0 == -INFINITY ? 0.f : n0;
-                b1 = n1 == -INFINITY ? 0.f : n1;
-                al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
-                al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
-            } else {  // a stage holds at least one key of the range: n0, n1 finite
-                al0 = fast_exp2(m0 - n0);
-                al1 = fast_exp2(m1 - n1);
-            }
-            m0 = n0;
-            m1 = n1;
-            uint32_t pb[4][2];
-            float ps0 = 0.f, ps1 = 0.f;
+                for (int kt = 0; kt < 4; ++kt) {
+                    const int r0 = kt * 16 + gr, r1 = r0 + 8;
+                    const bool v0 = r0 >= r_lo && r0 < r_hi, v1 = r1 >= r_lo && r1 < r_hi;
+                    sacc[j][kt][0] = v0 ? sacc[j][kt][0] * a.scale_log2 : -INFINITY;
+                    sacc[j][kt][1] = v0 ? sacc[j][kt][1] * a.scale_log2 : -INFINITY;
+                    sacc[j][kt][2] = v1 ? sacc[j][kt][2] * a.scale_log2 : -INFINITY;
+                    sacc[j][kt][3] = v1 ? sacc[j][kt][3] * a.scale_log2 : -INFINITY;
+                    mx0 = fmaxf(mx0, fmaxf(sacc[j][kt][0], sacc[j][kt][2]));
+                    mx1 = fmaxf(mx1, fmaxf(sacc[j][kt][1], sacc[j][kt][3]));
+                }
 #pragma unroll
-            for (int kt = 0; kt < 4; ++kt) {
-                const float p0 = fast_exp2(sacc[kt][0] - b0), p1 = fast_exp2(sacc[kt][1] - b1);
-                const float p2 = fast_exp2(sacc[kt][2] - b0), p3 = fast_exp2(sacc[kt][3] - b1);
-                const uint32_t x0 = pack_bf16(p0, p1), x1 = pack_bf16(p2, p3);
-                // sum what the MMA will see (the bf16-rounded weights)
-                const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162 *>(&x0);
-                const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162 *>(&x1);
-                ps0 += __low2float(r0) + __low2float(r1);
-                ps1 += __high2float(r0) + __high2float(r1);
-                pb[kt][0] = movmatrix_t(x0);
-                pb[kt][1] = movmatrix_t(x1);
-            }
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                // with several tokens a page can hold no key that a token
+                // sees (n = -inf): then nothing is kept and P stays 0
+                const float n0 = fmaxf(m0[j], mx0), n1 = fmaxf(m1[j], mx1);
+                float b0 = n0, b1 = n1, al0, al1;
+                if constexpr (kTok > 1) {
+                    b0 = n0 == -INFINITY ? 0.f : n0;
+                    b1 = n1 == -INFINITY ? 0.f : n1;
+                    al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0[j] - n0);
+                    al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1[j] - n1);
+                } else {  // a stage holds at least one key of the range: n0, n1 finite
+                    al0 = fast_exp2(m0[j] - n0);
+                    al1 = fast_exp2(m1[j] - n1);
+                }
+                m0[j] = n0;
+                m1[j] = n1;
+                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-            for (int dt = 0; dt < 8; ++dt) {
-                oacc[dt][0] *= al0;
-                oacc[dt][1] *= al1;
-                oacc[dt][2] *= al0;
-                oacc[dt][3] *= al1;
+                for (int kt = 0; kt < 4; ++kt) {
+                    const float p0 = fast_exp2(sacc[j][kt][0] - b0), p1 = fast_exp2(sacc[j][kt][1] - b1);
+                    const float p2 = fast_exp2(sacc[j][kt][2] - b0), p3 = fast_exp2(sacc[j][kt][3] - b1);
+                    const uint32_t x0 = pack_bf16(p0, p1), x1 = pack_bf16(p2, p3);
+                    // sum what the MMA will see (the bf16-rounded weights)
+                    const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162 *>(&x0);
+                    const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162 *>(&x1);
+                    ps0 += __low2float(r0) + __low2float(r1);
+                    ps1 += __high2float(r0) + __high2float(r1);
+                    pb[j][kt][0] = movmatrix_t(x0);
+                    pb[j][kt][1] = movmatrix_t(x1);
+                }
+                l0[j] = l0[j] * al0 + ps0;
+                l1[j] = l1[j] * al1 + ps1;
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    oacc[j][dt][0] *= al0;
+                    oacc[j][dt][1] *= al1;
+                    oacc[j][dt][2] *= al0;
+                    oacc[j][dt][3] *= al1;
+                }
             }
             // O^T += V^T P^T
-            const int j = lane >> 3;
+            const int jj = lane >> 3;
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
-                const int key = kt * 16 + (lane & 7) + (j >> 1) * 8;
+                const int key = kt * 16 + (lane & 7) + (jj >> 1) * 8;
 #pragma unroll
                 for (int dt = 0; dt < 8; ++dt) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vb + swz(key, dt * 16 + (j & 1) * 8), a0, a1, a2, a3);
-                    mma_bf16_16816(oacc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+                    ldsm_x4_t(vb + swz(key, dt * 16 + (jj & 1) * 8), a0, a1, a2, a3);
+#pragma unroll
+                    for (int j = 0; j < kTPW; ++j)
+                        mma_bf16_16816(oacc[j][dt], a0, a1, a2, a3, pb[j][kt][0], pb[j][kt][1]);
                 }
             }
         }
@@ -473,39 +492,44 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
 
         if (d.flags & kLast) {
-            float t0 = l0, t1 = l1;
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                t0 += __shfl_xor_sync(0xffffffffu, t0, off);
-                t1 += __shfl_xor_sync(0xffffffffu, t1, off);
-            }
-            const int h0 = 2 * qd, h1 = 2 * qd + 1;
-            if (d.flags & kDirect) {
-                const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
-                __nv_bfloat16 *o0 =
-                    a.o + (((int64_t)d.seq * a.n_tok + w) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
-                __nv_bfloat16 *o1 = o0 + kD;
+            for (int j = 0; j < kTPW; ++j) {
+                const int w = w0 + j;
+                if (kTPW > 1 && w >= a.n_tok) break;
+                float t0 = l0[j], t1 = l1[j];
 #pragma unroll
-                for (int dt = 0; dt < 8; ++dt) {
-                    o0[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][0] * i0);
-                    o1[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][1] * i1);
-                    o0[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][2] * i0);
-                    o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][3] * i1);
+                for (int off = 4; off < 32; off <<= 1) {
+                    t0 += __shfl_xor_sync(0xffffffffu, t0, off);
+                    t1 += __shfl_xor_sync(0xffffffffu, t1, off);
                 }
-            } else {
-                Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + w];
-                if (gr == 0) {
-                    p.m[h0] = m0;
-                    p.m[h1] = m1;
-                    p.l[h0] = t0;
-                    p.l[h1] = t1;
-                }
+                const int h0 = 2 * qd, h1 = 2 * qd + 1;
+                if (d.flags & kDirect) {
+                    const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
+                    __nv_bfloat16 *o0 =
+                        a.o + (((int64_t)d.seq * a.n_tok + w) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
+                    __nv_bfloat16 *o1 = o0 + kD;
 #pragma unroll
-                for (int dt = 0; dt < 8; ++dt) {
-                    p.o[h0][dt * 16 + gr] = oacc[dt][0];
-                    p.o[h1][dt * 16 + gr] = oacc[dt][1];
-                    p.o[h0][dt * 16 + gr + 8] = oacc[dt][2];
-                    p.o[h1][dt * 16 + gr + 8] = oacc[dt][3];
+                    for (int dt = 0; dt < 8; ++dt) {
+                        o0[dt * 16 + gr] = __float2bfloat16_rn(oacc[j][dt][0] * i0);
+                        o1[dt * 16 + gr] = __float2bfloat16_rn(oacc[j][dt][1] * i1);
+                        o0[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[j][dt][2] * i0);
+                        o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[j][dt][3] * i1);
+                    }
+                } else {
+                    Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + w];
+                    if (gr == 0) {
+                        p.m[h0] = m0[j];
+                        p.m[h1] = m1[j];
+                        p.l[h0] = t0;
+                        p.l[h1] = t1;
+                    }
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        p.o[h0][dt * 16 + gr] = oacc[j][dt][0];
+                        p.o[h1][dt * 16 + gr] = oacc[j][dt][1];
+                        p.o[h0][dt * 16 + gr + 8] = oacc[j][dt][2];
+                        p.o[h1][dt * 16 + gr + 8] = oacc[j][dt][3];
+                    }
                 }
             }
         }
@@ -513,17 +537,20 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
     }
 }
 
-template <int kTok>
-__global__ void __launch_bounds__(32 * (kTok + 1)) decode_mma_bf16_d128(const __grid_constant__ CUtensorMap tk,
-                                                                      const __grid_constant__ CUtensorMap tv,
-                                                                      DecodeArgs a) {
+// Consumer warps: kTok / kTPW, each with kTPW tokens; the last warp is the
+// producer. Warps whose first token is past n_tok stay idle.
+template <int kTok, int kTPW>
+__global__ void __launch_bounds__(32 * (kTok / kTPW + 1)) decode_mma_bf16_d128(const __grid_constant__ CUtensorMap tk,
+                                                                             const __grid_constant__ CUtensorMap tv,
+                                                                             DecodeArgs a) {
     using Smem = DecodeSmemT<kTok>;
+    constexpr int kWarps = kTok / kTPW;
     extern __shared__ uint8_t raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     if (threadIdx.x == 0) {
         for (int i = 0; i < Smem::kStages; ++i) {
             mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], a.n_tok);
+            mbar_init(&sm.empty[i], (a.n_tok + kTPW - 1) / kTPW);  // the active consumer warps
         }
         sm.abort = 0;
         fence_barrier_init();
@@ -535,10 +562,10 @@ __global__ void __launch_bounds__(32 * (kTok + 1)) decode_mma_bf16_d128(const __
     if (U == 0) return;
     const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
     const int warp = threadIdx.x >> 5;
-    if (warp == kTok)
+    if (warp == kWarps)
         decode_producer<false>(sm, &tk, &tv, a, u0, u1);
-    else if (warp < a.n_tok)
-        decode_consumer<kTok>(sm, a, u0, u1, warp);
+    else if (warp * kTPW < a.n_tok)
+        decode_consumer<kTok, kTPW>(sm, a, u0, u1, warp * kTPW);
 }
 
 // ---------------------------------------------------------- FP8 decode
@@ -1008,34 +1035,38 @@ bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *
            ((uintptr_t)layer->k_pool & 15) == 0 && ((uintptr_t)layer->v_pool & 15) == 0;
 }
 
-template <int kTok>
+template <int kTok, int kTPW>
 int decode_ctas_per_sm_t() {
     static int v = -1;
     if (v < 0) {
         constexpr size_t smem = decode_smem_bytes<kTok>();
-        if (cudaFuncSetAttribute(decode_mma_bf16_d128<kTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(decode_mma_bf16_d128<kTok, kTPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128<kTok>, 32 * (kTok + 1), smem) !=
-            cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128<kTok, kTPW>,
+                                                          32 * (kTok / kTPW + 1), smem) != cudaSuccess)
             n = 1;
         v = std::max(1, n);
     }
     return v;
 }
 
-int decode_ctas_per_sm() { return decode_ctas_per_sm_t<1>(); }
+int decode_ctas_per_sm() { return decode_ctas_per_sm_t<1, 1>(); }
 
-// Kernel instantiation (consumer warps) serving n_tok query tokens.
+// Kernel instantiation serving n_tok query tokens: up to 4 tokens one per
+// consumer warp; 5..8 tokens two per warp (4 warps), which halves the
+// shared-memory reads of a page (8 warps reading every page outrun the
+// shared-memory bandwidth; with 4 tokens the extra MMA work per warp costs
+// more than it saves).
 int tok_variant(int n_tok) { return n_tok <= 2 ? n_tok : n_tok <= 4 ? 4 : 8; }
 
 int decode_ctas_per_sm_for(int n_tok) {
     switch (tok_variant(n_tok)) {
-    case 1: return decode_ctas_per_sm_t<1>();
-    case 2: return decode_ctas_per_sm_t<2>();
-    case 4: return decode_ctas_per_sm_t<4>();
-    default: return decode_ctas_per_sm_t<8>();
+    case 1: return decode_ctas_per_sm_t<1, 1>();
+    case 2: return decode_ctas_per_sm_t<2, 1>();
+    case 4: return decode_ctas_per_sm_t<4, 1>();
+    default: return decode_ctas_per_sm_t<8, 2>();
     }
 }
 
@@ -1130,11 +1161,11 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
     return HSWA_OK;
 }
 
-template <int kTok>
+template <int kTok, int kTPW>
 cudaError_t launch_decode_kernel(int n_ctas, cudaStream_t st, const CUtensorMap &tk, const CUtensorMap &tv,
                                  const DecodeArgs &a) {
-    return launch_pdl(decode_mma_bf16_d128<kTok>, dim3(n_ctas), dim3(32 * (kTok + 1)), decode_smem_bytes<kTok>(), st,
-                      tk, tv, a);
+    return launch_pdl(decode_mma_bf16_d128<kTok, kTPW>, dim3(n_ctas), dim3(32 * (kTok / kTPW + 1)),
+                      decode_smem_bytes<kTok>(), st, tk, tv, a);
 }
 
 // Decode of n_tok query tokens per sequence, with an optional fused append
@@ -1196,10 +1227,10 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
         return HSWA_ERR_CUDA;
     cudaError_t e;
     switch (tok_variant(n_tok)) {
-    case 1: e = launch_decode_kernel<1>(n_ctas, st, tk, tv, a); break;
-    case 2: e = launch_decode_kernel<2>(n_ctas, st, tk, tv, a); break;
-    case 4: e = launch_decode_kernel<4>(n_ctas, st, tk, tv, a); break;
-    default: e = launch_decode_kernel<8>(n_ctas, st, tk, tv, a); break;
+    case 1: e = launch_decode_kernel<1, 1>(n_ctas, st, tk, tv, a); break;
+    case 2: e = launch_decode_kernel<2, 1>(n_ctas, st, tk, tv, a); break;
+    case 4: e = launch_decode_kernel<4, 1>(n_ctas, st, tk, tv, a); break;
+    default: e = launch_decode_kernel<8, 2>(n_ctas, st, tk, tv, a); break;
     }
     if (e != cudaSuccess ||
         launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * n_tok), dim3(256), 0, st, a, n_ctas) != cudaSuccess)
