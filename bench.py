@@ -440,7 +440,7 @@ class ChunkedPrefill:
     every step has the same prefixes. The SWA release of the chunk runs once,
     after the last step."""
 
-    def __init__(self, w):
+    def __init__(self, w, fp8=False):
         import torch
         import hybrid_sliding_window_dual_gb300 as H
         from hybrid_sliding_window_dual_gb300.session import DualPoolSession
@@ -451,8 +451,8 @@ class ChunkedPrefill:
         swa_pages = B * (math.ceil((W + C) / P) + 2) + 16
         max_pages = max(math.ceil((L + C) / P) for L in w.cached) + 1
         cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
-                       head_dim=w.head_dim, dtype=w.dtype, full_pages=full_pages, swa_pages=swa_pages,
-                       max_seqs=B, max_pages_per_seq=max_pages)
+                       head_dim=w.head_dim, dtype=H.HSWA_DTYPE_FP8_E4M3 if fp8 else w.dtype,
+                       full_pages=full_pages, swa_pages=swa_pages, max_seqs=B, max_pages_per_seq=max_pages)
         self.stream = torch.cuda.Stream()
         self.sess = DualPoolSession(cfg, [wl.KIND_FULL, wl.KIND_SWA], wl.permutation(full_pages, w.seed),
                                     wl.permutation(swa_pages, w.seed + 1), stream=self.stream, init="empty")
@@ -470,7 +470,15 @@ class ChunkedPrefill:
                     flat = t.view(-1)
                     for j in range(0, flat.numel(), 1 << 28):
                         n = min(1 << 28, flat.numel() - j)
-                        flat[j:j + n] = torch.randn(n, generator=g, device="cuda").to(t.dtype)
+                        if fp8:  # seeded E4M3 codes without the NaN patterns
+                            mag = torch.randint(0, 0x7F, (n,), generator=g, device="cuda", dtype=torch.int32)
+                            sgn = torch.randint(0, 2, (n,), generator=g, device="cuda", dtype=torch.int32)
+                            flat[j:j + n] = (mag | (sgn << 7)).to(torch.uint8)
+                        else:
+                            flat[j:j + n] = torch.randn(n, generator=g, device="cuda").to(t.dtype)
+                if fp8:
+                    self.sess.ks[i].uniform_(0.001, 0.011)
+                    self.sess.vs[i].uniform_(0.001, 0.011)
             self.sess.sync()
         T = B * C
         self.T, self.C = T, C
@@ -512,9 +520,10 @@ class ChunkedPrefill:
             raise RuntimeError("device status %d after benchmark" % st)
 
 
-def measure_prefill(steps, warmup, w):
-    """Whole-chunk TFLOP/s of the chunked-prefill workload (valid pairs only)."""
-    pb = ChunkedPrefill(w)
+def measure_prefill(steps, warmup, w, fp8=False):
+    """Whole-chunk TFLOP/s of the chunked-prefill workload (valid pairs only);
+    over FP8 pools when fp8 (the staging pass is inside each layer's time)."""
+    pb = ChunkedPrefill(w, fp8=fp8)
     for _ in range(warmup):
         pb.step()
     pb.stream.synchronize()
@@ -743,8 +752,8 @@ class SwaTransfer:
         swa_pages = 2 * B * (math.ceil((W + 64) / P) + 2) + math.ceil((W + 4096) / P) + 16
         max_pages = max(math.ceil((L + extra) / P) for L in w.cached) + 1
         cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
-                       head_dim=w.head_dim, dtype=w.dtype, full_pages=full_pages, swa_pages=swa_pages,
-                       max_seqs=B, max_pages_per_seq=max_pages)
+                       head_dim=w.head_dim, dtype=H.HSWA_DTYPE_FP8_E4M3 if fp8 else w.dtype,
+                       full_pages=full_pages, swa_pages=swa_pages, max_seqs=B, max_pages_per_seq=max_pages)
         self.stream = torch.cuda.Stream()
         self.sess = DualPoolSession(cfg, list(w.layer_kinds), None, wl.permutation(swa_pages, w.seed),
                                     stream=self.stream, init="empty")
@@ -934,6 +943,16 @@ def run_decode(args, world, rank, local):
             "valid_tflop_per_step": round(pf["valid_tflop_per_step"], 3),
             "ms_per_step": round(pf["ms_per_step"], 3), "tokens_per_s": round(pf["tokens_per_s"], 1),
             "kernel": "prefill_tc_bf16_d128"}
+        if not args.no_fp8:
+            del pf
+            torch.cuda.empty_cache()
+            p8 = measure_prefill(max(2, args.prefill_steps // 2), 1, workload(args, "chunked_prefill"), fp8=True)
+            line["prefill"]["fp8"] = {
+                "workload": "the same chunk over FP8 E4M3 pools (scale per token, kv head, 128-element tile)",
+                "tflops": round(p8["step_tflops"], 1), "frac": round(p8["step_tflops"] / bf16_sus, 4),
+                "full_layer_tflops": round(p8["full_tflops"], 1), "full_layer_ms": round(p8["full_ms"], 3),
+                "swa_layer_ms": round(p8["swa_ms"], 3), "ms_per_step": round(p8["ms_per_step"], 3),
+                "kernel": "prefill_stage_fp8 + prefill_q_to_f16 + prefill_tc_bf16_d128<f16> (staging inside the layer time)"}
     if not args.no_hybrid70:
         h = measure_hybrid70(args.hybrid_steps, 2)
         line["hybrid70"] = {

@@ -78,6 +78,9 @@ _SIG = {
                                ctypes.c_size_t, _P]),
     "hswa_prefill_chunk": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I, _I,
                                 ctypes.c_float, _P]),
+    "hswa_prefill_workspace_size": (ctypes.c_size_t, [_P, ctypes.POINTER(Layer), _I, _I]),
+    "hswa_prefill_chunk_ws": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I, _I,
+                                   ctypes.c_float, _P, ctypes.c_size_t, _P]),
     "hswa_swa_gather": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
     "hswa_swa_scatter": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
     "hswa_check": (_I, [_P]),
@@ -251,6 +254,17 @@ def hswa_prefill_chunk(pool, layer: Layer, q, o, d_bt, d_prefix_len, d_q_start, 
     _check(lib.hswa_prefill_chunk(pool, ctypes.byref(layer), _ptr(q), _ptr(o), _ptr(d_bt), _ptr(d_prefix_len),
                                   _ptr(d_q_start), int(n_seqs), int(total_q), int(max_q_len), float(scale),
                                   _stream(stream)), "hswa_prefill_chunk")
+
+
+def hswa_prefill_workspace_size(pool, layer: Layer, n_seqs, max_q_len):
+    return int(lib.hswa_prefill_workspace_size(pool, ctypes.byref(layer), int(n_seqs), int(max_q_len)))
+
+
+def hswa_prefill_chunk_ws(pool, layer: Layer, q, o, d_bt, d_prefix_len, d_q_start, n_seqs, total_q, max_q_len,
+                          scale, ws, ws_bytes, stream=None):
+    _check(lib.hswa_prefill_chunk_ws(pool, ctypes.byref(layer), _ptr(q), _ptr(o), _ptr(d_bt), _ptr(d_prefix_len),
+                                     _ptr(d_q_start), int(n_seqs), int(total_q), int(max_q_len), float(scale),
+                                     _ptr(ws), int(ws_bytes), _stream(stream)), "hswa_prefill_chunk_ws")
 
 
 def hswa_swa_gather(pool, layer: Layer, d_swa_bt, d_seq_len, d_tok_offset, n_seqs, dst, stream=None):

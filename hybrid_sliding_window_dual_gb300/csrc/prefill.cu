@@ -23,7 +23,18 @@
 //     of [0, t] for a Full layer, [t - W + 1, t] for an SWA layer.
 // Every wait is bounded; on a timeout the CTA records HSWA_ERR_TIMEOUT,
 // drains its copies and MMAs, frees its TMEM and returns.
+//
+// FP8 pools ("Baidu AI Cloud: Day-0 support for hybrid-architecture LLMs",
+// Optimization 2 item 2): a staging pass first writes fp16 copies of the
+// pages the chunk reads (code x scale, rounded once: 11 significant bits
+// against E4M3's 4, so the copy adds an error far below bf16's) and of q into
+// the caller's workspace, with a block table onto the page copies; the same
+// tensor-core kernel then runs with fp16 operands (q, K, V and P all fp16).
+// The chunk's attention is compute-bound (tens of TFLOP per chunk against a
+// few GB moved by the staging), so the pass costs about a percent.
 #include <algorithm>
+
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -52,6 +63,7 @@ struct PrefillSmem {
     uint32_t tmem_base;
     int32_t abort;
 };
+static_assert(offsetof(PrefillSmem, kv) % 1024 == 0, "128-byte swizzled tiles need 1024-byte alignment");
 constexpr size_t kPrefillSmemBytes = sizeof(PrefillSmem) + 1024;
 
 struct PrefillArgs {
@@ -79,13 +91,13 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N.
-constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+// Instruction descriptor, kind::f16, fp32 D, M x N: A and B both bf16
+// (format 1) or both fp16 (format 0), never mixed.
+constexpr uint32_t idesc_16(int M, int N, bool b_mn_major, bool f16) {
+    const uint32_t fmt = f16 ? 0u : 1u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
-constexpr uint32_t kIdescPV = idesc_bf16(kBM, kD, true);
 
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -151,6 +163,11 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" : HSWA_RW8(0), HSWA_RW8(8), HSWA_RW8(16), HSWA_RW8(24)::"memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
 
 // ------------------------------------------------------------- work unit
 struct Unit {
@@ -229,7 +246,9 @@ __device__ void prefill_producer(PrefillSmem &sm, const CUtensorMap *tq, const C
 
 // S_x = Q_x K^T over d = 128: 8 steps of K = 16 (32 bytes inside a 128-byte
 // swizzle row; the second half of d is the second 16 KB block).
+template <bool kF16>
 __device__ __forceinline__ void issue_s(uint32_t t_s, uint32_t q_addr, uint32_t k_addr) {
+    constexpr uint32_t kIdescQK = idesc_16(kBM, kBN, false, kF16);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -240,13 +259,16 @@ __device__ __forceinline__ void issue_s(uint32_t t_s, uint32_t q_addr, uint32_t 
 // O_x += P_x V over 128 keys: 8 steps of K = 16 keys; P_x (bf16 pairs) sits in
 // the first 64 columns of S_x, V is MN-major (d contiguous) with the two
 // 64-column halves 16 KB apart.
+template <bool kF16>
 __device__ __forceinline__ void issue_pv(uint32_t t_o, uint32_t t_p, uint32_t v_addr, bool first_tile) {
+    constexpr uint32_t kIdescPV = idesc_16(kBM, kD, true, kF16);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
         mma_ts(t_o, t_p + kk * 8, sdesc(v_addr + kk * 2048, kHalfBytes, 1024), kIdescPV,
                (first_tile && kk == 0) ? 0u : 1u);
 }
 
+template <bool kF16>
 __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u) {
     const uint32_t tbase = sm.tmem_base;
     const uint32_t ts0 = tbase, ts1 = tbase + 128, to0 = tbase + 256, to1 = tbase + 384;
@@ -259,9 +281,9 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
         if (ok) {
             tc_fence_after();
             const uint32_t k0 = smem_u32(sm.kv[0]);
-            issue_s(ts0, qa0, k0);
+            issue_s<kF16>(ts0, qa0, k0);
             mma_commit(&sm.s_full[0]);
-            issue_s(ts1, qa1, k0);
+            issue_s<kF16>(ts1, qa1, k0);
             mma_commit(&sm.s_full[1]);
             mma_commit(&sm.kv_empty[0]);
         }
@@ -273,7 +295,7 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
             if (!ok) break;
             tc_fence_after();
             const uint32_t v_addr = smem_u32(sm.kv[sv]);
-            issue_pv(to0, ts0, v_addr, j == 0);
+            issue_pv<kF16>(to0, ts0, v_addr, j == 0);
             const bool more = j + 1 < n;
             uint32_t k_addr = 0;
             if (more) {
@@ -281,16 +303,16 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
                 if (!ok) break;
                 tc_fence_after();
                 k_addr = smem_u32(sm.kv[sk]);
-                issue_s(ts0, qa0, k_addr);
+                issue_s<kF16>(ts0, qa0, k_addr);
                 mma_commit(&sm.s_full[0]);
             }
             ok = mbar_wait(&sm.p_full[1], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
-            issue_pv(to1, ts1, v_addr, j == 0);
+            issue_pv<kF16>(to1, ts1, v_addr, j == 0);
             mma_commit(&sm.kv_empty[sv]);
             if (more) {
-                issue_s(ts1, qa1, k_addr);
+                issue_s<kF16>(ts1, qa1, k_addr);
                 mma_commit(&sm.s_full[1]);
                 mma_commit(&sm.kv_empty[sk]);
             }
@@ -303,6 +325,7 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
     if (!ok) sm.abort = 1;
 }
 
+template <bool kF16>
 __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Unit &u, int x) {
     const int warp = (threadIdx.x >> 5) & 3;
     const int r = warp * 32 + (threadIdx.x & 31);  // query row of this thread
@@ -368,7 +391,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
                                             sc2, nm2);
                 const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                 sum2 = __fadd2_rn(sum2, p);
-                sr[c][i] = pack_bf16(p.x, p.y);
+                sr[c][i] = kF16 ? pack_f16(p.x, p.y) : pack_bf16(p.x, p.y);
             }
             tmem_st16(t_s + 16 * c, sr[c]);
         }
@@ -422,6 +445,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
     }
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_bf16_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, PrefillArgs a) {
@@ -454,12 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp < 8)
-        prefill_softmax(sm, a, u, warp >> 2);
+        prefill_softmax<kF16>(sm, a, u, warp >> 2);
     else if (warp == 8) {
         if ((threadIdx.x & 31) == 0) prefill_producer(sm, &tq, &tk, &tv, a, u);
         __syncwarp();
     } else {
-        if ((threadIdx.x & 31) == 0) prefill_mma(sm, a, u);
+        if ((threadIdx.x & 31) == 0) prefill_mma<kF16>(sm, a, u);
         __syncwarp();
     }
     tc_fence_before();
@@ -471,9 +495,184 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool prefill_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
     const hswa_config &c = pool->cfg;
     const int g = c.n_q_heads / c.n_kv_heads;
-    return c.dtype == HSWA_DTYPE_BF16 && c.head_dim == kD && c.page_size == kP && g % 2 == 0 &&
-           ((uintptr_t)q & 15) == 0 && ((uintptr_t)o & 15) == 0 && ((uintptr_t)layer->k_pool & 15) == 0 &&
-           ((uintptr_t)layer->v_pool & 15) == 0;
+    return (c.dtype == HSWA_DTYPE_BF16 || c.dtype == HSWA_DTYPE_FP8_E4M3) && c.head_dim == kD && c.page_size == kP &&
+           g % 2 == 0 && ((uintptr_t)q & 15) == 0 && ((uintptr_t)o & 15) == 0 &&
+           ((uintptr_t)layer->k_pool & 15) == 0 && ((uintptr_t)layer->v_pool & 15) == 0;
+}
+
+// ------------------------------------------------------------ FP8 staging
+// Pages per sequence the staging copy reserves: a Full layer may read every
+// logical page; an SWA layer's chunk of at most max_q_len rows reads keys
+// [prefix - W + 1, prefix + n), at most W - 1 + max_q_len keys.
+int32_t stage_pages_per_seq(const hswa_config &c, const hswa_layer *layer, int max_q_len) {
+    if (layer->kind != HSWA_KIND_SWA) return c.max_pages_per_seq;
+    const int64_t keys = (int64_t)layer->window - 1 + max_q_len;
+    return (int32_t)std::min<int64_t>(c.max_pages_per_seq, (keys + kP - 1) / kP + 1);
+}
+
+constexpr size_t align1k(size_t x) { return (x + 1023) & ~(size_t)1023; }
+
+// Workspace of an FP8 chunk: the staging block table, the fp16 K and V page
+// copies, and the fp16 copy of q (n_seqs * max_q_len rows at most).
+struct StageLayout {
+    int32_t per_seq;
+    size_t page_bytes, k_off, v_off, q_off, total;
+};
+
+StageLayout stage_layout(const hswa_config &c, const hswa_layer *layer, int n_seqs, int max_q_len) {
+    StageLayout l;
+    l.per_seq = stage_pages_per_seq(c, layer, max_q_len);
+    l.page_bytes = (size_t)c.n_kv_heads * kP * kD * sizeof(__half);
+    const size_t pages = (size_t)n_seqs * l.per_seq;
+    l.k_off = align1k((size_t)n_seqs * c.max_pages_per_seq * sizeof(int32_t));
+    l.v_off = l.k_off + align1k(pages * l.page_bytes);
+    l.q_off = l.v_off + align1k(pages * l.page_bytes);
+    l.total = l.q_off + align1k((size_t)n_seqs * max_q_len * c.n_q_heads * kD * sizeof(__half));
+    return l;
+}
+
+struct StageArgs {
+    const int32_t *bt, *prefix, *q_start;
+    const uint8_t *k_codes, *v_codes;  // [page][Hkv][P][d], V pages [page][Hkv][d][P]
+    const float *k_scale, *v_scale;    // [page][Hkv][P] (one 128-element tile per row)
+    int32_t *stage_bt;                 // [n_seqs][bt_stride]
+    __half *k_out, *v_out;             // [n_seqs * per_seq][Hkv][P][d]
+    int32_t n_seqs, bt_stride, hkv, window, num_pages, per_seq;
+    int *err;
+};
+
+// fp16 of an E4M3 code (exact) times its fp32 scale, rounded once to fp16;
+// magnitudes past the fp16 range saturate at 65504.
+__device__ __forceinline__ __half2 dequant_f16x2(uint8_t c0, uint8_t c1, float s0, float s1) {
+    const float2 f =
+        __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c0 | (c1 << 8)), __NV_E4M3)));
+    return __floats2half2_rn(fminf(fmaxf(f.x * s0, -65504.f), 65504.f), fminf(fmaxf(f.y * s1, -65504.f), 65504.f));
+}
+
+// One block per (logical page j, sequence s): writes the staging table entry
+// of (s, j) and, for a page the chunk reads, its fp16 copy (K rows stay
+// rows; each kv head's transposed V block [d][P] becomes [P][d]).
+__global__ void __launch_bounds__(256) prefill_stage_fp8(StageArgs a) {
+    const int32_t j = blockIdx.x, s = blockIdx.y;
+    const int32_t pre = a.prefix[s], n = a.q_start[s + 1] - a.q_start[s];
+    const int32_t lo_key = (a.window > 0 && pre - a.window + 1 > 0) ? pre - a.window + 1 : 0;
+    const int32_t lo_pg = lo_key / kP, hi_pg = n > 0 ? (pre + n - 1) / kP : -1;
+    int32_t page = -1, slot = -1;
+    if (j >= lo_pg && j <= hi_pg) {
+        page = a.bt[(int64_t)s * a.bt_stride + j];
+        if (j - lo_pg >= a.per_seq) {  // the workspace was sized for fewer rows
+            if (threadIdx.x == 0) set_error(a.err, HSWA_ERR_BOUNDS);
+            page = -1;
+        }
+        if (page >= 0 && page < a.num_pages) slot = s * a.per_seq + (j - lo_pg);
+    }
+    if (threadIdx.x == 0) a.stage_bt[(int64_t)s * a.bt_stride + j] = slot;  // -1: the kernel reports it if read
+    if (slot < 0) return;
+    // K: 16 codes per thread and step
+    const uint8_t *kc = a.k_codes + (int64_t)page * a.hkv * kP * kD;
+    const float *ks = a.k_scale + (int64_t)page * a.hkv * kP;
+    __half *ko = a.k_out + (int64_t)slot * a.hkv * kP * kD;
+    const int32_t chunks = a.hkv * kP * kD / 16;
+    for (int32_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+        const uint4 raw = reinterpret_cast<const uint4 *>(kc)[c];
+        const float sc = ks[c / (kD / 16)];  // row (kv head, key) of the chunk
+        const uint8_t *b = reinterpret_cast<const uint8_t *>(&raw);
+        __align__(16) __half2 out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = dequant_f16x2(b[2 * i], b[2 * i + 1], sc, sc);
+        reinterpret_cast<uint4 *>(ko)[2 * c] = reinterpret_cast<const uint4 *>(out)[0];
+        reinterpret_cast<uint4 *>(ko)[2 * c + 1] = reinterpret_cast<const uint4 *>(out)[1];
+    }
+    // V: each kv head's [d][P] code block is transposed to [P][d] through
+    // shared memory (row stride 65 bytes keeps the column reads off one bank)
+    __shared__ uint8_t tile[kD * 65];
+    __shared__ float vsc[kP];
+    const uint8_t *vc = a.v_codes + (int64_t)page * a.hkv * kD * kP;
+    const float *vs = a.v_scale + (int64_t)page * a.hkv * kP;
+    __half *vo = a.v_out + (int64_t)slot * a.hkv * kP * kD;
+    for (int32_t h = 0; h < a.hkv; ++h) {
+        __syncthreads();
+        for (int32_t c = threadIdx.x; c < kD * kP / 16; c += blockDim.x) {
+            const uint4 raw = reinterpret_cast<const uint4 *>(vc + (int64_t)h * kD * kP)[c];
+            const uint8_t *b = reinterpret_cast<const uint8_t *>(&raw);
+            const int32_t d = c / (kP / 16), p0 = (c % (kP / 16)) * 16;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tile[d * 65 + p0 + i] = b[i];
+        }
+        if (threadIdx.x < kP) vsc[threadIdx.x] = vs[h * kP + threadIdx.x];
+        __syncthreads();
+        for (int32_t c = threadIdx.x; c < kP * kD / 8; c += blockDim.x) {
+            const int32_t p = c / (kD / 8), d0 = (c % (kD / 8)) * 8;
+            const float sc = vsc[p];
+            __align__(16) __half2 out[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                out[i] = dequant_f16x2(tile[(d0 + 2 * i) * 65 + p], tile[(d0 + 2 * i + 1) * 65 + p], sc, sc);
+            *reinterpret_cast<uint4 *>(vo + ((int64_t)h * kP + p) * kD + d0) = *reinterpret_cast<const uint4 *>(out);
+        }
+    }
+}
+
+// q (bf16) to fp16 for the fp16 MMAs: exact for magnitudes in
+// [2^-14, 65504], subnormal below, saturated above. 8 elements per step.
+__global__ void __launch_bounds__(256) prefill_q_to_f16(const __nv_bfloat16 *__restrict__ q, __half *__restrict__ q16,
+                                                        int64_t n8) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 raw = reinterpret_cast<const uint4 *>(q)[i];
+        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+        __align__(16) __half2 out[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(b[k]);
+            out[k] = __floats2half2_rn(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
+        }
+        reinterpret_cast<uint4 *>(q16)[i] = *reinterpret_cast<const uint4 *>(out);
+    }
+}
+
+// The tensor-core prefill over 16-bit pages k_pool / v_pool (num_pages
+// pages) addressed through bt; q, K and V all bf16, or all fp16 (f16).
+int launch_prefill_tc(const hswa_config &c, int32_t window, const void *k_pool, const void *v_pool, bool f16,
+                      int32_t num_pages, const int32_t *bt, const void *q, void *o, const int32_t *d_prefix_len,
+                      const int32_t *d_q_start, int n_seqs, int total_q, int max_q_len, float scale,
+                      cudaStream_t st) {
+    const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
+    if (rows >= (1ull << 31)) return HSWA_ERR_UNSUPPORTED;
+    const CUtensorMapDataType ty = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_3d(&tq, q, kD, c.n_q_heads, (uint64_t)total_q, 64, 1, kBM, ty, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tk, k_pool, rows, kD, kP, 64, ty, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tv, v_pool, rows, kD, kP, 64, ty, CU_TENSOR_MAP_SWIZZLE_128B))
+        return HSWA_ERR_CUDA;
+    PrefillArgs a;
+    a.bt = bt;
+    a.prefix = d_prefix_len;
+    a.q_start = d_q_start;
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.n_seqs = n_seqs;
+    a.bt_stride = c.max_pages_per_seq;
+    a.hq = c.n_q_heads;
+    a.hkv = c.n_kv_heads;
+    a.window = window;
+    a.num_pages = num_pages;
+    a.kv_rows = (int32_t)rows;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.err = error_word();
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(prefill_tc_bf16_d128<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPrefillSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(prefill_tc_bf16_d128<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPrefillSmemBytes) != cudaSuccess)
+            return HSWA_ERR_CUDA;
+        attr = true;
+    }
+    dim3 grid(c.n_q_heads / 2, (max_q_len + kBM - 1) / kBM, n_seqs);
+    if (f16)
+        prefill_tc_bf16_d128<true><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
+    else
+        prefill_tc_bf16_d128<false><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
 }
 
 }  // namespace
@@ -481,9 +680,17 @@ bool prefill_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void 
 
 using namespace hswa;
 
-extern "C" int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
-                                  const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
-                                  int n_seqs, int total_q, int max_q_len, float scale, hswa_stream_t stream) {
+extern "C" size_t hswa_prefill_workspace_size(const hswa_pool *pool, const hswa_layer *layer, int n_seqs,
+                                              int max_q_len) {
+    if (!pool || !layer || n_seqs < 0 || max_q_len < 0 || pool->cfg.dtype != HSWA_DTYPE_FP8_E4M3) return 0;
+    if (layer->kind == HSWA_KIND_SWA && layer->window <= 0) return 0;
+    return stage_layout(pool->cfg, layer, n_seqs, max_q_len).total;
+}
+
+extern "C" int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                                     const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
+                                     int n_seqs, int total_q, int max_q_len, float scale, void *ws, size_t ws_bytes,
+                                     hswa_stream_t stream) {
     if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs || max_q_len < 0 || total_q < 0 ||
         !(scale > 0.f) ||
         (n_seqs > 0 && max_q_len > total_q) ||
@@ -494,45 +701,58 @@ extern "C" int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer
     if (!q || !o || !d_bt || !d_prefix_len || !d_q_start || !layer->k_pool || !layer->v_pool)
         return HSWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (pool->cfg.dtype == HSWA_DTYPE_FP8_E4M3) return HSWA_ERR_UNSUPPORTED;
+    const hswa_config &c = pool->cfg;
+    const int32_t window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
+    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
+    if (c.dtype == HSWA_DTYPE_FP8_E4M3) {
+        if (!prefill_fast_ok(pool, layer, q, o) || c.head_dim != 128 || !layer->k_scale || !layer->v_scale ||
+            ((uintptr_t)layer->k_pool & 15) || ((uintptr_t)layer->v_pool & 15))
+            return HSWA_ERR_UNSUPPORTED;
+        const StageLayout l = stage_layout(c, layer, n_seqs, max_q_len);
+        if (!ws || ((uintptr_t)ws & 255) || ws_bytes < l.total) return HSWA_ERR_INVALID_ARG;
+        if ((int64_t)total_q > (int64_t)n_seqs * max_q_len) return HSWA_ERR_INVALID_ARG;
+        const int64_t staged_pages = (int64_t)n_seqs * l.per_seq;
+        if (staged_pages * c.n_kv_heads * kP >= (1ll << 31)) return HSWA_ERR_UNSUPPORTED;
+        StageArgs sa;
+        sa.bt = d_bt;
+        sa.prefix = d_prefix_len;
+        sa.q_start = d_q_start;
+        sa.k_codes = static_cast<const uint8_t *>(layer->k_pool);
+        sa.v_codes = static_cast<const uint8_t *>(layer->v_pool);
+        sa.k_scale = layer->k_scale;
+        sa.v_scale = layer->v_scale;
+        uint8_t *base = static_cast<uint8_t *>(ws);
+        sa.stage_bt = reinterpret_cast<int32_t *>(base);
+        sa.k_out = reinterpret_cast<__half *>(base + l.k_off);
+        sa.v_out = reinterpret_cast<__half *>(base + l.v_off);
+        sa.n_seqs = n_seqs;
+        sa.bt_stride = c.max_pages_per_seq;
+        sa.hkv = c.n_kv_heads;
+        sa.window = window;
+        sa.num_pages = num_pages;
+        sa.per_seq = l.per_seq;
+        sa.err = error_word();
+        __half *q16 = reinterpret_cast<__half *>(base + l.q_off);
+        const int64_t n8 = (int64_t)total_q * c.n_q_heads * kD / 8;
+        set_last_kernel("prefill_stage_fp8+prefill_tc_bf16_d128<f16>");
+        prefill_stage_fp8<<<dim3(c.max_pages_per_seq, n_seqs), 256, 0, st>>>(sa);
+        prefill_q_to_f16<<<(int)std::min<int64_t>((n8 + 255) / 256, 4096), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(q), q16, n8);
+        if (cudaGetLastError() != cudaSuccess) return HSWA_ERR_CUDA;
+        return launch_prefill_tc(c, window, sa.k_out, sa.v_out, true, (int32_t)staged_pages, sa.stage_bt, q16, o,
+                                 d_prefix_len, d_q_start, n_seqs, total_q, max_q_len, scale, st);
+    }
     if (!prefill_fast_ok(pool, layer, q, o))
         return launch_attention_generic(pool, layer, q, o, d_bt, nullptr, d_prefix_len, d_q_start, max_q_len,
                                         n_seqs, scale, 1, st);
-    const hswa_config &c = pool->cfg;
-    const int32_t num_pages = layer->kind == HSWA_KIND_SWA ? c.swa_pages : c.full_pages;
-    const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
-    if (rows >= (1ull << 31)) return HSWA_ERR_UNSUPPORTED;
-    CUtensorMap tq, tk, tv;
-    if (!make_tmap_3d(&tq, q, kD, c.n_q_heads, (uint64_t)total_q, 64, 1, kBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_2d(&tk, layer->k_pool, rows, kD, kP, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_2d(&tv, layer->v_pool, rows, kD, kP, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
-        return HSWA_ERR_CUDA;
-    PrefillArgs a;
-    a.bt = d_bt;
-    a.prefix = d_prefix_len;
-    a.q_start = d_q_start;
-    a.o = static_cast<__nv_bfloat16 *>(o);
-    a.n_seqs = n_seqs;
-    a.bt_stride = c.max_pages_per_seq;
-    a.hq = c.n_q_heads;
-    a.hkv = c.n_kv_heads;
-    a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
-    a.num_pages = num_pages;
-    a.kv_rows = (int32_t)rows;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    a.err = error_word();
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(prefill_tc_bf16_d128, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPrefillSmemBytes) != cudaSuccess)
-            return HSWA_ERR_CUDA;
-        attr = true;
-    }
     set_last_kernel("prefill_tc_bf16_d128");
-    dim3 grid(c.n_q_heads / 2, (max_q_len + kBM - 1) / kBM, n_seqs);
-    prefill_tc_bf16_d128<<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
-    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+    return launch_prefill_tc(c, window, layer->k_pool, layer->v_pool, false, num_pages, d_bt, q, o, d_prefix_len,
+                             d_q_start, n_seqs, total_q, max_q_len, scale, st);
+}
+
+extern "C" int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                                  const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
+                                  int n_seqs, int total_q, int max_q_len, float scale, hswa_stream_t stream) {
+    return hswa_prefill_chunk_ws(pool, layer, q, o, d_bt, d_prefix_len, d_q_start, n_seqs, total_q, max_q_len, scale,
+                                 nullptr, 0, stream);
 }

@@ -65,6 +65,7 @@ class DualPoolSession:
                                        k_scale=ks.data_ptr() if ks is not None else None,
                                        v_scale=vs.data_ptr() if vs is not None else None))
         self.ws = None
+        self.prefill_ws = None
 
     def close(self):
         if self.pool:
@@ -129,8 +130,14 @@ class DualPoolSession:
                             scale, ws, ws.numel(), self.stream)
 
     def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale):
-        B.hswa_prefill_chunk(self.pool, self.layers[layer], q, o, self.bt(layer), d_prefix_len, d_q_start,
-                             n_seqs, q.shape[0], max_q_len, scale, self.stream)
+        need = B.hswa_prefill_workspace_size(self.pool, self.layers[layer], n_seqs, max_q_len)
+        ws = None
+        if need:  # FP8 pools stage bf16 copies of the pages the chunk reads
+            if self.prefill_ws is None or self.prefill_ws.numel() < need:
+                self.prefill_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+            ws = self.prefill_ws
+        B.hswa_prefill_chunk_ws(self.pool, self.layers[layer], q, o, self.bt(layer), d_prefix_len, d_q_start,
+                                n_seqs, q.shape[0], max_q_len, scale, ws, need, self.stream)
 
     def gather(self, layer, d_tok_offset, n_seqs, dst):
         B.hswa_swa_gather(self.pool, self.layers[layer], self.d_swa_bt, self.d_seq_len, d_tok_offset, n_seqs,

@@ -88,8 +88,9 @@ extern "C" {
  * v_scale [pages][Hkv][P][d / 128] fp32. q, o and the new K/V handed to the
  * append stay bf16; the append quantizes: scale = amax / 448 (1 if amax is
  * 0), code = round-to-nearest-even(x / scale) saturating at 448. Supported
- * by hswa_append_kv, hswa_decode and hswa_decode_append with d = 128,
- * 8 query heads per kv head and P = 64; other calls return
+ * by hswa_append_kv, hswa_decode, hswa_decode_append (d = 128, 8 query
+ * heads per kv head, P = 64) and hswa_prefill_chunk_ws (d = 128, an even
+ * number of query heads per kv head, P = 64); other calls return
  * HSWA_ERR_UNSUPPORTED. */
 #define HSWA_DTYPE_FP8_E4M3 2
 
@@ -269,6 +270,34 @@ int hswa_decode_multi(const hswa_pool *pool, const hswa_layer *layer, const void
 int hswa_prefill_chunk(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                        const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
                        int n_seqs, int total_q, int max_q_len, float scale, hswa_stream_t stream);
+
+/* Bytes of workspace hswa_prefill_chunk_ws needs for a chunk of n_seqs
+ * sequences with at most max_q_len new tokens each: 0 for bf16 and fp32
+ * pools (they need none); for an FP8 pool, room for an fp16 copy of every
+ * page the chunk can read (all of a sequence's table row for a Full layer,
+ * ceil((W - 1 + max_q_len) / P) + 1 pages for an SWA layer), a block table
+ * onto the copies and an fp16 copy of n_seqs * max_q_len query rows. */
+size_t hswa_prefill_workspace_size(const hswa_pool *pool, const hswa_layer *layer, int n_seqs,
+                                   int max_q_len);
+
+/* hswa_prefill_chunk with a workspace, which FP8 pools need ("Baidu AI
+ * Cloud: Day-0 support for hybrid-architecture LLMs", Optimization 2 item 2:
+ * an FP8 KV cache with one scale per token, head and 128-element tile).
+ * Same arguments and result as hswa_prefill_chunk. Over an FP8 pool the
+ * pages the chunk reads are first dequantized (E4M3 code x scale, rounded
+ * once to fp16, saturating at 65504) and q is converted to fp16 (exact for
+ * magnitudes in [2^-14, 65504]) into ws; the tensor-core kernel then
+ * attends with fp16 operands. q and o are bf16. ws: device, 256-byte
+ * aligned, at least
+ * hswa_prefill_workspace_size bytes (HSWA_ERR_INVALID_ARG otherwise),
+ * caller-owned, not read before it is written; it must not be reused until
+ * the call's work on stream has finished. Ignored (may be NULL) for bf16
+ * and fp32 pools. hswa_prefill_chunk on an FP8 pool returns
+ * HSWA_ERR_INVALID_ARG (no workspace). */
+int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
+                          const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
+                          int n_seqs, int total_q, int max_q_len, float scale, void *ws, size_t ws_bytes,
+                          hswa_stream_t stream);
 
 /* Transfer by SWA mask (Sec. 2.1, Data Transfer: only in-window data moves;
  * "Tiered KV Cache Offloading in vLLM", hybrid models: sliding-window

@@ -159,3 +159,30 @@ def test_device_calls_validate_before_launching():
     assert sizes[0] == H.hswa_decode_workspace_size(lp, 64)
     assert all(b > a for a, b in zip(sizes, sizes[1:]))
     H.hswa_pool_destroy(lp)
+
+
+def test_prefill_workspace_sizes():
+    """Only FP8 pools need a prefill workspace; an SWA layer stages at most
+    ceil((W - 1 + max_q_len) / P) + 1 pages per sequence, a Full layer its
+    whole table row."""
+    cfg, lp, _ = make_pair()
+    full = H.Layer(kind=H.HSWA_KIND_FULL, window=0, k_pool=16, v_pool=16)
+    assert H.hswa_prefill_workspace_size(lp, full, 4, 4096) == 0
+    H.hswa_pool_destroy(lp)
+    W, P, MP, hkv, d = 128, 64, 100, 8, 128
+    cfg = H.Config(window=W, page_size=P, n_q_heads=64, n_kv_heads=hkv, head_dim=d, dtype=H.HSWA_DTYPE_FP8_E4M3,
+                   full_pages=1000, swa_pages=100, max_seqs=8, max_pages_per_seq=MP)
+    lp = H.hswa_pool_create(cfg, None, None)
+    swa = H.Layer(kind=H.HSWA_KIND_SWA, window=W, k_pool=16, v_pool=16)
+    page = hkv * P * d * 2
+
+    def pages(n_bytes, n_seqs):
+        table = -(-n_seqs * MP * 4 // 1024) * 1024
+        return (n_bytes - table) / (2 * page)
+
+    assert pages(H.hswa_prefill_workspace_size(lp, full, 8, 4096), 8) == 8 * MP
+    for q in (1, 64, 65, 4096):
+        per = min(MP, -(-(W - 1 + q) // P) + 1)
+        assert pages(H.hswa_prefill_workspace_size(lp, swa, 8, q), 8) == 8 * per
+    assert H.hswa_prefill_workspace_size(lp, H.Layer(kind=H.HSWA_KIND_SWA, window=0), 8, 64) == 0
+    H.hswa_pool_destroy(lp)

@@ -36,11 +36,11 @@ def seeded_scales(shape, seed):
 
 
 class Fp8Case:
-    def __init__(self, cached, seed, kinds=(FULL, SWA)):
+    def __init__(self, cached, seed, kinds=(FULL, SWA), extra=8):
         B = len(cached)
-        full_pages = sum(math.ceil((L + 8) / P) for L in cached) + 4
-        swa_pages = B * 5 + 80
-        mp = max(math.ceil((L + 8) / P) for L in cached) + 1
+        full_pages = sum(math.ceil((L + extra) / P) for L in cached) + 4
+        swa_pages = B * (5 + math.ceil(extra / P)) + 80
+        mp = max(math.ceil((L + extra) / P) for L in cached) + 1
         self.cfg = H.Config(window=W, page_size=P, n_q_heads=HQ, n_kv_heads=HKV, head_dim=D,
                             dtype=H.HSWA_DTYPE_FP8_E4M3, full_pages=full_pages, swa_pages=swa_pages, max_seqs=B,
                             max_pages_per_seq=mp)
@@ -111,12 +111,86 @@ def test_fp8_append_and_decode_match_oracle(fused):
 
 @pytest.mark.gpu
 def test_fp8_unsupported_calls_say_so():
-    c = Fp8Case([100], seed=72)
+    c = Fp8Case([100], seed=72, kinds=(SWA,))
+    off = torch.tensor([0, 100], dtype=torch.int64, device="cuda")
+    buf = torch.zeros(2 * 100 * HKV * D, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(H.HswaError) as e:
-        q = torch.zeros(1, HQ, D, dtype=torch.bfloat16, device="cuda")
-        c.sess.prefill(0, q, q, torch.zeros(1, dtype=torch.int32, device="cuda"),
-                       torch.tensor([0, 1], dtype=torch.int32, device="cuda"), 1, 1, 0.1)
+        c.sess.gather(0, off, 1, buf)
     assert e.value.status == H.HSWA_ERR_UNSUPPORTED
+    # prefill over an FP8 pool needs the workspace variant
+    q = torch.zeros(1, HQ, D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_prefill_chunk(c.sess.pool, c.sess.layers[0], q, q.clone(), c.sess.bt(0),
+                             torch.zeros(1, dtype=torch.int32, device="cuda"),
+                             torch.tensor([0, 1], dtype=torch.int32, device="cuda"), 1, 1, 1, 0.1)
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    assert c.sess.check() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("swa_first", [False, True])
+def test_fp8_prefill_chunk_matches_oracle(swa_first):
+    """A ragged chunk over FP8 pools: the new tokens are quantized by the
+    append, the staging pass dequantizes every page the chunk reads, and the
+    tensor-core kernel attends; every output row against the oracle."""
+    cached = [0, 5, 63, 64, 127, 128, 129, 700, 3000]
+    chunk = [1, 60, 64, 65, 128, 200, 7, 129, 300]
+    kinds = (SWA, FULL) if swa_first else (FULL, SWA)
+    c = Fp8Case(cached, seed=74 + swa_first, kinds=kinds, extra=max(chunk) + 8)
+    B = c.B
+    fs, ss = c.sess.reserve(range(B), chunk)
+    efs, ess = c.ora.reserve(range(B), chunk)
+    assert np.array_equal(fs, efs) and np.array_equal(ss, ess)
+    c.sess.sync()
+    n_tot = sum(chunk)
+    q_start = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    d_prefix = torch.tensor(cached, dtype=torch.int32, device="cuda")
+    d_qs = torch.as_tensor(q_start, device="cuda")
+    q_seq = np.repeat(np.arange(B), chunk)
+    q_pos = np.concatenate([np.arange(L, L + n) for L, n in zip(cached, chunk)])
+    scale = 1 / math.sqrt(D)
+    for layer, kind in enumerate(c.kinds):
+        slots = fs if kind == FULL else ss
+        q = wl.normal((n_tot, HQ, D), 800 + layer, wl.DTYPE_BF16)
+        kn = wl.normal((n_tot, HKV, D), 810 + layer, wl.DTYPE_BF16) * 2
+        vn = wl.normal((n_tot, HKV, D), 820 + layer, wl.DTYPE_BF16)
+        c.sess.append(layer, kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"))
+        o = torch.full((n_tot, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, max(chunk), scale)
+        assert c.sess.check() == 0
+        assert H.hswa_last_kernel() == "prefill_stage_fp8+prefill_tc_bf16_d128<f16>"
+        kc, ks, vc, vs = c.host[layer]
+        oracle.append_kv_fp8(kc, ks, vc, vs, kn.float().numpy(), vn.float().numpy(), slots)
+        assert np.array_equal(c.sess.k[layer].cpu().numpy(), kc)
+        exp = oracle.attention_fp8(raw_host(q), kc, ks, vc, vs, c.table(layer), q_seq, q_pos,
+                                   0 if kind == FULL else W, scale)
+        got = o.float().cpu().numpy()
+        assert np.isfinite(got).all()
+        err = float(np.abs(got - exp).max())
+        assert err <= 2e-2, (layer, kind, err)
+
+
+@pytest.mark.gpu
+def test_fp8_prefill_rejects_small_workspace():
+    c = Fp8Case([100, 300], seed=76, extra=80)
+    B = c.B
+    c.sess.reserve(range(B), [64, 64])
+    c.ora.reserve(range(B), [64, 64])
+    c.sess.sync()
+    lay = c.sess.layers[0]
+    need = H.hswa_prefill_workspace_size(c.sess.pool, lay, B, 64)
+    assert need > 0
+    assert H.hswa_prefill_workspace_size(c.sess.pool, lay, B, 64) < \
+        H.hswa_prefill_workspace_size(c.sess.pool, lay, B + 1, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    q = torch.zeros(2 * 64, HQ, D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_prefill_chunk_ws(c.sess.pool, lay, q, q.clone(), c.sess.bt(0),
+                                torch.tensor([100, 300], dtype=torch.int32, device="cuda"),
+                                torch.tensor([0, 64, 128], dtype=torch.int32, device="cuda"), B, 128, 64, 0.1,
+                                ws, need - 1)
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    assert c.sess.check() == 0
 
 
 @pytest.mark.gpu
