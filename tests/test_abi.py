@@ -164,7 +164,7 @@ def test_device_calls_validate_before_launching():
 def test_prefill_workspace_sizes():
     """Only FP8 pools need a prefill workspace; an SWA layer stages at most
     ceil((W - 1 + max_q_len) / P) + 1 pages per sequence, a Full layer its
-    whole table row."""
+    whole table row, plus an fp16 copy of n_seqs * max_q_len query rows."""
     cfg, lp, _ = make_pair()
     full = H.Layer(kind=H.HSWA_KIND_FULL, window=0, k_pool=16, v_pool=16)
     assert H.hswa_prefill_workspace_size(lp, full, 4, 4096) == 0
@@ -174,15 +174,16 @@ def test_prefill_workspace_sizes():
                    full_pages=1000, swa_pages=100, max_seqs=8, max_pages_per_seq=MP)
     lp = H.hswa_pool_create(cfg, None, None)
     swa = H.Layer(kind=H.HSWA_KIND_SWA, window=W, k_pool=16, v_pool=16)
-    page = hkv * P * d * 2
+    page = hkv * P * d * 2  # one fp16 K (or V) page copy
 
-    def pages(n_bytes, n_seqs):
+    def pages(n_bytes, n_seqs, max_q):
         table = -(-n_seqs * MP * 4 // 1024) * 1024
-        return (n_bytes - table) / (2 * page)
+        q16 = -(-n_seqs * max_q * 64 * d * 2 // 1024) * 1024  # fp16 copy of the query rows
+        return (n_bytes - table - q16) / (2 * page)
 
-    assert pages(H.hswa_prefill_workspace_size(lp, full, 8, 4096), 8) == 8 * MP
+    assert pages(H.hswa_prefill_workspace_size(lp, full, 8, 4096), 8, 4096) == 8 * MP
     for q in (1, 64, 65, 4096):
         per = min(MP, -(-(W - 1 + q) // P) + 1)
-        assert pages(H.hswa_prefill_workspace_size(lp, swa, 8, q), 8) == 8 * per
+        assert pages(H.hswa_prefill_workspace_size(lp, swa, 8, q), 8, q) == 8 * per
     assert H.hswa_prefill_workspace_size(lp, H.Layer(kind=H.HSWA_KIND_SWA, window=0), 8, 64) == 0
     H.hswa_pool_destroy(lp)
