@@ -21,7 +21,11 @@ Readings where the pages are silent (each listed in the design doc):
   allocation pops from the head in ascending (sequence id, logical page);
   frees are appended in the same ascending order;
 * a page is released when every token on it is older than the last W:
-  (p + 1) * P <= L - W.
+  (p + 1) * P <= L - W;
+* a page may be held by several owners (a sequence's table and the prefix
+  tree, or several sequences sharing a cached prefix): it counts its
+  holders and goes back to the tail of its free list when the last one lets
+  go. Without sharing every count is 1 and the rules above are unchanged.
 """
 from __future__ import annotations
 
@@ -48,6 +52,32 @@ class DualPool:
         self.full_bt = np.full((max_seqs, max_pages_per_seq), -1, np.int32)
         self.swa_bt = np.full((max_seqs, max_pages_per_seq), -1, np.int32)
         self.seq_len = np.zeros(max_seqs, np.int64)
+        self.full_ref = np.zeros(full_pages, np.int64)  # holders of each page
+        self.swa_ref = np.zeros(swa_pages, np.int64)
+
+    # ------------------------------------------------------------ holders
+    def ref_full(self, page):
+        self.full_ref[page] += 1
+
+    def ref_swa(self, page):
+        self.swa_ref[page] += 1
+
+    def unref_full(self, page):
+        """One holder lets go; True if the page went back to the free list."""
+        self.full_ref[page] -= 1
+        assert self.full_ref[page] >= 0
+        if self.full_ref[page] == 0:
+            self.full_free.append(int(page))
+            return True
+        return False
+
+    def unref_swa(self, page):
+        self.swa_ref[page] -= 1
+        assert self.swa_ref[page] >= 0
+        if self.swa_ref[page] == 0:
+            self.swa_free.append(int(page))
+            return True
+        return False
 
     # ------------------------------------------------------------------ a1
     def reserve(self, seq_ids, n_new):
@@ -77,8 +107,10 @@ class DualPool:
             raise NoSpace()
         for s, p in need_full:
             self.full_bt[s, p] = self.full_free.popleft()
+            self.full_ref[self.full_bt[s, p]] = 1
         for s, p in need_swa:
             self.swa_bt[s, p] = self.swa_free.popleft()
+            self.swa_ref[self.swa_bt[s, p]] = 1
         full_slot, swa_slot = [], []
         for s, n in zip(seq_ids, n_new):
             L = int(self.seq_len[s])
@@ -98,9 +130,8 @@ class DualPool:
             L = int(self.seq_len[s])
             for p in range(self.swa_bt.shape[1]):
                 if self.swa_bt[s, p] >= 0 and (p + 1) * self.P <= L - self.W:
-                    self.swa_free.append(int(self.swa_bt[s, p]))
+                    freed += self.unref_swa(int(self.swa_bt[s, p]))
                     self.swa_bt[s, p] = -1
-                    freed += 1
         return freed
 
     def seq_free(self, seq_ids):
@@ -108,11 +139,11 @@ class DualPool:
         for s in sorted(int(x) for x in seq_ids):
             for p in range(self.full_bt.shape[1]):
                 if self.full_bt[s, p] >= 0:
-                    self.full_free.append(int(self.full_bt[s, p]))
+                    self.unref_full(int(self.full_bt[s, p]))
                     self.full_bt[s, p] = -1
             for p in range(self.swa_bt.shape[1]):
                 if self.swa_bt[s, p] >= 0:
-                    self.swa_free.append(int(self.swa_bt[s, p]))
+                    self.unref_swa(int(self.swa_bt[s, p]))
                     self.swa_bt[s, p] = -1
             self.seq_len[s] = 0
 
@@ -122,9 +153,8 @@ class DualPool:
         for s in sorted(int(x) for x in seq_ids):
             for p in range(self.swa_bt.shape[1]):
                 if self.swa_bt[s, p] >= 0:
-                    self.swa_free.append(int(self.swa_bt[s, p]))
+                    freed += self.unref_swa(int(self.swa_bt[s, p]))
                     self.swa_bt[s, p] = -1
-                    freed += 1
         return freed
 
     def swa_restore(self, seq_ids):
@@ -143,7 +173,37 @@ class DualPool:
             raise NoSpace()
         for s, p in need:
             self.swa_bt[s, p] = self.swa_free.popleft()
+            self.swa_ref[self.swa_bt[s, p]] = 1
         return len(need)
+
+    # ------------------------------------------------------ shared prefix
+    def share_prefix(self, s, full_pages, swa_pages):
+        """Start empty sequence s on a cached prefix of n = len(full_pages)
+        whole pages (MiMo Sec. 2.1, SWA-aware prefix cache tree: a hit reuses
+        the Full segment and the SWA window). The sequence holds every Full
+        page and the SWA pages of the logical pages that meet the last W
+        positions [n*P - W, n*P); each must be held already (by the tree).
+        Its length becomes n*P."""
+        s = int(s)
+        n = len(full_pages)
+        if self.seq_len[s] != 0 or (self.full_bt[s] >= 0).any() or (self.swa_bt[s] >= 0).any():
+            raise ValueError("sequence not empty")
+        if n > self.full_bt.shape[1]:
+            raise ValueError("prefix exceeds max_pages_per_seq")
+        first = max(0, n * self.P - self.W) // self.P
+        for p in range(n):
+            if not (0 <= full_pages[p] < self.full_pages) or self.full_ref[full_pages[p]] == 0:
+                raise ValueError("Full page not held")
+        for p in range(first, n):
+            if not (0 <= swa_pages[p] < self.swa_pages) or self.swa_ref[swa_pages[p]] == 0:
+                raise ValueError("SWA window page not held")
+        for p in range(n):
+            self.full_bt[s, p] = full_pages[p]
+            self.ref_full(int(full_pages[p]))
+        for p in range(first, n):
+            self.swa_bt[s, p] = swa_pages[p]
+            self.ref_swa(int(swa_pages[p]))
+        self.seq_len[s] = n * self.P
 
     # ------------------------------------------------------------ queries
     def live_swa_pages(self, s):
