@@ -967,6 +967,14 @@ def run_decode(args, world, rank, local):
                            "step_ms_layerwise_direct": round(h["reload"]["step_ms_direct"], 3),
                            "step_ms_layerwise_staged": round(h["reload"]["step_ms_staged"], 3)},
             "note": "the 10 Full layers read one physical 64 GiB Full pool"}
+    if not args.no_tree:
+        pt = measure_prefix_tree()
+        line["prefix_tree"] = {
+            "workload": "64 requests sharing a 16384-token system prompt + 4096 own tokens each, W 128, P 64; "
+                        "stored at their end, then a follow-up turn each (host bookkeeping)",
+            "unit": "us per call (median)", "match_us": round(pt["match"], 1), "share_us": round(pt["share"], 1),
+            "insert_us": round(pt["insert"], 1), "evict_64_pages_us": round(pt["evict"], 1),
+            "follow_up_full_hits": "%d/%d" % (pt["follow_up_hits"], pt["requests"])}
     if not args.no_transfer:
         t = measure_transfer(3)
         line["swa_transfer"] = {
@@ -1119,6 +1127,68 @@ def measure_hybrid70(steps, warmup, n_seqs=None):
     return out
 
 
+def measure_prefix_tree(n_req=64, prompt=16384, turn=4096, reps=3):
+    """Host cost of the SWA-aware prefix cache tree (bookkeeping only, no
+    device memory): n_req requests share a prompt-token system prompt, each
+    adds turn tokens of its own, runs as a chunked prefill (4096-token chunks,
+    release after each) and is stored at its end; then every request comes
+    back for a follow-up turn (match, share the hit). Each chunk's prefix is
+    stored right after the chunk's release, so the tree keeps the SWA window
+    of every chunk end (the system prompt's end among them). Returns
+    microseconds per call of match, share, insert, and of an eviction that
+    frees 64 pages of each kind."""
+    import hybrid_sliding_window_dual_gb300 as H
+    W, P = 128, 64
+    pages_per = (prompt + 2 * turn) // P + 2
+    full = n_req * ((turn * 2) // P + 2) + prompt // P + 64
+    swa = n_req * 16 + 64  # the tree keeps the window of every chunk end
+    cfg = H.Config(window=W, page_size=P, n_q_heads=64, n_kv_heads=8, head_dim=128, dtype=H.HSWA_DTYPE_BF16,
+                   full_pages=full, swa_pages=swa, max_seqs=n_req, max_pages_per_seq=pages_per)
+    rng = np.random.default_rng(6)
+    system = rng.integers(0, 32000, prompt).tolist()
+    reqs = [np.array(system + rng.integers(0, 32000, turn).tolist(), np.int32) for _ in range(n_req)]
+    t = {"match": [], "share": [], "insert": [], "evict": []}
+    for _ in range(reps):
+        pool = H.hswa_pool_create(cfg)
+        tree = H.hswa_tree_create(pool)
+        for s, toks in enumerate(reqs):
+            t0 = time.perf_counter()
+            m, fp, sp, raw = H.hswa_tree_match(tree, toks, pages_per)
+            t1 = time.perf_counter()
+            if m:
+                H.hswa_seq_share_prefix(pool, s, fp, sp)
+            t2 = time.perf_counter()
+            t["match"].append(t1 - t0)
+            if m:
+                t["share"].append(t2 - t1)
+            L = m * P
+            while L < len(toks):  # prefill chunks: release, then store the prefix
+                n = min(4096, len(toks) - L)
+                H.hswa_reserve(pool, [s], [n])
+                L += n
+                H.hswa_swa_release(pool, [s])
+                t0 = time.perf_counter()
+                H.hswa_tree_insert(tree, s, toks[:L])
+                t["insert"].append(time.perf_counter() - t0)
+            H.hswa_seq_free(pool, [s])
+        hits = 0
+        for s, toks in enumerate(reqs):  # follow-up turns
+            follow = np.concatenate([toks, np.ones(100, np.int32)])
+            t0 = time.perf_counter()
+            m, fp, sp, raw = H.hswa_tree_match(tree, follow, pages_per)
+            t["match"].append(time.perf_counter() - t0)
+            hits += m == len(toks) // P
+        t0 = time.perf_counter()
+        H.hswa_tree_evict(tree, 64, 64)
+        t["evict"].append(time.perf_counter() - t0)
+        H.hswa_tree_destroy(tree)
+        H.hswa_pool_destroy(pool)
+    out = {k: float(np.median(v)) * 1e6 for k, v in t.items()}
+    out["follow_up_hits"] = hits
+    out["requests"] = n_req
+    return out
+
+
 def measure_transfer(steps):
     import torch
     w = wl.swa_transfer()
@@ -1225,6 +1295,7 @@ def main():
     ap.add_argument("--no-multi", action="store_true")
     ap.add_argument("--no-hybrid70", action="store_true")
     ap.add_argument("--no-transfer", action="store_true")
+    ap.add_argument("--no-tree", action="store_true")
     ap.add_argument("--hybrid-steps", type=int, default=5)
     ap.add_argument("--breakdown", action="store_true", help="per-call device times of the decode step")
     ap.add_argument("--prefill-steps", type=int, default=5)

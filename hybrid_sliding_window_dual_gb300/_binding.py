@@ -65,6 +65,15 @@ _SIG = {
     "hswa_swa_restore": (_I, [_P, _I, _P, _P]),
     "hswa_get_tables": (_I, [_P, _P, _P, _P]),
     "hswa_get_free_list": (_I, [_P, _I, _P, ctypes.c_int32, _P]),
+    "hswa_seq_share_prefix": (_I, [_P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "hswa_get_page_refs": (_I, [_P, _I, _P, ctypes.c_int32]),
+    "hswa_tree_create": (_I, [_P, ctypes.POINTER(_P)]),
+    "hswa_tree_destroy": (_I, [_P]),
+    "hswa_tree_match": (_I, [_P, _P, ctypes.c_int64, _P, _P, ctypes.c_int32, _P, _P]),
+    "hswa_tree_insert": (_I, [_P, ctypes.c_int32, _P, ctypes.c_int64, _P]),
+    "hswa_tree_evict": (_I, [_P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "hswa_tree_stats": (_I, [_P, _P, _P, _P]),
+    "hswa_tree_nodes": (_I, [_P, _P, ctypes.c_int32, _P]),
     "hswa_sync_tables": (_I, [_P, _P, _P, _P, _P]),
     "hswa_append_kv": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P]),
     "hswa_decode_workspace_size": (ctypes.c_size_t, [_P, _I]),
@@ -204,6 +213,69 @@ def hswa_get_free_list(pool, kind):
     out = np.empty(count.value, np.int32)
     _check(lib.hswa_get_free_list(pool, kind, _ptr(out), count.value, ctypes.addressof(count)),
            "hswa_get_free_list")
+    return out
+
+
+# ------------------------------------------------------ prefix tree
+def hswa_seq_share_prefix(pool, seq_id, full_pages, swa_pages):
+    f, w = _i32(full_pages), _i32(swa_pages)
+    _check(lib.hswa_seq_share_prefix(pool, int(seq_id), len(f), _ptr(f), _ptr(w)), "hswa_seq_share_prefix")
+
+
+def hswa_get_page_refs(pool, kind, n_pages):
+    out = np.empty(int(n_pages), np.int32)
+    _check(lib.hswa_get_page_refs(pool, kind, _ptr(out), len(out)), "hswa_get_page_refs")
+    return out
+
+
+def hswa_tree_create(pool):
+    out = ctypes.c_void_p()
+    _check(lib.hswa_tree_create(pool, ctypes.byref(out)), "hswa_tree_create")
+    return out.value
+
+
+def hswa_tree_destroy(tree):
+    _check(lib.hswa_tree_destroy(tree), "hswa_tree_destroy")
+
+
+def hswa_tree_match(tree, tokens, cap_pages):
+    """(m, full_pages[:m], swa_pages[:m], raw_pages)."""
+    t = _i32(tokens)
+    full = np.empty(max(int(cap_pages), 0), np.int32)
+    swa = np.empty_like(full)
+    m, raw = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.hswa_tree_match(tree, _ptr(t), len(t), _ptr(full), _ptr(swa), len(full), ctypes.addressof(m),
+                               ctypes.addressof(raw)), "hswa_tree_match")
+    return m.value, full[:m.value].copy(), swa[:m.value].copy(), raw.value
+
+
+def hswa_tree_insert(tree, seq_id, tokens):
+    t = _i32(tokens)
+    n = ctypes.c_int32()
+    _check(lib.hswa_tree_insert(tree, int(seq_id), _ptr(t), len(t), ctypes.addressof(n)), "hswa_tree_insert")
+    return n.value
+
+
+def hswa_tree_evict(tree, want_full, want_swa):
+    ff, fs = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.hswa_tree_evict(tree, int(want_full), int(want_swa), ctypes.addressof(ff), ctypes.addressof(fs)),
+           "hswa_tree_evict")
+    return ff.value, fs.value
+
+
+def hswa_tree_stats(tree):
+    a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.hswa_tree_stats(tree, ctypes.addressof(a), ctypes.addressof(b), ctypes.addressof(c)),
+           "hswa_tree_stats")
+    return a.value, b.value, c.value
+
+
+def hswa_tree_nodes(tree):
+    """[n_nodes, 5] int32: id, parent id (-1 = root), logical page, Full page, SWA page."""
+    count = ctypes.c_int32()
+    _check(lib.hswa_tree_nodes(tree, None, 0, ctypes.addressof(count)), "hswa_tree_nodes")
+    out = np.empty((count.value, 5), np.int32)
+    _check(lib.hswa_tree_nodes(tree, _ptr(out), out.size, ctypes.addressof(count)), "hswa_tree_nodes")
     return out
 
 

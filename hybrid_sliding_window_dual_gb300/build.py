@@ -22,7 +22,7 @@ LIB = os.path.join(OUT_DIR, "libhswa.so")
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 
-SOURCES = ["runtime.cu", "decode.cu", "prefill.cu", "copy.cu", "pool.cpp"]
+SOURCES = ["runtime.cu", "decode.cu", "prefill.cu", "copy.cu", "pool.cpp", "tree.cpp"]
 HEADERS = ["common.cuh", "internal.h", "kernels.h"]
 
 FLAGS = [

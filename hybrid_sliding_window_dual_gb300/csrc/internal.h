@@ -37,6 +37,34 @@ struct hswa_pool {
     PageQueue full_free, swa_free;
     std::vector<int32_t> full_bt, swa_bt;  // [max_seqs][max_pages_per_seq]
     std::vector<int32_t> seq_len;          // [max_seqs]
+    // holders of each page (sequence tables and prefix-tree nodes); a page
+    // is on its free list exactly when its count is 0
+    std::vector<int32_t> full_ref, swa_ref;
+    int32_t trees = 0;  // prefix trees bound to this pool
+
+    void ref_full(int32_t page) { ++full_ref[page]; }
+    void ref_swa(int32_t page) { ++swa_ref[page]; }
+    // one holder lets go; true if the page went back to the free list
+    bool unref_full(int32_t page) {
+        if (--full_ref[page] > 0) return false;
+        full_free.push(page);
+        return true;
+    }
+    bool unref_swa(int32_t page) {
+        if (--swa_ref[page] > 0) return false;
+        swa_free.push(page);
+        return true;
+    }
+    int32_t take_full() {
+        const int32_t page = full_free.pop();
+        full_ref[page] = 1;
+        return page;
+    }
+    int32_t take_swa() {
+        const int32_t page = swa_free.pop();
+        swa_ref[page] = 1;
+        return page;
+    }
 
     // Entries changed since the last hswa_sync_tables, as flat indices into
     // the concatenation [full_bt | swa_bt | seq_len]; each index listed once.

@@ -10,7 +10,9 @@
 //
 // Free lists are FIFO queues; pages are taken from the head and returned to
 // the tail, always in ascending (sequence id, logical page) order, so that
-// the tables are a deterministic function of the call sequence.
+// the tables are a deterministic function of the call sequence. A page can
+// have several holders (sequence tables and prefix-tree nodes, which share
+// cached prefixes); it returns to its free list when the last one lets go.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -68,13 +70,15 @@ extern "C" int hswa_pool_create(const hswa_config *cfg, const int32_t *full_free
     p->full_bt.assign(entries, -1);
     p->swa_bt.assign(entries, -1);
     p->seq_len.assign(cfg->max_seqs, 0);
+    p->full_ref.assign(cfg->full_pages, 0);
+    p->swa_ref.assign(cfg->swa_pages, 0);
     p->dirty_flag.assign(2 * entries + cfg->max_seqs, 0);
     *out = p;
     return HSWA_OK;
 }
 
 extern "C" int hswa_pool_destroy(hswa_pool *pool) {
-    if (!pool) return HSWA_ERR_INVALID_ARG;
+    if (!pool || pool->trees > 0) return HSWA_ERR_INVALID_ARG;  // destroy its prefix trees first
     hswa_pool_release_device(pool);
     delete pool;
     return HSWA_OK;
@@ -109,8 +113,8 @@ extern "C" int hswa_reserve(hswa_pool *pool, int n, const int32_t *seq_ids, cons
         const int64_t L = pool->seq_len[s];
         if (n_new[i] == 0) continue;
         for (int64_t p = L / P; p <= (L + n_new[i] - 1) / P; ++p) {
-            if (pool->full_bt[(int64_t)s * MP + p] < 0) pool->set_full(s, (int32_t)p, pool->full_free.pop());
-            if (pool->swa_bt[(int64_t)s * MP + p] < 0) pool->set_swa(s, (int32_t)p, pool->swa_free.pop());
+            if (pool->full_bt[(int64_t)s * MP + p] < 0) pool->set_full(s, (int32_t)p, pool->take_full());
+            if (pool->swa_bt[(int64_t)s * MP + p] < 0) pool->set_swa(s, (int32_t)p, pool->take_swa());
         }
         for (int64_t t = L; t < L + n_new[i]; ++t, ++out) {
             if (full_slot_out)
@@ -135,9 +139,8 @@ extern "C" int hswa_swa_release(hswa_pool *pool, int n, const int32_t *seq_ids, 
         for (int64_t p = 0; p < n_old && p < MP; ++p) {
             const int32_t page = pool->swa_bt[s * MP + p];
             if (page < 0) continue;
-            pool->swa_free.push(page);
+            freed += pool->unref_swa(page);
             pool->set_swa(s, (int32_t)p, -1);
-            ++freed;
         }
     }
     if (n_freed_out) *n_freed_out = freed;
@@ -152,14 +155,14 @@ extern "C" int hswa_seq_free(hswa_pool *pool, int n, const int32_t *seq_ids) {
         for (int64_t p = 0; p < MP; ++p) {
             const int32_t page = pool->full_bt[s * MP + p];
             if (page >= 0) {
-                pool->full_free.push(page);
+                pool->unref_full(page);
                 pool->set_full(s, (int32_t)p, -1);
             }
         }
         for (int64_t p = 0; p < MP; ++p) {
             const int32_t page = pool->swa_bt[s * MP + p];
             if (page >= 0) {
-                pool->swa_free.push(page);
+                pool->unref_swa(page);
                 pool->set_swa(s, (int32_t)p, -1);
             }
         }
@@ -177,9 +180,8 @@ extern "C" int hswa_swa_drop(hswa_pool *pool, int n, const int32_t *seq_ids, int
         for (int64_t p = 0; p < MP; ++p) {
             const int32_t page = pool->swa_bt[s * MP + p];
             if (page < 0) continue;
-            pool->swa_free.push(page);
+            freed += pool->unref_swa(page);
             pool->set_swa(s, (int32_t)p, -1);
-            ++freed;
         }
     }
     if (n_freed_out) *n_freed_out = freed;
@@ -201,9 +203,46 @@ extern "C" int hswa_swa_restore(hswa_pool *pool, int n, const int32_t *seq_ids, 
         const int64_t L = pool->seq_len[s], nw = std::min(L, W);
         if (nw == 0) continue;
         for (int64_t p = (L - nw) / P; p <= (L - 1) / P; ++p)
-            if (pool->swa_bt[s * MP + p] < 0) pool->set_swa(s, (int32_t)p, pool->swa_free.pop());
+            if (pool->swa_bt[s * MP + p] < 0) pool->set_swa(s, (int32_t)p, pool->take_swa());
     }
     if (n_alloc_out) *n_alloc_out = (int32_t)need;
+    return HSWA_OK;
+}
+
+extern "C" int hswa_seq_share_prefix(hswa_pool *pool, int32_t seq_id, int32_t n_pages, const int32_t *full_pages,
+                                     const int32_t *swa_pages) {
+    if (!pool || seq_id < 0 || seq_id >= pool->cfg.max_seqs || n_pages < 0 ||
+        n_pages > pool->cfg.max_pages_per_seq || (n_pages > 0 && (!full_pages || !swa_pages)))
+        return HSWA_ERR_INVALID_ARG;
+    const int64_t P = pool->cfg.page_size, W = pool->cfg.window, MP = pool->cfg.max_pages_per_seq;
+    if (pool->seq_len[seq_id] != 0) return HSWA_ERR_INVALID_ARG;
+    for (int64_t p = 0; p < MP; ++p)
+        if (pool->full_bt[seq_id * MP + p] >= 0 || pool->swa_bt[seq_id * MP + p] >= 0) return HSWA_ERR_INVALID_ARG;
+    // logical pages meeting the last W positions [n*P - W, n*P) of the prefix
+    const int64_t first = std::max<int64_t>(0, n_pages * P - W) / P;
+    for (int32_t p = 0; p < n_pages; ++p)
+        if (full_pages[p] < 0 || full_pages[p] >= pool->cfg.full_pages || pool->full_ref[full_pages[p]] == 0)
+            return HSWA_ERR_INVALID_ARG;
+    for (int64_t p = first; p < n_pages; ++p)
+        if (swa_pages[p] < 0 || swa_pages[p] >= pool->cfg.swa_pages || pool->swa_ref[swa_pages[p]] == 0)
+            return HSWA_ERR_INVALID_ARG;
+    for (int32_t p = 0; p < n_pages; ++p) {
+        pool->set_full(seq_id, p, full_pages[p]);
+        pool->ref_full(full_pages[p]);
+    }
+    for (int64_t p = first; p < n_pages; ++p) {
+        pool->set_swa(seq_id, (int32_t)p, swa_pages[p]);
+        pool->ref_swa(swa_pages[p]);
+    }
+    pool->set_len(seq_id, (int32_t)(n_pages * P));
+    return HSWA_OK;
+}
+
+extern "C" int hswa_get_page_refs(const hswa_pool *pool, int kind, int32_t *out, int32_t cap) {
+    if (!pool || (kind != HSWA_KIND_FULL && kind != HSWA_KIND_SWA) || cap < 0 || (cap > 0 && !out))
+        return HSWA_ERR_INVALID_ARG;
+    const std::vector<int32_t> &r = kind == HSWA_KIND_FULL ? pool->full_ref : pool->swa_ref;
+    for (int64_t i = 0; i < (int64_t)r.size() && i < cap; ++i) out[i] = r[i];
     return HSWA_OK;
 }
 

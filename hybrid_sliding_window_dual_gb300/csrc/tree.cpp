@@ -1,0 +1,285 @@
+// SWA-aware prefix cache tree on the host.
+//
+// "MiMo-V2.5 Series Inference Full-Link Optimization", Sec. 2.1, SWA-aware
+// prefix cache tree: with an SWA pool that drops out-of-window slots, equal
+// tokens no longer mean reusable KV. The tree
+//   1. trims a match to the window-safety length: the last W positions of
+//      the matched prefix must still have SWA slots; past that is a miss;
+//   2. (its pages are released with the request lifecycle by the pool);
+//   3. keeps two indexes per node, a Full page and an SWA page, evicted
+//      apart: out-of-window SWA pages alone (the Full prefix stays reusable)
+//      or whole nodes.
+//
+// One node per page of P tokens. The tree holds one reference on every page
+// it stores; a page goes back to its pool's free list when no sequence and
+// no node holds it. Every choice is deterministic (a logical clock advanced
+// by each match and insert, then creation order), so the tree and the pool
+// tables are a function of the call sequence.
+#include <algorithm>
+#include <map>
+#include <new>
+#include <queue>
+#include <tuple>
+#include <unordered_map>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+struct TreeNode {
+    int32_t id = -1;     // creation order (a child is always newer than its parent)
+    int32_t index = -1;  // logical page index of the page in its sequences
+    int32_t full = -1, swa = -1;
+    uint64_t last = 0;   // clock of the last match or insert through the node
+    TreeNode *parent = nullptr;
+    std::vector<int32_t> tokens;  // the page's P tokens
+    uint64_t hash = 0;            // of tokens
+    std::unordered_multimap<uint64_t, TreeNode *> children;  // by token hash
+};
+
+// 64-bit hash of a page's tokens (FNV-1a over the 32-bit values, then a
+// final mix); equal hashes are confirmed by comparing the tokens.
+uint64_t page_hash(const int32_t *t, int64_t n) {
+    uint64_t h = 1469598103934665603ull;
+    for (int64_t i = 0; i < n; ++i) {
+        h ^= (uint32_t)t[i];
+        h *= 1099511628211ull;
+    }
+    h ^= h >> 33;
+    h *= 0xff51afd7ed558ccdull;
+    h ^= h >> 33;
+    return h;
+}
+
+TreeNode *find_child(TreeNode *node, const int32_t *t, int64_t n, uint64_t h) {
+    auto range = node->children.equal_range(h);
+    for (auto it = range.first; it != range.second; ++it)
+        if (std::equal(t, t + n, it->second->tokens.begin())) return it->second;
+    return nullptr;
+}
+
+}  // namespace
+
+struct hswa_tree {
+    hswa_pool *pool = nullptr;
+    TreeNode root;
+    uint64_t clock = 0;
+    int32_t next_id = 0;
+    std::map<int32_t, TreeNode *> nodes;  // every node but the root, by id
+};
+
+namespace {
+
+// Largest m <= n with an SWA page on every logical page that meets the last
+// W positions [m*P - W, m*P) of an m-page prefix.
+int32_t window_safe_pages(const std::vector<TreeNode *> &path, int64_t P, int64_t W) {
+    const int32_t n = (int32_t)path.size();
+    // missing[p]: pages without an SWA page among the first p, for O(1) range checks
+    std::vector<int32_t> missing(n + 1, 0);
+    for (int32_t p = 0; p < n; ++p) missing[p + 1] = missing[p] + (path[p]->swa < 0);
+    for (int32_t m = n; m > 0; --m) {
+        const int64_t first = std::max<int64_t>(0, m * P - W) / P;
+        if (missing[m] - missing[first] == 0) return m;
+    }
+    return 0;
+}
+
+void remove_node(hswa_tree *t, TreeNode *nd) {
+    auto range = nd->parent->children.equal_range(nd->hash);
+    for (auto it = range.first; it != range.second; ++it)
+        if (it->second == nd) {
+            nd->parent->children.erase(it);
+            break;
+        }
+    t->nodes.erase(nd->id);
+    delete nd;
+}
+
+}  // namespace
+
+extern "C" int hswa_tree_create(hswa_pool *pool, hswa_tree **out) {
+    if (!pool || !out) return HSWA_ERR_INVALID_ARG;
+    hswa_tree *t = new (std::nothrow) hswa_tree();
+    if (!t) return HSWA_ERR_INVALID_ARG;
+    t->pool = pool;
+    ++pool->trees;
+    *out = t;
+    return HSWA_OK;
+}
+
+extern "C" int hswa_tree_destroy(hswa_tree *t) {
+    if (!t) return HSWA_ERR_INVALID_ARG;
+    // let go of every page, nodes in creation order, Full page before SWA page
+    for (auto &kv : t->nodes) {
+        t->pool->unref_full(kv.second->full);
+        if (kv.second->swa >= 0) t->pool->unref_swa(kv.second->swa);
+    }
+    for (auto &kv : t->nodes) delete kv.second;
+    --t->pool->trees;
+    delete t;
+    return HSWA_OK;
+}
+
+extern "C" int hswa_tree_match(hswa_tree *t, const int32_t *tokens, int64_t n_tokens, int32_t *full_pages_out,
+                               int32_t *swa_pages_out, int32_t cap_pages, int32_t *n_pages_out,
+                               int32_t *raw_pages_out) {
+    if (!t || n_tokens < 0 || (n_tokens > 0 && !tokens) || cap_pages < 0) return HSWA_ERR_INVALID_ARG;
+    const int64_t P = t->pool->cfg.page_size, W = t->pool->cfg.window;
+    const int64_t n_pages = n_tokens / P;
+    if (cap_pages < std::min<int64_t>(n_pages, t->pool->cfg.max_pages_per_seq) ||
+        (cap_pages > 0 && (!full_pages_out || !swa_pages_out)))
+        return HSWA_ERR_INVALID_ARG;
+    ++t->clock;
+    std::vector<TreeNode *> path;
+    TreeNode *node = &t->root;
+    for (int64_t p = 0; p < n_pages; ++p) {
+        const int32_t *pt = tokens + p * P;
+        node = find_child(node, pt, P, page_hash(pt, P));
+        if (!node) break;
+        path.push_back(node);
+    }
+    for (TreeNode *nd : path) nd->last = t->clock;
+    const int32_t m = window_safe_pages(path, P, W);
+    for (int32_t p = 0; p < m; ++p) {
+        full_pages_out[p] = path[p]->full;
+        swa_pages_out[p] = path[p]->swa;
+    }
+    if (n_pages_out) *n_pages_out = m;
+    if (raw_pages_out) *raw_pages_out = (int32_t)path.size();
+    return HSWA_OK;
+}
+
+extern "C" int hswa_tree_insert(hswa_tree *t, int32_t seq_id, const int32_t *tokens, int64_t n_tokens,
+                                int32_t *n_new_out) {
+    if (!t || n_tokens < 0 || (n_tokens > 0 && !tokens)) return HSWA_ERR_INVALID_ARG;
+    hswa_pool *pool = t->pool;
+    if (seq_id < 0 || seq_id >= pool->cfg.max_seqs || n_tokens > pool->seq_len[seq_id]) return HSWA_ERR_INVALID_ARG;
+    const int64_t P = pool->cfg.page_size, MP = pool->cfg.max_pages_per_seq;
+    const int64_t n_pages = n_tokens / P;
+    const int32_t *frow = &pool->full_bt[(int64_t)seq_id * MP];
+    const int32_t *srow = &pool->swa_bt[(int64_t)seq_id * MP];
+    for (int64_t p = 0; p < n_pages; ++p)
+        if (frow[p] < 0) return HSWA_ERR_INVALID_ARG;
+    ++t->clock;
+    TreeNode *node = &t->root;
+    int32_t created = 0;
+    for (int64_t p = 0; p < n_pages; ++p) {
+        const int32_t *pt = tokens + p * P;
+        const uint64_t h = page_hash(pt, P);
+        TreeNode *nxt = find_child(node, pt, P, h);
+        if (!nxt) {
+            nxt = new TreeNode();
+            nxt->id = t->next_id++;
+            nxt->index = (int32_t)p;
+            nxt->full = frow[p];
+            nxt->swa = srow[p];
+            nxt->parent = node;
+            nxt->tokens.assign(pt, pt + P);
+            nxt->hash = h;
+            pool->ref_full(nxt->full);
+            if (nxt->swa >= 0) pool->ref_swa(nxt->swa);
+            node->children.emplace(h, nxt);
+            t->nodes.emplace(nxt->id, nxt);
+            ++created;
+        } else {
+            if (nxt->swa < 0 && srow[p] >= 0) {  // the sequence recomputed a lost window page
+                nxt->swa = srow[p];
+                pool->ref_swa(nxt->swa);
+            }
+        }
+        nxt->last = t->clock;
+        node = nxt;
+    }
+    if (n_new_out) *n_new_out = created;
+    return HSWA_OK;
+}
+
+extern "C" int hswa_tree_evict(hswa_tree *t, int32_t want_full, int32_t want_swa, int32_t *freed_full_out,
+                               int32_t *freed_swa_out) {
+    if (!t || want_full < 0 || want_swa < 0) return HSWA_ERR_INVALID_ARG;
+    hswa_pool *pool = t->pool;
+    const int64_t P = pool->cfg.page_size, W = pool->cfg.window;
+    int32_t freed_full = 0, freed_swa = 0;
+    if (want_swa > 0) {
+        // pages of the shallowest leaf at or below each node; children are
+        // newer than their parents, so descending ids visit children first
+        std::vector<int64_t> dmin(t->next_id, INT64_MAX);
+        for (auto it = t->nodes.rbegin(); it != t->nodes.rend(); ++it) {
+            TreeNode *nd = it->second;
+            int64_t d = nd->children.empty() ? (int64_t)nd->index + 1 : INT64_MAX;
+            for (auto &ch : nd->children) d = std::min(d, dmin[ch.second->id]);
+            dmin[nd->id] = d;
+        }
+        // SWA pages only the tree holds: outside every window below them
+        // first, then inside; oldest first, then creation order
+        std::vector<std::tuple<int, uint64_t, int32_t, TreeNode *>> cands;
+        for (auto &kv : t->nodes) {
+            TreeNode *nd = kv.second;
+            if (nd->swa < 0 || pool->swa_ref[nd->swa] != 1) continue;
+            const bool in_window = nd->index >= std::max<int64_t>(0, dmin[nd->id] * P - W) / P;
+            cands.emplace_back(in_window ? 1 : 0, nd->last, nd->id, nd);
+        }
+        std::sort(cands.begin(), cands.end(), [](const auto &a, const auto &b) {
+            return std::make_tuple(std::get<0>(a), std::get<1>(a), std::get<2>(a)) <
+                   std::make_tuple(std::get<0>(b), std::get<1>(b), std::get<2>(b));
+        });
+        for (auto &c : cands) {
+            if (freed_swa >= want_swa) break;
+            TreeNode *nd = std::get<3>(c);
+            freed_swa += pool->unref_swa(nd->swa);
+            nd->swa = -1;
+        }
+    }
+    if (want_full > 0) {
+        // leaves whose Full page only the tree holds, oldest first; a parent
+        // left without children joins the candidates
+        using Key = std::pair<uint64_t, int32_t>;
+        std::priority_queue<Key, std::vector<Key>, std::greater<Key>> heap;
+        auto evictable = [&](TreeNode *nd) { return nd->children.empty() && pool->full_ref[nd->full] == 1; };
+        for (auto &kv : t->nodes)
+            if (evictable(kv.second)) heap.emplace(kv.second->last, kv.second->id);
+        while (freed_full < want_full && !heap.empty()) {
+            TreeNode *nd = t->nodes.at(heap.top().second);
+            heap.pop();
+            TreeNode *parent = nd->parent;
+            freed_full += pool->unref_full(nd->full);
+            if (nd->swa >= 0) freed_swa += pool->unref_swa(nd->swa);
+            remove_node(t, nd);
+            if (parent != &t->root && evictable(parent)) heap.emplace(parent->last, parent->id);
+        }
+    }
+    if (freed_full_out) *freed_full_out = freed_full;
+    if (freed_swa_out) *freed_swa_out = freed_swa;
+    return HSWA_OK;
+}
+
+extern "C" int hswa_tree_stats(const hswa_tree *t, int32_t *n_nodes, int32_t *full_held, int32_t *swa_held) {
+    if (!t) return HSWA_ERR_INVALID_ARG;
+    int32_t swa = 0;
+    for (auto &kv : t->nodes) swa += kv.second->swa >= 0;
+    if (n_nodes) *n_nodes = (int32_t)t->nodes.size();
+    if (full_held) *full_held = (int32_t)t->nodes.size();
+    if (swa_held) *swa_held = swa;
+    return HSWA_OK;
+}
+
+extern "C" int hswa_tree_nodes(const hswa_tree *t, int32_t *out, int32_t cap, int32_t *count) {
+    if (!t || cap < 0 || (cap > 0 && !out)) return HSWA_ERR_INVALID_ARG;
+    // per node, in creation order: id, parent id (-1 = root), logical page, Full page, SWA page
+    int32_t i = 0;
+    for (auto &kv : t->nodes) {
+        const TreeNode *nd = kv.second;
+        if ((int64_t)(i + 1) * 5 <= cap) {
+            int32_t *r = out + (int64_t)i * 5;
+            r[0] = nd->id;
+            r[1] = nd->parent == &t->root ? -1 : nd->parent->id;
+            r[2] = nd->index;
+            r[3] = nd->full;
+            r[4] = nd->swa;
+        }
+        ++i;
+    }
+    if (count) *count = i;
+    return HSWA_OK;
+}

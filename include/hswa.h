@@ -147,19 +147,23 @@ int hswa_reserve(hswa_pool *pool, int n, const int32_t *seq_ids, const int32_t *
 /* Release out-of-window SWA pages (Sec. 2.1, SWA-aware prefix cache tree:
  * release after each prefill chunk, at request end and every N decode
  * tokens; keep at least the last W tokens). For each listed sequence of
- * length L, every SWA page on logical page p with (p + 1) * P <= L - W goes
- * to the tail of the SWA free list, in ascending (sequence, page) order, and
- * its entry becomes -1. seq_ids need not be sorted (they are processed in
- * ascending order). *n_freed_out (may be NULL) gets the count. */
+ * length L, every SWA page on logical page p with (p + 1) * P <= L - W is
+ * let go and its entry becomes -1; a page no one else holds (see Page
+ * holders below) goes to the tail of the SWA free list, in ascending
+ * (sequence, page) order. seq_ids need not be sorted (they are processed in
+ * ascending order). *n_freed_out (may be NULL) gets the number of pages
+ * that went back to the free list. */
 int hswa_swa_release(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_freed_out);
 
-/* Request end: return all Full and SWA pages of the sequences (ascending
- * sequence, then page) and set their lengths to 0. */
+/* Request end: let go of all Full and SWA pages of the sequences
+ * (ascending sequence, then page; pages no one else holds return to the
+ * free lists) and set their lengths to 0. */
 int hswa_seq_free(hswa_pool *pool, int n, const int32_t *seq_ids);
 
 /* Evict the SWA segment of each sequence alone, keeping its Full pages
  * (Sec. 2.1: the out-of-window SWA segment can be evicted while the Full
- * segment stays). Used after hswa_swa_gather has copied the window out. */
+ * segment stays). Used after hswa_swa_gather has copied the window out.
+ * *n_freed_out counts the pages that went back to the free list. */
 int hswa_swa_drop(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_freed_out);
 
 /* Give SWA pages to every in-window logical page (positions
@@ -176,6 +180,89 @@ int hswa_get_tables(const hswa_pool *pool, int32_t *full_bt, int32_t *swa_bt, in
 /* Free lists in FIFO order: kind HSWA_KIND_FULL or HSWA_KIND_SWA. *count
  * gets the length; out (may be NULL) receives up to cap entries. */
 int hswa_get_free_list(const hswa_pool *pool, int kind, int32_t *out, int32_t cap, int32_t *count);
+
+/* ------------------------------------ SWA-aware prefix cache tree (host)
+ *
+ * Page holders. A page can be held by several owners at once: the table
+ * rows of sequences that share a cached prefix, and the prefix tree. The
+ * pool counts the holders of each page; a page returns to the tail of its
+ * free list only when the last one lets go. Without sharing every count is
+ * 1 and the calls above behave as described there.
+ *
+ * The tree (Sec. 2.1, SWA-aware prefix cache tree) stores whole pages of
+ * finished sequences, one node per page of P tokens holding its Full page
+ * and its SWA page (-1: none), and keeps one hold on each. Three rules
+ * differ from a plain prefix cache:
+ *   1. window-safety length: a match of m pages needs, besides equal
+ *      tokens, an SWA page on every logical page that meets the last W
+ *      positions [m*P - W, m*P); the match is trimmed to the largest such
+ *      m, the rest is a miss;
+ *   2. release follows the request lifecycle (hswa_swa_release above);
+ *   3. two indexes per node, evicted apart: SWA pages alone (the Full
+ *      prefix stays reusable) or whole nodes.
+ * Recency is a logical clock advanced by every match and insert. All
+ * choices are deterministic (clock, then node creation order). */
+typedef struct hswa_tree hswa_tree; /* opaque, host-owned */
+
+/* Start holding the first n_pages cached pages for empty sequence seq_id
+ * (length 0, no pages): its table row gets every Full page and the SWA
+ * pages of the logical pages that meet the last W positions
+ * [n_pages*P - W, n_pages*P); each of those must be held already (by a
+ * tree or another sequence), else HSWA_ERR_INVALID_ARG and no change. The
+ * length becomes n_pages * P; new tokens start on a fresh page. */
+int hswa_seq_share_prefix(hswa_pool *pool, int32_t seq_id, int32_t n_pages, const int32_t *full_pages,
+                          const int32_t *swa_pages);
+
+/* Holder counts of the pool's pages (kind HSWA_KIND_FULL / HSWA_KIND_SWA),
+ * up to cap entries. */
+int hswa_get_page_refs(const hswa_pool *pool, int kind, int32_t *out, int32_t cap);
+
+/* A tree over one pool. Destroy every tree of a pool before the pool
+ * (hswa_pool_destroy returns HSWA_ERR_INVALID_ARG while one exists). */
+int hswa_tree_create(hswa_pool *pool, hswa_tree **out);
+/* Let go of every stored page (nodes in creation order, each Full page
+ * before its SWA page) and free the tree. */
+int hswa_tree_destroy(hswa_tree *tree);
+
+/* Window-safe hit for n_tokens tokens (whole pages only). *n_pages_out
+ * gets m, the usable pages; full_pages_out / swa_pages_out (host, cap_pages
+ * >= min(n_tokens / P, max_pages_per_seq) entries) the pages of logical
+ * pages [0, m); *raw_pages_out (may be NULL) the pages whose tokens matched
+ * before trimming. Stamps the nodes of the untrimmed match as used. Pass
+ * the pages to hswa_seq_share_prefix to reuse them. */
+int hswa_tree_match(hswa_tree *tree, const int32_t *tokens, int64_t n_tokens, int32_t *full_pages_out,
+                    int32_t *swa_pages_out, int32_t cap_pages, int32_t *n_pages_out, int32_t *raw_pages_out);
+
+/* Store the whole pages of the first n_tokens tokens of sequence seq_id
+ * (n_tokens <= its length; each of those pages must have a Full page):
+ * pages new to the tree become nodes holding the sequence's Full and SWA
+ * pages; where a node exists for the same tokens the tree keeps its own
+ * pages (the sequence's copy is freed with the sequence) and takes the
+ * sequence's SWA page if the node has none. Stamps the whole path as used.
+ * *n_new_out (may be NULL) gets the number of new nodes. Call before
+ * hswa_seq_free at request end. */
+int hswa_tree_insert(hswa_tree *tree, int32_t seq_id, const int32_t *tokens, int64_t n_tokens,
+                     int32_t *n_new_out);
+
+/* Make room: free at least want_swa SWA pages and want_full Full pages
+ * that only the tree holds, if it can. SWA pages first: those outside the
+ * window of every stored end below their node (a node on logical page i is
+ * inside it when i >= (D*P - W) / P for the shallowest leaf below or at it,
+ * D pages deep), oldest first, then the rest. Then whole leaf nodes whose
+ * Full page only the tree holds, oldest first, until want_full pages are
+ * free (their SWA pages go too). *freed_full_out / *freed_swa_out (may be
+ * NULL) get the pages that went back to the free lists. */
+int hswa_tree_evict(hswa_tree *tree, int32_t want_full, int32_t want_swa, int32_t *freed_full_out,
+                    int32_t *freed_swa_out);
+
+/* Nodes and pages held: *n_nodes = *full_held = nodes, *swa_held = nodes
+ * with an SWA page (any may be NULL). */
+int hswa_tree_stats(const hswa_tree *tree, int32_t *n_nodes, int32_t *full_held, int32_t *swa_held);
+
+/* The nodes in creation order, 5 int32 each: id, parent id (-1 = root),
+ * logical page, Full page, SWA page; up to cap / 5 nodes written, *count
+ * gets the node count. */
+int hswa_tree_nodes(const hswa_tree *tree, int32_t *out, int32_t cap, int32_t *count);
 
 /* ------------------------------------------------- device-side calls */
 
