@@ -752,7 +752,7 @@ class SwaTransfer:
         swa_pages = 2 * B * (math.ceil((W + 64) / P) + 2) + math.ceil((W + 4096) / P) + 16
         max_pages = max(math.ceil((L + extra) / P) for L in w.cached) + 1
         cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
-                       head_dim=w.head_dim, dtype=H.HSWA_DTYPE_FP8_E4M3 if fp8 else w.dtype,
+                       head_dim=w.head_dim, dtype=w.dtype,
                        full_pages=full_pages, swa_pages=swa_pages, max_seqs=B, max_pages_per_seq=max_pages)
         self.stream = torch.cuda.Stream()
         self.sess = DualPoolSession(cfg, list(w.layer_kinds), None, wl.permutation(swa_pages, w.seed),
@@ -971,7 +971,8 @@ def run_decode(args, world, rank, local):
         pt = measure_prefix_tree()
         line["prefix_tree"] = {
             "workload": "64 requests sharing a 16384-token system prompt + 4096 own tokens each, W 128, P 64; "
-                        "stored at their end, then a follow-up turn each (host bookkeeping)",
+                        "chunked prefill storing each chunk's prefix after its release, then a follow-up turn "
+                        "each (host bookkeeping)",
             "unit": "us per call (median)", "match_us": round(pt["match"], 1), "share_us": round(pt["share"], 1),
             "insert_us": round(pt["insert"], 1), "evict_64_pages_us": round(pt["evict"], 1),
             "follow_up_full_hits": "%d/%d" % (pt["follow_up_hits"], pt["requests"])}
