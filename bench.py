@@ -331,7 +331,12 @@ class DecodeBatch:
         self.h_q = [x.cpu().pin_memory() for x in self.q]
         self.h_kn = [x.cpu().pin_memory() for x in self.kn]
         self.h_vn = [x.cpu().pin_memory() for x in self.vn]
-        self.h_o = [torch.empty_like(x, device="cpu").pin_memory() for x in self.o]
+        # outputs double-buffered: step k's result is read on the host while
+        # step k + 1 runs (the host waits for step k's copy before it returns
+        # from step k + 1)
+        self.h_o = [[torch.empty_like(x, device="cpu").pin_memory() for x in self.o] for _ in range(2)]
+        self.out_ready = [None, None]
+        self.out_sum = 0.0
         torch.cuda.synchronize()
 
     def lens(self):
@@ -367,14 +372,24 @@ class DecodeBatch:
                     e1.record(self.stream)
                     self.decode_events.append((e0, e1))
                 if host_io:
-                    self.h_o[i].copy_(self.o[i], non_blocking=True)
+                    self.h_o[buf][i].copy_(self.o[i], non_blocking=True)
                 self.launches += 3
+            if host_io:
+                ev = torch.cuda.Event()
+                ev.record(self.stream)
+                self.out_ready[buf] = ev
         self.steps_done += 1
         if self.steps_done % 64 == 0:
             sess.release(range(B))
         if host_io:
-            # the step's result is read on the host
-            self.stream.synchronize()
+            # the previous step's result is read on the host (this one's next)
+            self.read_output(1 - buf)
+
+    def read_output(self, buf):
+        if self.out_ready[buf] is not None:
+            self.out_ready[buf].synchronize()
+            self.out_ready[buf] = None
+            self.out_sum += float(self.h_o[buf][0][0, 0, 0]) + float(self.h_o[buf][1][-1, -1, -1])
 
     def breakdown(self, steps):
         """Average device time of each call of the decode step (events around
@@ -871,6 +886,8 @@ def run_decode(args, world, rank, local):
         bd = bench.breakdown(50)
     # end to end: host buffers in, host buffers out, copies inside the timed region
     e2e_secs = time_steps(lambda: bench.step(host_io=True), args.steps, bench.stream, world)
+    for b in range(2):  # the last step's result
+        bench.read_output(b)
     bench.finish()
     secs = max_over_ranks(secs, world)
     e2e_secs = max_over_ranks(e2e_secs, world)

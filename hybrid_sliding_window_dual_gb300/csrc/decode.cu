@@ -571,8 +571,15 @@ __global__ void __launch_bounds__(32 * (kTok / kTPW + 1)) decode_mma_bf16_d128(c
 // ---------------------------------------------------------- FP8 decode
 // Key rows of a 16-key group in the order the QK MMA's A rows take them:
 // after the movmatrix transpose of S^T, thread (g, q) then holds P for the
-// keys 4q..4q+3 that one 32-bit load of an E4M3 row gives the PV MMA.
-__device__ __forceinline__ int key_of_row(int r) { return 4 * ((r & 7) >> 1) + (r & 1) + 2 * (r >> 3); }
+// keys 4q..4q+3 that one 32-bit load of an E4M3 row gives the PV MMA. A rows
+// 0-7 take keys {0,1,4,5,10,11,14,15} and rows 8-15 the others, so the eight
+// rows of each ldmatrix tile differ in (key & 7) and hit eight different
+// 16-byte chunks of the 128-byte swizzle. For q >= 2 the first P pair is
+// keys 4q+2, 4q+3: the PV side takes the word's upper two codes first there.
+__device__ __forceinline__ int key_of_row(int r) {
+    const int q = (r & 7) >> 1;
+    return 4 * q + (r & 1) + 2 * ((r >> 3) ^ (q >> 1));
+}
 
 // 16-byte chunk of (row, byte) in a [rows][128 B] tile with the 128-byte
 // swizzle, and in a [rows][64 B] tile with the 64-byte swizzle.
@@ -583,17 +590,14 @@ __device__ __forceinline__ uint32_t swz64(int row, int byte) {
     return (uint32_t)(row * 64 + ((((byte >> 4) ^ (row >> 1)) & 3) << 4));
 }
 
-// Four E4M3 codes (bytes b0..b3 of r) as two f16 pairs {b0, b1}, {b2, b3},
-// each value times 2^-8: the code's exponent and mantissa bits land in the
-// low exponent and high mantissa bits of the f16 (the exponent biases differ
-// by 8), which also holds for subnormals. The sign is moved up by adding the
-// sign bit to itself (the carry clears bit 7 and sets bit 8) before the
-// shift. Callers fold the 2^8 into the scales.
-__device__ __forceinline__ void e4m3x4_f16x2x2(uint32_t r, uint32_t &lo, uint32_t &hi) {
-    const uint32_t t0 = __byte_perm(r, 0u, 0x4140);  // {b0, 0, b1, 0}
-    const uint32_t t1 = __byte_perm(r, 0u, 0x4342);  // {b2, 0, b3, 0}
-    lo = (t0 + (t0 & 0x00800080u)) << 7;
-    hi = (t1 + (t1 & 0x00800080u)) << 7;
+// Four E4M3 codes (bytes b0..b3 of r) as two exact f16 pairs {b0, b1},
+// {b2, b3}: the hardware conversion, two instructions per word (every E4M3
+// value, subnormals included, is an f16 value).
+__device__ __forceinline__ void e4m3x4_f16x2x2_cvt(uint32_t r, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(r));
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -634,6 +638,9 @@ __device__ void decode_consumer_fp8(DecodeSmem8 &sm, const DecodeArgs &a, int64_
     const int j = lane >> 3;
     const int ar = (lane & 7) + 8 * (j & 1);  // A row this lane addresses in ldmatrix (QK)
     const int c0 = w * 16 + key_of_row(gr), c1 = w * 16 + key_of_row(gr + 8);  // keys of this thread's S rows
+    // a V word's code pairs in the order this thread's P pairs take them
+    // (key_of_row): as loaded, or its two halves swapped for q >= 2
+    const uint32_t vsel = qd >= 2 ? 0x1032u : 0x3210u;
 
     for (int64_t u = u0; u < u1; ++u) {
         bool ok = mbar_wait(&sm.full[stage], phase, a.err) && !*(volatile int32_t *)&sm.abort;
@@ -665,17 +672,17 @@ __device__ void decode_consumer_fp8(DecodeSmem8 &sm, const DecodeArgs &a, int64_
             for (int dc = 0; dc < 4; ++dc) {
                 uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
                 ldsm_x4(kb + swz128(key, dc * 32 + 16 * (j >> 1)), r0, r1, r2, r3);
-                e4m3x4_f16x2x2(r0, a0, a2);
-                e4m3x4_f16x2x2(r1, a1, a3);
+                e4m3x4_f16x2x2_cvt(r0, a0, a2);
+                e4m3x4_f16x2x2_cvt(r1, a1, a3);
                 mma_f16_16816(sacc, a0, a1, a2, a3, qf[2 * dc][0], qf[2 * dc][1]);
-                e4m3x4_f16x2x2(r2, a0, a2);
-                e4m3x4_f16x2x2(r3, a1, a3);
+                e4m3x4_f16x2x2_cvt(r2, a0, a2);
+                e4m3x4_f16x2x2_cvt(r3, a1, a3);
                 mma_f16_16816(sacc, a0, a1, a2, a3, qf[2 * dc + 1][0], qf[2 * dc + 1][1]);
             }
             const bool v0 = c0 >= d.lo && c0 < d.hi, v1 = c1 >= d.lo && c1 < d.hi;
-            // K codes entered the MMA as value * 2^-8
-            const float s0 = sm.ks[stage][c0] * (256.f * a.scale_log2);
-            const float s1 = sm.ks[stage][c1] * (256.f * a.scale_log2);
+            // K codes entered the MMA as their exact values
+            const float s0 = sm.ks[stage][c0] * a.scale_log2;
+            const float s1 = sm.ks[stage][c1] * a.scale_log2;
             sacc[0] = v0 ? sacc[0] * s0 : -INFINITY;
             sacc[1] = v0 ? sacc[1] * s0 : -INFINITY;
             sacc[2] = v1 ? sacc[2] * s1 : -INFINITY;
@@ -696,29 +703,33 @@ __device__ void decode_consumer_fp8(DecodeSmem8 &sm, const DecodeArgs &a, int64_
             m1 = n1;
             const float p0 = fast_exp2(sacc[0] - b0), p1 = fast_exp2(sacc[1] - b1);
             const float p2 = fast_exp2(sacc[2] - b0), p3 = fast_exp2(sacc[3] - b1);
-            l0 = l0 * al0 + (p0 + p2);
-            l1 = l1 * al1 + (p1 + p3);
-            // V codes enter the MMA as value * 2^-8: P carries the 2^8
+            // V codes enter the MMA as their exact values; P carries the V
+            // scale times 2^8 (keeping small weights out of f16's subnormal
+            // range), and so does the running sum: O / l stays exact
+            l0 = l0 * al0 + 256.f * (p0 + p2);
+            l1 = l1 * al1 + 256.f * (p1 + p3);
             const float w0 = sm.vs[stage][c0] * 256.f, w1 = sm.vs[stage][c1] * 256.f;
             const uint32_t pb0 = movmatrix_t(pack_f16(p0 * w0, p1 * w0));
             const uint32_t pb1 = movmatrix_t(pack_f16(p2 * w1, p3 * w1));
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {  // a head's max moved
 #pragma unroll
-            for (int dt = 0; dt < 8; ++dt) {
-                oacc[dt][0] *= al0;
-                oacc[dt][1] *= al1;
-                oacc[dt][2] *= al0;
-                oacc[dt][3] *= al1;
+                for (int dt = 0; dt < 8; ++dt) {
+                    oacc[dt][0] *= al0;
+                    oacc[dt][1] *= al1;
+                    oacc[dt][2] *= al0;
+                    oacc[dt][3] *= al1;
+                }
             }
             // O^T += V^T P^T: A rows are d (two 16-row tiles per load), 4 key codes per 32-bit word
 #pragma unroll
             for (int dp = 0; dp < 4; ++dp) {
                 uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
                 ldsm_x4(vb + swz64(dp * 32 + j * 8 + (lane & 7), w * 16), r0, r1, r2, r3);
-                e4m3x4_f16x2x2(r0, a0, a2);
-                e4m3x4_f16x2x2(r1, a1, a3);
+                e4m3x4_f16x2x2_cvt(__byte_perm(r0, 0u, vsel), a0, a2);
+                e4m3x4_f16x2x2_cvt(__byte_perm(r1, 0u, vsel), a1, a3);
                 mma_f16_16816(oacc[2 * dp], a0, a1, a2, a3, pb0, pb1);
-                e4m3x4_f16x2x2(r2, a0, a2);
-                e4m3x4_f16x2x2(r3, a1, a3);
+                e4m3x4_f16x2x2_cvt(__byte_perm(r2, 0u, vsel), a0, a2);
+                e4m3x4_f16x2x2_cvt(__byte_perm(r3, 0u, vsel), a1, a3);
                 mma_f16_16816(oacc[2 * dp + 1], a0, a1, a2, a3, pb0, pb1);
             }
         }
