@@ -66,9 +66,13 @@ class DualPoolSession:
                                        v_scale=vs.data_ptr() if vs is not None else None))
         self.ws = None
         self.prefill_ws = None
+        self.tree = None
 
     def close(self):
         if self.pool:
+            if self.tree:
+                B.hswa_tree_destroy(self.tree)
+                self.tree = None
             B.hswa_pool_destroy(self.pool)
             self.pool = None
 
@@ -93,6 +97,26 @@ class DualPoolSession:
 
     def swa_restore(self, seq_ids):
         return B.hswa_swa_restore(self.pool, seq_ids)
+
+    # ------------------------------------------------ prefix cache (host)
+    def prefix_tree(self):
+        """The pool's SWA-aware prefix cache tree (created on first use)."""
+        if self.tree is None:
+            self.tree = B.hswa_tree_create(self.pool)
+        return self.tree
+
+    def match_prefix(self, tokens):
+        """Window-safe hit: (pages m, Full pages, SWA pages, raw pages)."""
+        return B.hswa_tree_match(self.prefix_tree(), tokens, self.cfg.max_pages_per_seq)
+
+    def share_prefix(self, seq_id, full_pages, swa_pages):
+        B.hswa_seq_share_prefix(self.pool, seq_id, full_pages, swa_pages)
+
+    def store_prefix(self, seq_id, tokens):
+        return B.hswa_tree_insert(self.prefix_tree(), seq_id, tokens)
+
+    def evict(self, want_full, want_swa):
+        return B.hswa_tree_evict(self.prefix_tree(), want_full, want_swa)
 
     def tables(self):
         return B.hswa_get_tables(self.pool, self.cfg)
