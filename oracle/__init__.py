@@ -240,6 +240,68 @@ def swa_unpack(packed, k_pool, v_pool, swa_bt, seq_len, window):
                 pool[page, :, t % P, :] = block[:, i, :]
 
 
+def swa_pack_fp8(k_codes, k_scale, v_codes, v_scale, swa_bt, seq_len, window):
+    """Pack the in-window tokens of sequences 0..n-1 of one SWA layer over
+    FP8 pools ("Baidu AI Cloud: Day-0 support for hybrid-architecture LLMs",
+    Optimization 2 item 2: codes with one scale per token, head and
+    128-element tile; MiMo Sec. 2.1: only in-window data moves).
+
+    Pools: k_codes [pages][Hkv][P][d] uint8, v_codes [pages][Hkv][d][P]
+    (pages stored transposed), scales [pages][Hkv][P][d/128] float32 with
+    d = 128. For each sequence s in order, n_s = min(L_s, W) tokens at
+    positions [L_s - n_s, L_s), starting at byte 2 * Hkv * (d + 4) * (sum of
+    the earlier n): K codes [Hkv][n_s][d], V codes [Hkv][n_s][d] (token rows,
+    not transposed), K scales [Hkv][n_s] float32, V scales [Hkv][n_s]
+    float32. Returns a flat uint8 array."""
+    P, hkv, d = k_codes.shape[2], k_codes.shape[1], k_codes.shape[3]
+    assert d == 128 and k_scale.shape[-1] == 1
+    n, off = swa_window_counts(seq_len, window)
+    out = np.zeros(int(off[-1]) * 2 * hkv * (d + 4), np.uint8)
+    for s in range(len(n)):
+        L, ns = int(seq_len[s]), int(n[s])
+        kb = np.zeros((hkv, ns, d), np.uint8)
+        vb = np.zeros((hkv, ns, d), np.uint8)
+        kss = np.zeros((hkv, ns), np.float32)
+        vss = np.zeros((hkv, ns), np.float32)
+        for i, t in enumerate(range(L - ns, L)):
+            page = int(swa_bt[s, t // P])
+            if page < 0:
+                raise IndexError("in-window token without an SWA page")
+            row = t % P
+            kb[:, i, :] = k_codes[page, :, row, :]
+            vb[:, i, :] = v_codes[page, :, :, row]
+            kss[:, i] = k_scale[page, :, row, 0]
+            vss[:, i] = v_scale[page, :, row, 0]
+        blob = np.concatenate([kb.reshape(-1), vb.reshape(-1), kss.reshape(-1).view(np.uint8),
+                               vss.reshape(-1).view(np.uint8)])
+        start = int(off[s]) * 2 * hkv * (d + 4)
+        out[start:start + blob.size] = blob
+    return out
+
+
+def swa_unpack_fp8(packed, k_codes, k_scale, v_codes, v_scale, swa_bt, seq_len, window):
+    """Inverse of swa_pack_fp8: write the packed tokens back into the pools."""
+    P, hkv, d = k_codes.shape[2], k_codes.shape[1], k_codes.shape[3]
+    n, off = swa_window_counts(seq_len, window)
+    for s in range(len(n)):
+        L, ns = int(seq_len[s]), int(n[s])
+        start = int(off[s]) * 2 * hkv * (d + 4)
+        c = hkv * ns * d
+        kb = packed[start:start + c].reshape(hkv, ns, d)
+        vb = packed[start + c:start + 2 * c].reshape(hkv, ns, d)
+        kss = packed[start + 2 * c:start + 2 * c + 4 * hkv * ns].view(np.float32).reshape(hkv, ns)
+        vss = packed[start + 2 * c + 4 * hkv * ns:start + 2 * c + 8 * hkv * ns].view(np.float32).reshape(hkv, ns)
+        for i, t in enumerate(range(L - ns, L)):
+            page = int(swa_bt[s, t // P])
+            if page < 0:
+                raise IndexError("in-window token without an SWA page")
+            row = t % P
+            k_codes[page, :, row, :] = kb[:, i, :]
+            v_codes[page, :, :, row] = vb[:, i, :]
+            k_scale[page, :, row, 0] = kss[:, i]
+            v_scale[page, :, row, 0] = vss[:, i]
+
+
 def kv_bytes(pool: DualPool, layer_kinds, seq_ids, kv_bytes_per_token):
     """KV bytes held by the dual pool for the given sequences (live pages),
     summed over layers: Full layers count Full pages, SWA layers SWA pages."""

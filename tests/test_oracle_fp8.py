@@ -175,3 +175,52 @@ def test_fp8_pins_catch_planted_mistake(name, tmp_path):
             "print('FAILED' if not worst < 1e-12 else 'ok')\n" % (os.path.dirname(here), here, str(so)))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 or "FAILED" in r.stdout, r.stdout
+
+
+# ------------------------------------------------------------- FP8 transfer
+def fp8_pools(seed, pages=12, hkv=2, P=4):
+    rng = np.random.default_rng(seed)
+    kc = rng.integers(0, 0x7F, (pages, hkv, P, 128)).astype(np.uint8) | (rng.integers(0, 2, (pages, hkv, P, 128)) << 7).astype(np.uint8)
+    vc = rng.integers(0, 0x7F, (pages, hkv, 128, P)).astype(np.uint8)
+    ks = rng.uniform(0.001, 0.01, (pages, hkv, P, 1)).astype(np.float32)
+    vs = rng.uniform(0.001, 0.01, (pages, hkv, P, 1)).astype(np.float32)
+    return kc, ks, vc, vs
+
+
+def test_fp8_pack_is_the_dequantized_window():
+    """Dequantizing the packed codes with the packed scales gives the pool's
+    dequantized K and V at each window token (V read back from the
+    transposed pages), sequence by sequence."""
+    kc, ks, vc, vs = fp8_pools(3)
+    bt = np.array([[5, 2, 9, -1], [0, 7, 11, 3]], np.int32)  # W = 6: sequence 0 needs pages 1, 2 only
+    lens, W, hkv, P = [11, 14], 6, 2, 4
+    bt[0, 3] = -1
+    buf = oracle.swa_pack_fp8(kc, ks, vc, vs, bt, lens, W)
+    n, off = oracle.swa_window_counts(lens, W)
+    assert buf.size == int(off[-1]) * 2 * hkv * 132
+    kd = fp8.dequantize_tiles(kc, ks)                                  # [pages][Hkv][P][d]
+    vd = fp8.dequantize_tiles(np.transpose(vc, (0, 1, 3, 2)), vs)      # token rows
+    for s, L in enumerate(lens):
+        ns, base = int(n[s]), int(off[s]) * 2 * hkv * 132
+        c = hkv * ns * 128
+        kb = buf[base:base + c].reshape(hkv, ns, 128)
+        vb = buf[base + c:base + 2 * c].reshape(hkv, ns, 128)
+        kss = buf[base + 2 * c:base + 2 * c + 4 * hkv * ns].view(np.float32).reshape(hkv, ns)
+        vss = buf[base + 2 * c + 4 * hkv * ns:base + 2 * c + 8 * hkv * ns].view(np.float32).reshape(hkv, ns)
+        for i, t in enumerate(range(L - ns, L)):
+            pg, r = bt[s, t // P], t % P
+            assert np.array_equal(fp8.e4m3_decode(kb[:, i]) * kss[:, i, None], kd[pg, :, r])
+            assert np.array_equal(fp8.e4m3_decode(vb[:, i]) * vss[:, i, None], vd[pg, :, r])
+
+
+def test_fp8_unpack_restores_the_window_into_fresh_pages():
+    kc, ks, vc, vs = fp8_pools(4)
+    bt = np.array([[1, 4, 6], [2, 8, 10]], np.int32)
+    lens, W = [9, 12], 5
+    buf = oracle.swa_pack_fp8(kc, ks, vc, vs, bt, lens, W)
+    fresh = [np.zeros_like(x) for x in (kc, ks, vc, vs)]
+    bt2 = np.array([[0, 3, 5], [7, 9, 11]], np.int32)  # other pages
+    oracle.swa_unpack_fp8(buf, fresh[0], fresh[1], fresh[2], fresh[3], bt2, lens, W)
+    assert np.array_equal(oracle.swa_pack_fp8(*fresh, bt2, lens, W), buf)
+    # only window tokens were written: position 3 of sequence 0 (page 0, row 3) stays zero
+    assert not fresh[0][0, :, 3].any() and not fresh[2][0, :, :, 3].any()
