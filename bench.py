@@ -753,9 +753,10 @@ class SwaTransfer:
     256K), 60 SWA layers. A step gathers the in-window tokens of every layer
     into a pinned host buffer (the kernel writes host memory directly), evicts
     the SWA segments, gives the windows fresh pages and scatters the host
-    copies back."""
+    copies back. fp8=True: FP8 E4M3 pools with per-token-head scales (the
+    packed window carries codes and scales)."""
 
-    def __init__(self, w):
+    def __init__(self, w, fp8=False):
         import torch
         import hybrid_sliding_window_dual_gb300 as H
         from hybrid_sliding_window_dual_gb300.session import DualPoolSession, window_offsets
@@ -766,8 +767,9 @@ class SwaTransfer:
         full_pages = sum(math.ceil((L + extra) / P) for L in w.cached) + 16
         swa_pages = 2 * B * (math.ceil((W + 64) / P) + 2) + math.ceil((W + 4096) / P) + 16
         max_pages = max(math.ceil((L + extra) / P) for L in w.cached) + 1
+        self.fp8 = fp8
         cfg = H.Config(window=W, page_size=P, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
-                       head_dim=w.head_dim, dtype=w.dtype,
+                       head_dim=w.head_dim, dtype=H.HSWA_DTYPE_FP8_E4M3 if fp8 else w.dtype,
                        full_pages=full_pages, swa_pages=swa_pages, max_seqs=B, max_pages_per_seq=max_pages)
         self.stream = torch.cuda.Stream()
         self.sess = DualPoolSession(cfg, list(w.layer_kinds), None, wl.permutation(swa_pages, w.seed),
@@ -778,14 +780,28 @@ class SwaTransfer:
                 self.sess.release([s])
         with torch.cuda.stream(self.stream):
             for i in range(len(w.layer_kinds)):
-                fill_normal(self.sess.k[i], 5000 + 2 * i)
-                fill_normal(self.sess.v[i], 5001 + 2 * i)
+                if fp8:  # seeded E4M3 codes without the NaN patterns, seeded scales
+                    for t, seed in ((self.sess.k[i], 5000 + 2 * i), (self.sess.v[i], 5001 + 2 * i)):
+                        g = torch.Generator(device="cuda")
+                        g.manual_seed(seed)
+                        mag = torch.randint(0, 0x7F, t.shape, generator=g, device="cuda", dtype=torch.uint8)
+                        sgn = torch.randint(0, 2, t.shape, generator=g, device="cuda", dtype=torch.uint8)
+                        t.copy_(mag | (sgn << 7))
+                    self.sess.ks[i].uniform_(0.001, 0.011)
+                    self.sess.vs[i].uniform_(0.001, 0.011)
+                else:
+                    fill_normal(self.sess.k[i], 5000 + 2 * i)
+                    fill_normal(self.sess.v[i], 5001 + 2 * i)
             self.sess.sync()
         self.window_offsets = window_offsets
         self.refresh_offsets()
-        n = int(self.off[-1]) * 2 * w.n_kv_heads * w.head_dim
-        self.host = [torch.empty(n, dtype=wl.TORCH_DTYPE[w.dtype], pin_memory=True)
-                     for _ in range(len(w.layer_kinds))]
+        if fp8:
+            self.host = [torch.empty(self.moved_bytes(), dtype=torch.uint8, pin_memory=True)
+                         for _ in range(len(w.layer_kinds))]
+        else:
+            n = int(self.off[-1]) * 2 * w.n_kv_heads * w.head_dim
+            self.host = [torch.empty(n, dtype=wl.TORCH_DTYPE[w.dtype], pin_memory=True)
+                         for _ in range(len(w.layer_kinds))]
         self.launches = 0
         torch.cuda.synchronize()
 
@@ -795,6 +811,8 @@ class SwaTransfer:
         self.d_off = self.torch.as_tensor(self.off, device="cuda")
 
     def moved_bytes(self):
+        if self.fp8:  # a code byte per element plus an fp32 scale per token, head and tensor
+            return int(self.off[-1]) * 2 * self.w.n_kv_heads * (self.w.head_dim + 4)
         return int(self.off[-1]) * 2 * self.w.n_kv_heads * self.w.head_dim * KV_ROW[self.w.dtype]
 
     def gather_all(self):
@@ -1005,6 +1023,15 @@ def run_decode(args, world, rank, local):
             "gb_if_whole_sequences": round(t["bytes_if_full_sequences"] / 1e9, 1),
             "release_us_per_call": round(t["release_us_per_call"], 1),
             "max_live_swa_pages_per_seq_after_release": t["max_live_swa_pages_per_seq_after_release"]}
+        if not args.no_fp8:
+            t8 = measure_transfer(2, fp8=True)
+            line["swa_transfer"]["fp8"] = {
+                "workload": "the same windows over FP8 E4M3 pools (codes + per-token-head scales)",
+                "gather_gbs": round(t8["gather_gbs"], 1), "scatter_gbs": round(t8["scatter_gbs"], 1),
+                "gb_each_way": round(t8["bytes_each_way"] / 1e9, 3),
+                "gather_frac_of_memcpy": round(t8["gather_gbs"] / t8["memcpy_d2h_gbs"], 3),
+                "scatter_frac_of_memcpy": round(t8["scatter_gbs"] / t8["memcpy_h2d_gbs"], 3),
+                "kernel": "swa_xfer_fp8_kernel"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(w, budget_s=args.cpu_budget)
     return line
@@ -1207,10 +1234,10 @@ def measure_prefix_tree(n_req=64, prompt=16384, turn=4096, reps=3):
     return out
 
 
-def measure_transfer(steps):
+def measure_transfer(steps, fp8=False):
     import torch
     w = wl.swa_transfer()
-    tb = SwaTransfer(w)
+    tb = SwaTransfer(w, fp8=fp8)
     moved = tb.moved_bytes() * len(w.layer_kinds)
     # warm-up round trip
     tb.gather_all()

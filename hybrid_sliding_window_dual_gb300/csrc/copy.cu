@@ -82,6 +82,86 @@ __global__ void swa_xfer_kernel(chunk_t *kp, chunk_t *vp, chunk_t *packed, const
     }
 }
 
+// FP8 transfer (d = 128, P = 64): one CTA per (kv head, sequence) walks the
+// pages of the window. Packed order per sequence (at byte 2 * Hkv * 132 *
+// tok_offset): K codes [Hkv][n][128], V codes [Hkv][n][128] (token rows),
+// K scales [Hkv][n] and V scales [Hkv][n] (fp32). K rows and scales are
+// contiguous runs on both sides; a V page is stored transposed ([128][64]),
+// so its window columns go through a shared-memory tile.
+template <bool kGather>
+__global__ void __launch_bounds__(256) swa_xfer_fp8_kernel(uint8_t *kc, uint8_t *vc, float *ks, float *vs,
+                                                           uint8_t *packed, const int32_t *__restrict__ swa_bt,
+                                                           const int32_t *__restrict__ seq_len,
+                                                           const int64_t *__restrict__ tok_offset, int32_t bt_stride,
+                                                           int32_t hkv, int32_t window, int32_t num_pages, int *err) {
+    constexpr int kDd = 128, kPg = 64;
+    __shared__ __align__(16) uint8_t tile[kDd * kPg];
+    const int32_t g = blockIdx.x, s = blockIdx.y;
+    const int32_t L = seq_len[s];
+    const int32_t n = L < window ? L : window;
+    if (n <= 0) return;
+    const int32_t t_lo = L - n;
+    uint8_t *base = packed + tok_offset[s] * 2 * hkv * (kDd + 4);
+    uint8_t *pk = base + (int64_t)g * n * kDd;
+    uint8_t *pv = base + ((int64_t)hkv + g) * n * kDd;
+    float *pks = reinterpret_cast<float *>(base + 2 * (int64_t)hkv * n * kDd) + (int64_t)g * n;
+    float *pvs = pks + (int64_t)hkv * n;
+    const int32_t *btrow = swa_bt + (int64_t)s * bt_stride;
+    for (int32_t lp = t_lo / kPg; lp <= (L - 1) / kPg; ++lp) {
+        const int32_t pg = lp < bt_stride ? btrow[lp] : -1;
+        if (pg < 0 || pg >= num_pages) {
+            if (threadIdx.x == 0) set_error(err, HSWA_ERR_BOUNDS);
+            continue;
+        }
+        const int32_t r0 = max(t_lo, lp * kPg) - lp * kPg, r1 = min(L, (lp + 1) * kPg) - lp * kPg;
+        const int32_t nr = r1 - r0, i0 = lp * kPg + r0 - t_lo;  // window tokens on the page, first one's index
+        const int64_t blk = (int64_t)pg * hkv + g;                // (page, kv head) block
+        // K rows and both scale runs: 8-byte words (every run starts on an 8-byte boundary)
+        uint2 *kpool = reinterpret_cast<uint2 *>(kc + (blk * kPg + r0) * kDd);
+        uint2 *kpack = reinterpret_cast<uint2 *>(pk + (int64_t)i0 * kDd);
+        for (int32_t w = threadIdx.x; w < nr * kDd / 8; w += blockDim.x) {
+            if (kGather)
+                kpack[w] = kpool[w];
+            else
+                kpool[w] = kpack[w];
+        }
+        for (int32_t k = threadIdx.x; k < nr; k += blockDim.x) {
+            if (kGather) {
+                pks[i0 + k] = ks[blk * kPg + r0 + k];
+                pvs[i0 + k] = vs[blk * kPg + r0 + k];
+            } else {
+                ks[blk * kPg + r0 + k] = pks[i0 + k];
+                vs[blk * kPg + r0 + k] = pvs[i0 + k];
+            }
+        }
+        uint8_t *vpage = vc + blk * kDd * kPg;
+        if (kGather) {  // the page's [128][64] block, then token rows out of it
+            for (int32_t c = threadIdx.x; c < kDd * kPg / 16; c += blockDim.x)
+                reinterpret_cast<uint4 *>(tile)[c] = reinterpret_cast<const uint4 *>(vpage)[c];
+            __syncthreads();
+            for (int32_t w = threadIdx.x; w < nr * kDd / 8; w += blockDim.x) {
+                const int32_t k = w / (kDd / 8), d0 = (w % (kDd / 8)) * 8;
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    lo |= (uint32_t)tile[(d0 + e) * kPg + r0 + k] << (8 * e);
+                    hi |= (uint32_t)tile[(d0 + 4 + e) * kPg + r0 + k] << (8 * e);
+                }
+                reinterpret_cast<uint2 *>(pv + (int64_t)(i0 + k) * kDd)[d0 / 8] = make_uint2(lo, hi);
+            }
+        } else {  // the page's token rows into the tile, then its window columns back
+            for (int32_t w = threadIdx.x; w < nr * kDd / 8; w += blockDim.x)
+                reinterpret_cast<uint2 *>(tile)[w] = reinterpret_cast<const uint2 *>(pv + (int64_t)i0 * kDd)[w];
+            __syncthreads();
+            for (int32_t f = threadIdx.x; f < kDd * nr; f += blockDim.x) {
+                const int32_t dd = f / nr, k = f % nr;
+                vpage[dd * kPg + r0 + k] = tile[k * kDd + dd];
+            }
+        }
+        __syncthreads();  // the tile is reused by the next page
+    }
+}
+
 // FP8 append: one warp per (token, kv head). Each lane holds 4 of the 128
 // elements of the K row and of the V row; the warp's amax gives the tile's
 // scale = amax / 448 (1 for an all-zero tile), each element is divided by it
@@ -181,7 +261,27 @@ static int swa_xfer(const hswa_pool *pool, const hswa_layer *layer, const int32_
         !layer->v_pool)
         return HSWA_ERR_INVALID_ARG;
     const hswa_config &c = pool->cfg;
-    if (c.dtype == HSWA_DTYPE_FP8_E4M3) return HSWA_ERR_UNSUPPORTED;
+    if (c.dtype == HSWA_DTYPE_FP8_E4M3) {
+        if (c.head_dim != 128 || c.page_size != 64 || !layer->k_scale || !layer->v_scale || !aligned16(layer->k_pool) ||
+            !aligned16(layer->v_pool) || ((uintptr_t)layer->k_scale & 3) || ((uintptr_t)layer->v_scale & 3) ||
+            ((uintptr_t)buf & 7))
+            return HSWA_ERR_UNSUPPORTED;
+        if (n_seqs == 0) return HSWA_OK;
+        set_last_kernel(gather ? "swa_gather_fp8" : "swa_scatter_fp8");
+        cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+        const dim3 grid(c.n_kv_heads, n_seqs);
+        if (gather)
+            swa_xfer_fp8_kernel<true><<<grid, 256, 0, st>>>(
+                (uint8_t *)layer->k_pool, (uint8_t *)layer->v_pool, layer->k_scale, layer->v_scale, (uint8_t *)buf,
+                d_swa_bt, d_seq_len, d_tok_offset, c.max_pages_per_seq, c.n_kv_heads, layer->window, c.swa_pages,
+                error_word());
+        else
+            swa_xfer_fp8_kernel<false><<<grid, 256, 0, st>>>(
+                (uint8_t *)layer->k_pool, (uint8_t *)layer->v_pool, layer->k_scale, layer->v_scale, (uint8_t *)buf,
+                d_swa_bt, d_seq_len, d_tok_offset, c.max_pages_per_seq, c.n_kv_heads, layer->window, c.swa_pages,
+                error_word());
+        return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+    }
     const int64_t row_bytes = (int64_t)c.head_dim * esize(c);
     if (row_bytes % 16 || !aligned16(buf) || !aligned16(layer->k_pool) || !aligned16(layer->v_pool))
         return HSWA_ERR_UNSUPPORTED;

@@ -89,8 +89,9 @@ extern "C" {
  * append stay bf16; the append quantizes: scale = amax / 448 (1 if amax is
  * 0), code = round-to-nearest-even(x / scale) saturating at 448. Supported
  * by hswa_append_kv, hswa_decode, hswa_decode_append (d = 128, 8 query
- * heads per kv head, P = 64) and hswa_prefill_chunk_ws (d = 128, an even
- * number of query heads per kv head, P = 64); other calls return
+ * heads per kv head, P = 64), hswa_prefill_chunk_ws (d = 128, an even
+ * number of query heads per kv head, P = 64) and hswa_swa_gather /
+ * hswa_swa_scatter (d = 128, P = 64); other calls return
  * HSWA_ERR_UNSUPPORTED. */
 #define HSWA_DTYPE_FP8_E4M3 2
 
@@ -397,7 +398,10 @@ int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *layer, const 
  * pinned host memory mapped into the device address space. An in-window
  * token without an SWA page sets HSWA_ERR_BOUNDS and is skipped. The
  * caller must not reuse dst until work enqueued after this call on stream
- * has finished. */
+ * has finished. FP8 pools (d = 128, P = 64; dst 8-byte aligned): sequence
+ * i starts at byte 2 * Hkv * (d + 4) * d_tok_offset[i] and holds K codes
+ * [Hkv][n_i][d], V codes [Hkv][n_i][d] (token rows, not the pages'
+ * transposed layout), K scales [Hkv][n_i] and V scales [Hkv][n_i] (fp32). */
 int hswa_swa_gather(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
                     const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, void *dst,
                     hswa_stream_t stream);

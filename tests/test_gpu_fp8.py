@@ -112,11 +112,6 @@ def test_fp8_append_and_decode_match_oracle(fused):
 @pytest.mark.gpu
 def test_fp8_unsupported_calls_say_so():
     c = Fp8Case([100], seed=72, kinds=(SWA,))
-    off = torch.tensor([0, 100], dtype=torch.int64, device="cuda")
-    buf = torch.zeros(2 * 100 * HKV * D, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(H.HswaError) as e:
-        c.sess.gather(0, off, 1, buf)
-    assert e.value.status == H.HSWA_ERR_UNSUPPORTED
     # prefill over an FP8 pool needs the workspace variant
     q = torch.zeros(1, HQ, D, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(H.HswaError) as e:
@@ -201,3 +196,43 @@ def test_fp8_multi_token_decode_is_unsupported():
         c.sess.decode_multi(0, q, q.clone(), 2, 2, 0.1)
     assert e.value.status == H.HSWA_ERR_UNSUPPORTED
     assert c.sess.check() == 0
+
+
+def fp8_window_pack(c, layer, lens):
+    kc, ks, vc, vs = (x.cpu().numpy() for x in (c.sess.k[layer], c.sess.ks[layer], c.sess.v[layer], c.sess.vs[layer]))
+    return oracle.swa_pack_fp8(kc, ks, vc, vs, c.ora.swa_bt, lens, W)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dst_host", [False, True])
+def test_fp8_gather_scatter_round_trip(dst_host):
+    """Gather the windows of FP8 SWA layers (to device or pinned host memory)
+    and compare with the oracle's pack byte for byte; then drop the SWA
+    segments, give the windows other pages and scatter the buffers back: the
+    pools pack to the same bytes again."""
+    from hybrid_sliding_window_dual_gb300.session import window_offsets
+    cached = [0, 1, 63, 64, 65, 127, 128, 129, 700, 3000]
+    c = Fp8Case(cached, seed=77, kinds=(SWA, SWA))
+    B = len(cached)
+    lens = c.ora.seq_len[:B]
+    offs = window_offsets(lens, W)
+    off = torch.as_tensor(offs, device="cuda")
+    nbytes = int(offs[-1]) * 2 * HKV * (D + 4)
+    bufs = []
+    for layer in range(2):
+        buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) if dst_host else \
+            torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        c.sess.gather(layer, off, B, buf)
+        assert c.sess.check() == 0
+        assert H.hswa_last_kernel() == "swa_gather_fp8"
+        exp = fp8_window_pack(c, layer, lens)
+        assert np.array_equal(buf.cpu().numpy(), exp)
+        bufs.append((buf, exp))
+    assert c.sess.swa_drop(range(B)) == c.ora.swa_drop(range(B))
+    assert c.sess.swa_restore(range(B)) == c.ora.swa_restore(range(B))
+    c.sess.sync()
+    for layer in range(2):
+        c.sess.scatter(layer, off, B, bufs[layer][0])
+        assert c.sess.check() == 0
+        assert H.hswa_last_kernel() == "swa_scatter_fp8"
+        assert np.array_equal(fp8_window_pack(c, layer, lens), bufs[layer][1])
