@@ -130,3 +130,38 @@ def test_prefill_swa_after_release_reads_only_live_pages():
     sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=15, chunk=100, extra_tokens=600)
     assert (sc.ora.swa_bt[:, :10] < 0).any()
     run_prefill_chunk(sc, [200, 129, 64, 500], seed=4, expect_kernel="prefill_tc_bf16_d128")
+
+
+@pytest.mark.gpu
+def test_prefill_window_covers_whole_sequence_equals_full():
+    """W >= every position: the SWA layer's chunk attends to exactly the Full
+    layer's keys, so both layers give the same bits on the same history."""
+    cached = [0, 100, 700, 1500]
+    chunk = [130, 64, 300, 1]
+    sc = Scenario(64, 8, 128, 64, 4096, wl.DTYPE_BF16, cached, layer_kinds=(FULL, SWA), seed=16,
+                  extra_tokens=400, chunk=8192)
+    B = len(cached)
+    prefix = sc.ora.seq_len[:B].copy()
+    full_slots, swa_slots = sc.reserve(range(B), chunk)
+    sc.sess.sync()
+    q_start = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    T = int(q_start[-1])
+    kn = sc.to_dev(sc.gen((T, 8, 128), 1))
+    vn = sc.to_dev(sc.gen((T, 8, 128), 2))
+    q = sc.to_dev(sc.gen((T, 64, 128), 3))
+    d_prefix = torch.as_tensor(prefix.astype(np.int32), device="cuda")
+    d_qs = torch.as_tensor(q_start, device="cuda")
+    outs = []
+    for layer, slots in ((0, full_slots), (1, swa_slots)):
+        if layer == 1:  # the same K/V history in both layers
+            for s in range(B):
+                for p in range(int(prefix[s] + 63) // 64):
+                    sc.sess.k[1][sc.ora.swa_bt[s, p]] = sc.sess.k[0][sc.ora.full_bt[s, p]]
+                    sc.sess.v[1][sc.ora.swa_bt[s, p]] = sc.sess.v[0][sc.ora.full_bt[s, p]]
+        sc.sess.append(layer, kn, vn, torch.as_tensor(slots, device="cuda"))
+        o = torch.empty_like(q)
+        sc.sess.prefill(layer, q, o, d_prefix, d_qs, B, max(chunk), sc.scale)
+        assert H.hswa_last_kernel() == "prefill_tc_bf16_d128"
+        outs.append(o)
+    assert sc.sess.check() == 0
+    assert torch.equal(outs[0], outs[1])
