@@ -877,6 +877,16 @@ def workload(args, name):
     return w
 
 
+def decode_config(w, world):
+    """The decode-batch workload as both arms report it."""
+    kv = decode_bytes(w, np.asarray(w.cached, np.int64) + 1)
+    return {"workload": "decode_batch", "seqs": len(w.cached), "cached_len": "uniform[1024,32768] seed 2",
+            "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+            "page": w.page_size, "window": w.window, "layers": "1 Full + 1 SWA",
+            "l2": "inputs larger than L2 (%.1f GB KV per step)" % (kv["step"] / 1e9),
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_decode(args, world, rank, local):
     import torch
     w = workload(args, "decode_batch")
@@ -922,11 +932,7 @@ def run_decode(args, world, rank, local):
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "decode_batch", "seqs": B, "cached_len": "uniform[1024,32768] seed 2",
-                   "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
-                   "page": w.page_size, "window": w.window, "layers": "1 Full + 1 SWA",
-                   "l2": "inputs larger than L2 (%.1f GB KV per step)" % (step_bytes / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": decode_config(w, world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": decode_traffic(full_layer_bytes),
                      "kernel": "decode_mma_bf16_d128 with fused append (Full layer; plan + main + combine)",
@@ -1131,7 +1137,7 @@ def run_reference(args, world, rank):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode_batch", "seqs": B, "sample_per_step": per_step},
+        "config": decode_config(w, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": "%d of %d sequences per step, Full + SWA layer" % (per_step, B)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
