@@ -313,10 +313,23 @@ class DecodeBatch:
                     self.sess.vs[i].uniform_(0.001, 0.011)
             self.sess.sync()
         dt = wl.TORCH_DTYPE[w.dtype]
-        self.q = [wl.normal((B, w.n_q_heads, w.head_dim), 100 + i, w.dtype, "cuda") for i in range(2)]
-        self.kn = [wl.normal((B, w.n_kv_heads, w.head_dim), 200 + i, w.dtype, "cuda") for i in range(2)]
-        self.vn = [wl.normal((B, w.n_kv_heads, w.head_dim), 300 + i, w.dtype, "cuda") for i in range(2)]
-        self.o = [torch.empty(B, w.n_q_heads, w.head_dim, dtype=dt, device="cuda") for _ in range(2)]
+        # a step's inputs (q, new K, new V of both layers) and outputs each
+        # live in one contiguous block, so the host-buffer path moves them
+        # with one copy per direction
+        nq, nkv = B * w.n_q_heads * w.head_dim, B * w.n_kv_heads * w.head_dim
+        self.io_in = torch.empty(2 * (nq + 2 * nkv), dtype=dt, device="cuda")
+        self.io_out = torch.empty(2 * nq, dtype=dt, device="cuda")
+        views = lambda buf, off, n, shape: buf[off:off + n].view(shape)
+        qs, kvs = (B, w.n_q_heads, w.head_dim), (B, w.n_kv_heads, w.head_dim)
+        per = nq + 2 * nkv
+        self.q = [views(self.io_in, i * per, nq, qs) for i in range(2)]
+        self.kn = [views(self.io_in, i * per + nq, nkv, kvs) for i in range(2)]
+        self.vn = [views(self.io_in, i * per + nq + nkv, nkv, kvs) for i in range(2)]
+        for i in range(2):
+            self.q[i].copy_(wl.normal(qs, 100 + i, w.dtype, "cuda"))
+            self.kn[i].copy_(wl.normal(kvs, 200 + i, w.dtype, "cuda"))
+            self.vn[i].copy_(wl.normal(kvs, 300 + i, w.dtype, "cuda"))
+        self.o = [views(self.io_out, i * nq, nq, qs) for i in range(2)]
         # double-buffered pinned staging for the slots of a step, each buffer
         # reused only after its previous copy has run
         self.slot_host = [torch.empty(2, B, dtype=torch.int32, pin_memory=True) for _ in range(2)]
@@ -327,14 +340,12 @@ class DecodeBatch:
         self.steps_done = 0
         self.launches = 0
         self.decode_events = []
-        # host-buffer (end-to-end) variants
-        self.h_q = [x.cpu().pin_memory() for x in self.q]
-        self.h_kn = [x.cpu().pin_memory() for x in self.kn]
-        self.h_vn = [x.cpu().pin_memory() for x in self.vn]
-        # outputs double-buffered: step k's result is read on the host while
-        # step k + 1 runs (the host waits for step k's copy before it returns
+        # host-buffer (end-to-end) variants: the pinned input block, and the
+        # outputs double-buffered (step k's result is read on the host while
+        # step k + 1 runs; the host waits for step k's copy before it returns
         # from step k + 1)
-        self.h_o = [[torch.empty_like(x, device="cpu").pin_memory() for x in self.o] for _ in range(2)]
+        self.h_in = self.io_in.cpu().pin_memory()
+        self.h_o = [torch.empty_like(self.io_out, device="cpu").pin_memory() for _ in range(2)]
         self.out_ready = [None, None]
         self.out_sum = 0.0
         torch.cuda.synchronize()
@@ -357,11 +368,9 @@ class DecodeBatch:
             self.slot_ready[buf] = ev
             sess.sync()
             self.launches += 1
+            if host_io:  # the step's inputs, both layers, one copy
+                self.io_in.copy_(self.h_in, non_blocking=True)
             for i in range(2):
-                if host_io:
-                    self.q[i].copy_(self.h_q[i], non_blocking=True)
-                    self.kn[i].copy_(self.h_kn[i], non_blocking=True)
-                    self.vn[i].copy_(self.h_vn[i], non_blocking=True)
                 if time_full_decode and i == 0:
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
@@ -371,10 +380,9 @@ class DecodeBatch:
                 if time_full_decode and i == 0:
                     e1.record(self.stream)
                     self.decode_events.append((e0, e1))
-                if host_io:
-                    self.h_o[buf][i].copy_(self.o[i], non_blocking=True)
                 self.launches += 3
-            if host_io:
+            if host_io:  # the step's outputs, both layers, one copy
+                self.h_o[buf].copy_(self.io_out, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(self.stream)
                 self.out_ready[buf] = ev
@@ -389,7 +397,7 @@ class DecodeBatch:
         if self.out_ready[buf] is not None:
             self.out_ready[buf].synchronize()
             self.out_ready[buf] = None
-            self.out_sum += float(self.h_o[buf][0][0, 0, 0]) + float(self.h_o[buf][1][-1, -1, -1])
+            self.out_sum += float(self.h_o[buf][0]) + float(self.h_o[buf][-1])
 
     def breakdown(self, steps):
         """Average device time of each call of the decode step (events around
