@@ -1019,9 +1019,9 @@ def run_decode(args, world, rank, local):
     if not args.no_tree:
         pt = measure_prefix_tree()
         line["prefix_tree"] = {
-            "workload": "64 requests sharing a 16384-token system prompt + 4096 own tokens each, W 128, P 64; "
+            "workload": "1000 requests sharing a 16384-token system prompt + 4096 own tokens each, W 128, P 64; "
                         "chunked prefill storing each chunk's prefix after its release, then a follow-up turn "
-                        "each (host bookkeeping)",
+                        "each (host bookkeeping)", "tree_nodes": pt["nodes"],
             "unit": "us per call (median)", "match_us": round(pt["match"], 1), "share_us": round(pt["share"], 1),
             "insert_us": round(pt["insert"], 1), "evict_64_pages_us": round(pt["evict"], 1),
             "follow_up_full_hits": "%d/%d" % (pt["follow_up_hits"], pt["requests"])}
@@ -1186,7 +1186,7 @@ def measure_hybrid70(steps, warmup, n_seqs=None):
     return out
 
 
-def measure_prefix_tree(n_req=64, prompt=16384, turn=4096, reps=3):
+def measure_prefix_tree(n_req=1000, prompt=16384, turn=4096, reps=1):
     """Host cost of the SWA-aware prefix cache tree (bookkeeping only, no
     device memory): n_req requests share a prompt-token system prompt, each
     adds turn tokens of its own, runs as a chunked prefill (4096-token chunks,
@@ -1230,6 +1230,7 @@ def measure_prefix_tree(n_req=64, prompt=16384, turn=4096, reps=3):
                 H.hswa_tree_insert(tree, s, toks[:L])
                 t["insert"].append(time.perf_counter() - t0)
             H.hswa_seq_free(pool, [s])
+        nodes = H.hswa_tree_stats(tree)[0]
         hits = 0
         for s, toks in enumerate(reqs):  # follow-up turns
             follow = np.concatenate([toks, np.ones(100, np.int32)])
@@ -1245,6 +1246,7 @@ def measure_prefix_tree(n_req=64, prompt=16384, turn=4096, reps=3):
     out = {k: float(np.median(v)) * 1e6 for k, v in t.items()}
     out["follow_up_hits"] = hits
     out["requests"] = n_req
+    out["nodes"] = nodes
     return out
 
 

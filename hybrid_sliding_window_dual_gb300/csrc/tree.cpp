@@ -15,10 +15,17 @@
 // no node holds it. Every choice is deterministic (a logical clock advanced
 // by each match and insert, then creation order), so the tree and the pool
 // tables are a function of the call sequence.
+//
+// Eviction is incremental: the leaves are kept ordered by (clock, id) and
+// the nodes holding an SWA page by (inside a window, clock, id), where
+// "inside a window" depends on the shallowest leaf below the node, which is
+// kept per node and updated upward only when the tree's shape changes. A
+// call then costs O((pages freed + held pages passed over) log n) instead of
+// a pass over the whole tree.
 #include <algorithm>
 #include <map>
 #include <new>
-#include <queue>
+#include <set>
 #include <tuple>
 #include <unordered_map>
 #include <vector>
@@ -32,6 +39,7 @@ struct TreeNode {
     int32_t index = -1;  // logical page index of the page in its sequences
     int32_t full = -1, swa = -1;
     uint64_t last = 0;   // clock of the last match or insert through the node
+    int64_t dmin = 0;    // pages of the shallowest leaf at or below the node
     TreeNode *parent = nullptr;
     std::vector<int32_t> tokens;  // the page's P tokens
     uint64_t hash = 0;            // of tokens
@@ -59,6 +67,9 @@ TreeNode *find_child(TreeNode *node, const int32_t *t, int64_t n, uint64_t h) {
     return nullptr;
 }
 
+using LeafKey = std::pair<uint64_t, int32_t>;       // (last, id)
+using SwaKey = std::tuple<int, uint64_t, int32_t>;  // (inside a window, last, id)
+
 }  // namespace
 
 struct hswa_tree {
@@ -66,10 +77,50 @@ struct hswa_tree {
     TreeNode root;
     uint64_t clock = 0;
     int32_t next_id = 0;
+    int32_t n_swa = 0;                    // nodes holding an SWA page
     std::map<int32_t, TreeNode *> nodes;  // every node but the root, by id
+    std::set<LeafKey> leaves;             // every leaf
+    std::set<SwaKey> swa_nodes;           // every node holding an SWA page
 };
 
 namespace {
+
+bool in_window(const hswa_tree *t, const TreeNode *nd) {
+    const int64_t P = t->pool->cfg.page_size, W = t->pool->cfg.window;
+    return nd->index >= std::max<int64_t>(0, nd->dmin * P - W) / P;
+}
+
+// Take a node out of the ordered sets before one of its keys (last, dmin,
+// SWA page, children) changes, and put it back afterwards.
+void unindex(hswa_tree *t, const TreeNode *nd) {
+    if (nd->children.empty()) t->leaves.erase(LeafKey(nd->last, nd->id));
+    if (nd->swa >= 0) t->swa_nodes.erase(SwaKey(in_window(t, nd) ? 1 : 0, nd->last, nd->id));
+}
+
+void reindex(hswa_tree *t, const TreeNode *nd) {
+    if (nd->children.empty()) t->leaves.insert(LeafKey(nd->last, nd->id));
+    if (nd->swa >= 0) t->swa_nodes.insert(SwaKey(in_window(t, nd) ? 1 : 0, nd->last, nd->id));
+}
+
+// Recompute the shallowest-leaf depth from nd up to the root, stopping where
+// it no longer changes.
+void update_dmin_up(hswa_tree *t, TreeNode *nd) {
+    for (; nd && nd != &t->root; nd = nd->parent) {
+        int64_t d = nd->children.empty() ? (int64_t)nd->index + 1 : INT64_MAX;
+        for (auto &ch : nd->children) d = std::min(d, ch.second->dmin);
+        if (d == nd->dmin) return;
+        unindex(t, nd);
+        nd->dmin = d;
+        reindex(t, nd);
+    }
+}
+
+void touch(hswa_tree *t, TreeNode *nd, uint64_t clock) {
+    if (nd->last == clock) return;
+    unindex(t, nd);
+    nd->last = clock;
+    reindex(t, nd);
+}
 
 // Largest m <= n with an SWA page on every logical page that meets the last
 // W positions [m*P - W, m*P) of an m-page prefix.
@@ -85,15 +136,24 @@ int32_t window_safe_pages(const std::vector<TreeNode *> &path, int64_t P, int64_
     return 0;
 }
 
-void remove_node(hswa_tree *t, TreeNode *nd) {
-    auto range = nd->parent->children.equal_range(nd->hash);
+// Remove a leaf (its pages already let go of) and update its parent.
+void remove_leaf(hswa_tree *t, TreeNode *nd) {
+    unindex(t, nd);
+    if (nd->swa >= 0) --t->n_swa;
+    TreeNode *parent = nd->parent;
+    if (parent != &t->root) unindex(t, parent);
+    auto range = parent->children.equal_range(nd->hash);
     for (auto it = range.first; it != range.second; ++it)
         if (it->second == nd) {
-            nd->parent->children.erase(it);
+            parent->children.erase(it);
             break;
         }
     t->nodes.erase(nd->id);
     delete nd;
+    if (parent != &t->root) {
+        reindex(t, parent);  // a leaf now, if that was its last child
+        update_dmin_up(t, parent);
+    }
 }
 
 }  // namespace
@@ -139,7 +199,7 @@ extern "C" int hswa_tree_match(hswa_tree *t, const int32_t *tokens, int64_t n_to
         if (!node) break;
         path.push_back(node);
     }
-    for (TreeNode *nd : path) nd->last = t->clock;
+    for (TreeNode *nd : path) touch(t, nd, t->clock);
     const int32_t m = window_safe_pages(path, P, W);
     for (int32_t p = 0; p < m; ++p) {
         full_pages_out[p] = path[p]->full;
@@ -161,8 +221,9 @@ extern "C" int hswa_tree_insert(hswa_tree *t, int32_t seq_id, const int32_t *tok
     const int32_t *srow = &pool->swa_bt[(int64_t)seq_id * MP];
     for (int64_t p = 0; p < n_pages; ++p)
         if (frow[p] < 0) return HSWA_ERR_INVALID_ARG;
-    ++t->clock;
+    const uint64_t clock = ++t->clock;
     TreeNode *node = &t->root;
+    bool grew = false;
     int32_t created = 0;
     for (int64_t p = 0; p < n_pages; ++p) {
         const int32_t *pt = tokens + p * P;
@@ -177,20 +238,44 @@ extern "C" int hswa_tree_insert(hswa_tree *t, int32_t seq_id, const int32_t *tok
             nxt->parent = node;
             nxt->tokens.assign(pt, pt + P);
             nxt->hash = h;
+            nxt->last = clock;
+            nxt->dmin = p + 1;
             pool->ref_full(nxt->full);
-            if (nxt->swa >= 0) pool->ref_swa(nxt->swa);
+            if (nxt->swa >= 0) {
+                pool->ref_swa(nxt->swa);
+                ++t->n_swa;
+            }
+            if (node != &t->root) unindex(t, node);  // it may stop being a leaf
             node->children.emplace(h, nxt);
+            if (node != &t->root) reindex(t, node);
+            reindex(t, nxt);
             t->nodes.emplace(nxt->id, nxt);
+            grew = true;
             ++created;
         } else {
             if (nxt->swa < 0 && srow[p] >= 0) {  // the sequence recomputed a lost window page
+                unindex(t, nxt);
                 nxt->swa = srow[p];
                 pool->ref_swa(nxt->swa);
+                ++t->n_swa;
+                reindex(t, nxt);
             }
+            touch(t, nxt, clock);
         }
-        nxt->last = t->clock;
         node = nxt;
     }
+    // the new nodes form one chain ending at a leaf (each started with its
+    // own depth): recompute the depths bottom up along the whole path
+    if (grew)
+        for (TreeNode *nd = node; nd != &t->root; nd = nd->parent) {
+            int64_t d = nd->children.empty() ? (int64_t)nd->index + 1 : INT64_MAX;
+            for (auto &ch : nd->children) d = std::min(d, ch.second->dmin);
+            if (d != nd->dmin) {
+                unindex(t, nd);
+                nd->dmin = d;
+                reindex(t, nd);
+            }
+        }
     if (n_new_out) *n_new_out = created;
     return HSWA_OK;
 }
@@ -199,56 +284,38 @@ extern "C" int hswa_tree_evict(hswa_tree *t, int32_t want_full, int32_t want_swa
                                int32_t *freed_swa_out) {
     if (!t || want_full < 0 || want_swa < 0) return HSWA_ERR_INVALID_ARG;
     hswa_pool *pool = t->pool;
-    const int64_t P = pool->cfg.page_size, W = pool->cfg.window;
     int32_t freed_full = 0, freed_swa = 0;
-    if (want_swa > 0) {
-        // pages of the shallowest leaf at or below each node; children are
-        // newer than their parents, so descending ids visit children first
-        std::vector<int64_t> dmin(t->next_id, INT64_MAX);
-        for (auto it = t->nodes.rbegin(); it != t->nodes.rend(); ++it) {
-            TreeNode *nd = it->second;
-            int64_t d = nd->children.empty() ? (int64_t)nd->index + 1 : INT64_MAX;
-            for (auto &ch : nd->children) d = std::min(d, dmin[ch.second->id]);
-            dmin[nd->id] = d;
+    // SWA pages only the tree holds: outside every window below them first,
+    // then inside; oldest first, then creation order. Freeing one node's SWA
+    // page moves no other node in the order.
+    for (auto it = t->swa_nodes.begin(); freed_swa < want_swa && it != t->swa_nodes.end();) {
+        TreeNode *nd = t->nodes.at(std::get<2>(*it));
+        if (pool->swa_ref[nd->swa] != 1) {
+            ++it;
+            continue;
         }
-        // SWA pages only the tree holds: outside every window below them
-        // first, then inside; oldest first, then creation order
-        std::vector<std::tuple<int, uint64_t, int32_t, TreeNode *>> cands;
-        for (auto &kv : t->nodes) {
-            TreeNode *nd = kv.second;
-            if (nd->swa < 0 || pool->swa_ref[nd->swa] != 1) continue;
-            const bool in_window = nd->index >= std::max<int64_t>(0, dmin[nd->id] * P - W) / P;
-            cands.emplace_back(in_window ? 1 : 0, nd->last, nd->id, nd);
-        }
-        std::sort(cands.begin(), cands.end(), [](const auto &a, const auto &b) {
-            return std::make_tuple(std::get<0>(a), std::get<1>(a), std::get<2>(a)) <
-                   std::make_tuple(std::get<0>(b), std::get<1>(b), std::get<2>(b));
-        });
-        for (auto &c : cands) {
-            if (freed_swa >= want_swa) break;
-            TreeNode *nd = std::get<3>(c);
-            freed_swa += pool->unref_swa(nd->swa);
-            nd->swa = -1;
-        }
+        it = t->swa_nodes.erase(it);
+        freed_swa += pool->unref_swa(nd->swa);
+        nd->swa = -1;
+        --t->n_swa;
     }
-    if (want_full > 0) {
-        // leaves whose Full page only the tree holds, oldest first; a parent
-        // left without children joins the candidates
-        using Key = std::pair<uint64_t, int32_t>;
-        std::priority_queue<Key, std::vector<Key>, std::greater<Key>> heap;
-        auto evictable = [&](TreeNode *nd) { return nd->children.empty() && pool->full_ref[nd->full] == 1; };
-        for (auto &kv : t->nodes)
-            if (evictable(kv.second)) heap.emplace(kv.second->last, kv.second->id);
-        while (freed_full < want_full && !heap.empty()) {
-            TreeNode *nd = t->nodes.at(heap.top().second);
-            heap.pop();
-            TreeNode *parent = nd->parent;
-            freed_full += pool->unref_full(nd->full);
-            if (nd->swa >= 0) freed_swa += pool->unref_swa(nd->swa);
-            remove_node(t, nd);
-            if (parent != &t->root && evictable(parent)) heap.emplace(parent->last, parent->id);
+    // leaves whose Full page only the tree holds, oldest first; a parent left
+    // without children becomes a leaf and a candidate. Leaves held by a
+    // sequence are set aside for the rest of the call.
+    std::vector<LeafKey> held;
+    while (freed_full < want_full && !t->leaves.empty()) {
+        const LeafKey k = *t->leaves.begin();
+        TreeNode *nd = t->nodes.at(k.second);
+        if (pool->full_ref[nd->full] != 1) {
+            held.push_back(k);
+            t->leaves.erase(t->leaves.begin());
+            continue;
         }
+        freed_full += pool->unref_full(nd->full);
+        if (nd->swa >= 0) freed_swa += pool->unref_swa(nd->swa);
+        remove_leaf(t, nd);
     }
+    for (const LeafKey &k : held) t->leaves.insert(k);
     if (freed_full_out) *freed_full_out = freed_full;
     if (freed_swa_out) *freed_swa_out = freed_swa;
     return HSWA_OK;
@@ -256,11 +323,9 @@ extern "C" int hswa_tree_evict(hswa_tree *t, int32_t want_full, int32_t want_swa
 
 extern "C" int hswa_tree_stats(const hswa_tree *t, int32_t *n_nodes, int32_t *full_held, int32_t *swa_held) {
     if (!t) return HSWA_ERR_INVALID_ARG;
-    int32_t swa = 0;
-    for (auto &kv : t->nodes) swa += kv.second->swa >= 0;
     if (n_nodes) *n_nodes = (int32_t)t->nodes.size();
     if (full_held) *full_held = (int32_t)t->nodes.size();
-    if (swa_held) *swa_held = swa;
+    if (swa_held) *swa_held = t->n_swa;
     return HSWA_OK;
 }
 
