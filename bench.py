@@ -877,6 +877,8 @@ def time_steps(run, steps, stream, world):
 def workload(args, name):
     if name == "decode_batch":
         w = wl.decode_batch()
+    elif name == "swa_transfer":
+        w = wl.swa_transfer()
     else:
         w = wl.chunked_prefill()
     if args.seqs:
@@ -1250,9 +1252,9 @@ def measure_prefix_tree(n_req=1000, prompt=16384, turn=4096, reps=1):
     return out
 
 
-def measure_transfer(steps, fp8=False):
+def measure_transfer(steps, fp8=False, w=None):
     import torch
-    w = wl.swa_transfer()
+    w = w or wl.swa_transfer()
     tb = SwaTransfer(w, fp8=fp8)
     moved = tb.moved_bytes() * len(w.layer_kinds)
     # warm-up round trip
@@ -1308,6 +1310,24 @@ def measure_transfer(steps, fp8=False):
     return out
 
 
+def run_transfer_line(args, world, rank, local):
+    """--workload swa_transfer: one line whose value is the gather's GB/s into
+    pinned host memory (the 60-layer in-window transfer; --seqs cuts it to a
+    small profiling case)."""
+    w = workload(args, "swa_transfer")
+    t = measure_transfer(max(1, args.steps), fp8=args.fp8_pools, w=w)
+    return {
+        "metric": "Hybrid-SWA attn: SWA-mask transfer GB/s into pinned host memory",
+        "value": round(t["gather_gbs"], 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": 1, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8" if args.fp8_pools else "bf16", "data": "synthetic",
+        "config": {"workload": "swa_transfer", "seqs": len(w.cached), "layers": len(w.layer_kinds),
+                   "window": w.window, "gb_each_way": round(t["bytes_each_way"] / 1e9, 3)},
+        "scatter_gbs": round(t["scatter_gbs"], 2), "memcpy_d2h_gbs": round(t["memcpy_d2h_gbs"], 2),
+        "memcpy_h2d_gbs": round(t["memcpy_h2d_gbs"], 2), "gpu_launches": t["launches"],
+    }
+
+
 def run_prefill_line(args, world, rank, local):
     """--workload chunked_prefill: one line whose value is the chunk's TFLOP/s."""
     w = workload(args, "chunked_prefill")
@@ -1347,7 +1367,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="hswa", choices=["hswa", "reference"])
-    ap.add_argument("--workload", default="decode_batch", choices=["decode_batch", "chunked_prefill"])
+    ap.add_argument("--workload", default="decode_batch", choices=["decode_batch", "chunked_prefill", "swa_transfer"])
+    ap.add_argument("--fp8-pools", action="store_true", help="swa_transfer over FP8 pools")
     ap.add_argument("--seqs", type=int, default=0, help="use only the first N sequences (small profiling case)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1371,6 +1392,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.workload == "chunked_prefill":
         line = run_prefill_line(args, world, rank, local)
+    elif args.workload == "swa_transfer":
+        line = run_transfer_line(args, world, rank, local)
     else:
         line = run_decode(args, world, rank, local)
     if rank == 0:
