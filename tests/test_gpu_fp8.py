@@ -22,19 +22,6 @@ FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
 HQ, HKV, D, P, W = 64, 8, 128, 64, 128
 
 
-def seeded_codes(shape, seed):
-    """Random E4M3 codes without the NaN patterns 0x7f / 0xff."""
-    g = torch.Generator().manual_seed(seed)
-    mag = torch.randint(0, 0x7F, shape, generator=g, dtype=torch.int32)
-    sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int32) << 7
-    return (mag | sign).to(torch.uint8)
-
-
-def seeded_scales(shape, seed):
-    g = torch.Generator().manual_seed(seed)
-    return 0.001 + 0.01 * torch.rand(shape, generator=g, dtype=torch.float32)
-
-
 class Fp8Case:
     def __init__(self, cached, seed, kinds=(FULL, SWA), extra=8):
         B = len(cached)
@@ -56,11 +43,20 @@ class Fp8Case:
                 assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
                 assert self.sess.release([s]) == self.ora.swa_release([s])
         self.sess.sync()
-        for i in range(len(kinds)):
+        for i in range(len(kinds)):  # seeded on the device (the full-size pools hold GBs of codes)
             for t, seed_i in ((self.sess.k[i], 10), (self.sess.v[i], 20)):
-                t.copy_(seeded_codes(tuple(t.shape), seed * 100 + seed_i + i))
+                g = torch.Generator(device="cuda")
+                g.manual_seed(seed * 100 + seed_i + i)
+                flat = t.view(-1)
+                for j in range(0, flat.numel(), 1 << 28):
+                    n = min(1 << 28, flat.numel() - j)
+                    mag = torch.randint(0, 0x7F, (n,), generator=g, device="cuda", dtype=torch.uint8)
+                    sgn = torch.randint(0, 2, (n,), generator=g, device="cuda", dtype=torch.uint8)
+                    flat[j:j + n] = mag | (sgn << 7)
             for t, seed_i in ((self.sess.ks[i], 30), (self.sess.vs[i], 40)):
-                t.copy_(seeded_scales(tuple(t.shape), seed * 100 + seed_i + i))
+                g = torch.Generator(device="cuda")
+                g.manual_seed(seed * 100 + seed_i + i)
+                t.copy_(0.001 + 0.01 * torch.rand(t.shape, generator=g, device="cuda"))
         torch.cuda.synchronize()
         self.host = [[x.cpu().numpy().copy() for x in (self.sess.k[i], self.sess.ks[i], self.sess.v[i],
                                                         self.sess.vs[i])] for i in range(len(kinds))]
@@ -236,3 +232,77 @@ def test_fp8_gather_scatter_round_trip(dst_host):
         assert c.sess.check() == 0
         assert H.hswa_last_kernel() == "swa_scatter_fp8"
         assert np.array_equal(fp8_window_pack(c, layer, lens), bufs[layer][1])
+
+
+@pytest.mark.gpu
+def test_fp8_decode_batch_full_size_sampled():
+    """The decode-batch workload (64 sequences, cached lengths uniform in
+    [1024, 32768], 64/8 heads) over FP8 pools, in the launch configuration
+    the benchmark times: one fused append + decode step per layer, oracle on
+    sampled sequences."""
+    w = wl.decode_batch()
+    c = Fp8Case(list(w.cached), seed=81)
+    B = c.B
+    fs, ss = c.sess.reserve(range(B), [1] * B)
+    efs, ess = c.ora.reserve(range(B), [1] * B)
+    assert np.array_equal(fs, efs) and np.array_equal(ss, ess)
+    c.sess.sync()
+    samples = [0, 1, 17, 31, 32, 50, 63]
+    scale = 1 / math.sqrt(D)
+    for layer, kind in enumerate(c.kinds):
+        slots = fs if kind == FULL else ss
+        q = wl.normal((B, HQ, D), 900 + layer, wl.DTYPE_BF16)
+        kn = wl.normal((B, HKV, D), 910 + layer, wl.DTYPE_BF16)
+        vn = wl.normal((B, HKV, D), 920 + layer, wl.DTYPE_BF16)
+        o = torch.full((B, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        c.sess.decode_append(layer, q.cuda(), kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"), o, B,
+                             scale)
+        assert c.sess.check() == 0
+        kc, ks, vc, vs = (x.cpu().numpy() for x in (c.sess.k[layer], c.sess.ks[layer], c.sess.v[layer],
+                                                     c.sess.vs[layer]))
+        exp = oracle.attention_fp8(raw_host(q)[samples], kc, ks, vc, vs, c.table(layer), np.array(samples),
+                                   c.ora.seq_len[samples] - 1, 0 if kind == FULL else W, scale)
+        got = o.float().cpu().numpy()[samples]
+        assert np.isfinite(got).all()
+        assert float(np.abs(got - exp).max()) <= 2e-2, layer
+
+
+@pytest.mark.gpu
+def test_fp8_chunked_prefill_full_size_sampled():
+    """The chunked-prefill workload (8 sequences, prefixes uniform in
+    [8192, 65536], a 4096-token chunk each) over FP8 pools: the staging pass
+    and the fp16 tensor-core kernel at full size, oracle on rows at the tile
+    edges and the chunk ends of every sequence."""
+    w = wl.chunked_prefill()
+    C = w.n_new
+    c = Fp8Case(list(w.cached), seed=82, extra=C + 8)
+    B = c.B
+    fs, ss = c.sess.reserve(range(B), [C] * B)
+    efs, ess = c.ora.reserve(range(B), [C] * B)
+    assert np.array_equal(fs, efs) and np.array_equal(ss, ess)
+    c.sess.sync()
+    prefix = np.array(w.cached, np.int64)
+    d_prefix = torch.as_tensor(prefix.astype(np.int32), device="cuda")
+    d_qs = torch.arange(0, B * C + 1, C, dtype=torch.int32, device="cuda")
+    rows_in_chunk = [0, 1, 127, 128, 129, 2047, 4094, 4095]
+    rows = np.array([s * C + r for s in range(B) for r in rows_in_chunk])
+    q_seq = np.repeat(np.arange(B), len(rows_in_chunk))
+    q_pos = np.array([prefix[s] + r for s in range(B) for r in rows_in_chunk])
+    scale = 1 / math.sqrt(D)
+    for layer, kind in enumerate(c.kinds):
+        slots = fs if kind == FULL else ss
+        q = wl.normal((B * C, HQ, D), 930 + layer, wl.DTYPE_BF16)
+        kn = wl.normal((B * C, HKV, D), 940 + layer, wl.DTYPE_BF16)
+        vn = wl.normal((B * C, HKV, D), 950 + layer, wl.DTYPE_BF16)
+        c.sess.append(layer, kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"))
+        o = torch.full((B * C, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, C, scale)
+        assert c.sess.check() == 0
+        assert H.hswa_last_kernel() == "prefill_stage_fp8+prefill_tc_bf16_d128<f16>"
+        kc, ks, vc, vs = (x.cpu().numpy() for x in (c.sess.k[layer], c.sess.ks[layer], c.sess.v[layer],
+                                                     c.sess.vs[layer]))
+        exp = oracle.attention_fp8(raw_host(q)[rows], kc, ks, vc, vs, c.table(layer), q_seq, q_pos,
+                                   0 if kind == FULL else W, scale)
+        got = o.float().cpu().numpy()[rows]
+        assert np.isfinite(got).all()
+        assert float(np.abs(got - exp).max()) <= 2e-2, layer
