@@ -44,8 +44,8 @@ KV_ROW = {wl.DTYPE_BF16: 2, wl.DTYPE_F32: 4}
 # DRAM traffic of the decode kernel per launch over its algorithmic bytes, from
 # one ncu capture at full size (profiles/decode_mma_bf16_d128_decode_batch_traffic.md),
 # valid only for the kernel sources it was taken on.
-DECODE_TRAFFIC = {"ratio": 1.0030, "sources": ("decode.cu", "common.cuh"),
-                  "sha256": "88d7565fbf62b8f26e94d064691e0b4dbcbb4fb2b6486539b3a5b8c67a8442df"}
+DECODE_TRAFFIC = {"ratio": 1.0029, "sources": ("decode.cu", "common.cuh"),
+                  "sha256": "e4cadfbcb0c45aa494681a6e3dcfa27da08f84e4b7d9ad711facdcc834b52325"}
 
 
 def source_digest(names):
@@ -216,14 +216,14 @@ def measure_decode_fp8(steps, warmup):
     return out
 
 
-def measure_decode_multi(reps, token_counts=(1, 2, 4, 8)):
+def measure_decode_multi(reps, w, token_counts=(1, 2, 4, 8, 16)):
     """Multi-token decode (n_tok query tokens per sequence at positions
     L - n_tok .. L - 1) over the decode-batch pools: one step is the Full and
     the SWA layer of hswa_decode_multi, events around each layer. Returns per
     n_tok the step time, query tokens/s and the Full layer's GB/s (KV bytes
     read once, q and o of every token)."""
     import torch
-    w = wl.decode_batch()
+    from hybrid_sliding_window_dual_gb300 import hswa_last_kernel
     bench = DecodeBatch(w, 8, hold=max(token_counts))
     sess, B, es = bench.sess, bench.B, KV_ROW[w.dtype]
     lens = bench.lens()
@@ -246,11 +246,12 @@ def measure_decode_multi(reps, token_counts=(1, 2, 4, 8)):
                     ev.append(e)
         bench.stream.synchronize()
         assert sess.check() == 0
+        kernel = hswa_last_kernel()
         full_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
         step_ms = float(np.mean([a.elapsed_time(c) for a, _, c in ev]))
         full_bytes = kv["full_kv"] + 2 * B * T * w.n_q_heads * w.head_dim * es
         out[T] = {"step_ms": step_ms, "full_layer_ms": full_ms, "tokens_per_s": B * T / (step_ms / 1e3),
-                  "full_layer_gbs": full_bytes / (full_ms / 1e3) / 1e9}
+                  "full_layer_gbs": full_bytes / (full_ms / 1e3) / 1e9, "kernel": kernel}
     bench.finish()
     del bench
     torch.cuda.empty_cache()
@@ -969,13 +970,13 @@ def run_decode(args, world, rank, local):
     if not args.no_multi:
         del bench
         torch.cuda.empty_cache()
-        mt = measure_decode_multi(50)
+        mt = measure_decode_multi(50, workload(args, "decode_batch"))
         base = mt[1]["step_ms"]
         line["multi_token_decode"] = {
             "workload": "decode_batch, n_tok query tokens per sequence (MTP / speculative verification), "
                         "Full + SWA layer per step, no append",
-            "kernel": "decode_mma_bf16_d128<n_tok>",
-            "by_n_tok": {str(T): {"step_ms": round(v["step_ms"], 4), "tokens_per_s": round(v["tokens_per_s"], 1),
+            "by_n_tok": {str(T): {"kernel": v["kernel"], "step_ms": round(v["step_ms"], 4),
+                                  "tokens_per_s": round(v["tokens_per_s"], 1),
                                   "full_layer_gbs": round(v["full_layer_gbs"], 1),
                                   "frac": round(v["full_layer_gbs"] / hbm, 4),
                                   "time_vs_1": round(v["step_ms"] / base, 3)} for T, v in mt.items()}}

@@ -28,7 +28,7 @@ HSWA_KIND_SWA = 1
 HSWA_DTYPE_F32 = 0
 HSWA_DTYPE_BF16 = 1
 HSWA_DTYPE_FP8_E4M3 = 2
-HSWA_DECODE_MAX_TOKENS = 8
+HSWA_DECODE_MAX_TOKENS = 16
 
 
 class HswaError(RuntimeError):

@@ -23,7 +23,7 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 
 SOURCES = ["runtime.cu", "decode.cu", "prefill.cu", "copy.cu", "pool.cpp", "tree.cpp"]
-HEADERS = ["common.cuh", "internal.h", "kernels.h"]
+HEADERS = ["common.cuh", "internal.h", "kernels.h", "tc.cuh"]
 
 FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

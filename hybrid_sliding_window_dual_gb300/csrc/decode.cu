@@ -19,6 +19,13 @@
 //     mma.m16n8k16, the 8 GQA heads filling N = 8), an online softmax in the
 //     log2 domain, transposes P with movmatrix and accumulates
 //     O^T += V^T P^T with V^T read by ldmatrix.trans.
+// Multi-token decode (n_tok query tokens per sequence at positions
+// L - n_tok .. L - 1: the MTP verification step of "MiMo-V2.5 Series
+// Inference Full-Link Optimization", Sec. 5.2, and the multi-token
+// verification of "Following the Bottleneck: Optimizing MiniMax M3 on AMD
+// Instinct MI355X", EAGLE3 section): up to 4 tokens the same kernel with one
+// consumer warp per token; 5 to 16 tokens a tcgen05 kernel whose
+// (token, head) rows form one M = 128 tile ("tensor-core multi-token" below).
 // Generic path (any dtype / head_dim / ratio / page): one warp per
 // (sequence, query head) with CUDA-core dot products.
 #include <algorithm>
@@ -30,6 +37,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace hswa {
 namespace {
@@ -56,6 +64,7 @@ template <int kTok_>
 struct DecodeSmemT {
     static constexpr int kTok = kTok_;
     static constexpr int kStages = kTok_ <= 2 ? ::hswa::kStages : 2;
+    static constexpr bool kTcQ = false;  // q rows travel with the first page of a piece
     uint8_t k[kStages][kPageHeadBytes];
     uint8_t v[kStages][kPageHeadBytes];
     uint8_t q[kStages][kTok * kQBytes];
@@ -79,6 +88,7 @@ constexpr int kConsumers8 = 4;  // FP8 consumer warps, one 16-key group of a pag
 
 struct DecodeSmem8 {
     static constexpr int kStages = 3;
+    static constexpr bool kTcQ = false;
     uint8_t k[kStages][kK8Bytes];
     uint8_t v[kStages][kV8Bytes];
     uint8_t q[kStages][kQBytes];
@@ -121,6 +131,10 @@ struct DecodeArgs {
     float scale_log2;
     int *err;
 };
+
+// Tensor-core multi-token decode: copies of the 8 n_tok query rows in the
+// 128-row tile (each copy takes 64 / copies keys of every page).
+__host__ __device__ constexpr int tc_copies(int n_tok) { return n_tok <= 4 ? 4 : n_tok <= 8 ? 2 : 1; }
 
 // Keys [lo, hi) that the last n_tok query tokens of a sequence with L keys
 // attend together (positions L - n_tok .. L - 1; W keys each for SWA).
@@ -203,20 +217,28 @@ __device__ __forceinline__ uint32_t swz(int row, int d) {
     return (uint32_t)((d >> 6) * kBoxBytes + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4));
 }
 
+// Streams the pages of units [u0, u1) into the stage ring. With
+// Smem::kTcQ the query tile of each piece goes by tensor map tq into the
+// two-slot q buffer (released by the MMA thread through q_empty) instead of
+// travelling in the stage of the piece's first page.
 template <bool kFP8, class Smem>
 __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeArgs &a,
-                                int64_t u0, int64_t u1) {
+                                int64_t u0, int64_t u1, const CUtensorMap *tq = nullptr) {
     constexpr int kStages = Smem::kStages;
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
         prefetch_tmap(tk);
         prefetch_tmap(tv);
+        if constexpr (Smem::kTcQ) prefetch_tmap(tq);
     }
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_parity[kStages];
     bool issued[kStages];
     for (int i = 0; i < kStages; ++i) issued[i] = false, issued_parity[i] = 0;
+    int32_t pc = 0;  // pieces started (kTcQ: q slot pc & 1)
+    bool q_issued[2] = {false, false};
+    uint32_t q_parity[2] = {0, 0};
 
     int64_t u = u0;
     int32_t s = 0;
@@ -277,7 +299,27 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
             }
             bool ok = true;
             if (lane == 0) {
-                ok = mbar_wait(&sm.empty[stage], phase ^ 1, a.err) && !*(volatile int32_t *)&sm.abort;
+                if constexpr (Smem::kTcQ) {
+                    if (j == 0) {
+                        // the piece's n_tok x 8 query rows (token, head), once
+                        // per copy: copy cp starts at tile row cp * 128 / R
+                        const int b = pc % Smem::kQBufs;
+                        const uint32_t par = (pc / Smem::kQBufs) & 1;
+                        const int copies = tc_copies(a.n_tok);
+                        ok = mbar_wait(&sm.q_empty[b], par ^ 1, a.err) && !*(volatile int32_t *)&sm.abort;
+                        if (ok) {
+                            mbar_arrive_expect_tx(&sm.q_full[b], copies * a.n_tok * kQBytes);
+                            for (int cp = 0; cp < copies; ++cp)
+                                for (int dh = 0; dh < 2; ++dh)
+                                    tma_load_3d(sm.q[b] + dh * Smem::kQHalfBytes + cp * (128 / copies) * 128, tq,
+                                                dh * 64, g * kG, s * a.n_tok, &sm.q_full[b]);
+                            q_issued[b] = true;
+                            q_parity[b] = par;
+                        }
+                        ++pc;
+                    }
+                }
+                ok = ok && mbar_wait(&sm.empty[stage], phase ^ 1, a.err) && !*(volatile int32_t *)&sm.abort;
                 if (ok) {
                     const int32_t lp = pf + pi + j;
                     const int32_t key0 = lp * kP;
@@ -297,7 +339,8 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                     }
                     d.flags = flags;
                     const uint32_t page_bytes = kFP8 ? kK8Bytes + kV8Bytes + 2 * kScaleBytes : 4 * kBoxBytes;
-                    const uint32_t bytes = (valid ? page_bytes : 0) + (j == 0 ? a.n_tok * kQBytes : 0);
+                    const uint32_t q_bytes = (!Smem::kTcQ && j == 0) ? a.n_tok * kQBytes : 0;
+                    const uint32_t bytes = (valid ? page_bytes : 0) + q_bytes;
                     if (bytes) {
                         mbar_arrive_expect_tx(&sm.full[stage], bytes);
                         if (valid) {
@@ -316,11 +359,13 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                                 tma_load_2d(sm.v[stage] + kBoxBytes, tv, 64, row, &sm.full[stage]);
                             }
                         }
-                        if (j == 0)  // the 8 query rows of each token of this kv head
-                            for (int w = 0; w < a.n_tok; ++w)
-                                bulk_g2s(sm.q[stage] + w * kQBytes,
-                                         a.q + (((int64_t)s * a.n_tok + w) * a.hq + (int64_t)g * kG) * kD, kQBytes,
-                                         &sm.full[stage]);
+                        if constexpr (!Smem::kTcQ) {
+                            if (j == 0)  // the 8 query rows of each token of this kv head
+                                for (int w = 0; w < a.n_tok; ++w)
+                                    bulk_g2s(sm.q[stage] + w * kQBytes,
+                                             a.q + (((int64_t)s * a.n_tok + w) * a.hq + (int64_t)g * kG) * kD,
+                                             kQBytes, &sm.full[stage]);
+                        }
                     } else {
                         mbar_arrive(&sm.full[stage]);
                     }
@@ -338,25 +383,26 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
     }
 drain:
     // never leave the CTA with copies still landing in its shared memory
-    if (lane == 0)
+    if (lane == 0) {
         for (int i = 0; i < kStages; ++i)
             if (issued[i]) mbar_wait(&sm.full[i], issued_parity[i], a.err);
+        if constexpr (Smem::kTcQ)
+            for (int b = 0; b < Smem::kQBufs; ++b)
+                if (q_issued[b]) mbar_wait(&sm.q_full[b], q_parity[b], a.err);
+    }
 }
 
-// One consumer warp: kTPW query tokens (w0 .. w0 + kTPW - 1) of the stage's
-// (sequence, kv head), 8 query heads each. Every K and V fragment read from
-// shared memory feeds the MMAs of all kTPW tokens.
-template <int kTok, int kTPW>
-__device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int64_t u0, int64_t u1, int w0) {
+// One consumer warp: query token w (8 query heads) of the stage's (sequence,
+// kv head).
+template <int kTok>
+__device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int64_t u0, int64_t u1, int w) {
     constexpr int kStages = DecodeSmemT<kTok>::kStages;
     const int lane = threadIdx.x & 31;
     const int gr = lane >> 2;  // fragment row group
     const int qd = lane & 3;   // fragment column pair
-    uint32_t qf[kTPW][8][2];
-    float oacc[kTPW][8][4];
-    float m0[kTPW], m1[kTPW], l0[kTPW], l1[kTPW];
-#pragma unroll
-    for (int j = 0; j < kTPW; ++j) m0[j] = m1[j] = -INFINITY, l0[j] = l1[j] = 0.f;
+    uint32_t qf[8][2];
+    float oacc[8][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     int stage = 0;
     uint32_t phase = 0;
     const uint32_t kbase = smem_u32(sm.k[0]), vbase = smem_u32(sm.v[0]);
@@ -370,108 +416,96 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
         }
         const StageDesc d = sm.desc[stage];
         if (d.flags & kFirst) {
+            const uint32_t *qs = reinterpret_cast<const uint32_t *>(sm.q[stage] + w * kQBytes);
 #pragma unroll
-            for (int j = 0; j < kTPW; ++j) {
-                // a token past n_tok has no query row loaded; its keys are all
-                // masked below and it writes nothing
-                const uint32_t *qs = reinterpret_cast<const uint32_t *>(sm.q[stage] + (w0 + j) * kQBytes);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    qf[j][ks][0] = qs[(gr * kD + ks * 16 + 2 * qd) >> 1];
-                    qf[j][ks][1] = qs[(gr * kD + ks * 16 + 8 + 2 * qd) >> 1];
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) oacc[j][i][0] = oacc[j][i][1] = oacc[j][i][2] = oacc[j][i][3] = 0.f;
-                m0[j] = m1[j] = -INFINITY;
-                l0[j] = l1[j] = 0.f;
+            for (int ks = 0; ks < 8; ++ks) {
+                qf[ks][0] = qs[(gr * kD + ks * 16 + 2 * qd) >> 1];
+                qf[ks][1] = qs[(gr * kD + ks * 16 + 8 + 2 * qd) >> 1];
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
         }
         if (!(d.flags & kSkip)) {
             const uint32_t kb = kbase + stage * kPageHeadBytes, vb = vbase + stage * kPageHeadBytes;
-            // S^T = K Q^T : 4 tiles of 16 keys, per token
-            float sacc[kTPW][4][4];
+            // S^T = K Q^T : 4 tiles of 16 keys
+            float sacc[4][4];
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
-#pragma unroll
-                for (int j = 0; j < kTPW; ++j) sacc[j][kt][0] = sacc[j][kt][1] = sacc[j][kt][2] = sacc[j][kt][3] = 0.f;
+                sacc[kt][0] = sacc[kt][1] = sacc[kt][2] = sacc[kt][3] = 0.f;
                 const int row = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(kb + swz(row, ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
-#pragma unroll
-                    for (int j = 0; j < kTPW; ++j) mma_bf16_16816(sacc[j][kt], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
+                    mma_bf16_16816(sacc[kt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
                 }
             }
-            uint32_t pb[kTPW][4][2];
+            // scale to log2 units and mask the keys this token does not see:
+            // its position is t = len - n_tok + w; keys (key0 + r) <= t and,
+            // for SWA, > t - W, inside the page's part of the range [lo, hi)
+            int32_t r_lo = d.lo, r_hi = d.hi;  // one token: the stage's range is its own
+            if constexpr (kTok > 1) {
+                const int32_t t = d.len - a.n_tok + w;
+                r_hi = min(d.hi, t - d.key0 + 1);
+                if (a.window > 0) r_lo = max(d.lo, t - a.window + 1 - d.key0);
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < kTPW; ++j) {
-                // scale to log2 units and mask the keys this token does not
-                // see: its position is t = len - n_tok + w; keys (key0 + r)
-                // <= t and, for SWA, > t - W, inside the page's part of the
-                // range [lo, hi)
-                int32_t r_lo = d.lo, r_hi = d.hi;  // one token: the stage's range is its own
-                if constexpr (kTok > 1) {
-                    const int w = w0 + j;
-                    const int32_t t = d.len - a.n_tok + w;
-                    r_hi = w < a.n_tok ? min(d.hi, t - d.key0 + 1) : 0;
-                    if (a.window > 0) r_lo = max(d.lo, t - a.window + 1 - d.key0);
-                }
-                float mx0 = -INFINITY, mx1 = -INFINITY;
+            for (int kt = 0; kt < 4; ++kt) {
+                const int r0 = kt * 16 + gr, r1 = r0 + 8;
+                const bool v0 = r0 >= r_lo && r0 < r_hi, v1 = r1 >= r_lo && r1 < r_hi;
+                sacc[kt][0] = v0 ? sacc[kt][0] * a.scale_log2 : -INFINITY;
+                sacc[kt][1] = v0 ? sacc[kt][1] * a.scale_log2 : -INFINITY;
+                sacc[kt][2] = v1 ? sacc[kt][2] * a.scale_log2 : -INFINITY;
+                sacc[kt][3] = v1 ? sacc[kt][3] * a.scale_log2 : -INFINITY;
+                mx0 = fmaxf(mx0, fmaxf(sacc[kt][0], sacc[kt][2]));
+                mx1 = fmaxf(mx1, fmaxf(sacc[kt][1], sacc[kt][3]));
+            }
 #pragma unroll
-                for (int kt = 0; kt < 4; ++kt) {
-                    const int r0 = kt * 16 + gr, r1 = r0 + 8;
-                    const bool v0 = r0 >= r_lo && r0 < r_hi, v1 = r1 >= r_lo && r1 < r_hi;
-                    sacc[j][kt][0] = v0 ? sacc[j][kt][0] * a.scale_log2 : -INFINITY;
-                    sacc[j][kt][1] = v0 ? sacc[j][kt][1] * a.scale_log2 : -INFINITY;
-                    sacc[j][kt][2] = v1 ? sacc[j][kt][2] * a.scale_log2 : -INFINITY;
-                    sacc[j][kt][3] = v1 ? sacc[j][kt][3] * a.scale_log2 : -INFINITY;
-                    mx0 = fmaxf(mx0, fmaxf(sacc[j][kt][0], sacc[j][kt][2]));
-                    mx1 = fmaxf(mx1, fmaxf(sacc[j][kt][1], sacc[j][kt][3]));
-                }
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            // with several tokens a page can hold no key that a token sees
+            // (n = -inf): then nothing is kept and P stays 0
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            float b0 = n0, b1 = n1, al0, al1;
+            if constexpr (kTok > 1) {
+                b0 = n0 == -INFINITY ? 0.f : n0;
+                b1 = n1 == -INFINITY ? 0.f : n1;
+                al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
+                al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
+            } else {  // a stage holds at least one key of the range: n0, n1 finite
+                al0 = fast_exp2(m0 - n0);
+                al1 = fast_exp2(m1 - n1);
+            }
+            m0 = n0;
+            m1 = n1;
+            float ps0 = 0.f, ps1 = 0.f;
+            uint32_t pb[4][2];
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                }
-                // with several tokens a page can hold no key that a token
-                // sees (n = -inf): then nothing is kept and P stays 0
-                const float n0 = fmaxf(m0[j], mx0), n1 = fmaxf(m1[j], mx1);
-                float b0 = n0, b1 = n1, al0, al1;
-                if constexpr (kTok > 1) {
-                    b0 = n0 == -INFINITY ? 0.f : n0;
-                    b1 = n1 == -INFINITY ? 0.f : n1;
-                    al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0[j] - n0);
-                    al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1[j] - n1);
-                } else {  // a stage holds at least one key of the range: n0, n1 finite
-                    al0 = fast_exp2(m0[j] - n0);
-                    al1 = fast_exp2(m1[j] - n1);
-                }
-                m0[j] = n0;
-                m1[j] = n1;
-                float ps0 = 0.f, ps1 = 0.f;
+            for (int kt = 0; kt < 4; ++kt) {
+                const float p0 = fast_exp2(sacc[kt][0] - b0), p1 = fast_exp2(sacc[kt][1] - b1);
+                const float p2 = fast_exp2(sacc[kt][2] - b0), p3 = fast_exp2(sacc[kt][3] - b1);
+                const uint32_t x0 = pack_bf16(p0, p1), x1 = pack_bf16(p2, p3);
+                // sum what the MMA will see (the bf16-rounded weights)
+                const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162 *>(&x0);
+                const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162 *>(&x1);
+                ps0 += __low2float(r0) + __low2float(r1);
+                ps1 += __high2float(r0) + __high2float(r1);
+                pb[kt][0] = movmatrix_t(x0);
+                pb[kt][1] = movmatrix_t(x1);
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
 #pragma unroll
-                for (int kt = 0; kt < 4; ++kt) {
-                    const float p0 = fast_exp2(sacc[j][kt][0] - b0), p1 = fast_exp2(sacc[j][kt][1] - b1);
-                    const float p2 = fast_exp2(sacc[j][kt][2] - b0), p3 = fast_exp2(sacc[j][kt][3] - b1);
-                    const uint32_t x0 = pack_bf16(p0, p1), x1 = pack_bf16(p2, p3);
-                    // sum what the MMA will see (the bf16-rounded weights)
-                    const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162 *>(&x0);
-                    const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162 *>(&x1);
-                    ps0 += __low2float(r0) + __low2float(r1);
-                    ps1 += __high2float(r0) + __high2float(r1);
-                    pb[j][kt][0] = movmatrix_t(x0);
-                    pb[j][kt][1] = movmatrix_t(x1);
-                }
-                l0[j] = l0[j] * al0 + ps0;
-                l1[j] = l1[j] * al1 + ps1;
-#pragma unroll
-                for (int dt = 0; dt < 8; ++dt) {
-                    oacc[j][dt][0] *= al0;
-                    oacc[j][dt][1] *= al1;
-                    oacc[j][dt][2] *= al0;
-                    oacc[j][dt][3] *= al1;
-                }
+            for (int dt = 0; dt < 8; ++dt) {
+                oacc[dt][0] *= al0;
+                oacc[dt][1] *= al1;
+                oacc[dt][2] *= al0;
+                oacc[dt][3] *= al1;
             }
             // O^T += V^T P^T
             const int jj = lane >> 3;
@@ -482,9 +516,7 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
                 for (int dt = 0; dt < 8; ++dt) {
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(vb + swz(key, dt * 16 + (jj & 1) * 8), a0, a1, a2, a3);
-#pragma unroll
-                    for (int j = 0; j < kTPW; ++j)
-                        mma_bf16_16816(oacc[j][dt], a0, a1, a2, a3, pb[j][kt][0], pb[j][kt][1]);
+                    mma_bf16_16816(oacc[dt], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
                 }
             }
         }
@@ -492,44 +524,38 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
 
         if (d.flags & kLast) {
+            float t0 = l0, t1 = l1;
 #pragma unroll
-            for (int j = 0; j < kTPW; ++j) {
-                const int w = w0 + j;
-                if (kTPW > 1 && w >= a.n_tok) break;
-                float t0 = l0[j], t1 = l1[j];
+            for (int off = 4; off < 32; off <<= 1) {
+                t0 += __shfl_xor_sync(0xffffffffu, t0, off);
+                t1 += __shfl_xor_sync(0xffffffffu, t1, off);
+            }
+            const int h0 = 2 * qd, h1 = 2 * qd + 1;
+            if (d.flags & kDirect) {
+                const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
+                __nv_bfloat16 *o0 = a.o + (((int64_t)d.seq * a.n_tok + w) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
+                __nv_bfloat16 *o1 = o0 + kD;
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    t0 += __shfl_xor_sync(0xffffffffu, t0, off);
-                    t1 += __shfl_xor_sync(0xffffffffu, t1, off);
+                for (int dt = 0; dt < 8; ++dt) {
+                    o0[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][0] * i0);
+                    o1[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][1] * i1);
+                    o0[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][2] * i0);
+                    o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][3] * i1);
                 }
-                const int h0 = 2 * qd, h1 = 2 * qd + 1;
-                if (d.flags & kDirect) {
-                    const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
-                    __nv_bfloat16 *o0 =
-                        a.o + (((int64_t)d.seq * a.n_tok + w) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
-                    __nv_bfloat16 *o1 = o0 + kD;
+            } else {
+                Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + w];
+                if (gr == 0) {
+                    p.m[h0] = m0;
+                    p.m[h1] = m1;
+                    p.l[h0] = t0;
+                    p.l[h1] = t1;
+                }
 #pragma unroll
-                    for (int dt = 0; dt < 8; ++dt) {
-                        o0[dt * 16 + gr] = __float2bfloat16_rn(oacc[j][dt][0] * i0);
-                        o1[dt * 16 + gr] = __float2bfloat16_rn(oacc[j][dt][1] * i1);
-                        o0[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[j][dt][2] * i0);
-                        o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[j][dt][3] * i1);
-                    }
-                } else {
-                    Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + w];
-                    if (gr == 0) {
-                        p.m[h0] = m0[j];
-                        p.m[h1] = m1[j];
-                        p.l[h0] = t0;
-                        p.l[h1] = t1;
-                    }
-#pragma unroll
-                    for (int dt = 0; dt < 8; ++dt) {
-                        p.o[h0][dt * 16 + gr] = oacc[j][dt][0];
-                        p.o[h1][dt * 16 + gr] = oacc[j][dt][1];
-                        p.o[h0][dt * 16 + gr + 8] = oacc[j][dt][2];
-                        p.o[h1][dt * 16 + gr + 8] = oacc[j][dt][3];
-                    }
+                for (int dt = 0; dt < 8; ++dt) {
+                    p.o[h0][dt * 16 + gr] = oacc[dt][0];
+                    p.o[h1][dt * 16 + gr] = oacc[dt][1];
+                    p.o[h0][dt * 16 + gr + 8] = oacc[dt][2];
+                    p.o[h1][dt * 16 + gr + 8] = oacc[dt][3];
                 }
             }
         }
@@ -537,20 +563,19 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
     }
 }
 
-// Consumer warps: kTok / kTPW, each with kTPW tokens; the last warp is the
-// producer. Warps whose first token is past n_tok stay idle.
-template <int kTok, int kTPW>
-__global__ void __launch_bounds__(32 * (kTok / kTPW + 1)) decode_mma_bf16_d128(const __grid_constant__ CUtensorMap tk,
-                                                                             const __grid_constant__ CUtensorMap tv,
-                                                                             DecodeArgs a) {
+// Consumer warps 0 .. kTok - 1, one query token each (warps past n_tok stay
+// idle); warp kTok is the producer.
+template <int kTok>
+__global__ void __launch_bounds__(32 * (kTok + 1)) decode_mma_bf16_d128(const __grid_constant__ CUtensorMap tk,
+                                                                      const __grid_constant__ CUtensorMap tv,
+                                                                      DecodeArgs a) {
     using Smem = DecodeSmemT<kTok>;
-    constexpr int kWarps = kTok / kTPW;
     extern __shared__ uint8_t raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     if (threadIdx.x == 0) {
         for (int i = 0; i < Smem::kStages; ++i) {
             mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], (a.n_tok + kTPW - 1) / kTPW);  // the active consumer warps
+            mbar_init(&sm.empty[i], a.n_tok);  // the active consumer warps
         }
         sm.abort = 0;
         fence_barrier_init();
@@ -562,10 +587,436 @@ __global__ void __launch_bounds__(32 * (kTok / kTPW + 1)) decode_mma_bf16_d128(c
     if (U == 0) return;
     const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
     const int warp = threadIdx.x >> 5;
-    if (warp == kWarps)
+    if (warp == kTok)
         decode_producer<false>(sm, &tk, &tv, a, u0, u1);
-    else if (warp * kTPW < a.n_tok)
-        decode_consumer<kTok, kTPW>(sm, a, u0, u1, warp * kTPW);
+    else if (warp < a.n_tok)
+        decode_consumer<kTok>(sm, a, u0, u1, warp);
+}
+
+// ------------------------------------------------ tensor-core multi-token
+// Multi-token decode on the 5th-generation tensor cores. The n_tok query
+// tokens x 8 query heads of a (sequence, kv head) are the rows of one
+// M = 128 tile, so every streamed page costs the same two MMA groups:
+//   S = Q K^T    8 x tcgen05.mma M128 N64 K16 (the page's 64 keys)
+//   O += P V     4 x tcgen05.mma M128 N128 K16, P read from TMEM
+// With 8 n_tok <= 128 / R the query rows are repeated R times (R = 4 up to
+// 4 tokens, 2 up to 8, else 1): copy c of a row sees only keys
+// [c 64 / R, (c + 1) 64 / R) of every page (its P is zero elsewhere) and
+// keeps its own running max and sum, so the softmax of a page is spread
+// over all four warps instead of one. At the end of a piece the copies of
+// a row are merged (weights 2^(m_c - M)) through shared memory.
+// TMEM (512 columns): S double buffer (2 x 64), P double buffer (2 x 32
+// packed bf16 pairs), O (128). Warp 4 streams pages (and each piece's q
+// tile by tensor map). Warp 5 allocates TMEM and one of its threads issues
+// the QK MMAs, one thread of warp 6 the PV MMAs: an MMA takes some 70 cycles
+// to issue and a barrier wait as long, too much for one thread per page.
+// The scores of page i + 1 run on the tensor cores while the softmax of
+// page i runs. Warps 0-3: one tile row per thread: mask, online softmax in
+// the log2 domain with the lazy 2^8 rescale of O, P to TMEM, and the
+// end-of-piece merge and output.
+struct DecodeTcSmem {
+    static constexpr int kStages = 4;
+    static constexpr int kQBufs = 2;
+    static constexpr bool kTcQ = true;
+    static constexpr uint32_t kQHalfBytes = 128 * 128;  // 128 rows x 64 columns of bf16
+    uint8_t k[kStages][kPageHeadBytes];                // [d half][64 keys][128 B], 128-byte swizzle
+    uint8_t v[kStages][kPageHeadBytes];
+    uint8_t q[kQBufs][2 * kQHalfBytes];                // [d half][128 rows][128 B]
+    float obuf[kD][32];                                // merge: one 32-row block of O, column-major
+    float ep_m[128], ep_l[128];                        // merge: (max, sum) of every tile row
+    StageDesc desc[kStages];
+    uint64_t full[kStages], empty[kStages];
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full[2], p_full[2];
+    uint64_t mma_done[2], ep_bar;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+static_assert(offsetof(DecodeTcSmem, v) % 1024 == 0 && offsetof(DecodeTcSmem, q) % 1024 == 0,
+              "128-byte swizzled tiles need 1024-byte alignment");
+constexpr size_t kDecodeTcSmemBytes = sizeof(DecodeTcSmem) + 1024;
+constexpr int kTcThreads = 224;
+constexpr int kTcCols = 512;
+constexpr uint32_t kTmemP = 128, kTmemO = 256;  // column offsets of P and O
+constexpr float kTcRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
+
+// Two threads issue the MMAs of the CTA's n pages, each in page order and
+// each waiting only on its own barriers:
+//   warp 5, lane 0: QK(i) once page i (and, on a piece's first page, its q
+//     tile) has landed and the softmax of page i - 2 has read S buffer i & 1;
+//     commits s_full, and q_empty after the last QK of a piece;
+//   warp 6, lane 0: PV(i) once P(i) is in TMEM; commits empty (the page's
+//     stage: K was read by QK(i) before P(i) existed).
+// A commit arrives once every MMA its thread issued before has completed.
+__device__ bool decode_tc_qk(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
+    constexpr int kStages = DecodeTcSmem::kStages, kQB = DecodeTcSmem::kQBufs;
+    constexpr uint32_t kIdQK = idesc_16(128, kP, false, false);
+    const uint32_t tb = sm.tmem_base, kb = smem_u32(sm.k[0]), qb = smem_u32(sm.q[0]);
+    int32_t pc = -1;  // piece of the last scored page
+    for (int64_t i = 0; i < n; ++i) {
+        const int st = (int)(i % kStages);
+        if (!mbar_wait(&sm.full[st], (uint32_t)(i / kStages) & 1, a.err)) return false;
+        const int32_t flags = sm.desc[st].flags;
+        if (flags & kFirst) {
+            ++pc;
+            if (!mbar_wait(&sm.q_full[pc % kQB], (uint32_t)(pc / kQB) & 1, a.err)) return false;
+        }
+        if (i >= 2 && !mbar_wait(&sm.p_full[i & 1], (uint32_t)((i - 2) >> 1) & 1, a.err)) return false;
+        if (*(volatile int32_t *)&sm.abort) return false;
+        tc_fence_after();
+        if (!(flags & kSkip)) {
+            const uint32_t q = qb + (pc % kQB) * 2 * DecodeTcSmem::kQHalfBytes, k = kb + st * kPageHeadBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tb + 64 * (uint32_t)(i & 1),
+                       sdesc(q + (kk >> 2) * DecodeTcSmem::kQHalfBytes + (kk & 3) * 32, 16, 1024),
+                       sdesc(k + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024), kIdQK, kk > 0);
+        }
+        mma_commit(&sm.s_full[i & 1]);
+        if (flags & kLast) mma_commit(&sm.q_empty[pc % kQB]);
+    }
+    return true;
+}
+
+__device__ bool decode_tc_pv(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
+    constexpr int kStages = DecodeTcSmem::kStages;
+    constexpr uint32_t kIdPV = idesc_16(128, kD, true, false);
+    const uint32_t tb = sm.tmem_base, vb = smem_u32(sm.v[0]);
+    bool fresh = true;  // no PV yet in the current piece: the next one overwrites O
+    for (int64_t i = 0; i < n; ++i) {
+        if (!mbar_wait(&sm.p_full[i & 1], (uint32_t)(i >> 1) & 1, a.err) || *(volatile int32_t *)&sm.abort)
+            return false;
+        const int st = (int)(i % kStages);
+        const int32_t flags = sm.desc[st].flags;
+        if (flags & kFirst) fresh = true;
+        tc_fence_after();
+        if (!(flags & kSkip)) {
+            const uint32_t tp = tb + kTmemP + 32 * (uint32_t)(i & 1), v = vb + st * kPageHeadBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tb + kTmemO, tp + kk * 8, sdesc(v + kk * 2048, kBoxBytes, 1024), kIdPV,
+                       (fresh && kk == 0) ? 0u : 1u);
+            fresh = false;
+        }
+        mma_commit(&sm.empty[st]);
+    }
+    return true;
+}
+
+// Run one issuer role, then make sure every MMA it issued has completed
+// before TMEM is freed.
+template <bool kQK>
+__device__ void decode_tc_issue(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
+    bool ok = kQK ? decode_tc_qk(sm, a, n) : decode_tc_pv(sm, a, n);
+    mma_commit(&sm.mma_done[kQK ? 0 : 1]);
+    if (!mbar_wait(&sm.mma_done[kQK ? 0 : 1], 0, a.err)) ok = false;
+    if (!ok) sm.abort = 1;
+}
+
+// S columns [col, col + kN) of this thread's lane.
+template <int kN>
+__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, uint32_t (&r)[kN]) {
+    if constexpr (kN == 16) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15}, [%16];"
+            : HSWA_R8(0), HSWA_R8(8)
+            : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" : HSWA_RW8(0), HSWA_RW8(8)::"memory");
+    } else {
+#pragma unroll
+        for (int c = 0; c < kN / 32; ++c) tmem_ld32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+#pragma unroll
+        for (int c = 0; c < kN / 32; ++c) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+    }
+}
+
+// kN packed P columns of this thread's lane.
+template <int kN>
+__device__ __forceinline__ void tmem_st_p(uint32_t taddr, const uint32_t (&r)[kN]) {
+    if constexpr (kN == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     HSWA_W8(0)
+                     : "memory");
+    } else {
+#pragma unroll
+        for (int c = 0; c < kN / 16; ++c) tmem_st16(taddr + 16 * c, r + 16 * c);
+    }
+}
+
+// Bounded arrival + wait on the softmax warps' own barrier (128 threads).
+__device__ __forceinline__ bool ep_sync(DecodeTcSmem &sm, uint32_t &phase, int *err) {
+    mbar_arrive(&sm.ep_bar);
+    const bool ok = mbar_wait(&sm.ep_bar, phase, err);
+    phase ^= 1;
+    return ok;
+}
+
+// Warps 0-3: thread r owns tile row r, copy c = r / (128 / kR) of query
+// row j = r % (128 / kR) (token j / 8, head j % 8), for every page. Copy c
+// reads S columns [c kK, (c + 1) kK) and writes its P there. A warp whose
+// rows are all padding does no TMEM work but takes part in every barrier.
+template <int kR>
+__device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
+    constexpr int kStages = DecodeTcSmem::kStages;
+    constexpr int kRows = 128 / kR;  // tile rows per copy
+    constexpr int kK = kP / kR;      // keys of a page per copy
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = threadIdx.x, c = r / kRows, j = r % kRows;
+    const int w = j >> 3, h = j & 7;
+    const bool active = (((warp * 32) % kRows) >> 3) < a.n_tok;  // uniform over the warp
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_o = sm.tmem_base + lane_off + kTmemO;
+    const uint32_t t_p = sm.tmem_base + lane_off + kTmemP + c * (kK / 2);
+    if constexpr (kR > 1) {
+        // P outside this copy's keys stays zero; the copy's own columns are
+        // rewritten on every page
+        uint32_t z[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) z[x] = 0u;
+        tmem_st32(sm.tmem_base + lane_off + kTmemP, z);
+        tmem_st32(sm.tmem_base + lane_off + kTmemP + 32, z);
+        tmem_wait_st();
+    }
+    float m_used = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of P
+    uint32_t ep_phase = 0;
+    bool ok = true;
+    for (int64_t i = 0; i < n && ok; ++i) {
+        const int st = (int)(i % kStages);
+        ok = mbar_wait(&sm.full[st], (uint32_t)(i / kStages) & 1, a.err) &&
+             mbar_wait(&sm.s_full[i & 1], (uint32_t)(i >> 1) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const StageDesc d = sm.desc[st];
+        if (d.flags & kFirst) m_used = -INFINITY, l = 0.f;
+        if (active) {
+            tc_fence_after();
+            uint32_t sr[kK];
+            tmem_ld_s<kK>(sm.tmem_base + lane_off + 64 * (uint32_t)(i & 1) + c * kK, sr);
+            // keys of the page this row's token sees, relative to the copy's
+            // first key: [lo_c, hi_c) (position t = len - n_tok + w; W keys
+            // ending at t for SWA)
+            const int32_t t = d.len - a.n_tok + w;
+            const int32_t base = d.key0 + c * kK;
+            int32_t hi_c = min(d.hi - c * kK, t - base + 1), lo_c = d.lo - c * kK;
+            if (a.window > 0) lo_c = max(lo_c, t - a.window + 1 - base);
+            if (w >= a.n_tok || (d.flags & kSkip)) hi_c = 0;
+            float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+            for (int x = 0; x < kK; ++x)
+                if (x >= hi_c || x < lo_c) sr[x] = __float_as_uint(-INFINITY);
+#pragma unroll
+            for (int x = 0; x < kK; x += 4) {
+                m0 = max3(m0, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
+                m1 = max3(m1, __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]));
+            }
+            const float mx = fmaxf(m0, m1) * a.scale_log2;
+            const bool need = mx > m_used + kTcRescaleLog2;
+            const bool resc = need && m_used != -INFINITY;
+            const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
+            if (need) m_used = mx;
+            const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+            const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
+            float2 sum2 = make_float2(0.f, 0.f);
+            uint32_t pk[kK / 2];
+#pragma unroll
+            for (int x = 0; x < kK / 2; ++x) {
+                const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])),
+                                            sc2, nm2);
+                const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+                sum2 = __fadd2_rn(sum2, p);
+                pk[x] = pack_bf16(p.x, p.y);
+            }
+            // P buffer i & 1 was last read by PV(i - 2): the empty barrier of
+            // its stage. Its next phase needs P(i + 2), and PV(i - 2 - kStages)
+            // was waited for two pages ago, so the parity test is exact.
+            if (i >= 2)
+                ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[(i - 2) % kStages],
+                                                       (uint32_t)((i - 2) / kStages) & 1, a.err));
+            if (!ok) break;
+            tmem_st_p<kK / 2>(t_p + 32 * (uint32_t)(i & 1), pk);
+            if (__any_sync(0xffffffffu, resc)) {  // never on a piece's first page
+                // O holds the piece's earlier pages once PV(i - 1) is done:
+                // the empty barrier of its stage (its next phase needs
+                // P(i + 3); PV(i - 1 - kStages) came before PV(i - 2)).
+                ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[(i - 1) % kStages],
+                                                       (uint32_t)((i - 1) / kStages) & 1, a.err));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t ov[32];
+                    tmem_ld32(t_o + 32 * cc, ov);
+                    tmem_wait_ld(ov);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
+                    tmem_st32(t_o + 32 * cc, ov);
+                }
+            }
+            l = l * alpha + (sum2.x + sum2.y);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[i & 1]);
+        if (!(d.flags & kLast)) continue;
+        // ---- end of the piece: O is final once PV(i) is done, i.e. the next
+        // phase of the empty barrier of page i's stage (PV(i - kStages) came
+        // before PV(i - 2); PV(i + kStages) needs P(i + kStages))
+        if (active) ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[st], (uint32_t)(i / kStages) & 1, a.err));
+        float M = m_used, L = l, wt = 1.f;
+        if constexpr (kR > 1) {
+            // merge the copies of each row: weights 2^(m_c - M); copy 0 adds
+            // the other copies' weighted rows into its own, 32 rows at a time
+            sm.ep_m[r] = m_used;
+            sm.ep_l[r] = l;
+            ok = ep_sync(sm, ep_phase, a.err) && ok;
+            M = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < kR; ++cc) M = fmaxf(M, sm.ep_m[cc * kRows + j]);
+            L = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kR; ++cc) {
+                const float mc = sm.ep_m[cc * kRows + j];
+                L += mc == -INFINITY ? 0.f : fast_exp2(mc - M) * sm.ep_l[cc * kRows + j];
+            }
+            wt = m_used == -INFINITY ? 0.f : fast_exp2(m_used - M);
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 1; cc < kR; ++cc) {
+#pragma unroll 1
+                for (int b = 0; b < kRows / 32; ++b) {
+                    if (active && ok && warp == (cc * kRows) / 32 + b) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t ov[32];
+                            tmem_ld32(t_o + 32 * q4, ov);
+                            tmem_wait_ld(ov);
+#pragma unroll
+                            for (int x = 0; x < 32; ++x) sm.obuf[32 * q4 + x][lane] = __uint_as_float(ov[x]) * wt;
+                        }
+                    }
+                    ok = ep_sync(sm, ep_phase, a.err) && ok;
+                    if (active && ok && warp == b) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t ov[32];
+                            tmem_ld32(t_o + 32 * q4, ov);
+                            tmem_wait_ld(ov);
+                            const float own = cc == 1 ? wt : 1.f;  // copy 0's own weight, applied once
+#pragma unroll
+                            for (int x = 0; x < 32; ++x)
+                                ov[x] = __float_as_uint(__uint_as_float(ov[x]) * own + sm.obuf[32 * q4 + x][lane]);
+                            tmem_st32(t_o + 32 * q4, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                    ok = ep_sync(sm, ep_phase, a.err) && ok;
+                }
+            }
+            wt = 1.f;
+        }
+        if (!ok) break;
+        if (!active || c != 0) continue;
+        tc_fence_after();
+        const bool row = w < a.n_tok;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        if (d.flags & kDirect) {
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                a.o + (((int64_t)d.seq * a.n_tok + (row ? w : 0)) * a.hq + (int64_t)d.kvh * kG + h) * kD);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + 32 * q4, ov);
+                tmem_wait_ld(ov);
+                if (row) {
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        // L = 0: no key seen, write zeros (O may be unset)
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = L > 0.f ? __uint_as_float(ov[8 * x + e]) * inv : 0.f;
+                        dst[q4 * 4 + x] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                                     pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    }
+                }
+            }
+        } else {
+            Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + (row ? w : 0)];
+            float4 *dst = reinterpret_cast<float4 *>(p.o[h]);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + 32 * q4, ov);
+                tmem_wait_ld(ov);
+                if (row) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        float f[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) f[e] = L > 0.f ? __uint_as_float(ov[4 * x + e]) : 0.f;
+                        dst[q4 * 8 + x] = make_float4(f[0], f[1], f[2], f[3]);
+                    }
+                }
+            }
+            if (row) {
+                p.m[h] = M;
+                p.l[h] = L;
+            }
+        }
+    }
+    if (!ok) sm.abort = 1;
+}
+
+template <int kR>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    decode_tc_bf16_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ CUtensorMap tv, DecodeArgs a) {
+    extern __shared__ uint8_t raw[];
+    DecodeTcSmem &sm =
+        *reinterpret_cast<DecodeTcSmem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < DecodeTcSmem::kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.q_full[b], 1);
+            mbar_init(&sm.q_empty[b], 1);
+            mbar_init(&sm.s_full[b], 1);
+            mbar_init(&sm.p_full[b], 128);
+        }
+        mbar_init(&sm.mma_done[0], 1);
+        mbar_init(&sm.mma_done[1], 1);
+        mbar_init(&sm.ep_bar, 128);
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) tmem_alloc<kTcCols>(&sm.tmem_base);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();  // the plan (and the table update before it) is complete
+    pdl_launch_dependents();
+    const int64_t U = a.sdesc[a.n_seqs].x, N = gridDim.x;
+    const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
+    if (warp < 4) {
+        decode_tc_softmax<kR>(sm, a, u1 - u0);
+    } else if (warp == 4) {
+        decode_producer<false>(sm, &tk, &tv, a, u0, u1, &tq);
+    } else {
+        if ((threadIdx.x & 31) == 0) {
+            if (warp == 5)
+                decode_tc_issue<true>(sm, a, u1 - u0);
+            else
+                decode_tc_issue<false>(sm, a, u1 - u0);
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_free<kTcCols>(sm.tmem_base);
 }
 
 // ---------------------------------------------------------- FP8 decode
@@ -1046,38 +1497,63 @@ bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *
            ((uintptr_t)layer->k_pool & 15) == 0 && ((uintptr_t)layer->v_pool & 15) == 0;
 }
 
-template <int kTok, int kTPW>
+template <int kTok>
 int decode_ctas_per_sm_t() {
     static int v = -1;
     if (v < 0) {
         constexpr size_t smem = decode_smem_bytes<kTok>();
-        if (cudaFuncSetAttribute(decode_mma_bf16_d128<kTok, kTPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(decode_mma_bf16_d128<kTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128<kTok, kTPW>,
-                                                          32 * (kTok / kTPW + 1), smem) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128<kTok>, 32 * (kTok + 1), smem) !=
+            cudaSuccess)
             n = 1;
         v = std::max(1, n);
     }
     return v;
 }
 
-int decode_ctas_per_sm() { return decode_ctas_per_sm_t<1, 1>(); }
+int decode_ctas_per_sm() { return decode_ctas_per_sm_t<1>(); }
 
-// Kernel instantiation serving n_tok query tokens: up to 4 tokens one per
-// consumer warp; 5..8 tokens two per warp (4 warps), which halves the
-// shared-memory reads of a page (8 warps reading every page outrun the
-// shared-memory bandwidth; with 4 tokens the extra MMA work per warp costs
-// more than it saves).
-int tok_variant(int n_tok) { return n_tok <= 2 ? n_tok : n_tok <= 4 ? 4 : 8; }
+template <int kR>
+int decode_tc_ctas_per_sm_t() {
+    static int v = -1;
+    if (v < 0) {
+        if (cudaFuncSetAttribute(decode_tc_bf16_d128<kR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDecodeTcSmemBytes) != cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_bf16_d128<kR>, kTcThreads,
+                                                          kDecodeTcSmemBytes) != cudaSuccess)
+            n = 1;
+        v = std::max(1, n);
+    }
+    return v;
+}
+
+int decode_tc_ctas_per_sm(int n_tok) {
+    switch (tc_copies(n_tok)) {
+    case 4: return decode_tc_ctas_per_sm_t<4>();
+    case 2: return decode_tc_ctas_per_sm_t<2>();
+    default: return decode_tc_ctas_per_sm_t<1>();
+    }
+}
+
+// Query tokens per sequence from which the tensor-core kernel serves a
+// multi-token decode. Below it the mma.sync kernel (one consumer warp per
+// token) keeps up with HBM; from 5 tokens on its MMA work per page does not,
+// while the tensor-core kernel's cost per page hardly depends on n_tok.
+constexpr int kTcMinTokens = 5;
+
+// mma.sync kernel instantiation serving n_tok < kTcMinTokens query tokens.
+int tok_variant(int n_tok) { return n_tok <= 2 ? n_tok : 4; }
 
 int decode_ctas_per_sm_for(int n_tok) {
     switch (tok_variant(n_tok)) {
-    case 1: return decode_ctas_per_sm_t<1, 1>();
-    case 2: return decode_ctas_per_sm_t<2, 1>();
-    case 4: return decode_ctas_per_sm_t<4, 1>();
-    default: return decode_ctas_per_sm_t<8, 2>();
+    case 1: return decode_ctas_per_sm_t<1>();
+    case 2: return decode_ctas_per_sm_t<2>();
+    default: return decode_ctas_per_sm_t<4>();
     }
 }
 
@@ -1172,11 +1648,17 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
     return HSWA_OK;
 }
 
-template <int kTok, int kTPW>
+template <int kTok>
 cudaError_t launch_decode_kernel(int n_ctas, cudaStream_t st, const CUtensorMap &tk, const CUtensorMap &tv,
                                  const DecodeArgs &a) {
-    return launch_pdl(decode_mma_bf16_d128<kTok, kTPW>, dim3(n_ctas), dim3(32 * (kTok / kTPW + 1)),
+    return launch_pdl(decode_mma_bf16_d128<kTok>, dim3(n_ctas), dim3(32 * (kTok + 1)),
                       decode_smem_bytes<kTok>(), st, tk, tv, a);
+}
+
+template <int kR>
+cudaError_t launch_decode_tc(int n_ctas, cudaStream_t st, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const DecodeArgs &a) {
+    return launch_pdl(decode_tc_bf16_d128<kR>, dim3(n_ctas), dim3(kTcThreads), kDecodeTcSmemBytes, st, tq, tk, tv, a);
 }
 
 // Decode of n_tok query tokens per sequence, with an optional fused append
@@ -1211,7 +1693,8 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     if ((int64_t)n_seqs * n_tok > 65535) return HSWA_ERR_UNSUPPORTED;  // rows of the combine grid
     const int sms = sm_count();
     if (sms <= 0) return HSWA_ERR_CUDA;
-    const int per_sm = decode_ctas_per_sm_for(n_tok);
+    const bool tc = n_tok >= kTcMinTokens;
+    const int per_sm = tc ? decode_tc_ctas_per_sm(n_tok) : decode_ctas_per_sm_for(n_tok);
     if (per_sm <= 0) return HSWA_ERR_CUDA;
     const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
     if (!ws || ((uintptr_t)ws & 255) ||
@@ -1223,25 +1706,35 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     a.n_tok = n_tok;
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, tq;
     const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
     if (!make_tmap_2d(&tk, layer->k_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tv, layer->v_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return HSWA_ERR_CUDA;
-    set_last_kernel(fused ? "decode_mma_bf16_d128+append" : "decode_mma_bf16_d128");
+    // q as [n_seqs * n_tok][Hq][d]: one box is the n_tok x 8 query rows of a
+    // (sequence, kv head), 64 columns wide
+    if (tc && !make_tmap_3d(&tq, q, kD, (uint64_t)c.n_q_heads, (uint64_t)n_seqs * n_tok, 64, kG, (uint32_t)n_tok,
+                            CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B))
+        return HSWA_ERR_CUDA;
+    set_last_kernel(tc ? "decode_tc_bf16_d128" : fused ? "decode_mma_bf16_d128+append" : "decode_mma_bf16_d128");
     // three launches chained with programmatic dependent launch: each one
     // is scheduled while its predecessor finishes and waits for it on entry
     if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok,
                    static_cast<int4 *>(ws)) != cudaSuccess)
         return HSWA_ERR_CUDA;
     cudaError_t e;
-    switch (tok_variant(n_tok)) {
-    case 1: e = launch_decode_kernel<1, 1>(n_ctas, st, tk, tv, a); break;
-    case 2: e = launch_decode_kernel<2, 1>(n_ctas, st, tk, tv, a); break;
-    case 4: e = launch_decode_kernel<4, 1>(n_ctas, st, tk, tv, a); break;
-    default: e = launch_decode_kernel<8, 2>(n_ctas, st, tk, tv, a); break;
+    if (tc) {
+        switch (tc_copies(n_tok)) {
+        case 4: e = launch_decode_tc<4>(n_ctas, st, tq, tk, tv, a); break;
+        case 2: e = launch_decode_tc<2>(n_ctas, st, tq, tk, tv, a); break;
+        default: e = launch_decode_tc<1>(n_ctas, st, tq, tk, tv, a); break;
+        }
+    } else switch (tok_variant(n_tok)) {
+    case 1: e = launch_decode_kernel<1>(n_ctas, st, tk, tv, a); break;
+    case 2: e = launch_decode_kernel<2>(n_ctas, st, tk, tv, a); break;
+    default: e = launch_decode_kernel<4>(n_ctas, st, tk, tv, a); break;
     }
     if (e != cudaSuccess ||
         launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * n_tok), dim3(256), 0, st, a, n_ctas) != cudaSuccess)

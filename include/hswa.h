@@ -318,7 +318,7 @@ int hswa_decode_append(const hswa_pool *pool, const hswa_layer *layer, const voi
                        hswa_stream_t stream);
 
 /* Most query tokens per sequence hswa_decode_multi takes. */
-#define HSWA_DECODE_MAX_TOKENS 8
+#define HSWA_DECODE_MAX_TOKENS 16
 
 /* Bytes of workspace hswa_decode_multi needs for n_seqs sequences of n_tok
  * query tokens each (0 for an n_tok outside [1, HSWA_DECODE_MAX_TOKENS]). */
