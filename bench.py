@@ -216,7 +216,7 @@ def measure_decode_fp8(steps, warmup):
     return out
 
 
-def measure_decode_multi(reps, w, token_counts=(1, 2, 4, 8, 16)):
+def measure_decode_multi(reps, w, token_counts=(1, 2, 3, 4, 8, 16)):
     """Multi-token decode (n_tok query tokens per sequence at positions
     L - n_tok .. L - 1) over the decode-batch pools: one step is the Full and
     the SWA layer of hswa_decode_multi, events around each layer. Returns per

@@ -23,8 +23,8 @@
 // L - n_tok .. L - 1: the MTP verification step of "MiMo-V2.5 Series
 // Inference Full-Link Optimization", Sec. 5.2, and the multi-token
 // verification of "Following the Bottleneck: Optimizing MiniMax M3 on AMD
-// Instinct MI355X", EAGLE3 section): up to 4 tokens the same kernel with one
-// consumer warp per token; 5 to 16 tokens a tcgen05 kernel whose
+// Instinct MI355X", EAGLE3 section): up to 3 tokens the same kernel with one
+// consumer warp per token; 4 to 16 tokens a tcgen05 kernel whose
 // (token, head) rows form one M = 128 tile ("tensor-core multi-token" below).
 // Generic path (any dtype / head_dim / ratio / page): one warp per
 // (sequence, query head) with CUDA-core dot products.
@@ -59,7 +59,7 @@ struct StageDesc {
 };
 
 // kTok query tokens per sequence share every streamed page (one consumer
-// warp each): 1 for plain decode, up to 4 for multi-token decode.
+// warp each): 1 for plain decode, 2 or 3 for multi-token decode.
 template <int kTok_>
 struct DecodeSmemT {
     static constexpr int kTok = kTok_;
@@ -605,15 +605,17 @@ __global__ void __launch_bounds__(32 * (kTok + 1)) decode_mma_bf16_d128(const __
 // keeps its own running max and sum, so the softmax of a page is spread
 // over all four warps instead of one. At the end of a piece the copies of
 // a row are merged (weights 2^(m_c - M)) through shared memory.
-// TMEM (512 columns): S double buffer (2 x 64), P double buffer (2 x 32
-// packed bf16 pairs), O (128). Warp 4 streams pages (and each piece's q
-// tile by tensor map). Warp 5 allocates TMEM and one of its threads issues
-// the QK MMAs, one thread of warp 6 the PV MMAs: an MMA takes some 70 cycles
-// to issue and a barrier wait as long, too much for one thread per page.
+// TMEM (512 columns): S (4 x 64), P (4 x 32 packed bf16 pairs), O (128).
+// Page i uses S and P buffer i % 4; with 4 K/V stages, page i has landed
+// only after PV(i - 4) is done, so the buffers need no other wait.
+// Warp 4 streams pages (and each piece's q tile by tensor map). Warp 5
+// allocates TMEM and one of its threads issues the QK MMAs, one thread of
+// warp 6 the PV MMAs: an MMA takes some 70 cycles to issue and a barrier
+// wait after a commit several times that, too much for one thread per page.
 // The scores of page i + 1 run on the tensor cores while the softmax of
-// page i runs. Warps 0-3: one tile row per thread: mask, online softmax in
-// the log2 domain with the lazy 2^8 rescale of O, P to TMEM, and the
-// end-of-piece merge and output.
+// page i runs. Warps 0-3: one tile row per thread: mask (only on pages a
+// token does not see whole), online softmax in the log2 domain with the
+// lazy 2^8 rescale of O, P to TMEM, and the end-of-piece merge and output.
 struct DecodeTcSmem {
     static constexpr int kStages = 4;
     static constexpr int kQBufs = 2;
@@ -627,7 +629,7 @@ struct DecodeTcSmem {
     StageDesc desc[kStages];
     uint64_t full[kStages], empty[kStages];
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full[2], p_full[2];
+    uint64_t s_full[kStages], p_full[kStages];
     uint64_t mma_done[2], ep_bar;
     uint32_t tmem_base;
     int32_t abort;
@@ -637,17 +639,22 @@ static_assert(offsetof(DecodeTcSmem, v) % 1024 == 0 && offsetof(DecodeTcSmem, q)
 constexpr size_t kDecodeTcSmemBytes = sizeof(DecodeTcSmem) + 1024;
 constexpr int kTcThreads = 224;
 constexpr int kTcCols = 512;
-constexpr uint32_t kTmemP = 128, kTmemO = 256;  // column offsets of P and O
+constexpr uint32_t kTmemP = 256, kTmemO = 384;  // column offsets of P and O (S at 0)
 constexpr float kTcRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
 
 // Two threads issue the MMAs of the CTA's n pages, each in page order and
 // each waiting only on its own barriers:
-//   warp 5, lane 0: QK(i) once page i (and, on a piece's first page, its q
-//     tile) has landed and the softmax of page i - 2 has read S buffer i & 1;
-//     commits s_full, and q_empty after the last QK of a piece;
+//   warp 5, lane 0: QK(i) into S buffer i % 4 once page i (and, on a
+//     piece's first page, its q tile) has landed; commits s_full, and q_empty
+//     after the last QK of a piece;
 //   warp 6, lane 0: PV(i) once P(i) is in TMEM; commits empty (the page's
 //     stage: K was read by QK(i) before P(i) existed).
 // A commit arrives once every MMA its thread issued before has completed.
+// Page i lands only after the empty barrier of page i - 4: PV(i - 4), and
+// with it the softmax of page i - 4, are done, so S and P buffer i % 4 are
+// free. The s_full and p_full barriers are per buffer: each is at most one
+// phase ahead of a waiter for the same reason.
+static_assert(DecodeTcSmem::kStages == 4, "S / P buffer i % 4 relies on 4 K/V stages");
 __device__ bool decode_tc_qk(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
     constexpr int kStages = DecodeTcSmem::kStages, kQB = DecodeTcSmem::kQBufs;
     constexpr uint32_t kIdQK = idesc_16(128, kP, false, false);
@@ -661,18 +668,17 @@ __device__ bool decode_tc_qk(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
             ++pc;
             if (!mbar_wait(&sm.q_full[pc % kQB], (uint32_t)(pc / kQB) & 1, a.err)) return false;
         }
-        if (i >= 2 && !mbar_wait(&sm.p_full[i & 1], (uint32_t)((i - 2) >> 1) & 1, a.err)) return false;
         if (*(volatile int32_t *)&sm.abort) return false;
         tc_fence_after();
         if (!(flags & kSkip)) {
             const uint32_t q = qb + (pc % kQB) * 2 * DecodeTcSmem::kQHalfBytes, k = kb + st * kPageHeadBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tb + 64 * (uint32_t)(i & 1),
+                mma_ss(tb + 64 * (uint32_t)(i % kStages),
                        sdesc(q + (kk >> 2) * DecodeTcSmem::kQHalfBytes + (kk & 3) * 32, 16, 1024),
                        sdesc(k + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024), kIdQK, kk > 0);
         }
-        mma_commit(&sm.s_full[i & 1]);
+        mma_commit(&sm.s_full[st]);
         if (flags & kLast) mma_commit(&sm.q_empty[pc % kQB]);
     }
     return true;
@@ -684,14 +690,14 @@ __device__ bool decode_tc_pv(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
     const uint32_t tb = sm.tmem_base, vb = smem_u32(sm.v[0]);
     bool fresh = true;  // no PV yet in the current piece: the next one overwrites O
     for (int64_t i = 0; i < n; ++i) {
-        if (!mbar_wait(&sm.p_full[i & 1], (uint32_t)(i >> 1) & 1, a.err) || *(volatile int32_t *)&sm.abort)
-            return false;
         const int st = (int)(i % kStages);
+        if (!mbar_wait(&sm.p_full[st], (uint32_t)(i / kStages) & 1, a.err) || *(volatile int32_t *)&sm.abort)
+            return false;
         const int32_t flags = sm.desc[st].flags;
         if (flags & kFirst) fresh = true;
         tc_fence_after();
         if (!(flags & kSkip)) {
-            const uint32_t tp = tb + kTmemP + 32 * (uint32_t)(i & 1), v = vb + st * kPageHeadBytes;
+            const uint32_t tp = tb + kTmemP + 32 * st, v = vb + st * kPageHeadBytes;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_ts(tb + kTmemO, tp + kk * 8, sdesc(v + kk * 2048, kBoxBytes, 1024), kIdPV,
@@ -774,8 +780,8 @@ __device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t
         uint32_t z[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) z[x] = 0u;
-        tmem_st32(sm.tmem_base + lane_off + kTmemP, z);
-        tmem_st32(sm.tmem_base + lane_off + kTmemP + 32, z);
+#pragma unroll
+        for (int b = 0; b < kStages; ++b) tmem_st32(sm.tmem_base + lane_off + kTmemP + 32 * b, z);
         tmem_wait_st();
     }
     float m_used = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of P
@@ -784,7 +790,7 @@ __device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t
     for (int64_t i = 0; i < n && ok; ++i) {
         const int st = (int)(i % kStages);
         ok = mbar_wait(&sm.full[st], (uint32_t)(i / kStages) & 1, a.err) &&
-             mbar_wait(&sm.s_full[i & 1], (uint32_t)(i >> 1) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+             mbar_wait(&sm.s_full[st], (uint32_t)(i / kStages) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const StageDesc d = sm.desc[st];
@@ -792,7 +798,7 @@ __device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t
         if (active) {
             tc_fence_after();
             uint32_t sr[kK];
-            tmem_ld_s<kK>(sm.tmem_base + lane_off + 64 * (uint32_t)(i & 1) + c * kK, sr);
+            tmem_ld_s<kK>(sm.tmem_base + lane_off + 64 * st + c * kK, sr);
             // keys of the page this row's token sees, relative to the copy's
             // first key: [lo_c, hi_c) (position t = len - n_tok + w; W keys
             // ending at t for SWA)
@@ -802,9 +808,12 @@ __device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t
             if (a.window > 0) lo_c = max(lo_c, t - a.window + 1 - base);
             if (w >= a.n_tok || (d.flags & kSkip)) hi_c = 0;
             float m0 = -INFINITY, m1 = -INFINITY;
+            // most pages are seen whole by every token of the warp
+            if (__any_sync(0xffffffffu, lo_c > 0 || hi_c < kK)) {
 #pragma unroll
-            for (int x = 0; x < kK; ++x)
-                if (x >= hi_c || x < lo_c) sr[x] = __float_as_uint(-INFINITY);
+                for (int x = 0; x < kK; ++x)
+                    if (x >= hi_c || x < lo_c) sr[x] = __float_as_uint(-INFINITY);
+            }
 #pragma unroll
             for (int x = 0; x < kK; x += 4) {
                 m0 = max3(m0, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
@@ -827,18 +836,12 @@ __device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t
                 sum2 = __fadd2_rn(sum2, p);
                 pk[x] = pack_bf16(p.x, p.y);
             }
-            // P buffer i & 1 was last read by PV(i - 2): the empty barrier of
-            // its stage. Its next phase needs P(i + 2), and PV(i - 2 - kStages)
-            // was waited for two pages ago, so the parity test is exact.
-            if (i >= 2)
-                ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[(i - 2) % kStages],
-                                                       (uint32_t)((i - 2) / kStages) & 1, a.err));
-            if (!ok) break;
-            tmem_st_p<kK / 2>(t_p + 32 * (uint32_t)(i & 1), pk);
+            tmem_st_p<kK / 2>(t_p + 32 * st, pk);  // P buffer i % 4: free since page i landed
             if (__any_sync(0xffffffffu, resc)) {  // never on a piece's first page
                 // O holds the piece's earlier pages once PV(i - 1) is done:
                 // the empty barrier of its stage (its next phase needs
-                // P(i + 3); PV(i - 1 - kStages) came before PV(i - 2)).
+                // P(i + 3); PV(i - 1 - kStages) is done since page i - 1
+                // landed).
                 ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[(i - 1) % kStages],
                                                        (uint32_t)((i - 1) / kStages) & 1, a.err));
                 if (!ok) break;
@@ -857,11 +860,11 @@ __device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t
             tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(&sm.p_full[i & 1]);
+        mbar_arrive(&sm.p_full[st]);
         if (!(d.flags & kLast)) continue;
         // ---- end of the piece: O is final once PV(i) is done, i.e. the next
-        // phase of the empty barrier of page i's stage (PV(i - kStages) came
-        // before PV(i - 2); PV(i + kStages) needs P(i + kStages))
+        // phase of the empty barrier of page i's stage (PV(i - kStages) is
+        // done since page i landed; PV(i + kStages) needs P(i + kStages))
         if (active) ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[st], (uint32_t)(i / kStages) & 1, a.err));
         float M = m_used, L = l, wt = 1.f;
         if constexpr (kR > 1) {
@@ -983,6 +986,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.q_full[b], 1);
             mbar_init(&sm.q_empty[b], 1);
+        }
+        for (int b = 0; b < DecodeTcSmem::kStages; ++b) {
             mbar_init(&sm.s_full[b], 1);
             mbar_init(&sm.p_full[b], 128);
         }
@@ -1542,18 +1547,17 @@ int decode_tc_ctas_per_sm(int n_tok) {
 
 // Query tokens per sequence from which the tensor-core kernel serves a
 // multi-token decode. Below it the mma.sync kernel (one consumer warp per
-// token) keeps up with HBM; from 5 tokens on its MMA work per page does not,
-// while the tensor-core kernel's cost per page hardly depends on n_tok.
-constexpr int kTcMinTokens = 5;
-
-// mma.sync kernel instantiation serving n_tok < kTcMinTokens query tokens.
-int tok_variant(int n_tok) { return n_tok <= 2 ? n_tok : 4; }
+// token) streams faster; from 4 tokens on its MMA work per page costs more
+// than the tensor-core kernel, whose cost per page hardly depends on n_tok
+// (decode batch, Full layer: 3 tokens 6.52 against 6.35 TB/s, 4 tokens 6.28
+// against 6.39).
+constexpr int kTcMinTokens = 4;
 
 int decode_ctas_per_sm_for(int n_tok) {
-    switch (tok_variant(n_tok)) {
+    switch (n_tok) {
     case 1: return decode_ctas_per_sm_t<1>();
     case 2: return decode_ctas_per_sm_t<2>();
-    default: return decode_ctas_per_sm_t<4>();
+    default: return decode_ctas_per_sm_t<3>();
     }
 }
 
@@ -1731,10 +1735,10 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
         case 2: e = launch_decode_tc<2>(n_ctas, st, tq, tk, tv, a); break;
         default: e = launch_decode_tc<1>(n_ctas, st, tq, tk, tv, a); break;
         }
-    } else switch (tok_variant(n_tok)) {
+    } else switch (n_tok) {
     case 1: e = launch_decode_kernel<1>(n_ctas, st, tk, tv, a); break;
     case 2: e = launch_decode_kernel<2>(n_ctas, st, tk, tv, a); break;
-    default: e = launch_decode_kernel<4>(n_ctas, st, tk, tv, a); break;
+    default: e = launch_decode_kernel<3>(n_ctas, st, tk, tv, a); break;
     }
     if (e != cudaSuccess ||
         launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * n_tok), dim3(256), 0, st, a, n_ctas) != cudaSuccess)
