@@ -175,3 +175,60 @@ def test_multi_token_rejects_bad_token_counts_and_small_workspace():
                             sc.scale, ws, small)
     assert e.value.status == H.HSWA_ERR_INVALID_ARG
     assert sc.sess.check() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_tok", [3, 8, 16])
+def test_multi_token_positions_before_the_sequence_start(n_tok):
+    """Sequences shorter than n_tok: query token w sits at t = L - n_tok + w,
+    and a token with t < 0 has no key to attend and gets o = 0; the others
+    match the oracle at their positions (both kernels)."""
+    cached = [0, 1, 2, 5, 70]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=15, extra_tokens=16)
+    B = len(cached)
+    full_slots, swa_slots = sc.reserve(range(B), [1] * B)  # L = cached + 1
+    sc.sess.sync()
+    lens = sc.ora.seq_len[:B]
+    assert (lens < n_tok).any()
+    for layer, kind in enumerate(sc.kinds):
+        slots = full_slots if kind == FULL else swa_slots
+        kn = sc.gen((B, sc.hkv, sc.d), 1100 + layer)
+        vn = sc.gen((B, sc.hkv, sc.d), 1110 + layer)
+        sc.sess.append(layer, sc.to_dev(kn), sc.to_dev(vn), torch.as_tensor(slots, device="cuda"))
+        q = sc.gen((B * n_tok, sc.hq, sc.d), 1120 + layer)
+        o = torch.full_like(sc.to_dev(q), float("nan"))
+        sc.sess.decode_multi(layer, sc.to_dev(q), o, B, n_tok, sc.scale)
+        assert sc.sess.check() == 0
+        got = device_out(o)
+        pos = (lens[:, None] - n_tok + np.arange(n_tok)[None, :]).reshape(-1)
+        seq = np.repeat(np.arange(B), n_tok)
+        before = pos < 0
+        assert np.all(got[before] == 0.0)
+        snap = sc.snapshot(layer, list(range(B)))
+        exp = oracle.attention(raw_host(q)[~before], snap[0], snap[1], snap[2], seq[~before], pos[~before],
+                               sc.window(layer), sc.scale)
+        assert max_err(got[~before], exp) <= TOL[sc.dtype], (kind, n_tok)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_tok", [2, 8])
+def test_multi_token_bad_table_entries_set_bounds_and_skip(n_tok):
+    """Invalid block-table entries inside the key range (the first page of a
+    segment, a page past the pool, every page of one sequence) are skipped,
+    the call reports HSWA_ERR_BOUNDS and the output stays finite."""
+    cached = [300, 300, 60]
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=16, extra_tokens=16)
+    B = len(cached)
+    sc.reserve(range(B), [n_tok] * B)
+    sc.sess.sync()
+    sc.sess.d_full_bt[0, 0] = -1
+    sc.sess.d_full_bt[1, 3] = 1 << 30
+    sc.sess.d_full_bt[2, 0] = -1
+    sc.sess.d_full_bt[2, 1] = -1
+    q = sc.to_dev(sc.gen((B * n_tok, 64, 128), 1))
+    o = torch.full_like(q, float("nan"))
+    sc.sess.decode_multi(0, q, o, B, n_tok, sc.scale)
+    assert sc.sess.check() == H.HSWA_ERR_BOUNDS
+    assert sc.sess.check() == 0
+    assert torch.isfinite(o.float()).all()
+    assert torch.equal(o[2 * n_tok:].float(), torch.zeros_like(o[2 * n_tok:].float()))  # no key left
