@@ -216,18 +216,18 @@ def measure_decode_fp8(steps, warmup):
     return out
 
 
-def measure_decode_multi(reps, w, token_counts=(1, 2, 3, 4, 8, 16)):
+def measure_decode_multi(reps, w, token_counts=(1, 2, 3, 4, 8, 16), fp8=False):
     """Multi-token decode (n_tok query tokens per sequence at positions
-    L - n_tok .. L - 1) over the decode-batch pools: one step is the Full and
-    the SWA layer of hswa_decode_multi, events around each layer. Returns per
-    n_tok the step time, query tokens/s and the Full layer's GB/s (KV bytes
-    read once, q and o of every token)."""
+    L - n_tok .. L - 1) over the decode-batch pools (FP8 E4M3 pools when fp8):
+    one step is the Full and the SWA layer of hswa_decode_multi, events
+    around each layer. Returns per n_tok the step time, query tokens/s and
+    the Full layer's GB/s (KV bytes read once, q and o of every token)."""
     import torch
     from hybrid_sliding_window_dual_gb300 import hswa_last_kernel
-    bench = DecodeBatch(w, 8, hold=max(token_counts))
+    bench = DecodeBatch(w, 8, hold=max(token_counts), fp8=fp8)
     sess, B, es = bench.sess, bench.B, KV_ROW[w.dtype]
     lens = bench.lens()
-    kv = decode_bytes(w, lens)
+    kv = decode_bytes_fp8(w, lens) if fp8 else decode_bytes(w, lens)
     out = {}
     for T in token_counts:
         q = [wl.normal((B * T, w.n_q_heads, w.head_dim), 700 + 10 * T + i, w.dtype, "cuda") for i in range(2)]
@@ -980,6 +980,17 @@ def run_decode(args, world, rank, local):
                                   "full_layer_gbs": round(v["full_layer_gbs"], 1),
                                   "frac": round(v["full_layer_gbs"] / hbm, 4),
                                   "time_vs_1": round(v["step_ms"] / base, 3)} for T, v in mt.items()}}
+        if not args.no_fp8:
+            torch.cuda.empty_cache()
+            mt8 = measure_decode_multi(50, workload(args, "decode_batch"), token_counts=(1, 2, 4), fp8=True)
+            base8 = mt8[1]["step_ms"]
+            line["multi_token_decode_fp8"] = {
+                "workload": "decode_batch over FP8 E4M3 pools, n_tok query tokens per sequence, Full + SWA "
+                            "layer per step; the pages are streamed once per two tokens, GB/s counts them once",
+                "by_n_tok": {str(T): {"kernel": v["kernel"], "step_ms": round(v["step_ms"], 4),
+                                      "tokens_per_s": round(v["tokens_per_s"], 1),
+                                      "full_layer_gbs": round(v["full_layer_gbs"], 1),
+                                      "time_vs_1": round(v["step_ms"] / base8, 3)} for T, v in mt8.items()}}
         bench = None
     if not args.no_prefill:
         del bench

@@ -86,25 +86,28 @@ constexpr uint32_t kScaleBytes = kP * 4;
 
 constexpr int kConsumers8 = 4;  // FP8 consumer warps, one 16-key group of a page each
 
-struct DecodeSmem8 {
+template <int kTok>
+struct DecodeSmem8T {
     static constexpr int kStages = 3;
     static constexpr bool kTcQ = false;
     uint8_t k[kStages][kK8Bytes];
     uint8_t v[kStages][kV8Bytes];
-    uint8_t q[kStages][kQBytes];
+    uint8_t q[kStages][kTok * kQBytes];
     float ks[kStages][kP];
     float vs[kStages][kP];
     // end-of-piece merge of the consumer warps' (max, sum, o) states
-    float mo[kConsumers8 - 1][kG][kD];
-    float mm[kConsumers8 - 1][kG];
-    float ml[kConsumers8 - 1][kG];
+    float mo[kConsumers8 - 1][kTok][kG][kD];
+    float mm[kConsumers8 - 1][kTok][kG];
+    float ml[kConsumers8 - 1][kTok][kG];
     StageDesc desc[kStages];
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t merge;
     int32_t abort;
 };
 
-constexpr size_t kDecodeSmem8Bytes = sizeof(DecodeSmem8) + 1024;
+template <int kTok>
+constexpr size_t decode_smem8_bytes() { return sizeof(DecodeSmem8T<kTok>) + 1024; }
 
 struct Partial {
     float m[kG];
@@ -127,10 +130,18 @@ struct DecodeArgs {
     const __nv_bfloat16 *k_new, *v_new;
     int64_t pool_slots;
     int32_t n_seqs, bt_stride, hkv, hq, window, num_pages;
-    int32_t n_tok;  // query tokens per sequence (multi-token decode), 1 otherwise
+    // query tokens per sequence: q and o hold q_tok rows per sequence; this
+    // launch serves its rows tok0 .. tok0 + n_tok - 1, the last n_tok
+    // positions before the plan's key end (1, 1, 0 for plain decode)
+    int32_t n_tok, q_tok, tok0;
     float scale_log2;
     int *err;
 };
+
+// Row of q / o holding query token tok0 + w of sequence s.
+__device__ __forceinline__ int64_t q_row(const DecodeArgs &a, int32_t s, int32_t w) {
+    return (int64_t)s * a.q_tok + a.tok0 + w;
+}
 
 // Tensor-core multi-token decode: copies of the 8 n_tok query rows in the
 // 128-row tile (each copy takes 64 / copies keys of every page).
@@ -146,8 +157,10 @@ __device__ __forceinline__ void key_range(int32_t L, int32_t window, int32_t n_t
 // Per-sequence descriptors: the first unit of the sequence (prefix sum of
 // units(s) = Hkv * pages touched by the key range [lo, hi)), lo, hi, units.
 // desc[n].x is the total number of units.
+// len_off: the keys end len_off short of seq_len (a pass over the earlier
+// query tokens of a multi-token decode).
 __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int32_t hkv, int32_t page,
-                            int32_t window, int32_t n_tok, int4 *__restrict__ desc) {
+                            int32_t window, int32_t n_tok, int32_t len_off, int4 *__restrict__ desc) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -159,7 +172,7 @@ __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int3
         const int32_t i = base + tid;
         int32_t u = 0, lo = 0, hi = 0;
         if (i < n) {
-            key_range(seq_len[i], window, n_tok, lo, hi);
+            key_range(max(seq_len[i] - len_off, 0), window, n_tok, lo, hi);
             if (hi > lo) u = hkv * ((hi - 1) / page - lo / page + 1);
         }
         int32_t x = u;  // inclusive warp scan
@@ -312,7 +325,7 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                             for (int cp = 0; cp < copies; ++cp)
                                 for (int dh = 0; dh < 2; ++dh)
                                     tma_load_3d(sm.q[b] + dh * Smem::kQHalfBytes + cp * (128 / copies) * 128, tq,
-                                                dh * 64, g * kG, s * a.n_tok, &sm.q_full[b]);
+                                                dh * 64, g * kG, (int32_t)q_row(a, s, 0), &sm.q_full[b]);
                             q_issued[b] = true;
                             q_parity[b] = par;
                         }
@@ -346,11 +359,10 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                         if (valid) {
                             const int32_t blk = page * a.hkv + g;  // (page, kv head) block
                             if constexpr (kFP8) {
-                                auto &s8 = reinterpret_cast<DecodeSmem8 &>(sm);
-                                tma_load_2d(s8.k[stage], tk, 0, blk * kP, &sm.full[stage]);
-                                tma_load_2d(s8.v[stage], tv, 0, blk * kD, &sm.full[stage]);
-                                bulk_g2s(s8.ks[stage], a.k_scale + (int64_t)blk * kP, kScaleBytes, &sm.full[stage]);
-                                bulk_g2s(s8.vs[stage], a.v_scale + (int64_t)blk * kP, kScaleBytes, &sm.full[stage]);
+                                tma_load_2d(sm.k[stage], tk, 0, blk * kP, &sm.full[stage]);
+                                tma_load_2d(sm.v[stage], tv, 0, blk * kD, &sm.full[stage]);
+                                bulk_g2s(sm.ks[stage], a.k_scale + (int64_t)blk * kP, kScaleBytes, &sm.full[stage]);
+                                bulk_g2s(sm.vs[stage], a.v_scale + (int64_t)blk * kP, kScaleBytes, &sm.full[stage]);
                             } else {
                                 const int32_t row = blk * kP;
                                 tma_load_2d(sm.k[stage], tk, 0, row, &sm.full[stage]);
@@ -363,8 +375,8 @@ __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorM
                             if (j == 0)  // the 8 query rows of each token of this kv head
                                 for (int w = 0; w < a.n_tok; ++w)
                                     bulk_g2s(sm.q[stage] + w * kQBytes,
-                                             a.q + (((int64_t)s * a.n_tok + w) * a.hq + (int64_t)g * kG) * kD,
-                                             kQBytes, &sm.full[stage]);
+                                             a.q + (q_row(a, s, w) * a.hq + (int64_t)g * kG) * kD, kQBytes,
+                                             &sm.full[stage]);
                         }
                     } else {
                         mbar_arrive(&sm.full[stage]);
@@ -533,7 +545,7 @@ __device__ void decode_consumer(DecodeSmemT<kTok> &sm, const DecodeArgs &a, int6
             const int h0 = 2 * qd, h1 = 2 * qd + 1;
             if (d.flags & kDirect) {
                 const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
-                __nv_bfloat16 *o0 = a.o + (((int64_t)d.seq * a.n_tok + w) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
+                __nv_bfloat16 *o0 = a.o + (q_row(a, d.seq, w) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
                 __nv_bfloat16 *o1 = o0 + kD;
 #pragma unroll
                 for (int dt = 0; dt < 8; ++dt) {
@@ -925,7 +937,7 @@ __device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t
         const float inv = L > 0.f ? 1.f / L : 0.f;
         if (d.flags & kDirect) {
             uint4 *dst = reinterpret_cast<uint4 *>(
-                a.o + (((int64_t)d.seq * a.n_tok + (row ? w : 0)) * a.hq + (int64_t)d.kvh * kG + h) * kD);
+                a.o + (q_row(a, d.seq, row ? w : 0) * a.hq + (int64_t)d.kvh * kG + h) * kD);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t ov[32];
@@ -1071,28 +1083,40 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers8 * 32) : "memory"); }
+// Bounded arrival + wait on the consumer warps' merge barrier (128 threads):
+// a barrier that gives up (HSWA_ERR_TIMEOUT) if a warp never arrives.
+template <class Smem>
+__device__ __forceinline__ bool merge_sync(Smem &sm, uint32_t &phase, int *err) {
+    mbar_arrive(&sm.merge);
+    const bool ok = mbar_wait(&sm.merge, phase, err);
+    phase ^= 1;
+    return ok;
+}
 
-// The consumers over FP8 pages. Warp w takes the 16 keys 16w..16w+15 of
-// every page: S^T = (K codes as f16) Q^T with the key rows taken in
-// key_of_row order and d read 4 codes at a time (Q's fragments use the same d
-// order), times the per-key K scale; an online softmax of its own; P times
-// the per-key V scale feeds the f16 PV MMA, whose A operand (V^T) comes from
-// the transposed page without any transpose. At the end of a piece warps 1-3
-// hand their (max, sum, o) to warp 0 through shared memory, which merges and
-// writes.
-__device__ void decode_consumer_fp8(DecodeSmem8 &sm, const DecodeArgs &a, int64_t u0, int64_t u1) {
+// The consumers over FP8 pages, kTok query tokens per pass (1 or 2). Warp w
+// takes the 16 keys 16w..16w+15 of every page: S^T = (K codes as f16) Q^T
+// with the key rows taken in key_of_row order and d read 4 codes at a time
+// (Q's fragments use the same d order), times the per-key K scale; an online
+// softmax of its own per token; P times the per-key V scale feeds the f16 PV
+// MMA, whose A operand (V^T) comes from the transposed page without any
+// transpose. Every converted K and V fragment feeds the MMAs of all kTok
+// tokens. At the end of a piece warps 1-3 hand their (max, sum, o) to warp 0
+// through shared memory, which merges and writes.
+template <int kTok>
+__device__ void decode_consumer_fp8(DecodeSmem8T<kTok> &sm, const DecodeArgs &a, int64_t u0, int64_t u1) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int gr = lane >> 2, qd = lane & 3;
-    constexpr int kStages = DecodeSmem8::kStages;
-    uint32_t qf[8][2];
-    float oacc[8][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    constexpr int kStages = DecodeSmem8T<kTok>::kStages;
+    uint32_t qf[kTok][8][2];
+    float oacc[kTok][8][4];
+    float m0[kTok], m1[kTok], l0[kTok], l1[kTok];
+#pragma unroll
+    for (int j = 0; j < kTok; ++j) m0[j] = m1[j] = -INFINITY, l0[j] = l1[j] = 0.f;
     int stage = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, merge_phase = 0;
     const uint32_t kbase = smem_u32(sm.k[0]), vbase = smem_u32(sm.v[0]);
-    const int j = lane >> 3;
-    const int ar = (lane & 7) + 8 * (j & 1);  // A row this lane addresses in ldmatrix (QK)
+    const int jj = lane >> 3;
+    const int ar = (lane & 7) + 8 * (jj & 1);  // A row this lane addresses in ldmatrix (QK)
     const int c0 = w * 16 + key_of_row(gr), c1 = w * 16 + key_of_row(gr + 8);  // keys of this thread's S rows
     // a V word's code pairs in the order this thread's P pairs take them
     // (key_of_row): as loaded, or its two halves swapped for q >= 2
@@ -1107,190 +1131,229 @@ __device__ void decode_consumer_fp8(DecodeSmem8 &sm, const DecodeArgs &a, int64_
         }
         const StageDesc d = sm.desc[stage];
         if (d.flags & kFirst) {
-            const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm.q[stage]) + gr * kD;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const int c = ks * 16 + 4 * qd;
-                qf[ks][0] = pack_f16(__bfloat162float(qs[c]), __bfloat162float(qs[c + 1]));
-                qf[ks][1] = pack_f16(__bfloat162float(qs[c + 2]), __bfloat162float(qs[c + 3]));
+            for (int j = 0; j < kTok; ++j) {
+                const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm.q[stage] + j * kQBytes) + gr * kD;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int c = ks * 16 + 4 * qd;
+                    qf[j][ks][0] = pack_f16(__bfloat162float(qs[c]), __bfloat162float(qs[c + 1]));
+                    qf[j][ks][1] = pack_f16(__bfloat162float(qs[c + 2]), __bfloat162float(qs[c + 3]));
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) oacc[j][i][0] = oacc[j][i][1] = oacc[j][i][2] = oacc[j][i][3] = 0.f;
+                m0[j] = m1[j] = -INFINITY;
+                l0[j] = l1[j] = 0.f;
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
         }
         const bool any = !(d.flags & kSkip) && w * 16 + 15 >= d.lo && w * 16 < d.hi;
         if (any) {
             const uint32_t kb = kbase + stage * kK8Bytes, vb = vbase + stage * kV8Bytes;
-            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            float sacc[kTok][4];
+#pragma unroll
+            for (int j = 0; j < kTok; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
             const int key = w * 16 + key_of_row(ar);
 #pragma unroll
             for (int dc = 0; dc < 4; ++dc) {
                 uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
-                ldsm_x4(kb + swz128(key, dc * 32 + 16 * (j >> 1)), r0, r1, r2, r3);
+                ldsm_x4(kb + swz128(key, dc * 32 + 16 * (jj >> 1)), r0, r1, r2, r3);
                 e4m3x4_f16x2x2_cvt(r0, a0, a2);
                 e4m3x4_f16x2x2_cvt(r1, a1, a3);
-                mma_f16_16816(sacc, a0, a1, a2, a3, qf[2 * dc][0], qf[2 * dc][1]);
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) mma_f16_16816(sacc[j], a0, a1, a2, a3, qf[j][2 * dc][0], qf[j][2 * dc][1]);
                 e4m3x4_f16x2x2_cvt(r2, a0, a2);
                 e4m3x4_f16x2x2_cvt(r3, a1, a3);
-                mma_f16_16816(sacc, a0, a1, a2, a3, qf[2 * dc + 1][0], qf[2 * dc + 1][1]);
+#pragma unroll
+                for (int j = 0; j < kTok; ++j)
+                    mma_f16_16816(sacc[j], a0, a1, a2, a3, qf[j][2 * dc + 1][0], qf[j][2 * dc + 1][1]);
             }
-            const bool v0 = c0 >= d.lo && c0 < d.hi, v1 = c1 >= d.lo && c1 < d.hi;
             // K codes entered the MMA as their exact values
             const float s0 = sm.ks[stage][c0] * a.scale_log2;
             const float s1 = sm.ks[stage][c1] * a.scale_log2;
-            sacc[0] = v0 ? sacc[0] * s0 : -INFINITY;
-            sacc[1] = v0 ? sacc[1] * s0 : -INFINITY;
-            sacc[2] = v1 ? sacc[2] * s1 : -INFINITY;
-            sacc[3] = v1 ? sacc[3] * s1 : -INFINITY;
-            float mx0 = fmaxf(sacc[0], sacc[2]), mx1 = fmaxf(sacc[1], sacc[3]);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            // this warp saw at least one valid key in the piece so far (n > -inf),
-            // else it keeps nothing and P stays 0
-            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-            const float b0 = n0 == -INFINITY ? 0.f : n0, b1 = n1 == -INFINITY ? 0.f : n1;
-            const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
-            const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
-            m0 = n0;
-            m1 = n1;
-            const float p0 = fast_exp2(sacc[0] - b0), p1 = fast_exp2(sacc[1] - b1);
-            const float p2 = fast_exp2(sacc[2] - b0), p3 = fast_exp2(sacc[3] - b1);
             // V codes enter the MMA as their exact values; P carries the V
             // scale times 2^8 (keeping small weights out of f16's subnormal
             // range), and so does the running sum: O / l stays exact
-            l0 = l0 * al0 + 256.f * (p0 + p2);
-            l1 = l1 * al1 + 256.f * (p1 + p3);
             const float w0 = sm.vs[stage][c0] * 256.f, w1 = sm.vs[stage][c1] * 256.f;
-            const uint32_t pb0 = movmatrix_t(pack_f16(p0 * w0, p1 * w0));
-            const uint32_t pb1 = movmatrix_t(pack_f16(p2 * w1, p3 * w1));
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {  // a head's max moved
+            uint32_t pb0[kTok], pb1[kTok];
 #pragma unroll
-                for (int dt = 0; dt < 8; ++dt) {
-                    oacc[dt][0] *= al0;
-                    oacc[dt][1] *= al1;
-                    oacc[dt][2] *= al0;
-                    oacc[dt][3] *= al1;
+            for (int j = 0; j < kTok; ++j) {
+                // keys of the page token j sees: its position is
+                // t = len - n_tok + j; keys <= t and, for SWA, > t - W
+                int32_t lo = d.lo, hi = d.hi;  // one token: the stage's range is its own
+                if constexpr (kTok > 1) {
+                    const int32_t t = d.len - a.n_tok + j;
+                    hi = min(d.hi, t - d.key0 + 1);
+                    if (a.window > 0) lo = max(d.lo, t - a.window + 1 - d.key0);
+                }
+                const bool v0 = c0 >= lo && c0 < hi, v1 = c1 >= lo && c1 < hi;
+                sacc[j][0] = v0 ? sacc[j][0] * s0 : -INFINITY;
+                sacc[j][1] = v0 ? sacc[j][1] * s0 : -INFINITY;
+                sacc[j][2] = v1 ? sacc[j][2] * s1 : -INFINITY;
+                sacc[j][3] = v1 ? sacc[j][3] * s1 : -INFINITY;
+                float mx0 = fmaxf(sacc[j][0], sacc[j][2]), mx1 = fmaxf(sacc[j][1], sacc[j][3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                // this warp saw at least one valid key in the piece so far
+                // (n > -inf), else it keeps nothing and P stays 0
+                const float n0 = fmaxf(m0[j], mx0), n1 = fmaxf(m1[j], mx1);
+                const float b0 = n0 == -INFINITY ? 0.f : n0, b1 = n1 == -INFINITY ? 0.f : n1;
+                const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0[j] - n0);
+                const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1[j] - n1);
+                m0[j] = n0;
+                m1[j] = n1;
+                const float p0 = fast_exp2(sacc[j][0] - b0), p1 = fast_exp2(sacc[j][1] - b1);
+                const float p2 = fast_exp2(sacc[j][2] - b0), p3 = fast_exp2(sacc[j][3] - b1);
+                l0[j] = l0[j] * al0 + 256.f * (p0 + p2);
+                l1[j] = l1[j] * al1 + 256.f * (p1 + p3);
+                pb0[j] = movmatrix_t(pack_f16(p0 * w0, p1 * w0));
+                pb1[j] = movmatrix_t(pack_f16(p2 * w1, p3 * w1));
+                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {  // a head's max moved
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        oacc[j][dt][0] *= al0;
+                        oacc[j][dt][1] *= al1;
+                        oacc[j][dt][2] *= al0;
+                        oacc[j][dt][3] *= al1;
+                    }
                 }
             }
             // O^T += V^T P^T: A rows are d (two 16-row tiles per load), 4 key codes per 32-bit word
 #pragma unroll
             for (int dp = 0; dp < 4; ++dp) {
                 uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
-                ldsm_x4(vb + swz64(dp * 32 + j * 8 + (lane & 7), w * 16), r0, r1, r2, r3);
+                ldsm_x4(vb + swz64(dp * 32 + jj * 8 + (lane & 7), w * 16), r0, r1, r2, r3);
                 e4m3x4_f16x2x2_cvt(__byte_perm(r0, 0u, vsel), a0, a2);
                 e4m3x4_f16x2x2_cvt(__byte_perm(r1, 0u, vsel), a1, a3);
-                mma_f16_16816(oacc[2 * dp], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) mma_f16_16816(oacc[j][2 * dp], a0, a1, a2, a3, pb0[j], pb1[j]);
                 e4m3x4_f16x2x2_cvt(__byte_perm(r2, 0u, vsel), a0, a2);
                 e4m3x4_f16x2x2_cvt(__byte_perm(r3, 0u, vsel), a1, a3);
-                mma_f16_16816(oacc[2 * dp + 1], a0, a1, a2, a3, pb0, pb1);
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) mma_f16_16816(oacc[j][2 * dp + 1], a0, a1, a2, a3, pb0[j], pb1[j]);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
 
         if (d.flags & kLast) {
-            float t0 = l0, t1 = l1;
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                t0 += __shfl_xor_sync(0xffffffffu, t0, off);
-                t1 += __shfl_xor_sync(0xffffffffu, t1, off);
-            }
             const int h0 = 2 * qd, h1 = 2 * qd + 1;
-            if (w > 0) {  // hand this warp's state to warp 0
-                if (gr == 0) {
-                    sm.mm[w - 1][h0] = m0;
-                    sm.mm[w - 1][h1] = m1;
-                    sm.ml[w - 1][h0] = t0;
-                    sm.ml[w - 1][h1] = t1;
-                }
+            float t0[kTok], t1[kTok];
 #pragma unroll
-                for (int dt = 0; dt < 8; ++dt) {
-                    sm.mo[w - 1][h0][dt * 16 + gr] = oacc[dt][0];
-                    sm.mo[w - 1][h1][dt * 16 + gr] = oacc[dt][1];
-                    sm.mo[w - 1][h0][dt * 16 + gr + 8] = oacc[dt][2];
-                    sm.mo[w - 1][h1][dt * 16 + gr + 8] = oacc[dt][3];
+            for (int j = 0; j < kTok; ++j) {
+                t0[j] = l0[j];
+                t1[j] = l1[j];
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    t0[j] += __shfl_xor_sync(0xffffffffu, t0[j], off);
+                    t1[j] += __shfl_xor_sync(0xffffffffu, t1[j], off);
                 }
             }
-            consumer_bar();
-            if (w == 0) {
-                float M0 = m0, M1 = m1;
-                for (int i = 0; i < kConsumers8 - 1; ++i) {
-                    M0 = fmaxf(M0, sm.mm[i][h0]);
-                    M1 = fmaxf(M1, sm.mm[i][h1]);
-                }
-                const float e0 = M0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
-                const float e1 = M1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
-                t0 *= e0;
-                t1 *= e1;
+            if (w > 0) {  // hand this warp's states to warp 0
 #pragma unroll
-                for (int dt = 0; dt < 8; ++dt) {
-                    oacc[dt][0] *= e0;
-                    oacc[dt][1] *= e1;
-                    oacc[dt][2] *= e0;
-                    oacc[dt][3] *= e1;
-                }
-                for (int i = 0; i < kConsumers8 - 1; ++i) {
-                    const float f0 = M0 == -INFINITY ? 0.f : fast_exp2(sm.mm[i][h0] - M0);
-                    const float f1 = M1 == -INFINITY ? 0.f : fast_exp2(sm.mm[i][h1] - M1);
-                    t0 += f0 * sm.ml[i][h0];
-                    t1 += f1 * sm.ml[i][h1];
-#pragma unroll
-                    for (int dt = 0; dt < 8; ++dt) {
-                        oacc[dt][0] += f0 * sm.mo[i][h0][dt * 16 + gr];
-                        oacc[dt][1] += f1 * sm.mo[i][h1][dt * 16 + gr];
-                        oacc[dt][2] += f0 * sm.mo[i][h0][dt * 16 + gr + 8];
-                        oacc[dt][3] += f1 * sm.mo[i][h1][dt * 16 + gr + 8];
-                    }
-                }
-                if (d.flags & kDirect) {
-                    const float i0 = t0 > 0.f ? 1.f / t0 : 0.f, i1 = t1 > 0.f ? 1.f / t1 : 0.f;
-                    __nv_bfloat16 *o0 = a.o + ((int64_t)d.seq * a.hq + (int64_t)d.kvh * kG + h0) * kD;
-                    __nv_bfloat16 *o1 = o0 + kD;
-#pragma unroll
-                    for (int dt = 0; dt < 8; ++dt) {
-                        o0[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][0] * i0);
-                        o1[dt * 16 + gr] = __float2bfloat16_rn(oacc[dt][1] * i1);
-                        o0[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][2] * i0);
-                        o1[dt * 16 + gr + 8] = __float2bfloat16_rn(oacc[dt][3] * i1);
-                    }
-                } else {
-                    Partial &p = a.part[(int64_t)blockIdx.x * 2 + d.slot];
+                for (int j = 0; j < kTok; ++j) {
                     if (gr == 0) {
-                        p.m[h0] = M0;
-                        p.m[h1] = M1;
-                        p.l[h0] = t0;
-                        p.l[h1] = t1;
+                        sm.mm[w - 1][j][h0] = m0[j];
+                        sm.mm[w - 1][j][h1] = m1[j];
+                        sm.ml[w - 1][j][h0] = t0[j];
+                        sm.ml[w - 1][j][h1] = t1[j];
                     }
 #pragma unroll
                     for (int dt = 0; dt < 8; ++dt) {
-                        p.o[h0][dt * 16 + gr] = oacc[dt][0];
-                        p.o[h1][dt * 16 + gr] = oacc[dt][1];
-                        p.o[h0][dt * 16 + gr + 8] = oacc[dt][2];
-                        p.o[h1][dt * 16 + gr + 8] = oacc[dt][3];
+                        sm.mo[w - 1][j][h0][dt * 16 + gr] = oacc[j][dt][0];
+                        sm.mo[w - 1][j][h1][dt * 16 + gr] = oacc[j][dt][1];
+                        sm.mo[w - 1][j][h0][dt * 16 + gr + 8] = oacc[j][dt][2];
+                        sm.mo[w - 1][j][h1][dt * 16 + gr + 8] = oacc[j][dt][3];
                     }
                 }
             }
-            consumer_bar();  // the merge area is free again
+            ok = merge_sync(sm, merge_phase, a.err);
+            if (w == 0 && ok) {
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) {
+                    float M0 = m0[j], M1 = m1[j];
+                    for (int i = 0; i < kConsumers8 - 1; ++i) {
+                        M0 = fmaxf(M0, sm.mm[i][j][h0]);
+                        M1 = fmaxf(M1, sm.mm[i][j][h1]);
+                    }
+                    const float e0 = M0 == -INFINITY ? 0.f : fast_exp2(m0[j] - M0);
+                    const float e1 = M1 == -INFINITY ? 0.f : fast_exp2(m1[j] - M1);
+                    float L0 = t0[j] * e0, L1 = t1[j] * e1;
+                    float(&acc)[8][4] = oacc[j];  // merged in place: a new piece starts from zero
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        acc[dt][0] *= e0;
+                        acc[dt][1] *= e1;
+                        acc[dt][2] *= e0;
+                        acc[dt][3] *= e1;
+                    }
+                    for (int i = 0; i < kConsumers8 - 1; ++i) {
+                        const float f0 = M0 == -INFINITY ? 0.f : fast_exp2(sm.mm[i][j][h0] - M0);
+                        const float f1 = M1 == -INFINITY ? 0.f : fast_exp2(sm.mm[i][j][h1] - M1);
+                        L0 += f0 * sm.ml[i][j][h0];
+                        L1 += f1 * sm.ml[i][j][h1];
+#pragma unroll
+                        for (int dt = 0; dt < 8; ++dt) {
+                            acc[dt][0] += f0 * sm.mo[i][j][h0][dt * 16 + gr];
+                            acc[dt][1] += f1 * sm.mo[i][j][h1][dt * 16 + gr];
+                            acc[dt][2] += f0 * sm.mo[i][j][h0][dt * 16 + gr + 8];
+                            acc[dt][3] += f1 * sm.mo[i][j][h1][dt * 16 + gr + 8];
+                        }
+                    }
+                    if (d.flags & kDirect) {
+                        const float i0 = L0 > 0.f ? 1.f / L0 : 0.f, i1 = L1 > 0.f ? 1.f / L1 : 0.f;
+                        __nv_bfloat16 *o0 = a.o + (q_row(a, d.seq, j) * a.hq + (int64_t)d.kvh * kG + h0) * kD;
+                        __nv_bfloat16 *o1 = o0 + kD;
+#pragma unroll
+                        for (int dt = 0; dt < 8; ++dt) {
+                            o0[dt * 16 + gr] = __float2bfloat16_rn(acc[dt][0] * i0);
+                            o1[dt * 16 + gr] = __float2bfloat16_rn(acc[dt][1] * i1);
+                            o0[dt * 16 + gr + 8] = __float2bfloat16_rn(acc[dt][2] * i0);
+                            o1[dt * 16 + gr + 8] = __float2bfloat16_rn(acc[dt][3] * i1);
+                        }
+                    } else {
+                        Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + j];
+                        if (gr == 0) {
+                            p.m[h0] = M0;
+                            p.m[h1] = M1;
+                            p.l[h0] = L0;
+                            p.l[h1] = L1;
+                        }
+#pragma unroll
+                        for (int dt = 0; dt < 8; ++dt) {
+                            p.o[h0][dt * 16 + gr] = acc[dt][0];
+                            p.o[h1][dt * 16 + gr] = acc[dt][1];
+                            p.o[h0][dt * 16 + gr + 8] = acc[dt][2];
+                            p.o[h1][dt * 16 + gr + 8] = acc[dt][3];
+                        }
+                    }
+                }
+            }
+            ok = merge_sync(sm, merge_phase, a.err) && ok;  // the merge area is free again
+            if (!ok) {
+                if (lane == 0) sm.abort = 1;
+                return;
+            }
         }
         if (++stage == kStages) stage = 0, phase ^= 1;
     }
 }
 
+template <int kTok>
 __global__ void __launch_bounds__(32 * (kConsumers8 + 1)) decode_mma_fp8_d128(const __grid_constant__ CUtensorMap tk,
                                                                            const __grid_constant__ CUtensorMap tv,
                                                                            DecodeArgs a) {
+    using Smem = DecodeSmem8T<kTok>;
     extern __shared__ uint8_t raw[];
-    DecodeSmem8 &sm =
-        *reinterpret_cast<DecodeSmem8 *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     if (threadIdx.x == 0) {
-        for (int i = 0; i < DecodeSmem8::kStages; ++i) {
+        for (int i = 0; i < Smem::kStages; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], kConsumers8);
         }
+        mbar_init(&sm.merge, 32 * kConsumers8);
         sm.abort = 0;
         fence_barrier_init();
     }
@@ -1303,7 +1366,7 @@ __global__ void __launch_bounds__(32 * (kConsumers8 + 1)) decode_mma_fp8_d128(co
     if (threadIdx.x >= 32 * kConsumers8)
         decode_producer<true>(sm, &tk, &tv, a, u0, u1);
     else
-        decode_consumer_fp8(sm, a, u0, u1);
+        decode_consumer_fp8<kTok>(sm, a, u0, u1);
 }
 
 // Merge the partial records of segments split between CTAs; write zeros
@@ -1316,7 +1379,7 @@ __global__ void __launch_bounds__(256) decode_combine(DecodeArgs a, int32_t n_ct
     const int4 d = a.sdesc[s];
     const int32_t units = d.w;
     const int h = threadIdx.x >> 5, d0 = (threadIdx.x & 31) * 4;
-    __nv_bfloat16 *out = a.o + (((int64_t)s * a.n_tok + w) * a.hq + (int64_t)g * kG + h) * kD + d0;
+    __nv_bfloat16 *out = a.o + (q_row(a, s, w) * a.hq + (int64_t)g * kG + h) * kD + d0;
     if (units == 0) {
         for (int i = 0; i < 4; ++i) out[i] = __float2bfloat16_rn(0.f);
         return;
@@ -1479,21 +1542,26 @@ bool decode_fp8_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q
            ((uintptr_t)layer->k_scale & 15) == 0 && ((uintptr_t)layer->v_scale & 15) == 0;
 }
 
+template <int kTok>
 int decode_fp8_ctas_per_sm() {
     static int v = -1;
     if (v < 0) {
-        if (cudaFuncSetAttribute(decode_mma_fp8_d128, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDecodeSmem8Bytes) != cudaSuccess)
+        constexpr size_t smem = decode_smem8_bytes<kTok>();
+        if (cudaFuncSetAttribute(decode_mma_fp8_d128<kTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_fp8_d128, 32 * (kConsumers8 + 1),
-                                                          kDecodeSmem8Bytes) !=
-            cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_fp8_d128<kTok>, 32 * (kConsumers8 + 1),
+                                                          smem) != cudaSuccess)
             n = 1;
         v = std::max(1, n);
     }
     return v;
 }
+
+// Query tokens one pass of the FP8 decode kernel serves; more tokens take
+// several passes over the pages.
+constexpr int kFp8PassTokens = 2;
 
 bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
     const hswa_config &c = pool->cfg;
@@ -1609,24 +1677,30 @@ int fill_args(DecodeArgs &a, const hswa_pool *pool, const hswa_layer *layer, con
     a.hq = c.n_q_heads;
     a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
     a.num_pages = num_pages;
-    a.n_tok = 1;
+    a.n_tok = a.q_tok = 1;
+    a.tok0 = 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = error_word();
     return num_pages;
 }
 
-// Decode over an FP8 pool (a fused append quantizes first, as its own launch).
+// Decode over an FP8 pool (a fused append quantizes first, as its own
+// launch). n_tok query tokens per sequence go in passes of up to
+// kFp8PassTokens tokens: pass (tok0, P) plans the key range of tokens
+// tok0 .. tok0 + P - 1 (the keys end n_tok - tok0 - P short of seq_len),
+// streams those pages once for its P tokens and merges its own partials.
 int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o, const int32_t *d_bt,
-               const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes, const int32_t *slots,
-               const void *k_new, const void *v_new, hswa_stream_t stream) {
+               const int32_t *d_seq_len, int n_seqs, int n_tok, float scale, void *ws, size_t ws_bytes,
+               const int32_t *slots, const void *k_new, const void *v_new, hswa_stream_t stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (!decode_fp8_ok(pool, layer, q, o)) return HSWA_ERR_UNSUPPORTED;
     const int sms = sm_count();
-    const int per_sm = decode_fp8_ctas_per_sm();
-    if (sms <= 0 || per_sm <= 0) return HSWA_ERR_CUDA;
-    const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
-    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < desc_bytes(n_seqs) + (size_t)n_ctas * 2 * sizeof(Partial))
-        return HSWA_ERR_INVALID_ARG;
+    const int per_sm1 = decode_fp8_ctas_per_sm<1>(), per_sm2 = decode_fp8_ctas_per_sm<2>();
+    if (sms <= 0 || per_sm1 <= 0 || per_sm2 <= 0) return HSWA_ERR_CUDA;
+    const int n_ctas1 = sms * std::min(per_sm1, kMaxCtasPerSm), n_ctas2 = sms * std::min(per_sm2, kMaxCtasPerSm);
+    const int max_pass = std::min(n_tok, kFp8PassTokens);
+    const size_t part_bytes = (size_t)std::max(n_ctas1, max_pass > 1 ? 2 * n_ctas2 : 0) * 2 * sizeof(Partial);
+    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < desc_bytes(n_seqs) + part_bytes) return HSWA_ERR_INVALID_ARG;
     if (slots) {
         const int rc = hswa_append_kv(pool, layer, k_new, v_new, slots, n_seqs, stream);
         if (rc != HSWA_OK) return rc;
@@ -1642,13 +1716,23 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
                       CU_TENSOR_MAP_SWIZZLE_64B))
         return HSWA_ERR_CUDA;
     set_last_kernel(slots ? "append_kv_fp8+decode_mma_fp8_d128" : "decode_mma_fp8_d128");
-    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, 1,
-                   static_cast<int4 *>(ws)) != cudaSuccess ||
-        launch_pdl(decode_mma_fp8_d128, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)), kDecodeSmem8Bytes, st, tk, tv,
-                   a) !=
-            cudaSuccess ||
-        launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs), dim3(256), 0, st, a, n_ctas) != cudaSuccess)
-        return HSWA_ERR_CUDA;
+    a.q_tok = n_tok;
+    for (int tok0 = 0; tok0 < n_tok; tok0 += kFp8PassTokens) {
+        const int pass = std::min(kFp8PassTokens, n_tok - tok0);
+        const int n_ctas = pass == 1 ? n_ctas1 : n_ctas2;
+        a.n_tok = pass;
+        a.tok0 = tok0;
+        cudaError_t e = launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP,
+                                   a.window, pass, n_tok - tok0 - pass, static_cast<int4 *>(ws));
+        if (e == cudaSuccess)
+            e = pass == 1 ? launch_pdl(decode_mma_fp8_d128<1>, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)),
+                                       decode_smem8_bytes<1>(), st, tk, tv, a)
+                          : launch_pdl(decode_mma_fp8_d128<2>, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)),
+                                       decode_smem8_bytes<2>(), st, tk, tv, a);
+        if (e == cudaSuccess)
+            e = launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * pass), dim3(256), 0, st, a, n_ctas);
+        if (e != cudaSuccess) return HSWA_ERR_CUDA;
+    }
     return HSWA_OK;
 }
 
@@ -1680,9 +1764,9 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool fused = slots != nullptr;
     if (pool->cfg.dtype == HSWA_DTYPE_FP8_E4M3) {
-        if (n_tok != 1) return HSWA_ERR_UNSUPPORTED;
-        return decode_fp8(pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws, ws_bytes, slots, k_new, v_new,
-                          stream);
+        if ((int64_t)n_seqs * std::min(n_tok, kFp8PassTokens) > 65535) return HSWA_ERR_UNSUPPORTED;
+        return decode_fp8(pool, layer, q, o, d_bt, d_seq_len, n_seqs, n_tok, scale, ws, ws_bytes, slots, k_new,
+                          v_new, stream);
     }
     if (!decode_fast_ok(pool, layer, q, o) ||
         (fused && (((uintptr_t)k_new & 15) || ((uintptr_t)v_new & 15)))) {
@@ -1709,7 +1793,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     a.slots = slots;
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-    a.n_tok = n_tok;
+    a.n_tok = a.q_tok = n_tok;
     CUtensorMap tk, tv, tq;
     const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
     if (!make_tmap_2d(&tk, layer->k_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -1725,7 +1809,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     set_last_kernel(tc ? "decode_tc_bf16_d128" : fused ? "decode_mma_bf16_d128+append" : "decode_mma_bf16_d128");
     // three launches chained with programmatic dependent launch: each one
     // is scheduled while its predecessor finishes and waits for it on entry
-    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok,
+    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok, 0,
                    static_cast<int4 *>(ws)) != cudaSuccess)
         return HSWA_ERR_CUDA;
     cudaError_t e;

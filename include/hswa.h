@@ -338,8 +338,8 @@ size_t hswa_decode_multi_workspace_size(const hswa_pool *pool, int n_seqs, int n
  * i * n_tok + w). A token with t < 0 gets o = 0. n_tok = 1 is hswa_decode.
  * ws: device workspace of at least hswa_decode_multi_workspace_size bytes.
  * The SWA pages must still hold positions from L - n_tok + 1 - W on: release
- * out-of-window pages before the draft tokens are reserved. Bf16 pools only
- * for n_tok > 1 (HSWA_ERR_UNSUPPORTED on an FP8 pool); n_tok outside
+ * out-of-window pages before the draft tokens are reserved. Bf16 and FP8
+ * pools (an FP8 pool streams its pages once per two tokens); n_tok outside
  * [1, HSWA_DECODE_MAX_TOKENS] gives HSWA_ERR_INVALID_ARG. */
 int hswa_decode_multi(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                       const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, int n_tok, float scale,

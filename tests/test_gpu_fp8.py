@@ -184,14 +184,70 @@ def test_fp8_prefill_rejects_small_workspace():
     assert c.sess.check() == 0
 
 
+def fp8_multi_step(c, n_tok, seed, samples=None):
+    """Reserve n_tok tokens per sequence, append them (quantized), run one
+    multi-token decode per layer and compare the given sequences' rows with
+    the oracle at positions L - n_tok + w (tokens before position 0: o = 0)."""
+    B = c.B
+    samples = list(range(B)) if samples is None else samples
+    fs, ss = c.sess.reserve(range(B), [n_tok] * B)
+    efs, ess = c.ora.reserve(range(B), [n_tok] * B)
+    assert np.array_equal(fs, efs) and np.array_equal(ss, ess)
+    c.sess.sync()
+    scale = 1 / math.sqrt(D)
+    for layer, kind in enumerate(c.kinds):
+        slots = fs if kind == FULL else ss
+        kn = wl.normal((B * n_tok, HKV, D), seed + 10 * layer + 1, wl.DTYPE_BF16)
+        vn = wl.normal((B * n_tok, HKV, D), seed + 10 * layer + 2, wl.DTYPE_BF16)
+        c.sess.append(layer, kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"))
+        q = wl.normal((B * n_tok, HQ, D), seed + 10 * layer, wl.DTYPE_BF16)
+        o = torch.full((B * n_tok, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        c.sess.decode_multi(layer, q.cuda(), o, B, n_tok, scale)
+        assert c.sess.check() == 0
+        assert H.hswa_last_kernel() == "decode_mma_fp8_d128"
+        kc, ks, vc, vs = (x.cpu().numpy() for x in (c.sess.k[layer], c.sess.ks[layer], c.sess.v[layer],
+                                                     c.sess.vs[layer]))
+        lens = c.ora.seq_len[samples]
+        rows = (np.asarray(samples)[:, None] * n_tok + np.arange(n_tok)[None, :]).reshape(-1)
+        seq = np.repeat(np.asarray(samples), n_tok)
+        pos = (lens[:, None] - n_tok + np.arange(n_tok)[None, :]).reshape(-1)
+        got = o.float().cpu().numpy()[rows]
+        assert np.isfinite(got).all()
+        before = pos < 0
+        assert np.all(got[before] == 0.0)
+        exp = oracle.attention_fp8(raw_host(q)[rows[~before]], kc, ks, vc, vs, c.table(layer), seq[~before],
+                                   pos[~before], 0 if kind == FULL else W, scale)
+        err = float(np.abs(got[~before] - exp).max())
+        assert err <= 2e-2, (layer, n_tok, err)
+
+
 @pytest.mark.gpu
-def test_fp8_multi_token_decode_is_unsupported():
-    c = Fp8Case([100, 7], seed=73)
-    q = torch.zeros(2 * 2, HQ, D, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(H.HswaError) as e:
-        c.sess.decode_multi(0, q, q.clone(), 2, 2, 0.1)
-    assert e.value.status == H.HSWA_ERR_UNSUPPORTED
-    assert c.sess.check() == 0
+@pytest.mark.parametrize("n_tok", [2, 3, 4, 5, 8])
+def test_fp8_multi_token_decode_matches_oracle(n_tok):
+    """Multi-token decode over FP8 pools: passes of up to two tokens, lengths
+    around page edges and the window, one sequence shorter than n_tok."""
+    cached = [0, 1, 62, 63, 64, 125, 126, 127, 128, 700, 3000]
+    c = Fp8Case(cached, seed=73, extra=24)
+    fp8_multi_step(c, n_tok, seed=1300 + n_tok)
+
+
+@pytest.mark.gpu
+def test_fp8_multi_token_decode_steps_with_release():
+    """Verification steps of 3 tokens over FP8 pools, a release before each."""
+    c = Fp8Case([5, 130, 255, 1000, 2047], seed=74, extra=64)
+    for step in range(6):
+        assert c.sess.release(range(c.B)) == c.ora.swa_release(range(c.B))
+        c.sess.sync()
+        fp8_multi_step(c, 3, seed=1400 + 10 * step)
+
+
+@pytest.mark.gpu
+def test_fp8_multi_token_full_size_sampled():
+    """The decode-batch workload over FP8 pools with 4 query tokens per
+    sequence (two passes), oracle on sampled sequences."""
+    w = wl.decode_batch()
+    c = Fp8Case(list(w.cached), seed=82, extra=8)
+    fp8_multi_step(c, 4, seed=1500, samples=[0, 1, 17, 31, 32, 50, 63])
 
 
 def fp8_window_pack(c, layer, lens):
