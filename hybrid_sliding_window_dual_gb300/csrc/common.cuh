@@ -121,6 +121,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (TMA stores, tensor-core operands).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Order this thread's generic-proxy global writes before its later
 // async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -605,437 +605,6 @@ __global__ void __launch_bounds__(32 * (kTok + 1)) decode_mma_bf16_d128(const __
         decode_consumer<kTok>(sm, a, u0, u1, warp);
 }
 
-// ------------------------------------------------ tensor-core multi-token
-// Multi-token decode on the 5th-generation tensor cores. The n_tok query
-// tokens x 8 query heads of a (sequence, kv head) are the rows of one
-// M = 128 tile, so every streamed page costs the same two MMA groups:
-//   S = Q K^T    8 x tcgen05.mma M128 N64 K16 (the page's 64 keys)
-//   O += P V     4 x tcgen05.mma M128 N128 K16, P read from TMEM
-// With 8 n_tok <= 128 / R the query rows are repeated R times (R = 4 up to
-// 4 tokens, 2 up to 8, else 1): copy c of a row sees only keys
-// [c 64 / R, (c + 1) 64 / R) of every page (its P is zero elsewhere) and
-// keeps its own running max and sum, so the softmax of a page is spread
-// over all four warps instead of one. At the end of a piece the copies of
-// a row are merged (weights 2^(m_c - M)) through shared memory.
-// TMEM (512 columns): S (4 x 64), P (4 x 32 packed bf16 pairs), O (128).
-// Page i uses S and P buffer i % 4; with 4 K/V stages, page i has landed
-// only after PV(i - 4) is done, so the buffers need no other wait.
-// Warp 4 streams pages (and each piece's q tile by tensor map). Warp 5
-// allocates TMEM and one of its threads issues the QK MMAs, one thread of
-// warp 6 the PV MMAs: an MMA takes some 70 cycles to issue and a barrier
-// wait after a commit several times that, too much for one thread per page.
-// The scores of page i + 1 run on the tensor cores while the softmax of
-// page i runs. Warps 0-3: one tile row per thread: mask (only on pages a
-// token does not see whole), online softmax in the log2 domain with the
-// lazy 2^8 rescale of O, P to TMEM, and the end-of-piece merge and output.
-struct DecodeTcSmem {
-    static constexpr int kStages = 4;
-    static constexpr int kQBufs = 2;
-    static constexpr bool kTcQ = true;
-    static constexpr uint32_t kQHalfBytes = 128 * 128;  // 128 rows x 64 columns of bf16
-    uint8_t k[kStages][kPageHeadBytes];                // [d half][64 keys][128 B], 128-byte swizzle
-    uint8_t v[kStages][kPageHeadBytes];
-    uint8_t q[kQBufs][2 * kQHalfBytes];                // [d half][128 rows][128 B]
-    float obuf[kD][32];                                // merge: one 32-row block of O, column-major
-    float ep_m[128], ep_l[128];                        // merge: (max, sum) of every tile row
-    StageDesc desc[kStages];
-    uint64_t full[kStages], empty[kStages];
-    uint64_t q_full[2], q_empty[2];
-    uint64_t s_full[kStages], p_full[kStages];
-    uint64_t mma_done[2], ep_bar;
-    uint32_t tmem_base;
-    int32_t abort;
-};
-static_assert(offsetof(DecodeTcSmem, v) % 1024 == 0 && offsetof(DecodeTcSmem, q) % 1024 == 0,
-              "128-byte swizzled tiles need 1024-byte alignment");
-constexpr size_t kDecodeTcSmemBytes = sizeof(DecodeTcSmem) + 1024;
-constexpr int kTcThreads = 224;
-constexpr int kTcCols = 512;
-constexpr uint32_t kTmemP = 256, kTmemO = 384;  // column offsets of P and O (S at 0)
-constexpr float kTcRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
-
-// Two threads issue the MMAs of the CTA's n pages, each in page order and
-// each waiting only on its own barriers:
-//   warp 5, lane 0: QK(i) into S buffer i % 4 once page i (and, on a
-//     piece's first page, its q tile) has landed; commits s_full, and q_empty
-//     after the last QK of a piece;
-//   warp 6, lane 0: PV(i) once P(i) is in TMEM; commits empty (the page's
-//     stage: K was read by QK(i) before P(i) existed).
-// A commit arrives once every MMA its thread issued before has completed.
-// Page i lands only after the empty barrier of page i - 4: PV(i - 4), and
-// with it the softmax of page i - 4, are done, so S and P buffer i % 4 are
-// free. The s_full and p_full barriers are per buffer: each is at most one
-// phase ahead of a waiter for the same reason.
-static_assert(DecodeTcSmem::kStages == 4, "S / P buffer i % 4 relies on 4 K/V stages");
-__device__ bool decode_tc_qk(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
-    constexpr int kStages = DecodeTcSmem::kStages, kQB = DecodeTcSmem::kQBufs;
-    constexpr uint32_t kIdQK = idesc_16(128, kP, false, false);
-    const uint32_t tb = sm.tmem_base, kb = smem_u32(sm.k[0]), qb = smem_u32(sm.q[0]);
-    int32_t pc = -1;  // piece of the last scored page
-    for (int64_t i = 0; i < n; ++i) {
-        const int st = (int)(i % kStages);
-        if (!mbar_wait(&sm.full[st], (uint32_t)(i / kStages) & 1, a.err)) return false;
-        const int32_t flags = sm.desc[st].flags;
-        if (flags & kFirst) {
-            ++pc;
-            if (!mbar_wait(&sm.q_full[pc % kQB], (uint32_t)(pc / kQB) & 1, a.err)) return false;
-        }
-        if (*(volatile int32_t *)&sm.abort) return false;
-        tc_fence_after();
-        if (!(flags & kSkip)) {
-            const uint32_t q = qb + (pc % kQB) * 2 * DecodeTcSmem::kQHalfBytes, k = kb + st * kPageHeadBytes;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tb + 64 * (uint32_t)(i % kStages),
-                       sdesc(q + (kk >> 2) * DecodeTcSmem::kQHalfBytes + (kk & 3) * 32, 16, 1024),
-                       sdesc(k + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024), kIdQK, kk > 0);
-        }
-        mma_commit(&sm.s_full[st]);
-        if (flags & kLast) mma_commit(&sm.q_empty[pc % kQB]);
-    }
-    return true;
-}
-
-__device__ bool decode_tc_pv(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
-    constexpr int kStages = DecodeTcSmem::kStages;
-    constexpr uint32_t kIdPV = idesc_16(128, kD, true, false);
-    const uint32_t tb = sm.tmem_base, vb = smem_u32(sm.v[0]);
-    bool fresh = true;  // no PV yet in the current piece: the next one overwrites O
-    for (int64_t i = 0; i < n; ++i) {
-        const int st = (int)(i % kStages);
-        if (!mbar_wait(&sm.p_full[st], (uint32_t)(i / kStages) & 1, a.err) || *(volatile int32_t *)&sm.abort)
-            return false;
-        const int32_t flags = sm.desc[st].flags;
-        if (flags & kFirst) fresh = true;
-        tc_fence_after();
-        if (!(flags & kSkip)) {
-            const uint32_t tp = tb + kTmemP + 32 * st, v = vb + st * kPageHeadBytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tb + kTmemO, tp + kk * 8, sdesc(v + kk * 2048, kBoxBytes, 1024), kIdPV,
-                       (fresh && kk == 0) ? 0u : 1u);
-            fresh = false;
-        }
-        mma_commit(&sm.empty[st]);
-    }
-    return true;
-}
-
-// Run one issuer role, then make sure every MMA it issued has completed
-// before TMEM is freed.
-template <bool kQK>
-__device__ void decode_tc_issue(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
-    bool ok = kQK ? decode_tc_qk(sm, a, n) : decode_tc_pv(sm, a, n);
-    mma_commit(&sm.mma_done[kQK ? 0 : 1]);
-    if (!mbar_wait(&sm.mma_done[kQK ? 0 : 1], 0, a.err)) ok = false;
-    if (!ok) sm.abort = 1;
-}
-
-// S columns [col, col + kN) of this thread's lane.
-template <int kN>
-__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, uint32_t (&r)[kN]) {
-    if constexpr (kN == 16) {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-            "%14, %15}, [%16];"
-            : HSWA_R8(0), HSWA_R8(8)
-            : "r"(taddr));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" : HSWA_RW8(0), HSWA_RW8(8)::"memory");
-    } else {
-#pragma unroll
-        for (int c = 0; c < kN / 32; ++c) tmem_ld32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
-#pragma unroll
-        for (int c = 0; c < kN / 32; ++c) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
-    }
-}
-
-// kN packed P columns of this thread's lane.
-template <int kN>
-__device__ __forceinline__ void tmem_st_p(uint32_t taddr, const uint32_t (&r)[kN]) {
-    if constexpr (kN == 8) {
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                     HSWA_W8(0)
-                     : "memory");
-    } else {
-#pragma unroll
-        for (int c = 0; c < kN / 16; ++c) tmem_st16(taddr + 16 * c, r + 16 * c);
-    }
-}
-
-// Bounded arrival + wait on the softmax warps' own barrier (128 threads).
-__device__ __forceinline__ bool ep_sync(DecodeTcSmem &sm, uint32_t &phase, int *err) {
-    mbar_arrive(&sm.ep_bar);
-    const bool ok = mbar_wait(&sm.ep_bar, phase, err);
-    phase ^= 1;
-    return ok;
-}
-
-// Warps 0-3: thread r owns tile row r, copy c = r / (128 / kR) of query
-// row j = r % (128 / kR) (token j / 8, head j % 8), for every page. Copy c
-// reads S columns [c kK, (c + 1) kK) and writes its P there. A warp whose
-// rows are all padding does no TMEM work but takes part in every barrier.
-template <int kR>
-__device__ void decode_tc_softmax(DecodeTcSmem &sm, const DecodeArgs &a, int64_t n) {
-    constexpr int kStages = DecodeTcSmem::kStages;
-    constexpr int kRows = 128 / kR;  // tile rows per copy
-    constexpr int kK = kP / kR;      // keys of a page per copy
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = threadIdx.x, c = r / kRows, j = r % kRows;
-    const int w = j >> 3, h = j & 7;
-    const bool active = (((warp * 32) % kRows) >> 3) < a.n_tok;  // uniform over the warp
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_o = sm.tmem_base + lane_off + kTmemO;
-    const uint32_t t_p = sm.tmem_base + lane_off + kTmemP + c * (kK / 2);
-    if constexpr (kR > 1) {
-        // P outside this copy's keys stays zero; the copy's own columns are
-        // rewritten on every page
-        uint32_t z[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) z[x] = 0u;
-#pragma unroll
-        for (int b = 0; b < kStages; ++b) tmem_st32(sm.tmem_base + lane_off + kTmemP + 32 * b, z);
-        tmem_wait_st();
-    }
-    float m_used = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of P
-    uint32_t ep_phase = 0;
-    bool ok = true;
-    for (int64_t i = 0; i < n && ok; ++i) {
-        const int st = (int)(i % kStages);
-        ok = mbar_wait(&sm.full[st], (uint32_t)(i / kStages) & 1, a.err) &&
-             mbar_wait(&sm.s_full[st], (uint32_t)(i / kStages) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const StageDesc d = sm.desc[st];
-        if (d.flags & kFirst) m_used = -INFINITY, l = 0.f;
-        if (active) {
-            tc_fence_after();
-            uint32_t sr[kK];
-            tmem_ld_s<kK>(sm.tmem_base + lane_off + 64 * st + c * kK, sr);
-            // keys of the page this row's token sees, relative to the copy's
-            // first key: [lo_c, hi_c) (position t = len - n_tok + w; W keys
-            // ending at t for SWA)
-            const int32_t t = d.len - a.n_tok + w;
-            const int32_t base = d.key0 + c * kK;
-            int32_t hi_c = min(d.hi - c * kK, t - base + 1), lo_c = d.lo - c * kK;
-            if (a.window > 0) lo_c = max(lo_c, t - a.window + 1 - base);
-            if (w >= a.n_tok || (d.flags & kSkip)) hi_c = 0;
-            float m0 = -INFINITY, m1 = -INFINITY;
-            // most pages are seen whole by every token of the warp
-            if (__any_sync(0xffffffffu, lo_c > 0 || hi_c < kK)) {
-#pragma unroll
-                for (int x = 0; x < kK; ++x)
-                    if (x >= hi_c || x < lo_c) sr[x] = __float_as_uint(-INFINITY);
-            }
-#pragma unroll
-            for (int x = 0; x < kK; x += 4) {
-                m0 = max3(m0, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
-                m1 = max3(m1, __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]));
-            }
-            const float mx = fmaxf(m0, m1) * a.scale_log2;
-            const bool need = mx > m_used + kTcRescaleLog2;
-            const bool resc = need && m_used != -INFINITY;
-            const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
-            if (need) m_used = mx;
-            const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-            const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
-            float2 sum2 = make_float2(0.f, 0.f);
-            uint32_t pk[kK / 2];
-#pragma unroll
-            for (int x = 0; x < kK / 2; ++x) {
-                const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])),
-                                            sc2, nm2);
-                const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-                sum2 = __fadd2_rn(sum2, p);
-                pk[x] = pack_bf16(p.x, p.y);
-            }
-            tmem_st_p<kK / 2>(t_p + 32 * st, pk);  // P buffer i % 4: free since page i landed
-            if (__any_sync(0xffffffffu, resc)) {  // never on a piece's first page
-                // O holds the piece's earlier pages once PV(i - 1) is done:
-                // the empty barrier of its stage (its next phase needs
-                // P(i + 3); PV(i - 1 - kStages) is done since page i - 1
-                // landed).
-                ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[(i - 1) % kStages],
-                                                       (uint32_t)((i - 1) / kStages) & 1, a.err));
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t ov[32];
-                    tmem_ld32(t_o + 32 * cc, ov);
-                    tmem_wait_ld(ov);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
-                    tmem_st32(t_o + 32 * cc, ov);
-                }
-            }
-            l = l * alpha + (sum2.x + sum2.y);
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(&sm.p_full[st]);
-        if (!(d.flags & kLast)) continue;
-        // ---- end of the piece: O is final once PV(i) is done, i.e. the next
-        // phase of the empty barrier of page i's stage (PV(i - kStages) is
-        // done since page i landed; PV(i + kStages) needs P(i + kStages))
-        if (active) ok = __all_sync(0xffffffffu, mbar_wait(&sm.empty[st], (uint32_t)(i / kStages) & 1, a.err));
-        float M = m_used, L = l, wt = 1.f;
-        if constexpr (kR > 1) {
-            // merge the copies of each row: weights 2^(m_c - M); copy 0 adds
-            // the other copies' weighted rows into its own, 32 rows at a time
-            sm.ep_m[r] = m_used;
-            sm.ep_l[r] = l;
-            ok = ep_sync(sm, ep_phase, a.err) && ok;
-            M = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < kR; ++cc) M = fmaxf(M, sm.ep_m[cc * kRows + j]);
-            L = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < kR; ++cc) {
-                const float mc = sm.ep_m[cc * kRows + j];
-                L += mc == -INFINITY ? 0.f : fast_exp2(mc - M) * sm.ep_l[cc * kRows + j];
-            }
-            wt = m_used == -INFINITY ? 0.f : fast_exp2(m_used - M);
-            tc_fence_after();
-#pragma unroll 1
-            for (int cc = 1; cc < kR; ++cc) {
-#pragma unroll 1
-                for (int b = 0; b < kRows / 32; ++b) {
-                    if (active && ok && warp == (cc * kRows) / 32 + b) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t ov[32];
-                            tmem_ld32(t_o + 32 * q4, ov);
-                            tmem_wait_ld(ov);
-#pragma unroll
-                            for (int x = 0; x < 32; ++x) sm.obuf[32 * q4 + x][lane] = __uint_as_float(ov[x]) * wt;
-                        }
-                    }
-                    ok = ep_sync(sm, ep_phase, a.err) && ok;
-                    if (active && ok && warp == b) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t ov[32];
-                            tmem_ld32(t_o + 32 * q4, ov);
-                            tmem_wait_ld(ov);
-                            const float own = cc == 1 ? wt : 1.f;  // copy 0's own weight, applied once
-#pragma unroll
-                            for (int x = 0; x < 32; ++x)
-                                ov[x] = __float_as_uint(__uint_as_float(ov[x]) * own + sm.obuf[32 * q4 + x][lane]);
-                            tmem_st32(t_o + 32 * q4, ov);
-                        }
-                        tmem_wait_st();
-                    }
-                    ok = ep_sync(sm, ep_phase, a.err) && ok;
-                }
-            }
-            wt = 1.f;
-        }
-        if (!ok) break;
-        if (!active || c != 0) continue;
-        tc_fence_after();
-        const bool row = w < a.n_tok;
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        if (d.flags & kDirect) {
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                a.o + (q_row(a, d.seq, row ? w : 0) * a.hq + (int64_t)d.kvh * kG + h) * kD);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t ov[32];
-                tmem_ld32(t_o + 32 * q4, ov);
-                tmem_wait_ld(ov);
-                if (row) {
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        // L = 0: no key seen, write zeros (O may be unset)
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = L > 0.f ? __uint_as_float(ov[8 * x + e]) * inv : 0.f;
-                        dst[q4 * 4 + x] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                                     pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-                    }
-                }
-            }
-        } else {
-            Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + (row ? w : 0)];
-            float4 *dst = reinterpret_cast<float4 *>(p.o[h]);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t ov[32];
-                tmem_ld32(t_o + 32 * q4, ov);
-                tmem_wait_ld(ov);
-                if (row) {
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) {
-                        float f[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) f[e] = L > 0.f ? __uint_as_float(ov[4 * x + e]) : 0.f;
-                        dst[q4 * 8 + x] = make_float4(f[0], f[1], f[2], f[3]);
-                    }
-                }
-            }
-            if (row) {
-                p.m[h] = M;
-                p.l[h] = L;
-            }
-        }
-    }
-    if (!ok) sm.abort = 1;
-}
-
-template <int kR>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    decode_tc_bf16_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                        const __grid_constant__ CUtensorMap tv, DecodeArgs a) {
-    extern __shared__ uint8_t raw[];
-    DecodeTcSmem &sm =
-        *reinterpret_cast<DecodeTcSmem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
-    const int warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < DecodeTcSmem::kStages; ++i) {
-            mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.q_full[b], 1);
-            mbar_init(&sm.q_empty[b], 1);
-        }
-        for (int b = 0; b < DecodeTcSmem::kStages; ++b) {
-            mbar_init(&sm.s_full[b], 1);
-            mbar_init(&sm.p_full[b], 128);
-        }
-        mbar_init(&sm.mma_done[0], 1);
-        mbar_init(&sm.mma_done[1], 1);
-        mbar_init(&sm.ep_bar, 128);
-        sm.abort = 0;
-        fence_barrier_init();
-    }
-    if (warp == 5) tmem_alloc<kTcCols>(&sm.tmem_base);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    pdl_wait();  // the plan (and the table update before it) is complete
-    pdl_launch_dependents();
-    const int64_t U = a.sdesc[a.n_seqs].x, N = gridDim.x;
-    const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
-    if (warp < 4) {
-        decode_tc_softmax<kR>(sm, a, u1 - u0);
-    } else if (warp == 4) {
-        decode_producer<false>(sm, &tk, &tv, a, u0, u1, &tq);
-    } else {
-        if ((threadIdx.x & 31) == 0) {
-            if (warp == 5)
-                decode_tc_issue<true>(sm, a, u1 - u0);
-            else
-                decode_tc_issue<false>(sm, a, u1 - u0);
-        }
-        __syncwarp();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 5) tmem_free<kTcCols>(sm.tmem_base);
-}
-
 // ---------------------------------------------------------- FP8 decode
 // Key rows of a 16-key group in the order the QK MMA's A rows take them:
 // after the movmatrix transpose of S^T, thread (g, q) then holds P for the
@@ -1369,6 +938,612 @@ __global__ void __launch_bounds__(32 * (kConsumers8 + 1)) decode_mma_fp8_d128(co
         decode_consumer_fp8<kTok>(sm, a, u0, u1);
 }
 
+// ------------------------------------------------ tensor-core multi-token
+// Multi-token decode on the 5th-generation tensor cores. The n_tok query
+// tokens x 8 query heads of a (sequence, kv head) are the rows of one
+// M = 128 tile, so every streamed page costs the same two MMA groups:
+//   S = Q K^T    8 x tcgen05.mma M128 N64 K16 (the page's 64 keys)
+//   O += P V     4 x tcgen05.mma M128 N128 K16, P read from TMEM
+// With 8 n_tok <= 128 / R the query rows are repeated R times (R = 4 up to
+// 4 tokens, 2 up to 8, else 1): copy c of a row sees only keys
+// [c 64 / R, (c + 1) 64 / R) of every page (its P is zero elsewhere) and
+// keeps its own running max and sum, so the softmax of a page is spread
+// over all four warps instead of one. At the end of a piece the copies of
+// a row are merged (weights 2^(m_c - M)) through shared memory.
+// TMEM (512 columns): S (up to 4 x 64), P (up to 4 x 32 packed pairs), O
+// (128). Page i uses S and P buffer i % kSP; a page is ready to score only
+// once PV(i - kSP) is done (below), so the buffers need no other wait.
+// Warp 4 streams pages (and each piece's q tile by tensor map). Warp 5
+// allocates TMEM and one of its threads issues the QK MMAs, one thread of
+// warp 6 the PV MMAs: an MMA takes some 70 cycles to issue and a barrier
+// wait after a commit several times that, too much for one thread per page.
+// The scores of page i + 1 run on the tensor cores while the softmax of
+// page i runs. Warps 0-3: one tile row per thread: mask (only on pages a
+// token does not see whole), online softmax in the log2 domain with the
+// lazy 2^8 rescale of O, P to TMEM, and the end-of-piece merge and output.
+//
+// FP8 pools: warps 7-10 convert each E4M3 page into f16 K and V^T tiles
+// (every E4M3 value is an f16 value) and the piece's q tile from bf16 to
+// f16 in place; the MMAs run on f16 operands, the softmax multiplies the
+// scores by the per-key K scale and P by the per-key V scale.
+constexpr int kTcCols = 512;
+constexpr uint32_t kTmemP = 256, kTmemO = 384;  // column offsets of P and O (S at 0)
+constexpr float kTcRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
+
+// bf16 pools: page i is ready to score once its stage has landed, which
+// the producer only loads after PV(i - 4) emptied it.
+struct DecodeTcSmem {
+    static constexpr bool kFP8 = false;
+    static constexpr int kStages = 4;
+    static constexpr int kSP = kStages;  // S / P buffers
+    static constexpr int kQBufs = 2;
+    static constexpr bool kTcQ = true;
+    static constexpr int kThreads = 224;
+    static constexpr uint32_t kQHalfBytes = 128 * 128;  // 128 rows x 64 columns of 16-bit values
+    uint8_t k[kStages][kPageHeadBytes];                // [d half][64 keys][128 B], 128-byte swizzle
+    uint8_t v[kStages][kPageHeadBytes];
+    uint8_t q[kQBufs][2 * kQHalfBytes];                // [d half][128 rows][128 B]
+    float obuf[kD][32];                                // merge: one 32-row block of O, column-major
+    float ep_m[128], ep_l[128];                        // merge: (max, sum) of every tile row
+    StageDesc desc[kStages];
+    uint64_t full[kStages], empty[kStages];
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full[kSP], p_full[kSP];
+    uint64_t mma_done[2], ep_bar;
+    uint32_t tmem_base;
+    int32_t abort;
+
+    __device__ uint64_t *ready(int64_t i) { return &full[i % kStages]; }   // page i can be scored
+    __device__ uint64_t *pv_done(int64_t i) { return &empty[i % kStages]; }  // PV(i) has completed
+    static __device__ uint32_t par(int64_t i) { return (uint32_t)(i / kStages) & 1; }
+    __device__ const StageDesc &page(int64_t i) const { return desc[i % kStages]; }
+    __device__ uint64_t *q_ready(int32_t pc) { return &q_full[pc % kQBufs]; }
+    __device__ uint32_t k_addr(int64_t i) { return smem_u32(k[i % kStages]); }
+    __device__ uint32_t v_addr(int64_t i) { return smem_u32(v[i % kStages]); }
+};
+static_assert(offsetof(DecodeTcSmem, v) % 1024 == 0 && offsetof(DecodeTcSmem, q) % 1024 == 0,
+              "128-byte swizzled tiles need 1024-byte alignment");
+
+// FP8 pools: E4M3 pages land in 4 stages; the converter warps turn page i
+// into f16 buffer i % 2 once PV(i - 2) has emptied it, so page i is ready
+// to score when its conversion is done.
+struct DecodeTc8Smem {
+    static constexpr bool kFP8 = true;
+    static constexpr int kStages = 4;
+    static constexpr int kConv = 3;
+    static constexpr int kSP = kConv;
+    static constexpr int kQBufs = 1;
+    static constexpr bool kTcQ = true;
+    static constexpr int kThreads = 352;
+    static constexpr uint32_t kQHalfBytes = 128 * 128;
+    uint8_t k[kStages][kK8Bytes];   // E4M3 [64 keys][128 B], 128-byte swizzle
+    uint8_t v[kStages][kV8Bytes];   // E4M3 V^T [128 d][64 B], 64-byte swizzle
+    uint8_t q[kQBufs][2 * kQHalfBytes];
+    uint8_t kc[kConv][kPageHeadBytes];  // f16 K [d half][64 keys][128 B], 128-byte swizzle
+    uint8_t vc[kConv][kD * 128];        // f16 V^T [128 d][64 keys = 128 B], 128-byte swizzle
+    float ks[kStages][kP], vs[kStages][kP];
+    float ksc[kConv][kP], vsc[kConv][kP];
+    float obuf[kD][32];
+    float ep_m[128], ep_l[128];
+    StageDesc desc[kStages];
+    StageDesc descc[kConv];
+    uint64_t full[kStages], empty[kStages];
+    uint64_t conv_full[kConv], conv_empty[kConv];
+    uint64_t q_full[2], q_empty[2], q_conv[2];
+    uint64_t s_full[kSP], p_full[kSP];
+    uint64_t mma_done[2], ep_bar;
+    uint32_t tmem_base;
+    int32_t abort;
+
+    __device__ uint64_t *ready(int64_t i) { return &conv_full[i % kConv]; }
+    __device__ uint64_t *pv_done(int64_t i) { return &conv_empty[i % kConv]; }
+    static __device__ uint32_t par(int64_t i) { return (uint32_t)(i / kConv) & 1; }
+    __device__ const StageDesc &page(int64_t i) const { return descc[i % kConv]; }
+    __device__ uint64_t *q_ready(int32_t pc) { return &q_conv[pc % kQBufs]; }
+    __device__ uint32_t k_addr(int64_t i) { return smem_u32(kc[i % kConv]); }
+    __device__ uint32_t v_addr(int64_t i) { return smem_u32(vc[i % kConv]); }
+};
+static_assert(offsetof(DecodeTc8Smem, q) % 1024 == 0 && offsetof(DecodeTc8Smem, kc) % 1024 == 0 &&
+                  offsetof(DecodeTc8Smem, vc) % 1024 == 0,
+              "128-byte swizzled tiles need 1024-byte alignment");
+
+template <class Smem>
+constexpr size_t decode_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+
+// Two threads issue the MMAs of the CTA's n pages, each in page order and
+// each waiting only on its own barriers:
+//   warp 5, lane 0: QK(i) into S buffer i % kSP once page i is ready (and,
+//     on a piece's first page, its q tile); commits s_full, and q_empty after
+//     the last QK of a piece;
+//   warp 6, lane 0: PV(i) once P(i) is in TMEM; commits pv_done(i) (the
+//     bf16 stage, or the FP8 pool's f16 buffer: K was read by QK(i) before
+//     P(i) existed).
+// A commit arrives once every MMA its thread issued before has completed.
+// Page i is ready only after PV(i - kSP), and with it the softmax of page
+// i - kSP, are done, so S and P buffer i % kSP are free. The s_full and
+// p_full barriers are per buffer: each is at most one phase ahead of a
+// waiter for the same reason.
+template <class Smem>
+__device__ bool decode_tc_qk(Smem &sm, const DecodeArgs &a, int64_t n) {
+    constexpr int kSP = Smem::kSP, kQB = Smem::kQBufs;
+    constexpr uint32_t kIdQK = idesc_16(128, kP, false, Smem::kFP8);
+    const uint32_t tb = sm.tmem_base, qb = smem_u32(sm.q[0]);
+    int32_t pc = -1;  // piece of the last scored page
+    for (int64_t i = 0; i < n; ++i) {
+        if (!mbar_wait(sm.ready(i), Smem::par(i), a.err)) return false;
+        const int32_t flags = sm.page(i).flags;
+        if (flags & kFirst) {
+            ++pc;
+            if (!mbar_wait(sm.q_ready(pc), (uint32_t)(pc / kQB) & 1, a.err)) return false;
+        }
+        if (*(volatile int32_t *)&sm.abort) return false;
+        tc_fence_after();
+        if (!(flags & kSkip)) {
+            const uint32_t q = qb + (pc % kQB) * 2 * Smem::kQHalfBytes, k = sm.k_addr(i);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tb + 64 * (uint32_t)(i % kSP),
+                       sdesc(q + (kk >> 2) * Smem::kQHalfBytes + (kk & 3) * 32, 16, 1024),
+                       sdesc(k + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024), kIdQK, kk > 0);
+        }
+        mma_commit(&sm.s_full[i % kSP]);
+        if (flags & kLast) mma_commit(&sm.q_empty[pc % kQB]);
+    }
+    return true;
+}
+
+template <class Smem>
+__device__ bool decode_tc_pv(Smem &sm, const DecodeArgs &a, int64_t n) {
+    constexpr int kSP = Smem::kSP;
+    // bf16: V as loaded, [keys][d] (d contiguous: MN-major B, d halves 8 KB
+    // apart); FP8: the converted V^T, [d][keys] (keys contiguous: K-major)
+    constexpr uint32_t kIdPV = idesc_16(128, kD, !Smem::kFP8, Smem::kFP8);
+    const uint32_t tb = sm.tmem_base;
+    bool fresh = true;  // no PV yet in the current piece: the next one overwrites O
+    for (int64_t i = 0; i < n; ++i) {
+        const int b = (int)(i % kSP);
+        if (!mbar_wait(&sm.p_full[b], (uint32_t)(i / kSP) & 1, a.err) || *(volatile int32_t *)&sm.abort)
+            return false;
+        const int32_t flags = sm.page(i).flags;
+        if (flags & kFirst) fresh = true;
+        tc_fence_after();
+        if (!(flags & kSkip)) {
+            const uint32_t tp = tb + kTmemP + 32 * b, v = sm.v_addr(i);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t vd = Smem::kFP8 ? sdesc(v + kk * 32, 16, 1024) : sdesc(v + kk * 2048, kBoxBytes, 1024);
+                mma_ts(tb + kTmemO, tp + kk * 8, vd, kIdPV, (fresh && kk == 0) ? 0u : 1u);
+            }
+            fresh = false;
+        }
+        mma_commit(sm.pv_done(i));
+    }
+    return true;
+}
+
+// Run one issuer role, then make sure every MMA it issued has completed
+// before TMEM is freed.
+template <bool kQK, class Smem>
+__device__ void decode_tc_issue(Smem &sm, const DecodeArgs &a, int64_t n) {
+    bool ok = kQK ? decode_tc_qk(sm, a, n) : decode_tc_pv(sm, a, n);
+    mma_commit(&sm.mma_done[kQK ? 0 : 1]);
+    if (!mbar_wait(&sm.mma_done[kQK ? 0 : 1], 0, a.err)) ok = false;
+    if (!ok) sm.abort = 1;
+}
+
+// S columns [col, col + kN) of this thread's lane.
+template <int kN>
+__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, uint32_t (&r)[kN]) {
+    if constexpr (kN == 16) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15}, [%16];"
+            : HSWA_R8(0), HSWA_R8(8)
+            : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" : HSWA_RW8(0), HSWA_RW8(8)::"memory");
+    } else {
+#pragma unroll
+        for (int c = 0; c < kN / 32; ++c) tmem_ld32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+#pragma unroll
+        for (int c = 0; c < kN / 32; ++c) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+    }
+}
+
+// kN packed P columns of this thread's lane.
+template <int kN>
+__device__ __forceinline__ void tmem_st_p(uint32_t taddr, const uint32_t (&r)[kN]) {
+    if constexpr (kN == 8) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     HSWA_W8(0)
+                     : "memory");
+    } else {
+#pragma unroll
+        for (int c = 0; c < kN / 16; ++c) tmem_st16(taddr + 16 * c, r + 16 * c);
+    }
+}
+
+// Bounded arrival + wait on the softmax warps' own barrier (128 threads).
+template <class Smem>
+__device__ __forceinline__ bool ep_sync(Smem &sm, uint32_t &phase, int *err) {
+    mbar_arrive(&sm.ep_bar);
+    const bool ok = mbar_wait(&sm.ep_bar, phase, err);
+    phase ^= 1;
+    return ok;
+}
+
+template <int kR, class Smem>
+__device__ void decode_tc_softmax(Smem &sm, const DecodeArgs &a, int64_t n) {
+    constexpr int kSP = Smem::kSP;
+    constexpr int kRows = 128 / kR;  // tile rows per copy
+    constexpr int kK = kP / kR;      // keys of a page per copy
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = threadIdx.x, c = r / kRows, j = r % kRows;
+    const int w = j >> 3, h = j & 7;
+    const bool active = (((warp * 32) % kRows) >> 3) < a.n_tok;  // uniform over the warp
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_o = sm.tmem_base + lane_off + kTmemO;
+    const uint32_t t_p = sm.tmem_base + lane_off + kTmemP + c * (kK / 2);
+    if constexpr (kR > 1) {
+        // P outside this copy's keys stays zero; the copy's own columns are
+        // rewritten on every page
+        uint32_t z[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) z[x] = 0u;
+#pragma unroll
+        for (int b = 0; b < kSP; ++b) tmem_st32(sm.tmem_base + lane_off + kTmemP + 32 * b, z);
+        tmem_wait_st();
+    }
+    float m_used = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of P
+    uint32_t ep_phase = 0;
+    bool ok = true;
+    for (int64_t i = 0; i < n && ok; ++i) {
+        const int b = (int)(i % kSP);  // S / P buffer
+        ok = mbar_wait(sm.ready(i), Smem::par(i), a.err) &&
+             mbar_wait(&sm.s_full[b], (uint32_t)(i / kSP) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const StageDesc d = sm.page(i);
+        if (d.flags & kFirst) m_used = -INFINITY, l = 0.f;
+        if (active) {
+            tc_fence_after();
+            uint32_t sr[kK];
+            tmem_ld_s<kK>(sm.tmem_base + lane_off + 64 * b + c * kK, sr);
+            if constexpr (Smem::kFP8) {  // the K codes entered the MMA as their exact values
+                const float *ks = sm.ksc[i % Smem::kConv] + c * kK;
+#pragma unroll
+                for (int x = 0; x < kK; ++x) sr[x] = __float_as_uint(__uint_as_float(sr[x]) * ks[x]);
+            }
+            // keys of the page this row's token sees, relative to the copy's
+            // first key: [lo_c, hi_c) (position t = len - n_tok + w; W keys
+            // ending at t for SWA)
+            const int32_t t = d.len - a.n_tok + w;
+            const int32_t base = d.key0 + c * kK;
+            int32_t hi_c = min(d.hi - c * kK, t - base + 1), lo_c = d.lo - c * kK;
+            if (a.window > 0) lo_c = max(lo_c, t - a.window + 1 - base);
+            if (w >= a.n_tok || (d.flags & kSkip)) hi_c = 0;
+            float m0 = -INFINITY, m1 = -INFINITY;
+            // most pages are seen whole by every token of the warp
+            if (__any_sync(0xffffffffu, lo_c > 0 || hi_c < kK)) {
+#pragma unroll
+                for (int x = 0; x < kK; ++x)
+                    if (x >= hi_c || x < lo_c) sr[x] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int x = 0; x < kK; x += 4) {
+                m0 = max3(m0, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
+                m1 = max3(m1, __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]));
+            }
+            const float mx = fmaxf(m0, m1) * a.scale_log2;
+            const bool need = mx > m_used + kTcRescaleLog2;
+            const bool resc = need && m_used != -INFINITY;
+            const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
+            if (need) m_used = mx;
+            const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+            const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
+            float2 sum2 = make_float2(0.f, 0.f);
+            uint32_t pk[kK / 2];
+#pragma unroll
+            for (int x = 0; x < kK / 2; ++x) {
+                const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])),
+                                            sc2, nm2);
+                const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+                sum2 = __fadd2_rn(sum2, p);
+                if constexpr (Smem::kFP8) {  // P carries the V scale: V codes enter the MMA as they are
+                    const float *vs = sm.vsc[i % Smem::kConv] + c * kK;
+                    pk[x] = pack_f16(p.x * vs[2 * x], p.y * vs[2 * x + 1]);
+                } else {
+                    pk[x] = pack_bf16(p.x, p.y);
+                }
+            }
+            tmem_st_p<kK / 2>(t_p + 32 * b, pk);  // P buffer i % kSP: free since page i is ready
+            if (__any_sync(0xffffffffu, resc)) {  // never on a piece's first page
+                // O holds the piece's earlier pages once PV(i - 1) is done
+                // (its pv_done barrier's next phase needs P(i - 1 + kSP);
+                // PV(i - 1 - kSP) is done since page i - 1 was ready)
+                ok = __all_sync(0xffffffffu, mbar_wait(sm.pv_done(i - 1), Smem::par(i - 1), a.err));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t ov[32];
+                    tmem_ld32(t_o + 32 * cc, ov);
+                    tmem_wait_ld(ov);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
+                    tmem_st32(t_o + 32 * cc, ov);
+                }
+            }
+            l = l * alpha + (sum2.x + sum2.y);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[b]);
+        if (!(d.flags & kLast)) continue;
+        // ---- end of the piece: O is final once PV(i) is done, the next
+        // phase of its pv_done barrier (PV(i - kSP) is done since page i was
+        // ready; PV(i + kSP) needs P(i + kSP))
+        if (active) ok = __all_sync(0xffffffffu, mbar_wait(sm.pv_done(i), Smem::par(i), a.err));
+        float M = m_used, L = l, wt = 1.f;
+        if constexpr (kR > 1) {
+            // merge the copies of each row: weights 2^(m_c - M); copy 0 adds
+            // the other copies' weighted rows into its own, 32 rows at a time
+            sm.ep_m[r] = m_used;
+            sm.ep_l[r] = l;
+            ok = ep_sync(sm, ep_phase, a.err) && ok;
+            M = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < kR; ++cc) M = fmaxf(M, sm.ep_m[cc * kRows + j]);
+            L = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kR; ++cc) {
+                const float mc = sm.ep_m[cc * kRows + j];
+                L += mc == -INFINITY ? 0.f : fast_exp2(mc - M) * sm.ep_l[cc * kRows + j];
+            }
+            wt = m_used == -INFINITY ? 0.f : fast_exp2(m_used - M);
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 1; cc < kR; ++cc) {
+#pragma unroll 1
+                for (int b = 0; b < kRows / 32; ++b) {
+                    if (active && ok && warp == (cc * kRows) / 32 + b) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t ov[32];
+                            tmem_ld32(t_o + 32 * q4, ov);
+                            tmem_wait_ld(ov);
+#pragma unroll
+                            for (int x = 0; x < 32; ++x) sm.obuf[32 * q4 + x][lane] = __uint_as_float(ov[x]) * wt;
+                        }
+                    }
+                    ok = ep_sync(sm, ep_phase, a.err) && ok;
+                    if (active && ok && warp == b) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t ov[32];
+                            tmem_ld32(t_o + 32 * q4, ov);
+                            tmem_wait_ld(ov);
+                            const float own = cc == 1 ? wt : 1.f;  // copy 0's own weight, applied once
+#pragma unroll
+                            for (int x = 0; x < 32; ++x)
+                                ov[x] = __float_as_uint(__uint_as_float(ov[x]) * own + sm.obuf[32 * q4 + x][lane]);
+                            tmem_st32(t_o + 32 * q4, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                    ok = ep_sync(sm, ep_phase, a.err) && ok;
+                }
+            }
+            wt = 1.f;
+        }
+        if (!ok) break;
+        if (!active || c != 0) continue;
+        tc_fence_after();
+        const bool row = w < a.n_tok;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        if (d.flags & kDirect) {
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                a.o + (q_row(a, d.seq, row ? w : 0) * a.hq + (int64_t)d.kvh * kG + h) * kD);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + 32 * q4, ov);
+                tmem_wait_ld(ov);
+                if (row) {
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        // L = 0: no key seen, write zeros (O may be unset)
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = L > 0.f ? __uint_as_float(ov[8 * x + e]) * inv : 0.f;
+                        dst[q4 * 4 + x] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                                     pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    }
+                }
+            }
+        } else {
+            Partial &p = a.part[((int64_t)blockIdx.x * 2 + d.slot) * a.n_tok + (row ? w : 0)];
+            float4 *dst = reinterpret_cast<float4 *>(p.o[h]);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + 32 * q4, ov);
+                tmem_wait_ld(ov);
+                if (row) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        float f[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) f[e] = L > 0.f ? __uint_as_float(ov[4 * x + e]) : 0.f;
+                        dst[q4 * 8 + x] = make_float4(f[0], f[1], f[2], f[3]);
+                    }
+                }
+            }
+            if (row) {
+                p.m[h] = M;
+                p.l[h] = L;
+            }
+        }
+    }
+    if (!ok) sm.abort = 1;
+}
+
+
+// Eight bf16 (one 16-byte chunk) to f16 in place, clamped to f16's finite range.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float lo = fminf(fmaxf(__uint_as_float(w[e] << 16), -65504.f), 65504.f);
+        const float hi = fminf(fmaxf(__uint_as_float(w[e] & 0xFFFF0000u), -65504.f), 65504.f);
+        w[e] = pack_f16(lo, hi);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Sixteen E4M3 codes (one 16-byte chunk) as sixteen exact f16 values.
+__device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4 &lo, uint4 &hi) {
+    e4m3x4_f16x2x2_cvt(c.x, lo.x, lo.y);
+    e4m3x4_f16x2x2_cvt(c.y, lo.z, lo.w);
+    e4m3x4_f16x2x2_cvt(c.z, hi.x, hi.y);
+    e4m3x4_f16x2x2_cvt(c.w, hi.z, hi.w);
+}
+
+// Warps 7-10 (FP8 pools): page i's E4M3 stage to f16 buffer i % kConv, once
+// PV(i - kConv) has emptied it (the f16 buffer's pv_done barrier, waited for
+// on every page, so it is never two phases ahead). K [64 keys][128 B]
+// becomes [d half][64 keys][128 B] and V^T [128 d][64 B] becomes
+// [128 d][128 B], both with the 128-byte swizzle; the scales and the
+// stage's descriptor are copied along.
+// On a piece's first page the piece's q tile is turned into f16 in place
+// first. Then the stage is released to the producer.
+__device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_t n) {
+    constexpr int kStages = DecodeTc8Smem::kStages, kConv = DecodeTc8Smem::kConv, kQB = DecodeTc8Smem::kQBufs;
+    const int t = threadIdx.x - 7 * 32;  // 0 .. 127
+    int32_t pc = -1;
+    bool ok = true;
+    for (int64_t i = 0; i < n && ok; ++i) {
+        const int st = (int)(i % kStages), b = (int)(i % kConv);
+        ok = mbar_wait(&sm.full[st], (uint32_t)(i / kStages) & 1, a.err) &&
+             (i < kConv || mbar_wait(&sm.conv_empty[b], (uint32_t)((i - kConv) / kConv) & 1, a.err)) &&
+             !*(volatile int32_t *)&sm.abort;
+        const StageDesc d = sm.desc[st];
+        if (ok && (d.flags & kFirst)) {
+            ++pc;
+            ok = mbar_wait(&sm.q_full[pc % kQB], (uint32_t)(pc / kQB) & 1, a.err);
+            if (ok) {
+                uint4 *q = reinterpret_cast<uint4 *>(sm.q[pc % kQB]);
+#pragma unroll 4
+                for (int x = t; x < 2 * (int)DecodeTc8Smem::kQHalfBytes / 16; x += 128) q[x] = bf16x8_to_f16x8(q[x]);
+                fence_proxy_async_shared();
+                mbar_arrive(&sm.q_conv[pc % kQB]);
+            }
+        }
+        if (!ok) break;
+        if (!(d.flags & kSkip)) {
+            const uint8_t *k8 = sm.k[st], *v8 = sm.v[st];
+            uint8_t *kc = sm.kc[b], *vc = sm.vc[b];
+            // all eight loads first: the stores below could alias them as far
+            // as the compiler can tell, and would otherwise serialise them
+            uint4 kin[4], vin[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int x = t + 128 * e;
+                const int r = x >> 3, c8 = x & 7;    // K: row r (key), chunk c8 (d 16 c8 .. 16 c8 + 15)
+                const int dd = x >> 2, c4 = x & 3;   // V^T: row dd (d), chunk c4 (keys 16 c4 .. 16 c4 + 15)
+                kin[e] = *reinterpret_cast<const uint4 *>(k8 + r * 128 + ((c8 ^ (r & 7)) << 4));
+                vin[e] = *reinterpret_cast<const uint4 *>(v8 + dd * 64 + ((c4 ^ ((dd >> 1) & 3)) << 4));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int x = t + 128 * e;
+                const int r = x >> 3, c8 = x & 7, dd = x >> 2, c4 = x & 3;
+                uint4 lo, hi;
+                e4m3x16_to_f16(kin[e], lo, hi);
+                uint8_t *krow = kc + (c8 >> 2) * kBoxBytes + r * 128;
+                const int j0 = 2 * (c8 & 3);
+                *reinterpret_cast<uint4 *>(krow + ((j0 ^ (r & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4 *>(krow + (((j0 + 1) ^ (r & 7)) << 4)) = hi;
+                e4m3x16_to_f16(vin[e], lo, hi);
+                uint8_t *vrow = vc + dd * 128;
+                *reinterpret_cast<uint4 *>(vrow + (((2 * c4) ^ (dd & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4 *>(vrow + (((2 * c4 + 1) ^ (dd & 7)) << 4)) = hi;
+            }
+        }
+        if (t < kP)
+            sm.ksc[b][t] = sm.ks[st][t];
+        else
+            sm.vsc[b][t - kP] = sm.vs[st][t - kP];
+        if (t == 0) sm.descc[b] = d;
+        fence_proxy_async_shared();  // the f16 tiles are read by the tensor cores
+        mbar_arrive(&sm.conv_full[b]);
+        mbar_arrive(&sm.empty[st]);
+    }
+    if (!ok) sm.abort = 1;
+}
+
+template <int kR, class Smem>
+__global__ void __launch_bounds__(Smem::kThreads, 1)
+    decode_tc_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, DecodeArgs a) {
+    extern __shared__ uint8_t raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Smem::kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            // bf16: the PV thread's commit; FP8: the 128 converter threads
+            mbar_init(&sm.empty[i], Smem::kFP8 ? 128 : 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.q_full[b], 1);
+            mbar_init(&sm.q_empty[b], 1);
+        }
+        for (int b = 0; b < Smem::kSP; ++b) {
+            mbar_init(&sm.s_full[b], 1);
+            mbar_init(&sm.p_full[b], 128);
+        }
+        if constexpr (Smem::kFP8) {
+            for (int b = 0; b < Smem::kConv; ++b) {
+                mbar_init(&sm.conv_full[b], 128);
+                mbar_init(&sm.conv_empty[b], 1);
+            }
+            for (int b = 0; b < 2; ++b) mbar_init(&sm.q_conv[b], 128);
+        }
+        mbar_init(&sm.mma_done[0], 1);
+        mbar_init(&sm.mma_done[1], 1);
+        mbar_init(&sm.ep_bar, 128);
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) tmem_alloc<kTcCols>(&sm.tmem_base);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();  // the plan (and the table update before it) is complete
+    pdl_launch_dependents();
+    const int64_t U = a.sdesc[a.n_seqs].x, N = gridDim.x;
+    const int64_t u0 = cta_start(blockIdx.x, U, N), u1 = cta_start(blockIdx.x + 1, U, N);
+    if (warp < 4) {
+        decode_tc_softmax<kR>(sm, a, u1 - u0);
+    } else if (warp == 4) {
+        decode_producer<Smem::kFP8>(sm, &tk, &tv, a, u0, u1, &tq);
+    } else if (warp < 7) {
+        if ((threadIdx.x & 31) == 0) {
+            if (warp == 5)
+                decode_tc_issue<true>(sm, a, u1 - u0);
+            else
+                decode_tc_issue<false>(sm, a, u1 - u0);
+        }
+        __syncwarp();
+    } else if constexpr (Smem::kFP8) {
+        decode_tc_convert(sm, a, u1 - u0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_free<kTcCols>(sm.tmem_base);
+}
+
 // Merge the partial records of segments split between CTAs; write zeros
 // for sequences without keys.
 __global__ void __launch_bounds__(256) decode_combine(DecodeArgs a, int32_t n_ctas) {
@@ -1560,8 +1735,10 @@ int decode_fp8_ctas_per_sm() {
 }
 
 // Query tokens one pass of the FP8 decode kernel serves; more tokens take
-// several passes over the pages.
+// several passes over the pages, unless the tensor-core kernel serves them
+// (from kTcMinTokensFp8 tokens) in one.
 constexpr int kFp8PassTokens = 2;
+constexpr int kTcMinTokensFp8 = 3;
 
 bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
     const hswa_config &c = pool->cfg;
@@ -1589,28 +1766,48 @@ int decode_ctas_per_sm_t() {
 
 int decode_ctas_per_sm() { return decode_ctas_per_sm_t<1>(); }
 
-template <int kR>
+template <int kR, class Smem>
 int decode_tc_ctas_per_sm_t() {
     static int v = -1;
     if (v < 0) {
-        if (cudaFuncSetAttribute(decode_tc_bf16_d128<kR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDecodeTcSmemBytes) != cudaSuccess)
+        constexpr size_t smem = decode_tc_smem_bytes<Smem>();
+        if (cudaFuncSetAttribute(decode_tc_d128<kR, Smem>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
             return -1;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_bf16_d128<kR>, kTcThreads,
-                                                          kDecodeTcSmemBytes) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_d128<kR, Smem>, Smem::kThreads, smem) !=
+            cudaSuccess)
             n = 1;
         v = std::max(1, n);
     }
     return v;
 }
 
+template <class Smem>
 int decode_tc_ctas_per_sm(int n_tok) {
     switch (tc_copies(n_tok)) {
-    case 4: return decode_tc_ctas_per_sm_t<4>();
-    case 2: return decode_tc_ctas_per_sm_t<2>();
-    default: return decode_tc_ctas_per_sm_t<1>();
+    case 4: return decode_tc_ctas_per_sm_t<4, Smem>();
+    case 2: return decode_tc_ctas_per_sm_t<2, Smem>();
+    default: return decode_tc_ctas_per_sm_t<1, Smem>();
     }
+}
+
+template <class Smem>
+cudaError_t launch_decode_tc(int n_tok, int n_ctas, cudaStream_t st, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const DecodeArgs &a) {
+    constexpr size_t smem = decode_tc_smem_bytes<Smem>();
+    switch (tc_copies(n_tok)) {
+    case 4: return launch_pdl(decode_tc_d128<4, Smem>, dim3(n_ctas), dim3(Smem::kThreads), smem, st, tq, tk, tv, a);
+    case 2: return launch_pdl(decode_tc_d128<2, Smem>, dim3(n_ctas), dim3(Smem::kThreads), smem, st, tq, tk, tv, a);
+    default: return launch_pdl(decode_tc_d128<1, Smem>, dim3(n_ctas), dim3(Smem::kThreads), smem, st, tq, tk, tv, a);
+    }
+}
+
+// q as [n_seqs * n_tok][Hq][d] for the tensor-core multi-token kernels: one
+// box is the n_tok x 8 query rows of a (sequence, kv head), 64 columns wide.
+bool make_q_tmap(CUtensorMap *tq, const void *q, const hswa_config &c, int n_seqs, int n_tok) {
+    return make_tmap_3d(tq, q, kD, (uint64_t)c.n_q_heads, (uint64_t)n_seqs * n_tok, 64, kG, (uint32_t)n_tok,
+                        CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Query tokens per sequence from which the tensor-core kernel serves a
@@ -1695,11 +1892,23 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (!decode_fp8_ok(pool, layer, q, o)) return HSWA_ERR_UNSUPPORTED;
     const int sms = sm_count();
-    const int per_sm1 = decode_fp8_ctas_per_sm<1>(), per_sm2 = decode_fp8_ctas_per_sm<2>();
-    if (sms <= 0 || per_sm1 <= 0 || per_sm2 <= 0) return HSWA_ERR_CUDA;
-    const int n_ctas1 = sms * std::min(per_sm1, kMaxCtasPerSm), n_ctas2 = sms * std::min(per_sm2, kMaxCtasPerSm);
-    const int max_pass = std::min(n_tok, kFp8PassTokens);
-    const size_t part_bytes = (size_t)std::max(n_ctas1, max_pass > 1 ? 2 * n_ctas2 : 0) * 2 * sizeof(Partial);
+    if (sms <= 0) return HSWA_ERR_CUDA;
+    const bool tc = n_tok >= kTcMinTokensFp8;
+    int n_ctas1 = 0, n_ctas2 = 0, n_ctas_tc = 0;
+    size_t part_bytes;
+    if (tc) {
+        const int per_sm = decode_tc_ctas_per_sm<DecodeTc8Smem>(n_tok);
+        if (per_sm <= 0) return HSWA_ERR_CUDA;
+        n_ctas_tc = sms * std::min(per_sm, kMaxCtasPerSm);
+        part_bytes = (size_t)n_ctas_tc * 2 * n_tok * sizeof(Partial);
+    } else {
+        const int per_sm1 = decode_fp8_ctas_per_sm<1>(), per_sm2 = decode_fp8_ctas_per_sm<2>();
+        if (per_sm1 <= 0 || per_sm2 <= 0) return HSWA_ERR_CUDA;
+        n_ctas1 = sms * std::min(per_sm1, kMaxCtasPerSm);
+        n_ctas2 = sms * std::min(per_sm2, kMaxCtasPerSm);
+        const int max_pass = std::min(n_tok, kFp8PassTokens);
+        part_bytes = (size_t)std::max(n_ctas1, max_pass > 1 ? 2 * n_ctas2 : 0) * 2 * sizeof(Partial);
+    }
     if (!ws || ((uintptr_t)ws & 255) || ws_bytes < desc_bytes(n_seqs) + part_bytes) return HSWA_ERR_INVALID_ARG;
     if (slots) {
         const int rc = hswa_append_kv(pool, layer, k_new, v_new, slots, n_seqs, stream);
@@ -1715,8 +1924,21 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
         !make_tmap_2d(&tv, layer->v_pool, blocks * kD, kP, kD, kP, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                       CU_TENSOR_MAP_SWIZZLE_64B))
         return HSWA_ERR_CUDA;
-    set_last_kernel(slots ? "append_kv_fp8+decode_mma_fp8_d128" : "decode_mma_fp8_d128");
     a.q_tok = n_tok;
+    if (tc) {  // one pass over the pages for all n_tok tokens, on the tensor cores
+        CUtensorMap tq;
+        if (!make_q_tmap(&tq, q, c, n_seqs, n_tok)) return HSWA_ERR_CUDA;
+        set_last_kernel("decode_tc_fp8_d128");
+        a.n_tok = n_tok;
+        if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok,
+                       0, static_cast<int4 *>(ws)) != cudaSuccess ||
+            launch_decode_tc<DecodeTc8Smem>(n_tok, n_ctas_tc, st, tq, tk, tv, a) != cudaSuccess ||
+            launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * n_tok), dim3(256), 0, st, a, n_ctas_tc) !=
+                cudaSuccess)
+            return HSWA_ERR_CUDA;
+        return HSWA_OK;
+    }
+    set_last_kernel(slots ? "append_kv_fp8+decode_mma_fp8_d128" : "decode_mma_fp8_d128");
     for (int tok0 = 0; tok0 < n_tok; tok0 += kFp8PassTokens) {
         const int pass = std::min(kFp8PassTokens, n_tok - tok0);
         const int n_ctas = pass == 1 ? n_ctas1 : n_ctas2;
@@ -1743,12 +1965,6 @@ cudaError_t launch_decode_kernel(int n_ctas, cudaStream_t st, const CUtensorMap 
                       decode_smem_bytes<kTok>(), st, tk, tv, a);
 }
 
-template <int kR>
-cudaError_t launch_decode_tc(int n_ctas, cudaStream_t st, const CUtensorMap &tq, const CUtensorMap &tk,
-                             const CUtensorMap &tv, const DecodeArgs &a) {
-    return launch_pdl(decode_tc_bf16_d128<kR>, dim3(n_ctas), dim3(kTcThreads), kDecodeTcSmemBytes, st, tq, tk, tv, a);
-}
-
 // Decode of n_tok query tokens per sequence, with an optional fused append
 // of one new token (slots / k_new / v_new non-null, n_tok == 1 only).
 int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o, const int32_t *d_bt,
@@ -1764,7 +1980,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool fused = slots != nullptr;
     if (pool->cfg.dtype == HSWA_DTYPE_FP8_E4M3) {
-        if ((int64_t)n_seqs * std::min(n_tok, kFp8PassTokens) > 65535) return HSWA_ERR_UNSUPPORTED;
+        if ((int64_t)n_seqs * n_tok > 65535) return HSWA_ERR_UNSUPPORTED;  // rows of the combine grid
         return decode_fp8(pool, layer, q, o, d_bt, d_seq_len, n_seqs, n_tok, scale, ws, ws_bytes, slots, k_new,
                           v_new, stream);
     }
@@ -1782,7 +1998,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     const int sms = sm_count();
     if (sms <= 0) return HSWA_ERR_CUDA;
     const bool tc = n_tok >= kTcMinTokens;
-    const int per_sm = tc ? decode_tc_ctas_per_sm(n_tok) : decode_ctas_per_sm_for(n_tok);
+    const int per_sm = tc ? decode_tc_ctas_per_sm<DecodeTcSmem>(n_tok) : decode_ctas_per_sm_for(n_tok);
     if (per_sm <= 0) return HSWA_ERR_CUDA;
     const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
     if (!ws || ((uintptr_t)ws & 255) ||
@@ -1801,11 +2017,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
         !make_tmap_2d(&tv, layer->v_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return HSWA_ERR_CUDA;
-    // q as [n_seqs * n_tok][Hq][d]: one box is the n_tok x 8 query rows of a
-    // (sequence, kv head), 64 columns wide
-    if (tc && !make_tmap_3d(&tq, q, kD, (uint64_t)c.n_q_heads, (uint64_t)n_seqs * n_tok, 64, kG, (uint32_t)n_tok,
-                            CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B))
-        return HSWA_ERR_CUDA;
+    if (tc && !make_q_tmap(&tq, q, c, n_seqs, n_tok)) return HSWA_ERR_CUDA;
     set_last_kernel(tc ? "decode_tc_bf16_d128" : fused ? "decode_mma_bf16_d128+append" : "decode_mma_bf16_d128");
     // three launches chained with programmatic dependent launch: each one
     // is scheduled while its predecessor finishes and waits for it on entry
@@ -1814,11 +2026,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
         return HSWA_ERR_CUDA;
     cudaError_t e;
     if (tc) {
-        switch (tc_copies(n_tok)) {
-        case 4: e = launch_decode_tc<4>(n_ctas, st, tq, tk, tv, a); break;
-        case 2: e = launch_decode_tc<2>(n_ctas, st, tq, tk, tv, a); break;
-        default: e = launch_decode_tc<1>(n_ctas, st, tq, tk, tv, a); break;
-        }
+        e = launch_decode_tc<DecodeTcSmem>(n_tok, n_ctas, st, tq, tk, tv, a);
     } else switch (n_tok) {
     case 1: e = launch_decode_kernel<1>(n_ctas, st, tk, tv, a); break;
     case 2: e = launch_decode_kernel<2>(n_ctas, st, tk, tv, a); break;

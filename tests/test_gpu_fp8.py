@@ -204,7 +204,7 @@ def fp8_multi_step(c, n_tok, seed, samples=None):
         o = torch.full((B * n_tok, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
         c.sess.decode_multi(layer, q.cuda(), o, B, n_tok, scale)
         assert c.sess.check() == 0
-        assert H.hswa_last_kernel() == "decode_mma_fp8_d128"
+        assert H.hswa_last_kernel() in ("decode_mma_fp8_d128", "decode_tc_fp8_d128")
         kc, ks, vc, vs = (x.cpu().numpy() for x in (c.sess.k[layer], c.sess.ks[layer], c.sess.v[layer],
                                                      c.sess.vs[layer]))
         lens = c.ora.seq_len[samples]
@@ -222,10 +222,11 @@ def fp8_multi_step(c, n_tok, seed, samples=None):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("n_tok", [2, 3, 4, 5, 8])
+@pytest.mark.parametrize("n_tok", [2, 3, 4, 5, 8, 9, 16])
 def test_fp8_multi_token_decode_matches_oracle(n_tok):
-    """Multi-token decode over FP8 pools: passes of up to two tokens, lengths
-    around page edges and the window, one sequence shorter than n_tok."""
+    """Multi-token decode over FP8 pools (passes of two tokens on mma.sync,
+    or one pass on the tensor cores with the pages converted to f16 in
+    shared memory), lengths around page edges and the window."""
     cached = [0, 1, 62, 63, 64, 125, 126, 127, 128, 700, 3000]
     c = Fp8Case(cached, seed=73, extra=24)
     fp8_multi_step(c, n_tok, seed=1300 + n_tok)
@@ -242,12 +243,13 @@ def test_fp8_multi_token_decode_steps_with_release():
 
 
 @pytest.mark.gpu
-def test_fp8_multi_token_full_size_sampled():
-    """The decode-batch workload over FP8 pools with 4 query tokens per
-    sequence (two passes), oracle on sampled sequences."""
+@pytest.mark.parametrize("n_tok", [2, 8])
+def test_fp8_multi_token_full_size_sampled(n_tok):
+    """The decode-batch workload over FP8 pools with n_tok query tokens per
+    sequence, oracle on sampled sequences."""
     w = wl.decode_batch()
     c = Fp8Case(list(w.cached), seed=82, extra=8)
-    fp8_multi_step(c, 4, seed=1500, samples=[0, 1, 17, 31, 32, 50, 63])
+    fp8_multi_step(c, n_tok, seed=1500 + n_tok, samples=[0, 1, 17, 31, 32, 50, 63])
 
 
 def fp8_window_pack(c, layer, lens):
