@@ -130,17 +130,14 @@ struct DecodeArgs {
     const __nv_bfloat16 *k_new, *v_new;
     int64_t pool_slots;
     int32_t n_seqs, bt_stride, hkv, hq, window, num_pages;
-    // query tokens per sequence: q and o hold q_tok rows per sequence; this
-    // launch serves its rows tok0 .. tok0 + n_tok - 1, the last n_tok
-    // positions before the plan's key end (1, 1, 0 for plain decode)
-    int32_t n_tok, q_tok, tok0;
+    int32_t n_tok;  // query tokens per sequence (multi-token decode), 1 otherwise
     float scale_log2;
     int *err;
 };
 
-// Row of q / o holding query token tok0 + w of sequence s.
+// Row of q / o holding query token w of sequence s.
 __device__ __forceinline__ int64_t q_row(const DecodeArgs &a, int32_t s, int32_t w) {
-    return (int64_t)s * a.q_tok + a.tok0 + w;
+    return (int64_t)s * a.n_tok + w;
 }
 
 // Tensor-core multi-token decode: copies of the 8 n_tok query rows in the
@@ -157,10 +154,8 @@ __device__ __forceinline__ void key_range(int32_t L, int32_t window, int32_t n_t
 // Per-sequence descriptors: the first unit of the sequence (prefix sum of
 // units(s) = Hkv * pages touched by the key range [lo, hi)), lo, hi, units.
 // desc[n].x is the total number of units.
-// len_off: the keys end len_off short of seq_len (a pass over the earlier
-// query tokens of a multi-token decode).
 __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int32_t hkv, int32_t page,
-                            int32_t window, int32_t n_tok, int32_t len_off, int4 *__restrict__ desc) {
+                            int32_t window, int32_t n_tok, int4 *__restrict__ desc) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -172,7 +167,7 @@ __global__ void decode_plan(const int32_t *__restrict__ seq_len, int32_t n, int3
         const int32_t i = base + tid;
         int32_t u = 0, lo = 0, hi = 0;
         if (i < n) {
-            key_range(max(seq_len[i] - len_off, 0), window, n_tok, lo, hi);
+            key_range(seq_len[i], window, n_tok, lo, hi);
             if (hi > lo) u = hkv * ((hi - 1) / page - lo / page + 1);
         }
         int32_t x = u;  // inclusive warp scan
@@ -1734,10 +1729,8 @@ int decode_fp8_ctas_per_sm() {
     return v;
 }
 
-// Query tokens one pass of the FP8 decode kernel serves; more tokens take
-// several passes over the pages, unless the tensor-core kernel serves them
-// (from kTcMinTokensFp8 tokens) in one.
-constexpr int kFp8PassTokens = 2;
+// Query tokens per sequence from which an FP8 decode runs on the tensor-core
+// kernel (below it, decode_mma_fp8_d128 serves 1 or 2 tokens in one pass).
 constexpr int kTcMinTokensFp8 = 3;
 
 bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
@@ -1874,18 +1867,15 @@ int fill_args(DecodeArgs &a, const hswa_pool *pool, const hswa_layer *layer, con
     a.hq = c.n_q_heads;
     a.window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
     a.num_pages = num_pages;
-    a.n_tok = a.q_tok = 1;
-    a.tok0 = 0;
+    a.n_tok = 1;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = error_word();
     return num_pages;
 }
 
 // Decode over an FP8 pool (a fused append quantizes first, as its own
-// launch). n_tok query tokens per sequence go in passes of up to
-// kFp8PassTokens tokens: pass (tok0, P) plans the key range of tokens
-// tok0 .. tok0 + P - 1 (the keys end n_tok - tok0 - P short of seq_len),
-// streams those pages once for its P tokens and merges its own partials.
+// launch): 1 or 2 query tokens per sequence on decode_mma_fp8_d128, more on
+// the tensor-core kernel with the pages turned into f16 in shared memory.
 int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o, const int32_t *d_bt,
                const int32_t *d_seq_len, int n_seqs, int n_tok, float scale, void *ws, size_t ws_bytes,
                const int32_t *slots, const void *k_new, const void *v_new, hswa_stream_t stream) {
@@ -1894,22 +1884,13 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
     const int sms = sm_count();
     if (sms <= 0) return HSWA_ERR_CUDA;
     const bool tc = n_tok >= kTcMinTokensFp8;
-    int n_ctas1 = 0, n_ctas2 = 0, n_ctas_tc = 0;
-    size_t part_bytes;
-    if (tc) {
-        const int per_sm = decode_tc_ctas_per_sm<DecodeTc8Smem>(n_tok);
-        if (per_sm <= 0) return HSWA_ERR_CUDA;
-        n_ctas_tc = sms * std::min(per_sm, kMaxCtasPerSm);
-        part_bytes = (size_t)n_ctas_tc * 2 * n_tok * sizeof(Partial);
-    } else {
-        const int per_sm1 = decode_fp8_ctas_per_sm<1>(), per_sm2 = decode_fp8_ctas_per_sm<2>();
-        if (per_sm1 <= 0 || per_sm2 <= 0) return HSWA_ERR_CUDA;
-        n_ctas1 = sms * std::min(per_sm1, kMaxCtasPerSm);
-        n_ctas2 = sms * std::min(per_sm2, kMaxCtasPerSm);
-        const int max_pass = std::min(n_tok, kFp8PassTokens);
-        part_bytes = (size_t)std::max(n_ctas1, max_pass > 1 ? 2 * n_ctas2 : 0) * 2 * sizeof(Partial);
-    }
-    if (!ws || ((uintptr_t)ws & 255) || ws_bytes < desc_bytes(n_seqs) + part_bytes) return HSWA_ERR_INVALID_ARG;
+    const int per_sm = tc ? decode_tc_ctas_per_sm<DecodeTc8Smem>(n_tok)
+                          : n_tok == 1 ? decode_fp8_ctas_per_sm<1>() : decode_fp8_ctas_per_sm<2>();
+    if (per_sm <= 0) return HSWA_ERR_CUDA;
+    const int n_ctas = sms * std::min(per_sm, kMaxCtasPerSm);
+    if (!ws || ((uintptr_t)ws & 255) ||
+        ws_bytes < desc_bytes(n_seqs) + (size_t)n_ctas * 2 * n_tok * sizeof(Partial))
+        return HSWA_ERR_INVALID_ARG;
     if (slots) {
         const int rc = hswa_append_kv(pool, layer, k_new, v_new, slots, n_seqs, stream);
         if (rc != HSWA_OK) return rc;
@@ -1917,45 +1898,31 @@ int decode_fp8(const hswa_pool *pool, const hswa_layer *layer, const void *q, vo
     const hswa_config &c = pool->cfg;
     DecodeArgs a;
     const int32_t num_pages = fill_args(a, pool, layer, q, o, d_bt, d_seq_len, n_seqs, scale, ws);
+    a.n_tok = n_tok;
     const uint64_t blocks = (uint64_t)num_pages * c.n_kv_heads;
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, tq;
     if (!make_tmap_2d(&tk, layer->k_pool, blocks * kP, kD, kP, kD, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tv, layer->v_pool, blocks * kD, kP, kD, kP, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                      CU_TENSOR_MAP_SWIZZLE_64B))
+                      CU_TENSOR_MAP_SWIZZLE_64B) ||
+        (tc && !make_q_tmap(&tq, q, c, n_seqs, n_tok)))
         return HSWA_ERR_CUDA;
-    a.q_tok = n_tok;
-    if (tc) {  // one pass over the pages for all n_tok tokens, on the tensor cores
-        CUtensorMap tq;
-        if (!make_q_tmap(&tq, q, c, n_seqs, n_tok)) return HSWA_ERR_CUDA;
-        set_last_kernel("decode_tc_fp8_d128");
-        a.n_tok = n_tok;
-        if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok,
-                       0, static_cast<int4 *>(ws)) != cudaSuccess ||
-            launch_decode_tc<DecodeTc8Smem>(n_tok, n_ctas_tc, st, tq, tk, tv, a) != cudaSuccess ||
-            launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * n_tok), dim3(256), 0, st, a, n_ctas_tc) !=
-                cudaSuccess)
-            return HSWA_ERR_CUDA;
-        return HSWA_OK;
+    set_last_kernel(tc ? "decode_tc_fp8_d128" : slots ? "append_kv_fp8+decode_mma_fp8_d128" : "decode_mma_fp8_d128");
+    cudaError_t e = launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP,
+                               a.window, n_tok, static_cast<int4 *>(ws));
+    if (e == cudaSuccess) {
+        if (tc)
+            e = launch_decode_tc<DecodeTc8Smem>(n_tok, n_ctas, st, tq, tk, tv, a);
+        else if (n_tok == 1)
+            e = launch_pdl(decode_mma_fp8_d128<1>, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)),
+                           decode_smem8_bytes<1>(), st, tk, tv, a);
+        else
+            e = launch_pdl(decode_mma_fp8_d128<2>, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)),
+                           decode_smem8_bytes<2>(), st, tk, tv, a);
     }
-    set_last_kernel(slots ? "append_kv_fp8+decode_mma_fp8_d128" : "decode_mma_fp8_d128");
-    for (int tok0 = 0; tok0 < n_tok; tok0 += kFp8PassTokens) {
-        const int pass = std::min(kFp8PassTokens, n_tok - tok0);
-        const int n_ctas = pass == 1 ? n_ctas1 : n_ctas2;
-        a.n_tok = pass;
-        a.tok0 = tok0;
-        cudaError_t e = launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP,
-                                   a.window, pass, n_tok - tok0 - pass, static_cast<int4 *>(ws));
-        if (e == cudaSuccess)
-            e = pass == 1 ? launch_pdl(decode_mma_fp8_d128<1>, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)),
-                                       decode_smem8_bytes<1>(), st, tk, tv, a)
-                          : launch_pdl(decode_mma_fp8_d128<2>, dim3(n_ctas), dim3(32 * (kConsumers8 + 1)),
-                                       decode_smem8_bytes<2>(), st, tk, tv, a);
-        if (e == cudaSuccess)
-            e = launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * pass), dim3(256), 0, st, a, n_ctas);
-        if (e != cudaSuccess) return HSWA_ERR_CUDA;
-    }
-    return HSWA_OK;
+    if (e == cudaSuccess)
+        e = launch_pdl(decode_combine, dim3(c.n_kv_heads, n_seqs * n_tok), dim3(256), 0, st, a, n_ctas);
+    return e == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
 }
 
 template <int kTok>
@@ -2009,7 +1976,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     a.slots = slots;
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-    a.n_tok = a.q_tok = n_tok;
+    a.n_tok = n_tok;
     CUtensorMap tk, tv, tq;
     const uint64_t rows = (uint64_t)num_pages * c.n_kv_heads * kP;
     if (!make_tmap_2d(&tk, layer->k_pool, rows, kD, 64, 64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -2021,7 +1988,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
     set_last_kernel(tc ? "decode_tc_bf16_d128" : fused ? "decode_mma_bf16_d128+append" : "decode_mma_bf16_d128");
     // three launches chained with programmatic dependent launch: each one
     // is scheduled while its predecessor finishes and waits for it on entry
-    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok, 0,
+    if (launch_pdl(decode_plan, dim3(1), dim3(1024), 0, st, d_seq_len, n_seqs, c.n_kv_heads, kP, a.window, n_tok,
                    static_cast<int4 *>(ws)) != cudaSuccess)
         return HSWA_ERR_CUDA;
     cudaError_t e;
