@@ -232,3 +232,14 @@ def test_multi_token_bad_table_entries_set_bounds_and_skip(n_tok):
     assert sc.sess.check() == 0
     assert torch.isfinite(o.float()).all()
     assert torch.equal(o[2 * n_tok:].float(), torch.zeros_like(o[2 * n_tok:].float()))  # no key left
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_tok", [3, 8, 16])
+def test_multi_token_decode_window_shorter_than_the_draft(n_tok):
+    """A window of 8 keys (W < n_tok for the longer drafts): each token's
+    keys end at itself and start W - 1 before it, so the first drafts fall
+    out of the later tokens' windows; both kernels, ragged lengths."""
+    cached = [0, 5, 60, 63, 64, 200, 1000]
+    sc = Scenario(64, 8, 128, 64, 8, wl.DTYPE_BF16, cached, seed=17, extra_tokens=16)
+    run_multi_step(sc, n_tok, seed=1700 + n_tok, expect_kernel=FAST)
