@@ -364,3 +364,27 @@ def test_fp8_chunked_prefill_full_size_sampled():
         got = o.float().cpu().numpy()[rows]
         assert np.isfinite(got).all()
         assert float(np.abs(got - exp).max()) <= 2e-2, layer
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_tok", [2, 8])
+def test_fp8_multi_token_bad_table_entries_set_bounds_and_skip(n_tok):
+    """Invalid block-table entries inside the key range of an FP8 multi-token
+    decode (the first page of a segment, a page past the pool, every page of
+    one sequence): HSWA_ERR_BOUNDS, pages skipped, output finite, zeros where
+    no key is left. Three sequences leave most CTAs without work."""
+    c = Fp8Case([300, 300, 60], seed=75, extra=16)
+    B = c.B
+    c.sess.reserve(range(B), [n_tok] * B)
+    c.sess.sync()
+    c.sess.d_full_bt[0, 0] = -1
+    c.sess.d_full_bt[1, 3] = 1 << 30
+    c.sess.d_full_bt[2, 0] = -1
+    c.sess.d_full_bt[2, 1] = -1
+    q = wl.normal((B * n_tok, HQ, D), 1600, wl.DTYPE_BF16).cuda()
+    o = torch.full_like(q, float("nan"))
+    c.sess.decode_multi(0, q, o, B, n_tok, 1 / math.sqrt(D))
+    assert c.sess.check() == H.HSWA_ERR_BOUNDS
+    assert c.sess.check() == 0
+    assert torch.isfinite(o.float()).all()
+    assert torch.equal(o[2 * n_tok:].float(), torch.zeros_like(o[2 * n_tok:].float()))
