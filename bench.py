@@ -1288,24 +1288,24 @@ def measure_transfer(steps, fp8=False, w=None):
         tb.stream.synchronize()
         g_s += e[0].elapsed_time(e[1]) / 1e3
         s_s += e[2].elapsed_time(e[3]) / 1e3
-    # the host-link ceiling: a copy-engine memcpy of one layer's packed bytes
+    # the host-link ceiling: a copy-engine memcpy of one layer's packed bytes,
+    # two warm-up copies each way, then the median of seven timed copies
     one = tb.host[0].numel()
     dev = torch.empty(one, dtype=tb.host[0].dtype, device="cuda")
-    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    with torch.cuda.stream(tb.stream):
-        for _ in range(2):
-            dev.copy_(tb.host[0], non_blocking=True)
-        e[0].record(tb.stream)
-        for _ in range(5):
-            tb.host[1].copy_(dev, non_blocking=True)
-        e[1].record(tb.stream)
-        for _ in range(5):
-            dev.copy_(tb.host[1], non_blocking=True)
-        e[2].record(tb.stream)
-    tb.stream.synchronize()
     nbytes = one * dev.element_size()
-    d2h = 5 * nbytes / (e[0].elapsed_time(e[1]) / 1e3) / 1e9
-    h2d = 5 * nbytes / (e[1].elapsed_time(e[2]) / 1e3) / 1e9
+    link = {}
+    with torch.cuda.stream(tb.stream):
+        for name, dst, src in (("d2h", tb.host[1], dev), ("h2d", dev, tb.host[1])):
+            for _ in range(2):
+                dst.copy_(src, non_blocking=True)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+            ev[0].record(tb.stream)
+            for k in range(7):
+                dst.copy_(src, non_blocking=True)
+                ev[k + 1].record(tb.stream)
+            tb.stream.synchronize()
+            link[name] = float(np.median([nbytes / (ev[k].elapsed_time(ev[k + 1]) / 1e3) / 1e9 for k in range(7)]))
+    d2h, h2d = link["d2h"], link["h2d"]
     del dev
     rel_times, live = tb.release_rounds()
     st = tb.sess.check()
