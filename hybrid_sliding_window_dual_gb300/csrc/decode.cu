@@ -1009,7 +1009,8 @@ struct DecodeTc8Smem {
     static constexpr int kSP = kConv;
     static constexpr int kQBufs = 1;
     static constexpr bool kTcQ = true;
-    static constexpr int kThreads = 352;
+    static constexpr int kConvThreads = 128;  // converter warps 7 ..
+    static constexpr int kThreads = 224 + kConvThreads;
     static constexpr uint32_t kQHalfBytes = 128 * 128;
     uint8_t k[kStages][kK8Bytes];   // E4M3 [64 keys][128 B], 128-byte swizzle
     uint8_t v[kStages][kV8Bytes];   // E4M3 V^T [128 d][64 B], 64-byte swizzle
@@ -1413,7 +1414,8 @@ __device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4 &lo, uint4 &hi) {
 // first. Then the stage is released to the producer.
 __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_t n) {
     constexpr int kStages = DecodeTc8Smem::kStages, kConv = DecodeTc8Smem::kConv, kQB = DecodeTc8Smem::kQBufs;
-    const int t = threadIdx.x - 7 * 32;  // 0 .. 127
+    constexpr int kCT = DecodeTc8Smem::kConvThreads, kPer = 512 / kCT;  // 16-byte chunks per thread and tile
+    const int t = threadIdx.x - 7 * 32;  // 0 .. kCT - 1
     int32_t pc = -1;
     bool ok = true;
     for (int64_t i = 0; i < n && ok; ++i) {
@@ -1428,7 +1430,7 @@ __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_
             if (ok) {
                 uint4 *q = reinterpret_cast<uint4 *>(sm.q[pc % kQB]);
 #pragma unroll 4
-                for (int x = t; x < 2 * (int)DecodeTc8Smem::kQHalfBytes / 16; x += 128) q[x] = bf16x8_to_f16x8(q[x]);
+                for (int x = t; x < 2 * (int)DecodeTc8Smem::kQHalfBytes / 16; x += kCT) q[x] = bf16x8_to_f16x8(q[x]);
                 fence_proxy_async_shared();
                 mbar_arrive(&sm.q_conv[pc % kQB]);
             }
@@ -1439,18 +1441,18 @@ __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_
             uint8_t *kc = sm.kc[b], *vc = sm.vc[b];
             // all eight loads first: the stores below could alias them as far
             // as the compiler can tell, and would otherwise serialise them
-            uint4 kin[4], vin[4];
+            uint4 kin[kPer], vin[kPer];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int x = t + 128 * e;
+            for (int e = 0; e < kPer; ++e) {
+                const int x = t + kCT * e;
                 const int r = x >> 3, c8 = x & 7;    // K: row r (key), chunk c8 (d 16 c8 .. 16 c8 + 15)
                 const int dd = x >> 2, c4 = x & 3;   // V^T: row dd (d), chunk c4 (keys 16 c4 .. 16 c4 + 15)
                 kin[e] = *reinterpret_cast<const uint4 *>(k8 + r * 128 + ((c8 ^ (r & 7)) << 4));
                 vin[e] = *reinterpret_cast<const uint4 *>(v8 + dd * 64 + ((c4 ^ ((dd >> 1) & 3)) << 4));
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int x = t + 128 * e;
+            for (int e = 0; e < kPer; ++e) {
+                const int x = t + kCT * e;
                 const int r = x >> 3, c8 = x & 7, dd = x >> 2, c4 = x & 3;
                 uint4 lo, hi;
                 e4m3x16_to_f16(kin[e], lo, hi);
@@ -1466,7 +1468,7 @@ __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_
         }
         if (t < kP)
             sm.ksc[b][t] = sm.ks[st][t];
-        else
+        else if (t < 2 * kP)
             sm.vsc[b][t - kP] = sm.vs[st][t - kP];
         if (t == 0) sm.descc[b] = d;
         fence_proxy_async_shared();  // the f16 tiles are read by the tensor cores
@@ -1487,7 +1489,7 @@ __global__ void __launch_bounds__(Smem::kThreads, 1)
         for (int i = 0; i < Smem::kStages; ++i) {
             mbar_init(&sm.full[i], 1);
             // bf16: the PV thread's commit; FP8: the 128 converter threads
-            mbar_init(&sm.empty[i], Smem::kFP8 ? 128 : 1);
+            mbar_init(&sm.empty[i], Smem::kFP8 ? Smem::kThreads - 224 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.q_full[b], 1);
@@ -1499,10 +1501,10 @@ __global__ void __launch_bounds__(Smem::kThreads, 1)
         }
         if constexpr (Smem::kFP8) {
             for (int b = 0; b < Smem::kConv; ++b) {
-                mbar_init(&sm.conv_full[b], 128);
+                mbar_init(&sm.conv_full[b], Smem::kThreads - 224);
                 mbar_init(&sm.conv_empty[b], 1);
             }
-            for (int b = 0; b < 2; ++b) mbar_init(&sm.q_conv[b], 128);
+            for (int b = 0; b < 2; ++b) mbar_init(&sm.q_conv[b], Smem::kThreads - 224);
         }
         mbar_init(&sm.mma_done[0], 1);
         mbar_init(&sm.mma_done[1], 1);
