@@ -319,7 +319,10 @@ class DecodeBatch:
         # with one copy per direction
         nq, nkv = B * w.n_q_heads * w.head_dim, B * w.n_kv_heads * w.head_dim
         self.io_in = torch.empty(2 * (nq + 2 * nkv), dtype=dt, device="cuda")
-        self.io_out = torch.empty(2 * nq, dtype=dt, device="cuda")
+        # two output blocks: the end-to-end step reads block k % 2 back on a
+        # copy stream while the next step writes the other one
+        self.io_outs = [torch.empty(2 * nq, dtype=dt, device="cuda") for _ in range(2)]
+        self.io_out = self.io_outs[0]
         views = lambda buf, off, n, shape: buf[off:off + n].view(shape)
         qs, kvs = (B, w.n_q_heads, w.head_dim), (B, w.n_kv_heads, w.head_dim)
         per = nq + 2 * nkv
@@ -330,7 +333,8 @@ class DecodeBatch:
             self.q[i].copy_(wl.normal(qs, 100 + i, w.dtype, "cuda"))
             self.kn[i].copy_(wl.normal(kvs, 200 + i, w.dtype, "cuda"))
             self.vn[i].copy_(wl.normal(kvs, 300 + i, w.dtype, "cuda"))
-        self.o = [views(self.io_out, i * nq, nq, qs) for i in range(2)]
+        self.o_bufs = [[views(blk, i * nq, nq, qs) for i in range(2)] for blk in self.io_outs]
+        self.o = self.o_bufs[0]
         # double-buffered pinned staging for the slots of a step, each buffer
         # reused only after its previous copy has run
         self.slot_host = [torch.empty(2, B, dtype=torch.int32, pin_memory=True) for _ in range(2)]
@@ -342,12 +346,14 @@ class DecodeBatch:
         self.launches = 0
         self.decode_events = []
         # host-buffer (end-to-end) variants: the pinned input block, and the
-        # outputs double-buffered (step k's result is read on the host while
-        # step k + 1 runs; the host waits for step k's copy before it returns
-        # from step k + 1)
+        # outputs double-buffered: step k's result goes back to the host on a
+        # copy stream while step k + 1 runs (the host waits for step k's copy
+        # before it returns from step k + 1, and step k + 2 writes the block
+        # only after that copy)
         self.h_in = self.io_in.cpu().pin_memory()
         self.h_o = [torch.empty_like(self.io_out, device="cpu").pin_memory() for _ in range(2)]
         self.out_ready = [None, None]
+        self.copy_stream = torch.cuda.Stream()
         self.out_sum = 0.0
         torch.cuda.synchronize()
 
@@ -371,21 +377,28 @@ class DecodeBatch:
             self.launches += 1
             if host_io:  # the step's inputs, both layers, one copy
                 self.io_in.copy_(self.h_in, non_blocking=True)
+                if self.out_ready[buf] is not None:  # block buf's previous copy to the host
+                    self.stream.wait_event(self.out_ready[buf])
+            out = self.o_bufs[buf] if host_io else self.o
             for i in range(2):
                 if time_full_decode and i == 0:
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(self.stream)
                 # append the new token's K/V and attend, one call (plan, main, combine)
-                sess.decode_append(i, self.q[i], self.kn[i], self.vn[i], self.slot_dev[i], self.o[i], B, self.scale)
+                sess.decode_append(i, self.q[i], self.kn[i], self.vn[i], self.slot_dev[i], out[i], B, self.scale)
                 if time_full_decode and i == 0:
                     e1.record(self.stream)
                     self.decode_events.append((e0, e1))
                 self.launches += 3
-            if host_io:  # the step's outputs, both layers, one copy
-                self.h_o[buf].copy_(self.io_out, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(self.stream)
+            if host_io:  # the step's outputs, both layers, one copy, on the copy stream
+                done = torch.cuda.Event()
+                done.record(self.stream)
+                self.copy_stream.wait_event(done)
+                with torch.cuda.stream(self.copy_stream):
+                    self.h_o[buf].copy_(self.io_outs[buf], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(self.copy_stream)
                 self.out_ready[buf] = ev
         self.steps_done += 1
         if self.steps_done % 64 == 0:
@@ -393,6 +406,12 @@ class DecodeBatch:
         if host_io:
             # the previous step's result is read on the host (this one's next)
             self.read_output(1 - buf)
+
+    def join_copies(self):
+        """The compute stream waits for the result copies still in flight."""
+        for ev in self.out_ready:
+            if ev is not None:
+                self.stream.wait_event(ev)
 
     def read_output(self, buf):
         if self.out_ready[buf] is not None:
@@ -860,7 +879,9 @@ class SwaTransfer:
         return times, live
 
 
-def time_steps(run, steps, stream, world):
+def time_steps(run, steps, stream, world, finish=None):
+    """Seconds for `steps` calls of run(), events on `stream`; finish() (if
+    given) makes `stream` wait for work the steps left on other streams."""
     import torch
     barrier(world)
     torch.cuda.synchronize()
@@ -869,6 +890,8 @@ def time_steps(run, steps, stream, world):
     e0.record(stream)
     for _ in range(steps):
         run()
+    if finish is not None:
+        finish()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -924,7 +947,8 @@ def run_decode(args, world, rank, local):
     if args.breakdown:
         bd = bench.breakdown(50)
     # end to end: host buffers in, host buffers out, copies inside the timed region
-    e2e_secs = time_steps(lambda: bench.step(host_io=True), args.steps, bench.stream, world)
+    e2e_secs = time_steps(lambda: bench.step(host_io=True), args.steps, bench.stream, world,
+                          finish=bench.join_copies)
     for b in range(2):  # the last step's result
         bench.read_output(b)
     bench.finish()
