@@ -156,7 +156,7 @@ class DualPoolSession:
     def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale):
         need = B.hswa_prefill_workspace_size(self.pool, self.layers[layer], n_seqs, max_q_len)
         ws = None
-        if need:  # FP8 pools stage bf16 copies of the pages the chunk reads
+        if need:  # FP8 pools stage f16 copies of the pages the chunk reads (and of q)
             if self.prefill_ws is None or self.prefill_ws.numel() < need:
                 self.prefill_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
             ws = self.prefill_ws
