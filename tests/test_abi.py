@@ -161,6 +161,23 @@ def test_device_calls_validate_before_launching():
     H.hswa_pool_destroy(lp)
 
 
+@pytest.mark.parametrize("dtype", [H.HSWA_DTYPE_BF16, H.HSWA_DTYPE_FP8_E4M3])
+def test_decode_refuses_more_rows_than_the_merge_grid_takes(dtype):
+    """The partial-record merge runs one CTA row per (sequence, token): at
+    most 65535 rows, so 4096 sequences of 16 tokens are refused with
+    HSWA_ERR_UNSUPPORTED before any launch, and 4095 are not refused for
+    that reason."""
+    cfg = H.Config(window=128, page_size=64, n_q_heads=64, n_kv_heads=8, head_dim=128, dtype=dtype,
+                   full_pages=64, swa_pages=64, max_seqs=4096, max_pages_per_seq=4)
+    lp = H.hswa_pool_create(cfg, None, None)
+    scales = dict(k_scale=16, v_scale=16) if dtype == H.HSWA_DTYPE_FP8_E4M3 else {}
+    layer = H.Layer(kind=H.HSWA_KIND_FULL, window=0, k_pool=16, v_pool=16, **scales)
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_decode_multi(lp, layer, 16, 16, 16, 16, 4096, 16, 1.0, 256, 1 << 30)
+    assert e.value.status == H.HSWA_ERR_UNSUPPORTED
+    H.hswa_pool_destroy(lp)
+
+
 def test_prefill_workspace_sizes():
     """Only FP8 pools need a prefill workspace; an SWA layer stages at most
     ceil((W - 1 + max_q_len) / P) + 1 pages per sequence, a Full layer its

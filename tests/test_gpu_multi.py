@@ -243,3 +243,23 @@ def test_multi_token_decode_window_shorter_than_the_draft(n_tok):
     cached = [0, 5, 60, 63, 64, 200, 1000]
     sc = Scenario(64, 8, 128, 64, 8, wl.DTYPE_BF16, cached, seed=17, extra_tokens=16)
     run_multi_step(sc, n_tok, seed=1700 + n_tok, expect_kernel=FAST)
+
+
+@pytest.mark.gpu
+def test_multi_token_empty_batch_is_a_no_op():
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, [10], seed=18)
+    q = torch.zeros(0, 64, 128, dtype=torch.bfloat16, device="cuda")
+    for n_tok in (2, 8, 16):
+        sc.sess.decode_multi(0, q, q, 0, n_tok, sc.scale)
+    assert sc.sess.check() == 0
+
+
+@pytest.mark.gpu
+def test_multi_token_largest_batch_the_combine_grid_takes():
+    """n_seqs x n_tok up to 65535 rows (the merge kernel's grid rows): 4095
+    short sequences of 16 tokens, oracle on samples (the refusal past the
+    limit is checked without a GPU in test_abi.py)."""
+    rng = np.random.default_rng(19)
+    cached = list(rng.integers(0, 150, 4095))
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=19, extra_tokens=16, chunk=4096)
+    run_multi_step(sc, 16, seed=1900, samples=[0, 1, 2047, 4093, 4094], expect_kernel=FAST)
