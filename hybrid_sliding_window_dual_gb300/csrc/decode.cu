@@ -959,10 +959,16 @@ __global__ void __launch_bounds__(32 * (kConsumers8 + 1)) decode_mma_fp8_d128(co
 //
 // FP8 pools: warps 7-10 convert each E4M3 page into f16 K and V^T tiles
 // (every E4M3 value is an f16 value) and the piece's q tile from bf16 to
-// f16 in place; the MMAs run on f16 operands, the softmax multiplies the
-// scores by the per-key K scale and P by the per-key V scale.
+// f16. With copies (R > 1) q goes into TMEM as f16 pairs (columns 192-255,
+// free with 3 S buffers) and the QK MMAs read it from there as their A
+// operand, which spares the shared memory the q reads of every page; with
+// R = 1, where the softmax bounds the kernel, q stays in shared memory,
+// converted in place (measured: TMEM q is 4-8 % faster up to 8 tokens and
+// 5-7 % slower at 16). The MMAs run on f16 operands; the softmax multiplies
+// the scores by the per-key K scale and P by the per-key V scale.
 constexpr int kTcCols = 512;
 constexpr uint32_t kTmemP = 256, kTmemO = 384;  // column offsets of P and O (S at 0)
+constexpr uint32_t kTmemQ = 192;                // FP8 pools: the q tile, 64 columns of f16 pairs
 constexpr float kTcRescaleLog2 = 8.0f;          // rescale O only when the max grows by > 2^8
 
 // bf16 pools: page i is ready to score once its stage has landed, which
@@ -973,6 +979,7 @@ struct DecodeTcSmem {
     static constexpr int kSP = kStages;  // S / P buffers
     static constexpr int kQBufs = 2;
     static constexpr bool kTcQ = true;
+    static constexpr bool kQTmem = false;  // QK reads q from shared memory
     static constexpr int kThreads = 224;
     static constexpr uint32_t kQHalfBytes = 128 * 128;  // 128 rows x 64 columns of 16-bit values
     uint8_t k[kStages][kPageHeadBytes];                // [d half][64 keys][128 B], 128-byte swizzle
@@ -1009,6 +1016,7 @@ struct DecodeTc8Smem {
     static constexpr int kSP = kConv;
     static constexpr int kQBufs = 1;
     static constexpr bool kTcQ = true;
+    static constexpr bool kQTmem = true;  // with copies (R > 1) QK reads q from TMEM column kTmemQ
     static constexpr int kConvThreads = 128;  // converter warps 7 ..
     static constexpr int kThreads = 224 + kConvThreads;
     static constexpr uint32_t kQHalfBytes = 128 * 128;
@@ -1018,7 +1026,7 @@ struct DecodeTc8Smem {
     uint8_t kc[kConv][kPageHeadBytes];  // f16 K [d half][64 keys][128 B], 128-byte swizzle
     uint8_t vc[kConv][kD * 128];        // f16 V^T [128 d][64 keys = 128 B], 128-byte swizzle
     float ks[kStages][kP], vs[kStages][kP];
-    float ksc[kConv][kP], vsc[kConv][kP];
+    float ksc[kConv][kP], vsc[kConv][kP];  // ksc: the K scale times scale log2 e
     float obuf[kD][32];
     float ep_m[128], ep_l[128];
     StageDesc desc[kStages];
@@ -1039,6 +1047,9 @@ struct DecodeTc8Smem {
     __device__ uint32_t k_addr(int64_t i) { return smem_u32(kc[i % kConv]); }
     __device__ uint32_t v_addr(int64_t i) { return smem_u32(vc[i % kConv]); }
 };
+static_assert(offsetof(DecodeTc8Smem, ksc) % 16 == 0 && offsetof(DecodeTc8Smem, vsc) % 16 == 0,
+              "the softmax reads the scales 4 at a time");
+static_assert(DecodeTc8Smem::kSP * 64 <= (int)kTmemQ && kTmemQ + 64 <= kTmemP, "q sits between S and P in TMEM");
 static_assert(offsetof(DecodeTc8Smem, q) % 1024 == 0 && offsetof(DecodeTc8Smem, kc) % 1024 == 0 &&
                   offsetof(DecodeTc8Smem, vc) % 1024 == 0,
               "128-byte swizzled tiles need 1024-byte alignment");
@@ -1050,7 +1061,8 @@ constexpr size_t decode_tc_smem_bytes() { return sizeof(Smem) + 1024; }
 // each waiting only on its own barriers:
 //   warp 5, lane 0: QK(i) into S buffer i % kSP once page i is ready (and,
 //     on a piece's first page, its q tile); commits s_full, and q_empty after
-//     the last QK of a piece;
+//     the last QK of a piece (the q tile, in shared memory or TMEM, is then
+//     free for the next piece);
 //   warp 6, lane 0: PV(i) once P(i) is in TMEM; commits pv_done(i) (the
 //     bf16 stage, or the FP8 pool's f16 buffer: K was read by QK(i) before
 //     P(i) existed).
@@ -1059,7 +1071,7 @@ constexpr size_t decode_tc_smem_bytes() { return sizeof(Smem) + 1024; }
 // i - kSP, are done, so S and P buffer i % kSP are free. The s_full and
 // p_full barriers are per buffer: each is at most one phase ahead of a
 // waiter for the same reason.
-template <class Smem>
+template <bool kQT, class Smem>
 __device__ bool decode_tc_qk(Smem &sm, const DecodeArgs &a, int64_t n) {
     constexpr int kSP = Smem::kSP, kQB = Smem::kQBufs;
     constexpr uint32_t kIdQK = idesc_16(128, kP, false, Smem::kFP8);
@@ -1076,11 +1088,15 @@ __device__ bool decode_tc_qk(Smem &sm, const DecodeArgs &a, int64_t n) {
         tc_fence_after();
         if (!(flags & kSkip)) {
             const uint32_t q = qb + (pc % kQB) * 2 * Smem::kQHalfBytes, k = sm.k_addr(i);
+            const uint32_t ts = tb + 64 * (uint32_t)(i % kSP);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tb + 64 * (uint32_t)(i % kSP),
-                       sdesc(q + (kk >> 2) * Smem::kQHalfBytes + (kk & 3) * 32, 16, 1024),
-                       sdesc(k + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024), kIdQK, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t kd = sdesc(k + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+                if constexpr (kQT)  // d 16 kk .. 16 kk + 15 are columns 8 kk .. 8 kk + 7
+                    mma_ts(ts, tb + kTmemQ + 8 * kk, kd, kIdQK, kk > 0);
+                else
+                    mma_ss(ts, sdesc(q + (kk >> 2) * Smem::kQHalfBytes + (kk & 3) * 32, 16, 1024), kd, kIdQK, kk > 0);
+            }
         }
         mma_commit(&sm.s_full[i % kSP]);
         if (flags & kLast) mma_commit(&sm.q_empty[pc % kQB]);
@@ -1119,9 +1135,9 @@ __device__ bool decode_tc_pv(Smem &sm, const DecodeArgs &a, int64_t n) {
 
 // Run one issuer role, then make sure every MMA it issued has completed
 // before TMEM is freed.
-template <bool kQK, class Smem>
+template <bool kQK, bool kQT, class Smem>
 __device__ void decode_tc_issue(Smem &sm, const DecodeArgs &a, int64_t n) {
-    bool ok = kQK ? decode_tc_qk(sm, a, n) : decode_tc_pv(sm, a, n);
+    bool ok = kQK ? decode_tc_qk<kQT>(sm, a, n) : decode_tc_pv(sm, a, n);
     mma_commit(&sm.mma_done[kQK ? 0 : 1]);
     if (!mbar_wait(&sm.mma_done[kQK ? 0 : 1], 0, a.err)) ok = false;
     if (!ok) sm.abort = 1;
@@ -1204,10 +1220,21 @@ __device__ void decode_tc_softmax(Smem &sm, const DecodeArgs &a, int64_t n) {
             tc_fence_after();
             uint32_t sr[kK];
             tmem_ld_s<kK>(sm.tmem_base + lane_off + 64 * b + c * kK, sr);
-            if constexpr (Smem::kFP8) {  // the K codes entered the MMA as their exact values
-                const float *ks = sm.ksc[i % Smem::kConv] + c * kK;
+            if constexpr (Smem::kFP8) {
+                // the K codes entered the MMA as their exact values: a score
+                // in log2 units is S times the key's scale times scale log2 e,
+                // a product the converter stored per key
+                const float4 *ks = reinterpret_cast<const float4 *>(sm.ksc[i % Smem::kConv] + c * kK);
 #pragma unroll
-                for (int x = 0; x < kK; ++x) sr[x] = __float_as_uint(__uint_as_float(sr[x]) * ks[x]);
+                for (int x = 0; x < kK / 4; ++x) {
+                    const float4 k4 = ks[x];
+                    const float2 lo = __fmul2_rn(make_float2(__uint_as_float(sr[4 * x]), __uint_as_float(sr[4 * x + 1])),
+                                                 make_float2(k4.x, k4.y));
+                    const float2 hi = __fmul2_rn(
+                        make_float2(__uint_as_float(sr[4 * x + 2]), __uint_as_float(sr[4 * x + 3])), make_float2(k4.z, k4.w));
+                    sr[4 * x] = __float_as_uint(lo.x), sr[4 * x + 1] = __float_as_uint(lo.y);
+                    sr[4 * x + 2] = __float_as_uint(hi.x), sr[4 * x + 3] = __float_as_uint(hi.y);
+                }
             }
             // keys of the page this row's token sees, relative to the copy's
             // first key: [lo_c, hi_c) (position t = len - n_tok + w; W keys
@@ -1229,7 +1256,7 @@ __device__ void decode_tc_softmax(Smem &sm, const DecodeArgs &a, int64_t n) {
                 m0 = max3(m0, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
                 m1 = max3(m1, __uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3]));
             }
-            const float mx = fmaxf(m0, m1) * a.scale_log2;
+            const float mx = Smem::kFP8 ? fmaxf(m0, m1) : fmaxf(m0, m1) * a.scale_log2;
             const bool need = mx > m_used + kTcRescaleLog2;
             const bool resc = need && m_used != -INFINITY;
             const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
@@ -1240,13 +1267,14 @@ __device__ void decode_tc_softmax(Smem &sm, const DecodeArgs &a, int64_t n) {
             uint32_t pk[kK / 2];
 #pragma unroll
             for (int x = 0; x < kK / 2; ++x) {
-                const float2 y = __ffma2_rn(make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])),
-                                            sc2, nm2);
+                const float2 sx = make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1]));
+                const float2 y = Smem::kFP8 ? __fadd2_rn(sx, nm2) : __ffma2_rn(sx, sc2, nm2);
                 const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
                 sum2 = __fadd2_rn(sum2, p);
                 if constexpr (Smem::kFP8) {  // P carries the V scale: V codes enter the MMA as they are
-                    const float *vs = sm.vsc[i % Smem::kConv] + c * kK;
-                    pk[x] = pack_f16(p.x * vs[2 * x], p.y * vs[2 * x + 1]);
+                    const float4 v4 = reinterpret_cast<const float4 *>(sm.vsc[i % Smem::kConv] + c * kK)[x >> 1];
+                    const float2 pv = __fmul2_rn(p, (x & 1) ? make_float2(v4.z, v4.w) : make_float2(v4.x, v4.y));
+                    pk[x] = pack_f16(pv.x, pv.y);
                 } else {
                     pk[x] = pack_bf16(p.x, p.y);
                 }
@@ -1410,12 +1438,20 @@ __device__ __forceinline__ void e4m3x16_to_f16(uint4 c, uint4 &lo, uint4 &hi) {
 // becomes [d half][64 keys][128 B] and V^T [128 d][64 B] becomes
 // [128 d][128 B], both with the 128-byte swizzle; the scales and the
 // stage's descriptor are copied along.
-// On a piece's first page the piece's q tile is turned into f16 in place
-// first. Then the stage is released to the producer.
+// On a piece's first page the piece's q tile is converted first: with kQT
+// into TMEM, where thread (warp w, lane l) writes tile row 32 (w mod 4) + l,
+// the lanes its warp may reach, as 64 columns of f16 pairs (the producer
+// loads that q tile only after the last QK of the previous piece, q_empty,
+// so the TMEM columns are free by the time it lands); else in place in
+// shared memory. Then the stage is released to the producer.
+template <bool kQT>
 __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_t n) {
     constexpr int kStages = DecodeTc8Smem::kStages, kConv = DecodeTc8Smem::kConv, kQB = DecodeTc8Smem::kQBufs;
     constexpr int kCT = DecodeTc8Smem::kConvThreads, kPer = 512 / kCT;  // 16-byte chunks per thread and tile
+    constexpr uint32_t kQH = DecodeTc8Smem::kQHalfBytes;
     const int t = threadIdx.x - 7 * 32;  // 0 .. kCT - 1
+    const int quad = (threadIdx.x >> 5) & 3, row = 32 * quad + (threadIdx.x & 31);
+    const uint32_t t_q = sm.tmem_base + ((uint32_t)(32 * quad) << 16) + kTmemQ;
     int32_t pc = -1;
     bool ok = true;
     for (int64_t i = 0; i < n && ok; ++i) {
@@ -1427,15 +1463,32 @@ __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_
         if (ok && (d.flags & kFirst)) {
             ++pc;
             ok = mbar_wait(&sm.q_full[pc % kQB], (uint32_t)(pc / kQB) & 1, a.err);
-            if (ok) {
-                uint4 *q = reinterpret_cast<uint4 *>(sm.q[pc % kQB]);
-#pragma unroll 4
-                for (int x = t; x < 2 * (int)DecodeTc8Smem::kQHalfBytes / 16; x += kCT) q[x] = bf16x8_to_f16x8(q[x]);
-                fence_proxy_async_shared();
-                mbar_arrive(&sm.q_conv[pc % kQB]);
-            }
         }
+        // the TMEM stores below are warp-wide: the warp goes on or stops as one
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        if ((d.flags & kFirst) && !kQT) {  // f16 in place, for QK from shared memory
+            uint4 *q = reinterpret_cast<uint4 *>(sm.q[pc % kQB]);
+#pragma unroll 4
+            for (int x = t; x < 2 * (int)DecodeTc8Smem::kQHalfBytes / 16; x += kCT) q[x] = bf16x8_to_f16x8(q[x]);
+            fence_proxy_async_shared();
+            mbar_arrive(&sm.q_conv[pc % kQB]);
+        } else if (d.flags & kFirst) {  // f16 pairs into TMEM
+            const uint8_t *q = sm.q[pc % kQB] + row * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // d half h: columns 32 h .. 32 h + 31
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 f = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(q + h * kQH + ((c ^ (row & 7)) << 4)));
+                    w[4 * c] = f.x, w[4 * c + 1] = f.y, w[4 * c + 2] = f.z, w[4 * c + 3] = f.w;
+                }
+                tmem_st32(t_q + 32 * h, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm.q_conv[pc % kQB]);
+        }
         if (!(d.flags & kSkip)) {
             const uint8_t *k8 = sm.k[st], *v8 = sm.v[st];
             uint8_t *kc = sm.kc[b], *vc = sm.vc[b];
@@ -1467,7 +1520,7 @@ __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_
             }
         }
         if (t < kP)
-            sm.ksc[b][t] = sm.ks[st][t];
+            sm.ksc[b][t] = sm.ks[st][t] * a.scale_log2;
         else if (t < 2 * kP)
             sm.vsc[b][t - kP] = sm.vs[st][t - kP];
         if (t == 0) sm.descc[b] = d;
@@ -1527,13 +1580,13 @@ __global__ void __launch_bounds__(Smem::kThreads, 1)
     } else if (warp < 7) {
         if ((threadIdx.x & 31) == 0) {
             if (warp == 5)
-                decode_tc_issue<true>(sm, a, u1 - u0);
+                decode_tc_issue<true, Smem::kQTmem && (kR > 1)>(sm, a, u1 - u0);
             else
-                decode_tc_issue<false>(sm, a, u1 - u0);
+                decode_tc_issue<false, false>(sm, a, u1 - u0);
         }
         __syncwarp();
     } else if constexpr (Smem::kFP8) {
-        decode_tc_convert(sm, a, u1 - u0);
+        decode_tc_convert<Smem::kQTmem && (kR > 1)>(sm, a, u1 - u0);
     }
     tc_fence_before();
     __syncthreads();
