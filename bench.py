@@ -582,7 +582,8 @@ def measure_prefill(steps, warmup, w, fp8=False):
     full_ms = float(np.mean([a.elapsed_time(b) for a, b in pb.events[0]]))
     swa_ms = float(np.mean([a.elapsed_time(b) for a, b in pb.events[1]]))
     pb.finish()
-    return {"step_tflops": f["step"] * steps / secs / 1e12, "ms_per_step": secs / steps * 1e3,
+    from hybrid_sliding_window_dual_gb300 import hswa_last_kernel
+    return {"kernel": hswa_last_kernel(), "step_tflops": f["step"] * steps / secs / 1e12, "ms_per_step": secs / steps * 1e3,
             "full_tflops": f["full"] / (full_ms / 1e3) / 1e12, "full_ms": full_ms,
             "swa_tflops": f["swa"] / (swa_ms / 1e3) / 1e12, "swa_ms": swa_ms,
             "valid_tflop_per_step": f["step"] / 1e12, "tokens_per_s": pb.T * steps / secs,
@@ -1029,7 +1030,7 @@ def run_decode(args, world, rank, local):
             "swa_layer_tflops": round(pf["swa_tflops"], 2), "swa_layer_ms": round(pf["swa_ms"], 3),
             "valid_tflop_per_step": round(pf["valid_tflop_per_step"], 3),
             "ms_per_step": round(pf["ms_per_step"], 3), "tokens_per_s": round(pf["tokens_per_s"], 1),
-            "kernel": "prefill_tc_bf16_d128"}
+            "kernel": pf["kernel"]}
         if not args.no_fp8:
             del pf
             torch.cuda.empty_cache()
@@ -1039,7 +1040,7 @@ def run_decode(args, world, rank, local):
                 "tflops": round(p8["step_tflops"], 1), "frac": round(p8["step_tflops"] / bf16_sus, 4),
                 "full_layer_tflops": round(p8["full_tflops"], 1), "full_layer_ms": round(p8["full_ms"], 3),
                 "swa_layer_ms": round(p8["swa_ms"], 3), "ms_per_step": round(p8["ms_per_step"], 3),
-                "kernel": "prefill_stage_fp8 + prefill_q_to_f16 + prefill_tc_bf16_d128<f16> (staging inside the layer time)"}
+                "kernel": p8["kernel"].replace("+", " + prefill_q_to_f16 + ") + " (staging inside the layer time)"}
     if not args.no_hybrid70:
         h = measure_hybrid70(args.hybrid_steps, 2)
         line["hybrid70"] = {
@@ -1388,7 +1389,7 @@ def run_prefill_line(args, world, rank, local):
                    "l2": "inputs larger than L2", "flops": "4 d Hq per valid (query, key) pair"},
         "roofline": {"bound": "tensor", "achieved": round(pf["full_tflops"], 1), "peak": bf16_sus,
                      "unit": "TFLOP/s", "frac": round(pf["full_tflops"] / bf16_sus, 4), "traffic": None,
-                     "kernel": "prefill_tc_bf16_d128 (Full layer)", "peak_source": kind + " sustained",
+                     "kernel": pf["kernel"] + " (Full layer)", "peak_source": kind + " sustained",
                      "frac_of_burst": round(pf["full_tflops"] / bf16, 4)},
         "swa_layer_tflops": round(pf["swa_tflops"], 2),
         "gpu_launches": 4 * args.steps,

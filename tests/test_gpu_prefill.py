@@ -108,6 +108,17 @@ def test_prefill_fast_path_dispatch_and_window_wider_than_chunk():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (24, 4), (32, 8), (48, 4)])
+def test_prefill_query_heads_per_kv_head(hq, hkv):
+    """2, 6, 4 and 12 query heads per kv head: a CTA takes a pair of query
+    heads of one kv head, so every even group size runs on the tensor-core
+    kernel. Ragged chunks and prefixes, Full and SWA layer."""
+    cached = [0, 70, 1000, 129]
+    sc = Scenario(hq, hkv, 128, 64, 128, wl.DTYPE_BF16, cached, seed=17, extra_tokens=600)
+    run_prefill_chunk(sc, [300, 1, 513, 129], seed=6, expect_kernel="prefill_tc_bf16_d128")
+
+
+@pytest.mark.gpu
 def test_chunked_prefill_full_size_sampled():
     """8 sequences, cached prefix uniform in [8192, 65536], 4096-token chunk,
     64/8 heads, d 128, page 64: the chunked-prefill workload in the launch
