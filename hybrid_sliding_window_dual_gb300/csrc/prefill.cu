@@ -263,7 +263,9 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
         const bool masked = (k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1);
         const int32_t hi_c = t - k0;                       // keys c <= hi_c
         const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;  // keys c >= lo_c
-        float m0 = -INFINITY, m1 = -INFINITY;
+        // one max per chunk, each a chain of 8: short dependency chains for a
+        // thread that has few warps beside it to hide them
+        float mc[4];
         tmem_ld32(t_s, sr[0]);
         tmem_wait_ld(sr[0]);
 #pragma unroll
@@ -277,14 +279,16 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
                     if (col > hi_c || col < lo_c) sr[c][i] = __float_as_uint(-INFINITY);
                 }
             }
+            float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 m0 = max3(m0, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
                 m1 = max3(m1, __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
             }
+            mc[c] = fmaxf(m0, m1);
             if (c + 1 < 4) tmem_wait_ld(sr[c + 1]);
         }
-        const float mx = fmaxf(m0, m1) * a.scale_log2;
+        const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * a.scale_log2;
         // A new reference max only when the row max grows by more than 2^8;
         // then O (nothing before the first PV) and l are rescaled.
         const bool need = mx > m_used + kRescaleLog2;
@@ -293,9 +297,11 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
         if (need) m_used = mx;
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
         const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
-        float2 sum2 = make_float2(0.f, 0.f);
+        float2 sums[4];  // one running sum per chunk (chains of 16, not 64)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+            float2 &sum2 = sums[c];
+            sum2 = make_float2(0.f, 0.f);
             // P = 2^(s * scale - m) two keys at a time (packed f32x2 FMA and
             // add), packed to bf16 pairs in place, then its 16 columns (32
             // keys) written over the start of S
@@ -323,6 +329,8 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
                 tmem_st32(t_o + 32 * c, ov);
             }
         }
+        const float2 s01 = __fadd2_rn(sums[0], sums[1]), s23 = __fadd2_rn(sums[2], sums[3]);
+        const float2 sum2 = __fadd2_rn(s01, s23);
         l = l * alpha + (sum2.x + sum2.y);
         tmem_wait_st();
         tc_fence_before();
