@@ -227,7 +227,7 @@ __device__ __forceinline__ uint32_t swz(int row, int d) {
 
 // Streams the pages of units [u0, u1) into the stage ring. With
 // Smem::kTcQ the query tile of each piece goes by tensor map tq into the
-// two-slot q buffer (released by the MMA thread through q_empty) instead of
+// q buffer of Smem::kQBufs slots (released by the MMA thread through q_empty) instead of
 // travelling in the stage of the piece's first page.
 template <bool kFP8, class Smem>
 __device__ void decode_producer(Smem &sm, const CUtensorMap *tk, const CUtensorMap *tv, const DecodeArgs &a,
@@ -1007,7 +1007,7 @@ static_assert(offsetof(DecodeTcSmem, v) % 1024 == 0 && offsetof(DecodeTcSmem, q)
               "128-byte swizzled tiles need 1024-byte alignment");
 
 // FP8 pools: E4M3 pages land in 4 stages; the converter warps turn page i
-// into f16 buffer i % 2 once PV(i - 2) has emptied it, so page i is ready
+// into f16 buffer i % 3 once PV(i - 3) has emptied it, so page i is ready
 // to score when its conversion is done.
 struct DecodeTc8Smem {
     static constexpr bool kFP8 = true;
