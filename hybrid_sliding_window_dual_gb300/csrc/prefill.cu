@@ -159,14 +159,17 @@ __device__ void prefill_producer(PrefillSmem &sm, const CUtensorMap *tq, const C
 }
 
 // S_x = Q_x K^T over d = 128: 8 steps of K = 16 (32 bytes inside a 128-byte
-// swizzle row; the second half of d is the second 16 KB block).
+// swizzle row; the second half of d is the second 16 KB block). qd and kd
+// are the descriptors of the tiles' first bytes: a step's descriptor is that
+// plus its byte offset / 16 in the address field (no carry: shared-memory
+// addresses stay below 2^18).
 template <bool kF16>
-__device__ __forceinline__ void issue_s(uint32_t t_s, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_s(uint32_t t_s, uint64_t qd, uint64_t kd) {
     constexpr uint32_t kIdescQK = idesc_16(kBM, kBN, false, kF16);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-        mma_ss(t_s, sdesc(q_addr + off, 16, 1024), sdesc(k_addr + off, 16, 1024), kIdescQK, kk > 0);
+        const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+        mma_ss(t_s, qd + off16, kd + off16, kIdescQK, kk > 0);
     }
 }
 
@@ -174,19 +177,18 @@ __device__ __forceinline__ void issue_s(uint32_t t_s, uint32_t q_addr, uint32_t 
 // the first 64 columns of S_x, V is MN-major (d contiguous) with the two
 // 64-column halves 16 KB apart.
 template <bool kF16>
-__device__ __forceinline__ void issue_pv(uint32_t t_o, uint32_t t_p, uint32_t v_addr, bool first_tile) {
+__device__ __forceinline__ void issue_pv(uint32_t t_o, uint32_t t_p, uint64_t vd, bool first_tile) {
     constexpr uint32_t kIdescPV = idesc_16(kBM, kD, true, kF16);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        mma_ts(t_o, t_p + kk * 8, sdesc(v_addr + kk * 2048, kHalfBytes, 1024), kIdescPV,
-               (first_tile && kk == 0) ? 0u : 1u);
+        mma_ts(t_o, t_p + kk * 8, vd + kk * (2048 >> 4), kIdescPV, (first_tile && kk == 0) ? 0u : 1u);
 }
 
 template <bool kF16>
 __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u) {
     const uint32_t tbase = sm.tmem_base;
     const uint32_t ts0 = tbase, ts1 = tbase + 128, to0 = tbase + 256, to1 = tbase + 384;
-    const uint32_t qa0 = smem_u32(sm.q[0]), qa1 = smem_u32(sm.q[1]);
+    const uint64_t qd0 = sdesc(smem_u32(sm.q[0]), 16, 1024), qd1 = sdesc(smem_u32(sm.q[1]), 16, 1024);
     bool ok = mbar_wait(&sm.q_full, 0, a.err);
     tc_fence_after();
     const int n = u.n_tiles;
@@ -194,10 +196,10 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
         ok = mbar_wait(&sm.kv_full[0], 0, a.err);  // K(0)
         if (ok) {
             tc_fence_after();
-            const uint32_t k0 = smem_u32(sm.kv[0]);
-            issue_s<kF16>(ts0, qa0, k0);
+            const uint64_t k0 = sdesc(smem_u32(sm.kv[0]), 16, 1024);
+            issue_s<kF16>(ts0, qd0, k0);
             mma_commit(&sm.s_full[0]);
-            issue_s<kF16>(ts1, qa1, k0);
+            issue_s<kF16>(ts1, qd1, k0);
             mma_commit(&sm.s_full[1]);
             mma_commit(&sm.kv_empty[0]);
         }
@@ -208,25 +210,25 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
                  !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
-            const uint32_t v_addr = smem_u32(sm.kv[sv]);
-            issue_pv<kF16>(to0, ts0, v_addr, j == 0);
+            const uint64_t vd = sdesc(smem_u32(sm.kv[sv]), kHalfBytes, 1024);
+            issue_pv<kF16>(to0, ts0, vd, j == 0);
             const bool more = j + 1 < n;
-            uint32_t k_addr = 0;
+            uint64_t kd = 0;
             if (more) {
                 ok = mbar_wait(&sm.kv_full[sk], (ik / kSlots) & 1, a.err);
                 if (!ok) break;
                 tc_fence_after();
-                k_addr = smem_u32(sm.kv[sk]);
-                issue_s<kF16>(ts0, qa0, k_addr);
+                kd = sdesc(smem_u32(sm.kv[sk]), 16, 1024);
+                issue_s<kF16>(ts0, qd0, kd);
                 mma_commit(&sm.s_full[0]);
             }
             ok = mbar_wait(&sm.p_full[1], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
-            issue_pv<kF16>(to1, ts1, v_addr, j == 0);
+            issue_pv<kF16>(to1, ts1, vd, j == 0);
             mma_commit(&sm.kv_empty[sv]);
             if (more) {
-                issue_s<kF16>(ts1, qa1, k_addr);
+                issue_s<kF16>(ts1, qd1, kd);
                 mma_commit(&sm.s_full[1]);
                 mma_commit(&sm.kv_empty[sk]);
             }
