@@ -45,7 +45,7 @@ KV_ROW = {wl.DTYPE_BF16: 2, wl.DTYPE_F32: 4}
 # one ncu capture at full size (profiles/decode_mma_bf16_d128_decode_batch_traffic.md),
 # valid only for the kernel sources it was taken on.
 DECODE_TRAFFIC = {"ratio": 1.0030, "sources": ("decode.cu", "common.cuh"),
-                  "sha256": "54ef9d58835deab02fa5d48eaaf3115bf9aa1d38425c6094f6af97d87d2c1cda"}
+                  "sha256": "3889ce10a8d9e47a729182c008ce69e81e6a4c887591df0fa7b71c4bf39143d2"}
 
 
 def source_digest(names):

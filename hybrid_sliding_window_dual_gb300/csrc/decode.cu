@@ -1087,15 +1087,19 @@ __device__ bool decode_tc_qk(Smem &sm, const DecodeArgs &a, int64_t n) {
         if (*(volatile int32_t *)&sm.abort) return false;
         tc_fence_after();
         if (!(flags & kSkip)) {
-            const uint32_t q = qb + (pc % kQB) * 2 * Smem::kQHalfBytes, k = sm.k_addr(i);
+            // descriptors of the tiles' first bytes; a step adds its byte
+            // offset / 16 to the address field (shared memory < 2^18 bytes:
+            // no carry out of it)
+            const uint64_t qd = sdesc(qb + (pc % kQB) * 2 * Smem::kQHalfBytes, 16, 1024);
+            const uint64_t kd = sdesc(sm.k_addr(i), 16, 1024);
             const uint32_t ts = tb + 64 * (uint32_t)(i % kSP);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t kd = sdesc(k + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+                const uint32_t koff = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
                 if constexpr (kQT)  // d 16 kk .. 16 kk + 15 are columns 8 kk .. 8 kk + 7
-                    mma_ts(ts, tb + kTmemQ + 8 * kk, kd, kIdQK, kk > 0);
+                    mma_ts(ts, tb + kTmemQ + 8 * kk, kd + koff, kIdQK, kk > 0);
                 else
-                    mma_ss(ts, sdesc(q + (kk >> 2) * Smem::kQHalfBytes + (kk & 3) * 32, 16, 1024), kd, kIdQK, kk > 0);
+                    mma_ss(ts, qd + (((kk >> 2) * Smem::kQHalfBytes + (kk & 3) * 32) >> 4), kd + koff, kIdQK, kk > 0);
             }
         }
         mma_commit(&sm.s_full[i % kSP]);
@@ -1121,11 +1125,11 @@ __device__ bool decode_tc_pv(Smem &sm, const DecodeArgs &a, int64_t n) {
         tc_fence_after();
         if (!(flags & kSkip)) {
             const uint32_t tp = tb + kTmemP + 32 * b, v = sm.v_addr(i);
+            const uint64_t vd = Smem::kFP8 ? sdesc(v, 16, 1024) : sdesc(v, kBoxBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t vd = Smem::kFP8 ? sdesc(v + kk * 32, 16, 1024) : sdesc(v + kk * 2048, kBoxBytes, 1024);
-                mma_ts(tb + kTmemO, tp + kk * 8, vd, kIdPV, (fresh && kk == 0) ? 0u : 1u);
-            }
+            for (int kk = 0; kk < 4; ++kk)  // 16 keys a step: 32 bytes on (FP8 V^T rows) or 16 rows of 128 B
+                mma_ts(tb + kTmemO, tp + kk * 8, vd + (Smem::kFP8 ? kk * (32 >> 4) : kk * (2048 >> 4)), kIdPV,
+                       (fresh && kk == 0) ? 0u : 1u);
             fresh = false;
         }
         mma_commit(sm.pv_done(i));
