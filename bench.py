@@ -82,7 +82,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+        # raw samples (the JSON line carries their summary); HSWA_CLOCKS_DIR picks the folder
+        out = os.environ.get("HSWA_CLOCKS_DIR") or os.path.join(ROOT, "bench_out")
+        self.path = os.path.join(out, "clocks_rank%d.csv" % gpu_index)
 
     def start(self):
         try:
