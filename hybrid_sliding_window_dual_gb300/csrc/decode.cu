@@ -1512,11 +1512,17 @@ __device__ void decode_tc_convert(DecodeTc8Smem &sm, const DecodeArgs &a, int64_
                 const int x = t + kCT * e;
                 const int r = x >> 3, c8 = x & 7, dd = x >> 2, c4 = x & 3;
                 uint4 lo, hi;
-                e4m3x16_to_f16(kin[e], lo, hi);
+                // K: chunks j0 and j0 + 1 of the row in d half c8 / 4. The eight
+                // threads of a quarter warp share the row; the four in the
+                // second d half (8 KB on: the same banks) store the upper chunk
+                // first, so each store instruction meets 8 distinct chunks
+                const bool sw = (c8 & 4) != 0;
+                const uint4 kq = sw ? make_uint4(kin[e].z, kin[e].w, kin[e].x, kin[e].y) : kin[e];
+                e4m3x16_to_f16(kq, lo, hi);
                 uint8_t *krow = kc + (c8 >> 2) * kBoxBytes + r * 128;
-                const int j0 = 2 * (c8 & 3);
+                const int j0 = 2 * (c8 & 3) + (sw ? 1 : 0), j1 = j0 ^ 1;
                 *reinterpret_cast<uint4 *>(krow + ((j0 ^ (r & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4 *>(krow + (((j0 + 1) ^ (r & 7)) << 4)) = hi;
+                *reinterpret_cast<uint4 *>(krow + ((j1 ^ (r & 7)) << 4)) = hi;
                 e4m3x16_to_f16(vin[e], lo, hi);
                 uint8_t *vrow = vc + dd * 128;
                 *reinterpret_cast<uint4 *>(vrow + (((2 * c4) ^ (dd & 7)) << 4)) = lo;
