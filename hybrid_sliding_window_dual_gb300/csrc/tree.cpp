@@ -102,16 +102,41 @@ void reindex(hswa_tree *t, const TreeNode *nd) {
     if (nd->swa >= 0) t->swa_nodes.insert(SwaKey(in_window(t, nd) ? 1 : 0, nd->last, nd->id));
 }
 
-// Recompute the shallowest-leaf depth from nd up to the root, stopping where
-// it no longer changes.
-void update_dmin_up(hswa_tree *t, TreeNode *nd) {
+constexpr int64_t kNoLeaf = INT64_MAX;
+
+// One child of nd went from shallowest-leaf depth a to b (a = kNoLeaf: the
+// child is new; b = kNoLeaf: it was removed). Update the depths from nd up
+// to the root, stopping where they no longer change. A node's children are
+// scanned only when the changed child held its minimum and got deeper or
+// went; otherwise the new minimum follows from the old one (a prompt shared
+// by many requests has many children).
+void update_dmin_up(hswa_tree *t, TreeNode *nd, int64_t a, int64_t b) {
     for (; nd && nd != &t->root; nd = nd->parent) {
-        int64_t d = nd->children.empty() ? (int64_t)nd->index + 1 : INT64_MAX;
-        for (auto &ch : nd->children) d = std::min(d, ch.second->dmin);
-        if (d == nd->dmin) return;
-        unindex(t, nd);
+        const int64_t D = nd->dmin;
+        int64_t d;
+        if (nd->children.empty()) {
+            d = (int64_t)nd->index + 1;  // a leaf now
+        } else if (a == kNoLeaf && nd->children.size() == 1) {
+            d = b;  // a leaf until this child came
+        } else if (b <= D) {
+            d = b;  // the changed child is (one of) the shallowest
+        } else if (a > D) {
+            d = D;  // the changed child did not hold the minimum
+        } else {
+            d = kNoLeaf;
+            for (auto &ch : nd->children) d = std::min(d, ch.second->dmin);
+        }
+        if (d == D) return;
+        // the leaf-set key (last, id) holds no depth; the SWA-node key moves
+        // only if the node's window side flips (near the leaf it is over)
+        const bool was_in = in_window(t, nd);
         nd->dmin = d;
-        reindex(t, nd);
+        if (nd->swa >= 0 && in_window(t, nd) != was_in) {
+            t->swa_nodes.erase(SwaKey(was_in ? 1 : 0, nd->last, nd->id));
+            t->swa_nodes.insert(SwaKey(was_in ? 0 : 1, nd->last, nd->id));
+        }
+        a = D;
+        b = d;
     }
 }
 
@@ -141,6 +166,7 @@ void remove_leaf(hswa_tree *t, TreeNode *nd) {
     unindex(t, nd);
     if (nd->swa >= 0) --t->n_swa;
     TreeNode *parent = nd->parent;
+    const int64_t gone = nd->dmin;
     if (parent != &t->root) unindex(t, parent);
     auto range = parent->children.equal_range(nd->hash);
     for (auto it = range.first; it != range.second; ++it)
@@ -152,7 +178,7 @@ void remove_leaf(hswa_tree *t, TreeNode *nd) {
     delete nd;
     if (parent != &t->root) {
         reindex(t, parent);  // a leaf now, if that was its last child
-        update_dmin_up(t, parent);
+        update_dmin_up(t, parent, gone, kNoLeaf);
     }
 }
 
@@ -223,7 +249,7 @@ extern "C" int hswa_tree_insert(hswa_tree *t, int32_t seq_id, const int32_t *tok
         if (frow[p] < 0) return HSWA_ERR_INVALID_ARG;
     const uint64_t clock = ++t->clock;
     TreeNode *node = &t->root;
-    bool grew = false;
+    TreeNode *attach = nullptr;  // the existing node the new chain hangs from
     int32_t created = 0;
     for (int64_t p = 0; p < n_pages; ++p) {
         const int32_t *pt = tokens + p * P;
@@ -239,7 +265,7 @@ extern "C" int hswa_tree_insert(hswa_tree *t, int32_t seq_id, const int32_t *tok
             nxt->tokens.assign(pt, pt + P);
             nxt->hash = h;
             nxt->last = clock;
-            nxt->dmin = p + 1;
+            nxt->dmin = n_pages;  // new nodes form one chain down to the leaf at page n_pages - 1
             pool->ref_full(nxt->full);
             if (nxt->swa >= 0) {
                 pool->ref_swa(nxt->swa);
@@ -250,7 +276,7 @@ extern "C" int hswa_tree_insert(hswa_tree *t, int32_t seq_id, const int32_t *tok
             if (node != &t->root) reindex(t, node);
             reindex(t, nxt);
             t->nodes.emplace(nxt->id, nxt);
-            grew = true;
+            if (!created) attach = node;
             ++created;
         } else {
             if (nxt->swa < 0 && srow[p] >= 0) {  // the sequence recomputed a lost window page
@@ -264,18 +290,9 @@ extern "C" int hswa_tree_insert(hswa_tree *t, int32_t seq_id, const int32_t *tok
         }
         node = nxt;
     }
-    // the new nodes form one chain ending at a leaf (each started with its
-    // own depth): recompute the depths bottom up along the whole path
-    if (grew)
-        for (TreeNode *nd = node; nd != &t->root; nd = nd->parent) {
-            int64_t d = nd->children.empty() ? (int64_t)nd->index + 1 : INT64_MAX;
-            for (auto &ch : nd->children) d = std::min(d, ch.second->dmin);
-            if (d != nd->dmin) {
-                unindex(t, nd);
-                nd->dmin = d;
-                reindex(t, nd);
-            }
-        }
+    // the node the chain hangs from gained a child whose shallowest leaf is
+    // n_pages deep
+    if (created) update_dmin_up(t, attach, kNoLeaf, n_pages);
     if (n_new_out) *n_new_out = created;
     return HSWA_OK;
 }
