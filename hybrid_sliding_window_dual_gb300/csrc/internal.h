@@ -37,6 +37,9 @@ struct hswa_pool {
     PageQueue full_free, swa_free;
     std::vector<int32_t> full_bt, swa_bt;  // [max_seqs][max_pages_per_seq]
     std::vector<int32_t> seq_len;          // [max_seqs]
+    // per sequence: no logical page below holds an SWA page (set_swa lowers
+    // it, a release raises it), so a release scans only the pages it frees
+    std::vector<int32_t> swa_low;          // [max_seqs]
     // holders of each page (sequence tables and prefix-tree nodes); a page
     // is on its free list exactly when its count is 0
     std::vector<int32_t> full_ref, swa_ref;
@@ -95,6 +98,7 @@ struct hswa_pool {
     void set_swa(int32_t s, int32_t p, int32_t v) {
         int64_t i = (int64_t)s * cfg.max_pages_per_seq + p;
         swa_bt[i] = v;
+        if (v >= 0 && p < swa_low[s]) swa_low[s] = p;
         mark(table_entries() + i);
     }
     void set_len(int32_t s, int32_t v) {

@@ -70,6 +70,7 @@ extern "C" int hswa_pool_create(const hswa_config *cfg, const int32_t *full_free
     p->full_bt.assign(entries, -1);
     p->swa_bt.assign(entries, -1);
     p->seq_len.assign(cfg->max_seqs, 0);
+    p->swa_low.assign(cfg->max_seqs, 0);
     p->full_ref.assign(cfg->full_pages, 0);
     p->swa_ref.assign(cfg->swa_pages, 0);
     p->dirty_flag.assign(2 * entries + cfg->max_seqs, 0);
@@ -135,13 +136,14 @@ extern "C" int hswa_swa_release(hswa_pool *pool, int n, const int32_t *seq_ids, 
     for (int32_t s : ids) {
         const int64_t L = pool->seq_len[s];
         // pages p with (p + 1) * P <= L - W hold only tokens older than the window
-        const int64_t n_old = L - W > 0 ? (L - W) / P : 0;
-        for (int64_t p = 0; p < n_old && p < MP; ++p) {
+        const int64_t n_old = std::min<int64_t>(L - W > 0 ? (L - W) / P : 0, MP);
+        for (int64_t p = pool->swa_low[s]; p < n_old; ++p) {  // pages below hold none
             const int32_t page = pool->swa_bt[s * MP + p];
             if (page < 0) continue;
             freed += pool->unref_swa(page);
             pool->set_swa(s, (int32_t)p, -1);
         }
+        if (n_old > pool->swa_low[s]) pool->swa_low[s] = (int32_t)n_old;
     }
     if (n_freed_out) *n_freed_out = freed;
     return HSWA_OK;
