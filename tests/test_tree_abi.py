@@ -179,3 +179,47 @@ def test_tree_argument_errors_change_nothing():
     H.hswa_seq_free(x.pool, [0])
     x.opool.seq_free([0])
     x.close()
+
+
+def test_depth_updates_on_a_prompt_shared_by_branches():
+    """One prompt shared by branches of different depths, checked against
+    the oracle after every call. Evicting the shallowest branch makes the
+    prompt's shallowest leaf deeper (its children are looked at again); a new
+    shallower branch makes it shallower; a branch that extends a stored leaf
+    turns that leaf into an inner node; SWA evictions in between take pages
+    on both sides of the window as leaves go."""
+    W, P = 8, 4
+    x = Pair(W, P, 400, 400, 4, 40, 7)
+    prompt = list(range(100, 100 + 6 * P))  # 6 pages
+
+    def store(tokens):
+        m, fpages, spages, raw = x.match(tokens)
+        if m:
+            H.hswa_seq_share_prefix(x.pool, 0, fpages, spages)
+            x.opool.share_prefix(0, list(fpages), list(spages))
+        L = m * P
+        while L < len(tokens):
+            n = min(5, len(tokens) - L)
+            assert x.reserve(0, n) is not None
+            assert H.hswa_swa_release(x.pool, [0]) == x.opool.swa_release([0])
+            L += n
+        assert H.hswa_tree_insert(x.tree, 0, tokens) == x.otree.insert(0, tokens)
+        H.hswa_seq_free(x.pool, [0])
+        x.opool.seq_free([0])
+        x.check()
+
+    # branches 1, 3, 5 and 2 pages below the prompt, the shallowest stored first (oldest)
+    for b, k in ((1, 1), (2, 3), (3, 5), (4, 2)):
+        store(prompt + [b] * (P * k))
+    for _ in range(6):  # leaves oldest first: the one-page branch goes first
+        assert H.hswa_tree_evict(x.tree, 1, 0) == x.otree.evict(1, 0)
+        x.check()
+        assert H.hswa_tree_evict(x.tree, 0, 1) == x.otree.evict(0, 1)
+        x.check()
+    store(prompt + [5] * P)                    # shallower than every branch left
+    store(prompt + [4] * (P * 2) + [6] * P)    # extends the two-page branch's leaf
+    for _ in range(30):
+        assert H.hswa_tree_evict(x.tree, 2, 1) == x.otree.evict(2, 1)
+        x.check()
+    assert H.hswa_tree_stats(x.tree)[0] == 0
+    x.close()
