@@ -339,8 +339,10 @@ size_t hswa_decode_multi_workspace_size(const hswa_pool *pool, int n_seqs, int n
  * ws: device workspace of at least hswa_decode_multi_workspace_size bytes.
  * The SWA pages must still hold positions from L - n_tok + 1 - W on: release
  * out-of-window pages before the draft tokens are reserved. Bf16 and FP8
- * pools (an FP8 pool streams its pages once per two tokens); n_tok outside
- * [1, HSWA_DECODE_MAX_TOKENS] gives HSWA_ERR_INVALID_ARG. */
+ * pools; every page is streamed once for all n_tok tokens. n_tok outside
+ * [1, HSWA_DECODE_MAX_TOKENS] gives HSWA_ERR_INVALID_ARG; n_seqs * n_tok
+ * above 65535 (query rows the merge of split pages takes in one launch)
+ * gives HSWA_ERR_UNSUPPORTED. */
 int hswa_decode_multi(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                       const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, int n_tok, float scale,
                       void *ws, size_t ws_bytes, hswa_stream_t stream);
