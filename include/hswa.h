@@ -88,8 +88,8 @@ extern "C" {
  * v_scale [pages][Hkv][P][d / 128] fp32. q, o and the new K/V handed to the
  * append stay bf16; the append quantizes: scale = amax / 448 (1 if amax is
  * 0), code = round-to-nearest-even(x / scale) saturating at 448. Supported
- * by hswa_append_kv, hswa_decode, hswa_decode_append (d = 128, 8 query
- * heads per kv head, P = 64), hswa_prefill_chunk_ws (d = 128, an even
+ * by hswa_append_kv, hswa_decode, hswa_decode_append, hswa_decode_multi
+ * (d = 128, 8 query heads per kv head, P = 64), hswa_prefill_chunk_ws (d = 128, an even
  * number of query heads per kv head, P = 64) and hswa_swa_gather /
  * hswa_swa_scatter (d = 128, P = 64); other calls return
  * HSWA_ERR_UNSUPPORTED. */
