@@ -184,10 +184,12 @@ def test_fp8_prefill_rejects_small_workspace():
     assert c.sess.check() == 0
 
 
-def fp8_multi_step(c, n_tok, seed, samples=None):
+def fp8_multi_step(c, n_tok, seed, samples=None, grow=False):
     """Reserve n_tok tokens per sequence, append them (quantized), run one
     multi-token decode per layer and compare the given sequences' rows with
-    the oracle at positions L - n_tok + w (tokens before position 0: o = 0)."""
+    the oracle at positions L - n_tok + w (tokens before position 0: o = 0).
+    grow: new keys scaled by 1 + their draft position and q by 4, so that the
+    row max jumps by far more than 2^8 on the last page."""
     B = c.B
     samples = list(range(B)) if samples is None else samples
     fs, ss = c.sess.reserve(range(B), [n_tok] * B)
@@ -199,8 +201,11 @@ def fp8_multi_step(c, n_tok, seed, samples=None):
         slots = fs if kind == FULL else ss
         kn = wl.normal((B * n_tok, HKV, D), seed + 10 * layer + 1, wl.DTYPE_BF16)
         vn = wl.normal((B * n_tok, HKV, D), seed + 10 * layer + 2, wl.DTYPE_BF16)
-        c.sess.append(layer, kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"))
         q = wl.normal((B * n_tok, HQ, D), seed + 10 * layer, wl.DTYPE_BF16)
+        if grow:
+            kn = (kn.float() * (1.0 + torch.arange(B * n_tok) % n_tok).view(-1, 1, 1)).to(torch.bfloat16)
+            q = (q.float() * 4.0).to(torch.bfloat16)
+        c.sess.append(layer, kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"))
         o = torch.full((B * n_tok, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
         c.sess.decode_multi(layer, q.cuda(), o, B, n_tok, scale)
         assert c.sess.check() == 0
@@ -230,6 +235,20 @@ def test_fp8_multi_token_decode_matches_oracle(n_tok):
     cached = [0, 1, 62, 63, 64, 125, 126, 127, 128, 700, 3000]
     c = Fp8Case(cached, seed=73, extra=24)
     fp8_multi_step(c, n_tok, seed=1300 + n_tok)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n_tok", [2, 3, 8, 16])
+def test_fp8_multi_token_large_max_jumps(n_tok):
+    """Keys growing with the draft position and a scaled query: the row max
+    jumps by far more than 2^8 on the last page, so the lazy O rescale fires
+    in each kernel variant (two tokens per mma.sync pass; the tensor-core
+    kernel with 4, 2 and 1 copies of the rows), over steps with releases."""
+    c = Fp8Case([40, 300, 1500, 4000], seed=91, extra=3 * n_tok + 8)
+    for step in range(3):
+        assert c.sess.release(range(c.B)) == c.ora.swa_release(range(c.B))
+        c.sess.sync()
+        fp8_multi_step(c, n_tok, seed=1600 + 10 * step, grow=True)
 
 
 @pytest.mark.gpu
