@@ -90,6 +90,7 @@ _SIG = {
     "hswa_prefill_workspace_size": (ctypes.c_size_t, [_P, ctypes.POINTER(Layer), _I, _I]),
     "hswa_prefill_chunk_ws": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I, _I,
                                    ctypes.c_float, _P, ctypes.c_size_t, _P]),
+    "hswa_swa_window_offsets": (_I, [_P, ctypes.POINTER(Layer), _I, _P, _P, _P]),
     "hswa_swa_gather": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
     "hswa_swa_scatter": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _I, _P, _P]),
     "hswa_check": (_I, [_P]),
@@ -337,6 +338,19 @@ def hswa_prefill_chunk_ws(pool, layer: Layer, q, o, d_bt, d_prefix_len, d_q_star
     _check(lib.hswa_prefill_chunk_ws(pool, ctypes.byref(layer), _ptr(q), _ptr(o), _ptr(d_bt), _ptr(d_prefix_len),
                                      _ptr(d_q_start), int(n_seqs), int(total_q), int(max_q_len), float(scale),
                                      _ptr(ws), int(ws_bytes), _stream(stream)), "hswa_prefill_chunk_ws")
+
+
+def hswa_swa_window_offsets(pool, layer: Layer, n_seqs, seq_len=None):
+    """(tok_offset int64 [n_seqs + 1], packed bytes); seq_len None = the
+    pool's current lengths."""
+    out = np.empty(int(n_seqs) + 1, np.int64)
+    nbytes = ctypes.c_size_t()
+    lens = None if seq_len is None else np.ascontiguousarray(seq_len, np.int32)
+    if lens is not None and lens.shape != (int(n_seqs),):
+        raise ValueError("seq_len must hold n_seqs lengths")
+    _check(lib.hswa_swa_window_offsets(pool, ctypes.byref(layer), int(n_seqs), _ptr(lens), _ptr(out),
+                                       ctypes.addressof(nbytes)), "hswa_swa_window_offsets")
+    return out, int(nbytes.value)
 
 
 def hswa_swa_gather(pool, layer: Layer, d_swa_bt, d_seq_len, d_tok_offset, n_seqs, dst, stream=None):

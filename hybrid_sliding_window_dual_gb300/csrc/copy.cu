@@ -306,6 +306,28 @@ static int swa_xfer(const hswa_pool *pool, const hswa_layer *layer, const int32_
     return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
 }
 
+extern "C" int hswa_swa_window_offsets(const hswa_pool *pool, const hswa_layer *layer, int n_seqs,
+                                       const int32_t *seq_len, int64_t *tok_offset_out, size_t *packed_bytes_out) {
+    if (!pool || !layer || !tok_offset_out || n_seqs < 0 || n_seqs > pool->cfg.max_seqs ||
+        layer->kind != HSWA_KIND_SWA || layer->window <= 0)
+        return HSWA_ERR_INVALID_ARG;
+    const hswa_config &c = pool->cfg;
+    const int32_t *lens = seq_len ? seq_len : pool->seq_len.data();
+    int64_t off = 0;
+    tok_offset_out[0] = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        if (lens[i] < 0) return HSWA_ERR_INVALID_ARG;
+        off += std::min<int64_t>(lens[i], layer->window);
+        tok_offset_out[i + 1] = off;
+    }
+    if (packed_bytes_out) {
+        const int64_t per_token = c.dtype == HSWA_DTYPE_FP8_E4M3 ? 2LL * c.n_kv_heads * (c.head_dim + 4)
+                                                                 : 2LL * c.n_kv_heads * c.head_dim * esize(c);
+        *packed_bytes_out = (size_t)(off * per_token);
+    }
+    return HSWA_OK;
+}
+
 extern "C" int hswa_swa_gather(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
                                const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, void *dst,
                                hswa_stream_t stream) {

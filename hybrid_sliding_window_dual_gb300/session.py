@@ -163,6 +163,11 @@ class DualPoolSession:
         B.hswa_prefill_chunk_ws(self.pool, self.layers[layer], q, o, self.bt(layer), d_prefix_len, d_q_start,
                                 n_seqs, q.shape[0], max_q_len, scale, ws, need, self.stream)
 
+    def window_offsets(self, layer, n_seqs, seq_len=None):
+        """Packed-buffer token offsets [n_seqs + 1] (host int64) and the
+        buffer's bytes, from the library (seq_len None: current lengths)."""
+        return B.hswa_swa_window_offsets(self.pool, self.layers[layer], n_seqs, seq_len)
+
     def gather(self, layer, d_tok_offset, n_seqs, dst):
         B.hswa_swa_gather(self.pool, self.layers[layer], self.d_swa_bt, self.d_seq_len, d_tok_offset, n_seqs,
                           dst, self.stream)
@@ -187,14 +192,6 @@ class DualPoolSession:
 
     def check(self):
         return B.hswa_check(self.stream)
-
-
-def window_offsets(seq_len, window):
-    """Prefix sum of min(L_s, W) as int64 [n + 1] (packed-buffer offsets)."""
-    n = np.minimum(np.asarray(seq_len, np.int64), window)
-    off = np.zeros(len(n) + 1, np.int64)
-    off[1:] = np.cumsum(n)
-    return off
 
 
 class LayerwiseReload:

@@ -408,6 +408,21 @@ int hswa_swa_gather(const hswa_pool *pool, const hswa_layer *layer, const int32_
                     const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, void *dst,
                     hswa_stream_t stream);
 
+/* Where each sequence's window starts in the packed buffer of
+ * hswa_swa_gather / hswa_swa_scatter (Sec. 2.1, Data Transfer: only the
+ * in-window tokens move, so sequence i takes n_i = min(L_i, W) token slots,
+ * W = layer->window). Host call, no device work: tok_offset_out (host int64
+ * [n_seqs + 1]) receives 0, n_0, n_0 + n_1, ..., the d_tok_offset the
+ * transfer calls take once the caller has copied it to the device.
+ * seq_len: host int32 [n_seqs], the lengths the transfer will read from
+ * d_seq_len; NULL takes the pool's own current lengths of sequences
+ * 0..n_seqs-1. packed_bytes_out (may be NULL) receives the size of the
+ * packed buffer in bytes: 2 * Hkv * d * element size per token, or
+ * 2 * Hkv * (d + 4) on FP8 pools. HSWA_ERR_INVALID_ARG for a non-SWA layer,
+ * a negative length or n_seqs outside [0, max_seqs]. */
+int hswa_swa_window_offsets(const hswa_pool *pool, const hswa_layer *layer, int n_seqs,
+                            const int32_t *seq_len, int64_t *tok_offset_out, size_t *packed_bytes_out);
+
 /* Inverse of hswa_swa_gather: write a packed buffer back into the layer's
  * SWA pool pages named by d_swa_bt (after hswa_swa_restore). */
 int hswa_swa_scatter(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,

@@ -16,7 +16,7 @@ Follows "MiMo-V2.5 Series Inference Full-Link Optimization", Sec. 2.1
   end and every N decode tokens, keeping at least the last W tokens
   (the window-safety rule).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 * free lists are FIFO queues initialised from a caller-given order;
   allocation pops from the head in ascending (sequence id, logical page);
   frees are appended in the same ascending order;

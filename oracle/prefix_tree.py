@@ -15,7 +15,7 @@ pool drops out-of-window slots; the tree therefore
    evicts them apart: out-of-window SWA segments alone (the Full prefix
    stays reusable) or whole segments.
 
-Readings where the page is silent (each listed in the design doc):
+Readings taken where the page is silent:
 * granularity: one node per page of P tokens; a node holds the page's
   tokens, its Full page and its SWA page (-1: none); matches and inserts
   are whole pages;

@@ -14,7 +14,7 @@ import torch
 import hswa_workloads as wl
 import oracle
 import hybrid_sliding_window_dual_gb300 as H
-from hybrid_sliding_window_dual_gb300.session import DualPoolSession, window_offsets
+from hybrid_sliding_window_dual_gb300.session import DualPoolSession
 
 TOL = {wl.DTYPE_BF16: 2e-2, wl.DTYPE_F32: 1e-5}
 
@@ -132,6 +132,16 @@ class Scenario:
 
     def to_dev(self, x):
         return x.to(self.sess.device)
+
+
+def window_offsets(sess, layer, lens, W):
+    """The library's packed-buffer token offsets and byte count for these
+    lengths (hswa_swa_window_offsets), with the offsets checked against the
+    oracle's in-window counts."""
+    lens = np.asarray(lens, np.int64)
+    off, nbytes = sess.window_offsets(layer, len(lens), lens.astype(np.int32))
+    assert np.array_equal(off, oracle.swa_window_counts(lens, W)[1])
+    return off, nbytes
 
 
 def max_err(got, exp):

@@ -204,3 +204,44 @@ def test_prefill_workspace_sizes():
         assert pages(H.hswa_prefill_workspace_size(lp, swa, 8, q), 8, q) == 8 * per
     assert H.hswa_prefill_workspace_size(lp, H.Layer(kind=H.HSWA_KIND_SWA, window=0), 8, 64) == 0
     H.hswa_pool_destroy(lp)
+
+
+@pytest.mark.parametrize("dtype", [H.HSWA_DTYPE_BF16, H.HSWA_DTYPE_F32, H.HSWA_DTYPE_FP8_E4M3])
+def test_swa_window_offsets_match_oracle(dtype):
+    """hswa_swa_window_offsets (host): the packed-buffer token offsets are the
+    prefix sum of the oracle's in-window counts min(L, W), from given lengths
+    and from the pool's own lengths after a reserve trace; the byte count
+    follows the packed layout of the pool's element type."""
+    W, P, hkv, d = 128, 16, 2, 128
+    cfg = H.Config(window=W, page_size=P, n_q_heads=8, n_kv_heads=hkv, head_dim=d, dtype=dtype,
+                   full_pages=4000, swa_pages=400, max_seqs=6, max_pages_per_seq=256)
+    pool = H.hswa_pool_create(cfg, None, None)
+    ora = oracle.DualPool(W, P, 4000, 400, 6, 256)
+    swa = H.Layer(kind=H.HSWA_KIND_SWA, window=W)
+    per_token = 2 * hkv * (d + 4) if dtype == H.HSWA_DTYPE_FP8_E4M3 else 2 * hkv * d * (4 if dtype == 0 else 2)
+    try:
+        lens = np.array([0, 1, 127, 128, 129, 5000], np.int32)
+        off, nbytes = H.hswa_swa_window_offsets(pool, swa, len(lens), lens)
+        exp = oracle.swa_window_counts(lens, W)[1]
+        assert np.array_equal(off, exp) and nbytes == int(exp[-1]) * per_token
+        rng = np.random.default_rng(5)
+        for _ in range(20):
+            ids = np.sort(rng.choice(6, size=rng.integers(1, 7), replace=False))
+            n_new = rng.integers(0, 300, size=ids.size)
+            H.hswa_reserve(pool, ids, n_new)
+            ora.reserve(ids, n_new)
+            H.hswa_swa_release(pool, ids)
+            ora.swa_release(ids)
+            for n in (0, 3, 6):
+                off, nbytes = H.hswa_swa_window_offsets(pool, swa, n)
+                exp = oracle.swa_window_counts(ora.seq_len[:n], W)[1]
+                assert np.array_equal(off, exp) and nbytes == int(exp[-1]) * per_token
+        full = H.Layer(kind=H.HSWA_KIND_FULL, window=W)
+        with pytest.raises(H.HswaError):
+            H.hswa_swa_window_offsets(pool, full, 3)
+        with pytest.raises(H.HswaError):
+            H.hswa_swa_window_offsets(pool, swa, 7)
+        with pytest.raises(H.HswaError):
+            H.hswa_swa_window_offsets(pool, swa, 1, np.array([-1], np.int32))
+    finally:
+        H.hswa_pool_destroy(pool)

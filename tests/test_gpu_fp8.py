@@ -283,14 +283,14 @@ def test_fp8_gather_scatter_round_trip(dst_host):
     and compare with the oracle's pack byte for byte; then drop the SWA
     segments, give the windows other pages and scatter the buffers back: the
     pools pack to the same bytes again."""
-    from hybrid_sliding_window_dual_gb300.session import window_offsets
+    from scenario import window_offsets
     cached = [0, 1, 63, 64, 65, 127, 128, 129, 700, 3000]
     c = Fp8Case(cached, seed=77, kinds=(SWA, SWA))
     B = len(cached)
     lens = c.ora.seq_len[:B]
-    offs = window_offsets(lens, W)
+    offs, nbytes = window_offsets(c.sess, 0, lens, W)
     off = torch.as_tensor(offs, device="cuda")
-    nbytes = int(offs[-1]) * 2 * HKV * (D + 4)
+    assert nbytes == int(offs[-1]) * 2 * HKV * (D + 4)
     bufs = []
     for layer in range(2):
         buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) if dst_host else \

@@ -21,8 +21,7 @@ import torch
 
 import hswa_workloads as wl
 import oracle
-from hybrid_sliding_window_dual_gb300.session import window_offsets
-from scenario import Scenario, TOL, device_out, max_err, raw_host
+from scenario import Scenario, TOL, device_out, max_err, raw_host, window_offsets
 
 FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
 
@@ -70,9 +69,10 @@ def test_swa_transfer_round_trip_and_ring_release():
                   layer_kinds=w.layer_kinds, seed=w.seed, extra_tokens=4 * 64 + 8, swa_pages=B * 6 + 100)
     n_layers = len(w.layer_kinds)
     lens = sc.ora.seq_len[:B].copy()
-    off = window_offsets(lens, W)
+    off, nbytes = window_offsets(sc.sess, 0, lens, W)
     d_off = torch.as_tensor(off, device="cuda")
     n = int(off[-1]) * 2 * w.n_kv_heads * w.head_dim
+    assert nbytes == 2 * n
     # only in-window tokens move: n_s = min(L_s, W) per sequence
     assert int(off[-1]) == int(np.minimum(lens, W).sum())
     host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(n_layers)]

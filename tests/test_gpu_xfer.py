@@ -8,22 +8,20 @@ import torch
 import hswa_workloads as wl
 import oracle
 import hybrid_sliding_window_dual_gb300 as H
-from hybrid_sliding_window_dual_gb300.session import window_offsets
-from scenario import Scenario, raw_host
+from scenario import Scenario, raw_host, window_offsets
 
 SWA = wl.KIND_SWA
-
-
-def packed_bytes(seq_len, W, hkv, d, esize):
-    return int(window_offsets(seq_len, W)[-1]) * 2 * hkv * d * esize
 
 
 def gather_and_compare(sc, layer, dst_host):
     B = len(sc.cached)
     lens = sc.ora.seq_len[:B]
-    off = torch.as_tensor(window_offsets(lens, sc.W), device="cuda")
-    n_elem = int(window_offsets(lens, sc.W)[-1]) * 2 * sc.hkv * sc.d
+    off_h, nbytes = window_offsets(sc.sess, layer, lens, sc.W)
+    off = torch.as_tensor(off_h, device="cuda")
     dt = sc.sess.dtype
+    esize = torch.empty(0, dtype=dt).element_size()
+    n_elem = int(off_h[-1]) * 2 * sc.hkv * sc.d
+    assert nbytes == n_elem * esize
     if dst_host:
         buf = torch.empty(n_elem, dtype=dt, pin_memory=True)
     else:
@@ -63,9 +61,10 @@ def test_offload_drop_restore_reload_round_trip():
     sc.sess.sync()
     sc.assert_tables_equal(device=True)
     lens = sc.ora.seq_len[:B - 1]
-    off = torch.as_tensor(window_offsets(lens, sc.W), device="cuda")
+    off_h, nbytes = window_offsets(sc.sess, 0, lens, sc.W)
+    off = torch.as_tensor(off_h, device="cuda")
     for layer in range(3):
-        n = int(window_offsets(lens, sc.W)[-1]) * 2 * sc.hkv * sc.d
+        n = nbytes // 2
         src = bufs[layer][0][:n]
         sc.sess.scatter(layer, off, B - 1, src)
         assert sc.sess.check() == 0
@@ -86,7 +85,7 @@ def test_offload_drop_restore_reload_round_trip():
 def test_gather_of_released_window_page_sets_bounds():
     sc = Scenario(8, 2, 128, 64, 128, wl.DTYPE_BF16, [500], layer_kinds=(SWA,), seed=33)
     sc.sess.d_swa_bt[0, 7] = -1  # a page inside the window
-    off = torch.as_tensor(window_offsets([500], 128), device="cuda")
+    off = torch.as_tensor(window_offsets(sc.sess, 0, [500], 128)[0], device="cuda")
     buf = torch.zeros(128 * 2 * 2 * 128, dtype=torch.bfloat16, device="cuda")
     sc.sess.gather(0, off, 1, buf)
     assert sc.sess.check() == H.HSWA_ERR_BOUNDS
