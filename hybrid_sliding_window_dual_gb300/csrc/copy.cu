@@ -222,6 +222,7 @@ using namespace hswa;
 
 extern "C" int hswa_append_kv(const hswa_pool *pool, const hswa_layer *layer, const void *k, const void *v,
                               const int32_t *d_slots, int n_tokens, hswa_stream_t stream) {
+    HSWA_NVTX("hswa_append_kv");
     if (!pool || !layer || n_tokens < 0 || (n_tokens > 0 && (!k || !v || !d_slots)) || !layer->k_pool ||
         !layer->v_pool || (layer->kind != HSWA_KIND_FULL && layer->kind != HSWA_KIND_SWA))
         return HSWA_ERR_INVALID_ARG;
@@ -331,12 +332,14 @@ extern "C" int hswa_swa_window_offsets(const hswa_pool *pool, const hswa_layer *
 extern "C" int hswa_swa_gather(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
                                const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, void *dst,
                                hswa_stream_t stream) {
+    HSWA_NVTX("hswa_swa_gather");
     return swa_xfer(pool, layer, d_swa_bt, d_seq_len, d_tok_offset, n_seqs, dst, true, stream);
 }
 
 extern "C" int hswa_swa_scatter(const hswa_pool *pool, const hswa_layer *layer, const int32_t *d_swa_bt,
                                 const int32_t *d_seq_len, const int64_t *d_tok_offset, int n_seqs, const void *src,
                                 hswa_stream_t stream) {
+    HSWA_NVTX("hswa_swa_scatter");
     return swa_xfer(pool, layer, d_swa_bt, d_seq_len, d_tok_offset, n_seqs, const_cast<void *>(src), false,
                     stream);
 }

@@ -2076,6 +2076,7 @@ int decode_impl(const hswa_pool *pool, const hswa_layer *layer, const void *q, v
 extern "C" int hswa_decode(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                            const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale, void *ws,
                            size_t ws_bytes, hswa_stream_t stream) {
+    HSWA_NVTX("hswa_decode");
     return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, 1, scale, ws, ws_bytes, nullptr, nullptr, nullptr,
                        stream);
 }
@@ -2084,6 +2085,7 @@ extern "C" int hswa_decode_append(const hswa_pool *pool, const hswa_layer *layer
                                   const void *v_new, const int32_t *d_slots, void *o, const int32_t *d_bt,
                                   const int32_t *d_seq_len, int n_seqs, float scale, void *ws, size_t ws_bytes,
                                   hswa_stream_t stream) {
+    HSWA_NVTX("hswa_decode_append");
     if (!k_new || !v_new || !d_slots) return HSWA_ERR_INVALID_ARG;
     return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, 1, scale, ws, ws_bytes, d_slots, k_new, v_new,
                        stream);
@@ -2092,6 +2094,7 @@ extern "C" int hswa_decode_append(const hswa_pool *pool, const hswa_layer *layer
 extern "C" int hswa_decode_multi(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                                  const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, int n_tok, float scale,
                                  void *ws, size_t ws_bytes, hswa_stream_t stream) {
+    HSWA_NVTX("hswa_decode_multi");
     return decode_impl(pool, layer, q, o, d_bt, d_seq_len, n_seqs, n_tok, scale, ws, ws_bytes, nullptr, nullptr,
                        nullptr, stream);
 }
@@ -2125,6 +2128,7 @@ void *decode_scratch() {
 extern "C" int hswa_decode_noalloc(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
                                    const int32_t *d_bt, const int32_t *d_seq_len, int n_seqs, float scale,
                                    hswa_stream_t stream) {
+    HSWA_NVTX("hswa_decode_noalloc");
     if (!pool || n_seqs < 0 || n_seqs > HSWA_DECODE_NOALLOC_MAX_SEQS) return HSWA_ERR_INVALID_ARG;
     if (n_seqs > 0 && layer && decode_fast_ok(pool, layer, q, o)) {
         // the exact scratch the fast path will use must fit the fixed array

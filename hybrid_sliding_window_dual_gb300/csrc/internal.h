@@ -4,7 +4,20 @@
 #include <cstdint>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "hswa.h"
+
+// An NVTX range around one ABI call, so that a profile of a serving step can
+// be split by call (the kernels each call launches sit inside its range).
+// Without a profiler attached a push / pop costs a function-pointer test.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define HSWA_NVTX(name) NvtxRange hswa_nvtx_range_(name)
 
 // FIFO free list of page indices (ring buffer; never holds more than the
 // pool's page count).

@@ -87,6 +87,7 @@ extern "C" int hswa_pool_destroy(hswa_pool *pool) {
 
 extern "C" int hswa_reserve(hswa_pool *pool, int n, const int32_t *seq_ids, const int32_t *n_new,
                             int32_t *full_slot_out, int32_t *swa_slot_out) {
+    HSWA_NVTX("hswa_reserve");
     if (!pool || n < 0 || (n > 0 && (!seq_ids || !n_new))) return HSWA_ERR_INVALID_ARG;
     const int32_t P = pool->cfg.page_size, MP = pool->cfg.max_pages_per_seq;
     // validate and count the pages each pool must give
@@ -129,6 +130,7 @@ extern "C" int hswa_reserve(hswa_pool *pool, int n, const int32_t *seq_ids, cons
 }
 
 extern "C" int hswa_swa_release(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_freed_out) {
+    HSWA_NVTX("hswa_swa_release");
     std::vector<int32_t> ids;
     if (!pool || !sorted_ids(pool, n, seq_ids, ids)) return HSWA_ERR_INVALID_ARG;
     const int64_t P = pool->cfg.page_size, W = pool->cfg.window, MP = pool->cfg.max_pages_per_seq;
@@ -150,6 +152,7 @@ extern "C" int hswa_swa_release(hswa_pool *pool, int n, const int32_t *seq_ids, 
 }
 
 extern "C" int hswa_seq_free(hswa_pool *pool, int n, const int32_t *seq_ids) {
+    HSWA_NVTX("hswa_seq_free");
     std::vector<int32_t> ids;
     if (!pool || !sorted_ids(pool, n, seq_ids, ids)) return HSWA_ERR_INVALID_ARG;
     const int64_t MP = pool->cfg.max_pages_per_seq;
@@ -174,6 +177,7 @@ extern "C" int hswa_seq_free(hswa_pool *pool, int n, const int32_t *seq_ids) {
 }
 
 extern "C" int hswa_swa_drop(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_freed_out) {
+    HSWA_NVTX("hswa_swa_drop");
     std::vector<int32_t> ids;
     if (!pool || !sorted_ids(pool, n, seq_ids, ids)) return HSWA_ERR_INVALID_ARG;
     const int64_t MP = pool->cfg.max_pages_per_seq;
@@ -191,6 +195,7 @@ extern "C" int hswa_swa_drop(hswa_pool *pool, int n, const int32_t *seq_ids, int
 }
 
 extern "C" int hswa_swa_restore(hswa_pool *pool, int n, const int32_t *seq_ids, int32_t *n_alloc_out) {
+    HSWA_NVTX("hswa_swa_restore");
     std::vector<int32_t> ids;
     if (!pool || !sorted_ids(pool, n, seq_ids, ids)) return HSWA_ERR_INVALID_ARG;
     const int64_t P = pool->cfg.page_size, W = pool->cfg.window, MP = pool->cfg.max_pages_per_seq;

@@ -131,6 +131,7 @@ __global__ void selftest_bounded_wait(int *err) {
 using namespace hswa;
 
 extern "C" int hswa_selftest_bounded_wait(hswa_stream_t stream) {
+    HSWA_NVTX("hswa_selftest_bounded_wait");
     int *err = error_word();
     if (!err) return HSWA_ERR_CUDA;
     set_last_kernel("selftest_bounded_wait");
@@ -152,6 +153,7 @@ void hswa_pool_release_device(hswa_pool *pool) {
 
 extern "C" int hswa_sync_tables(hswa_pool *pool, int32_t *d_full_bt, int32_t *d_swa_bt, int32_t *d_seq_len,
                                 hswa_stream_t stream) {
+    HSWA_NVTX("hswa_sync_tables");
     if (!pool || !d_full_bt || !d_swa_bt || !d_seq_len) return HSWA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int64_t E = pool->table_entries();
@@ -219,6 +221,7 @@ extern "C" int hswa_sync_tables(hswa_pool *pool, int32_t *d_full_bt, int32_t *d_
 }
 
 extern "C" int hswa_check(hswa_stream_t stream) {
+    HSWA_NVTX("hswa_check");
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return HSWA_ERR_CUDA;
     int *w = error_word();
     if (!w) return HSWA_ERR_CUDA;

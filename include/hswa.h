@@ -55,6 +55,12 @@
  * returns one of the HSWA_* status codes below; no exception crosses the
  * ABI. Device-side index checks and bounded waits do not trap: they set a
  * device error word that hswa_check reads back.
+ *
+ * Device lifetime. The library looks up, once per device, the addresses of
+ * its own device variables (the error word, the no-allocation decode
+ * scratch) and sets its kernels' shared-memory attributes. Do not use it on
+ * a device after cudaDeviceReset of that device in the same process: the
+ * cached addresses and attributes belong to the context that was reset.
  */
 #ifndef HSWA_H
 #define HSWA_H
@@ -441,11 +447,17 @@ int hswa_swa_scatter(const hswa_pool *pool, const hswa_layer *layer, const int32
  * HSWA_DECODE_NOALLOC_SCRATCH_BYTES in the library's device image, which
  * every GPU that loads the library keeps until the process exits.
  *
- * Limits: n_seqs <= HSWA_DECODE_NOALLOC_MAX_SEQS, and the launch must fit
- * the fixed scratch (it does on any part with up to 500 resident decode
- * CTAs); otherwise the call returns HSWA_ERR_INVALID_ARG and launches
- * nothing. The first call on a device looks up the scratch address with
- * that device current; make that first call before any stream capture.
+ * Limits: n_seqs <= HSWA_DECODE_NOALLOC_MAX_SEQS, and the scratch the
+ * launch needs must fit the array:
+ *   round_up(16 * (n_seqs + 1), 256) + 2 * 4160 * n_ctas
+ *       <= HSWA_DECODE_NOALLOC_SCRATCH_BYTES,
+ * with n_ctas = SM count * resident decode CTAs per SM (at most 4). On a
+ * 152-SM GB300 that is 304 CTAs over bf16 pools and 456 over FP8 pools
+ * (2 and 3 per SM), 2.8 and 4.06 MB at the largest batch, so every batch
+ * fits there; a part with more SMs or more resident CTAs per SM can reject
+ * large batches. A batch that does not fit returns HSWA_ERR_INVALID_ARG and
+ * launches nothing. The first call on a device looks up the scratch address
+ * with that device current; make that first call before any stream capture.
  * All calls on a device share the one scratch array: two calls whose work
  * overlaps on the GPU (different streams, no ordering between them) race
  * on it. Nothing in the scratch has to start at zero; it keeps whatever the
