@@ -34,7 +34,10 @@ HSWA_DECODE_MAX_TOKENS = 16
 class HswaError(RuntimeError):
     def __init__(self, status, call):
         self.status = status
-        super().__init__("%s: %s (status %d)" % (call, status_string(status), status))
+        detail = ""
+        if status == HSWA_ERR_CUDA:
+            detail = " [%s]" % lib.hswa_last_cuda_error().decode()
+        super().__init__("%s: %s (status %d)%s" % (call, status_string(status), status, detail))
 
 
 class NoSpace(HswaError):
@@ -96,6 +99,7 @@ _SIG = {
     "hswa_check": (_I, [_P]),
     "hswa_selftest_bounded_wait": (_I, [_P]),
     "hswa_last_kernel": (ctypes.c_char_p, []),
+    "hswa_last_cuda_error": (ctypes.c_char_p, []),
     "hswa_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -374,3 +378,7 @@ def hswa_selftest_bounded_wait(stream=None):
 
 def hswa_last_kernel():
     return lib.hswa_last_kernel().decode()
+
+
+def hswa_last_cuda_error():
+    return lib.hswa_last_cuda_error().decode()

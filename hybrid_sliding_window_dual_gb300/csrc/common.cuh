@@ -22,6 +22,9 @@ __device__ __forceinline__ void set_error(int *err, int code) {
 int *error_word();
 // Host: set the name returned by hswa_last_kernel().
 void set_last_kernel(const char *name);
+// Host: record a failed CUDA call (returned by hswa_last_cuda_error) and
+// return HSWA_ERR_CUDA.
+int cuda_fail(cudaError_t e, const char *where);
 // Host: number of SMs of the current device (cached per device).
 int sm_count();
 // Host: launch a kernel with programmatic stream serialization (PDL).
@@ -151,6 +154,21 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
+
+// 3-D tiled tensor copy shared -> global (whole box; coordinates past the
+// tensor's extent are not written), tracked by this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int32_t x, int32_t y,
+                                             int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

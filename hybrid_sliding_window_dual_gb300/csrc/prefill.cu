@@ -73,6 +73,8 @@ struct PrefillArgs {
     const int32_t *q_start;
     __nv_bfloat16 *o;
     int32_t n_seqs, bt_stride, hq, hkv, window, num_pages;
+    int32_t nqb;      // 128-row blocks per sequence in the grid
+    int32_t lpt;      // 1: sequences ranked longest first
     int32_t kv_rows;  // rows of the pool tensor map (OOB row = zero fill)
     float scale_log2;
     int *err;
@@ -94,10 +96,40 @@ struct Unit {
     int32_t L;          // keys of the sequence after the chunk
 };
 
-__device__ __forceinline__ bool make_unit(const PrefillArgs &a, Unit &u) {
-    u.hp = blockIdx.x;
-    u.qb = blockIdx.y;
-    u.s = blockIdx.z;
+// Batches up to this many sequences are scheduled longest first.
+constexpr int kLptMaxSeqs = 64;
+
+// The sequence of a given rank when sequences are ordered by their keys
+// after the chunk, longest first (ties by index). Warp-wide; n_seqs <= 64.
+__device__ __forceinline__ int32_t seq_of_rank(const PrefillArgs &a, int32_t rank) {
+    const int lane = threadIdx.x & 31;
+    int32_t found = -1;
+    for (int i = lane; i < a.n_seqs; i += 32) {
+        const int32_t key = a.prefix[i] + a.q_start[i + 1] - a.q_start[i];
+        int32_t r = 0;
+        for (int j = 0; j < a.n_seqs; ++j) {
+            const int32_t kj = a.prefix[j] + a.q_start[j + 1] - a.q_start[j];
+            r += (kj > key) || (kj == key && j < i);
+        }
+        if (r == rank) found = i;
+    }
+    for (int o = 16; o > 0; o >>= 1) found = max(found, __shfl_xor_sync(0xffffffffu, found, o));
+    return found;
+}
+
+// The unit of this CTA. The 1-D grid runs through (sequence rank, block,
+// head pair) with the head pair fastest, so the pairs of one kv head run
+// side by side and share its K / V tiles in L2; sequences come longest
+// first and each sequence's blocks last row first, so the hardware hands
+// the longest units out first and the short ones fill the tail.
+__device__ __forceinline__ bool make_unit(const PrefillArgs &a, Unit &u, int32_t seq) {
+    const int32_t n_hp = a.hq / 2;
+    int64_t lin = blockIdx.x;
+    u.hp = (int32_t)(lin % n_hp);
+    lin /= n_hp;
+    u.qb = a.nqb - 1 - (int32_t)(lin % a.nqb);
+    u.s = seq;
+    if (u.s < 0) return false;
     const int32_t g_heads = a.hq / a.hkv;
     u.g = (2 * u.hp) / g_heads;
     const int32_t q0 = a.q_start[u.s], n = a.q_start[u.s + 1] - q0;
@@ -241,45 +273,121 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
     if (!ok) sm.abort = 1;
 }
 
+// One S tile of one query row (this thread's TMEM lane): mask on the raw
+// scores where the tile needs it (keys past t, or before t - W + 1), update
+// the running max (log2 units) and sum, write P over the start of S, and
+// rescale O in TMEM when the max grows by more than 2^8. TMEM loads and
+// stores are warp-wide: every lane of the warp calls this.
 template <bool kF16>
-__device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Unit &u, int x) {
-    const int warp = (threadIdx.x >> 5) & 3;
-    const int r = warp * 32 + (threadIdx.x & 31);  // query row of this thread
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_s = sm.tmem_base + lane_off + 128 * x;
-    const uint32_t t_o = sm.tmem_base + lane_off + 256 + 128 * x;
-    const int32_t t = u.p0 + min(r, u.n_rows - 1);  // rows past the chunk repeat the last valid row
-    const int32_t t_min = u.p0, t_max = u.p0 + u.n_rows - 1;
-    const int32_t W = a.window;
-    float m_used = -INFINITY, l = 0.f;  // running max (log2 units) and sum of P
-    bool ok = true;
-    for (int j = 0; j < u.n_tiles; ++j) {
-        ok = mbar_wait(&sm.s_full[x], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        // S row in four 32-column chunks; each load overlaps the mask and
-        // max work of the chunk before it
-        uint32_t sr[4][32];
-        const int32_t k0 = (u.tile_lo + j) * kBN;
-        const bool masked = (k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1);
-        const int32_t hi_c = t - k0;                       // keys c <= hi_c
-        const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;  // keys c >= lo_c
-        // one max per chunk, each a chain of 8: short dependency chains for a
-        // thread that has few warps beside it to hide them
-        float mc[4];
-        tmem_ld32(t_s, sr[0]);
-        tmem_wait_ld(sr[0]);
+__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int32_t k0, int32_t t, int32_t t_min,
+                                             int32_t t_max, int32_t W, float scale_log2, bool first_tile,
+                                             float &m_used, float &l) {
+    // S row in four 32-column chunks; each load overlaps the mask and max
+    // work of the chunk before it
+    uint32_t sr[4][32];
+    const bool masked = (k0 + kBN - 1 > t_min) || (W > 0 && k0 < t_max - W + 1);
+    const int32_t hi_c = t - k0;                       // keys c <= hi_c
+    const int32_t lo_c = W > 0 ? t - W + 1 - k0 : -1;  // keys c >= lo_c
+    // one max per chunk, each a chain of 8: short dependency chains for a
+    // thread that has few warps beside it to hide them
+    float mc[4];
+    tmem_ld32(t_s, sr[0]);
+    tmem_wait_ld(sr[0]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c + 1 < 4) tmem_ld32(t_s + 32 * (c + 1), sr[c + 1]);
+        // raw scores: the scale (> 0) does not change which keys win the max
+        if (masked) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int col = c * 32 + i;
+                if (col > hi_c || col < lo_c) sr[c][i] = __float_as_uint(-INFINITY);
+            }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            m0 = max3(m0, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+            m1 = max3(m1, __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
+        }
+        mc[c] = fmaxf(m0, m1);
+        if (c + 1 < 4) tmem_wait_ld(sr[c + 1]);
+    }
+    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * scale_log2;
+    // A new reference max only when the row max grows by more than 2^8;
+    // then O (nothing before the first PV) and l are rescaled.
+    const bool need = mx > m_used + kRescaleLog2;
+    const bool resc = need && !first_tile && m_used != -INFINITY;
+    const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
+    if (need) m_used = mx;
+    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+    const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
+    float2 sums[4];  // one running sum per chunk (chains of 16, not 64)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float2 &sum2 = sums[c];
+        sum2 = make_float2(0.f, 0.f);
+        // P = 2^(s * scale - m) two keys at a time (packed f32x2 FMA and
+        // add), packed to 16-bit pairs in place, then its 16 columns (32
+        // keys) written over the start of S
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                                        sc2, nm2);
+            const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            sum2 = __fadd2_rn(sum2, p);
+            sr[c][i] = kF16 ? pack_f16(p.x, p.y) : pack_bf16(p.x, p.y);
+        }
+        tmem_st16(t_s + 16 * c, sr[c]);
+    }
+    // the O rescale comes after the P store (the S registers are free
+    // then); the whole warp takes this path when any of its rows needs it
+    // (the others scale by 1)
+    if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            if (c + 1 < 4) tmem_ld32(t_s + 32 * (c + 1), sr[c + 1]);
-            // raw scores: the scale (> 0) does not change which keys win the max
-            if (masked) {
+            uint32_t ov[32];
+            tmem_ld32(t_o + 32 * c, ov);
+            tmem_wait_ld(ov);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = c * 32 + i;
-                    if (col > hi_c || col < lo_c) sr[c][i] = __float_as_uint(-INFINITY);
-                }
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(t_o + 32 * c, ov);
+        }
+    }
+    const float2 s01 = __fadd2_rn(sums[0], sums[1]), s23 = __fadd2_rn(sums[2], sums[3]);
+    const float2 sum2 = __fadd2_rn(s01, s23);
+    l = l * alpha + (sum2.x + sum2.y);
+    tmem_wait_st();
+}
+
+// One S tile of a window block (SWA layer): this lane's row t sees keys
+// [t - W + 1, t]; the warp's rows are t_first..t_last. A 32-key chunk that
+// no row of the warp sees is neither loaded nor exponentiated (its P is 0),
+// and only a chunk that some row sees in part is masked key by key. With
+// blocks on 128-key boundaries a warp has one partial chunk per tile and
+// skips three of the eight chunks of a block's two tiles.
+template <bool kF16>
+__device__ __forceinline__ void softmax_tile_band(uint32_t t_s, uint32_t t_o, int32_t k0, int32_t t, int32_t t_first,
+                                                  int32_t t_last, int32_t W, float scale_log2, bool first_tile,
+                                                  float &m_used, float &l) {
+    uint32_t sr[4][32];
+    // chunks [c_lo, c_hi] meet some row's window; the others are skipped
+    const int32_t c_lo = max(0, (t_first - W + 1 - k0) >> 5), c_hi = min(3, (t_last - k0) >> 5);
+    const int32_t lo_c = t - W + 1 - k0;  // keys c of the tile with lo_c <= c <= lo_c + W - 1
+    float mc[4];
+    tmem_ld32(t_s, sr[0]);
+    tmem_wait_ld(sr[0]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c + 1 < 4) tmem_ld32(t_s + 32 * (c + 1), sr[c + 1]);
+        mc[c] = -INFINITY;
+        if (c_lo <= c && c <= c_hi) {  // the same for every lane
+            // a chunk every row of the warp sees whole needs no mask
+            const bool full = k0 + 32 * c >= t_last - W + 1 && k0 + 32 * c + 31 <= t_first;
+            if (!full) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if ((uint32_t)(c * 32 + i - lo_c) > (uint32_t)(W - 1)) sr[c][i] = __float_as_uint(-INFINITY);
             }
             float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
@@ -288,74 +396,64 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
                 m1 = max3(m1, __uint_as_float(sr[c][i + 2]), __uint_as_float(sr[c][i + 3]));
             }
             mc[c] = fmaxf(m0, m1);
-            if (c + 1 < 4) tmem_wait_ld(sr[c + 1]);
         }
-        const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * a.scale_log2;
-        // A new reference max only when the row max grows by more than 2^8;
-        // then O (nothing before the first PV) and l are rescaled.
-        const bool need = mx > m_used + kRescaleLog2;
-        const bool resc = need && j > 0 && m_used != -INFINITY;
-        const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
-        if (need) m_used = mx;
-        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(neg_m, neg_m);
-        float2 sums[4];  // one running sum per chunk (chains of 16, not 64)
+        if (c + 1 < 4) tmem_wait_ld(sr[c + 1]);
+    }
+    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * scale_log2;
+    const bool need = mx > m_used + kRescaleLog2;
+    const bool resc = need && !first_tile && m_used != -INFINITY;
+    const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
+    if (need) m_used = mx;
+    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+    const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
+    float2 sums[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float2 &sum2 = sums[c];
-            sum2 = make_float2(0.f, 0.f);
-            // P = 2^(s * scale - m) two keys at a time (packed f32x2 FMA and
-            // add), packed to bf16 pairs in place, then its 16 columns (32
-            // keys) written over the start of S
+    for (int c = 0; c < 4; ++c) {
+        float2 &sum2 = sums[c];
+        sum2 = make_float2(0.f, 0.f);
+        if (c_lo <= c && c <= c_hi) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
-                                            sc2, nm2);
+                const float2 x = __ffma2_rn(
+                    make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sc2, nm2);
                 const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                 sum2 = __fadd2_rn(sum2, p);
                 sr[c][i] = kF16 ? pack_f16(p.x, p.y) : pack_bf16(p.x, p.y);
             }
-            tmem_st16(t_s + 16 * c, sr[c]);
-        }
-        // the O rescale comes after the P store (the S registers are free
-        // then); TMEM loads and stores are warp-wide, so the whole warp takes
-        // this path when any of its rows needs it (the others scale by 1)
-        if (__any_sync(0xffffffffu, resc)) {
+        } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(t_o + 32 * c, ov);
-                tmem_wait_ld(ov);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                tmem_st32(t_o + 32 * c, ov);
-            }
+            for (int i = 0; i < 16; ++i) sr[c][i] = 0u;  // no row of the warp sees these keys
         }
-        const float2 s01 = __fadd2_rn(sums[0], sums[1]), s23 = __fadd2_rn(sums[2], sums[3]);
-        const float2 sum2 = __fadd2_rn(s01, s23);
-        l = l * alpha + (sum2.x + sum2.y);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&sm.p_full[x]);
+        tmem_st16(t_s + 16 * c, sr[c]);
     }
-    // epilogue: wait for the last PV (always: TMEM is freed after this
-    // function returns), normalise this row of O and store it
-    const bool fin = mbar_wait(&sm.o_final[x], 0, a.err);
-    ok = __all_sync(0xffffffffu, ok && fin);
-    if (!ok) {
-        sm.abort = 1;
-        return;
+    if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(t_o + 32 * c, ov);
+            tmem_wait_ld(ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(t_o + 32 * c, ov);
+        }
     }
-    tc_fence_after();
+    const float2 s01 = __fadd2_rn(sums[0], sums[1]), s23 = __fadd2_rn(sums[2], sums[3]);
+    const float2 sum2 = __fadd2_rn(s01, s23);
+    l = l * alpha + (sum2.x + sum2.y);
+    tmem_wait_st();
+}
+
+// Normalise this thread's row of O (TMEM) by 1 / l and store it as bf16 at
+// dst (when valid; the TMEM loads are warp-wide, every lane calls this).
+__device__ __forceinline__ void store_o_row(uint32_t t_o, float l, __nv_bfloat16 *dst_row, bool valid) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    const int h = 2 * u.hp + x;
-    uint4 *dst = reinterpret_cast<uint4 *>(a.o + ((int64_t)(u.row0 + r) * a.hq + h) * kD);
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint32_t ov[32];
         tmem_ld32(t_o + 32 * c, ov);
         tmem_wait_ld(ov);
-        if (r < u.n_rows) {
+        if (valid) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 uint4 w;
@@ -369,12 +467,97 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
     }
 }
 
+// Normalise this thread's row of O (TMEM) and write the warp's 32 rows: one
+// 64-column half at a time through the warp's 4 KB shared-memory stage
+// (128-byte swizzle) and a TMA store, so that the writes reach memory as
+// whole rows instead of one 16-byte piece per row and instruction. A warp
+// with rows past the block's end stores its valid rows from registers.
+__device__ __forceinline__ void store_o_rows_staged(uint32_t t_o, float l, uint8_t *stage, const CUtensorMap *to,
+                                                    int32_t head, int32_t row_first, bool full_warp,
+                                                    __nv_bfloat16 *dst_row, bool valid) {
+    if (!full_warp) {
+        store_o_row(t_o, l, dst_row, valid);
+        return;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int dh = 0; dh < 2; ++dh) {
+        uint32_t ov[2][32];
+        tmem_ld32(t_o + 64 * dh, ov[0]);
+        tmem_ld32(t_o + 64 * dh + 32, ov[1]);
+        tmem_wait_ld(ov[0]);
+        tmem_wait_ld(ov[1]);
+        // the stage is free once the warp's previous store has read it
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        uint8_t *row = stage + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // 16-byte chunk j: columns 8j .. 8j + 7 of the half
+            const uint32_t *v = ov[j >> 2] + (j & 3) * 8;
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
+            w.y = pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+            w.z = pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
+            w.w = pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
+            *reinterpret_cast<uint4 *>(row + ((j ^ (lane & 7)) << 4)) = w;
+        }
+        fence_proxy_async_shared();  // the stage is read by the TMA store
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(to, stage, dh * 64, head, row_first);
+            bulk_commit();
+        }
+    }
+}
+
+template <bool kF16>
+__device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Unit &u, int x) {
+    const int warp = (threadIdx.x >> 5) & 3;
+    const int r = warp * 32 + (threadIdx.x & 31);  // query row of this thread
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_s = sm.tmem_base + lane_off + 128 * x;
+    const uint32_t t_o = sm.tmem_base + lane_off + 256 + 128 * x;
+    const int32_t t = u.p0 + min(r, u.n_rows - 1);  // rows past the chunk repeat the last valid row
+    const int32_t t_min = u.p0, t_max = u.p0 + u.n_rows - 1;
+    float m_used = -INFINITY, l = 0.f;  // running max (log2 units) and sum of P
+    bool ok = true;
+    for (int j = 0; j < u.n_tiles; ++j) {
+        ok = mbar_wait(&sm.s_full[x], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        softmax_tile<kF16>(t_s, t_o, (u.tile_lo + j) * kBN, t, t_min, t_max, a.window, a.scale_log2, j == 0, m_used,
+                           l);
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[x]);
+    }
+    // epilogue: wait for the last PV (always: TMEM is freed after this
+    // function returns), normalise this row of O and store it
+    const bool fin = mbar_wait(&sm.o_final[x], 0, a.err);
+    ok = __all_sync(0xffffffffu, ok && fin);
+    if (!ok) {
+        sm.abort = 1;
+        return;
+    }
+    tc_fence_after();
+    const int h = 2 * u.hp + x;
+    store_o_row(t_o, l, a.o + ((int64_t)(u.row0 + r) * a.hq + h) * kD, r < u.n_rows);
+}
+
 template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_bf16_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, PrefillArgs a) {
+    __shared__ int32_t unit_seq;
+    if (threadIdx.x < 32) {
+        const int32_t rank = (int32_t)(blockIdx.x / ((int64_t)(a.hq / 2) * a.nqb));
+        const int32_t seq = a.lpt ? seq_of_rank(a, rank) : rank;
+        if (threadIdx.x == 0) unit_seq = seq;
+    }
+    __syncthreads();
     Unit u;
-    if (!make_unit(a, u)) return;
+    if (!make_unit(a, u, unit_seq)) return;
     extern __shared__ uint8_t raw[];
     PrefillSmem &sm =
         *reinterpret_cast<PrefillSmem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
@@ -414,6 +597,503 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 9) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(sm.tmem_base));
+}
+
+// ------------------------------------------ SWA layers: persistent CTAs
+// Sliding-window layers with W <= 128 ("MiMo-V2.5 Series Inference
+// Full-Link Optimization", Sec. 1.1: an SWA query attends only to the last W
+// tokens). A block of query rows at positions [128 m, 128 m + 128) sees keys
+// [128 m - W + 1, 128 m + 127]: key tiles m - 1 and m, never more. Blocks are
+// cut at these absolute boundaries (a chunk's first and last block may be
+// partial) and each CTA is persistent, one per SM, walking a contiguous share
+// of the unit list
+//     for each sequence, for each kv head g, for each block m,
+//         for each pair of query heads of g
+// so the head pairs of one block reuse its two K / V tiles and the next
+// block reuses tile m: a tile is loaded into shared memory once per CTA that
+// needs it. TMEM, barriers and the ring are set up once per CTA; a head's
+// next queries load as soon as its last QK MMA of the current unit is done,
+// and O leaves through a per-warp shared-memory stage and TMA stores.
+// Roles as in prefill_tc_bf16_d128: warps 0-7 softmax (two heads), warp 8
+// lane 0 loads Q and lane 1 loads K / V, warp 9 issues the MMAs.
+
+constexpr int kQBufs = 2;
+constexpr int kDescs = 4;
+constexpr uint32_t kStageBytes = 32 * 128;  // one warp's 32 rows x 64 columns of O, bf16
+
+// What the softmax warps need of a unit (written by the Q loader).
+struct SwaDesc {
+    int32_t p0, n_rows, row0, lo, hi, hp;
+};
+
+struct SwaSmem {
+    uint8_t q[kQBufs][kTileBytes];     // Q of one head: [d half][128 rows][128 B]
+    uint8_t kv[kSlots][kTileBytes];    // K or V tiles: [d half][128 keys][128 B]
+    uint8_t ostage[8][kStageBytes];    // per softmax warp: O rows on their way out
+    uint64_t q_full[kQBufs], q_empty[kQBufs];
+    uint64_t kv_full[kSlots], kv_empty[kSlots];
+    uint64_t s_full[2], p_full[2], o_final[2], mma_done;
+    uint64_t desc_full[kDescs], desc_empty[kDescs];
+    SwaDesc desc[kDescs];
+    uint32_t tmem_base;
+    int32_t abort;
+    int32_t start_seq, start_off, n_units;  // this CTA's share of the unit list
+};
+static_assert(offsetof(SwaSmem, kv) % 1024 == 0, "128-byte swizzled tiles need 1024-byte alignment");
+static_assert(offsetof(SwaSmem, ostage) % 1024 == 0, "128-byte swizzled tiles need 1024-byte alignment");
+constexpr size_t kSwaSmemBytes = sizeof(SwaSmem) + 1024;
+static_assert(kSwaSmemBytes <= 232448, "one CTA per SM must fit");
+
+// Units (blocks x kv heads x head pairs) of sequence s.
+__device__ __forceinline__ int32_t swa_seq_units(const PrefillArgs &a, int32_t s, int32_t pairs) {
+    const int32_t pre = a.prefix[s], n = a.q_start[s + 1] - a.q_start[s];
+    if (n <= 0) return 0;
+    return ((pre + n - 1) / kBM - pre / kBM + 1) * a.hkv * pairs;
+}
+
+// Warp 0: this CTA's share [c U / G, (c + 1) U / G) of the U units of all
+// sequences, as (first sequence, unit within it, count).
+__device__ void swa_partition(SwaSmem &sm, const PrefillArgs &a, int32_t pairs) {
+    const int lane = threadIdx.x & 31;
+    int64_t total = 0;
+    for (int32_t base = 0; base < a.n_seqs; base += 32) {
+        const int32_t i = base + lane;
+        int64_t u = i < a.n_seqs ? swa_seq_units(a, i, pairs) : 0;
+        for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+        total += u;
+    }
+    const int64_t u0 = total * blockIdx.x / gridDim.x, u1 = total * (blockIdx.x + 1) / gridDim.x;
+    int64_t before = 0, off = 0;
+    int32_t s0 = -1;
+    for (int32_t base = 0; base < a.n_seqs && s0 < 0; base += 32) {
+        const int32_t i = base + lane;
+        const int64_t u = i < a.n_seqs ? swa_seq_units(a, i, pairs) : 0;
+        int64_t inc = u;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int64_t excl = before + inc - u;
+        const unsigned hit = __ballot_sync(0xffffffffu, u > 0 && excl <= u0 && u0 < excl + u);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            s0 = base + src;
+            off = __shfl_sync(0xffffffffu, u0 - excl, src);
+        }
+        before += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) {
+        sm.start_seq = s0;
+        sm.start_off = (int32_t)off;
+        sm.n_units = (s0 >= 0 && u1 > u0) ? (int32_t)(u1 - u0) : 0;
+    }
+}
+
+// Walk over the unit list; every role walks it the same way.
+struct SwaWalk {
+    int32_t s, g, m, hpi, left;
+    int32_t pre, n, q0, m_lo, m_hi;
+
+    __device__ void seq(const PrefillArgs &a) {
+        q0 = a.q_start[s];
+        n = a.q_start[s + 1] - q0;
+        pre = a.prefix[s];
+        m_lo = pre / kBM;
+        m_hi = n > 0 ? (pre + n - 1) / kBM : m_lo - 1;
+    }
+    __device__ void start(const PrefillArgs &a, const SwaSmem &sm, int32_t pairs) {
+        s = sm.start_seq;
+        left = sm.n_units;
+        seq(a);
+        const int32_t nb = m_hi - m_lo + 1, off = sm.start_off;
+        g = off / (nb * pairs);
+        const int32_t r = off - g * nb * pairs;
+        m = m_lo + r / pairs;
+        hpi = r % pairs;
+    }
+    __device__ void next(const PrefillArgs &a, int32_t pairs) {
+        if (--left <= 0) return;
+        if (++hpi < pairs) return;
+        hpi = 0;
+        if (++m <= m_hi) return;
+        m = m_lo;
+        if (++g < a.hkv) return;
+        g = 0;
+        do {
+            if (++s >= a.n_seqs) {  // the share ran past the last unit: stop
+                left = 0;
+                return;
+            }
+            seq(a);
+        } while (m_hi < m_lo);
+        m = m_lo;
+    }
+};
+
+struct SwaBlock {
+    int32_t s, g, hp;              // sequence, kv head, pair of query heads
+    int32_t p0, n_rows, row0, L;   // first position, rows, first q row, keys after the chunk
+    int32_t lo, hi;                // key tiles of the block
+    int32_t first_page, last_page; // logical pages its rows can see
+    int64_t tile_base;             // identity of tile 0 of (s, g)
+};
+
+__device__ __forceinline__ SwaBlock swa_block(const SwaWalk &w, const PrefillArgs &a, int32_t pairs) {
+    SwaBlock b;
+    b.s = w.s;
+    b.g = w.g;
+    b.hp = w.g * pairs + w.hpi;
+    b.p0 = max(w.pre, w.m * kBM);
+    const int32_t p_end = min(w.pre + w.n, (w.m + 1) * kBM);
+    b.n_rows = p_end - b.p0;
+    b.row0 = w.q0 + (b.p0 - w.pre);
+    b.L = w.pre + w.n;
+    const int32_t key_lo = max(0, b.p0 - a.window + 1);
+    b.lo = key_lo / kBN;
+    b.hi = w.m;
+    b.first_page = key_lo / kP;
+    b.last_page = (b.L - 1) / kP;
+    b.tile_base = ((int64_t)b.s * a.hkv + b.g) << 32;
+    return b;
+}
+
+// The two K / V tiles in the ring. A tile takes two consecutive loads (K,
+// then V) in load order; load i sits in slot i % kSlots. The producer and
+// the MMA thread make the same calls in the same order, so they agree on
+// every load index.
+struct TileRing {
+    int64_t id0, id1;  // resident tiles (-1: none)
+    int32_t k0, k1;    // load index of each one's K; its V is the next load
+    int32_t next;
+
+    __device__ void init() {
+        id0 = id1 = -1;
+        next = 0;
+    }
+    // Load index of tile tid's K, or -1 when it is not in the ring.
+    __device__ int32_t find(int64_t tid) const { return id0 == tid ? k0 : id1 == tid ? k1 : -1; }
+    // New tile tid for a block needing tiles [lo_id, hi_id]: it replaces the
+    // entry that block does not need (a block needs at most two tiles).
+    __device__ int32_t place(int64_t tid, int64_t lo_id, int64_t hi_id) {
+        const int32_t k = next;
+        next += 2;
+        if (id0 >= lo_id && id0 <= hi_id) {
+            id1 = tid;
+            k1 = k;
+        } else {
+            id0 = tid;
+            k0 = k;
+        }
+        return k;
+    }
+};
+
+__device__ void swa_load_q(SwaSmem &sm, const CUtensorMap *tq, const PrefillArgs &a, int32_t pairs) {
+    prefetch_tmap(tq);
+    SwaWalk w;
+    w.start(a, sm, pairs);
+    int32_t issued = 0;
+    for (int32_t ub = 0; ub < sm.n_units; ++ub) {
+        const SwaBlock b = swa_block(w, a, pairs);
+        // the unit's descriptor for the softmax warps; its slot was freed
+        // (all 256 softmax threads arrived) when unit ub - 4 was stored
+        const int dslot = ub % kDescs;
+        bool ok = ub < kDescs || (mbar_wait(&sm.desc_empty[dslot], ((ub / kDescs) + 1) & 1, a.err) &&
+                                  !*(volatile int32_t *)&sm.abort);
+        if (ok) {
+            SwaDesc &d = sm.desc[dslot];
+            d.p0 = b.p0;
+            d.n_rows = b.n_rows;
+            d.row0 = b.row0;
+            d.lo = b.lo;
+            d.hi = b.hi;
+            d.hp = b.hp;
+            mbar_arrive(&sm.desc_full[dslot]);  // release: the fields are visible to the waiters
+        }
+        for (int x = 0; x < 2 && ok; ++x) {
+            const int32_t qi = 2 * ub + x, slot = qi % kQBufs;
+            // the buffer's previous item (qi - kQBufs) has been read by its
+            // last QK MMA; parity waits stay at most one phase behind
+            // because each item waits for the release of the one before
+            if (qi >= kQBufs)
+                ok = mbar_wait(&sm.q_empty[slot], ((qi / kQBufs) + 1) & 1, a.err) &&
+                     !*(volatile int32_t *)&sm.abort;
+            if (!ok) break;
+            mbar_arrive_expect_tx(&sm.q_full[slot], kTileBytes);
+            for (int dh = 0; dh < 2; ++dh)
+                tma_load_3d(sm.q[slot] + dh * kHalfBytes, tq, dh * 64, 2 * b.hp + x, b.row0, &sm.q_full[slot]);
+            ++issued;
+        }
+        if (!ok) {
+            sm.abort = 1;
+            break;
+        }
+        w.next(a, pairs);
+    }
+    // drain: never leave copies landing in shared memory after the CTA ends
+    for (int32_t i = max(0, issued - kQBufs); i < issued; ++i)
+        mbar_wait(&sm.q_full[i % kQBufs], (i / kQBufs) & 1, a.err);
+}
+
+__device__ void swa_load_kv(SwaSmem &sm, const CUtensorMap *tk, const CUtensorMap *tv, const PrefillArgs &a,
+                            int32_t pairs) {
+    prefetch_tmap(tk);
+    prefetch_tmap(tv);
+    SwaWalk w;
+    w.start(a, sm, pairs);
+    TileRing ring;
+    ring.init();
+    int32_t issued = 0;
+    bool ok = true;
+    for (int32_t ub = 0; ok && ub < sm.n_units; ++ub) {
+        const SwaBlock b = swa_block(w, a, pairs);
+        const int64_t lo_id = b.tile_base + b.lo, hi_id = b.tile_base + b.hi;
+        const int32_t *btrow = a.bt + (int64_t)b.s * a.bt_stride;
+        for (int32_t t = b.lo; ok && t <= b.hi; ++t) {
+            if (ring.find(b.tile_base + t) >= 0) continue;  // still in the ring
+            const int32_t k = ring.place(b.tile_base + t, lo_id, hi_id);
+            for (int kv = 0; kv < 2; ++kv) {
+                const int32_t i = k + kv;
+                const int slot = i % kSlots;
+                if (i >= kSlots)
+                    ok = mbar_wait(&sm.kv_empty[slot], ((i / kSlots) + 1) & 1, a.err) &&
+                         !*(volatile int32_t *)&sm.abort;
+                if (!ok) break;
+                const CUtensorMap *map = kv ? tv : tk;
+                mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
+                for (int pg = 0; pg < 2; ++pg) {
+                    // pages outside the block's view (older window pages,
+                    // possibly released, or past the sequence) fill with zeros
+                    const int32_t lp = t * 2 + pg;
+                    int32_t row = a.kv_rows;
+                    if (lp >= b.first_page && lp <= b.last_page) {
+                        const int32_t page = lp < a.bt_stride ? btrow[lp] : -1;
+                        if (page >= 0 && page < a.num_pages)
+                            row = (page * a.hkv + b.g) * kP;
+                        else
+                            set_error(a.err, HSWA_ERR_BOUNDS);
+                    }
+                    for (int dh = 0; dh < 2; ++dh)
+                        tma_load_2d(sm.kv[slot] + dh * kHalfBytes + pg * kBoxBytes, map, dh * 64, row,
+                                    &sm.kv_full[slot]);
+                }
+                ++issued;
+            }
+        }
+        w.next(a, pairs);
+    }
+    if (!ok) sm.abort = 1;
+    for (int32_t i = max(0, issued - kSlots); i < issued; ++i)
+        mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err);
+}
+
+template <bool kF16>
+__device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs) {
+    const uint32_t tbase = sm.tmem_base;
+    const uint32_t ts0 = tbase, ts1 = tbase + 128, to0 = tbase + 256, to1 = tbase + 384;
+    SwaWalk w;
+    w.start(a, sm, pairs);
+    TileRing ring;
+    ring.init();
+    int32_t tcount = 0;  // S tiles so far (per head): the s_full / p_full phase
+    bool ok = true;
+    auto wait_kv = [&](int32_t i) { return mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err); };
+    for (int32_t ub = 0; ok && ub < sm.n_units; ++ub) {
+        const SwaBlock b = swa_block(w, a, pairs);
+        SwaWalk nw = w;
+        nw.next(a, pairs);
+        // tiles the next unit needs stay in the ring after this one
+        int64_t keep_lo = 0, keep_hi = -1;
+        if (ub + 1 < sm.n_units && nw.left > 0) {
+            const SwaBlock nb = swa_block(nw, a, pairs);
+            keep_lo = nb.tile_base + nb.lo;
+            keep_hi = nb.tile_base + nb.hi;
+        }
+        const int64_t lo_id = b.tile_base + b.lo, hi_id = b.tile_base + b.hi;
+        const int n_t = b.hi - b.lo + 1;  // 1 or 2
+        // load index of each tile's K (its V is the next load); a tile
+        // loaded for this unit is waited for at its first use
+        int32_t k0 = ring.find(lo_id), k1 = -1;
+        const bool fresh0 = k0 < 0;
+        if (fresh0) k0 = ring.place(lo_id, lo_id, hi_id);
+        bool fresh1 = false;
+        if (n_t > 1) {
+            k1 = ring.find(hi_id);
+            fresh1 = k1 < 0;
+            if (fresh1) k1 = ring.place(hi_id, lo_id, hi_id);
+        }
+        const int32_t qa = 2 * ub, qb = qa + 1, sa = qa % kQBufs, sb = qb % kQBufs;
+        const uint64_t qd0 = sdesc(smem_u32(sm.q[sa]), 16, 1024), qd1 = sdesc(smem_u32(sm.q[sb]), 16, 1024);
+        // S of the first tile for both heads
+        ok = (!fresh0 || wait_kv(k0)) && mbar_wait(&sm.q_full[sa], (qa / kQBufs) & 1, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        uint64_t kd = sdesc(smem_u32(sm.kv[k0 % kSlots]), 16, 1024);
+        issue_s<kF16>(ts0, qd0, kd);
+        mma_commit(&sm.s_full[0]);
+        if (n_t == 1) mma_commit(&sm.q_empty[sa]);
+        ok = mbar_wait(&sm.q_full[sb], (qb / kQBufs) & 1, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s<kF16>(ts1, qd1, kd);
+        mma_commit(&sm.s_full[1]);
+        if (n_t == 1) mma_commit(&sm.q_empty[sb]);
+        if (!(lo_id >= keep_lo && lo_id <= keep_hi)) mma_commit(&sm.kv_empty[k0 % kSlots]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (j >= n_t) break;
+            const int64_t tid = lo_id + j;
+            const int32_t kj = j ? k1 : k0;
+            const bool fresh = j ? fresh1 : fresh0;
+            ok = (!fresh || wait_kv(kj + 1)) && mbar_wait(&sm.p_full[0], tcount & 1, a.err) &&
+                 !*(volatile int32_t *)&sm.abort;
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t vd = sdesc(smem_u32(sm.kv[(kj + 1) % kSlots]), kHalfBytes, 1024);
+            issue_pv<kF16>(to0, ts0, vd, j == 0);
+            const bool more = j + 1 < n_t;  // only for j == 0
+            if (!more) mma_commit(&sm.o_final[0]);  // head A's O is final once this completes
+            if (more) {
+                ok = !fresh1 || wait_kv(k1);
+                if (!ok) break;
+                tc_fence_after();
+                kd = sdesc(smem_u32(sm.kv[k1 % kSlots]), 16, 1024);
+                issue_s<kF16>(ts0, qd0, kd);
+                mma_commit(&sm.s_full[0]);
+                mma_commit(&sm.q_empty[sa]);
+            }
+            ok = mbar_wait(&sm.p_full[1], tcount & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv<kF16>(to1, ts1, vd, j == 0);
+            if (!more) mma_commit(&sm.o_final[1]);
+            if (!(tid >= keep_lo && tid <= keep_hi)) mma_commit(&sm.kv_empty[(kj + 1) % kSlots]);
+            if (more) {
+                issue_s<kF16>(ts1, qd1, kd);
+                mma_commit(&sm.s_full[1]);
+                mma_commit(&sm.q_empty[sb]);
+                if (!(hi_id >= keep_lo && hi_id <= keep_hi)) mma_commit(&sm.kv_empty[k1 % kSlots]);
+            }
+            ++tcount;
+        }
+        if (!ok) break;
+        w = nw;
+    }
+    if (!ok) sm.abort = 1;
+    // every MMA issued above has completed before the TMEM is freed
+    mma_commit(&sm.mma_done);
+    mbar_wait(&sm.mma_done, 0, a.err);
+}
+
+template <bool kF16>
+__device__ void swa_softmax(SwaSmem &sm, const CUtensorMap *to, const PrefillArgs &a, int x) {
+    const int warp = (threadIdx.x >> 5) & 3;
+    const int r = warp * 32 + (threadIdx.x & 31);  // query row of this thread
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_s = sm.tmem_base + lane_off + 128 * x;  // O of the head sits 256 columns on
+    uint8_t *stage = sm.ostage[threadIdx.x >> 5];
+    int32_t tcount = 0;
+    for (int32_t ub = 0; ub < sm.n_units; ++ub) {
+        const int dslot = ub % kDescs;
+        bool ok = mbar_wait(&sm.desc_full[dslot], (ub / kDescs) & 1, a.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+            sm.abort = 1;
+            break;
+        }
+        // the slot stays ours until this unit's O is stored, so fields
+        // needed only then are read then
+        const SwaDesc &d = sm.desc[dslot];
+        const int32_t lo = d.lo, hi = d.hi;
+        const int32_t last = d.n_rows - 1;  // rows past the block repeat its last row
+        const int32_t t = d.p0 + min(r, last);
+        const int32_t t_first = d.p0 + min(warp * 32, last), t_last = d.p0 + min(warp * 32 + 31, last);
+        float m_used = -INFINITY, l = 0.f;
+        for (int32_t tile = lo; tile <= hi; ++tile, ++tcount) {
+            // S of this tile: the MMA thread writes the next S only after
+            // this tile's P has been read, so the wait is never two phases
+            // behind
+            ok = mbar_wait(&sm.s_full[x], tcount & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            softmax_tile_band<kF16>(t_s, t_s + 256, tile * kBN, t, t_first, t_last, a.window, a.scale_log2,
+                                    tile == lo, m_used, l);
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[x]);
+        }
+        const bool fin = ok && mbar_wait(&sm.o_final[x], ub & 1, a.err);
+        if (!__all_sync(0xffffffffu, fin)) {
+            sm.abort = 1;
+            break;
+        }
+        tc_fence_after();
+        // O is read before this thread reports the next tile's P, and the
+        // first PV of the next unit (which overwrites O) waits for that P
+        const int32_t h = 2 * d.hp + x;
+        store_o_rows_staged(t_s + 256, l, stage, to, h, d.row0 + warp * 32, warp * 32 + 31 <= last,
+                            a.o + ((int64_t)(d.row0 + r) * a.hq + h) * kD, r <= last);
+        mbar_arrive(&sm.desc_empty[dslot]);
+    }
+    // the TMA stores are complete before the CTA ends
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    __syncwarp();
+}
+
+template <bool kF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_swa_tc_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                        PrefillArgs a) {
+    extern __shared__ uint8_t raw[];
+    SwaSmem &sm = *reinterpret_cast<SwaSmem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int32_t pairs = (a.hq / a.hkv) / 2;
+    if (warp == 0) swa_partition(sm, a, pairs);
+    __syncthreads();
+    if (sm.n_units == 0) return;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kQBufs; ++i) {
+            mbar_init(&sm.q_full[i], 1);
+            mbar_init(&sm.q_empty[i], 1);
+        }
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&sm.kv_full[i], 1);
+            mbar_init(&sm.kv_empty[i], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&sm.s_full[x], 1);
+            mbar_init(&sm.p_full[x], 128);
+            mbar_init(&sm.o_final[x], 1);
+        }
+        mbar_init(&sm.mma_done, 1);
+        for (int i = 0; i < kDescs; ++i) {
+            mbar_init(&sm.desc_full[i], 1);
+            mbar_init(&sm.desc_empty[i], 256);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 9) tmem_alloc<512>(&sm.tmem_base);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp < 8) {
+        swa_softmax<kF16>(sm, &to, a, warp >> 2);
+    } else if (warp == 8) {
+        const int lane = threadIdx.x & 31;
+        if (lane == 0)
+            swa_load_q(sm, &tq, a, pairs);
+        else if (lane == 1)
+            swa_load_kv(sm, &tk, &tv, a, pairs);
+        __syncwarp();
+    } else {
+        if ((threadIdx.x & 31) == 0) swa_mma<kF16>(sm, a, pairs);
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_free<512>(sm.tmem_base);
 }
 
 bool prefill_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q, const void *o) {
@@ -567,7 +1247,7 @@ int launch_prefill_tc(const hswa_config &c, int32_t window, const void *k_pool, 
     if (!make_tmap_3d(&tq, q, kD, c.n_q_heads, (uint64_t)total_q, 64, 1, kBM, ty, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tk, k_pool, rows, kD, kP, 64, ty, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tv, v_pool, rows, kD, kP, 64, ty, CU_TENSOR_MAP_SWIZZLE_128B))
-        return HSWA_ERR_CUDA;
+        return cuda_fail(cudaErrorInvalidValue, "prefill tensor maps");
     PrefillArgs a;
     a.bt = bt;
     a.prefix = d_prefix_len;
@@ -584,19 +1264,47 @@ int launch_prefill_tc(const hswa_config &c, int32_t window, const void *k_pool, 
     a.err = error_word();
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(prefill_tc_bf16_d128<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPrefillSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_tc_bf16_d128<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPrefillSmemBytes) != cudaSuccess)
-            return HSWA_ERR_CUDA;
+        cudaError_t e;
+        if ((e = cudaFuncSetAttribute(prefill_tc_bf16_d128<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kPrefillSmemBytes)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prefill_tc_bf16_d128<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kPrefillSmemBytes)) != cudaSuccess)
+            return cuda_fail(e, "prefill_tc_bf16_d128 shared memory");
+        if ((e = cudaFuncSetAttribute(prefill_swa_tc_d128<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSwaSmemBytes)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prefill_swa_tc_d128<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSwaSmemBytes)) != cudaSuccess)
+            return cuda_fail(e, "prefill_swa_tc_d128 shared memory");
         attr = true;
     }
-    dim3 grid(c.n_q_heads / 2, (max_q_len + kBM - 1) / kBM, n_seqs);
+    if (window > 0 && window <= kBN) {
+        // at most two key tiles per block: the persistent window kernel
+        const int sms = sm_count();
+        if (sms <= 0) return HSWA_ERR_CUDA;
+        CUtensorMap to;
+        if (!make_tmap_3d(&to, o, kD, c.n_q_heads, (uint64_t)total_q, 64, 1, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return cuda_fail(cudaErrorInvalidValue, "prefill output tensor map");
+        const int64_t units = (int64_t)n_seqs * ((max_q_len + kBM - 1) / kBM + 1) * (c.n_q_heads / 2);
+        const dim3 grid((unsigned)std::min<int64_t>(sms, units));
+        if (f16)
+            prefill_swa_tc_d128<true><<<grid, kThreads, kSwaSmemBytes, st>>>(tq, tk, tv, to, a);
+        else
+            prefill_swa_tc_d128<false><<<grid, kThreads, kSwaSmemBytes, st>>>(tq, tk, tv, to, a);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? HSWA_OK : cuda_fail(e, "prefill_swa_tc_d128 launch");
+    }
+    a.nqb = (max_q_len + kBM - 1) / kBM;
+    a.lpt = n_seqs <= kLptMaxSeqs;
+    const int64_t units = (int64_t)n_seqs * a.nqb * (c.n_q_heads / 2);
+    if (units >= (1ll << 31)) return HSWA_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)units);
     if (f16)
         prefill_tc_bf16_d128<true><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
     else
         prefill_tc_bf16_d128<false><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
-    return cudaGetLastError() == cudaSuccess ? HSWA_OK : HSWA_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? HSWA_OK : cuda_fail(e, "prefill_tc_bf16_d128 launch");
 }
 
 }  // namespace
@@ -615,6 +1323,7 @@ extern "C" int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *la
                                      const int32_t *d_bt, const int32_t *d_prefix_len, const int32_t *d_q_start,
                                      int n_seqs, int total_q, int max_q_len, float scale, void *ws, size_t ws_bytes,
                                      hswa_stream_t stream) {
+    HSWA_NVTX("hswa_prefill_chunk_ws");
     if (!pool || !layer || n_seqs < 0 || n_seqs > pool->cfg.max_seqs || max_q_len < 0 || total_q < 0 ||
         !(scale > 0.f) ||
         (n_seqs > 0 && max_q_len > total_q) ||
@@ -658,7 +1367,8 @@ extern "C" int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *la
         sa.err = error_word();
         __half *q16 = reinterpret_cast<__half *>(base + l.q_off);
         const int64_t n8 = (int64_t)total_q * c.n_q_heads * kD / 8;
-        set_last_kernel("prefill_stage_fp8+prefill_tc_bf16_d128<f16>");
+        set_last_kernel(window > 0 && window <= kBN ? "prefill_stage_fp8+prefill_swa_tc_d128<f16>"
+                                                     : "prefill_stage_fp8+prefill_tc_bf16_d128<f16>");
         prefill_stage_fp8<<<dim3(c.max_pages_per_seq, n_seqs), 256, 0, st>>>(sa);
         prefill_q_to_f16<<<(int)std::min<int64_t>((n8 + 255) / 256, 4096), 256, 0, st>>>(
             static_cast<const __nv_bfloat16 *>(q), q16, n8);
@@ -669,7 +1379,7 @@ extern "C" int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *la
     if (!prefill_fast_ok(pool, layer, q, o))
         return launch_attention_generic(pool, layer, q, o, d_bt, nullptr, d_prefix_len, d_q_start, max_q_len,
                                         n_seqs, scale, 1, st);
-    set_last_kernel("prefill_tc_bf16_d128");
+    set_last_kernel(window > 0 && window <= kBN ? "prefill_swa_tc_d128" : "prefill_tc_bf16_d128");
     return launch_prefill_tc(c, window, layer->k_pool, layer->v_pool, false, num_pages, d_bt, q, o, d_prefix_len,
                              d_q_start, n_seqs, total_q, max_q_len, scale, st);
 }

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -20,6 +21,7 @@ int *g_err_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 std::mutex g_mu;
 thread_local const char *g_last_kernel = "";
+thread_local const char *g_last_cuda_error = "";
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int current_device() {
@@ -54,6 +56,13 @@ int sm_count() {
 }
 
 void set_last_kernel(const char *name) { g_last_kernel = name; }
+
+int cuda_fail(cudaError_t e, const char *where) {
+    static thread_local char buf[256];
+    snprintf(buf, sizeof(buf), "%s: %s", where, cudaGetErrorString(e));
+    g_last_cuda_error = buf;
+    return HSWA_ERR_CUDA;
+}
 
 static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -235,3 +244,5 @@ extern "C" int hswa_check(hswa_stream_t stream) {
 }
 
 extern "C" const char *hswa_last_kernel(void) { return g_last_kernel; }
+
+extern "C" const char *hswa_last_cuda_error(void) { return g_last_cuda_error; }

@@ -485,6 +485,10 @@ int hswa_selftest_bounded_wait(hswa_stream_t stream);
  * launched (e.g. "decode_mma_bf16_d128"); "" before any launch. */
 const char *hswa_last_kernel(void);
 
+/* The CUDA error behind the last HSWA_ERR_CUDA a launch path on this host
+ * thread returned ("where: message"), "" if none has been recorded. */
+const char *hswa_last_cuda_error(void);
+
 /* Human-readable name of a status code. */
 const char *hswa_status_string(int status);
 

@@ -144,6 +144,13 @@ def window_offsets(sess, layer, lens, W):
     return off, nbytes
 
 
+def prefill_kernel(kind, window, fp8=False):
+    """Name hswa_last_kernel reports after a tensor-core prefill of this
+    layer kind: SWA layers with W <= 128 run the persistent window kernel."""
+    name = "prefill_swa_tc_d128" if kind == wl.KIND_SWA and 0 < window <= 128 else "prefill_tc_bf16_d128"
+    return "prefill_stage_fp8+%s<f16>" % name if fp8 else name
+
+
 def max_err(got, exp):
     return float(np.abs(got.astype(np.float64) - exp).max()) if exp.size else 0.0
 

@@ -16,7 +16,7 @@ import hswa_workloads as wl
 import oracle
 import hybrid_sliding_window_dual_gb300 as H
 from hybrid_sliding_window_dual_gb300.session import DualPoolSession
-from scenario import raw_host
+from scenario import prefill_kernel, raw_host
 
 FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
 HQ, HKV, D, P, W = 64, 8, 128, 64, 128
@@ -149,7 +149,7 @@ def test_fp8_prefill_chunk_matches_oracle(swa_first):
         o = torch.full((n_tot, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
         c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, max(chunk), scale)
         assert c.sess.check() == 0
-        assert H.hswa_last_kernel() == "prefill_stage_fp8+prefill_tc_bf16_d128<f16>"
+        assert H.hswa_last_kernel() == prefill_kernel(kind, 0 if kind == FULL else W, fp8=True)
         kc, ks, vc, vs = c.host[layer]
         oracle.append_kv_fp8(kc, ks, vc, vs, kn.float().numpy(), vn.float().numpy(), slots)
         assert np.array_equal(c.sess.k[layer].cpu().numpy(), kc)
@@ -375,7 +375,7 @@ def test_fp8_chunked_prefill_full_size_sampled():
         o = torch.full((B * C, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
         c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, C, scale)
         assert c.sess.check() == 0
-        assert H.hswa_last_kernel() == "prefill_stage_fp8+prefill_tc_bf16_d128<f16>"
+        assert H.hswa_last_kernel() == prefill_kernel(kind, 0 if kind == FULL else W, fp8=True)
         kc, ks, vc, vs = (x.cpu().numpy() for x in (c.sess.k[layer], c.sess.ks[layer], c.sess.v[layer],
                                                      c.sess.vs[layer]))
         exp = oracle.attention_fp8(raw_host(q)[rows], kc, ks, vc, vs, c.table(layer), q_seq, q_pos,

@@ -12,14 +12,15 @@ import torch
 import hswa_workloads as wl
 import oracle
 import hybrid_sliding_window_dual_gb300 as H
-from scenario import Scenario, TOL, device_out, max_err, raw_host
+from scenario import Scenario, TOL, device_out, max_err, prefill_kernel, raw_host
 
 FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
 
 
-def run_prefill_chunk(sc, chunk, seed, row_samples=None, expect_kernel=None):
+def run_prefill_chunk(sc, chunk, seed, row_samples=None, expect_kernel=False):
     """chunk[s] new tokens for sequence s. row_samples: per-sequence list of
-    chunk rows to check (None = all)."""
+    chunk rows to check (None = all). expect_kernel: check that each layer
+    ran the tensor-core kernel of its kind."""
     B = len(sc.cached)
     prefix = sc.ora.seq_len[:B].copy()
     chunk = np.asarray(chunk, np.int64)
@@ -44,7 +45,7 @@ def run_prefill_chunk(sc, chunk, seed, row_samples=None, expect_kernel=None):
         sc.sess.prefill(layer, qd, o, d_prefix, d_qs, B, int(chunk.max()) if B else 0, sc.scale)
         assert sc.sess.check() == 0
         if expect_kernel:
-            assert H.hswa_last_kernel() == expect_kernel
+            assert H.hswa_last_kernel() == prefill_kernel(kind, sc.window(layer))
         sc.oracle_append(snap, slots, (raw_host(kn), raw_host(vn)), sc.P)
         rows, q_seq, q_pos = [], [], []
         for s in range(B):
@@ -104,7 +105,7 @@ def test_prefill_fast_path_dispatch_and_window_wider_than_chunk():
     """Tile-aligned and unaligned prefixes around the window edge."""
     cached = [127, 128, 255, 256, 60]
     sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=14, extra_tokens=400)
-    run_prefill_chunk(sc, [128, 129, 1, 256, 300], seed=3, expect_kernel="prefill_tc_bf16_d128")
+    run_prefill_chunk(sc, [128, 129, 1, 256, 300], seed=3, expect_kernel=True)
 
 
 @pytest.mark.gpu
@@ -115,7 +116,7 @@ def test_prefill_query_heads_per_kv_head(hq, hkv):
     kernel. Ragged chunks and prefixes, Full and SWA layer."""
     cached = [0, 70, 1000, 129]
     sc = Scenario(hq, hkv, 128, 64, 128, wl.DTYPE_BF16, cached, seed=17, extra_tokens=600)
-    run_prefill_chunk(sc, [300, 1, 513, 129], seed=6, expect_kernel="prefill_tc_bf16_d128")
+    run_prefill_chunk(sc, [300, 1, 513, 129], seed=6, expect_kernel=True)
 
 
 @pytest.mark.gpu
@@ -129,7 +130,7 @@ def test_chunked_prefill_full_size_sampled():
                   extra_tokens=w.n_new + 64)
     rows = [0, 1, 127, 128, 129, 1000, 2047, 4094, 4095]
     run_prefill_chunk(sc, [w.n_new] * len(w.cached), seed=77, row_samples=[rows] * len(w.cached),
-                      expect_kernel="prefill_tc_bf16_d128")
+                      expect_kernel=True)
 
 
 @pytest.mark.gpu
@@ -140,7 +141,34 @@ def test_prefill_swa_after_release_reads_only_live_pages():
     cached = [1000, 777, 130, 2049]
     sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, seed=15, chunk=100, extra_tokens=600)
     assert (sc.ora.swa_bt[:, :10] < 0).any()
-    run_prefill_chunk(sc, [200, 129, 64, 500], seed=4, expect_kernel="prefill_tc_bf16_d128")
+    run_prefill_chunk(sc, [200, 129, 64, 500], seed=4, expect_kernel=True)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("W", [1, 40, 127, 128, 129])
+def test_prefill_swa_windows_many_sequences(W):
+    """SWA windows around the two-key-tile limit of the persistent window
+    kernel (W <= 128 runs it, W = 129 the general kernel), over 40 sequences
+    with ragged chunks (some empty) and prefixes, so that the CTAs' shares of
+    the unit list start and end inside (sequence, kv head, block) groups and
+    K / V tiles are reused across head pairs and blocks; every row against
+    the oracle."""
+    rng = np.random.default_rng(100 + W)
+    cached = [int(x) for x in rng.integers(0, 3000, size=40)]
+    chunk = [int(x) for x in rng.integers(0, 400, size=40)]
+    chunk[3] = 0
+    sc = Scenario(16, 2, 128, 64, W, wl.DTYPE_BF16, cached, layer_kinds=(SWA,), seed=18, extra_tokens=420)
+    run_prefill_chunk(sc, chunk, seed=8, expect_kernel=True)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cached,chunk", [([1000], [5]), ([0], [1]), ([127], [130]), ([300, 0], [0, 700])])
+def test_prefill_swa_few_units(cached, chunk):
+    """Chunks so small that most CTAs of the persistent window kernel get no
+    unit; a chunk inside one block, one from position 0, one crossing a
+    block edge, an empty chunk next to a long one."""
+    sc = Scenario(64, 8, 128, 64, 128, wl.DTYPE_BF16, cached, layer_kinds=(SWA,), seed=19, extra_tokens=720)
+    run_prefill_chunk(sc, chunk, seed=9, expect_kernel=True)
 
 
 @pytest.mark.gpu

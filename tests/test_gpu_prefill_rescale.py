@@ -1,8 +1,10 @@
 """The tensor-core prefill's lazy O rescale, forced on purpose, against the
 float64 oracle on every output row.
 
-prefill_tc_bf16_d128 keeps a running reference max per query row and rescales
-O (in tensor memory) only when a key tile's max exceeds it by more than 2^8.
+The tensor-core prefill kernels (prefill_tc_bf16_d128 for Full layers,
+prefill_swa_tc_d128 for SWA layers) keep a running reference max per query
+row and rescale O (in tensor memory) only when a key tile's max exceeds it by
+more than 2^8.
 With N(0, 1) data that almost never happens, so these inputs steer every
 score: each query's first coordinate is fixed at 8 and each key's first
 coordinate is set so that its score sits on a chosen level (in log2 units,
@@ -35,7 +37,7 @@ import hswa_workloads as wl
 import oracle
 import hybrid_sliding_window_dual_gb300 as H
 from hybrid_sliding_window_dual_gb300.session import DualPoolSession
-from scenario import raw_host
+from scenario import prefill_kernel, raw_host
 
 FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
 HQ, HKV, D, P, W = 16, 2, 128, 64, 128
@@ -215,8 +217,7 @@ def test_prefill_lazy_rescale_fires_and_matches_oracle(fp8):
         o = torch.full((T, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
         c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, max(CHUNK), SCALE)
         assert c.sess.check() == 0
-        assert H.hswa_last_kernel() == ("prefill_stage_fp8+prefill_tc_bf16_d128<f16>" if fp8
-                                        else "prefill_tc_bf16_d128")
+        assert H.hswa_last_kernel() == prefill_kernel(kind, 0 if kind == FULL else W, fp8=bool(fp8))
         exp = c.expected(kind, q, q_seq, q_pos)
         got = o.float().cpu().numpy().astype(np.float64)
         assert np.isfinite(got).all()

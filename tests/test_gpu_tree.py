@@ -19,7 +19,7 @@ import oracle
 from oracle import prefix_tree as PT
 import hybrid_sliding_window_dual_gb300 as H
 from hybrid_sliding_window_dual_gb300.session import DualPoolSession
-from scenario import TOL, device_out, max_err, raw_host
+from scenario import TOL, device_out, max_err, prefill_kernel, raw_host
 
 FULL, SWA = wl.KIND_FULL, wl.KIND_SWA
 HQ, HKV, D, P, W = 64, 8, 128, 64, 128
@@ -74,7 +74,7 @@ class Case:
             assert self.sess.check() == 0
             if not check:
                 continue
-            assert H.hswa_last_kernel() == "prefill_tc_bf16_d128"
+            assert H.hswa_last_kernel() == prefill_kernel(kind, 0 if kind == FULL else W)
             bt = self.ora.full_bt if kind == FULL else self.ora.swa_bt
             exp = oracle.attention(raw_host(q), raw_host(self.sess.k[layer]), raw_host(self.sess.v[layer]), bt,
                                    np.full(n, s), np.arange(prefix, prefix + n), 0 if kind == FULL else W,
