@@ -261,11 +261,25 @@ def measure_decode_multi(reps, w, token_counts=(1, 2, 3, 4, 8, 16), fp8=False):
 
 
 def prefill_flops(w, prefix, chunk):
-    """Valid (query, key) pairs x 4 d Hq for a Full and an SWA layer."""
+    """Valid (query, key) pairs x 4 d Hq for a Full and an SWA layer, and the
+    pairs the tensor-core kernels execute: 128 query rows x 128 keys per key
+    tile of a block. Full-layer blocks are 128 chunk rows from the prefix and
+    read key tiles [0, last row]; SWA blocks (W <= 128) sit on 128-position
+    boundaries and read the tiles from their first row's window start."""
     full = sum(c * p + c * (c + 1) // 2 for p, c in zip(prefix, chunk))
     swa = sum(sum(min(p + r + 1, w.window) for r in range(c)) for p, c in zip(prefix, chunk))
+    full_exec = swa_exec = 0
+    for p, c in zip(prefix, chunk):
+        for qb in range((c + 127) // 128):
+            last = p + min(c, 128 * (qb + 1)) - 1
+            full_exec += (last // 128 + 1) * 128 * 128
+        if c > 0:
+            for m in range(p // 128, (p + c - 1) // 128 + 1):
+                p0 = max(p, 128 * m)
+                swa_exec += (m - max(0, p0 - w.window + 1) // 128 + 1) * 128 * 128
     k = 4 * w.head_dim * w.n_q_heads
-    return {"full": k * full, "swa": k * swa, "step": k * (full + swa)}
+    return {"full": k * full, "swa": k * swa, "step": k * (full + swa), "full_exec": k * full_exec,
+            "swa_exec": k * swa_exec}
 
 
 class DecodeBatch:
@@ -566,8 +580,10 @@ class ChunkedPrefill:
         self.o = [torch.empty(T, w.n_q_heads, w.head_dim, dtype=dt, device="cuda") for _ in range(2)]
         self.d_prefix = torch.as_tensor(self.prefix.astype(np.int32), device="cuda")
         self.d_qs = torch.arange(0, T + 1, C, dtype=torch.int32, device="cuda")
+        self.q_start_host = np.arange(0, T + 1, C)
         self.scale = 1.0 / math.sqrt(w.head_dim)
         self.events = [[], []]
+        self.kernels = ["", ""]
         self.launches = 0
         torch.cuda.synchronize()
 
@@ -576,13 +592,16 @@ class ChunkedPrefill:
 
     def step(self, timed=False):
         torch = self.torch
+        from hybrid_sliding_window_dual_gb300 import hswa_last_kernel
         with torch.cuda.stream(self.stream):
             for i in range(2):
                 self.sess.append(i, self.kn[i], self.vn[i], self.slots[i])
                 if timed:
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(self.stream)
-                self.sess.prefill(i, self.q[i], self.o[i], self.d_prefix, self.d_qs, self.B, self.C, self.scale)
+                self.sess.prefill(i, self.q[i], self.o[i], self.d_prefix, self.d_qs, self.B, self.C, self.scale,
+                                  prefix_host=self.prefix, q_start_host=self.q_start_host)
+                self.kernels[i] = hswa_last_kernel()
                 if timed:
                     e1.record(self.stream)
                     self.events[i].append((e0, e1))
@@ -615,10 +634,12 @@ def measure_prefill(steps, warmup, w, fp8=False):
     full_ms = float(np.mean([a.elapsed_time(b) for a, b in pb.events[0]]))
     swa_ms = float(np.mean([a.elapsed_time(b) for a, b in pb.events[1]]))
     pb.finish()
-    from hybrid_sliding_window_dual_gb300 import hswa_last_kernel
-    return {"kernel": hswa_last_kernel(), "step_tflops": f["step"] * steps / secs / 1e12, "ms_per_step": secs / steps * 1e3,
+    return {"kernel": pb.kernels[0], "swa_kernel": pb.kernels[1],
+            "step_tflops": f["step"] * steps / secs / 1e12, "ms_per_step": secs / steps * 1e3,
             "full_tflops": f["full"] / (full_ms / 1e3) / 1e12, "full_ms": full_ms,
+            "full_exec_tflops": f["full_exec"] / (full_ms / 1e3) / 1e12,
             "swa_tflops": f["swa"] / (swa_ms / 1e3) / 1e12, "swa_ms": swa_ms,
+            "swa_exec_tflops": f["swa_exec"] / (swa_ms / 1e3) / 1e12,
             "valid_tflop_per_step": f["step"] / 1e12, "tokens_per_s": pb.T * steps / secs,
             "launches": pb.launches}
 
@@ -1064,10 +1085,13 @@ def run_decode(args, world, rank, local):
             "frac_of_sustained": round(pf["step_tflops"] / bf16_sus, 4), "peak_sustained": bf16_sus,
             "full_layer_frac": round(pf["full_tflops"] / bf16, 4),
             "full_layer_tflops": round(pf["full_tflops"], 1), "full_layer_ms": round(pf["full_ms"], 3),
+            "full_layer_exec_tflops": round(pf["full_exec_tflops"], 1),
             "swa_layer_tflops": round(pf["swa_tflops"], 2), "swa_layer_ms": round(pf["swa_ms"], 3),
+            "swa_layer_exec_tflops": round(pf["swa_exec_tflops"], 2),
+            "swa_layer_frac": round(pf["swa_tflops"] / bf16, 4),
             "valid_tflop_per_step": round(pf["valid_tflop_per_step"], 3),
             "ms_per_step": round(pf["ms_per_step"], 3), "tokens_per_s": round(pf["tokens_per_s"], 1),
-            "kernel": pf["kernel"]}
+            "kernel": pf["kernel"], "swa_kernel": pf["swa_kernel"]}
         if not args.no_fp8:
             del pf
             torch.cuda.empty_cache()
@@ -1432,7 +1456,8 @@ def run_prefill_line(args, world, rank, local):
                      "unit": "TFLOP/s", "frac": round(pf["full_tflops"] / bf16, 4), "traffic": None,
                      "kernel": pf["kernel"] + " (Full layer)", "peak_source": kind + " burst",
                      "frac_of_sustained": round(pf["full_tflops"] / bf16_sus, 4)},
-        "swa_layer_tflops": round(pf["swa_tflops"], 2),
+        "swa_layer_tflops": round(pf["swa_tflops"], 2), "swa_layer_exec_tflops": round(pf["swa_exec_tflops"], 2),
+        "swa_kernel": pf["swa_kernel"],
         "gpu_launches": 4 * args.steps,
         "clocks": clock_info,
         "tokens_per_s": round(world * pf["tokens_per_s"], 1),

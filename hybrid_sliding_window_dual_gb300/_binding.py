@@ -91,6 +91,7 @@ _SIG = {
     "hswa_prefill_chunk": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I, _I,
                                 ctypes.c_float, _P]),
     "hswa_prefill_workspace_size": (ctypes.c_size_t, [_P, ctypes.POINTER(Layer), _I, _I]),
+    "hswa_prefill_workspace_size_exact": (ctypes.c_size_t, [_P, ctypes.POINTER(Layer), _I, _P, _P]),
     "hswa_prefill_chunk_ws": (_I, [_P, ctypes.POINTER(Layer), _P, _P, _P, _P, _P, _I, _I, _I,
                                    ctypes.c_float, _P, ctypes.c_size_t, _P]),
     "hswa_swa_window_offsets": (_I, [_P, ctypes.POINTER(Layer), _I, _P, _P, _P]),
@@ -335,6 +336,14 @@ def hswa_prefill_chunk(pool, layer: Layer, q, o, d_bt, d_prefix_len, d_q_start, 
 
 def hswa_prefill_workspace_size(pool, layer: Layer, n_seqs, max_q_len):
     return int(lib.hswa_prefill_workspace_size(pool, ctypes.byref(layer), int(n_seqs), int(max_q_len)))
+
+
+def hswa_prefill_workspace_size_exact(pool, layer: Layer, prefix_len, q_start):
+    pre = np.ascontiguousarray(prefix_len, np.int32)
+    qs = np.ascontiguousarray(q_start, np.int32)
+    if qs.shape != (pre.size + 1,):
+        raise ValueError("q_start must hold len(prefix_len) + 1 offsets")
+    return int(lib.hswa_prefill_workspace_size_exact(pool, ctypes.byref(layer), int(pre.size), _ptr(pre), _ptr(qs)))
 
 
 def hswa_prefill_chunk_ws(pool, layer: Layer, q, o, d_bt, d_prefix_len, d_q_start, n_seqs, total_q, max_q_len,

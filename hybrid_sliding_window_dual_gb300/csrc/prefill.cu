@@ -1105,34 +1105,52 @@ bool prefill_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void 
 }
 
 // ------------------------------------------------------------ FP8 staging
-// Pages per sequence the staging copy reserves: a Full layer may read every
-// logical page; an SWA layer's chunk of at most max_q_len rows reads keys
-// [prefix - W + 1, prefix + n), at most W - 1 + max_q_len keys.
+// Pages per sequence the staging copy can need at most: a Full layer may
+// read every logical page; an SWA layer's chunk of at most max_q_len rows
+// reads keys [prefix - W + 1, prefix + n), at most W - 1 + max_q_len keys.
 int32_t stage_pages_per_seq(const hswa_config &c, const hswa_layer *layer, int max_q_len) {
     if (layer->kind != HSWA_KIND_SWA) return c.max_pages_per_seq;
     const int64_t keys = (int64_t)layer->window - 1 + max_q_len;
     return (int32_t)std::min<int64_t>(c.max_pages_per_seq, (keys + kP - 1) / kP + 1);
 }
 
+// Logical pages [lo, hi] of a sequence the chunk reads (hi < lo: none):
+// keys [0, prefix + n) for a Full layer, [prefix - W + 1, prefix + n) for an
+// SWA layer.
+__host__ __device__ __forceinline__ void chunk_pages(int32_t pre, int32_t n, int32_t window, int32_t &lo,
+                                                     int32_t &hi) {
+    const int32_t lo_key = (window > 0 && pre - window + 1 > 0) ? pre - window + 1 : 0;
+    lo = lo_key / kP;
+    hi = n > 0 ? (pre + n - 1) / kP : lo - 1;
+}
+
 constexpr size_t align1k(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
-// Workspace of an FP8 chunk: the staging block table, the fp16 K and V page
-// copies, and the fp16 copy of q (n_seqs * max_q_len rows at most).
+// Workspace of an FP8 chunk: the staging block table [n_seqs][bt_stride],
+// each sequence's first page copy (a prefix sum over the pages the chunk
+// reads, [n_seqs + 1]), the fp16 copy of the q rows, then as many fp16 K
+// and V page copies as the rest holds ("capacity"), packed: sequence s's
+// pages take copies off[s] .. off[s + 1] - 1.
 struct StageLayout {
-    int32_t per_seq;
-    size_t page_bytes, k_off, v_off, q_off, total;
+    size_t page_bytes, off_off, q_off, k_off, v_off;
+    int64_t cap;
 };
 
-StageLayout stage_layout(const hswa_config &c, const hswa_layer *layer, int n_seqs, int max_q_len) {
+StageLayout stage_layout(const hswa_config &c, int n_seqs, int64_t q_rows, size_t ws_bytes) {
     StageLayout l;
-    l.per_seq = stage_pages_per_seq(c, layer, max_q_len);
     l.page_bytes = (size_t)c.n_kv_heads * kP * kD * sizeof(__half);
-    const size_t pages = (size_t)n_seqs * l.per_seq;
-    l.k_off = align1k((size_t)n_seqs * c.max_pages_per_seq * sizeof(int32_t));
-    l.v_off = l.k_off + align1k(pages * l.page_bytes);
-    l.q_off = l.v_off + align1k(pages * l.page_bytes);
-    l.total = l.q_off + align1k((size_t)n_seqs * max_q_len * c.n_q_heads * kD * sizeof(__half));
+    l.off_off = align1k((size_t)n_seqs * c.max_pages_per_seq * sizeof(int32_t));
+    l.q_off = l.off_off + align1k((size_t)(n_seqs + 1) * sizeof(int32_t));
+    l.k_off = l.q_off + align1k((size_t)q_rows * c.n_q_heads * kD * sizeof(__half));
+    l.cap = ws_bytes > l.k_off ? (int64_t)((ws_bytes - l.k_off) / (2 * l.page_bytes)) : 0;
+    l.v_off = l.k_off + (size_t)l.cap * l.page_bytes;
     return l;
+}
+
+// Bytes of a workspace holding q_rows query rows and `pages` page copies.
+size_t stage_bytes(const hswa_config &c, int n_seqs, int64_t q_rows, int64_t pages) {
+    const StageLayout l = stage_layout(c, n_seqs, q_rows, 0);
+    return l.k_off + 2 * (size_t)pages * l.page_bytes;
 }
 
 struct StageArgs {
@@ -1140,10 +1158,42 @@ struct StageArgs {
     const uint8_t *k_codes, *v_codes;  // [page][Hkv][P][d], V pages [page][Hkv][d][P]
     const float *k_scale, *v_scale;    // [page][Hkv][P] (one 128-element tile per row)
     int32_t *stage_bt;                 // [n_seqs][bt_stride]
-    __half *k_out, *v_out;             // [n_seqs * per_seq][Hkv][P][d]
-    int32_t n_seqs, bt_stride, hkv, window, num_pages, per_seq;
+    int32_t *stage_off;                // [n_seqs + 1]: first copy of each sequence
+    __half *k_out, *v_out;             // [cap][Hkv][P][d]
+    int32_t n_seqs, bt_stride, hkv, window, num_pages, cap;
     int *err;
 };
+
+// One block: stage_off = prefix sum of the pages each sequence's chunk reads.
+__global__ void __launch_bounds__(256) prefill_stage_plan(StageArgs a) {
+    __shared__ int32_t part[256];
+    const int32_t per = (a.n_seqs + 255) / 256, s0 = threadIdx.x * per;
+    int32_t sum = 0;
+    for (int32_t s = s0; s < min(a.n_seqs, s0 + per); ++s) {
+        int32_t lo, hi;
+        chunk_pages(a.prefix[s], a.q_start[s + 1] - a.q_start[s], a.window, lo, hi);
+        sum += max(0, hi - lo + 1);
+    }
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {  // 256 partial sums: a serial scan is short
+        int32_t run = 0;
+        for (int i = 0; i < 256; ++i) {
+            const int32_t v = part[i];
+            part[i] = run;
+            run += v;
+        }
+        a.stage_off[a.n_seqs] = run;
+    }
+    __syncthreads();
+    int32_t run = part[threadIdx.x];
+    for (int32_t s = s0; s < min(a.n_seqs, s0 + per); ++s) {
+        a.stage_off[s] = run;
+        int32_t lo, hi;
+        chunk_pages(a.prefix[s], a.q_start[s + 1] - a.q_start[s], a.window, lo, hi);
+        run += max(0, hi - lo + 1);
+    }
+}
 
 // fp16 of an E4M3 code (exact) times its fp32 scale, rounded once to fp16;
 // magnitudes past the fp16 range saturate at 65504.
@@ -1158,17 +1208,17 @@ __device__ __forceinline__ __half2 dequant_f16x2(uint8_t c0, uint8_t c1, float s
 // rows; each kv head's transposed V block [d][P] becomes [P][d]).
 __global__ void __launch_bounds__(256) prefill_stage_fp8(StageArgs a) {
     const int32_t j = blockIdx.x, s = blockIdx.y;
-    const int32_t pre = a.prefix[s], n = a.q_start[s + 1] - a.q_start[s];
-    const int32_t lo_key = (a.window > 0 && pre - a.window + 1 > 0) ? pre - a.window + 1 : 0;
-    const int32_t lo_pg = lo_key / kP, hi_pg = n > 0 ? (pre + n - 1) / kP : -1;
+    int32_t lo_pg, hi_pg;
+    chunk_pages(a.prefix[s], a.q_start[s + 1] - a.q_start[s], a.window, lo_pg, hi_pg);
     int32_t page = -1, slot = -1;
     if (j >= lo_pg && j <= hi_pg) {
         page = a.bt[(int64_t)s * a.bt_stride + j];
-        if (j - lo_pg >= a.per_seq) {  // the workspace was sized for fewer rows
+        const int32_t copy = a.stage_off[s] + (j - lo_pg);
+        if (copy >= a.cap) {  // the workspace holds fewer copies than the chunk reads
             if (threadIdx.x == 0) set_error(a.err, HSWA_ERR_BOUNDS);
             page = -1;
         }
-        if (page >= 0 && page < a.num_pages) slot = s * a.per_seq + (j - lo_pg);
+        if (page >= 0 && page < a.num_pages) slot = copy;
     }
     if (threadIdx.x == 0) a.stage_bt[(int64_t)s * a.bt_stride + j] = slot;  // -1: the kernel reports it if read
     if (slot < 0) return;
@@ -1316,7 +1366,24 @@ extern "C" size_t hswa_prefill_workspace_size(const hswa_pool *pool, const hswa_
                                               int max_q_len) {
     if (!pool || !layer || n_seqs < 0 || max_q_len < 0 || pool->cfg.dtype != HSWA_DTYPE_FP8_E4M3) return 0;
     if (layer->kind == HSWA_KIND_SWA && layer->window <= 0) return 0;
-    return stage_layout(pool->cfg, layer, n_seqs, max_q_len).total;
+    return stage_bytes(pool->cfg, n_seqs, (int64_t)n_seqs * max_q_len,
+                       (int64_t)n_seqs * stage_pages_per_seq(pool->cfg, layer, max_q_len));
+}
+
+extern "C" size_t hswa_prefill_workspace_size_exact(const hswa_pool *pool, const hswa_layer *layer, int n_seqs,
+                                                    const int32_t *prefix_len, const int32_t *q_start) {
+    if (!pool || !layer || n_seqs < 0 || (n_seqs > 0 && (!prefix_len || !q_start)) ||
+        pool->cfg.dtype != HSWA_DTYPE_FP8_E4M3)
+        return 0;
+    if (layer->kind == HSWA_KIND_SWA && layer->window <= 0) return 0;
+    const int32_t window = layer->kind == HSWA_KIND_SWA ? layer->window : 0;
+    int64_t pages = 0;
+    for (int i = 0; i < n_seqs; ++i) {
+        int32_t lo, hi;
+        chunk_pages(prefix_len[i], q_start[i + 1] - q_start[i], window, lo, hi);
+        pages += std::max(0, hi - lo + 1);
+    }
+    return stage_bytes(pool->cfg, n_seqs, n_seqs > 0 ? q_start[n_seqs] : 0, pages);
 }
 
 extern "C" int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *layer, const void *q, void *o,
@@ -1341,10 +1408,10 @@ extern "C" int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *la
         if (!prefill_fast_ok(pool, layer, q, o) || c.head_dim != 128 || !layer->k_scale || !layer->v_scale ||
             ((uintptr_t)layer->k_pool & 15) || ((uintptr_t)layer->v_pool & 15))
             return HSWA_ERR_UNSUPPORTED;
-        const StageLayout l = stage_layout(c, layer, n_seqs, max_q_len);
-        if (!ws || ((uintptr_t)ws & 255) || ws_bytes < l.total) return HSWA_ERR_INVALID_ARG;
+        const StageLayout l = stage_layout(c, n_seqs, total_q, ws_bytes);
+        if (!ws || ((uintptr_t)ws & 255) || l.cap < 1) return HSWA_ERR_INVALID_ARG;
         if ((int64_t)total_q > (int64_t)n_seqs * max_q_len) return HSWA_ERR_INVALID_ARG;
-        const int64_t staged_pages = (int64_t)n_seqs * l.per_seq;
+        const int64_t staged_pages = std::min<int64_t>(l.cap, (int64_t)n_seqs * c.max_pages_per_seq);
         if (staged_pages * c.n_kv_heads * kP >= (1ll << 31)) return HSWA_ERR_UNSUPPORTED;
         StageArgs sa;
         sa.bt = d_bt;
@@ -1356,19 +1423,21 @@ extern "C" int hswa_prefill_chunk_ws(const hswa_pool *pool, const hswa_layer *la
         sa.v_scale = layer->v_scale;
         uint8_t *base = static_cast<uint8_t *>(ws);
         sa.stage_bt = reinterpret_cast<int32_t *>(base);
+        sa.stage_off = reinterpret_cast<int32_t *>(base + l.off_off);
         sa.k_out = reinterpret_cast<__half *>(base + l.k_off);
-        sa.v_out = reinterpret_cast<__half *>(base + l.v_off);
+        sa.v_out = reinterpret_cast<__half *>(base + l.k_off + (size_t)staged_pages * l.page_bytes);
         sa.n_seqs = n_seqs;
         sa.bt_stride = c.max_pages_per_seq;
         sa.hkv = c.n_kv_heads;
         sa.window = window;
         sa.num_pages = num_pages;
-        sa.per_seq = l.per_seq;
+        sa.cap = (int32_t)staged_pages;
         sa.err = error_word();
         __half *q16 = reinterpret_cast<__half *>(base + l.q_off);
         const int64_t n8 = (int64_t)total_q * c.n_q_heads * kD / 8;
         set_last_kernel(window > 0 && window <= kBN ? "prefill_stage_fp8+prefill_swa_tc_d128<f16>"
                                                      : "prefill_stage_fp8+prefill_tc_bf16_d128<f16>");
+        prefill_stage_plan<<<1, 256, 0, st>>>(sa);
         prefill_stage_fp8<<<dim3(c.max_pages_per_seq, n_seqs), 256, 0, st>>>(sa);
         prefill_q_to_f16<<<(int)std::min<int64_t>((n8 + 255) / 256, 4096), 256, 0, st>>>(
             static_cast<const __nv_bfloat16 *>(q), q16, n8);

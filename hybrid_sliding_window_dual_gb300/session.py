@@ -153,8 +153,15 @@ class DualPoolSession:
         B.hswa_decode_multi(self.pool, self.layers[layer], q, o, self.bt(layer), self.d_seq_len, n_seqs, n_tok,
                             scale, ws, ws.numel(), self.stream)
 
-    def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale):
-        need = B.hswa_prefill_workspace_size(self.pool, self.layers[layer], n_seqs, max_q_len)
+    def prefill(self, layer, q, o, d_prefix_len, d_q_start, n_seqs, max_q_len, scale, prefix_host=None,
+                q_start_host=None):
+        """prefix_host / q_start_host: host copies of the device arrays; with
+        them an FP8 pool's staging workspace is sized for this chunk exactly,
+        without them for any chunk of n_seqs sequences of max_q_len rows."""
+        if prefix_host is not None and q_start_host is not None:
+            need = B.hswa_prefill_workspace_size_exact(self.pool, self.layers[layer], prefix_host, q_start_host)
+        else:
+            need = B.hswa_prefill_workspace_size(self.pool, self.layers[layer], n_seqs, max_q_len)
         ws = None
         if need:  # FP8 pools stage f16 copies of the pages the chunk reads (and of q)
             if self.prefill_ws is None or self.prefill_ws.numel() < need:

@@ -179,12 +179,17 @@ def test_decode_refuses_more_rows_than_the_merge_grid_takes(dtype):
 
 
 def test_prefill_workspace_sizes():
-    """Only FP8 pools need a prefill workspace; an SWA layer stages at most
-    ceil((W - 1 + max_q_len) / P) + 1 pages per sequence, a Full layer its
-    whole table row, plus an fp16 copy of n_seqs * max_q_len query rows."""
+    """Only FP8 pools need a prefill workspace. Its layout: the staging table
+    [n_seqs][table row], a first-copy offset per sequence [n_seqs + 1], the
+    fp16 copy of the q rows, then fp16 K and V page copies. The upper bound
+    holds, per sequence, its whole table row (Full layer) or
+    ceil((W - 1 + max_q_len) / P) + 1 pages (SWA layer) and n_seqs * max_q_len
+    query rows; the exact size holds the pages the chunk reads: logical pages
+    0 .. (prefix + n - 1) / P (Full), from (prefix - W + 1) / P (SWA)."""
     cfg, lp, _ = make_pair()
     full = H.Layer(kind=H.HSWA_KIND_FULL, window=0, k_pool=16, v_pool=16)
     assert H.hswa_prefill_workspace_size(lp, full, 4, 4096) == 0
+    assert H.hswa_prefill_workspace_size_exact(lp, full, [0], [0, 5]) == 0
     H.hswa_pool_destroy(lp)
     W, P, MP, hkv, d = 128, 64, 100, 8, 128
     cfg = H.Config(window=W, page_size=P, n_q_heads=64, n_kv_heads=hkv, head_dim=d, dtype=H.HSWA_DTYPE_FP8_E4M3,
@@ -193,16 +198,28 @@ def test_prefill_workspace_sizes():
     swa = H.Layer(kind=H.HSWA_KIND_SWA, window=W, k_pool=16, v_pool=16)
     page = hkv * P * d * 2  # one fp16 K (or V) page copy
 
-    def pages(n_bytes, n_seqs, max_q):
-        table = -(-n_seqs * MP * 4 // 1024) * 1024
-        q16 = -(-n_seqs * max_q * 64 * d * 2 // 1024) * 1024  # fp16 copy of the query rows
-        return (n_bytes - table - q16) / (2 * page)
+    def up1k(x):
+        return -(-x // 1024) * 1024
 
-    assert pages(H.hswa_prefill_workspace_size(lp, full, 8, 4096), 8, 4096) == 8 * MP
+    def pages(n_bytes, n_seqs, q_rows):
+        fixed = up1k(n_seqs * MP * 4) + up1k((n_seqs + 1) * 4) + up1k(q_rows * 64 * d * 2)
+        return (n_bytes - fixed) / (2 * page)
+
+    assert pages(H.hswa_prefill_workspace_size(lp, full, 8, 4096), 8, 8 * 4096) == 8 * MP
     for q in (1, 64, 65, 4096):
         per = min(MP, -(-(W - 1 + q) // P) + 1)
-        assert pages(H.hswa_prefill_workspace_size(lp, swa, 8, q), 8, q) == 8 * per
+        assert pages(H.hswa_prefill_workspace_size(lp, swa, 8, q), 8, 8 * q) == 8 * per
     assert H.hswa_prefill_workspace_size(lp, H.Layer(kind=H.HSWA_KIND_SWA, window=0), 8, 64) == 0
+    # exact sizes: prefixes around page and window edges, an empty chunk
+    prefix = np.array([0, 63, 64, 127, 128, 1000, 5000, 77], np.int32)
+    chunk = np.array([1, 1, 64, 130, 0, 300, 129, 64], np.int32)
+    q_start = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    exp_full = sum(-(-(p + n) // P) for p, n in zip(prefix, chunk) if n > 0)
+    exp_swa = sum((p + n - 1) // P - max(0, p - W + 1) // P + 1 for p, n in zip(prefix, chunk) if n > 0)
+    assert pages(H.hswa_prefill_workspace_size_exact(lp, full, prefix, q_start), 8, int(q_start[-1])) == exp_full
+    assert pages(H.hswa_prefill_workspace_size_exact(lp, swa, prefix, q_start), 8, int(q_start[-1])) == exp_swa
+    assert H.hswa_prefill_workspace_size_exact(lp, full, prefix, q_start) < \
+        H.hswa_prefill_workspace_size(lp, full, 8, int(chunk.max()))
     H.hswa_pool_destroy(lp)
 
 

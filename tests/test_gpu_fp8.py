@@ -147,7 +147,8 @@ def test_fp8_prefill_chunk_matches_oracle(swa_first):
         vn = wl.normal((n_tot, HKV, D), 820 + layer, wl.DTYPE_BF16)
         c.sess.append(layer, kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"))
         o = torch.full((n_tot, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
-        c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, max(chunk), scale)
+        c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, max(chunk), scale, prefix_host=np.array(cached),
+                       q_start_host=q_start)
         assert c.sess.check() == 0
         assert H.hswa_last_kernel() == prefill_kernel(kind, 0 if kind == FULL else W, fp8=True)
         kc, ks, vc, vs = c.host[layer]
@@ -162,25 +163,33 @@ def test_fp8_prefill_chunk_matches_oracle(swa_first):
 
 
 @pytest.mark.gpu
-def test_fp8_prefill_rejects_small_workspace():
+def test_fp8_prefill_workspace_too_small():
+    """A workspace without room for the tables, the q copy and one page copy
+    is refused before any launch; one short of the chunk's page copies
+    stages what fits, reads the rest as zeros and reports HSWA_ERR_BOUNDS."""
     c = Fp8Case([100, 300], seed=76, extra=80)
     B = c.B
     c.sess.reserve(range(B), [64, 64])
     c.ora.reserve(range(B), [64, 64])
     c.sess.sync()
     lay = c.sess.layers[0]
-    need = H.hswa_prefill_workspace_size(c.sess.pool, lay, B, 64)
-    assert need > 0
-    assert H.hswa_prefill_workspace_size(c.sess.pool, lay, B, 64) < \
-        H.hswa_prefill_workspace_size(c.sess.pool, lay, B + 1, 64)
+    prefix, q_start = np.array([100, 300], np.int32), np.array([0, 64, 128], np.int32)
+    need = H.hswa_prefill_workspace_size_exact(c.sess.pool, lay, prefix, q_start)
+    assert 0 < need < H.hswa_prefill_workspace_size(c.sess.pool, lay, B, 64)
+    page = HKV * 64 * D * 2
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    q = torch.zeros(2 * 64, HQ, D, dtype=torch.bfloat16, device="cuda")
+    q = wl.normal((128, HQ, D), 77, wl.DTYPE_BF16).cuda()
+    args = (c.sess.pool, lay, q, torch.empty_like(q), c.sess.bt(0), torch.as_tensor(prefix, device="cuda"),
+            torch.as_tensor(q_start, device="cuda"), B, 128, 64, 0.1, ws)
     with pytest.raises(H.HswaError) as e:
-        H.hswa_prefill_chunk_ws(c.sess.pool, lay, q, q.clone(), c.sess.bt(0),
-                                torch.tensor([100, 300], dtype=torch.int32, device="cuda"),
-                                torch.tensor([0, 64, 128], dtype=torch.int32, device="cuda"), B, 128, 64, 0.1,
-                                ws, need - 1)
+        H.hswa_prefill_chunk_ws(*args, need - 2 * page * ((100 + 64 + 63) // 64 + (300 + 64 + 63) // 64))
     assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    assert c.sess.check() == 0
+    o = torch.full_like(q, float("nan"))
+    H.hswa_prefill_chunk_ws(*(args[:3] + (o,) + args[4:]), need - 2 * page)
+    assert c.sess.check() == H.HSWA_ERR_BOUNDS
+    assert torch.isfinite(o.float()).all()
+    H.hswa_prefill_chunk_ws(*(args[:3] + (o,) + args[4:]), need)
     assert c.sess.check() == 0
 
 
@@ -373,7 +382,8 @@ def test_fp8_chunked_prefill_full_size_sampled():
         vn = wl.normal((B * C, HKV, D), 950 + layer, wl.DTYPE_BF16)
         c.sess.append(layer, kn.cuda(), vn.cuda(), torch.as_tensor(slots, device="cuda"))
         o = torch.full((B * C, HQ, D), float("nan"), dtype=torch.bfloat16, device="cuda")
-        c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, C, scale)
+        c.sess.prefill(layer, q.cuda(), o, d_prefix, d_qs, B, C, scale, prefix_host=prefix,
+                       q_start_host=np.arange(0, B * C + 1, C))
         assert c.sess.check() == 0
         assert H.hswa_last_kernel() == prefill_kernel(kind, 0 if kind == FULL else W, fp8=True)
         kc, ks, vc, vs = (x.cpu().numpy() for x in (c.sess.k[layer], c.sess.ks[layer], c.sess.v[layer],
