@@ -619,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 constexpr int kQBufs = 2;
 constexpr int kDescs = 4;
+constexpr int kSwaThreads = kThreads + 32;  // warp 10: head B's MMA issuer
 constexpr uint32_t kStageBytes = 32 * 128;  // one warp's 32 rows x 64 columns of O, bf16
 
 // What the softmax warps need of a unit (written by the Q loader).
@@ -632,7 +633,7 @@ struct SwaSmem {
     uint8_t ostage[8][kStageBytes];    // per softmax warp: O rows on their way out
     uint64_t q_full[kQBufs], q_empty[kQBufs];
     uint64_t kv_full[kSlots], kv_empty[kSlots];
-    uint64_t s_full[2], p_full[2], o_final[2], mma_done;
+    uint64_t s_full[2], p_full[2], o_final[2], mma_done[2];
     uint64_t desc_full[kDescs], desc_empty[kDescs];
     SwaDesc desc[kDescs];
     uint32_t tmem_base;
@@ -887,15 +888,21 @@ __device__ void swa_load_kv(SwaSmem &sm, const CUtensorMap *tk, const CUtensorMa
         mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err);
 }
 
+// One MMA issuer per query head (warp 9: head A, warp 10: head B), each
+// walking the units in order and waiting only on its own head's barriers:
+//   QK(0) | PV(0) QK(1) | PV(1)
+// A K / V slot is released once both heads' last uses of it have completed
+// (kv_empty counts one commit from each issuer), so the heads run apart and
+// one head's softmax and O store overlap the other head's MMAs.
 template <bool kF16>
-__device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs) {
-    const uint32_t tbase = sm.tmem_base;
-    const uint32_t ts0 = tbase, ts1 = tbase + 128, to0 = tbase + 256, to1 = tbase + 384;
+__device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs, int x) {
+    const uint32_t ts = sm.tmem_base + 128 * x, to = sm.tmem_base + 256 + 128 * x;
+    const uint64_t qd = sdesc(smem_u32(sm.q[x]), 16, 1024);  // one Q buffer per head
     SwaWalk w;
     w.start(a, sm, pairs);
     TileRing ring;
     ring.init();
-    int32_t tcount = 0;  // S tiles so far (per head): the s_full / p_full phase
+    int32_t tcount = 0;  // S tiles so far: the s_full / p_full phase
     bool ok = true;
     auto wait_kv = [&](int32_t i) { return mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err); };
     for (int32_t ub = 0; ok && ub < sm.n_units; ++ub) {
@@ -911,8 +918,6 @@ __device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs) {
         }
         const int64_t lo_id = b.tile_base + b.lo, hi_id = b.tile_base + b.hi;
         const int n_t = b.hi - b.lo + 1;  // 1 or 2
-        // load index of each tile's K (its V is the next load); a tile
-        // loaded for this unit is waited for at its first use
         int32_t k0 = ring.find(lo_id), k1 = -1;
         const bool fresh0 = k0 < 0;
         if (fresh0) k0 = ring.place(lo_id, lo_id, hi_id);
@@ -922,22 +927,12 @@ __device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs) {
             fresh1 = k1 < 0;
             if (fresh1) k1 = ring.place(hi_id, lo_id, hi_id);
         }
-        const int32_t qa = 2 * ub, qb = qa + 1, sa = qa % kQBufs, sb = qb % kQBufs;
-        const uint64_t qd0 = sdesc(smem_u32(sm.q[sa]), 16, 1024), qd1 = sdesc(smem_u32(sm.q[sb]), 16, 1024);
-        // S of the first tile for both heads
-        ok = (!fresh0 || wait_kv(k0)) && mbar_wait(&sm.q_full[sa], (qa / kQBufs) & 1, a.err);
+        ok = (!fresh0 || wait_kv(k0)) && mbar_wait(&sm.q_full[x], ub & 1, a.err);
         if (!ok) break;
         tc_fence_after();
-        uint64_t kd = sdesc(smem_u32(sm.kv[k0 % kSlots]), 16, 1024);
-        issue_s<kF16>(ts0, qd0, kd);
-        mma_commit(&sm.s_full[0]);
-        if (n_t == 1) mma_commit(&sm.q_empty[sa]);
-        ok = mbar_wait(&sm.q_full[sb], (qb / kQBufs) & 1, a.err);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s<kF16>(ts1, qd1, kd);
-        mma_commit(&sm.s_full[1]);
-        if (n_t == 1) mma_commit(&sm.q_empty[sb]);
+        issue_s<kF16>(ts, qd, sdesc(smem_u32(sm.kv[k0 % kSlots]), 16, 1024));
+        mma_commit(&sm.s_full[x]);
+        if (n_t == 1) mma_commit(&sm.q_empty[x]);
         if (!(lo_id >= keep_lo && lo_id <= keep_hi)) mma_commit(&sm.kv_empty[k0 % kSlots]);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -945,44 +940,31 @@ __device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs) {
             const int64_t tid = lo_id + j;
             const int32_t kj = j ? k1 : k0;
             const bool fresh = j ? fresh1 : fresh0;
-            ok = (!fresh || wait_kv(kj + 1)) && mbar_wait(&sm.p_full[0], tcount & 1, a.err) &&
+            ok = (!fresh || wait_kv(kj + 1)) && mbar_wait(&sm.p_full[x], tcount & 1, a.err) &&
                  !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
-            const uint64_t vd = sdesc(smem_u32(sm.kv[(kj + 1) % kSlots]), kHalfBytes, 1024);
-            issue_pv<kF16>(to0, ts0, vd, j == 0);
-            const bool more = j + 1 < n_t;  // only for j == 0
-            if (!more) mma_commit(&sm.o_final[0]);  // head A's O is final once this completes
-            if (more) {
+            issue_pv<kF16>(to, ts, sdesc(smem_u32(sm.kv[(kj + 1) % kSlots]), kHalfBytes, 1024), j == 0);
+            if (!(tid >= keep_lo && tid <= keep_hi)) mma_commit(&sm.kv_empty[(kj + 1) % kSlots]);
+            if (j + 1 < n_t) {
                 ok = !fresh1 || wait_kv(k1);
                 if (!ok) break;
                 tc_fence_after();
-                kd = sdesc(smem_u32(sm.kv[k1 % kSlots]), 16, 1024);
-                issue_s<kF16>(ts0, qd0, kd);
-                mma_commit(&sm.s_full[0]);
-                mma_commit(&sm.q_empty[sa]);
-            }
-            ok = mbar_wait(&sm.p_full[1], tcount & 1, a.err) && !*(volatile int32_t *)&sm.abort;
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv<kF16>(to1, ts1, vd, j == 0);
-            if (!more) mma_commit(&sm.o_final[1]);
-            if (!(tid >= keep_lo && tid <= keep_hi)) mma_commit(&sm.kv_empty[(kj + 1) % kSlots]);
-            if (more) {
-                issue_s<kF16>(ts1, qd1, kd);
-                mma_commit(&sm.s_full[1]);
-                mma_commit(&sm.q_empty[sb]);
+                issue_s<kF16>(ts, qd, sdesc(smem_u32(sm.kv[k1 % kSlots]), 16, 1024));
+                mma_commit(&sm.s_full[x]);
+                mma_commit(&sm.q_empty[x]);
                 if (!(hi_id >= keep_lo && hi_id <= keep_hi)) mma_commit(&sm.kv_empty[k1 % kSlots]);
+            } else {
+                mma_commit(&sm.o_final[x]);  // the head's O is final once this completes
             }
             ++tcount;
         }
-        if (!ok) break;
         w = nw;
     }
     if (!ok) sm.abort = 1;
     // every MMA issued above has completed before the TMEM is freed
-    mma_commit(&sm.mma_done);
-    mbar_wait(&sm.mma_done, 0, a.err);
+    mma_commit(&sm.mma_done[x]);
+    mbar_wait(&sm.mma_done[x], 0, a.err);
 }
 
 template <bool kF16>
@@ -1040,7 +1022,7 @@ __device__ void swa_softmax(SwaSmem &sm, const CUtensorMap *to, const PrefillArg
 }
 
 template <bool kF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSwaThreads, 1)
     prefill_swa_tc_d128(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                         PrefillArgs a) {
@@ -1058,14 +1040,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&sm.kv_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
+            mbar_init(&sm.kv_empty[i], 2);  // one commit from each head's issuer
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
             mbar_init(&sm.p_full[x], 128);
             mbar_init(&sm.o_final[x], 1);
         }
-        mbar_init(&sm.mma_done, 1);
+        mbar_init(&sm.mma_done[0], 1);
+        mbar_init(&sm.mma_done[1], 1);
         for (int i = 0; i < kDescs; ++i) {
             mbar_init(&sm.desc_full[i], 1);
             mbar_init(&sm.desc_empty[i], 256);
@@ -1087,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             swa_load_kv(sm, &tk, &tv, a, pairs);
         __syncwarp();
     } else {
-        if ((threadIdx.x & 31) == 0) swa_mma<kF16>(sm, a, pairs);
+        if ((threadIdx.x & 31) == 0) swa_mma<kF16>(sm, a, pairs, warp - 9);
         __syncwarp();
     }
     tc_fence_before();
@@ -1338,9 +1321,9 @@ int launch_prefill_tc(const hswa_config &c, int32_t window, const void *k_pool, 
         const int64_t units = (int64_t)n_seqs * ((max_q_len + kBM - 1) / kBM + 1) * (c.n_q_heads / 2);
         const dim3 grid((unsigned)std::min<int64_t>(sms, units));
         if (f16)
-            prefill_swa_tc_d128<true><<<grid, kThreads, kSwaSmemBytes, st>>>(tq, tk, tv, to, a);
+            prefill_swa_tc_d128<true><<<grid, kSwaThreads, kSwaSmemBytes, st>>>(tq, tk, tv, to, a);
         else
-            prefill_swa_tc_d128<false><<<grid, kThreads, kSwaSmemBytes, st>>>(tq, tk, tv, to, a);
+            prefill_swa_tc_d128<false><<<grid, kSwaThreads, kSwaSmemBytes, st>>>(tq, tk, tv, to, a);
         const cudaError_t e = cudaGetLastError();
         return e == cudaSuccess ? HSWA_OK : cuda_fail(e, "prefill_swa_tc_d128 launch");
     }
