@@ -172,6 +172,18 @@ def test_prefill_swa_few_units(cached, chunk):
 
 
 @pytest.mark.gpu
+def test_prefill_many_sequences_keep_their_order():
+    """70 sequences: past 64 the Full-layer grid keeps the sequences' own
+    order instead of ranking them longest first; ragged chunks and prefixes,
+    every row of both layers against the oracle."""
+    rng = np.random.default_rng(70)
+    cached = [int(x) for x in rng.integers(0, 1500, size=70)]
+    chunk = [int(x) for x in rng.integers(0, 200, size=70)]
+    sc = Scenario(16, 2, 128, 64, 128, wl.DTYPE_BF16, cached, seed=20, extra_tokens=210)
+    run_prefill_chunk(sc, chunk, seed=10, expect_kernel=True)
+
+
+@pytest.mark.gpu
 def test_prefill_window_covers_whole_sequence_equals_full():
     """W >= every position: the SWA layer's chunk attends to exactly the Full
     layer's keys, so both layers give the same bits on the same history."""
