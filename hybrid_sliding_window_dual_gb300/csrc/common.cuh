@@ -7,6 +7,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <mutex>
+
 #include "hswa.h"
 
 namespace hswa {
@@ -27,6 +30,30 @@ void set_last_kernel(const char *name);
 int cuda_fail(cudaError_t e, const char *where);
 // Host: number of SMs of the current device (cached per device).
 int sm_count();
+// Host: index of the current device (-1 if it cannot be read).
+int device_index();
+// Host: the lock that guards the per-device kernel set-up below.
+std::mutex &setup_mutex();
+
+// Host: on the first call per device, allow `kernel` its dynamic shared
+// memory and count the CTAs of `threads` threads that fit on one SM; later
+// calls on that device return the count. Kernel attributes belong to a
+// device, so each device is set up on its own. -1 on failure.
+constexpr int kMaxDevices = 64;
+template <typename Kernel>
+int kernel_setup(Kernel kernel, size_t smem, int threads, int (&cache)[kMaxDevices]) {
+    const int dev = device_index();
+    if (dev < 0 || dev >= kMaxDevices) return -1;
+    std::lock_guard<std::mutex> lock(setup_mutex());
+    if (cache[dev] == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) n = 1;
+        cache[dev] = std::max(1, n);
+    }
+    return cache[dev];
+}
 // Host: launch a kernel with programmatic stream serialization (PDL).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

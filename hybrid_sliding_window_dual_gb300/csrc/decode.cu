@@ -1779,19 +1779,8 @@ bool decode_fp8_ok(const hswa_pool *pool, const hswa_layer *layer, const void *q
 
 template <int kTok>
 int decode_fp8_ctas_per_sm() {
-    static int v = -1;
-    if (v < 0) {
-        constexpr size_t smem = decode_smem8_bytes<kTok>();
-        if (cudaFuncSetAttribute(decode_mma_fp8_d128<kTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return -1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_fp8_d128<kTok>, 32 * (kConsumers8 + 1),
-                                                          smem) != cudaSuccess)
-            n = 1;
-        v = std::max(1, n);
-    }
-    return v;
+    static int cache[kMaxDevices] = {};
+    return kernel_setup(decode_mma_fp8_d128<kTok>, decode_smem8_bytes<kTok>(), 32 * (kConsumers8 + 1), cache);
 }
 
 // Query tokens per sequence from which an FP8 decode runs on the tensor-core
@@ -1807,38 +1796,16 @@ bool decode_fast_ok(const hswa_pool *pool, const hswa_layer *layer, const void *
 
 template <int kTok>
 int decode_ctas_per_sm_t() {
-    static int v = -1;
-    if (v < 0) {
-        constexpr size_t smem = decode_smem_bytes<kTok>();
-        if (cudaFuncSetAttribute(decode_mma_bf16_d128<kTok>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return -1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_bf16_d128<kTok>, 32 * (kTok + 1), smem) !=
-            cudaSuccess)
-            n = 1;
-        v = std::max(1, n);
-    }
-    return v;
+    static int cache[kMaxDevices] = {};
+    return kernel_setup(decode_mma_bf16_d128<kTok>, decode_smem_bytes<kTok>(), 32 * (kTok + 1), cache);
 }
 
 int decode_ctas_per_sm() { return decode_ctas_per_sm_t<1>(); }
 
 template <int kR, class Smem>
 int decode_tc_ctas_per_sm_t() {
-    static int v = -1;
-    if (v < 0) {
-        constexpr size_t smem = decode_tc_smem_bytes<Smem>();
-        if (cudaFuncSetAttribute(decode_tc_d128<kR, Smem>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return -1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_d128<kR, Smem>, Smem::kThreads, smem) !=
-            cudaSuccess)
-            n = 1;
-        v = std::max(1, n);
-    }
-    return v;
+    static int cache[kMaxDevices] = {};
+    return kernel_setup(decode_tc_d128<kR, Smem>, decode_tc_smem_bytes<Smem>(), Smem::kThreads, cache);
 }
 
 template <class Smem>

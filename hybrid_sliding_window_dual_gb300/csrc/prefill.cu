@@ -1295,21 +1295,14 @@ int launch_prefill_tc(const hswa_config &c, int32_t window, const void *k_pool, 
     a.kv_rows = (int32_t)rows;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = error_word();
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e;
-        if ((e = cudaFuncSetAttribute(prefill_tc_bf16_d128<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kPrefillSmemBytes)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(prefill_tc_bf16_d128<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kPrefillSmemBytes)) != cudaSuccess)
-            return cuda_fail(e, "prefill_tc_bf16_d128 shared memory");
-        if ((e = cudaFuncSetAttribute(prefill_swa_tc_d128<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kSwaSmemBytes)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(prefill_swa_tc_d128<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kSwaSmemBytes)) != cudaSuccess)
-            return cuda_fail(e, "prefill_swa_tc_d128 shared memory");
-        attr = true;
-    }
+    // the kernels' shared-memory opt-in, once per device
+    static int full_b[kMaxDevices], full_h[kMaxDevices], swa_b[kMaxDevices], swa_h[kMaxDevices];
+    if (kernel_setup(prefill_tc_bf16_d128<false>, kPrefillSmemBytes, kThreads, full_b) < 0 ||
+        kernel_setup(prefill_tc_bf16_d128<true>, kPrefillSmemBytes, kThreads, full_h) < 0)
+        return cuda_fail(cudaGetLastError(), "prefill_tc_bf16_d128 shared memory");
+    if (kernel_setup(prefill_swa_tc_d128<false>, kSwaSmemBytes, kSwaThreads, swa_b) < 0 ||
+        kernel_setup(prefill_swa_tc_d128<true>, kSwaSmemBytes, kSwaThreads, swa_h) < 0)
+        return cuda_fail(cudaGetLastError(), "prefill_swa_tc_d128 shared memory");
     if (window > 0 && window <= kBN) {
         // at most two key tiles per block: the persistent window kernel
         const int sms = sm_count();

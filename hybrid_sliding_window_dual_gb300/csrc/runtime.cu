@@ -16,7 +16,6 @@ namespace hswa {
 __device__ int g_error_word = 0;
 
 namespace {
-constexpr int kMaxDevices = 64;
 int *g_err_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 std::mutex g_mu;
@@ -29,7 +28,12 @@ int current_device() {
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     return dev;
 }
+std::mutex g_setup_mu;
 }  // namespace
+
+int device_index() { return current_device(); }
+
+std::mutex &setup_mutex() { return g_setup_mu; }
 
 int *error_word() {
     const int dev = current_device();
