@@ -192,8 +192,12 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
         : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until this thread's bulk stores have read their shared-memory source.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until at most kPending of this thread's latest bulk store groups
+// have not yet read their shared-memory source.
+template <int kPending = 0>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
+}
 // Wait until this thread's bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

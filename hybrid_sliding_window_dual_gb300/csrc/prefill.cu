@@ -54,6 +54,7 @@ constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column half (128 rows
 constexpr uint32_t kBoxBytes = kP * 128;         // one page x 64 columns
 constexpr int kThreads = 320;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr uint32_t kStageBytes = 32 * 128;  // per warp: two buffers of 32 rows x 32 columns of O, bf16
 
 struct PrefillSmem {
     uint8_t q[2][kTileBytes];          // Q_A, Q_B: [d half][128 rows][128 B]
@@ -360,29 +361,31 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int32_t
     tmem_wait_st();
 }
 
-// One S tile of a window block (SWA layer): this lane's row t sees keys
-// [t - W + 1, t]; the warp's rows are t_first..t_last. A 32-key chunk that
-// no row of the warp sees is neither loaded nor exponentiated (its P is 0),
-// and only a chunk that some row sees in part is masked key by key. With
-// blocks on 128-key boundaries a warp has one partial chunk per tile and
-// skips three of the eight chunks of a block's two tiles.
+// One 64-key page of a window block's S (SWA layer): this lane's row t sees
+// keys [t - W + 1, t] and the warp's rows are t_first..t_last. A 32-key
+// chunk that no row of the warp sees is neither loaded into the max nor
+// exponentiated (its P is 0), and only a chunk that some row sees in part is
+// masked key by key: with blocks on 128-key boundaries a warp sees five of
+// the eight chunks of a block's four pages, two of them in part. A page's scores
+// can be ready while the PV of the page before still runs, so a rescale of
+// O first waits for that PV (phase pv_par of pv_bar). False when that wait
+// gave up (the warp agrees).
 template <bool kF16>
-__device__ __forceinline__ void softmax_tile_band(uint32_t t_s, uint32_t t_o, int32_t k0, int32_t t, int32_t t_first,
-                                                  int32_t t_last, int32_t W, float scale_log2, bool first_tile,
-                                                  float &m_used, float &l) {
-    uint32_t sr[4][32];
-    // chunks [c_lo, c_hi] meet some row's window; the others are skipped
-    const int32_t c_lo = max(0, (t_first - W + 1 - k0) >> 5), c_hi = min(3, (t_last - k0) >> 5);
-    const int32_t lo_c = t - W + 1 - k0;  // keys c of the tile with lo_c <= c <= lo_c + W - 1
-    float mc[4];
+__device__ __forceinline__ bool softmax_page_band(uint32_t t_s, uint32_t t_o, int32_t k0, int32_t t, int32_t t_first,
+                                                  int32_t t_last, int32_t W, float scale_log2, bool first_page,
+                                                  float &m_used, float &l, uint64_t *pv_bar, uint32_t pv_par,
+                                                  int *err) {
+    uint32_t sr[2][32];
+    const int32_t c_lo = max(0, (t_first - W + 1 - k0) >> 5), c_hi = min(1, (t_last - k0) >> 5);
+    const int32_t lo_c = t - W + 1 - k0;  // keys c of the page with lo_c <= c <= lo_c + W - 1
+    float mc[2];
     tmem_ld32(t_s, sr[0]);
     tmem_wait_ld(sr[0]);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        if (c + 1 < 4) tmem_ld32(t_s + 32 * (c + 1), sr[c + 1]);
+    for (int c = 0; c < 2; ++c) {
+        if (c == 0) tmem_ld32(t_s + 32, sr[1]);
         mc[c] = -INFINITY;
         if (c_lo <= c && c <= c_hi) {  // the same for every lane
-            // a chunk every row of the warp sees whole needs no mask
             const bool full = k0 + 32 * c >= t_last - W + 1 && k0 + 32 * c + 31 <= t_first;
             if (!full) {
 #pragma unroll
@@ -397,18 +400,18 @@ __device__ __forceinline__ void softmax_tile_band(uint32_t t_s, uint32_t t_o, in
             }
             mc[c] = fmaxf(m0, m1);
         }
-        if (c + 1 < 4) tmem_wait_ld(sr[c + 1]);
+        if (c == 0) tmem_wait_ld(sr[1]);
     }
-    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * scale_log2;
+    const float mx = fmaxf(mc[0], mc[1]) * scale_log2;
     const bool need = mx > m_used + kRescaleLog2;
-    const bool resc = need && !first_tile && m_used != -INFINITY;
+    const bool resc = need && !first_page && m_used != -INFINITY;
     const float alpha = resc ? fast_exp2(m_used - mx) : 1.f;
     if (need) m_used = mx;
     const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
     const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(neg_m, neg_m);
-    float2 sums[4];
+    float2 sums[2];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
         float2 &sum2 = sums[c];
         sum2 = make_float2(0.f, 0.f);
         if (c_lo <= c && c <= c_hi) {
@@ -426,21 +429,26 @@ __device__ __forceinline__ void softmax_tile_band(uint32_t t_s, uint32_t t_o, in
         }
         tmem_st16(t_s + 16 * c, sr[c]);
     }
+    bool ok = true;
     if (__any_sync(0xffffffffu, resc)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(pv_bar, pv_par, err));
+        tc_fence_after();
+        if (ok) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(t_o + 32 * c, ov);
-            tmem_wait_ld(ov);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + 32 * c, ov);
+                tmem_wait_ld(ov);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(t_o + 32 * c, ov);
+                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                tmem_st32(t_o + 32 * c, ov);
+            }
         }
     }
-    const float2 s01 = __fadd2_rn(sums[0], sums[1]), s23 = __fadd2_rn(sums[2], sums[3]);
-    const float2 sum2 = __fadd2_rn(s01, s23);
+    const float2 sum2 = __fadd2_rn(sums[0], sums[1]);
     l = l * alpha + (sum2.x + sum2.y);
     tmem_wait_st();
+    return ok;
 }
 
 // Normalise this thread's row of O (TMEM) by 1 / l and store it as bf16 at
@@ -467,11 +475,12 @@ __device__ __forceinline__ void store_o_row(uint32_t t_o, float l, __nv_bfloat16
     }
 }
 
-// Normalise this thread's row of O (TMEM) and write the warp's 32 rows: one
-// 64-column half at a time through the warp's 4 KB shared-memory stage
-// (128-byte swizzle) and a TMA store, so that the writes reach memory as
-// whole rows instead of one 16-byte piece per row and instruction. A warp
-// with rows past the block's end stores its valid rows from registers.
+// Normalise this thread's row of O (TMEM) and write the warp's 32 rows in
+// four 32-column quarters through two 2 KB shared-memory buffers (64-byte
+// swizzle) and TMA stores: a buffer is refilled once the store before the
+// last has read it, so the stores overlap the packing of the next quarter
+// and the writes reach memory as whole 64-byte row pieces. A warp with rows
+// past the block's end stores its valid rows from registers.
 __device__ __forceinline__ void store_o_rows_staged(uint32_t t_o, float l, uint8_t *stage, const CUtensorMap *to,
                                                     int32_t head, int32_t row_first, bool full_warp,
                                                     __nv_bfloat16 *dst_row, bool valid) {
@@ -481,34 +490,40 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t t_o, float l, uint8
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int dh = 0; dh < 2; ++dh) {
-        uint32_t ov[2][32];
-        tmem_ld32(t_o + 64 * dh, ov[0]);
-        tmem_ld32(t_o + 64 * dh + 32, ov[1]);
-        tmem_wait_ld(ov[0]);
-        tmem_wait_ld(ov[1]);
-        // the stage is free once the warp's previous store has read it
-        if (lane == 0) bulk_wait_read();
+    uint32_t ov[2][32];
+    auto put = [&](int qt, const uint32_t (&v)[32]) {
+        uint8_t *buf = stage + (qt & 1) * (kStageBytes / 2);
+        if (lane == 0) bulk_wait_read<1>();  // the buffer's previous store has read it
         __syncwarp();
-        uint8_t *row = stage + lane * 128;
+        uint8_t *row = buf + lane * 64;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {  // 16-byte chunk j: columns 8j .. 8j + 7 of the half
-            const uint32_t *v = ov[j >> 2] + (j & 3) * 8;
+        for (int j = 0; j < 4; ++j) {  // 16-byte chunk j: columns 8j .. 8j + 7 of the quarter
             uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
-            w.y = pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
-            w.z = pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
-            w.w = pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
-            *reinterpret_cast<uint4 *>(row + ((j ^ (lane & 7)) << 4)) = w;
+            w.x = pack_bf16(__uint_as_float(v[8 * j + 0]) * inv, __uint_as_float(v[8 * j + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(v[8 * j + 2]) * inv, __uint_as_float(v[8 * j + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(v[8 * j + 4]) * inv, __uint_as_float(v[8 * j + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(v[8 * j + 6]) * inv, __uint_as_float(v[8 * j + 7]) * inv);
+            *reinterpret_cast<uint4 *>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = w;
         }
-        fence_proxy_async_shared();  // the stage is read by the TMA store
+        fence_proxy_async_shared();  // the buffer is read by the TMA store
         __syncwarp();
         if (lane == 0) {
-            tma_store_3d(to, stage, dh * 64, head, row_first);
+            tma_store_3d(to, buf, qt * 32, head, row_first);
             bulk_commit();
         }
-    }
+    };
+    tmem_ld32(t_o, ov[0]);
+    tmem_ld32(t_o + 32, ov[1]);
+    tmem_wait_ld(ov[0]);
+    tmem_wait_ld(ov[1]);
+    put(0, ov[0]);
+    tmem_ld32(t_o + 64, ov[0]);
+    put(1, ov[1]);
+    tmem_ld32(t_o + 96, ov[1]);
+    tmem_wait_ld(ov[0]);
+    tmem_wait_ld(ov[1]);
+    put(2, ov[0]);
+    put(3, ov[1]);
 }
 
 template <bool kF16>
@@ -603,37 +618,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Sliding-window layers with W <= 128 ("MiMo-V2.5 Series Inference
 // Full-Link Optimization", Sec. 1.1: an SWA query attends only to the last W
 // tokens). A block of query rows at positions [128 m, 128 m + 128) sees keys
-// [128 m - W + 1, 128 m + 127]: key tiles m - 1 and m, never more. Blocks are
-// cut at these absolute boundaries (a chunk's first and last block may be
-// partial) and each CTA is persistent, one per SM, walking a contiguous share
-// of the unit list
+// [128 m - W + 1, 128 m + 127]: the 64-key pages 2m - 2 .. 2m + 1, never
+// more (fewer when the block is partial or its first key is past a page
+// start). Blocks are cut at these absolute boundaries (a chunk's first and
+// last block may be partial) and each CTA is persistent, one per SM, walking
+// a contiguous share of the unit list
 //     for each sequence, for each kv head g, for each block m,
 //         for each pair of query heads of g
-// so the head pairs of one block reuse its two K / V tiles and the next
-// block reuses tile m: a tile is loaded into shared memory once per CTA that
-// needs it. TMEM, barriers and the ring are set up once per CTA; a head's
-// next queries load as soon as its last QK MMA of the current unit is done,
-// and O leaves through a per-warp shared-memory stage and TMA stores.
-// Roles as in prefill_tc_bf16_d128: warps 0-7 softmax (two heads), warp 8
-// lane 0 loads Q and lane 1 loads K / V, warp 9 issues the MMAs.
+// so the head pairs of one block reuse its four K / V pages and the next
+// block reuses pages 2m and 2m + 1: a page is loaded into shared memory once
+// per CTA that needs it. The scores of a head are computed one page at a
+// time into two alternating TMEM buffers, so the QK of the next page runs
+// while the softmax works on this one. TMEM, barriers and the ring are set
+// up once per CTA; a head's next queries load as soon as its last QK MMA of
+// the current unit is done, and O leaves through a per-warp shared-memory
+// stage and TMA stores. Warps 0-7 softmax (two heads), warp 8 lane 0 loads
+// Q and lane 1 loads K / V, warps 9 and 10 issue head A's and head B's MMAs.
 
 constexpr int kQBufs = 2;
 constexpr int kDescs = 4;
 constexpr int kSwaThreads = kThreads + 32;  // warp 10: head B's MMA issuer
-constexpr uint32_t kStageBytes = 32 * 128;  // one warp's 32 rows x 64 columns of O, bf16
 
 // What the softmax warps need of a unit (written by the Q loader).
 struct SwaDesc {
     int32_t p0, n_rows, row0, lo, hi, hp;
 };
 
+constexpr uint32_t kPgBytes = kP * kD * 2;  // one K or V page of one kv head: [d half][64 keys][128 B]
+constexpr int kPgSlots = 8;                  // K and V of the last four pages
+
 struct SwaSmem {
     uint8_t q[kQBufs][kTileBytes];     // Q of one head: [d half][128 rows][128 B]
-    uint8_t kv[kSlots][kTileBytes];    // K or V tiles: [d half][128 keys][128 B]
+    uint8_t kv[kPgSlots][kPgBytes];    // K or V pages: [d half][64 keys][128 B]
     uint8_t ostage[8][kStageBytes];    // per softmax warp: O rows on their way out
     uint64_t q_full[kQBufs], q_empty[kQBufs];
-    uint64_t kv_full[kSlots], kv_empty[kSlots];
-    uint64_t s_full[2], p_full[2], o_final[2], mma_done[2];
+    uint64_t kv_full[kPgSlots], kv_empty[kPgSlots];
+    uint64_t s_full[2][2], p_full[2][2];  // [head][S buffer]
+    uint64_t pv_done[2], o_final[2], mma_done[2];
     uint64_t desc_full[kDescs], desc_empty[kDescs];
     SwaDesc desc[kDescs];
     uint32_t tmem_base;
@@ -734,9 +755,9 @@ struct SwaWalk {
 struct SwaBlock {
     int32_t s, g, hp;              // sequence, kv head, pair of query heads
     int32_t p0, n_rows, row0, L;   // first position, rows, first q row, keys after the chunk
-    int32_t lo, hi;                // key tiles of the block
+    int32_t lo, hi;                // logical pages of keys the block's rows see
     int32_t first_page, last_page; // logical pages its rows can see
-    int64_t tile_base;             // identity of tile 0 of (s, g)
+    int64_t tile_base;             // identity of page 0 of (s, g)
 };
 
 __device__ __forceinline__ SwaBlock swa_block(const SwaWalk &w, const PrefillArgs &a, int32_t pairs) {
@@ -750,42 +771,43 @@ __device__ __forceinline__ SwaBlock swa_block(const SwaWalk &w, const PrefillArg
     b.row0 = w.q0 + (b.p0 - w.pre);
     b.L = w.pre + w.n;
     const int32_t key_lo = max(0, b.p0 - a.window + 1);
-    b.lo = key_lo / kBN;
-    b.hi = w.m;
+    b.lo = key_lo / kP;
+    b.hi = (p_end - 1) / kP;
     b.first_page = key_lo / kP;
     b.last_page = (b.L - 1) / kP;
     b.tile_base = ((int64_t)b.s * a.hkv + b.g) << 32;
     return b;
 }
 
-// The two K / V tiles in the ring. A tile takes two consecutive loads (K,
-// then V) in load order; load i sits in slot i % kSlots. The producer and
-// the MMA thread make the same calls in the same order, so they agree on
-// every load index.
-struct TileRing {
-    int64_t id0, id1;  // resident tiles (-1: none)
-    int32_t k0, k1;    // load index of each one's K; its V is the next load
-    int32_t next;
+// The K / V pages in the ring: the last four placed, K and V of placement p
+// being loads 2p and 2p + 1 in slots (2p) % 8 and (2p + 1) % 8. A block
+// needs at most four pages (W <= 128: keys [128 m - 127, 128 m + 127]),
+// consecutive and later than those of the blocks before it in its (sequence,
+// kv head), so the page a placement replaces is never one the block needs.
+// The loader and the MMA issuers make the same calls in the same order and
+// agree on every load index.
+struct PageRing {
+    int64_t id0, id1, id2, id3;  // page of placement p sits in entry p % 4 (-1: none)
+    int32_t next;                // placements so far
 
     __device__ void init() {
-        id0 = id1 = -1;
+        id0 = id1 = id2 = id3 = -1;
         next = 0;
     }
-    // Load index of tile tid's K, or -1 when it is not in the ring.
-    __device__ int32_t find(int64_t tid) const { return id0 == tid ? k0 : id1 == tid ? k1 : -1; }
-    // New tile tid for a block needing tiles [lo_id, hi_id]: it replaces the
-    // entry that block does not need (a block needs at most two tiles).
-    __device__ int32_t place(int64_t tid, int64_t lo_id, int64_t hi_id) {
-        const int32_t k = next;
-        next += 2;
-        if (id0 >= lo_id && id0 <= hi_id) {
-            id1 = tid;
-            k1 = k;
-        } else {
-            id0 = tid;
-            k0 = k;
+    // Load index of page pid's K, or -1 when it is not in the ring.
+    __device__ int32_t find(int64_t pid) const {
+        const int32_t e = id0 == pid ? 0 : id1 == pid ? 1 : id2 == pid ? 2 : id3 == pid ? 3 : -1;
+        return e < 0 ? -1 : 2 * (next - 1 - ((next - 1 - e) & 3));
+    }
+    __device__ int32_t place(int64_t pid) {
+        const int32_t p = next++;
+        switch (p & 3) {
+            case 0: id0 = pid; break;
+            case 1: id1 = pid; break;
+            case 2: id2 = pid; break;
+            default: id3 = pid; break;
         }
-        return k;
+        return 2 * p;
     }
 };
 
@@ -842,123 +864,150 @@ __device__ void swa_load_kv(SwaSmem &sm, const CUtensorMap *tk, const CUtensorMa
     prefetch_tmap(tv);
     SwaWalk w;
     w.start(a, sm, pairs);
-    TileRing ring;
+    PageRing ring;
     ring.init();
     int32_t issued = 0;
     bool ok = true;
     for (int32_t ub = 0; ok && ub < sm.n_units; ++ub) {
         const SwaBlock b = swa_block(w, a, pairs);
-        const int64_t lo_id = b.tile_base + b.lo, hi_id = b.tile_base + b.hi;
         const int32_t *btrow = a.bt + (int64_t)b.s * a.bt_stride;
-        for (int32_t t = b.lo; ok && t <= b.hi; ++t) {
-            if (ring.find(b.tile_base + t) >= 0) continue;  // still in the ring
-            const int32_t k = ring.place(b.tile_base + t, lo_id, hi_id);
+        for (int32_t lp = b.lo; ok && lp <= b.hi; ++lp) {
+            if (ring.find(b.tile_base + lp) >= 0) continue;  // still in the ring
+            const int32_t k = ring.place(b.tile_base + lp);
+            // a page outside the block's view (an older window page, maybe
+            // released, or past the sequence) fills with zeros
+            int32_t row = a.kv_rows;
+            if (lp >= b.first_page && lp <= b.last_page) {
+                const int32_t page = lp < a.bt_stride ? btrow[lp] : -1;
+                if (page >= 0 && page < a.num_pages)
+                    row = (page * a.hkv + b.g) * kP;
+                else
+                    set_error(a.err, HSWA_ERR_BOUNDS);
+            }
             for (int kv = 0; kv < 2; ++kv) {
                 const int32_t i = k + kv;
-                const int slot = i % kSlots;
-                if (i >= kSlots)
-                    ok = mbar_wait(&sm.kv_empty[slot], ((i / kSlots) + 1) & 1, a.err) &&
+                const int slot = i % kPgSlots;
+                // the slot's previous load (i - 8) belongs to a page no
+                // later block of this CTA needs; both issuers released it
+                if (i >= kPgSlots)
+                    ok = mbar_wait(&sm.kv_empty[slot], ((i / kPgSlots) + 1) & 1, a.err) &&
                          !*(volatile int32_t *)&sm.abort;
                 if (!ok) break;
-                const CUtensorMap *map = kv ? tv : tk;
-                mbar_arrive_expect_tx(&sm.kv_full[slot], kTileBytes);
-                for (int pg = 0; pg < 2; ++pg) {
-                    // pages outside the block's view (older window pages,
-                    // possibly released, or past the sequence) fill with zeros
-                    const int32_t lp = t * 2 + pg;
-                    int32_t row = a.kv_rows;
-                    if (lp >= b.first_page && lp <= b.last_page) {
-                        const int32_t page = lp < a.bt_stride ? btrow[lp] : -1;
-                        if (page >= 0 && page < a.num_pages)
-                            row = (page * a.hkv + b.g) * kP;
-                        else
-                            set_error(a.err, HSWA_ERR_BOUNDS);
-                    }
-                    for (int dh = 0; dh < 2; ++dh)
-                        tma_load_2d(sm.kv[slot] + dh * kHalfBytes + pg * kBoxBytes, map, dh * 64, row,
-                                    &sm.kv_full[slot]);
-                }
+                mbar_arrive_expect_tx(&sm.kv_full[slot], kPgBytes);
+                for (int dh = 0; dh < 2; ++dh)
+                    tma_load_2d(sm.kv[slot] + dh * kBoxBytes, kv ? tv : tk, dh * 64, row, &sm.kv_full[slot]);
                 ++issued;
             }
         }
         w.next(a, pairs);
     }
     if (!ok) sm.abort = 1;
-    for (int32_t i = max(0, issued - kSlots); i < issued; ++i)
-        mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err);
+    for (int32_t i = max(0, issued - kPgSlots); i < issued; ++i)
+        mbar_wait(&sm.kv_full[i % kPgSlots], (i / kPgSlots) & 1, a.err);
+}
+
+// S = Q K^T for one 64-key page: 8 steps of K = 16 over d (the Q tile's d
+// halves are 16 KB apart, the page's 8 KB).
+template <bool kF16>
+__device__ __forceinline__ void issue_s_page(uint32_t t_s, uint64_t qd, uint64_t kd) {
+    constexpr uint32_t kIdesc = idesc_16(kBM, kP, false, kF16);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ss(t_s, qd + (((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4),
+               kd + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4), kIdesc, kk > 0);
+}
+
+// O += P V over one 64-key page: 4 steps of K = 16 keys; P (16-bit pairs)
+// sits in the first 32 columns of the S buffer, V is MN-major (d
+// contiguous) with the page's two 64-column halves 8 KB apart.
+template <bool kF16>
+__device__ __forceinline__ void issue_pv_page(uint32_t t_o, uint32_t t_p, uint64_t vd, bool first) {
+    constexpr uint32_t kIdesc = idesc_16(kBM, kD, true, kF16);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_ts(t_o, t_p + kk * 8, vd + kk * (2048 >> 4), kIdesc, (first && kk == 0) ? 0u : 1u);
 }
 
 // One MMA issuer per query head (warp 9: head A, warp 10: head B), each
-// walking the units in order and waiting only on its own head's barriers:
-//   QK(0) | PV(0) QK(1) | PV(1)
-// A K / V slot is released once both heads' last uses of it have completed
-// (kv_empty counts one commit from each issuer), so the heads run apart and
-// one head's softmax and O store overlap the other head's MMAs.
+// walking the units in order and waiting only on its own head's barriers.
+// A head has two 64-column S buffers, so the scores of page j + 1 are
+// computed while the softmax works on page j:
+//   QK(0) QK(1) | PV(0) QK(2) | PV(1) QK(3) | PV(2) | PV(3)
+// QK(j + 2) reuses page j's buffer once PV(j) has read its P (MMAs of one
+// thread run in issue order). A K / V slot is released once both heads'
+// last uses of it have completed (kv_empty counts a commit from each
+// issuer).
 template <bool kF16>
 __device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs, int x) {
-    const uint32_t ts = sm.tmem_base + 128 * x, to = sm.tmem_base + 256 + 128 * x;
+    const uint32_t ts0 = sm.tmem_base + 128 * x, to = sm.tmem_base + 256 + 128 * x;
     const uint64_t qd = sdesc(smem_u32(sm.q[x]), 16, 1024);  // one Q buffer per head
     SwaWalk w;
     w.start(a, sm, pairs);
-    TileRing ring;
+    PageRing ring;
     ring.init();
-    int32_t tcount = 0;  // S tiles so far: the s_full / p_full phase
+    int32_t tcount = 0;  // pages so far: S buffer tcount % 2, phase (tcount / 2) & 1
     bool ok = true;
-    auto wait_kv = [&](int32_t i) { return mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err); };
+    auto wait_kv = [&](int32_t i) { return mbar_wait(&sm.kv_full[i % kPgSlots], (i / kPgSlots) & 1, a.err); };
     for (int32_t ub = 0; ok && ub < sm.n_units; ++ub) {
         const SwaBlock b = swa_block(w, a, pairs);
         SwaWalk nw = w;
         nw.next(a, pairs);
-        // tiles the next unit needs stay in the ring after this one
+        // pages the next unit needs stay in the ring after this one
         int64_t keep_lo = 0, keep_hi = -1;
         if (ub + 1 < sm.n_units && nw.left > 0) {
             const SwaBlock nb = swa_block(nw, a, pairs);
             keep_lo = nb.tile_base + nb.lo;
             keep_hi = nb.tile_base + nb.hi;
         }
-        const int64_t lo_id = b.tile_base + b.lo, hi_id = b.tile_base + b.hi;
-        const int n_t = b.hi - b.lo + 1;  // 1 or 2
-        int32_t k0 = ring.find(lo_id), k1 = -1;
-        const bool fresh0 = k0 < 0;
-        if (fresh0) k0 = ring.place(lo_id, lo_id, hi_id);
-        bool fresh1 = false;
-        if (n_t > 1) {
-            k1 = ring.find(hi_id);
-            fresh1 = k1 < 0;
-            if (fresh1) k1 = ring.place(hi_id, lo_id, hi_id);
-        }
-        ok = (!fresh0 || wait_kv(k0)) && mbar_wait(&sm.q_full[x], ub & 1, a.err);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s<kF16>(ts, qd, sdesc(smem_u32(sm.kv[k0 % kSlots]), 16, 1024));
-        mma_commit(&sm.s_full[x]);
-        if (n_t == 1) mma_commit(&sm.q_empty[x]);
-        if (!(lo_id >= keep_lo && lo_id <= keep_hi)) mma_commit(&sm.kv_empty[k0 % kSlots]);
+        const int n = b.hi - b.lo + 1;  // 1 .. 4 pages
+        int32_t kidx[4];
+        bool fresh[4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            if (j >= n_t) break;
-            const int64_t tid = lo_id + j;
-            const int32_t kj = j ? k1 : k0;
-            const bool fresh = j ? fresh1 : fresh0;
-            ok = (!fresh || wait_kv(kj + 1)) && mbar_wait(&sm.p_full[x], tcount & 1, a.err) &&
+        for (int j = 0; j < 4; ++j) {
+            kidx[j] = -1;
+            fresh[j] = false;
+            if (j < n) {
+                kidx[j] = ring.find(b.tile_base + b.lo + j);
+                fresh[j] = kidx[j] < 0;
+                if (fresh[j]) kidx[j] = ring.place(b.tile_base + b.lo + j);
+            }
+        }
+        auto qk = [&](int j) {  // QK of page j into buffer (tcount + j) % 2
+            const int32_t ki = kidx[j];
+            bool good = !fresh[j] || wait_kv(ki);
+            if (good) {
+                tc_fence_after();
+                issue_s_page<kF16>(ts0 + 64 * ((tcount + j) & 1), qd, sdesc(smem_u32(sm.kv[ki % kPgSlots]), 16, 1024));
+                mma_commit(&sm.s_full[x][(tcount + j) & 1]);
+                if (j == n - 1) mma_commit(&sm.q_empty[x]);
+                const int64_t pid = b.tile_base + b.lo + j;
+                if (!(pid >= keep_lo && pid <= keep_hi)) mma_commit(&sm.kv_empty[ki % kPgSlots]);
+            }
+            return good;
+        };
+        ok = mbar_wait(&sm.q_full[x], ub & 1, a.err) && qk(0) && (n < 2 || qk(1));
+        if (!ok) break;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j >= n) break;
+            const int32_t t = tcount + j, vi = kidx[j] + 1;
+            ok = (!fresh[j] || wait_kv(vi)) && mbar_wait(&sm.p_full[x][t & 1], (t >> 1) & 1, a.err) &&
                  !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
-            issue_pv<kF16>(to, ts, sdesc(smem_u32(sm.kv[(kj + 1) % kSlots]), kHalfBytes, 1024), j == 0);
-            if (!(tid >= keep_lo && tid <= keep_hi)) mma_commit(&sm.kv_empty[(kj + 1) % kSlots]);
-            if (j + 1 < n_t) {
-                ok = !fresh1 || wait_kv(k1);
+            issue_pv_page<kF16>(to, ts0 + 64 * (t & 1), sdesc(smem_u32(sm.kv[vi % kPgSlots]), kBoxBytes, 1024),
+                                j == 0);
+            mma_commit(&sm.pv_done[x]);
+            const int64_t pid = b.tile_base + b.lo + j;
+            if (!(pid >= keep_lo && pid <= keep_hi)) mma_commit(&sm.kv_empty[vi % kPgSlots]);
+            if (j + 2 < n) {
+                ok = qk(j + 2);
                 if (!ok) break;
-                tc_fence_after();
-                issue_s<kF16>(ts, qd, sdesc(smem_u32(sm.kv[k1 % kSlots]), 16, 1024));
-                mma_commit(&sm.s_full[x]);
-                mma_commit(&sm.q_empty[x]);
-                if (!(hi_id >= keep_lo && hi_id <= keep_hi)) mma_commit(&sm.kv_empty[k1 % kSlots]);
-            } else {
-                mma_commit(&sm.o_final[x]);  // the head's O is final once this completes
             }
-            ++tcount;
+            if (j == n - 1) mma_commit(&sm.o_final[x]);  // the head's O is final once this completes
         }
+        if (!ok) break;
+        tcount += n;
         w = nw;
     }
     if (!ok) sm.abort = 1;
@@ -990,18 +1039,20 @@ __device__ void swa_softmax(SwaSmem &sm, const CUtensorMap *to, const PrefillArg
         const int32_t t = d.p0 + min(r, last);
         const int32_t t_first = d.p0 + min(warp * 32, last), t_last = d.p0 + min(warp * 32 + 31, last);
         float m_used = -INFINITY, l = 0.f;
-        for (int32_t tile = lo; tile <= hi; ++tile, ++tcount) {
-            // S of this tile: the MMA thread writes the next S only after
-            // this tile's P has been read, so the wait is never two phases
-            // behind
-            ok = mbar_wait(&sm.s_full[x], tcount & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+        for (int32_t pg = lo; pg <= hi; ++pg, ++tcount) {
+            // S of this page in buffer tcount % 2: the MMA thread writes
+            // that buffer again only after this page's P has been read, so
+            // the wait is never two phases behind
+            const int buf = tcount & 1;
+            ok = mbar_wait(&sm.s_full[x][buf], (tcount >> 1) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            softmax_tile_band<kF16>(t_s, t_s + 256, tile * kBN, t, t_first, t_last, a.window, a.scale_log2,
-                                    tile == lo, m_used, l);
+            ok = softmax_page_band<kF16>(t_s + 64 * buf, t_s + 256, pg * kP, t, t_first, t_last, a.window,
+                                         a.scale_log2, pg == lo, m_used, l, &sm.pv_done[x], (tcount - 1) & 1, a.err);
+            if (!ok) break;
             tc_fence_before();
-            mbar_arrive(&sm.p_full[x]);
+            mbar_arrive(&sm.p_full[x][buf]);
         }
         const bool fin = ok && mbar_wait(&sm.o_final[x], ub & 1, a.err);
         if (!__all_sync(0xffffffffu, fin)) {
@@ -1038,13 +1089,16 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
             mbar_init(&sm.q_full[i], 1);
             mbar_init(&sm.q_empty[i], 1);
         }
-        for (int i = 0; i < kSlots; ++i) {
+        for (int i = 0; i < kPgSlots; ++i) {
             mbar_init(&sm.kv_full[i], 1);
             mbar_init(&sm.kv_empty[i], 2);  // one commit from each head's issuer
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(&sm.s_full[x], 1);
-            mbar_init(&sm.p_full[x], 128);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&sm.s_full[x][b], 1);
+                mbar_init(&sm.p_full[x][b], 128);
+            }
+            mbar_init(&sm.pv_done[x], 1);
             mbar_init(&sm.o_final[x], 1);
         }
         mbar_init(&sm.mma_done[0], 1);
@@ -1308,8 +1362,8 @@ int launch_prefill_tc(const hswa_config &c, int32_t window, const void *k_pool, 
         const int sms = sm_count();
         if (sms <= 0) return HSWA_ERR_CUDA;
         CUtensorMap to;
-        if (!make_tmap_3d(&to, o, kD, c.n_q_heads, (uint64_t)total_q, 64, 1, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!make_tmap_3d(&to, o, kD, c.n_q_heads, (uint64_t)total_q, 32, 1, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_64B))
             return cuda_fail(cudaErrorInvalidValue, "prefill output tensor map");
         const int64_t units = (int64_t)n_seqs * ((max_q_len + kBM - 1) / kBM + 1) * (c.n_q_heads / 2);
         const dim3 grid((unsigned)std::min<int64_t>(sms, units));
