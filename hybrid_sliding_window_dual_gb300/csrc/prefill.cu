@@ -86,6 +86,28 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// O *= alpha for this thread's row (TMEM, warp-wide): the rare lazy
+// rescale, kept out of line so the page loop stays small.
+__device__ __noinline__ void rescale_o_row(uint32_t t_o, float alpha) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(t_o + 32 * c, ov);
+        tmem_wait_ld(ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+        tmem_st32(t_o + 32 * c, ov);
+    }
+}
+
+// Out-of-line slow part of a wait: the spin after a first try failed.
+__device__ __noinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, int *err) {
+    return mbar_wait(bar, parity, err);
+}
+__device__ __forceinline__ bool mbar_wait_small(uint64_t *bar, uint32_t parity, int *err) {
+    return mbar_try_wait(bar, parity) || mbar_wait_spin(bar, parity, err);
+}
+
 // ------------------------------------------------------------- work unit
 struct Unit {
     int32_t s, qb, hp, g;
@@ -165,7 +187,7 @@ __device__ void prefill_producer(PrefillSmem &sm, const CUtensorMap *tq, const C
     int issued = 0;
     for (int i = 0; i < 2 * u.n_tiles; ++i) {
         const int slot = i % kSlots;
-        if (!mbar_wait(&sm.kv_empty[slot], ((i / kSlots) & 1) ^ 1, a.err) || *(volatile int32_t *)&sm.abort) {
+        if (!mbar_wait_small(&sm.kv_empty[slot], ((i / kSlots) & 1) ^ 1, a.err) || *(volatile int32_t *)&sm.abort) {
             sm.abort = 1;
             break;
         }
@@ -188,7 +210,7 @@ __device__ void prefill_producer(PrefillSmem &sm, const CUtensorMap *tq, const C
         ++issued;
     }
     // drain: never leave copies landing in shared memory after the CTA ends
-    for (int i = max(0, issued - kSlots); i < issued; ++i) mbar_wait(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err);
+    for (int i = max(0, issued - kSlots); i < issued; ++i) mbar_wait_small(&sm.kv_full[i % kSlots], (i / kSlots) & 1, a.err);
 }
 
 // S_x = Q_x K^T over d = 128: 8 steps of K = 16 (32 bytes inside a 128-byte
@@ -222,11 +244,11 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
     const uint32_t tbase = sm.tmem_base;
     const uint32_t ts0 = tbase, ts1 = tbase + 128, to0 = tbase + 256, to1 = tbase + 384;
     const uint64_t qd0 = sdesc(smem_u32(sm.q[0]), 16, 1024), qd1 = sdesc(smem_u32(sm.q[1]), 16, 1024);
-    bool ok = mbar_wait(&sm.q_full, 0, a.err);
+    bool ok = mbar_wait_small(&sm.q_full, 0, a.err);
     tc_fence_after();
     const int n = u.n_tiles;
     if (ok && n > 0) {
-        ok = mbar_wait(&sm.kv_full[0], 0, a.err);  // K(0)
+        ok = mbar_wait_small(&sm.kv_full[0], 0, a.err);  // K(0)
         if (ok) {
             tc_fence_after();
             const uint64_t k0 = sdesc(smem_u32(sm.kv[0]), 16, 1024);
@@ -239,7 +261,7 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
         for (int j = 0; ok && j < n; ++j) {
             const int iv = 2 * j + 1, ik = 2 * j + 2;  // ring items V(j), K(j + 1)
             const int sv = iv % kSlots, sk = ik % kSlots;
-            ok = mbar_wait(&sm.kv_full[sv], (iv / kSlots) & 1, a.err) && mbar_wait(&sm.p_full[0], j & 1, a.err) &&
+            ok = mbar_wait_small(&sm.kv_full[sv], (iv / kSlots) & 1, a.err) && mbar_wait_small(&sm.p_full[0], j & 1, a.err) &&
                  !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
@@ -248,14 +270,14 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
             const bool more = j + 1 < n;
             uint64_t kd = 0;
             if (more) {
-                ok = mbar_wait(&sm.kv_full[sk], (ik / kSlots) & 1, a.err);
+                ok = mbar_wait_small(&sm.kv_full[sk], (ik / kSlots) & 1, a.err);
                 if (!ok) break;
                 tc_fence_after();
                 kd = sdesc(smem_u32(sm.kv[sk]), 16, 1024);
                 issue_s<kF16>(ts0, qd0, kd);
                 mma_commit(&sm.s_full[0]);
             }
-            ok = mbar_wait(&sm.p_full[1], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+            ok = mbar_wait_small(&sm.p_full[1], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
             issue_pv<kF16>(to1, ts1, vd, j == 0);
@@ -279,6 +301,7 @@ __device__ void prefill_mma(PrefillSmem &sm, const PrefillArgs &a, const Unit &u
 // the running max (log2 units) and sum, write P over the start of S, and
 // rescale O in TMEM when the max grows by more than 2^8. TMEM loads and
 // stores are warp-wide: every lane of the warp calls this.
+
 template <bool kF16>
 __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int32_t k0, int32_t t, int32_t t_min,
                                              int32_t t_max, int32_t W, float scale_log2, bool first_tile,
@@ -344,17 +367,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int32_t
     // the O rescale comes after the P store (the S registers are free
     // then); the whole warp takes this path when any of its rows needs it
     // (the others scale by 1)
-    if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(t_o + 32 * c, ov);
-            tmem_wait_ld(ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(t_o + 32 * c, ov);
-        }
-    }
+    if (__any_sync(0xffffffffu, resc)) rescale_o_row(t_o, alpha);
     const float2 s01 = __fadd2_rn(sums[0], sums[1]), s23 = __fadd2_rn(sums[2], sums[3]);
     const float2 sum2 = __fadd2_rn(s01, s23);
     l = l * alpha + (sum2.x + sum2.y);
@@ -431,19 +444,9 @@ __device__ __forceinline__ bool softmax_page_band(uint32_t t_s, uint32_t t_o, in
     }
     bool ok = true;
     if (__any_sync(0xffffffffu, resc)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(pv_bar, pv_par, err));
+        ok = __all_sync(0xffffffffu, mbar_wait_small(pv_bar, pv_par, err));
         tc_fence_after();
-        if (ok) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(t_o + 32 * c, ov);
-                tmem_wait_ld(ov);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                tmem_st32(t_o + 32 * c, ov);
-            }
-        }
+        if (ok) rescale_o_row(t_o, alpha);
     }
     const float2 sum2 = __fadd2_rn(sums[0], sums[1]);
     l = l * alpha + (sum2.x + sum2.y);
@@ -453,7 +456,29 @@ __device__ __forceinline__ bool softmax_page_band(uint32_t t_s, uint32_t t_o, in
 
 // Normalise this thread's row of O (TMEM) by 1 / l and store it as bf16 at
 // dst (when valid; the TMEM loads are warp-wide, every lane calls this).
-__device__ __forceinline__ void store_o_row(uint32_t t_o, float l, __nv_bfloat16 *dst_row, bool valid) {
+__device__ __noinline__ void store_o_row(uint32_t t_o, float l, __nv_bfloat16 *dst_row, bool valid) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(t_o + 32 * c, ov);
+        tmem_wait_ld(ov);
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
+                w.y = pack_bf16(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
+                w.z = pack_bf16(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
+                w.w = pack_bf16(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
+                dst[c * 4 + i] = w;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void store_o_row_inl(uint32_t t_o, float l, __nv_bfloat16 *dst_row, bool valid) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
 #pragma unroll
@@ -538,7 +563,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
     float m_used = -INFINITY, l = 0.f;  // running max (log2 units) and sum of P
     bool ok = true;
     for (int j = 0; j < u.n_tiles; ++j) {
-        ok = mbar_wait(&sm.s_full[x], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+        ok = mbar_wait_small(&sm.s_full[x], j & 1, a.err) && !*(volatile int32_t *)&sm.abort;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -549,7 +574,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
     }
     // epilogue: wait for the last PV (always: TMEM is freed after this
     // function returns), normalise this row of O and store it
-    const bool fin = mbar_wait(&sm.o_final[x], 0, a.err);
+    const bool fin = mbar_wait_small(&sm.o_final[x], 0, a.err);
     ok = __all_sync(0xffffffffu, ok && fin);
     if (!ok) {
         sm.abort = 1;
@@ -557,7 +582,7 @@ __device__ void prefill_softmax(PrefillSmem &sm, const PrefillArgs &a, const Uni
     }
     tc_fence_after();
     const int h = 2 * u.hp + x;
-    store_o_row(t_o, l, a.o + ((int64_t)(u.row0 + r) * a.hq + h) * kD, r < u.n_rows);
+    store_o_row_inl(t_o, l, a.o + ((int64_t)(u.row0 + r) * a.hq + h) * kD, r < u.n_rows);
 }
 
 template <bool kF16>
@@ -821,7 +846,7 @@ __device__ void swa_load_q(SwaSmem &sm, const CUtensorMap *tq, const PrefillArgs
         // the unit's descriptor for the softmax warps; its slot was freed
         // (all 256 softmax threads arrived) when unit ub - 4 was stored
         const int dslot = ub % kDescs;
-        bool ok = ub < kDescs || (mbar_wait(&sm.desc_empty[dslot], ((ub / kDescs) + 1) & 1, a.err) &&
+        bool ok = ub < kDescs || (mbar_wait_small(&sm.desc_empty[dslot], ((ub / kDescs) + 1) & 1, a.err) &&
                                   !*(volatile int32_t *)&sm.abort);
         if (ok) {
             SwaDesc &d = sm.desc[dslot];
@@ -839,7 +864,7 @@ __device__ void swa_load_q(SwaSmem &sm, const CUtensorMap *tq, const PrefillArgs
             // last QK MMA; parity waits stay at most one phase behind
             // because each item waits for the release of the one before
             if (qi >= kQBufs)
-                ok = mbar_wait(&sm.q_empty[slot], ((qi / kQBufs) + 1) & 1, a.err) &&
+                ok = mbar_wait_small(&sm.q_empty[slot], ((qi / kQBufs) + 1) & 1, a.err) &&
                      !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             mbar_arrive_expect_tx(&sm.q_full[slot], kTileBytes);
@@ -855,7 +880,7 @@ __device__ void swa_load_q(SwaSmem &sm, const CUtensorMap *tq, const PrefillArgs
     }
     // drain: never leave copies landing in shared memory after the CTA ends
     for (int32_t i = max(0, issued - kQBufs); i < issued; ++i)
-        mbar_wait(&sm.q_full[i % kQBufs], (i / kQBufs) & 1, a.err);
+        mbar_wait_small(&sm.q_full[i % kQBufs], (i / kQBufs) & 1, a.err);
 }
 
 __device__ void swa_load_kv(SwaSmem &sm, const CUtensorMap *tk, const CUtensorMap *tv, const PrefillArgs &a,
@@ -890,7 +915,7 @@ __device__ void swa_load_kv(SwaSmem &sm, const CUtensorMap *tk, const CUtensorMa
                 // the slot's previous load (i - 8) belongs to a page no
                 // later block of this CTA needs; both issuers released it
                 if (i >= kPgSlots)
-                    ok = mbar_wait(&sm.kv_empty[slot], ((i / kPgSlots) + 1) & 1, a.err) &&
+                    ok = mbar_wait_small(&sm.kv_empty[slot], ((i / kPgSlots) + 1) & 1, a.err) &&
                          !*(volatile int32_t *)&sm.abort;
                 if (!ok) break;
                 mbar_arrive_expect_tx(&sm.kv_full[slot], kPgBytes);
@@ -903,7 +928,7 @@ __device__ void swa_load_kv(SwaSmem &sm, const CUtensorMap *tk, const CUtensorMa
     }
     if (!ok) sm.abort = 1;
     for (int32_t i = max(0, issued - kPgSlots); i < issued; ++i)
-        mbar_wait(&sm.kv_full[i % kPgSlots], (i / kPgSlots) & 1, a.err);
+        mbar_wait_small(&sm.kv_full[i % kPgSlots], (i / kPgSlots) & 1, a.err);
 }
 
 // S = Q K^T for one 64-key page: 8 steps of K = 16 over d (the Q tile's d
@@ -947,7 +972,7 @@ __device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs, int x)
     ring.init();
     int32_t tcount = 0;  // pages so far: S buffer tcount % 2, phase (tcount / 2) & 1
     bool ok = true;
-    auto wait_kv = [&](int32_t i) { return mbar_wait(&sm.kv_full[i % kPgSlots], (i / kPgSlots) & 1, a.err); };
+    auto wait_kv = [&](int32_t i) { return mbar_wait_small(&sm.kv_full[i % kPgSlots], (i / kPgSlots) & 1, a.err); };
     for (int32_t ub = 0; ok && ub < sm.n_units; ++ub) {
         const SwaBlock b = swa_block(w, a, pairs);
         SwaWalk nw = w;
@@ -985,13 +1010,13 @@ __device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs, int x)
             }
             return good;
         };
-        ok = mbar_wait(&sm.q_full[x], ub & 1, a.err) && qk(0) && (n < 2 || qk(1));
+        ok = mbar_wait_small(&sm.q_full[x], ub & 1, a.err) && qk(0) && (n < 2 || qk(1));
         if (!ok) break;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (j >= n) break;
             const int32_t t = tcount + j, vi = kidx[j] + 1;
-            ok = (!fresh[j] || wait_kv(vi)) && mbar_wait(&sm.p_full[x][t & 1], (t >> 1) & 1, a.err) &&
+            ok = (!fresh[j] || wait_kv(vi)) && mbar_wait_small(&sm.p_full[x][t & 1], (t >> 1) & 1, a.err) &&
                  !*(volatile int32_t *)&sm.abort;
             if (!ok) break;
             tc_fence_after();
@@ -1013,7 +1038,7 @@ __device__ void swa_mma(SwaSmem &sm, const PrefillArgs &a, int32_t pairs, int x)
     if (!ok) sm.abort = 1;
     // every MMA issued above has completed before the TMEM is freed
     mma_commit(&sm.mma_done[x]);
-    mbar_wait(&sm.mma_done[x], 0, a.err);
+    mbar_wait_small(&sm.mma_done[x], 0, a.err);
 }
 
 template <bool kF16>
@@ -1026,7 +1051,7 @@ __device__ void swa_softmax(SwaSmem &sm, const CUtensorMap *to, const PrefillArg
     int32_t tcount = 0;
     for (int32_t ub = 0; ub < sm.n_units; ++ub) {
         const int dslot = ub % kDescs;
-        bool ok = mbar_wait(&sm.desc_full[dslot], (ub / kDescs) & 1, a.err);
+        bool ok = mbar_wait_small(&sm.desc_full[dslot], (ub / kDescs) & 1, a.err);
         if (!__all_sync(0xffffffffu, ok)) {
             sm.abort = 1;
             break;
@@ -1044,7 +1069,7 @@ __device__ void swa_softmax(SwaSmem &sm, const CUtensorMap *to, const PrefillArg
             // that buffer again only after this page's P has been read, so
             // the wait is never two phases behind
             const int buf = tcount & 1;
-            ok = mbar_wait(&sm.s_full[x][buf], (tcount >> 1) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
+            ok = mbar_wait_small(&sm.s_full[x][buf], (tcount >> 1) & 1, a.err) && !*(volatile int32_t *)&sm.abort;
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -1054,7 +1079,7 @@ __device__ void swa_softmax(SwaSmem &sm, const CUtensorMap *to, const PrefillArg
             tc_fence_before();
             mbar_arrive(&sm.p_full[x][buf]);
         }
-        const bool fin = ok && mbar_wait(&sm.o_final[x], ub & 1, a.err);
+        const bool fin = ok && mbar_wait_small(&sm.o_final[x], ub & 1, a.err);
         if (!__all_sync(0xffffffffu, fin)) {
             sm.abort = 1;
             break;
