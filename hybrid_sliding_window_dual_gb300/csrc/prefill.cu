@@ -86,6 +86,12 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Two fp32 values (bit patterns) times inv2, as a bf16 pair.
+__device__ __forceinline__ uint32_t scale_pack_bf16(uint32_t a, uint32_t b, float2 inv2) {
+    const float2 y = __fmul2_rn(make_float2(__uint_as_float(a), __uint_as_float(b)), inv2);
+    return pack_bf16(y.x, y.y);
+}
+
 // O *= alpha for this thread's row (TMEM, warp-wide): the rare lazy
 // rescale, kept out of line so the page loop stays small.
 __device__ __noinline__ void rescale_o_row(uint32_t t_o, float alpha) {
@@ -513,7 +519,9 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t t_o, float l, uint8
         store_o_row(t_o, l, dst_row, valid);
         return;
     }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    // 1 / l to within 2 ulp (the row is rounded to bf16 after the multiply)
+    const float inv = l > 0.f ? __fdividef(1.f, l) : 0.f;
+    const float2 inv2 = make_float2(inv, inv);
     const int lane = threadIdx.x & 31;
     uint32_t ov[2][32];
     auto put = [&](int qt, const uint32_t (&v)[32]) {
@@ -524,10 +532,10 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t t_o, float l, uint8
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // 16-byte chunk j: columns 8j .. 8j + 7 of the quarter
             uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[8 * j + 0]) * inv, __uint_as_float(v[8 * j + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(v[8 * j + 2]) * inv, __uint_as_float(v[8 * j + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(v[8 * j + 4]) * inv, __uint_as_float(v[8 * j + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(v[8 * j + 6]) * inv, __uint_as_float(v[8 * j + 7]) * inv);
+            w.x = scale_pack_bf16(v[8 * j + 0], v[8 * j + 1], inv2);
+            w.y = scale_pack_bf16(v[8 * j + 2], v[8 * j + 3], inv2);
+            w.z = scale_pack_bf16(v[8 * j + 4], v[8 * j + 5], inv2);
+            w.w = scale_pack_bf16(v[8 * j + 6], v[8 * j + 7], inv2);
             *reinterpret_cast<uint4 *>(row + ((j ^ ((lane >> 1) & 3)) << 4)) = w;
         }
         fence_proxy_async_shared();  // the buffer is read by the TMA store
