@@ -24,6 +24,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -75,16 +76,23 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 100 ms in the background; with mark() the
+    summary keeps only the samples taken between the first and the last
+    mark (host clock)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, tag=""):
         self.gpu = gpu_index
         self.proc = None
         # raw samples (the JSON line carries their summary); HSWA_CLOCKS_DIR picks the folder
         out = os.environ.get("HSWA_CLOCKS_DIR") or os.path.join(ROOT, "bench_out")
-        self.path = os.path.join(out, "clocks_rank%d.csv" % gpu_index)
+        self.path = os.path.join(out, "clocks%s_rank%d.csv" % (tag, gpu_index))
+        self.marks = []
+
+    def mark(self):
+        self.marks.append(time.time())
 
     def start(self):
         try:
@@ -107,16 +115,21 @@ class ClockSampler:
         self.fh.close()
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        lo, hi = (min(self.marks), max(self.marks)) if len(self.marks) >= 2 else (None, None)
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                if lo is not None:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    if not lo <= ts <= hi:
+                        continue
+                sm.append(float(parts[2]))
+                mx = float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            for name, val in zip(names, parts[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
@@ -615,10 +628,16 @@ class ChunkedPrefill:
             raise RuntimeError("device status %d after benchmark" % st)
 
 
-def measure_prefill(steps, warmup, w, fp8=False):
+def measure_prefill(steps, warmup, w, fp8=False, clocks=None):
     """Whole-chunk TFLOP/s of the chunked-prefill workload (valid pairs only);
-    over FP8 pools when fp8 (the staging pass is inside each layer's time)."""
+    over FP8 pools when fp8 (the staging pass is inside each layer's time).
+    clocks: a ClockSampler, summarised over the warm-up and timed steps."""
+    if clocks is not None:
+        clocks.start()  # before the set-up, so that sampling runs by the first step
     pb = ChunkedPrefill(w, fp8=fp8)
+    if clocks is not None:
+        pb.stream.synchronize()
+        clocks.mark()
     for _ in range(warmup):
         pb.step()
     pb.stream.synchronize()
@@ -629,6 +648,9 @@ def measure_prefill(steps, warmup, w, fp8=False):
         pb.step(timed=True)
     e1.record(pb.stream)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark()
+    clock_info = clocks.stop() if clocks is not None else None
     secs = e0.elapsed_time(e1) / 1e3
     f = pb.flops()
     full_ms = float(np.mean([a.elapsed_time(b) for a, b in pb.events[0]]))
@@ -641,7 +663,7 @@ def measure_prefill(steps, warmup, w, fp8=False):
             "swa_tflops": f["swa"] / (swa_ms / 1e3) / 1e12, "swa_ms": swa_ms,
             "swa_exec_tflops": f["swa_exec"] / (swa_ms / 1e3) / 1e12,
             "valid_tflop_per_step": f["step"] / 1e12, "tokens_per_s": pb.T * steps / secs,
-            "launches": pb.launches}
+            "launches": pb.launches, "clocks": clock_info}
 
 
 def fill_normal(t, seed):
@@ -1077,7 +1099,8 @@ def run_decode(args, world, rank, local):
         del bench
         torch.cuda.empty_cache()
         _, bf16, bf16_sus, _ = peaks()
-        pf = measure_prefill(args.prefill_steps, 1, workload(args, "chunked_prefill"))
+        pf = measure_prefill(args.prefill_steps, 1, workload(args, "chunked_prefill"),
+                             clocks=ClockSampler(local, "_prefill"))
         line["prefill"] = {
             "workload": "chunked_prefill (8 seqs, prefix U[8192,65536] seed 3, chunk 4096, Full + SWA layer)",
             "tflops": round(pf["step_tflops"], 1), "unit": "TFLOP/s", "frac": round(pf["step_tflops"] / bf16, 4),
@@ -1091,7 +1114,7 @@ def run_decode(args, world, rank, local):
             "swa_layer_frac": round(pf["swa_tflops"] / bf16, 4),
             "valid_tflop_per_step": round(pf["valid_tflop_per_step"], 3),
             "ms_per_step": round(pf["ms_per_step"], 3), "tokens_per_s": round(pf["tokens_per_s"], 1),
-            "kernel": pf["kernel"], "swa_kernel": pf["swa_kernel"]}
+            "kernel": pf["kernel"], "swa_kernel": pf["swa_kernel"], "clocks": pf["clocks"]}
         if not args.no_fp8:
             del pf
             torch.cuda.empty_cache()
