@@ -275,10 +275,10 @@ def measure_decode_multi(reps, w, token_counts=(1, 2, 3, 4, 8, 16), fp8=False):
 
 def prefill_flops(w, prefix, chunk):
     """Valid (query, key) pairs x 4 d Hq for a Full and an SWA layer, and the
-    pairs the tensor-core kernels execute: 128 query rows x 128 keys per key
-    tile of a block. Full-layer blocks are 128 chunk rows from the prefix and
-    read key tiles [0, last row]; SWA blocks (W <= 128) sit on 128-position
-    boundaries and read the tiles from their first row's window start."""
+    pairs the tensor-core kernels execute. Full-layer blocks are 128 chunk
+    rows from the prefix and read 128-key tiles [0, last row]; SWA blocks
+    (W <= 128) sit on 128-position boundaries and read the 64-key pages from
+    their first row's window start to their last row."""
     full = sum(c * p + c * (c + 1) // 2 for p, c in zip(prefix, chunk))
     swa = sum(sum(min(p + r + 1, w.window) for r in range(c)) for p, c in zip(prefix, chunk))
     full_exec = swa_exec = 0
@@ -288,11 +288,21 @@ def prefill_flops(w, prefix, chunk):
             full_exec += (last // 128 + 1) * 128 * 128
         if c > 0:
             for m in range(p // 128, (p + c - 1) // 128 + 1):
-                p0 = max(p, 128 * m)
-                swa_exec += (m - max(0, p0 - w.window + 1) // 128 + 1) * 128 * 128
+                p0, p_end = max(p, 128 * m), min(p + c, 128 * (m + 1))
+                P = w.page_size
+                swa_exec += ((p_end - 1) // P - max(0, p0 - w.window + 1) // P + 1) * P * 128
     k = 4 * w.head_dim * w.n_q_heads
     return {"full": k * full, "swa": k * swa, "step": k * (full + swa), "full_exec": k * full_exec,
             "swa_exec": k * swa_exec}
+
+
+def swa_prefill_bytes(w, prefix, chunk):
+    """Algorithmic bytes of an SWA layer's chunk: q read and o written
+    (rows x Hq x d) and every K / V page the chunk's windows touch, once."""
+    es, P = KV_ROW[w.dtype], w.page_size
+    qo = 2 * sum(chunk) * w.n_q_heads * w.head_dim * es
+    pages = sum((p + c - 1) // P - max(0, p - w.window + 1) // P + 1 for p, c in zip(prefix, chunk) if c > 0)
+    return qo + pages * w.n_kv_heads * 2 * P * w.head_dim * es
 
 
 class DecodeBatch:
@@ -662,6 +672,7 @@ def measure_prefill(steps, warmup, w, fp8=False, clocks=None):
             "full_exec_tflops": f["full_exec"] / (full_ms / 1e3) / 1e12,
             "swa_tflops": f["swa"] / (swa_ms / 1e3) / 1e12, "swa_ms": swa_ms,
             "swa_exec_tflops": f["swa_exec"] / (swa_ms / 1e3) / 1e12,
+            "swa_gbs": swa_prefill_bytes(w, pb.prefix.tolist(), [pb.C] * pb.B) / (swa_ms / 1e3) / 1e9,
             "valid_tflop_per_step": f["step"] / 1e12, "tokens_per_s": pb.T * steps / secs,
             "launches": pb.launches, "clocks": clock_info}
 
@@ -1098,7 +1109,7 @@ def run_decode(args, world, rank, local):
     if not args.no_prefill:
         del bench
         torch.cuda.empty_cache()
-        _, bf16, bf16_sus, _ = peaks()
+        hbm, bf16, bf16_sus, _ = peaks()
         pf = measure_prefill(args.prefill_steps, 1, workload(args, "chunked_prefill"),
                              clocks=ClockSampler(local, "_prefill"))
         line["prefill"] = {
@@ -1112,6 +1123,7 @@ def run_decode(args, world, rank, local):
             "swa_layer_tflops": round(pf["swa_tflops"], 2), "swa_layer_ms": round(pf["swa_ms"], 3),
             "swa_layer_exec_tflops": round(pf["swa_exec_tflops"], 2),
             "swa_layer_frac": round(pf["swa_tflops"] / bf16, 4),
+            "swa_layer_gbs": round(pf["swa_gbs"], 1), "swa_layer_hbm_frac": round(pf["swa_gbs"] / hbm, 4),
             "valid_tflop_per_step": round(pf["valid_tflop_per_step"], 3),
             "ms_per_step": round(pf["ms_per_step"], 3), "tokens_per_s": round(pf["tokens_per_s"], 1),
             "kernel": pf["kernel"], "swa_kernel": pf["swa_kernel"], "clocks": pf["clocks"]}
