@@ -13,7 +13,8 @@
 //     the PV MMA straight from TMEM.
 //   * Warp 8 streams Q (once) and K / V tiles of 128 keys (two pages, two
 //     64-column boxes per page, 128-byte swizzle) by TMA into a 4-slot ring.
-//   * Warp 9 issues the MMAs (one thread) and commits them to mbarriers.
+//   * Warp 9 issues the MMAs of both heads (one thread, the heads in
+//     lockstep over each K / V tile) and commits them to mbarriers.
 //   * Warps 0-3 and 4-7 own query head A and B: one thread per query row
 //     reads its row of S from TMEM, applies the causal / window mask on the
 //     tiles that need it, keeps the running max in the log2 domain and only
@@ -21,6 +22,9 @@
 //     and at the end normalises its row of O and stores it.
 //   * The KV range of a block is clipped to the tiles its rows can see: all
 //     of [0, t] for a Full layer, [t - W + 1, t] for an SWA layer.
+// SWA layers with W <= 128 run a persistent window kernel instead
+// (prefill_swa_tc_d128, below): 64-key pages, two score buffers per head,
+// an MMA issuer per head and the pages of a block reused by its head pairs.
 // Every wait is bounded; on a timeout the CTA records HSWA_ERR_TIMEOUT,
 // drains its copies and MMAs, frees its TMEM and returns.
 //
@@ -1093,8 +1097,8 @@ __device__ void swa_softmax(SwaSmem &sm, const CUtensorMap *to, const PrefillArg
             break;
         }
         tc_fence_after();
-        // O is read before this thread reports the next tile's P, and the
-        // first PV of the next unit (which overwrites O) waits for that P
+        // O is read before this thread reports the next unit's first P, and
+        // the first PV of the next unit (which overwrites O) waits for that P
         const int32_t h = 2 * d.hp + x;
         store_o_rows_staged(t_s + 256, l, stage, to, h, d.row0 + warp * 32, warp * 32 + 31 <= last,
                             a.o + ((int64_t)(d.row0 + r) * a.hq + h) * kD, r <= last);
@@ -1391,7 +1395,7 @@ int launch_prefill_tc(const hswa_config &c, int32_t window, const void *k_pool, 
         kernel_setup(prefill_swa_tc_d128<true>, kSwaSmemBytes, kSwaThreads, swa_h) < 0)
         return cuda_fail(cudaGetLastError(), "prefill_swa_tc_d128 shared memory");
     if (window > 0 && window <= kBN) {
-        // at most two key tiles per block: the persistent window kernel
+        // at most four 64-key pages per block: the persistent window kernel
         const int sms = sm_count();
         if (sms <= 0) return HSWA_ERR_CUDA;
         CUtensorMap to;
