@@ -162,6 +162,20 @@ def test_prefill_swa_windows_many_sequences(W):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("W", [128, 64])
+def test_prefill_swa_many_short_sequences(W):
+    """300 sequences with chunks of 0-150 tokens: each persistent CTA's share
+    of the window kernel's unit list runs across many sequences, partial
+    blocks and kv heads, so its K / V page ring is refilled at every
+    sequence boundary; every row against the oracle."""
+    rng = np.random.default_rng(300 + W)
+    cached = [int(x) for x in rng.integers(0, 700, size=300)]
+    chunk = [int(x) for x in rng.integers(0, 151, size=300)]
+    sc = Scenario(16, 2, 128, 64, W, wl.DTYPE_BF16, cached, layer_kinds=(SWA,), seed=21, extra_tokens=160)
+    run_prefill_chunk(sc, chunk, seed=11, expect_kernel=True)
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("cached,chunk", [([1000], [5]), ([0], [1]), ([127], [130]), ([300, 0], [0, 700])])
 def test_prefill_swa_few_units(cached, chunk):
     """Chunks so small that most CTAs of the persistent window kernel get no
