@@ -413,6 +413,11 @@ class DecodeBatch:
         buf = self.steps_done & 1
         if self.slot_ready[buf] is not None:
             self.slot_ready[buf].synchronize()
+        if host_io:
+            # the result of the step two back, which used output block buf,
+            # is read on the host before this step's copy overwrites it:
+            # two steps stay in flight
+            self.read_output(buf)
         with torch.cuda.stream(self.stream):
             q, kn, vn = self.q, self.kn, self.vn
             if host_io:
@@ -461,9 +466,6 @@ class DecodeBatch:
         self.steps_done += 1
         if self.steps_done % 64 == 0:
             sess.release(range(B))
-        if host_io:
-            # the previous step's result is read on the host (this one's next)
-            self.read_output(1 - buf)
 
     def copy_in(self, b):
         """Copy a step's inputs from pinned host memory into input block b on
@@ -1036,7 +1038,7 @@ def run_decode(args, world, rank, local):
     e2e_before = decode_bytes(w, bench.lens() + 1)
     e2e_secs = time_steps(lambda: bench.step(host_io=True), args.steps, bench.stream, world,
                           finish=bench.join_copies)
-    for b in range(2):  # the last step's result
+    for b in range(2):  # the last two steps' results
         bench.read_output(b)
     e2e_after = decode_bytes(w, bench.lens())
     e2e_step_bytes = 0.5 * (e2e_before["step"] + e2e_after["step"])
