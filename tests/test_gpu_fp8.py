@@ -271,12 +271,13 @@ def test_fp8_multi_token_decode_steps_with_release():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("n_tok", [2, 8])
+@pytest.mark.parametrize("n_tok", [2, 4, 8, 16])
 def test_fp8_multi_token_full_size_sampled(n_tok):
     """The decode-batch workload over FP8 pools with n_tok query tokens per
-    sequence, oracle on sampled sequences."""
+    sequence, oracle on sampled sequences: two tokens per mma.sync pass, and
+    the tensor-core kernel with 4, 2 and 1 copies of the rows."""
     w = wl.decode_batch()
-    c = Fp8Case(list(w.cached), seed=82, extra=8)
+    c = Fp8Case(list(w.cached), seed=82, extra=max(8, n_tok))
     fp8_multi_step(c, n_tok, seed=1500 + n_tok, samples=[0, 1, 17, 31, 32, 50, 63])
 
 
