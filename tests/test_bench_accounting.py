@@ -145,3 +145,35 @@ def test_clock_record_keeps_only_the_marked_window(tmp_path, monkeypatch):
     c.marks = [now, now + 2]
     info = c.stop()
     assert info["samples"] == 3 and info["sm_mhz"] == 2070.0 and info["reasons"] == ["sw_power_cap"]
+
+
+def _reference_line(env):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
+                       cwd=root, env={**os.environ, **env}, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_line_keeps_the_contract():
+    """The reference arm (the oracle on the host cores) prints one JSON line
+    with the keys, types and units of the library's own line, and an e2e
+    object of its own value with no host-device bytes."""
+    lines = _reference_line({"RANK": "0", "WORLD_SIZE": "1"})
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None and d["data"] == "synthetic"
+    assert d["config"]["workload"] == "decode_batch"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    assert _reference_line({"RANK": "1", "WORLD_SIZE": "2"}) == []
