@@ -161,6 +161,31 @@ def test_device_calls_validate_before_launching():
     H.hswa_pool_destroy(lp)
 
 
+def test_empty_batches_return_before_any_launch():
+    """A chunked prefill with no sequences or no query rows, and a window
+    gather or scatter with no sequences, return HSWA_OK before touching a
+    device pointer (the pointers given here are not device memory)."""
+    cfg, lp, _ = make_pair()
+    full = H.Layer(kind=H.HSWA_KIND_FULL, window=0, k_pool=16, v_pool=16)
+    swa = H.Layer(kind=H.HSWA_KIND_SWA, window=128, k_pool=16, v_pool=16)
+    for layer in (full, swa):
+        H.hswa_prefill_chunk(lp, layer, 16, 16, 16, 16, 16, 0, 0, 0, 1.0)
+        H.hswa_prefill_chunk(lp, layer, 16, 16, 16, 16, 16, 3, 0, 0, 1.0)
+    H.hswa_swa_gather(lp, swa, 16, 16, 16, 0, 16)
+    H.hswa_swa_scatter(lp, swa, 16, 16, 16, 0, 16)
+    # but a negative count, or more rows in one sequence than in the chunk, is refused
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_prefill_chunk(lp, full, 16, 16, 16, 16, 16, -1, 0, 0, 1.0)
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_prefill_chunk(lp, full, 16, 16, 16, 16, 16, 2, 3, 4, 1.0)
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    with pytest.raises(H.HswaError) as e:
+        H.hswa_swa_gather(lp, swa, 16, 16, 16, -1, 16)
+    assert e.value.status == H.HSWA_ERR_INVALID_ARG
+    H.hswa_pool_destroy(lp)
+
+
 @pytest.mark.parametrize("dtype", [H.HSWA_DTYPE_BF16, H.HSWA_DTYPE_FP8_E4M3])
 def test_decode_refuses_more_rows_than_the_merge_grid_takes(dtype):
     """The partial-record merge runs one CTA row per (sequence, token): at
